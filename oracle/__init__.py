@@ -1,0 +1,191 @@
+"""fp64 CPU oracle for paged MLA decode — test infrastructure only.
+
+The arithmetic lives in ``mla_oracle.c`` (plain C, fp64); this module only
+compiles it with gcc and marshals numpy/torch CPU buffers through ctypes.
+Only the tests, the smoke check and the benchmark's CPU-baseline leg may use
+it.  It shares nothing with the CUDA library.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mla_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_libs = {}
+
+D_QK = 576
+D_V = 512
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile the oracle with gcc (no fast-math: IEEE semantics are part of the definition)."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+        tmp = out + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, src,
+                               "-lm", "-lpthread"])
+        os.replace(tmp, out)
+    return out
+
+
+_active = [None]  # path of the library the module functions use (None = the default build)
+
+
+class use_library:
+    """Context manager: route the module functions to another build (mutation tests)."""
+
+    def __init__(self, path):
+        self.path = path
+
+    def __enter__(self):
+        self.prev = _active[0]
+        _active[0] = self.path
+
+    def __exit__(self, *exc):
+        _active[0] = self.prev
+
+
+def _load():
+    path = _active[0] or build()
+    with _lock:
+        lib = _libs.get(path)
+        if lib is None:
+            lib = ctypes.CDLL(path)
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            I64 = ctypes.c_int64
+            D = ctypes.c_double
+            common = [P, P, I, I, I, P, I, P, I, I, I, P, I, D, I, P, I64]
+            lib.oracle_mla_decode.argtypes = common + [P, P, I]
+            lib.oracle_mla_decode.restype = I
+            lib.oracle_mla_partial.argtypes = common + [I64, I64, P, P, I]
+            lib.oracle_mla_partial.restype = I
+            lib.oracle_lse_merge.argtypes = [I, P, P, P, P]
+            lib.oracle_lse_merge.restype = None
+            lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_to_double.restype = D
+            lib.oracle_dequant_row.argtypes = [P, P]
+            lib.oracle_dequant_row.restype = None
+            _libs[path] = lib
+    return lib
+
+
+def _np(x, dtype):
+    """Contiguous numpy view of a CPU tensor/array reinterpreted as ``dtype``."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor
+        x = x.detach().contiguous().cpu()
+        import torch
+        if x.dtype == torch.bfloat16:
+            x = x.view(torch.int16)
+        if x.dtype == torch.float8_e4m3fn:
+            x = x.view(torch.uint8)
+        x = x.numpy()
+    x = np.ascontiguousarray(x)
+    if x.dtype != dtype:
+        x = x.view(dtype) if x.dtype.itemsize == np.dtype(dtype).itemsize else x.astype(dtype)
+    return x
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _args(q, kvcache, block_table, cache_seqlens, sm_scale, is_causal, indices):
+    qn = _np(q, np.uint16)
+    batch, s_q, h_q, d = qn.shape
+    assert d == D_QK
+    kv = kvcache
+    if hasattr(kv, "dtype") and str(kv.dtype) in ("torch.uint8", "uint8"):
+        kvn = _np(kv, np.uint8)
+        is_fp8 = 1
+        assert kvn.shape[-1] == 656
+    else:
+        kvn = _np(kv, np.uint16)
+        is_fp8 = 0
+        assert kvn.shape[-1] == D_QK
+    num_pages, page_size = kvn.shape[0], kvn.shape[1]
+    bt = _np(block_table, np.int32)
+    sl = _np(cache_seqlens, np.int32)
+    idx = _np(indices, np.int32)
+    topk = 0 if idx is None else idx.shape[-1]
+    keep = (qn, kvn, bt, sl, idx)
+    a = [_ptr(qn), _ptr(kvn), is_fp8, num_pages, page_size, _ptr(bt), bt.shape[1], _ptr(sl), batch,
+         s_q, h_q, _ptr(idx), topk, float(sm_scale), int(bool(is_causal))]
+    return a, keep, (batch, s_q, h_q)
+
+
+def mla_decode(q, kvcache, block_table, cache_seqlens, sm_scale, is_causal=False, indices=None,
+               rows=None, n_threads=None):
+    """Oracle decode.  Returns (out float64 [n_rows, 512], lse float64 [n_rows]).
+
+    ``rows`` selects flat output rows ((b*s_q + i)*h_q + h); None = all rows
+    (then out is reshaped to [b, s_q, h_q, 512] and lse to [b, s_q, h_q]).
+    """
+    lib = _load()
+    a, keep, (batch, s_q, h_q) = _args(q, kvcache, block_table, cache_seqlens, sm_scale, is_causal,
+                                       indices)
+    all_rows = rows is None
+    r = None if all_rows else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = batch * s_q * h_q if all_rows else r.shape[0]
+    out = np.zeros((n, D_V), np.float64)
+    lse = np.zeros((n,), np.float64)
+    nt = n_threads or os.cpu_count() or 1
+    rc = lib.oracle_mla_decode(*a, _ptr(r), n, _ptr(out), _ptr(lse), int(nt))
+    if rc != 0:
+        raise ValueError("oracle: block_table holds an entry outside [0, num_pages)")
+    del keep
+    if all_rows:
+        return out.reshape(batch, s_q, h_q, D_V), lse.reshape(batch, s_q, h_q)
+    return out, lse
+
+
+def mla_partial(q, kvcache, block_table, cache_seqlens, sm_scale, k0, k1, is_causal=False,
+                indices=None, rows=None, n_threads=None):
+    """Oracle restricted to key-set positions [k0, k1) of every row (flat rows)."""
+    lib = _load()
+    a, keep, (batch, s_q, h_q) = _args(q, kvcache, block_table, cache_seqlens, sm_scale, is_causal,
+                                       indices)
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = batch * s_q * h_q if r is None else r.shape[0]
+    out = np.zeros((n, D_V), np.float64)
+    lse = np.zeros((n,), np.float64)
+    nt = n_threads or os.cpu_count() or 1
+    rc = lib.oracle_mla_partial(*a, _ptr(r), n, int(k0), int(k1), _ptr(out), _ptr(lse), int(nt))
+    if rc != 0:
+        raise ValueError("oracle: block_table holds an entry outside [0, num_pages)")
+    del keep
+    return out, lse
+
+
+def lse_merge(outs, lses):
+    """Merge partials of one row: outs [n, 512], lses [n] -> (out [512], lse)."""
+    lib = _load()
+    o = np.ascontiguousarray(np.asarray(outs, np.float64))
+    l = np.ascontiguousarray(np.asarray(lses, np.float64))
+    out = np.zeros((D_V,), np.float64)
+    lse = np.zeros((1,), np.float64)
+    lib.oracle_lse_merge(int(l.shape[0]), _ptr(o), _ptr(l), _ptr(out), _ptr(lse))
+    return out, float(lse[0])
+
+
+def e4m3_to_double(code: int) -> float:
+    return float(_load().oracle_e4m3_to_double(ctypes.c_uint8(code)))
+
+
+def dequant_row(row656) -> np.ndarray:
+    """Dequantise one 656-byte FP8 token row into 576 float64 (bf16-valued) numbers."""
+    r = np.ascontiguousarray(np.asarray(row656, np.uint8))
+    assert r.shape == (656,)
+    k = np.zeros((D_QK,), np.float64)
+    _load().oracle_dequant_row(_ptr(r), _ptr(k))
+    return k

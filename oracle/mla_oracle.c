@@ -1,0 +1,329 @@
+/*
+ * Plain fp64 CPU oracle for paged Multi-head Latent Attention (MLA) decode.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously-correct
+ * definition that the CUDA path is checked against.  It shares no code,
+ * header, table or helper with the CUDA library; only the test-suite, the
+ * smoke check and the benchmark's CPU-baseline leg may load it.
+ *
+ * What it computes (one output row per batch element b, query token i,
+ * query head h):
+ *
+ *   1. Key set J.
+ *        dense : J = {0 .. L-1}, L = cache_seqlens[b]; with is_causal the
+ *                query token i sits at position L - s_q + i (bottom-right
+ *                aligned), so J = {0 .. L - s_q + i}.
+ *        sparse: J = the multiset {indices[b,i,k] : 0 <= indices[b,i,k] < L},
+ *                in k order; ids outside [0, L) (e.g. -1) are skipped and a
+ *                repeated id counts once per occurrence, as a gather does.
+ *      ("Why FlashMLA's decode kernel reaches 660 TFLOPS", usage section:
+ *       sparse semantics written as kv[indices] gather then softmax.)
+ *   2. Token fetch through the block table: page = table[b][j / page_size],
+ *      slot = j % page_size.  (Modular design-doc overview, section 4
+ *      "PagedAttention": divmod(token, page_size) then a lookup-table read.)
+ *        bf16 cache : K_j = the 576 stored bf16 values, exactly.
+ *        fp8 cache  : 656-byte row = 512 float8_e4m3 codes, 4 float32
+ *                     scales (scale k covers dims [128k, 128k+128)), 64 bf16
+ *                     RoPE values.  K_j[d] = bf16_rne(fp32_rn(e4m3 * scale))
+ *                     for d < 512; the RoPE dims are copied.
+ *      ("Why FlashMLA ...", Design 2: FP8 KV cache, 512 + 16 + 128 = 656
+ *       bytes per token, dequantised to bf16 before every MMA.)
+ *      V_j = K_j[0:512]  (Modular overview, section 9 "Multi-Head Latent
+ *      Attention": MQA form with V = K[:, :, :512]).
+ *   3. s_j = sm_scale * sum_d q[d] * K_j[d]          (fp64)
+ *   4. two-pass softmax: m = max s_j, Z = sum exp(s_j - m),
+ *      out = sum exp(s_j - m) V_j / Z, lse = (m + ln Z) / ln 2, i.e. the
+ *      base-2 log-sum-exp log2(sum_j e^{s_j}).
+ *   5. empty J: out = 0, lse = -inf.
+ *
+ * Two helpers expose the split-KV view used by the invariant tests:
+ * oracle_mla_partial restricts J to a window [k0, k1) of its natural order,
+ * and oracle_lse_merge combines partials (Modular overview, section 6:
+ * online softmax rescales partial sums by exp(old_max - new_max)).
+ *
+ * No blocking, fusion or reordering beyond these definitions.  Built with
+ * plain gcc (no fast-math), threaded only over independent output rows.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define D_QK 576
+#define D_V 512
+#define FP8_ROW_BYTES 656
+#define FP8_SCALE_OFFSET 512
+#define FP8_ROPE_OFFSET 528
+
+static double bf16_bits_to_double(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* float -> bf16 bits, round to nearest even (NaN kept quiet). */
+static uint16_t float_to_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu)) return (uint16_t)((u >> 16) | 0x40);
+  uint32_t lsb = (u >> 16) & 1u;
+  u += 0x7fffu + lsb;
+  return (uint16_t)(u >> 16);
+}
+
+/* E4M3 ("fn" variant): sign, 4 exponent bits with bias 7, 3 mantissa bits;
+ * exponent field 0 encodes subnormals 2^-6 * m/8; S.1111.111 is NaN; there
+ * is no infinity, so the largest finite magnitude is 1.75 * 2^8 = 448. */
+double oracle_e4m3_to_double(uint8_t code) {
+  int sign = code >> 7;
+  int e = (code >> 3) & 0xf;
+  int m = code & 0x7;
+  double v;
+  if (e == 0xf && m == 0x7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+/* Dequantise one 656-byte token row into 576 doubles (bf16 values). */
+void oracle_dequant_row(const uint8_t* row, double* k) {
+  for (int d = 0; d < D_V; ++d) {
+    float scale;
+    memcpy(&scale, row + FP8_SCALE_OFFSET + 4 * (d / 128), sizeof scale);
+    /* e4m3 has a 4-bit significand and the scale 24 bits: the double
+     * product is exact, and the cast to float is the single fp32 rounding. */
+    float prod = (float)(oracle_e4m3_to_double(row[d]) * (double)scale);
+    k[d] = bf16_bits_to_double(float_to_bf16_rne(prod));
+  }
+  for (int d = D_V; d < D_QK; ++d) {
+    uint16_t h;
+    memcpy(&h, row + FP8_ROPE_OFFSET + 2 * (d - D_V), sizeof h);
+    k[d] = bf16_bits_to_double(h);
+  }
+}
+
+typedef struct {
+  const uint16_t* q;        /* bf16 bits [batch, s_q, h_q, 576] */
+  const void* kvcache;      /* bf16 [pages, page_size, 576] or uint8 [pages, page_size, 656] */
+  int is_fp8;
+  int num_pages;
+  int page_size;
+  const int32_t* block_table;
+  int block_table_stride;
+  const int32_t* cache_seqlens;
+  int batch, s_q, h_q;
+  const int32_t* indices;   /* int32 [batch, s_q, topk] or NULL */
+  int topk;
+  double sm_scale;
+  int is_causal;
+} oracle_problem;
+
+/* Fetch logical token j of element b as 576 doubles. Returns 0 when the
+ * block-table entry is not a valid page. */
+static int fetch_token(const oracle_problem* p, int b, int j, double* k) {
+  int page = p->block_table[(int64_t)b * p->block_table_stride + j / p->page_size];
+  int slot = j % p->page_size;
+  if (page < 0 || page >= p->num_pages) return 0;
+  int64_t token = (int64_t)page * p->page_size + slot;
+  if (p->is_fp8) {
+    oracle_dequant_row((const uint8_t*)p->kvcache + token * FP8_ROW_BYTES, k);
+  } else {
+    const uint16_t* row = (const uint16_t*)p->kvcache + token * D_QK;
+    for (int d = 0; d < D_QK; ++d) k[d] = bf16_bits_to_double(row[d]);
+  }
+  return 1;
+}
+
+/* Build the key set J of output row (b, i) as logical token ids, in the
+ * natural order.  Returns |J|. keys must hold max(seqlen, topk) entries. */
+static int64_t key_set(const oracle_problem* p, int b, int i, int32_t* keys) {
+  int L = p->cache_seqlens[b];
+  int64_t n = 0;
+  if (p->indices) {
+    const int32_t* idx = p->indices + ((int64_t)b * p->s_q + i) * p->topk;
+    for (int k = 0; k < p->topk; ++k)
+      if (idx[k] >= 0 && idx[k] < L) keys[n++] = idx[k];
+  } else {
+    int last = L - 1;
+    if (p->is_causal) last = L - p->s_q + i;
+    if (last > L - 1) last = L - 1;
+    for (int j = 0; j <= last; ++j) keys[n++] = j;
+  }
+  return n;
+}
+
+/* One output row over the window [k0, k1) of its key set (k1 < 0: to the
+ * end).  out[512], lse (base 2).  Returns 0 on a bad page id. */
+static int one_row(const oracle_problem* p, int64_t row, int64_t k0, int64_t k1, double* out,
+                   double* lse, int32_t* keys, double* s, double* kbuf) {
+  int h = (int)(row % p->h_q);
+  int i = (int)((row / p->h_q) % p->s_q);
+  int b = (int)(row / ((int64_t)p->h_q * p->s_q));
+  const uint16_t* q = p->q + row * D_QK;
+  int64_t n = key_set(p, b, i, keys);
+  (void)h;
+  if (k1 < 0 || k1 > n) k1 = n;
+  if (k0 < 0) k0 = 0;
+  for (int d = 0; d < D_V; ++d) out[d] = 0.0;
+  if (k0 >= k1) {
+    *lse = -INFINITY;
+    return 1;
+  }
+  /* pass 1: logits */
+  for (int64_t t = k0; t < k1; ++t) {
+    if (!fetch_token(p, b, keys[t], kbuf)) return 0;
+    double acc = 0.0;
+    for (int d = 0; d < D_QK; ++d) acc += bf16_bits_to_double(q[d]) * kbuf[d];
+    s[t - k0] = p->sm_scale * acc;
+  }
+  double m = -INFINITY;
+  for (int64_t t = 0; t < k1 - k0; ++t)
+    if (s[t] > m) m = s[t];
+  /* pass 2: weights and weighted sum of V */
+  double z = 0.0;
+  for (int64_t t = k0; t < k1; ++t) {
+    double w = exp(s[t - k0] - m);
+    z += w;
+    fetch_token(p, b, keys[t], kbuf);
+    for (int d = 0; d < D_V; ++d) out[d] += w * kbuf[d];
+  }
+  for (int d = 0; d < D_V; ++d) out[d] /= z;
+  *lse = (m + log(z)) / log(2.0);
+  return 1;
+}
+
+typedef struct {
+  const oracle_problem* p;
+  const int64_t* rows;
+  int64_t n_rows;
+  int64_t k0, k1;
+  double* out;
+  double* lse;
+  int64_t next;      /* shared work counter (guarded by mu) */
+  int bad;
+  pthread_mutex_t mu;
+} oracle_job;
+
+static void* worker(void* arg) {
+  oracle_job* job = (oracle_job*)arg;
+  const oracle_problem* p = job->p;
+  int64_t cap = p->topk > 0 ? p->topk : 0;
+  for (int b = 0; b < p->batch; ++b)
+    if (p->cache_seqlens[b] > cap) cap = p->cache_seqlens[b];
+  if (cap < 1) cap = 1;
+  int32_t* keys = (int32_t*)malloc(sizeof(int32_t) * cap);
+  double* s = (double*)malloc(sizeof(double) * cap);
+  double kbuf[D_QK];
+  for (;;) {
+    pthread_mutex_lock(&job->mu);
+    int64_t r = job->next++;
+    pthread_mutex_unlock(&job->mu);
+    if (r >= job->n_rows) break;
+    int64_t row = job->rows ? job->rows[r] : r;
+    if (!one_row(p, row, job->k0, job->k1, job->out + r * D_V, job->lse + r, keys, s, kbuf)) {
+      pthread_mutex_lock(&job->mu);
+      job->bad = 1;
+      pthread_mutex_unlock(&job->mu);
+    }
+  }
+  free(keys);
+  free(s);
+  return NULL;
+}
+
+static int run(const oracle_problem* p, const int64_t* rows, int64_t n_rows, int64_t k0, int64_t k1,
+               double* out, double* lse, int n_threads) {
+  oracle_job job;
+  memset(&job, 0, sizeof job);
+  job.p = p;
+  job.rows = rows;
+  job.n_rows = n_rows;
+  job.k0 = k0;
+  job.k1 = k1;
+  job.out = out;
+  job.lse = lse;
+  pthread_mutex_init(&job.mu, NULL);
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads > 256) n_threads = 256;
+  pthread_t tid[256];
+  for (int t = 1; t < n_threads; ++t) pthread_create(&tid[t], NULL, worker, &job);
+  worker(&job);
+  for (int t = 1; t < n_threads; ++t) pthread_join(tid[t], NULL);
+  pthread_mutex_destroy(&job.mu);
+  return job.bad ? 1 : 0;
+}
+
+static void fill_problem(oracle_problem* p, const uint16_t* q, const void* kvcache, int is_fp8,
+                         int num_pages, int page_size, const int32_t* block_table,
+                         int block_table_stride, const int32_t* cache_seqlens, int batch, int s_q,
+                         int h_q, const int32_t* indices, int topk, double sm_scale, int is_causal) {
+  p->q = q;
+  p->kvcache = kvcache;
+  p->is_fp8 = is_fp8;
+  p->num_pages = num_pages;
+  p->page_size = page_size;
+  p->block_table = block_table;
+  p->block_table_stride = block_table_stride;
+  p->cache_seqlens = cache_seqlens;
+  p->batch = batch;
+  p->s_q = s_q;
+  p->h_q = h_q;
+  p->indices = indices;
+  p->topk = topk;
+  p->sm_scale = sm_scale;
+  p->is_causal = is_causal;
+}
+
+/* Full decode for the listed flat rows ((b*s_q + i)*h_q + h); rows == NULL
+ * means every row in order.  out: [n_rows, 512], lse: [n_rows].
+ * Returns 0, or 1 if some block-table entry was not a valid page. */
+int oracle_mla_decode(const uint16_t* q, const void* kvcache, int is_fp8, int num_pages,
+                      int page_size, const int32_t* block_table, int block_table_stride,
+                      const int32_t* cache_seqlens, int batch, int s_q, int h_q,
+                      const int32_t* indices, int topk, double sm_scale, int is_causal,
+                      const int64_t* rows, int64_t n_rows, double* out, double* lse,
+                      int n_threads) {
+  oracle_problem p;
+  fill_problem(&p, q, kvcache, is_fp8, num_pages, page_size, block_table, block_table_stride,
+               cache_seqlens, batch, s_q, h_q, indices, topk, sm_scale, is_causal);
+  return run(&p, rows, n_rows, 0, -1, out, lse, n_threads);
+}
+
+/* Same, restricted to positions [k0, k1) of each row's key set. */
+int oracle_mla_partial(const uint16_t* q, const void* kvcache, int is_fp8, int num_pages,
+                       int page_size, const int32_t* block_table, int block_table_stride,
+                       const int32_t* cache_seqlens, int batch, int s_q, int h_q,
+                       const int32_t* indices, int topk, double sm_scale, int is_causal,
+                       const int64_t* rows, int64_t n_rows, int64_t k0, int64_t k1, double* out,
+                       double* lse, int n_threads) {
+  oracle_problem p;
+  fill_problem(&p, q, kvcache, is_fp8, num_pages, page_size, block_table, block_table_stride,
+               cache_seqlens, batch, s_q, h_q, indices, topk, sm_scale, is_causal);
+  return run(&p, rows, n_rows, k0, k1, out, lse, n_threads);
+}
+
+/* Merge n partial results of one row by their base-2 log-sum-exps:
+ * L = log2 sum_i 2^{lse_i}, out = sum_i 2^{lse_i - L} out_i.  Partials with
+ * lse = -inf contribute nothing; all empty gives out = 0, lse = -inf. */
+void oracle_lse_merge(int n, const double* outs, const double* lses, double* out, double* lse) {
+  double mx = -INFINITY;
+  for (int i = 0; i < n; ++i)
+    if (lses[i] > mx) mx = lses[i];
+  for (int d = 0; d < D_V; ++d) out[d] = 0.0;
+  if (mx == -INFINITY) {
+    *lse = -INFINITY;
+    return;
+  }
+  double sum = 0.0;
+  for (int i = 0; i < n; ++i) sum += exp2(lses[i] - mx);
+  double L = mx + log2(sum);
+  for (int i = 0; i < n; ++i) {
+    double w = exp2(lses[i] - L);
+    for (int d = 0; d < D_V; ++d) out[d] += w * outs[(int64_t)i * D_V + d];
+  }
+  *lse = L;
+}

@@ -1,0 +1,223 @@
+"""Seeded synthetic inputs for paged MLA decode.
+
+This module is shared by the tests, the benchmark and the smoke check.  It
+only draws random numbers and writes them into the storage formats; it holds
+none of the attention arithmetic.  The FP8 cache rows are produced with
+torch's own float8_e4m3fn cast (a library routine).
+
+Storage formats (one KV head, page size 64):
+  q            bf16  [batch, s_q, h_q, 576]
+  kvcache bf16 bf16  [num_pages, page_size, 1, 576]
+  kvcache fp8  uint8 [num_pages, page_size, 1, 656]: bytes [0,512) e4m3 codes
+               of dims 0..511, [512,528) four little-endian float32 scales
+               (scale k covers dims [128k, 128k+128)), [528,656) 64 bf16
+               RoPE values (dims 512..575)
+  block_table  int32 [batch, max_blocks]  (unused slots hold 0)
+  cache_seqlens int32 [batch]
+  indices      int32 [batch, s_q, topk] logical token ids, -1 = unused
+
+The five named workloads follow the decode shapes of the FlashMLA article
+("Why FlashMLA's decode kernel reaches 660 TFLOPS": h_q = 128 with s_q = 2
+for the compute-bound case, top-k 2048 / 32768 for sparse FP8 decode) plus a
+tiny case and a small-head memory-bound case.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+from typing import List, Optional, Tuple
+
+import numpy as np
+import torch
+
+D_QK = 576
+D_V = 512
+D_ROPE = 64
+FP8_ROW_BYTES = 656
+PAGE_SIZE = 64
+E4M3_MAX = 448.0
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    batch: int
+    h_q: int
+    s_q: int
+    mode: str                                   # "dense" (bf16 cache) or "sparse" (fp8 cache + indices)
+    seqlens: Optional[Tuple[int, ...]] = None   # explicit lengths
+    seqlen_range: Optional[Tuple[int, int]] = None  # uniform integer [lo, hi]
+    seqlen: Optional[int] = None                # fixed length
+    topk: int = 0
+    causal: bool = False
+    invalid_frac: float = 0.05                  # sparse: trailing fraction of each index row set to -1
+    page_size: int = PAGE_SIZE
+    sm_scale: Optional[float] = None            # default 1/sqrt(576)
+
+    @property
+    def is_fp8(self) -> bool:
+        return self.mode == "sparse"
+
+    @property
+    def scale(self) -> float:
+        return self.sm_scale if self.sm_scale is not None else 1.0 / math.sqrt(D_QK)
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", batch=2, h_q=16, s_q=1, mode="dense", seqlens=(100, 257)),
+    "dense_membound": Workload("dense_membound", batch=128, h_q=16, s_q=1, mode="dense",
+                               seqlen_range=(1024, 8192)),
+    "dense_computebound": Workload("dense_computebound", batch=64, h_q=128, s_q=2, mode="dense",
+                                   seqlen=4096, causal=True),
+    "sparse_fp8": Workload("sparse_fp8", batch=128, h_q=128, s_q=2, mode="sparse", seqlen=32768,
+                           topk=2048),
+    "sparse_fp8_long": Workload("sparse_fp8_long", batch=16, h_q=128, s_q=1, mode="sparse",
+                                seqlen_range=(65536, 131072), topk=32768),
+}
+# Seed per named workload: 1000 + its position (1-based) in the list above.
+SEEDS = {name: 1000 + i for i, name in enumerate(WORKLOADS, start=1)}
+
+
+@dataclass
+class Inputs:
+    workload: Workload
+    q: torch.Tensor
+    kvcache: torch.Tensor
+    block_table: torch.Tensor
+    cache_seqlens: torch.Tensor
+    indices: Optional[torch.Tensor]
+    sm_scale: float
+    seed: int
+    meta: dict = field(default_factory=dict)
+
+    def to(self, device) -> "Inputs":
+        mv = lambda t: None if t is None else t.to(device)
+        return Inputs(self.workload, mv(self.q), mv(self.kvcache), mv(self.block_table),
+                      mv(self.cache_seqlens), mv(self.indices), self.sm_scale, self.seed,
+                      dict(self.meta))
+
+
+def draw_seqlens(w: Workload, rng: np.random.Generator) -> np.ndarray:
+    if w.seqlens is not None:
+        lens = np.asarray(w.seqlens, dtype=np.int64)
+        assert lens.shape == (w.batch,)
+        return lens
+    if w.seqlen is not None:
+        return np.full((w.batch,), w.seqlen, dtype=np.int64)
+    lo, hi = w.seqlen_range
+    return rng.integers(lo, hi + 1, size=w.batch, dtype=np.int64)
+
+
+def _paging(lens: np.ndarray, page_size: int, rng: np.random.Generator):
+    """Random permutation of exactly sum(ceil(len/page)) pages shared by all elements."""
+    nblk = (lens + page_size - 1) // page_size
+    total = int(nblk.sum())
+    perm = rng.permutation(total).astype(np.int32)
+    width = max(1, int(nblk.max()) if len(nblk) else 1)
+    table = np.zeros((len(lens), width), dtype=np.int32)
+    off = 0
+    for b, n in enumerate(nblk):
+        table[b, :n] = perm[off:off + n]
+        off += n
+    return table, max(total, 1)
+
+
+def _normal_bf16(n_rows: int, gen: torch.Generator, device) -> torch.Tensor:
+    return torch.randn((n_rows, D_QK), generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+def encode_fp8_rows(x: torch.Tensor) -> torch.Tensor:
+    """Source values [n, 576] float32 -> [n, 656] uint8 rows in the FP8 cache format.
+
+    Each 1x128 tile of dims 0..511 gets scale = amax/448 (float32; scale 1 for
+    an all-zero tile) and codes = float8_e4m3fn(x / scale) via torch's cast;
+    dims 512..575 are stored as bf16.
+    """
+    n = x.shape[0]
+    nope = x[:, :D_V].float().reshape(n, 4, 128)
+    amax = nope.abs().amax(dim=2)
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    codes = (nope / scale[:, :, None]).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    rope = x[:, D_V:].to(torch.bfloat16)
+    row = torch.empty((n, FP8_ROW_BYTES), dtype=torch.uint8, device=x.device)
+    row[:, :D_V] = codes.reshape(n, D_V).view(torch.uint8)
+    row[:, D_V:D_V + 16] = scale.contiguous().view(torch.uint8).reshape(n, 16)
+    row[:, D_V + 16:] = rope.contiguous().view(torch.uint8).reshape(n, 2 * D_ROPE)
+    return row
+
+
+def make_inputs(w, seed: Optional[int] = None, device="cpu", poison_tail: bool = True,
+                chunk_pages: int = 2048) -> Inputs:
+    """Draw one batch of inputs for workload ``w`` (a Workload or a name in WORKLOADS).
+
+    Structure (lengths, page permutation, indices) comes from numpy's PCG64
+    seeded with ``seed``; values (q, kv) from a torch generator with the same
+    seed on ``device``.  With ``poison_tail`` the unused slots of each
+    element's last page hold NaN so that any read past the length shows.
+    """
+    if isinstance(w, str):
+        if seed is None:
+            seed = SEEDS[w]
+        w = WORKLOADS[w]
+    if seed is None:
+        seed = 1234
+    rng = np.random.default_rng(seed)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    lens = draw_seqlens(w, rng)
+    table, num_pages = _paging(lens, w.page_size, rng)
+
+    q = torch.randn((w.batch, w.s_q, w.h_q, D_QK), generator=gen, device=device,
+                    dtype=torch.float32).to(torch.bfloat16)
+    ntok = num_pages * w.page_size
+    if w.is_fp8:
+        kv = torch.empty((ntok, FP8_ROW_BYTES), dtype=torch.uint8, device=device)
+    else:
+        kv = torch.empty((ntok, D_QK), dtype=torch.bfloat16, device=device)
+    step = chunk_pages * w.page_size
+    for t0 in range(0, ntok, step):
+        t1 = min(ntok, t0 + step)
+        x = torch.randn((t1 - t0, D_QK), generator=gen, device=device, dtype=torch.float32)
+        kv[t0:t1] = encode_fp8_rows(x) if w.is_fp8 else x.to(torch.bfloat16)
+
+    if poison_tail:
+        for b, L in enumerate(lens.tolist()):
+            nblk = (L + w.page_size - 1) // w.page_size
+            used = L - (nblk - 1) * w.page_size if nblk else 0
+            if nblk == 0 or used == w.page_size:
+                continue
+            page = int(table[b, nblk - 1])
+            s0 = page * w.page_size + used
+            s1 = (page + 1) * w.page_size
+            if w.is_fp8:
+                kv[s0:s1] = 0x7F  # e4m3 NaN codes; scale / RoPE bytes 0x7F7F.. are NaN too
+            else:
+                kv[s0:s1] = float("nan")
+
+    indices = None
+    if w.mode == "sparse":
+        indices_np = np.full((w.batch, w.s_q, w.topk), -1, dtype=np.int32)
+        n_invalid = int(math.floor(w.invalid_frac * w.topk))
+        n_valid = w.topk - n_invalid
+        for b in range(w.batch):
+            L = int(lens[b])
+            for i in range(w.s_q):
+                k = min(n_valid, L)
+                if k > 0:
+                    indices_np[b, i, :k] = rng.choice(L, size=k, replace=False).astype(np.int32)
+        indices = torch.from_numpy(indices_np).to(device)
+
+    kv = kv.reshape(num_pages, w.page_size, 1, FP8_ROW_BYTES if w.is_fp8 else D_QK)
+    return Inputs(w, q, kv, torch.from_numpy(table).to(device),
+                  torch.from_numpy(lens.astype(np.int32)).to(device), indices, w.scale, seed,
+                  meta={"num_pages": num_pages})
+
+
+def custom(name="custom", **kw) -> Workload:
+    """A Workload with explicit fields (tests)."""
+    return Workload(name=name, **kw)
+
+
+def with_fields(w: Workload, **kw) -> Workload:
+    return replace(w, **kw)
+
