@@ -1,0 +1,424 @@
+#!/usr/bin/env python
+"""Benchmark: paged MLA decode on GB300.
+
+One step = the whole decode path for one batch of synthetic inputs already
+resident in HBM: schedule (mla_get_metadata) + split-KV decode + combine
+(mla_decode).  The headline workload is the memory-bound dense mix (batch
+128, 16 heads, lengths U[1024, 8192]); its KV (~680 MB) is larger than L2, so
+no flush is needed between steps.  At one GPU the compute-bound dense and the
+two sparse FP8 workloads are measured too and reported under "workloads".
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mla|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the fp64 CPU oracle
+on a bounded sample of the same workload (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_mla_decode_07_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MLA decode TFLOPS & KV GB/s (bf16 dense, fp8 sparse) as % of GB300 roofline"
+HEADLINE = "dense_membound"
+D_QK, D_V, FP8_ROW = 576, 512, 656
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work per step
+# ----------------------------------------------------------------------------
+def algorithmic(inp) -> dict:
+    """Nominal FLOPs 2*h_q*s_q*s_k*(576+512) (s_k = length, or topk in sparse mode), the valid-only
+    FLOPs, and the bytes the path must move once: KV rows (each cached token once per element in
+    dense mode; each valid gathered row in sparse mode) + q + out + lse + tables/indices."""
+    w = inp.workload
+    lens = inp.cache_seqlens.cpu().numpy().astype(np.int64)
+    rows = w.batch * w.s_q * w.h_q
+    q_bytes = rows * D_QK * 2
+    out_bytes = rows * D_V * 2 + rows * 4
+    if w.mode == "sparse":
+        idx = inp.indices
+        valid = ((idx >= 0) & (idx < inp.cache_seqlens.view(-1, 1, 1))).sum().item()
+        kv_bytes = valid * FP8_ROW
+        flops = 2.0 * w.h_q * w.s_q * w.topk * w.batch * (D_QK + D_V)
+        vflops = 2.0 * w.h_q * valid * (D_QK + D_V)
+        tab = idx.numel() * 4 + inp.block_table.numel() * 4
+    else:
+        kv_bytes = int(lens.sum()) * D_QK * 2
+        flops = 2.0 * w.h_q * w.s_q * float(lens.sum()) * (D_QK + D_V)
+        if w.causal:
+            vk = sum(max(0, min(L, L - w.s_q + i + 1)) for L in lens for i in range(w.s_q))
+            vflops = 2.0 * w.h_q * vk * (D_QK + D_V)
+        else:
+            vflops = flops
+        tab = int(((lens + 63) // 64).sum()) * 4 + w.batch * 4
+    return dict(flops=flops, valid_flops=vflops, kv_bytes=kv_bytes,
+                bytes=kv_bytes + q_bytes + out_bytes + tab)
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        lines = [l.strip() for l in open(self.file.name) if l.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# the CUDA path
+# ----------------------------------------------------------------------------
+class DecodeStep:
+    """Device-resident inputs + preallocated outputs; __call__ runs one step on the current stream."""
+
+    def __init__(self, inp, device):
+        import paged_mla_decode_07_gb300 as mla
+        self.mla = mla
+        self.w = inp.workload
+        self.d = inp.to(device) if inp.q.device != torch.device(device) else inp
+        self.topk = 0 if self.d.indices is None else self.d.indices.shape[-1]
+        b, s, h = self.w.batch, self.w.s_q, self.w.h_q
+        self.out = torch.empty((b, s, h, D_V), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((b, s, h), dtype=torch.float32, device=device)
+        self.ws = torch.empty(max(256, mla.workspace_size(b, s, h, self.topk)), dtype=torch.uint8, device=device)
+        ns, nn = mla.metadata_size(b, s, h, self.topk)
+        self.sched = torch.empty(ns, dtype=torch.int32, device=device)
+        self.nsplit = torch.empty(nn, dtype=torch.int32, device=device)
+
+    def metadata(self):
+        self.mla.get_metadata(self.d.cache_seqlens, self.w.s_q, self.w.h_q, self.topk, sched=self.sched,
+                              num_splits=self.nsplit)
+
+    def decode(self):
+        d = self.d
+        self.mla.decode(d.q, d.kvcache, d.block_table, d.cache_seqlens, d.sm_scale, self.sched, self.nsplit,
+                        is_causal=self.w.causal, indices=d.indices, out=self.out, lse=self.lse,
+                        workspace=self.ws)
+
+    def __call__(self):
+        self.metadata()
+        self.decode()
+
+
+def time_events(fn, n: int):
+    """Per-call device durations (ms) with CUDA events on the current stream."""
+    s = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record(s)
+        fn()
+        b.record(s)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def e2e_step_factory(inp, device):
+    """End to end through the public API: pinned host inputs -> H2D copies -> schedule + decode ->
+    D2H of out and lse, every step."""
+    import paged_mla_decode_07_gb300 as mla
+    w = inp.workload
+    host = {k: getattr(inp, k).cpu().pin_memory() for k in ("q", "kvcache", "block_table", "cache_seqlens")}
+    if inp.indices is not None:
+        host["indices"] = inp.indices.cpu().pin_memory()
+    dev = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    topk = 0 if inp.indices is None else inp.indices.shape[-1]
+    b, s, h = w.batch, w.s_q, w.h_q
+    out = torch.empty((b, s, h, D_V), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((b, s, h), dtype=torch.float32, device=device)
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    ws = torch.empty(max(256, mla.workspace_size(b, s, h, topk)), dtype=torch.uint8, device=device)
+    ns, nn = mla.metadata_size(b, s, h, topk)
+    sched = torch.empty(ns, dtype=torch.int32, device=device)
+    nsplit = torch.empty(nn, dtype=torch.int32, device=device)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out.numel() * 2 + lse.numel() * 4
+
+    def step():
+        for k, v in host.items():
+            dev[k].copy_(v, non_blocking=True)
+        mla.get_metadata(dev["cache_seqlens"], s, h, topk, sched=sched, num_splits=nsplit)
+        mla.decode(dev["q"], dev["kvcache"], dev["block_table"], dev["cache_seqlens"], inp.sm_scale, sched, nsplit,
+                   is_causal=w.causal, indices=dev.get("indices"), out=out, lse=lse, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    return step, h2d, d2h
+
+
+def measure_workload(name, device, reps=20, warmup=3):
+    """Kernel-level measurement of one workload (decode call = split-KV kernel + combine)."""
+    inp = W.make_inputs(name, device=device)
+    st = DecodeStep(inp, device)
+    st.metadata()
+    for _ in range(warmup):
+        st.decode()
+    times = time_events(st.decode, reps)
+    a = algorithmic(inp)
+    ms = statistics.median(times)
+    return inp, a, ms, st
+
+
+def run_mla(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import paged_mla_decode_07_gb300 as mla
+    mla.build()
+    peaks = load_peaks()
+
+    # ---- headline workload: full steps
+    inp = W.make_inputs(HEADLINE, device=device)
+    a = algorithmic(inp)
+    step = DecodeStep(inp, device)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(args.steps):
+            step()
+        t1.record()
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms = total_ms / args.steps
+    flags = mla.device_status()
+    value = a["bytes"] * world / (ms * 1e-3) / 1e9  # GB/s over all ranks
+
+    # ---- dominant kernel: decode call (split-KV kernel + combine), same workload
+    step.metadata()
+    dts = time_events(step.decode, max(10, args.steps))
+    dec_ms = statistics.mean(dts)
+    achieved = a["bytes"] / (dec_ms * 1e-3) / 1e9
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 q/KV, random page permutation)",
+        "config": {"workload": HEADLINE, "batch": inp.workload.batch, "h_q": inp.workload.h_q,
+                   "s_q": inp.workload.s_q, "seqlens": "uniform int [1024, 8192], seed 1002",
+                   "page_size": 64, "mode": "dense bf16 cache", "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (KV %.0f MB > 129 MB), no flush" % (a["kv_bytes"] / 1e6)},
+        "tflops": round(a["flops"] * world / (ms * 1e-3) / 1e12, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "kernel": "mla_decode_kernel<16,dense> + combine (one decode call)",
+                     "peak_source": peaks["source"]},
+        "gpu_launches": 3 * args.steps,
+        "device_status": flags,
+        "clocks": clk.summary(),
+    }
+    del step
+    torch.cuda.empty_cache()
+
+    if rank == 0 and world == 1 and not args.no_extras:
+        # ---- end to end through the public API with host buffers
+        estep, h2d, d2h = e2e_step_factory(inp, device)
+        for _ in range(2):
+            estep()
+        et = time_events(estep, max(3, min(args.steps, 10)))
+        ems = statistics.mean(et)
+        result["e2e"] = {"value": round(a["bytes"] / (ems * 1e-3) / 1e9, 1), "unit": "GB/s",
+                         "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                         "ms_per_step": round(ems, 4), "note": "inputs incl. the whole KV cache copied from pinned host memory each step"}
+        del estep
+        torch.cuda.empty_cache()
+        # ---- the other workloads (kernel level)
+        extra = {}
+        for name in ("tiny", "dense_computebound", "sparse_fp8", "sparse_fp8_long"):
+            winp, wa, wms, st = measure_workload(name, device)
+            bound = "hbm" if name == "tiny" else "tensor"
+            e = {"ms": round(wms, 5), "tflops": round(wa["flops"] / (wms * 1e-3) / 1e12, 2),
+                 "tflops_valid": round(wa["valid_flops"] / (wms * 1e-3) / 1e12, 2),
+                 "kv_gbs": round(wa["bytes"] / (wms * 1e-3) / 1e9, 1)}
+            if bound == "tensor":
+                e["frac_of_bf16_peak"] = round(e["tflops"] / peaks["bf16_tflops"], 4)
+            else:
+                e["frac_of_hbm"] = round(e["kv_gbs"] / peaks["hbm_gbs"], 4)
+            extra[name] = e
+            del st, winp
+            torch.cuda.empty_cache()
+        result["workloads"] = extra
+        # ---- the oracle on the host cores, bounded sample
+        result["cpu_baseline"] = cpu_baseline(inp, target_s=args.cpu_seconds)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# the oracle (CPU baseline / reference arm)
+# ----------------------------------------------------------------------------
+def _oracle_sample(inp_cpu, n_elems):
+    """Oracle decode of the first n_elems batch elements; returns (seconds, kv bytes processed)."""
+    import oracle
+    w = inp_cpu.workload
+    rows_per = w.s_q * w.h_q
+    rows = np.arange(n_elems * rows_per, dtype=np.int64)
+    t = time.perf_counter()
+    oracle.mla_decode(inp_cpu.q, inp_cpu.kvcache, inp_cpu.block_table, inp_cpu.cache_seqlens, inp_cpu.sm_scale,
+                      is_causal=w.causal, indices=inp_cpu.indices, rows=rows)
+    dt = time.perf_counter() - t
+    lens = inp_cpu.cache_seqlens[:n_elems].numpy().astype(np.int64)
+    kv = int(lens.sum()) * D_QK * 2 + n_elems * rows_per * (D_QK * 2 + D_V * 2 + 4)
+    return dt, kv
+
+
+def cpu_baseline(inp, target_s=15.0):
+    import oracle
+    oracle.build()
+    cpu = inp.to("cpu")
+    n = 1
+    dt, kv = _oracle_sample(cpu, n)
+    n = max(1, min(cpu.workload.batch, int(n * target_s / max(dt, 1e-3))))
+    dt, kv = _oracle_sample(cpu, n)
+    return {"value": round(kv / dt / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {n} of {cpu.workload.batch} batch elements (all heads) of {HEADLINE}, "
+                      f"{dt:.1f} s, fp64, {os.cpu_count()} threads"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    inp = W.make_inputs(HEADLINE)
+    a = algorithmic(inp)
+    # size one step to about 2 s of CPU work, capped so the whole run stays within minutes
+    dt1, _ = _oracle_sample(inp, 1)
+    per_step = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    n = max(1, min(inp.workload.batch, int(per_step / max(dt1, 1e-3))))
+    for _ in range(args.warmup):
+        _oracle_sample(inp, n)
+    times, kvs = [], []
+    for _ in range(args.steps):
+        dt, kv = _oracle_sample(inp, n)
+        times.append(dt)
+        kvs.append(kv)
+    ms = 1e3 * sum(times) / len(times)
+    value = sum(kvs) / sum(times) / 1e9
+    sample = f"first {n} of {inp.workload.batch} batch elements (all heads) per step, fp64, {os.cpu_count()} threads"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": HEADLINE, "batch": inp.workload.batch, "h_q": inp.workload.h_q,
+                   "s_q": inp.workload.s_q, "page_size": 64, "mode": "dense bf16 cache"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "algorithmic_bytes_full_step": a["bytes"],
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["mla", "reference"], default="mla")
+    ap.add_argument("--no-extras", action="store_true", help="headline workload only")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_mla(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,138 @@
+/*
+ * libmla — paged Multi-head Latent Attention (MLA) decode for GB300 (sm_103a).
+ *
+ * C ABI.  Plain pointers and sizes only; every pointer named "device" must
+ * point to memory of the current CUDA device.  The library never allocates
+ * device memory: the caller sizes buffers with mla_metadata_size() and
+ * mla_workspace_size() and passes them in.  All work is enqueued on the
+ * caller's stream and is asynchronous; host-detectable errors return at once
+ * with no launch, and mla_last_error() then names the offending argument.
+ *
+ * The two compute calls follow the decode API described in "Why FlashMLA's
+ * decode kernel reaches 660 TFLOPS" (usage section): a scheduling-metadata
+ * call made once per decode step and reused by every layer, then one decode
+ * call per layer that returns the attention output and its log-sum-exp.
+ *
+ * Shapes (one KV head; the MQA form of MLA from the Modular design-doc
+ * overview, section 9 "Multi-Head Latent Attention": a query row is 576-wide,
+ * keys are 576-wide and the value is the first 512 dims of the key):
+ *   q             bf16  [batch, s_q, h_q, 576], contiguous
+ *   kvcache dense bf16  [num_pages, page_size, 1, 576], contiguous
+ *   kvcache fp8   uint8 [num_pages, page_size, 1, 656], contiguous; per token
+ *                 bytes [0,512) float8_e4m3 codes of dims 0..511, [512,528)
+ *                 four float32 scales (scale k covers dims [128k,128k+128)),
+ *                 [528,656) 64 bf16 RoPE values (FlashMLA article, Design 2)
+ *   block_table   int32 [batch, block_table_stride]; logical token t of
+ *                 element b lives in page block_table[b][t / page_size],
+ *                 slot t % page_size (Modular overview, section 4
+ *                 "PagedAttention")
+ *   cache_seqlens int32 [batch]
+ *   indices       int32 [batch, s_q, topk] logical token ids (sparse mode);
+ *                 ids outside [0, cache_seqlens[b]) — e.g. -1 — are skipped,
+ *                 repeated ids count once per occurrence
+ *   out           bf16  [batch, s_q, h_q, 512]
+ *   lse           fp32  [batch, s_q, h_q], base 2: log2(sum_j exp(s_j))
+ *
+ * out = softmax(q K^T * sm_scale) V over the key set of each query row:
+ * dense mode = tokens [0, seqlen) (with is_causal: [0, seqlen - s_q + i] for
+ * query token i), sparse mode = the valid ids of indices[b, i, :].  A row
+ * with an empty key set gets out = 0 and lse = -inf.
+ *
+ * Supported modes: dense over a bf16 cache and sparse (top-k) over an FP8
+ * cache, page_size 64.  Other combinations return MLA_ERR_UNSUPPORTED.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The caller's CUDA stream (a cudaStream_t / CUstream); NULL = legacy default stream. */
+typedef struct CUstream_st* mla_stream_t;
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,    /* null pointer, bad size or alignment; see mla_last_error() */
+  MLA_ERR_UNSUPPORTED = 2,    /* valid request outside the supported modes/shapes */
+  MLA_ERR_WORKSPACE = 3,      /* workspace missing or smaller than mla_workspace_size() */
+  MLA_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed; message has the error */
+  MLA_ERR_DEVICE_BOUNDS = 5,  /* device status: a block-table entry outside [0, num_pages) */
+  MLA_ERR_DEVICE_TIMEOUT = 6  /* device status: a bounded wait inside a kernel gave up */
+} mla_status;
+
+/* Device status bits, reported by mla_get_device_status(). */
+#define MLA_DEVICE_BAD_PAGE 0x1u     /* a page id outside [0, num_pages) was skipped (token masked) */
+#define MLA_DEVICE_TIMEOUT 0x2u      /* a pipeline wait exceeded its limit; results are invalid */
+#define MLA_DEVICE_BAD_SCHEDULE 0x4u /* the schedule did not match the arguments; results invalid */
+
+/* ABI version of this header (incremented on incompatible change). */
+#define MLA_ABI_VERSION 1
+int mla_abi_version(void);
+
+/* Sizes of the two metadata arrays for a decode configuration on the
+ * current device (int32 element counts).  topk = 0 selects dense mode.
+ * sched has one 8-int record per scheduled work part; num_splits has one
+ * entry per problem plus one (problem = batch element in dense mode,
+ * (batch element, query token) pair in sparse mode). */
+mla_status mla_metadata_size(int batch, int s_q, int h_q, int topk, int* sched_elems,
+                             int* num_splits_elems);
+
+/* Scratch bytes that mla_decode needs for split-KV partial results
+ * (fp32 partial outputs and their log-sum-exps). */
+mla_status mla_workspace_size(int batch, int s_q, int h_q, int topk, size_t* bytes);
+
+/* (1) Tile schedule for one decode step ("get_mla_metadata").
+ * cache_seqlens: device int32 [batch]; sched, num_splits: device int32
+ * buffers of the sizes above, written on `stream`.  The work of all problems
+ * (128-token tiles of their key ranges) is divided into contiguous ranges of
+ * near-equal cost, one per part; num_splits holds the exclusive prefix sum of
+ * the number of parts that touch each problem.  Reusable by every layer of
+ * the step as long as cache_seqlens, batch, s_q, h_q and topk are unchanged. */
+mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, int h_q, int topk,
+                            int32_t* sched, int32_t* num_splits, mla_stream_t stream);
+
+/* Arguments of mla_decode.  Pointers are device pointers unless noted. */
+typedef struct {
+  const void* q;                  /* bf16 [batch, s_q, h_q, 576] */
+  int batch, s_q, h_q;
+  const void* kvcache;            /* bf16 [num_pages,64,1,576] or uint8 [num_pages,64,1,656] */
+  int num_pages, page_size;       /* page_size must be 64 */
+  const int32_t* block_table;     /* int32 [batch, block_table_stride] */
+  int block_table_stride;         /* >= ceil(max seqlen / page_size) */
+  const int32_t* cache_seqlens;   /* int32 [batch] */
+  float sm_scale;                 /* softmax scale applied to q.k */
+  int is_causal;                  /* dense only: query token i sees keys <= seqlen - s_q + i */
+  int is_fp8;                     /* 1: FP8 656-byte cache (sparse mode only) */
+  const int32_t* indices;         /* sparse: int32 [batch, s_q, topk]; NULL for dense */
+  int topk;                       /* 0 for dense */
+  const int32_t* sched;           /* from mla_get_metadata with the same batch/s_q/h_q/topk */
+  const int32_t* num_splits;
+  void* workspace;                /* >= mla_workspace_size() bytes, 256-byte aligned */
+  size_t workspace_bytes;
+  void* out;                      /* bf16 [batch, s_q, h_q, 512] */
+  float* lse;                     /* fp32 [batch, s_q, h_q] */
+} mla_decode_args;
+
+/* (2) Decode ("flash_mla_with_kvcache"): split-KV attention kernel followed
+ * by a log-sum-exp combine of the split partials, both on `stream`.
+ * Alignment: q, kvcache, out, lse, workspace 16-byte aligned. */
+mla_status mla_decode(const mla_decode_args* args, mla_stream_t stream);
+
+/* Synchronises `stream`, returns the device status bits accumulated since the
+ * last call in *flags (0 = clean) and clears them.  Returns
+ * MLA_ERR_DEVICE_TIMEOUT / MLA_ERR_DEVICE_BOUNDS when the matching bit is set. */
+mla_status mla_get_device_status(mla_stream_t stream, uint32_t* flags);
+
+/* Thread-local description of the last error returned on this thread
+ * (empty string if none).  The pointer stays valid until the next call. */
+const char* mla_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

@@ -1,0 +1,235 @@
+"""Paged MLA decode for GB300 — thin Python binding over the libmla C ABI.
+
+The binding only marshals arguments: it checks tensor dtypes/devices/shapes
+(raising ValueError that names the argument, the MAX kernel-wrapper
+convention), allocates outputs and scratch with torch when the caller does
+not pass them, and calls the C entry points on the current CUDA stream.
+Every step of decode runs in the library's CUDA kernels; there is no other
+code path.  If ``libmla.so`` has not been built, every call raises.
+
+    sched, num_splits = get_metadata(cache_seqlens, s_q, h_q, topk)
+    out, lse = decode(q, kvcache, block_table, cache_seqlens, sm_scale,
+                      sched, num_splits, is_causal=..., indices=...)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+from . import builder as _build
+
+D_QK = 576
+D_V = 512
+PAGE_SIZE = 64
+FP8_ROW_BYTES = 656
+
+MLA_OK = 0
+STATUS_NAMES = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_WORKSPACE",
+                4: "MLA_ERR_CUDA", 5: "MLA_ERR_DEVICE_BOUNDS", 6: "MLA_ERR_DEVICE_TIMEOUT"}
+DEVICE_BAD_PAGE = 0x1
+DEVICE_TIMEOUT = 0x2
+DEVICE_BAD_SCHEDULE = 0x4
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MLAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class DecodeArgs(ctypes.Structure):
+    """Mirror of ``mla_decode_args`` in include/mla.h."""
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("batch", ctypes.c_int), ("s_q", ctypes.c_int), ("h_q", ctypes.c_int),
+        ("kvcache", ctypes.c_void_p), ("num_pages", ctypes.c_int), ("page_size", ctypes.c_int),
+        ("block_table", ctypes.c_void_p), ("block_table_stride", ctypes.c_int),
+        ("cache_seqlens", ctypes.c_void_p), ("sm_scale", ctypes.c_float), ("is_causal", ctypes.c_int),
+        ("is_fp8", ctypes.c_int), ("indices", ctypes.c_void_p), ("topk", ctypes.c_int),
+        ("sched", ctypes.c_void_p), ("num_splits", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+    ]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libmla.so (built in-tree by ``build()``); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"libmla.so not found at {path}: run paged_mla_decode_07_gb300.build.build()")
+            L = ctypes.CDLL(path)
+            I, P, S = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+            L.mla_abi_version.restype = I
+            L.mla_last_error.restype = ctypes.c_char_p
+            L.mla_metadata_size.argtypes = [I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)]
+            L.mla_metadata_size.restype = I
+            L.mla_workspace_size.argtypes = [I, I, I, I, ctypes.POINTER(S)]
+            L.mla_workspace_size.restype = I
+            L.mla_get_metadata.argtypes = [P, I, I, I, I, P, P, P]
+            L.mla_get_metadata.restype = I
+            L.mla_decode.argtypes = [ctypes.POINTER(DecodeArgs), P]
+            L.mla_decode.restype = I
+            L.mla_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+            L.mla_get_device_status.restype = I
+            _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().mla_last_error().decode()
+
+
+def _check(status: int):
+    if status != MLA_OK:
+        msg = last_error()
+        if status in (1, 2, 3):
+            raise ValueError(f"{STATUS_NAMES[status]}: {msg}")
+        raise MLAError(status, msg)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t, name, dtype, device=None, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must have dtype {dtype} (got {t.dtype})")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device} (got {t.device})")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions (got {tuple(t.shape)})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def metadata_size(batch: int, s_q: int, h_q: int, topk: int = 0) -> Tuple[int, int]:
+    a, b = ctypes.c_int(), ctypes.c_int()
+    _check(lib().mla_metadata_size(batch, s_q, h_q, topk, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def workspace_size(batch: int, s_q: int, h_q: int, topk: int = 0) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().mla_workspace_size(batch, s_q, h_q, topk, ctypes.byref(n)))
+    return n.value
+
+
+def get_metadata(cache_seqlens: torch.Tensor, s_q: int, h_q: int, topk: int = 0, stream=None,
+                 sched: Optional[torch.Tensor] = None, num_splits: Optional[torch.Tensor] = None):
+    """Tile schedule for one decode step; reuse it for every layer of the step."""
+    _need(cache_seqlens, "cache_seqlens", torch.int32, ndim=1)
+    if not cache_seqlens.is_cuda:
+        raise ValueError("cache_seqlens must be a CUDA tensor")
+    dev = cache_seqlens.device
+    batch = cache_seqlens.shape[0]
+    ns, nn = metadata_size(batch, s_q, h_q, topk)
+    if sched is None:
+        sched = torch.empty(ns, dtype=torch.int32, device=dev)
+    if num_splits is None:
+        num_splits = torch.empty(nn, dtype=torch.int32, device=dev)
+    if sched.numel() < ns or num_splits.numel() < nn:
+        raise ValueError("sched / num_splits buffers are too small")
+    _check(lib().mla_get_metadata(ctypes.c_void_p(cache_seqlens.data_ptr()), batch, s_q, h_q, topk,
+                                  ctypes.c_void_p(sched.data_ptr()), ctypes.c_void_p(num_splits.data_ptr()),
+                                  _stream(stream)))
+    return sched, num_splits
+
+
+def decode(q: torch.Tensor, kvcache: torch.Tensor, block_table: torch.Tensor, cache_seqlens: torch.Tensor,
+           sm_scale: float, sched: torch.Tensor, num_splits: torch.Tensor, is_causal: bool = False,
+           indices: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+           lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Paged MLA decode.  Returns (out bf16 [b, s_q, h_q, 512], lse fp32 [b, s_q, h_q], base 2)."""
+    _need(q, "q", torch.bfloat16, ndim=4)
+    if not q.is_cuda:
+        raise ValueError("q must be a CUDA tensor")
+    dev = q.device
+    batch, s_q, h_q, d = q.shape
+    if d != D_QK:
+        raise ValueError(f"q must have last dimension {D_QK} (got {d})")
+    is_fp8 = kvcache.dtype == torch.uint8
+    if is_fp8:
+        _need(kvcache, "kvcache", torch.uint8, dev, 4)
+        if kvcache.shape[-1] != FP8_ROW_BYTES or kvcache.shape[2] != 1:
+            raise ValueError(f"FP8 kvcache must be [pages, page_size, 1, {FP8_ROW_BYTES}]")
+    else:
+        _need(kvcache, "kvcache", torch.bfloat16, dev, 4)
+        if kvcache.shape[-1] != D_QK or kvcache.shape[2] != 1:
+            raise ValueError(f"bf16 kvcache must be [pages, page_size, 1, {D_QK}]")
+    _need(block_table, "block_table", torch.int32, dev, 2)
+    _need(cache_seqlens, "cache_seqlens", torch.int32, dev, 1)
+    if block_table.shape[0] != batch or cache_seqlens.shape[0] != batch:
+        raise ValueError("block_table and cache_seqlens must have batch rows")
+    topk = 0
+    if indices is not None:
+        _need(indices, "indices", torch.int32, dev, 3)
+        if tuple(indices.shape[:2]) != (batch, s_q):
+            raise ValueError(f"indices must be [batch, s_q, topk] (got {tuple(indices.shape)})")
+        topk = indices.shape[2]
+    _need(sched, "sched", torch.int32, dev)
+    _need(num_splits, "num_splits", torch.int32, dev)
+    if out is None:
+        out = torch.empty((batch, s_q, h_q, D_V), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((batch, s_q, h_q), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    if out.numel() != batch * s_q * h_q * D_V or lse.numel() != batch * s_q * h_q:
+        raise ValueError("out / lse have the wrong size")
+    if workspace is None:
+        workspace = torch.empty(max(workspace_size(batch, s_q, h_q, topk), 256), dtype=torch.uint8, device=dev)
+    a = DecodeArgs()
+    a.q = q.data_ptr()
+    a.batch, a.s_q, a.h_q = batch, s_q, h_q
+    a.kvcache = kvcache.data_ptr()
+    a.num_pages, a.page_size = kvcache.shape[0], kvcache.shape[1]
+    a.block_table = block_table.data_ptr()
+    a.block_table_stride = block_table.shape[1]
+    a.cache_seqlens = cache_seqlens.data_ptr()
+    a.sm_scale = float(sm_scale)
+    a.is_causal = int(bool(is_causal))
+    a.is_fp8 = int(is_fp8)
+    a.indices = indices.data_ptr() if indices is not None else None
+    a.topk = topk
+    a.sched = sched.data_ptr()
+    a.num_splits = num_splits.data_ptr()
+    a.workspace = workspace.data_ptr()
+    a.workspace_bytes = workspace.numel() * workspace.element_size()
+    a.out = out.data_ptr()
+    a.lse = lse.data_ptr()
+    _check(lib().mla_decode(ctypes.byref(a), _stream(stream)))
+    return out.view(batch, s_q, h_q, D_V), lse.view(batch, s_q, h_q)
+
+
+def device_status(stream=None, raise_on_error: bool = False) -> int:
+    """Synchronise the stream, return and clear the device status bits."""
+    flags = ctypes.c_uint32()
+    st = lib().mla_get_device_status(_stream(stream), ctypes.byref(flags))
+    if raise_on_error:
+        _check(st)
+    elif st not in (MLA_OK, 5, 6, 1):
+        _check(st)
+    return flags.value
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libmla.so for sm_103a (nvcc) into the package's _build folder."""
+    global _lib
+    path = _build.build(force=force, verbose=verbose)
+    return path

@@ -1,0 +1,343 @@
+// libmla host side: argument validation, geometry, TMA tensor maps, launches,
+// device status and error reporting for the C ABI declared in include/mla.h.
+//
+// Error convention: each entry point checks every argument it can on the
+// host and returns a status code without launching anything on failure; the
+// thread-local message names the offending argument (the validation style of
+// the MAX kernel wrappers, max.nn.kernels module overview).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "mla_internal.h"
+
+namespace mla {
+
+size_t metadata_smem_bytes(int np, int num_parts);
+
+namespace {
+
+thread_local std::string g_error;
+
+mla_status fail(mla_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_error = buf;
+  return s;
+}
+
+mla_status ok() {
+  g_error.clear();
+  return MLA_OK;
+}
+
+mla_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MLA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Device status word: one per device (a module global), its address fetched
+// once per device.
+__device__ uint32_t g_device_status;
+constexpr int kMaxDevices = 64;
+uint32_t* g_status_ptr[kMaxDevices];
+int g_sm_count[kMaxDevices];
+std::mutex g_mu;
+
+mla_status device_info(uint32_t** status, int* sm_count) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(MLA_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_device_status);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    g_status_ptr[dev] = static_cast<uint32_t*>(ptr);
+    g_sm_count[dev] = sms;
+  }
+  if (status) *status = g_status_ptr[dev];
+  if (sm_count) *sm_count = g_sm_count[dev];
+  return MLA_OK;
+}
+
+int sm_count_override() {
+  const char* s = getenv("MLA_NUM_PARTS");
+  return s ? atoi(s) : 0;
+}
+
+mla_status geometry(int batch, int s_q, int h_q, int topk, Geometry* g) {
+  if (batch < 1) return fail(MLA_ERR_INVALID_ARG, "batch must be >= 1 (got %d)", batch);
+  if (s_q < 1) return fail(MLA_ERR_INVALID_ARG, "s_q must be >= 1 (got %d)", s_q);
+  if (h_q < 1) return fail(MLA_ERR_INVALID_ARG, "h_q must be >= 1 (got %d)", h_q);
+  if (topk < 0) return fail(MLA_ERR_INVALID_ARG, "topk must be >= 0 (got %d)", topk);
+  const long long np = topk > 0 ? static_cast<long long>(batch) * s_q : batch;
+  const long long rows = topk > 0 ? h_q : static_cast<long long>(s_q) * h_q;
+  if (np > kMaxProblems)
+    return fail(MLA_ERR_UNSUPPORTED, "%s = %lld exceeds the supported %d problems",
+                topk > 0 ? "batch*s_q" : "batch", np, kMaxProblems);
+  if (rows > 1024)
+    return fail(MLA_ERR_UNSUPPORTED, "%s = %lld query rows per problem exceeds 1024",
+                topk > 0 ? "h_q" : "s_q*h_q", rows);
+  if (topk > (1 << 24)) return fail(MLA_ERR_UNSUPPORTED, "topk = %d too large", topk);
+  int sms = 0;
+  mla_status st = device_info(nullptr, &sms);
+  if (st != MLA_OK) return st;
+  const int ov = sm_count_override();
+  if (ov > 0) sms = ov;
+  g->num_problems = static_cast<int>(np);
+  g->rows = static_cast<int>(rows);
+  g->rpc = rows_per_cta(g->rows);
+  g->row_groups = (g->rows + g->rpc - 1) / g->rpc;
+  g->sm_count = sms;
+  g->num_parts = sms / g->row_groups;
+  if (g->num_parts < 1) g->num_parts = 1;
+  return MLA_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+void workspace_layout(const Geometry& g, size_t* o_bytes, size_t* lse_bytes) {
+  const size_t slots = static_cast<size_t>(g.num_problems) + g.num_parts;
+  *o_bytes = align256(slots * g.rows * kDv * sizeof(float));
+  *lse_bytes = align256(slots * g.rows * sizeof(float));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 576-wide bf16 rows viewed as [rows][9 chunks][64]: dim0 = 64 elements
+// (128 B, the swizzle atom width), dim1 = chunk (stride 128 B), dim2 = row
+// (stride 1152 B).  A box of {64, 1, box_rows} lands in shared memory as
+// box_rows x 128 B with the 128-byte swizzle, the canonical K-major operand
+// layout of the tcgen05 MMAs.
+mla_status encode_rows_map(CUtensorMap* map, const void* base, long long nrows, int box_rows, const char* what) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint64_t dims[3] = {64, 9, static_cast<cuuint64_t>(nrows)};
+  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(kDqk * 2)};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what, (int)r);
+  return MLA_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+uint64_t watchdog_ns() {
+  const char* s = getenv("MLA_WATCHDOG_NS");
+  if (s) {
+    unsigned long long v = strtoull(s, nullptr, 10);
+    if (v > 0) return v;
+  }
+  return 2000000000ull;  // 2 s: far above any legitimate wait, short enough to unwind quickly
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+int mla_abi_version(void) { return MLA_ABI_VERSION; }
+
+const char* mla_last_error(void) { return g_error.c_str(); }
+
+mla_status mla_metadata_size(int batch, int s_q, int h_q, int topk, int* sched_elems, int* num_splits_elems) {
+  if (!sched_elems) return fail(MLA_ERR_INVALID_ARG, "sched_elems is NULL");
+  if (!num_splits_elems) return fail(MLA_ERR_INVALID_ARG, "num_splits_elems is NULL");
+  Geometry g{};
+  mla_status st = geometry(batch, s_q, h_q, topk, &g);
+  if (st != MLA_OK) return st;
+  *sched_elems = g.num_parts * kSchedInts;
+  *num_splits_elems = g.num_problems + 1;
+  return ok();
+}
+
+mla_status mla_workspace_size(int batch, int s_q, int h_q, int topk, size_t* bytes) {
+  if (!bytes) return fail(MLA_ERR_INVALID_ARG, "bytes is NULL");
+  Geometry g{};
+  mla_status st = geometry(batch, s_q, h_q, topk, &g);
+  if (st != MLA_OK) return st;
+  size_t ob, lb;
+  workspace_layout(g, &ob, &lb);
+  *bytes = ob + lb;
+  return ok();
+}
+
+mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, int h_q, int topk, int32_t* sched,
+                            int32_t* num_splits, mla_stream_t stream) {
+  if (!cache_seqlens) return fail(MLA_ERR_INVALID_ARG, "cache_seqlens is NULL");
+  if (!sched) return fail(MLA_ERR_INVALID_ARG, "sched is NULL");
+  if (!num_splits) return fail(MLA_ERR_INVALID_ARG, "num_splits is NULL");
+  Geometry g{};
+  mla_status st = geometry(batch, s_q, h_q, topk, &g);
+  if (st != MLA_OK) return st;
+  uint32_t* status = nullptr;
+  st = device_info(&status, nullptr);
+  if (st != MLA_OK) return st;
+  cudaError_t e = launch_metadata(cache_seqlens, batch, s_q, h_q, topk, g, sched, num_splits, status,
+                                  reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "metadata kernel launch");
+  return ok();
+}
+
+mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
+  if (!a) return fail(MLA_ERR_INVALID_ARG, "args is NULL");
+  const bool sparse = a->topk > 0;
+  if (a->topk < 0) return fail(MLA_ERR_INVALID_ARG, "topk must be >= 0 (got %d)", a->topk);
+  if (!a->q) return fail(MLA_ERR_INVALID_ARG, "q is NULL");
+  if (!a->kvcache) return fail(MLA_ERR_INVALID_ARG, "kvcache is NULL");
+  if (!a->block_table) return fail(MLA_ERR_INVALID_ARG, "block_table is NULL");
+  if (!a->cache_seqlens) return fail(MLA_ERR_INVALID_ARG, "cache_seqlens is NULL");
+  if (!a->sched) return fail(MLA_ERR_INVALID_ARG, "sched is NULL");
+  if (!a->num_splits) return fail(MLA_ERR_INVALID_ARG, "num_splits is NULL");
+  if (!a->out) return fail(MLA_ERR_INVALID_ARG, "out is NULL");
+  if (!a->lse) return fail(MLA_ERR_INVALID_ARG, "lse is NULL");
+  if (sparse && !a->indices) return fail(MLA_ERR_INVALID_ARG, "indices is NULL with topk = %d", a->topk);
+  if (!sparse && a->indices) return fail(MLA_ERR_INVALID_ARG, "indices given with topk = 0");
+  if (a->page_size != kPageSize)
+    return fail(MLA_ERR_UNSUPPORTED, "page_size must be %d (got %d)", kPageSize, a->page_size);
+  if (a->num_pages < 1) return fail(MLA_ERR_INVALID_ARG, "num_pages must be >= 1 (got %d)", a->num_pages);
+  if (static_cast<long long>(a->num_pages) * kPageSize > (1ll << 31) - 1)
+    return fail(MLA_ERR_UNSUPPORTED, "num_pages = %d exceeds 2^31 tokens", a->num_pages);
+  if (a->block_table_stride < 1)
+    return fail(MLA_ERR_INVALID_ARG, "block_table_stride must be >= 1 (got %d)", a->block_table_stride);
+  if (a->is_fp8 && !sparse)
+    return fail(MLA_ERR_UNSUPPORTED, "is_fp8 = 1 requires sparse mode (topk > 0): dense decode reads a bf16 cache");
+  if (!a->is_fp8 && sparse)
+    return fail(MLA_ERR_UNSUPPORTED, "sparse mode (topk > 0) requires the FP8 cache (is_fp8 = 1)");
+  if (a->is_causal && sparse) return fail(MLA_ERR_UNSUPPORTED, "is_causal applies to dense mode only");
+  if (!std::isfinite(a->sm_scale)) return fail(MLA_ERR_INVALID_ARG, "sm_scale is not finite");
+  if (!aligned(a->q, 16)) return fail(MLA_ERR_INVALID_ARG, "q is not 16-byte aligned");
+  if (!aligned(a->kvcache, 16)) return fail(MLA_ERR_INVALID_ARG, "kvcache is not 16-byte aligned");
+  if (!aligned(a->out, 16)) return fail(MLA_ERR_INVALID_ARG, "out is not 16-byte aligned");
+  if (!aligned(a->lse, 4)) return fail(MLA_ERR_INVALID_ARG, "lse is not 4-byte aligned");
+  if (!aligned(a->block_table, 4)) return fail(MLA_ERR_INVALID_ARG, "block_table is not 4-byte aligned");
+
+  Geometry g{};
+  mla_status st = geometry(a->batch, a->s_q, a->h_q, a->topk, &g);
+  if (st != MLA_OK) return st;
+  size_t ob, lb;
+  workspace_layout(g, &ob, &lb);
+  if (!a->workspace) return fail(MLA_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", ob + lb);
+  if (a->workspace_bytes < ob + lb)
+    return fail(MLA_ERR_WORKSPACE, "workspace_bytes = %zu < %zu needed", a->workspace_bytes, ob + lb);
+  if (!aligned(a->workspace, 256)) return fail(MLA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+
+  uint32_t* status = nullptr;
+  st = device_info(&status, nullptr);
+  if (st != MLA_OK) return st;
+
+  CUtensorMap tm_q, tm_kv;
+  const long long qrows = static_cast<long long>(a->batch) * a->s_q * a->h_q;
+  st = encode_rows_map(&tm_q, a->q, qrows, g.rpc, "q");
+  if (st != MLA_OK) return st;
+  if (!sparse) {
+    st = encode_rows_map(&tm_kv, a->kvcache, static_cast<long long>(a->num_pages) * kPageSize, kPageSize,
+                         "kvcache");
+    if (st != MLA_OK) return st;
+  } else {
+    tm_kv = tm_q;  // unused in sparse mode (the FP8 rows are gathered with plain loads)
+  }
+
+  DecodeParams p;
+  memset(&p, 0, sizeof p);
+  p.block_table = a->block_table;
+  p.cache_seqlens = a->cache_seqlens;
+  p.indices = a->indices;
+  p.sched = a->sched;
+  p.num_splits = a->num_splits;
+  p.kv_fp8 = static_cast<const uint8_t*>(a->kvcache);
+  p.out = a->out;
+  p.lse = a->lse;
+  p.o_accum = static_cast<float*>(a->workspace);
+  p.lse_accum = reinterpret_cast<float*>(static_cast<char*>(a->workspace) + ob);
+  p.status = status;
+  p.timeout_ns = watchdog_ns();
+  p.batch = a->batch;
+  p.s_q = a->s_q;
+  p.h_q = a->h_q;
+  p.topk = a->topk;
+  p.num_pages = a->num_pages;
+  p.block_table_stride = a->block_table_stride;
+  p.num_problems = g.num_problems;
+  p.rows = g.rows;
+  p.row_groups = g.row_groups;
+  p.num_parts = g.num_parts;
+  p.max_slots = g.num_problems + g.num_parts;
+  p.is_causal = a->is_causal ? 1 : 0;
+  p.evict_first = g.row_groups == 1 ? 1 : 0;
+  p.scale_log2 = a->sm_scale * 1.4426950408889634f;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode(tm_q, tm_kv, p, g.rpc, sparse, s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+
+  CombineParams cp;
+  cp.num_splits = a->num_splits;
+  cp.o_accum = p.o_accum;
+  cp.lse_accum = p.lse_accum;
+  cp.out = a->out;
+  cp.lse = a->lse;
+  cp.num_problems = g.num_problems;
+  cp.rows = g.rows;
+  cp.max_slots = p.max_slots;
+  cp.status = status;
+  e = launch_combine(cp, s, true);
+  if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
+  return ok();
+}
+
+mla_status mla_get_device_status(mla_stream_t stream, uint32_t* flags) {
+  if (!flags) return fail(MLA_ERR_INVALID_ARG, "flags is NULL");
+  uint32_t* status = nullptr;
+  mla_status st = device_info(&status, nullptr);
+  if (st != MLA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  uint32_t v = 0;
+  e = cudaMemcpyAsync(&v, status, sizeof v, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof v, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  *flags = v;
+  if (v & MLA_DEVICE_TIMEOUT) return fail(MLA_ERR_DEVICE_TIMEOUT, "a kernel wait exceeded its limit (status 0x%x)", v);
+  if (v & MLA_DEVICE_BAD_PAGE)
+    return fail(MLA_ERR_DEVICE_BOUNDS, "a block-table entry was outside [0, num_pages) (status 0x%x)", v);
+  if (v & MLA_DEVICE_BAD_SCHEDULE)
+    return fail(MLA_ERR_INVALID_ARG, "the schedule did not match the decode arguments (status 0x%x)", v);
+  return ok();
+}
+
+}  // extern "C"

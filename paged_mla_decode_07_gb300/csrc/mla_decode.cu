@@ -1,0 +1,717 @@
+// K1 — split-KV paged MLA decode on sm_103a (tcgen05 tensor cores, TMEM
+// accumulators, TMA), dense bf16 and sparse FP8 modes.
+//
+// What is computed (per query row r of a problem and a range of its keys):
+// out = softmax(q K^T * sm_scale) V with V = K[:, :512] — the MQA form of MLA
+// (Modular design-doc overview, section 9 "Multi-Head Latent Attention") —
+// with online softmax across 128-token tiles (overview, section 6 "Matmul to
+// Flash Attention": running row max, exp(old_max - new_max) correction of
+// the running sum and output).  A CTA covering only part of a problem's keys
+// writes an fp32 partial and its log-sum-exp for the combine kernel
+// ("split-KV", FlashMLA article, Design 5; overview, section 6).
+//
+// Formulation: the MMAs run transposed, as proposed in the overview's section
+// 8 "U/WGMMA Flash Decoding" (option 0: P goes back through shared memory):
+//     S^T[tok, row] = K[tok, :] . Q[row, :]^T      M = 128 tokens, N = rows, K = 576
+//     O^T[dv, row] += V^T[dv, tok] . P^T[tok, row]  M = 128 dv (x4),  N = rows, K = 128 tokens
+// so every tcgen05.mma has M = 128 whatever the head count, and the fp32
+// accumulator O^T (4*rows TMEM columns) fits beside S^T in 512 columns.
+// The same shared-memory K tile is the K-major A operand of the first MMA and
+// (dims 0..511) the MN-major A operand of the second; no separate V load.
+//
+// Shared memory (1024-byte aligned):
+//   KV tile : 9 chunks x [128 tokens][64 dims] bf16, 128-byte swizzle  (144 KB)
+//   Q       : 9 chunks x [rows][64 dims] bf16, 128-byte swizzle        (rows*1152 B)
+//   P       : [2][rows][64 tokens] bf16, aliases KV chunk 8 (RoPE dims),
+//             which is dead once S^T of the tile is computed
+//   barriers, row statistics
+// TMEM: O^T at columns [0, 4*rows), S^T double buffer at [4*rows, 6*rows).
+//
+// Warp roles: warp 0 = TMA producer (Q; dense KV pages), warp 1 = MMA
+// issuer, warp 2 = TMEM allocator, warps 4-7 = softmax + epilogue (thread t
+// owns token t of the tile and TMEM lane t), sparse only: warps 8-11 = FP8
+// gather + dequantisation (thread t fills token t of the tile).
+//
+// The FP8 row (FlashMLA article, Design 2): 512 e4m3 codes, 4 fp32 scales
+// (one per 128 dims), 64 bf16 RoPE values; dequantised value =
+// bf16_rn(fp32(e4m3) * scale), computed here as e4m3x2 -> f16x2 (exact),
+// f16 -> f32 (exact), one fp32 multiply, cvt.rn to bf16.
+//
+// Every wait is bounded (watchdog); on expiry the CTA records
+// MLA_DEVICE_TIMEOUT, all roles unwind, in-flight copies and MMAs are drained
+// with a bounded wait, and TMEM is freed.
+#include "mla_device.cuh"
+#include "mla_internal.h"
+
+namespace mla {
+namespace {
+
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 before a max update is forced
+
+template <int R, bool SPARSE>
+struct Cfg {
+  static constexpr int kWarps = SPARSE ? 12 : 8;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kKvChunkBytes = kTileTokens * 128;  // 16 KB
+  static constexpr int kKvBytes = kNumChunks * kKvChunkBytes;
+  static constexpr int kQChunkBytes = R * 128;
+  static constexpr int kQOff = kKvBytes;
+  static constexpr int kQBytes = kNumChunks * kQChunkBytes;
+  static constexpr int kPOff = 8 * kKvChunkBytes;
+  static constexpr int kPHalfBytes = R * 128;  // [R rows][64 tokens] bf16
+  static constexpr int kAuxOff = kQOff + kQBytes;
+  // barriers
+  static constexpr int kNumBars = 2 + 2 * kNumChunks + 4 + 3 + 2;
+  static constexpr int kBarBytes = kNumBars * 8;
+  // aux floats: m[R], alpha[R], inv_l[R], lse[R], red[4][R]; ints: vote[2][4], abort, tmem
+  static constexpr int kAuxBytes = kBarBytes + 8 * R * 4 + 64;
+  static constexpr int kSmemBytes = kAuxOff + kAuxBytes + 1024;  // + alignment slack
+  static constexpr int kOCol = 0;
+  static constexpr int kSCol = 4 * R;
+  static constexpr int kTmemCols = (6 * R <= 128) ? 128 : ((6 * R <= 256) ? 256 : 512);
+  static_assert(2 * kPHalfBytes <= kKvChunkBytes, "P must fit in the RoPE chunk");
+  static_assert(R == 16 || R == 32 || R == 64, "rows per CTA");
+};
+
+struct Bars {
+  uint64_t* q_full;
+  uint64_t* q_empty;
+  uint64_t* kv_full;   // [9]
+  uint64_t* kv_empty;  // [9]
+  uint64_t* s_full;    // [2]
+  uint64_t* s_empty;   // [2]
+  uint64_t* p_full;
+  uint64_t* o_full;
+  uint64_t* o_empty;
+  uint64_t* mma_done;
+  uint64_t* grp;       // softmax group barrier (128 threads)
+};
+
+// Segment iterator shared by all roles: the part walks problems p0..p1 and,
+// inside each, a tile range.  All roles derive the identical sequence.
+struct Segments {
+  int p0, t0, p1, t1, np, s_q, topk;
+  const int32_t* seqlens;
+  __device__ int last() const { return p1 < np ? p1 : np - 1; }
+  __device__ void range(int p, int& tb, int& te) const {
+    int n = problem_tiles(seqlens, p, s_q, topk);
+    tb = (p == p0) ? t0 : 0;
+    te = (p == p1) ? t1 : n;
+    if (te > n) te = n;
+  }
+};
+
+// Bounded wait that ignores the abort flag (used to drain own async work).
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
+// Warp-uniform bounded wait: if any lane fails, every lane sees failure.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
+  bool ok = mbar_wait(bar, parity, wd);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// 128-thread group barrier on an mbarrier (bounded; see Watchdog).
+__device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& phase, const Watchdog& wd) {
+  mbar_arrive(bar);
+  bool ok = warp_wait(bar, phase & 1, wd);
+  ++phase;
+  return ok;
+}
+
+// ---------------------------------------------------------------------------
+// producer: Q (always) and dense KV pages by TMA
+// ---------------------------------------------------------------------------
+template <int R, bool SPARSE>
+__device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, const DecodeParams& p,
+                         const Segments& sg, int g, uint8_t* kv, uint8_t* qs, const Bars& bars,
+                         const Watchdog& wd) {
+  using C = Cfg<R, SPARSE>;
+  const uint64_t pol_kv = p.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
+  const uint64_t pol_q = l2_policy_evict_normal();
+  int armed[kNumChunks];
+#pragma unroll
+  for (int c = 0; c < kNumChunks; ++c) armed[c] = 0;
+  int q_armed = 0, jt = 0;
+  for (int prob = sg.p0; prob <= sg.last(); ++prob) {
+    int tb, te;
+    sg.range(prob, tb, te);
+    if (tb >= te) continue;
+    if (q_armed > 0 && !mbar_wait(bars.q_empty, (q_armed - 1) & 1, wd)) goto drain;
+    {
+      const int row0 = prob * p.rows + g * R;
+      mbar_arrive_expect_tx(bars.q_full, kNumChunks * C::kQChunkBytes);
+#pragma unroll 1
+      for (int c = 0; c < kNumChunks; ++c)
+        tma_load_3d(qs + c * C::kQChunkBytes, tm_q, bars.q_full, 0, c, row0, pol_q);
+      ++q_armed;
+    }
+    if (!SPARSE) {
+      const int b = prob;
+      const int L = sg.seqlens[b];
+      const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
+      for (int j = tb; j < te; ++j, ++jt) {
+        const bool in_a = 2 * j < p.block_table_stride;
+        const bool has_b = kTileTokens * j + kPageSize < L;
+        const bool in_b = has_b && 2 * j + 1 < p.block_table_stride;
+        const int pa = in_a ? bt[2 * j] : -1;
+        const int pb = in_b ? bt[2 * j + 1] : -1;
+        const bool ok_a = pa >= 0 && pa < p.num_pages;
+        const bool ok_b = has_b && pb >= 0 && pb < p.num_pages;
+        if (!ok_a || (has_b && !ok_b)) atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
+        const uint32_t bytes = (ok_a ? 8192u : 0u) + (ok_b ? 8192u : 0u);
+#pragma unroll 1
+        for (int c = 0; c < kNumChunks; ++c) {
+          if (armed[c] > 0 && !mbar_wait(bars.kv_empty + c, (armed[c] - 1) & 1, wd)) goto drain;
+          mbar_arrive_expect_tx(bars.kv_full + c, bytes);
+          uint8_t* dst = kv + c * C::kKvChunkBytes;
+          if (ok_a) tma_load_3d(dst, tm_kv, bars.kv_full + c, 0, c, pa * kPageSize, pol_kv);
+          if (ok_b) tma_load_3d(dst + 8192, tm_kv, bars.kv_full + c, 0, c, pb * kPageSize, pol_kv);
+          ++armed[c];
+        }
+      }
+    }
+  }
+drain:
+  // wait (bounded) for this thread's own copies still in flight
+  if (!SPARSE) {
+#pragma unroll 1
+    for (int c = 0; c < kNumChunks; ++c)
+      if (armed[c] > 0) mbar_wait_drain(bars.kv_full + c, (armed[c] - 1) & 1, wd.limit_ns);
+  }
+  if (q_armed > 0) mbar_wait_drain(bars.q_full, (q_armed - 1) & 1, wd.limit_ns);
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer (one thread)
+// ---------------------------------------------------------------------------
+template <int R, bool SPARSE>
+__device__ void mma_issuer(const Segments& sg, uint32_t tmem, uint8_t* kv, uint8_t* qs, const Bars& bars,
+                           const Watchdog& wd) {
+  using C = Cfg<R, SPARSE>;
+  constexpr uint32_t kIdS = idesc_bf16_f32(128, R, 0, 0);  // A = K tile (K-major), B = Q (K-major)
+  constexpr uint32_t kIdO = idesc_bf16_f32(128, R, 1, 0);  // A = V^T (MN-major), B = P (K-major)
+  const uint32_t kv_base = smem_u32(kv);
+  const uint32_t q_base = smem_u32(qs);
+  const uint32_t p_base = kv_base + C::kPOff;
+  int jt = 0, seg = 0;
+  for (int prob = sg.p0; prob <= sg.last(); ++prob) {
+    int tb, te;
+    sg.range(prob, tb, te);
+    if (tb >= te) continue;
+    if (!mbar_wait(bars.q_full, seg & 1, wd)) goto done;
+    tc_fence_after();
+    for (int j = tb; j < te; ++j, ++jt) {
+      const int sb = jt & 1;
+      if (jt >= 2 && !mbar_wait(bars.s_empty + sb, ((jt >> 1) - 1) & 1, wd)) goto done;
+      tc_fence_after();
+      const uint32_t d_s = tmem + C::kSCol + sb * R;
+#pragma unroll 1
+      for (int c = 0; c < kNumChunks; ++c) {
+        if (!mbar_wait(bars.kv_full + c, jt & 1, wd)) goto done;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t a = smem_desc(kv_base + c * C::kKvChunkBytes + kk * 32, 16, 1024);
+          const uint64_t b = smem_desc(q_base + c * C::kQChunkBytes + kk * 32, 16, 1024);
+          umma_bf16_ss(d_s, a, b, kIdS, (c | kk) != 0);
+        }
+      }
+      umma_commit(bars.s_full + sb);
+      if (j == te - 1) umma_commit(bars.q_empty);
+      if (!mbar_wait(bars.p_full, jt & 1, wd)) goto done;
+      tc_fence_after();
+      if (j == tb && seg > 0) {
+        if (!mbar_wait(bars.o_empty, (seg - 1) & 1, wd)) goto done;
+        tc_fence_after();
+      }
+#pragma unroll 1
+      for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a = smem_desc(kv_base + 2 * blk * C::kKvChunkBytes + kk * 2048, C::kKvChunkBytes, 1024);
+          const uint64_t b = smem_desc(p_base + (kk >> 2) * C::kPHalfBytes + (kk & 3) * 32, 16, 1024);
+          umma_bf16_ss(tmem + C::kOCol + blk * R, a, b, kIdO, !(j == tb && kk == 0));
+        }
+        umma_commit(bars.kv_empty + 2 * blk);
+        umma_commit(bars.kv_empty + 2 * blk + 1);
+      }
+      umma_commit(bars.kv_empty + 8);
+      if (j == te - 1) umma_commit(bars.o_full);
+    }
+    ++seg;
+  }
+done:
+  umma_commit(bars.mma_done);
+  mbar_wait_drain(bars.mma_done, 0, wd.limit_ns);
+}
+
+// ---------------------------------------------------------------------------
+// FP8 gather + dequantisation (sparse, 128 threads; thread t -> token t)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t dequant2(uint32_t codes16, float scale) {
+  const uint32_t h2 = e4m3x2_to_f16x2(static_cast<uint16_t>(codes16));
+  const float lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu)));
+  const float hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+  return pack_bf16x2(lo * scale, hi * scale);
+}
+
+template <int R>
+__device__ void gather_fp8(const DecodeParams& p, const Segments& sg, uint8_t* kv, const Bars& bars,
+                           const Watchdog& wd) {
+  using C = Cfg<R, true>;
+  const int tid = threadIdx.x - 256;
+  const uint32_t row_addr = smem_u32(kv) + tid * 128;
+  const uint32_t sw = tid & 7;
+  int jt = 0;
+  for (int prob = sg.p0; prob <= sg.last(); ++prob) {
+    int tb, te;
+    sg.range(prob, tb, te);
+    if (tb >= te) continue;
+    const int b = prob / p.s_q;
+    const int L = sg.seqlens[b];
+    const int32_t* idx_row = p.indices + static_cast<int64_t>(prob) * p.topk;
+    const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
+    int t_next = (tb * kTileTokens + tid < p.topk) ? idx_row[tb * kTileTokens + tid] : -1;
+    for (int j = tb; j < te; ++j, ++jt) {
+      const int t = t_next;
+      {
+        const int kn = (j + 1) * kTileTokens + tid;
+        t_next = (j + 1 < te && kn < p.topk) ? idx_row[kn] : -1;
+      }
+      bool ok = t >= 0 && t < L;
+      const bool in_table = ok && (t >> 6) < p.block_table_stride;
+      int page = in_table ? bt[t >> 6] : -1;
+      if (ok && (page < 0 || page >= p.num_pages)) {
+        ok = false;
+        page = 0;
+        atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
+      }
+      const uint8_t* src = p.kv_fp8 + (static_cast<int64_t>(page) * kPageSize + (t & 63)) * kFp8RowBytes;
+      uint4 cs[33];  // 512 codes + 4 scales
+#pragma unroll
+      for (int i = 0; i < 33; ++i) cs[i] = ok ? ld_global_nc_v4(src + 16 * i) : make_uint4(0, 0, 0, 0);
+      uint4 rope[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        if (jt > 0 && !warp_wait(bars.kv_empty + c, (jt - 1) & 1, wd)) return;
+        const uint32_t sw_word = (c >> 1) == 0 ? cs[32].x : ((c >> 1) == 1 ? cs[32].y : ((c >> 1) == 2 ? cs[32].z : cs[32].w));
+        const float scale = __uint_as_float(sw_word);
+        const uint32_t base = row_addr + c * C::kKvChunkBytes;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 v = cs[4 * c + (q >> 1)];
+          const uint32_t w0 = (q & 1) ? v.z : v.x;
+          const uint32_t w1 = (q & 1) ? v.w : v.y;
+          st_shared_v4(base + ((q ^ sw) << 4), dequant2(w0 & 0xffffu, scale), dequant2(w0 >> 16, scale),
+                       dequant2(w1 & 0xffffu, scale), dequant2(w1 >> 16, scale));
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bars.kv_full + c);
+        if (c == 1) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) rope[i] = ok ? ld_global_nc_v4(src + 528 + 16 * i) : make_uint4(0, 0, 0, 0);
+        }
+      }
+      if (jt > 0 && !warp_wait(bars.kv_empty + 8, (jt - 1) & 1, wd)) return;
+      {
+        const uint32_t base = row_addr + 8 * C::kKvChunkBytes;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) st_shared_v4(base + ((q ^ sw) << 4), rope[q].x, rope[q].y, rope[q].z, rope[q].w);
+        fence_proxy_async_smem();
+        mbar_arrive(bars.kv_full + 8);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// softmax + epilogue (128 threads; thread t -> token t of the tile, TMEM lane t)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <int R, bool SPARSE>
+__device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int g, int split0, uint32_t tmem,
+                                 uint8_t* kv, const Bars& bars, float* aux, int* vote, const Watchdog& wd) {
+  using C = Cfg<R, SPARSE>;
+  const int tid = threadIdx.x - 128;
+  const int warp_q = (threadIdx.x >> 5) & 3;
+  const int lane = threadIdx.x & 31;
+  const uint32_t lane_base = static_cast<uint32_t>(warp_q * 32) << 16;
+  float* m_s = aux;            // running row max (log2 units)
+  float* alpha_s = aux + R;    // rescale factors
+  float* inv_s = aux + 2 * R;  // 1 / row sum
+  float* lse_s = aux + 3 * R;  // row lse
+  float* red = aux + 4 * R;    // [4][R] cross-warp reduction
+  const uint32_t p_base = smem_u32(kv) + C::kPOff;
+  const uint32_t p_row_off = (tid >> 6) * C::kPHalfBytes + (tid & 7) * 2;
+  const uint32_t p_chunk = (tid & 63) >> 3;
+  uint32_t gphase = 0;
+  int jt = 0, seg = 0;
+  float l[R];
+
+  for (int prob = sg.p0; prob <= sg.last(); ++prob) {
+    int tb, te;
+    sg.range(prob, tb, te);
+    if (tb >= te) continue;
+    const int b = SPARSE ? prob / p.s_q : prob;
+    const int L = sg.seqlens[b];
+    const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
+    const int32_t* idx_row = SPARSE ? p.indices + static_cast<int64_t>(prob) * p.topk : nullptr;
+    // causal limit per row: query token i sees keys <= L - s_q + i (dense only)
+    int lim_min = L - 1;
+    if (!SPARSE && p.is_causal) {
+      const int i_first = (g * R) / p.h_q;
+      lim_min = min(L - 1, L - p.s_q + i_first);
+    }
+    if (tid < R) m_s[tid] = kNegInf;
+#pragma unroll
+    for (int r = 0; r < R; ++r) l[r] = 0.f;
+    if (!group_sync(bars.grp, gphase, wd)) return;
+
+    for (int j = tb; j < te; ++j, ++jt) {
+      const int sb = jt & 1;
+      // token validity (loads issued before the wait for S)
+      int pos;
+      bool tok_ok;
+      if (SPARSE) {
+        const int k = j * kTileTokens + tid;
+        pos = k < p.topk ? idx_row[k] : -1;
+        tok_ok = pos >= 0 && pos < L && (pos >> 6) < p.block_table_stride;
+        if (tok_ok) {
+          const int pg = bt[pos >> 6];
+          tok_ok = pg >= 0 && pg < p.num_pages;
+        }
+      } else {
+        pos = j * kTileTokens + tid;
+        tok_ok = pos < L && (pos >> 6) < p.block_table_stride;
+        if (tok_ok) {
+          const int pg = bt[pos >> 6];
+          tok_ok = pg >= 0 && pg < p.num_pages;
+        }
+      }
+      if (!warp_wait(bars.s_full + sb, (jt >> 1) & 1, wd)) return;
+      tc_fence_after();
+      float x[R];
+#pragma unroll
+      for (int q = 0; q < R / 16; ++q) {
+        float v[16];
+        tmem_ld_x16(tmem + lane_base + C::kSCol + sb * R + 16 * q, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[16 * q + e] = v[e];
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(bars.s_empty + sb);
+
+      // logits in log2 units, masked -> -inf
+      const bool all_rows = tok_ok && (SPARSE || pos <= lim_min);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        bool ok = all_rows;
+        if (!SPARSE && !all_rows && tok_ok) {
+          const int fr = g * R + r;
+          const int lim = p.is_causal ? L - p.s_q + fr / p.h_q : L - 1;
+          ok = pos <= lim;
+        }
+        x[r] = ok ? x[r] * p.scale_log2 : kNegInf;
+      }
+
+      // lazy max update: only when some logit exceeds the running max by the threshold
+      bool need = (j == tb);
+      if (!need) {
+        float loc = kNegInf;
+#pragma unroll
+        for (int r = 0; r < R; ++r) loc = fmaxf(loc, x[r] - m_s[r]);
+        const bool w_need = __any_sync(0xffffffffu, loc > kRescaleThreshold);
+        if (lane == 0) vote[(jt & 1) * 4 + warp_q] = w_need ? 1 : 0;
+        if (!group_sync(bars.grp, gphase, wd)) return;
+        const int* vv = vote + (jt & 1) * 4;
+        need = (vv[0] | vv[1] | vv[2] | vv[3]) != 0;
+      }
+      if (need) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float v = warp_max(x[r]);
+          if (lane == (r & 31)) red[warp_q * R + r] = v;
+        }
+        if (!group_sync(bars.grp, gphase, wd)) return;
+        if (tid < R) {
+          const float mx = fmaxf(fmaxf(red[tid], red[R + tid]), fmaxf(red[2 * R + tid], red[3 * R + tid]));
+          const float mo = m_s[tid];
+          const float mn = fmaxf(mo, mx);
+          alpha_s[tid] = (mo == kNegInf) ? 0.f : fast_exp2(mo - mn);
+          m_s[tid] = mn;
+        }
+        if (!group_sync(bars.grp, gphase, wd)) return;
+#pragma unroll
+        for (int r = 0; r < R; ++r) l[r] *= alpha_s[r];
+        if (j != tb) {
+          // O^T of the previous tiles is complete (its MMAs precede this tile's S^T);
+          // rescale each row's column by alpha.
+#pragma unroll 1
+          for (int blk = 0; blk < 4; ++blk) {
+#pragma unroll
+            for (int q = 0; q < R / 16; ++q) {
+              float v[16];
+              const uint32_t ta = tmem + lane_base + C::kOCol + blk * R + 16 * q;
+              tmem_ld_x16(ta, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) v[e] *= alpha_s[16 * q + e];
+              tmem_st_x16(ta, v);
+            }
+          }
+          tmem_st_wait();
+        }
+      }
+
+      // probabilities -> P (bf16, K-major 128B-swizzled [2][R][64 tokens]) and row sums
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float mr = m_s[r];
+        const float pr = (x[r] == kNegInf) ? 0.f : fast_exp2(x[r] - mr);
+        l[r] += pr;
+        const uint32_t addr = p_base + p_row_off + r * 128 + ((p_chunk ^ (r & 7)) << 4);
+        st_shared_u16(addr, __bfloat16_as_ushort(__float2bfloat16_rn(pr)));
+      }
+      if (!SPARSE && !tok_ok) {
+        // a masked token's V row must be finite (0 * NaN would poison O): zero it
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t base = smem_u32(kv) + c * C::kKvChunkBytes + tid * 128;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) st_shared_v4(base + 16 * q, 0u, 0u, 0u, 0u);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bars.p_full);
+    }
+
+    // ---- epilogue: O / l -> out (single piece) or fp32 partial (split problem)
+    if (!warp_wait(bars.o_full, seg & 1, wd)) return;
+    tc_fence_after();
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const float v = warp_sum(l[r]);
+      if (lane == (r & 31)) red[warp_q * R + r] = v;
+    }
+    if (!group_sync(bars.grp, gphase, wd)) return;
+    if (tid < R) {
+      const float lt = red[tid] + red[R + tid] + red[2 * R + tid] + red[3 * R + tid];
+      inv_s[tid] = lt > 0.f ? 1.0f / lt : 0.f;
+      lse_s[tid] = lt > 0.f ? m_s[tid] + log2f(lt) : kNegInf;
+    }
+    if (!group_sync(bars.grp, gphase, wd)) return;
+    const int nsplit = p.num_splits[prob + 1] - p.num_splits[prob];
+    const bool final_out = nsplit == 1;
+    int slot = p.num_splits[prob] + (prob == sg.p0 ? split0 : 0);
+    const int row0 = g * R;
+    bool write_ok = true;
+    if (!final_out && (slot < 0 || slot >= p.max_slots)) {
+      write_ok = false;  // schedule does not match this call: record it, write nothing
+      if (tid == 0) atomicOr(p.status, MLA_DEVICE_BAD_SCHEDULE);
+    }
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+      const int dv = blk * 128 + tid;
+#pragma unroll
+      for (int q = 0; q < R / 16; ++q) {
+        float v[16];
+        tmem_ld_x16(tmem + lane_base + C::kOCol + blk * R + 16 * q, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int r = 16 * q + e;
+          if (write_ok && row0 + r < p.rows) {
+            const float o = v[e] * inv_s[r];
+            if (final_out) {
+              __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+              out[(static_cast<int64_t>(prob) * p.rows + row0 + r) * kDv + dv] = __float2bfloat16_rn(o);
+            } else {
+              p.o_accum[(static_cast<int64_t>(slot) * p.rows + row0 + r) * kDv + dv] = o;
+            }
+          }
+        }
+      }
+    }
+    if (write_ok && tid < R && row0 + tid < p.rows) {
+      if (final_out)
+        p.lse[static_cast<int64_t>(prob) * p.rows + row0 + tid] = lse_s[tid];
+      else
+        p.lse_accum[static_cast<int64_t>(slot) * p.rows + row0 + tid] = lse_s[tid];
+    }
+    tc_fence_before();
+    mbar_arrive(bars.o_empty);
+    ++seg;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// kernel
+// ---------------------------------------------------------------------------
+template <int R, bool SPARSE>
+__global__ void __launch_bounds__(Cfg<R, SPARSE>::kThreads, 1)
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
+                      const DecodeParams p) {
+  using C = Cfg<R, SPARSE>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* kv = smem;
+  uint8_t* qs = smem + C::kQOff;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kAuxOff);
+  float* aux = reinterpret_cast<float*>(smem + C::kAuxOff + C::kBarBytes);
+  int* vote = reinterpret_cast<int*>(aux + 8 * R);
+  volatile int* abort_flag = vote + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vote + 9);
+
+  Bars bars;
+  bars.q_full = bar + 0;
+  bars.q_empty = bar + 1;
+  bars.kv_full = bar + 2;
+  bars.kv_empty = bar + 2 + kNumChunks;
+  bars.s_full = bar + 2 + 2 * kNumChunks;
+  bars.s_empty = bars.s_full + 2;
+  bars.p_full = bars.s_empty + 2;
+  bars.o_full = bars.p_full + 1;
+  bars.o_empty = bars.o_full + 1;
+  bars.mma_done = bars.o_empty + 1;
+  bars.grp = bars.mma_done + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int part = blockIdx.x / p.row_groups;
+  const int g = blockIdx.x % p.row_groups;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bars.q_full, 1);
+    mbar_init(bars.q_empty, 1);
+    for (int c = 0; c < kNumChunks; ++c) {
+      mbar_init(bars.kv_full + c, SPARSE ? 128 : 1);
+      mbar_init(bars.kv_empty + c, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars.s_full + i, 1);
+      mbar_init(bars.s_empty + i, 128);
+    }
+    mbar_init(bars.p_full, 128);
+    mbar_init(bars.o_full, 1);
+    mbar_init(bars.o_empty, 128);
+    mbar_init(bars.mma_done, 1);
+    mbar_init(bars.grp, 128);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    if (!SPARSE) tma_prefetch_desc(&tm_kv);
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  Watchdog wd{abort_flag, p.status, p.timeout_ns};
+  Segments sg;
+  const int32_t* sr = p.sched + static_cast<int64_t>(part) * kSchedInts;
+  sg.p0 = sr[kSchedP0];
+  sg.t0 = sr[kSchedT0];
+  sg.p1 = sr[kSchedP1];
+  sg.t1 = sr[kSchedT1];
+  const int split0 = sr[kSchedSplit0];
+  sg.np = p.num_problems;
+  sg.s_q = p.s_q;
+  sg.topk = p.topk;
+  sg.seqlens = p.cache_seqlens;
+  if (sg.p0 < 0 || sg.p0 > sg.np || sg.p1 < sg.p0 || sg.p1 > sg.np || sg.t0 < 0 || sg.t1 < 0) {
+    if (threadIdx.x == 0) atomicOr(p.status, MLA_DEVICE_BAD_SCHEDULE);
+    sg.p0 = sg.np;  // nothing to do
+    sg.p1 = sg.np;
+  }
+
+  if (warp == 0) {
+    if (lane == 0) producer<R, SPARSE>(&tm_q, &tm_kv, p, sg, g, kv, qs, bars, wd);
+  } else if (warp == 1) {
+    if (lane == 0) mma_issuer<R, SPARSE>(sg, tmem, kv, qs, bars, wd);
+  } else if (warp >= 4 && warp < 8) {
+    softmax_epilogue<R, SPARSE>(p, sg, g, split0, tmem, kv, bars, aux, vote, wd);
+  } else if (SPARSE && warp >= 8) {
+    gather_fp8<R>(p, sg, kv, bars, wd);
+  }
+
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int R, bool SPARSE>
+cudaError_t launch_one(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const DecodeParams& p,
+                       cudaStream_t stream) {
+  using C = Cfg<R, SPARSE>;
+  auto kern = mla_decode_kernel<R, SPARSE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = p.num_parts * p.row_groups;
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_kv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t decode_smem_bytes(int rpc, bool sparse) {
+  if (sparse) {
+    switch (rpc) {
+      case 16: return Cfg<16, true>::kSmemBytes;
+      case 32: return Cfg<32, true>::kSmemBytes;
+      default: return Cfg<64, true>::kSmemBytes;
+    }
+  }
+  switch (rpc) {
+    case 16: return Cfg<16, false>::kSmemBytes;
+    case 32: return Cfg<32, false>::kSmemBytes;
+    default: return Cfg<64, false>::kSmemBytes;
+  }
+}
+
+cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const DecodeParams& p, int rpc,
+                          bool sparse, cudaStream_t stream) {
+  if (sparse) {
+    switch (rpc) {
+      case 16: return launch_one<16, true>(tm_q, tm_kv, p, stream);
+      case 32: return launch_one<32, true>(tm_q, tm_kv, p, stream);
+      case 64: return launch_one<64, true>(tm_q, tm_kv, p, stream);
+    }
+  } else {
+    switch (rpc) {
+      case 16: return launch_one<16, false>(tm_q, tm_kv, p, stream);
+      case 32: return launch_one<32, false>(tm_q, tm_kv, p, stream);
+      case 64: return launch_one<64, false>(tm_q, tm_kv, p, stream);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mla

@@ -1,0 +1,97 @@
+// Internal definitions shared by the libmla translation units (host API and
+// kernels).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+constexpr int kDqk = 576;          // latent (512 NoPE) + 64 RoPE dims per token
+constexpr int kDv = 512;           // value dims = first 512 key dims
+constexpr int kChunk = 64;         // dims per 128-byte swizzle atom row (bf16)
+constexpr int kNumChunks = 9;      // 576 / 64
+constexpr int kPageSize = 64;      // tokens per page
+constexpr int kTileTokens = 128;   // tokens per KV tile = MMA M of S^T = K Q^T
+constexpr int kFp8RowBytes = 656;  // 512 e4m3 + 4 fp32 scales + 64 bf16
+constexpr int kFp8ScaleOffset = 512;
+constexpr int kFp8RopeOffset = 528;
+constexpr int kSchedInts = 8;      // ints per schedule record
+constexpr int kCostOverheadTiles = 2;  // fixed cost of starting a problem segment, in tiles
+
+// Schedule record of one part (a group of `row_groups` CTAs that walk the
+// same tiles, one CTA per row group):
+//   [0] first problem  [1] first tile in it  [2] last problem (inclusive bound)
+//   [3] end tile in the last problem (exclusive)  [4] split index of the
+//   part's piece of its first problem  [5..7] unused (0)
+enum SchedField { kSchedP0 = 0, kSchedT0 = 1, kSchedP1 = 2, kSchedT1 = 3, kSchedSplit0 = 4 };
+
+constexpr int kMaxProblems = 16384;    // metadata kernel keeps per-problem prefix sums in smem
+
+// Number of 128-token tiles of problem p: dense covers the cached tokens
+// [0, seqlen), sparse covers the topk index slots of the query token.
+__host__ __device__ inline int problem_tiles(const int32_t* cache_seqlens, int p, int s_q, int topk) {
+  if (topk > 0) return (topk + kTileTokens - 1) / kTileTokens;
+  int L = cache_seqlens[p];
+  return L > 0 ? (L + kTileTokens - 1) / kTileTokens : 0;
+}
+
+// Rows per CTA for a problem with `rows` query rows sharing one key set.
+inline int rows_per_cta(int rows) { return rows > 32 ? 64 : (rows > 16 ? 32 : 16); }
+
+struct Geometry {
+  int num_problems;  // dense: batch; sparse: batch * s_q
+  int rows;          // query rows per problem: dense s_q*h_q; sparse h_q
+  int rpc;           // rows per CTA (16, 32, 64)
+  int row_groups;    // ceil(rows / rpc)
+  int num_parts;     // schedule parts (each = row_groups CTAs)
+  int sm_count;
+};
+
+struct DecodeParams {
+  const int32_t* block_table;
+  const int32_t* cache_seqlens;
+  const int32_t* indices;
+  const int32_t* sched;
+  const int32_t* num_splits;
+  const uint8_t* kv_fp8;      // sparse: raw FP8 cache
+  void* out;                  // bf16 [num_problems * rows, 512]
+  float* lse;                 // [num_problems * rows]
+  float* o_accum;             // [slots, rows, 512]
+  float* lse_accum;           // [slots, rows]
+  uint32_t* status;
+  uint64_t timeout_ns;
+  int batch, s_q, h_q, topk;
+  int num_pages, block_table_stride;
+  int num_problems, rows, row_groups, num_parts;
+  int max_slots;              // partial-result slots the workspace holds
+  int is_causal;
+  int evict_first;
+  float scale_log2;           // sm_scale * log2(e)
+};
+
+struct CombineParams {
+  const int32_t* num_splits;
+  const float* o_accum;
+  const float* lse_accum;
+  void* out;
+  float* lse;
+  int num_problems, rows;
+  int max_slots;
+  uint32_t* status;
+};
+
+// Kernel launchers (defined in the .cu files); return a CUDA error code.
+cudaError_t launch_metadata(const int32_t* cache_seqlens, int batch, int s_q, int h_q, int topk,
+                            const Geometry& g, int32_t* sched, int32_t* num_splits, uint32_t* status,
+                            cudaStream_t stream);
+cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const DecodeParams& p, int rpc,
+                          bool sparse, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
+size_t decode_smem_bytes(int rpc, bool sparse);
+
+}  // namespace mla

@@ -1,0 +1,161 @@
+// K0 — decode tile schedule ("get_mla_metadata").
+//
+// The FlashMLA article ("Why FlashMLA's decode kernel reaches 660 TFLOPS",
+// Design 5) describes a tile scheduler that spreads requests and KV blocks
+// evenly over the SMs, computed once per decode step and reused by every
+// layer.  Here every problem (a batch element in dense mode, a (batch
+// element, query token) pair in sparse mode) is a run of 128-token tiles plus
+// a fixed start-up cost; the concatenated cost line is cut into num_parts
+// contiguous pieces of equal cost.  A piece may start or end inside a
+// problem; such a problem is then split and its pieces are merged by the
+// combine kernel.  num_splits is the exclusive prefix sum of the number of
+// pieces per problem, which doubles as the partial-result slot base.
+//
+// One CTA of 1024 threads; per-problem prefix sums live in shared memory.
+#include "mla_device.cuh"
+#include "mla_internal.h"
+
+namespace mla {
+namespace {
+
+constexpr int kThreads = 1024;
+
+struct Pos {
+  int p, t;
+};
+
+__device__ __forceinline__ bool pos_less(Pos a, Pos b) { return a.p < b.p || (a.p == b.p && a.t < b.t); }
+
+// Cost-line position x -> (problem, tile).  pre[q] = cost of problems < q.
+__device__ Pos locate(const long long* pre, int np, long long x, const int32_t* seqlens, int s_q, int topk) {
+  if (x >= pre[np]) return Pos{np, 0};
+  // largest p with pre[p] <= x (problems of zero cost share a prefix value; take the last)
+  int lo = 0, hi = np - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= x)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  long long o = x - pre[lo] - kCostOverheadTiles;
+  int n = problem_tiles(seqlens, lo, s_q, topk);
+  int t = o > 0 ? static_cast<int>(o) : 0;
+  if (t >= n) return Pos{lo + 1, 0};
+  return Pos{lo, t};
+}
+
+// In-place inclusive scan of v[0..n) (long long) by the whole block.
+__device__ void block_inclusive_scan(long long* v, int n, long long* partial) {
+  const int tid = threadIdx.x;
+  const int per = (n + kThreads - 1) / kThreads;
+  const int b = tid * per;
+  const int e = min(n, b + per);
+  long long s = 0;
+  for (int i = b; i < e; ++i) {
+    s += v[i];
+    v[i] = s;
+  }
+  partial[tid] = s;
+  __syncthreads();
+  for (int off = 1; off < kThreads; off <<= 1) {
+    long long add = tid >= off ? partial[tid - off] : 0;
+    __syncthreads();
+    partial[tid] += add;
+    __syncthreads();
+  }
+  long long base = tid > 0 ? partial[tid - 1] : 0;
+  for (int i = b; i < e; ++i) v[i] += base;
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    metadata_kernel(const int32_t* __restrict__ cache_seqlens, int np, int s_q, int topk, int num_parts,
+                    int32_t* __restrict__ sched, int32_t* __restrict__ num_splits, uint32_t* status) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  long long* pre = reinterpret_cast<long long*>(smem);             // [np + 1]
+  long long* partial = pre + (np + 1);                             // [kThreads]
+  long long* cnt = pre;                                            // [np], reuses pre after step 2
+  Pos* starts = reinterpret_cast<Pos*>(partial + kThreads);        // [num_parts + 1]
+  const int tid = threadIdx.x;
+
+  // 1. problem costs and their prefix sums
+  for (int p = tid; p < np; p += kThreads) {
+    int n = problem_tiles(cache_seqlens, p, s_q, topk);
+    pre[p + 1] = n > 0 ? static_cast<long long>(n) + kCostOverheadTiles : 0;
+  }
+  if (tid == 0) pre[0] = 0;
+  __syncthreads();
+  block_inclusive_scan(pre + 1, np, partial);
+  const long long total = pre[np];
+
+  // 2. cut the cost line into num_parts equal pieces
+  for (int k = tid; k <= num_parts; k += kThreads) {
+    long long x = total * static_cast<long long>(k) / num_parts;
+    starts[k] = locate(pre, np, x, cache_seqlens, s_q, topk);
+  }
+  __syncthreads();
+
+  // 3. pieces per problem
+  for (int p = tid; p < np; p += kThreads) {
+    int n = problem_tiles(cache_seqlens, p, s_q, topk);
+    long long c = 0;
+    if (n > 0) {
+      Pos first{p, 0}, end{p, n};
+      for (int k = 0; k < num_parts; ++k) {
+        Pos a = starts[k], b = starts[k + 1];
+        if (pos_less(a, b) && pos_less(a, end) && pos_less(first, b)) ++c;
+      }
+    }
+    cnt[p] = c;
+  }
+  __syncthreads();
+  block_inclusive_scan(cnt, np, partial);
+  for (int p = tid; p <= np; p += kThreads) num_splits[p] = p == 0 ? 0 : static_cast<int32_t>(cnt[p - 1]);
+
+  // 4. schedule records
+  for (int k = tid; k < num_parts; k += kThreads) {
+    Pos a = starts[k], b = starts[k + 1];
+    int split0 = 0;
+    if (pos_less(a, b) && a.p < np) {
+      int n = problem_tiles(cache_seqlens, a.p, s_q, topk);
+      Pos first{a.p, 0}, end{a.p, n};
+      for (int j = 0; j < k; ++j) {
+        Pos c = starts[j], d = starts[j + 1];
+        if (pos_less(c, d) && pos_less(c, end) && pos_less(first, d)) ++split0;
+      }
+    }
+    int32_t* r = sched + static_cast<size_t>(k) * kSchedInts;
+    r[kSchedP0] = a.p;
+    r[kSchedT0] = a.t;
+    r[kSchedP1] = b.p;
+    r[kSchedT1] = b.t;
+    r[kSchedSplit0] = split0;
+    r[5] = 0;
+    r[6] = 0;
+    r[7] = 0;
+  }
+  (void)status;
+}
+
+}  // namespace
+
+size_t metadata_smem_bytes(int np, int num_parts) {
+  return sizeof(long long) * (np + 1) + sizeof(long long) * kThreads + sizeof(int) * 2 * (num_parts + 1);
+}
+
+cudaError_t launch_metadata(const int32_t* cache_seqlens, int batch, int s_q, int h_q, int topk,
+                            const Geometry& g, int32_t* sched, int32_t* num_splits, uint32_t* status,
+                            cudaStream_t stream) {
+  (void)batch;
+  (void)h_q;
+  size_t smem = metadata_smem_bytes(g.num_problems, g.num_parts);
+  cudaError_t e = cudaFuncSetAttribute(metadata_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  metadata_kernel<<<1, kThreads, smem, stream>>>(cache_seqlens, g.num_problems, s_q, topk, g.num_parts, sched,
+                                                 num_splits, status);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,119 @@
+"""The C-ABI library builds, loads and exports every declared entry point;
+host-side argument validation answers without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_mla_decode_07_gb300 as mla
+from paged_mla_decode_07_gb300 import builder as mla_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mla_build.build()
+    return mla.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(mla_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["mla_metadata_size", "mla_workspace_size", "mla_get_metadata", "mla_decode",
+              "mla_get_device_status", "mla_last_error", "mla_abi_version"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libmla.so does not export {name}"
+    assert lib.mla_abi_version() == 1
+
+
+def test_decode_args_struct_matches_header():
+    # field order and count of mla_decode_args
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct \{(.*?)\} mla_decode_args;", text, flags=re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        names = [n.strip().lstrip("*") for n in re.sub(r"^(const\s+)?[\w]+\s*\*?", "", decl).split(",")]
+        fields += [n for n in names if n]
+    assert fields == [f for f, _ in mla.DecodeArgs._fields_]
+
+
+def test_null_args_rejected(lib):
+    assert lib.mla_decode(None, None) == 1
+    assert "args is NULL" in mla.last_error()
+
+
+def _args(**kw):
+    a = mla.DecodeArgs()
+    for f, v in dict(q=16, batch=1, s_q=1, h_q=16, kvcache=16, num_pages=1, page_size=64, block_table=16,
+                     block_table_stride=1, cache_seqlens=16, sm_scale=0.1, sched=16, num_splits=16,
+                     workspace=256, workspace_bytes=1 << 20, out=16, lse=16).items():
+        setattr(a, f, v)
+    for f, v in kw.items():
+        setattr(a, f, v)
+    return a
+
+
+@pytest.mark.parametrize("field,value,status,needle", [
+    ("q", None, 1, "q is NULL"),
+    ("kvcache", None, 1, "kvcache is NULL"),
+    ("out", None, 1, "out is NULL"),
+    ("lse", None, 1, "lse is NULL"),
+    ("page_size", 32, 2, "page_size must be 64"),
+    ("num_pages", 0, 1, "num_pages"),
+    ("block_table_stride", 0, 1, "block_table_stride"),
+    ("is_fp8", 1, 2, "requires sparse mode"),
+    ("q", 18, 1, "q is not 16-byte aligned"),
+    ("sm_scale", float("nan"), 1, "sm_scale"),
+])
+def test_host_validation(lib, field, value, status, needle):
+    a = _args(**{field: value})
+    assert lib.mla_decode(ctypes.byref(a), None) == status
+    assert needle in mla.last_error()
+
+
+def test_sparse_mode_rules(lib):
+    a = _args(topk=64, indices=None, is_fp8=1)
+    assert lib.mla_decode(ctypes.byref(a), None) == 1 and "indices is NULL" in mla.last_error()
+    a = _args(topk=64, indices=16, is_fp8=0)
+    assert lib.mla_decode(ctypes.byref(a), None) == 2 and "FP8 cache" in mla.last_error()
+    a = _args(topk=64, indices=16, is_fp8=1, is_causal=1)
+    assert lib.mla_decode(ctypes.byref(a), None) == 2 and "dense mode only" in mla.last_error()
+    a = _args(topk=0, indices=16)
+    assert lib.mla_decode(ctypes.byref(a), None) == 1
+
+
+def test_size_queries_validate_before_touching_a_device(lib):
+    a, b = ctypes.c_int(), ctypes.c_int()
+    assert lib.mla_metadata_size(0, 1, 16, 0, ctypes.byref(a), ctypes.byref(b)) == 1
+    assert "batch" in mla.last_error()
+    n = ctypes.c_size_t()
+    assert lib.mla_workspace_size(1, 0, 16, 0, ctypes.byref(n)) == 1
+    assert "s_q" in mla.last_error()
+    assert lib.mla_workspace_size(1, 1, 2048, 0, ctypes.byref(n)) in (2, 4)
+    assert lib.mla_get_metadata(None, 1, 1, 16, 0, None, None, None) == 1
+
+
+def test_python_binding_rejects_bad_tensors():
+    import torch
+    q = torch.zeros(1, 1, 16, 576, dtype=torch.float32)
+    with pytest.raises(ValueError, match="q must have dtype"):
+        mla.decode(q, q, q, q, 0.1, q, q)
+    q = torch.zeros(1, 1, 16, 576, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        mla.decode(q, q, q, q, 0.1, q, q)

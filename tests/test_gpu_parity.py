@@ -1,0 +1,222 @@
+"""Parity of the CUDA decode path (through the C ABI) with the fp64 oracle.
+
+Small cases compare every output element; the five named workloads run at
+full size in the benchmark's launch configuration and are compared on
+sampled rows the oracle computes one by one, plus whole-output properties.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import paged_mla_decode_07_gb300 as mla
+from paged_mla_decode_07_gb300 import workloads as W
+
+from gpu_helpers import compare, env, run_cuda, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mla.build()
+    mla.lib()
+
+
+def check(w, seed, parts=None, poison=True, **mk):
+    inp = W.make_inputs(w, seed=seed, poison_tail=poison, **mk)
+    with env(MLA_NUM_PARTS=parts):
+        out, lse, flags = run_cuda(inp)
+    ref_out, ref_lse = run_oracle(inp)
+    assert flags == 0, f"device status 0x{flags:x}"
+    compare(out, lse, ref_out, ref_lse, w.name)
+    return out, lse, ref_out, ref_lse
+
+
+# ---------------------------------------------------------------- dense mode
+def test_tiny_workload():
+    check(W.WORKLOADS["tiny"], W.SEEDS["tiny"])
+
+
+@pytest.mark.parametrize("L", [1, 2, 63, 64, 65, 127, 128, 129, 255, 256, 300, 1000])
+def test_dense_lengths(L):
+    check(W.custom(name=f"len{L}", batch=2, h_q=16, s_q=1, mode="dense", seqlens=(L, max(1, L // 3))), 10 + L)
+
+
+@pytest.mark.parametrize("h_q,s_q", [(16, 1), (8, 1), (32, 1), (24, 1), (64, 1), (48, 1), (128, 1),
+                                     (128, 2), (16, 4), (40, 3)])
+def test_dense_row_shapes(h_q, s_q):
+    """rows per problem = s_q*h_q covers 16/32/64-row CTAs, several row groups and ghost rows."""
+    check(W.custom(name=f"h{h_q}s{s_q}", batch=3, h_q=h_q, s_q=s_q, mode="dense", seqlens=(200, 77, 513)),
+          100 + h_q + s_q)
+
+
+@pytest.mark.parametrize("s_q", [1, 2, 3])
+def test_dense_causal(s_q):
+    check(W.custom(name=f"causal{s_q}", batch=3, h_q=64, s_q=s_q, mode="dense", seqlens=(129, 64, 1),
+                   causal=True), 200 + s_q)
+
+
+def test_dense_empty_and_single():
+    w = W.custom(name="empty", batch=4, h_q=16, s_q=1, mode="dense", seqlens=(0, 1, 0, 70))
+    out, lse, _, _ = check(w, 7)
+    assert np.all(out[0] == 0) and np.all(np.isneginf(lse[0]))
+    assert np.all(out[2] == 0) and np.all(np.isneginf(lse[2]))
+
+
+@pytest.mark.parametrize("parts", [1, 2, 3, 7, 40, 152, 400])
+def test_forced_split_counts(parts):
+    """Any partition of the tile line (1 part .. more parts than tiles) gives the same answer."""
+    w = W.custom(name=f"parts{parts}", batch=5, h_q=64, s_q=2, mode="dense",
+                 seqlens=(1000, 130, 1, 700, 2049), causal=True)
+    check(w, 300, parts=parts)
+
+
+def test_rescale_path_large_logits():
+    """Large sm_scale: the running max grows by far more than the lazy-rescale threshold."""
+    check(W.custom(name="bigscale", batch=2, h_q=64, s_q=1, mode="dense", seqlens=(1500, 800), sm_scale=0.6),
+          11)
+
+
+def test_rescale_path_increasing_logits():
+    """Logits that grow along the sequence force an O rescale on every tile."""
+    w = W.custom(name="ramp", batch=1, h_q=32, s_q=1, mode="dense", seqlens=(1100,), sm_scale=1.0)
+    inp = W.make_inputs(w, seed=12)
+    q = inp.q.float()
+    unit = q[0, 0, 0] / q[0, 0, 0].norm()
+    kv = inp.kvcache.float()
+    for j in range(1100):
+        page, slot = int(inp.block_table[0, j // 64]), j % 64
+        kv[page, slot, 0] = kv[page, slot, 0] * 0.1 + unit * (j * 0.05)
+    inp.kvcache = kv.to(torch.bfloat16)
+    with env(MLA_NUM_PARTS=1):
+        out, lse, flags = run_cuda(inp)
+    ref_out, ref_lse = run_oracle(inp)
+    assert flags == 0
+    compare(out, lse, ref_out, ref_lse, "ramp")
+
+
+# ---------------------------------------------------------------- sparse mode
+@pytest.mark.parametrize("h_q,topk", [(16, 64), (16, 200), (64, 128), (128, 300), (32, 1000), (48, 129)])
+def test_sparse_small(h_q, topk):
+    w = W.custom(name=f"sp{h_q}_{topk}", batch=2, h_q=h_q, s_q=2, mode="sparse", seqlens=(1500, 400),
+                 topk=topk)
+    check(w, 400 + h_q + topk)
+
+
+def test_sparse_duplicates_and_invalid_ids():
+    w = W.custom(name="spdup", batch=2, h_q=64, s_q=2, mode="sparse", seqlens=(300, 90), topk=256)
+    inp = W.make_inputs(w, seed=21)
+    idx = inp.indices.clone()
+    idx[0, 0, :40] = 7           # one id forty times
+    idx[0, 1, 5] = 300           # == seqlen: skipped
+    idx[1, 0, 9] = 10 ** 7       # far out of range: skipped
+    idx[1, 1, :] = -1            # empty key set
+    inp.indices = idx
+    out, lse, flags = run_cuda(inp)
+    ref_out, ref_lse = run_oracle(inp)
+    assert flags == 0
+    compare(out, lse, ref_out, ref_lse, "spdup")
+    assert np.all(out[1, 1] == 0) and np.all(np.isneginf(lse[1, 1]))
+
+
+@pytest.mark.parametrize("parts", [1, 5, 300])
+def test_sparse_forced_splits(parts):
+    w = W.custom(name=f"sparts{parts}", batch=3, h_q=128, s_q=2, mode="sparse", seqlens=(5000, 3000, 700),
+                 topk=640)
+    check(w, 500 + parts, parts=parts)
+
+
+def test_sparse_equals_dense_over_all_tokens():
+    """indices = all tokens of the FP8 cache equals dense decode over the dequantised bf16 cache."""
+    L = (700, 129)
+    w = W.custom(name="spall", batch=2, h_q=64, s_q=1, mode="sparse", seqlens=L, topk=768, invalid_frac=0.0)
+    inp = W.make_inputs(w, seed=31, poison_tail=False)
+    idx = torch.full((2, 1, 768), -1, dtype=torch.int32)
+    for b in range(2):
+        idx[b, 0, :L[b]] = torch.randperm(L[b], generator=torch.Generator().manual_seed(b)).int()
+    inp.indices = idx
+    out_s, lse_s, _ = run_cuda(inp)
+    flat = inp.kvcache.reshape(-1, 656)
+    n = flat.shape[0]
+    codes = flat[:, :512].contiguous().view(torch.float8_e4m3fn).float().reshape(n, 4, 128)
+    scales = flat[:, 512:528].contiguous().view(torch.float32).reshape(n, 4)
+    nope = (codes * scales[:, :, None]).reshape(n, 512).to(torch.bfloat16)
+    rope = flat[:, 528:].contiguous().view(torch.bfloat16)
+    kvb = torch.cat([nope, rope], 1).reshape(inp.kvcache.shape[0], 64, 1, 576)
+    dense = W.Inputs(W.custom(name="d", batch=2, h_q=64, s_q=1, mode="dense", seqlens=L), inp.q, kvb,
+                     inp.block_table, inp.cache_seqlens, None, inp.sm_scale, 0)
+    out_d, lse_d, _ = run_cuda(dense)
+    compare(out_s, lse_s, out_d, lse_d, "sparse-vs-dense")
+
+
+# ---------------------------------------------------------------- schedule
+@pytest.mark.parametrize("topk,lens", [(0, (5000, 1, 0, 130, 64, 20000)), (512, (100, 100, 100))])
+def test_schedule_covers_every_tile_once(topk, lens):
+    s_q, h_q = 2, 128
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    sched, ns = mla.get_metadata(sl, s_q, h_q, topk)
+    sched = sched.view(-1, 8).cpu().numpy()
+    ns = ns.cpu().numpy()
+    np_ = len(lens) * (s_q if topk else 1)
+    tiles = [math.ceil(topk / 128) if topk else math.ceil(L / 128) for L in
+             ([lens[p // s_q] for p in range(np_)] if topk else lens)]
+    seen = {}
+    count = np.zeros(np_, int)
+    for k, (p0, t0, p1, t1, sp0, *_rest) in enumerate(sched):
+        touched = []
+        for p in range(p0, min(p1, np_ - 1) + 1):
+            tb = t0 if p == p0 else 0
+            te = t1 if p == p1 else tiles[p]
+            for t in range(tb, min(te, tiles[p])):
+                assert (p, t) not in seen
+                seen[(p, t)] = k
+            if tb < min(te, tiles[p]):
+                touched.append(p)
+        for p in touched:
+            count[p] += 1
+        if touched and touched[0] == p0:
+            assert sp0 == count[p0] - 1
+    assert len(seen) == sum(tiles)
+    assert ns[0] == 0 and np.array_equal(np.diff(ns), count)
+
+
+# ---------------------------------------------------------------- device status
+def test_bad_page_is_flagged_not_faulted():
+    w = W.custom(name="badpage", batch=2, h_q=16, s_q=1, mode="dense", seqlens=(200, 100))
+    inp = W.make_inputs(w, seed=3)
+    bt = inp.block_table.clone()
+    bt[0, 1] = inp.kvcache.shape[0] + 5
+    inp.block_table = bt
+    out, lse, flags = run_cuda(inp)
+    assert flags & mla.DEVICE_BAD_PAGE
+    assert np.all(np.isfinite(out))
+    assert mla.device_status() == 0  # cleared by the previous read
+
+
+# ---------------------------------------------------------------- full-size workloads
+def _sample_rows(inp, n_problems, rng):
+    w = inp.workload
+    rows_per_problem = w.h_q if w.mode == "sparse" else w.s_q * w.h_q
+    n_total_problems = w.batch * (w.s_q if w.mode == "sparse" else 1)
+    probs = rng.choice(n_total_problems, size=min(n_problems, n_total_problems), replace=False)
+    return np.sort(np.concatenate([p * rows_per_problem + np.arange(rows_per_problem) for p in probs]))
+
+
+@pytest.mark.parametrize("name,n_problems", [("tiny", 2), ("dense_membound", 12), ("dense_computebound", 3),
+                                             ("sparse_fp8", 6), ("sparse_fp8_long", 2)])
+def test_full_size_workload(name, n_problems):
+    inp = W.make_inputs(name)
+    out, lse, flags = run_cuda(inp)
+    assert flags == 0
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+    rows = _sample_rows(inp, n_problems, np.random.default_rng(7))
+    ref_out, ref_lse = run_oracle(inp, rows=rows)
+    compare(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, name)
+    # property at any size: each output row is a convex combination of value rows
+    if inp.workload.mode == "dense":
+        vmax = float(inp.kvcache[..., :512].float().nan_to_num(0.0).abs().max())
+        assert float(np.abs(out).max()) <= vmax * (1 + 1e-2)
