@@ -297,6 +297,10 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
   p.max_slots = g.num_problems + g.num_parts;
   p.is_causal = a->is_causal ? 1 : 0;
   p.evict_first = g.row_groups == 1 ? 1 : 0;
+  {
+    const char* s = getenv("MLA_DEBUG_STALL");  // watchdog test hook (tests only)
+    p.debug_stall = (s && atoi(s) != 0) ? 1 : 0;
+  }
   p.scale_log2 = a->sm_scale * 1.4426950408889634f;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -363,6 +363,11 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
   uint32_t gphase = 0;
   int jt = 0, seg = 0;
   float l[R];
+  if (p.debug_stall) {
+    // Watchdog test: mma_done only completes after this role has finished, so
+    // this wait can only end by the watchdog limit.
+    if (!warp_wait(bars.mma_done, 0, wd)) return;
+  }
 
   for (int prob = sg.p0; prob <= sg.last(); ++prob) {
     int tb, te;
@@ -406,37 +411,36 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
       }
       if (!warp_wait(bars.s_full + sb, (jt >> 1) & 1, wd)) return;
       tc_fence_after();
-      float x[R];
-#pragma unroll
-      for (int q = 0; q < R / 16; ++q) {
-        float v[16];
-        tmem_ld_x16(tmem + lane_base + C::kSCol + sb * R + 16 * q, v);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) x[16 * q + e] = v[e];
-      }
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(bars.s_empty + sb);
-
-      // logits in log2 units, masked -> -inf
+      // Logits are read from TMEM 16 columns at a time (twice: once for the
+      // max test, once for P), which keeps the per-thread state to l[R].
       const bool all_rows = tok_ok && (SPARSE || pos <= lim_min);
+      const uint32_t s_addr = tmem + lane_base + C::kSCol + sb * R;
+      auto load16 = [&](int q, float (&v)[16]) {
+        tmem_ld_x16(s_addr + 16 * q, v);
+        tmem_ld_wait();
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        bool ok = all_rows;
-        if (!SPARSE && !all_rows && tok_ok) {
-          const int fr = g * R + r;
-          const int lim = p.is_causal ? L - p.s_q + fr / p.h_q : L - 1;
-          ok = pos <= lim;
+        for (int e = 0; e < 16; ++e) {
+          bool ok = all_rows;
+          if (!SPARSE && !all_rows && tok_ok) {
+            const int fr = g * R + 16 * q + e;
+            const int lim = p.is_causal ? L - p.s_q + fr / p.h_q : L - 1;
+            ok = pos <= lim;
+          }
+          v[e] = ok ? v[e] * p.scale_log2 : kNegInf;  // log2 units, masked -> -inf
         }
-        x[r] = ok ? x[r] * p.scale_log2 : kNegInf;
-      }
+      };
 
       // lazy max update: only when some logit exceeds the running max by the threshold
       bool need = (j == tb);
       if (!need) {
         float loc = kNegInf;
 #pragma unroll
-        for (int r = 0; r < R; ++r) loc = fmaxf(loc, x[r] - m_s[r]);
+        for (int q = 0; q < R / 16; ++q) {
+          float v[16];
+          load16(q, v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) loc = fmaxf(loc, v[e] - m_s[16 * q + e]);
+        }
         const bool w_need = __any_sync(0xffffffffu, loc > kRescaleThreshold);
         if (lane == 0) vote[(jt & 1) * 4 + warp_q] = w_need ? 1 : 0;
         if (!group_sync(bars.grp, gphase, wd)) return;
@@ -445,9 +449,14 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
       }
       if (need) {
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float v = warp_max(x[r]);
-          if (lane == (r & 31)) red[warp_q * R + r] = v;
+        for (int q = 0; q < R / 16; ++q) {
+          float v[16];
+          load16(q, v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float mx = warp_max(v[e]);
+            if (lane == ((16 * q + e) & 31)) red[warp_q * R + 16 * q + e] = mx;
+          }
         }
         if (!group_sync(bars.grp, gphase, wd)) return;
         if (tid < R) {
@@ -482,13 +491,20 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
 
       // probabilities -> P (bf16, K-major 128B-swizzled [2][R][64 tokens]) and row sums
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float mr = m_s[r];
-        const float pr = (x[r] == kNegInf) ? 0.f : fast_exp2(x[r] - mr);
-        l[r] += pr;
-        const uint32_t addr = p_base + p_row_off + r * 128 + ((p_chunk ^ (r & 7)) << 4);
-        st_shared_u16(addr, __bfloat16_as_ushort(__float2bfloat16_rn(pr)));
+      for (int q = 0; q < R / 16; ++q) {
+        float v[16];
+        load16(q, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int r = 16 * q + e;
+          const float pr = (v[e] == kNegInf) ? 0.f : fast_exp2(v[e] - m_s[r]);
+          l[r] += pr;
+          const uint32_t addr = p_base + p_row_off + r * 128 + ((p_chunk ^ (r & 7)) << 4);
+          st_shared_u16(addr, __bfloat16_as_ushort(__float2bfloat16_rn(pr)));
+        }
       }
+      tc_fence_before();
+      mbar_arrive(bars.s_empty + sb);
       if (!SPARSE && !tok_ok) {
         // a masked token's V row must be finite (0 * NaN would poison O): zero it
 #pragma unroll 1

@@ -71,6 +71,8 @@ struct DecodeParams {
   int max_slots;              // partial-result slots the workspace holds
   int is_causal;
   int evict_first;
+  int debug_stall;            // test hook: the softmax role waits on a barrier nothing completes
+
   float scale_log2;           // sm_scale * log2(e)
 };
 

@@ -82,15 +82,21 @@ def test_rescale_path_large_logits():
 
 
 def test_rescale_path_increasing_logits():
-    """Logits that grow along the sequence force an O rescale on every tile."""
-    w = W.custom(name="ramp", batch=1, h_q=32, s_q=1, mode="dense", seqlens=(1100,), sm_scale=1.0)
+    """Logits that grow along the sequence force an O rescale on every tile.
+
+    Key j is pushed along head 0's query direction by 0.15*j*24/|q|, so head 0's logit grows by
+    about 19 (28 in log2 units, above the threshold of 8) per 128-token tile and ends near 165:
+    large enough to exercise the rescale, small enough for fp32 accumulation to meet the
+    absolute lse bound."""
+    w = W.custom(name="ramp", batch=1, h_q=32, s_q=1, mode="dense", seqlens=(1100,))
     inp = W.make_inputs(w, seed=12)
     q = inp.q.float()
-    unit = q[0, 0, 0] / q[0, 0, 0].norm()
+    qn = q[0, 0, 0].norm()
+    unit = q[0, 0, 0] / qn
     kv = inp.kvcache.float()
     for j in range(1100):
         page, slot = int(inp.block_table[0, j // 64]), j % 64
-        kv[page, slot, 0] = kv[page, slot, 0] * 0.1 + unit * (j * 0.05)
+        kv[page, slot, 0] = kv[page, slot, 0] * 0.1 + unit * (0.15 * j * 24.0 / qn)
     inp.kvcache = kv.to(torch.bfloat16)
     with env(MLA_NUM_PARTS=1):
         out, lse, flags = run_cuda(inp)
