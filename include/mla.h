@@ -122,6 +122,21 @@ typedef struct {
  * Alignment: q, kvcache, out, lse, workspace 16-byte aligned. */
 mla_status mla_decode(const mla_decode_args* args, mla_stream_t stream);
 
+/* Decode without any caller scratch, for callers that cannot allocate device
+ * memory when they decode (for example code inside a runtime or plugin host
+ * that owns no CUDA memory pool, or a latency-critical path where cudaMalloc
+ * is not allowed).  The pages describe no such entry point; it is an addition
+ * of this library.  Same arguments and results as mla_decode, except that
+ * workspace/workspace_bytes are ignored: the split-KV partials go to a fixed
+ * 32 MiB array in the library's device memory, which every GPU that loads
+ * this part of the library keeps until exit.  A decode whose scratch (see
+ * mla_workspace_size) exceeds 32 MiB returns MLA_ERR_WORKSPACE without
+ * launching anything.  The first call on a device looks the array up (once
+ * per device) and should come before any stream capture.  All calls share the
+ * array, so calls that overlap on the GPU race; serialise them.  Nothing in
+ * the array needs to start at zero. */
+mla_status mla_decode_noalloc(const mla_decode_args* args, mla_stream_t stream);
+
 /* Synchronises `stream`, returns the device status bits accumulated since the
  * last call in *flags (0 = clean) and clears them.  Returns
  * MLA_ERR_DEVICE_TIMEOUT / MLA_ERR_DEVICE_BOUNDS when the matching bit is set. */

@@ -162,6 +162,9 @@ uint64_t watchdog_ns() {
 }
 
 }  // namespace
+
+void set_error_message(const std::string& msg) { g_error = msg; }
+
 }  // namespace mla
 
 using namespace mla;

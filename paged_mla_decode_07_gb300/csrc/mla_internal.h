@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <string>
+
 #include "../../include/mla.h"
 
 namespace mla {
@@ -95,5 +97,7 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, con
                           bool sparse, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
 size_t decode_smem_bytes(int rpc, bool sparse);
+// Sets the thread-local message returned by mla_last_error().
+void set_error_message(const std::string& msg);
 
 }  // namespace mla
