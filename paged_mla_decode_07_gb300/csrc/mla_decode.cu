@@ -44,26 +44,74 @@
 #include "mla_internal.h"
 
 namespace mla {
+
+// Pipeline tracing (built only with -DMLA_TRACE): clock64() stamps of the
+// main pipeline events of CTA 0, one slot per (event, tile).
+enum TraceEvent {
+  kTrProdChunk0 = 0, kTrProdChunk8, kTrMmaKv0, kTrMmaKv8, kTrMmaSDone, kTrSmSFull, kTrSmVote, kTrSmPFull,
+  kTrMmaPFull, kTrMmaODone, kTrGatherStart, kTrGatherDone, kTrEpiStart, kTrEpiEnd, kTrNumEvents
+};
+#ifdef MLA_TRACE
+constexpr int kTraceTiles = 1024;
+__device__ unsigned long long g_mla_trace[kTrNumEvents * kTraceTiles];
+#define MLA_TR(ev, idx)                                                                      \
+  do {                                                                                       \
+    if (blockIdx.x == 0 && (idx) < kTraceTiles) g_mla_trace[(ev) * kTraceTiles + (idx)] = clock64(); \
+  } while (0)
+#else
+#define MLA_TR(ev, idx) \
+  do {                  \
+  } while (0)
+#endif
+
 namespace {
 
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 before a max update is forced
+constexpr uint32_t kSoftmaxBar = 1;        // named barrier of the 128 softmax threads
 
 template <int R, bool SPARSE>
 struct Cfg {
-  static constexpr int kWarps = SPARSE ? 12 : 8;
+  // softmax warpgroups: with 64 rows two warpgroups split the rows
+  static constexpr int kSmWG = (R == 64) ? 2 : 1;
+  static constexpr int kGatherWarp0 = 4 + 4 * kSmWG;  // sparse: first FP8 gather warp
+  static constexpr int kWarps = kGatherWarp0 + (SPARSE ? 4 : 0);
+  // sparse with two softmax warpgroups: 512 threads at 128 registers; the
+  // producer/MMA warpgroup gives 72 registers per thread to the gather
+  // warpgroup (128*56 + 2*128*128 + 128*200 = 65536 = the launch's total)
+  static constexpr bool kRegSplit = SPARSE && kSmWG == 2;
+  static constexpr uint32_t kRegsCtl = 56, kRegsGather = 200;
   static constexpr int kThreads = kWarps * 32;
-  static constexpr int kKvChunkBytes = kTileTokens * 128;  // 16 KB
-  static constexpr int kKvBytes = kNumChunks * kKvChunkBytes;
+  static constexpr int kKvChunkBytes = kTileTokens * 128;  // 16 KB: [128 tokens][64 dims] bf16
+  static constexpr int kPairBytes = 2 * kKvChunkBytes;    // chunks 2b, 2b+1: one 128-dv block of V
   static constexpr int kQChunkBytes = R * 128;
-  static constexpr int kQOff = kKvBytes;
   static constexpr int kQBytes = kNumChunks * kQChunkBytes;
-  static constexpr int kPOff = 8 * kKvChunkBytes;
-  static constexpr int kPHalfBytes = R * 128;  // [R rows][64 tokens] bf16
-  static constexpr int kAuxOff = kQOff + kQBytes;
-  // barriers
-  static constexpr int kNumBars = 2 + 2 * kNumChunks + 4 + 3 + 2;
-  static constexpr int kBarBytes = kNumBars * 8;
+  static constexpr int kPHalfBytes = R * 128;  // [R rows][64 tokens] bf16 (K-major P)
+  // KV staging ring: kNA pair slots + kNB RoPE-chunk slots.  A tile occupies
+  // 4 pair slots and 1 RoPE slot.  With 16 or 32 rows Q is small enough for a
+  // spare pair slot, an extra RoPE slot and a separate P buffer, so the next
+  // tile starts loading while this one is in the softmax and PV stages
+  // (kRing).  With 64 rows the ring is exactly one tile and P reuses the RoPE
+  // slot once S^T is done.
+  static constexpr bool kRing = !SPARSE && R <= 32;
+  static constexpr int kNA = kRing ? 5 : 4;
+  static constexpr int kNB = kRing ? (R == 16 ? 2 : 1) : 1;
+  static constexpr int kPairOff = 0;
+  static constexpr int kRopeOff = kNA * kPairBytes;
+  static constexpr int kQOff = kRopeOff + kNB * kKvChunkBytes;
+  static constexpr int kPOff = kRing ? kQOff + kQBytes : kRopeOff;
+  static constexpr int kPBytes = kRing ? 2 * kPHalfBytes : 0;  // separate P buffer (ring only)
+  // With 64 rows P is stored MN-major ([128 tokens][64 rows], one 128-byte
+  // swizzle atom per token): eight 16-byte stores per thread.
+  static constexpr bool kPMnMajor = (R == 64);
+  static constexpr int kAuxOff = (kQOff + kQBytes + kPBytes + 1023) / 1024 * 1024;
+  // barriers: q_full, q_empty, chunk_full[2*kNA + kNB], pair_empty[kNA], rope_empty[kNB],
+  // s_full[2], s_empty[2], p_full, o_full, o_empty, mma_done
+  static constexpr int kNumFull = 2 * kNA + kNB;
+  static constexpr int kNumBars = 2 + kNumFull + kNA + kNB + 4 + 3 + 1;
+  // rounded to 128 bytes so the row statistics after the barriers are 16-byte
+  // aligned (they are read with 16-byte vector loads)
+  static constexpr int kBarBytes = (kNumBars * 8 + 127) / 128 * 128;
   // aux floats: m[R], alpha[R], inv_l[R], lse[R], red[4][R]; ints: vote[2][4], abort, tmem
   static constexpr int kAuxBytes = kBarBytes + 8 * R * 4 + 64;
   static constexpr int kSmemBytes = kAuxOff + kAuxBytes + 1024;  // + alignment slack
@@ -71,21 +119,23 @@ struct Cfg {
   static constexpr int kSCol = 4 * R;
   static constexpr int kTmemCols = (6 * R <= 128) ? 128 : ((6 * R <= 256) ? 256 : 512);
   static_assert(2 * kPHalfBytes <= kKvChunkBytes, "P must fit in the RoPE chunk");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(R == 16 || R == 32 || R == 64, "rows per CTA");
+  static_assert((kAuxOff + kBarBytes) % 16 == 0, "row statistics must be 16-byte aligned");
 };
 
 struct Bars {
   uint64_t* q_full;
   uint64_t* q_empty;
-  uint64_t* kv_full;   // [9]
-  uint64_t* kv_empty;  // [9]
+  uint64_t* full;        // [kNumFull]: pair slot s chunk h -> 2s+h; RoPE slot t -> 2*kNA+t
+  uint64_t* pair_empty;  // [kNA]
+  uint64_t* rope_empty;  // [kNB]
   uint64_t* s_full;    // [2]
   uint64_t* s_empty;   // [2]
   uint64_t* p_full;
   uint64_t* o_full;
   uint64_t* o_empty;
   uint64_t* mma_done;
-  uint64_t* grp;       // softmax group barrier (128 threads)
 };
 
 // Segment iterator shared by all roles: the part walks problems p0..p1 and,
@@ -102,6 +152,25 @@ struct Segments {
   }
 };
 
+// Ring bookkeeping.  Tile number jt (counted over all of a CTA's segments)
+// uses pair items 4*jt + b (b = 0..3) and RoPE item jt; item n of a ring of
+// size k lives in slot n % k and is that slot's (n / k)-th use (the parity of
+// its barriers' phases).
+template <class C>
+struct Ring {
+  __device__ static int pair_slot(int jt, int b) { return (4 * jt + b) % C::kNA; }
+  __device__ static uint32_t pair_use(int jt, int b) { return static_cast<uint32_t>((4 * jt + b) / C::kNA); }
+  __device__ static int rope_slot(int jt) { return jt % C::kNB; }
+  __device__ static uint32_t rope_use(int jt) { return static_cast<uint32_t>(jt / C::kNB); }
+  // byte offset of chunk c (0..8) of tile jt in the KV region
+  __device__ static uint32_t chunk_off(int jt, int c) {
+    return c < 8 ? C::kPairOff + pair_slot(jt, c >> 1) * C::kPairBytes + (c & 1) * C::kKvChunkBytes
+                 : C::kRopeOff + rope_slot(jt) * C::kKvChunkBytes;
+  }
+  __device__ static int full_index(int jt, int c) { return c < 8 ? 2 * pair_slot(jt, c >> 1) + (c & 1) : 2 * C::kNA + rope_slot(jt); }
+  __device__ static uint32_t full_use(int jt, int c) { return c < 8 ? pair_use(jt, c >> 1) : rope_use(jt); }
+};
+
 // Bounded wait that ignores the abort flag (used to drain own async work).
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
@@ -116,14 +185,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
-// 128-thread group barrier on an mbarrier (bounded; see Watchdog).
-__device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& phase, const Watchdog& wd) {
-  mbar_arrive(bar);
-  bool ok = warp_wait(bar, phase & 1, wd);
-  ++phase;
-  return ok;
-}
-
 // ---------------------------------------------------------------------------
 // producer: Q (always) and dense KV pages by TMA
 // ---------------------------------------------------------------------------
@@ -134,9 +195,10 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, cons
   using C = Cfg<R, SPARSE>;
   const uint64_t pol_kv = p.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
   const uint64_t pol_q = l2_policy_evict_normal();
-  int armed[kNumChunks];
+  using RG = Ring<C>;
+  int armed[C::kNumFull];  // phases armed per full barrier (for the drain)
 #pragma unroll
-  for (int c = 0; c < kNumChunks; ++c) armed[c] = 0;
+  for (int k = 0; k < C::kNumFull; ++k) armed[k] = 0;
   int q_armed = 0, jt = 0;
   for (int prob = sg.p0; prob <= sg.last(); ++prob) {
     int tb, te;
@@ -165,14 +227,33 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, cons
         const bool ok_b = has_b && pb >= 0 && pb < p.num_pages;
         if (!ok_a || (has_b && !ok_b)) atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
         const uint32_t bytes = (ok_a ? 8192u : 0u) + (ok_b ? 8192u : 0u);
+        // ring: the RoPE chunk first (its slot frees early); one-tile ring: pairs first
 #pragma unroll 1
-        for (int c = 0; c < kNumChunks; ++c) {
-          if (armed[c] > 0 && !mbar_wait(bars.kv_empty + c, (armed[c] - 1) & 1, wd)) goto drain;
-          mbar_arrive_expect_tx(bars.kv_full + c, bytes);
-          uint8_t* dst = kv + c * C::kKvChunkBytes;
-          if (ok_a) tma_load_3d(dst, tm_kv, bars.kv_full + c, 0, c, pa * kPageSize, pol_kv);
-          if (ok_b) tma_load_3d(dst + 8192, tm_kv, bars.kv_full + c, 0, c, pb * kPageSize, pol_kv);
-          ++armed[c];
+        for (int step = 0; step < 5; ++step) {
+          const int item = C::kRing ? (step == 0 ? 4 : step - 1) : step;  // 0..3 pairs, 4 RoPE
+          int c0, nc;
+          if (item < 4) {
+            const uint32_t use = RG::pair_use(jt, item);
+            if (use > 0 && !mbar_wait(bars.pair_empty + RG::pair_slot(jt, item), (use - 1) & 1, wd)) goto drain;
+            c0 = 2 * item;
+            nc = 2;
+          } else {
+            const uint32_t use = RG::rope_use(jt);
+            if (use > 0 && !mbar_wait(bars.rope_empty + RG::rope_slot(jt), (use - 1) & 1, wd)) goto drain;
+            c0 = 8;
+            nc = 1;
+          }
+          for (int c = c0; c < c0 + nc; ++c) {
+            const int fi = RG::full_index(jt, c);
+            uint64_t* fb = bars.full + fi;
+            mbar_arrive_expect_tx(fb, bytes);
+            ++armed[fi];
+            if (c == 0) MLA_TR(kTrProdChunk0, jt);
+            if (c == 8) MLA_TR(kTrProdChunk8, jt);
+            uint8_t* dst = kv + RG::chunk_off(jt, c);
+            if (ok_a) tma_load_3d(dst, tm_kv, fb, 0, c, pa * kPageSize, pol_kv);
+            if (ok_b) tma_load_3d(dst + 8192, tm_kv, fb, 0, c, pb * kPageSize, pol_kv);
+          }
         }
       }
     }
@@ -181,8 +262,8 @@ drain:
   // wait (bounded) for this thread's own copies still in flight
   if (!SPARSE) {
 #pragma unroll 1
-    for (int c = 0; c < kNumChunks; ++c)
-      if (armed[c] > 0) mbar_wait_drain(bars.kv_full + c, (armed[c] - 1) & 1, wd.limit_ns);
+    for (int k = 0; k < C::kNumFull; ++k)
+      if (armed[k] > 0) mbar_wait_drain(bars.full + k, (armed[k] - 1) & 1, wd.limit_ns);
   }
   if (q_armed > 0) mbar_wait_drain(bars.q_full, (q_armed - 1) & 1, wd.limit_ns);
 }
@@ -194,8 +275,9 @@ template <int R, bool SPARSE>
 __device__ void mma_issuer(const Segments& sg, uint32_t tmem, uint8_t* kv, uint8_t* qs, const Bars& bars,
                            const Watchdog& wd) {
   using C = Cfg<R, SPARSE>;
+  using RG = Ring<C>;
   constexpr uint32_t kIdS = idesc_bf16_f32(128, R, 0, 0);  // A = K tile (K-major), B = Q (K-major)
-  constexpr uint32_t kIdO = idesc_bf16_f32(128, R, 1, 0);  // A = V^T (MN-major), B = P (K-major)
+  constexpr uint32_t kIdO = idesc_bf16_f32(128, R, 1, C::kPMnMajor ? 1 : 0);  // A = V^T (MN-major), B = P
   const uint32_t kv_base = smem_u32(kv);
   const uint32_t q_base = smem_u32(qs);
   const uint32_t p_base = kv_base + C::kPOff;
@@ -213,35 +295,44 @@ __device__ void mma_issuer(const Segments& sg, uint32_t tmem, uint8_t* kv, uint8
       const uint32_t d_s = tmem + C::kSCol + sb * R;
 #pragma unroll 1
       for (int c = 0; c < kNumChunks; ++c) {
-        if (!mbar_wait(bars.kv_full + c, jt & 1, wd)) goto done;
+        if (!mbar_wait(bars.full + RG::full_index(jt, c), RG::full_use(jt, c) & 1, wd)) goto done;
         tc_fence_after();
+        if (c == 0) MLA_TR(kTrMmaKv0, jt);
+        if (c == 8) MLA_TR(kTrMmaKv8, jt);
+        const uint32_t chunk = kv_base + RG::chunk_off(jt, c);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t a = smem_desc(kv_base + c * C::kKvChunkBytes + kk * 32, 16, 1024);
+          const uint64_t a = smem_desc(chunk + kk * 32, 16, 1024);
           const uint64_t b = smem_desc(q_base + c * C::kQChunkBytes + kk * 32, 16, 1024);
           umma_bf16_ss(d_s, a, b, kIdS, (c | kk) != 0);
         }
       }
       umma_commit(bars.s_full + sb);
+      // with a separate P buffer the RoPE chunk is free once S^T is done
+      if (C::kRing) umma_commit(bars.rope_empty + RG::rope_slot(jt));
+      MLA_TR(kTrMmaSDone, jt);
       if (j == te - 1) umma_commit(bars.q_empty);
       if (!mbar_wait(bars.p_full, jt & 1, wd)) goto done;
       tc_fence_after();
+      MLA_TR(kTrMmaPFull, jt);
       if (j == tb && seg > 0) {
         if (!mbar_wait(bars.o_empty, (seg - 1) & 1, wd)) goto done;
         tc_fence_after();
       }
 #pragma unroll 1
       for (int blk = 0; blk < 4; ++blk) {
+        const uint32_t pair = kv_base + C::kPairOff + RG::pair_slot(jt, blk) * C::kPairBytes;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = smem_desc(kv_base + 2 * blk * C::kKvChunkBytes + kk * 2048, C::kKvChunkBytes, 1024);
-          const uint64_t b = smem_desc(p_base + (kk >> 2) * C::kPHalfBytes + (kk & 3) * 32, 16, 1024);
+          const uint64_t a = smem_desc(pair + kk * 2048, C::kKvChunkBytes, 1024);
+          const uint64_t b = C::kPMnMajor ? smem_desc(p_base + kk * 2048, 16, 1024)
+                                          : smem_desc(p_base + (kk >> 2) * C::kPHalfBytes + (kk & 3) * 32, 16, 1024);
           umma_bf16_ss(tmem + C::kOCol + blk * R, a, b, kIdO, !(j == tb && kk == 0));
         }
-        umma_commit(bars.kv_empty + 2 * blk);
-        umma_commit(bars.kv_empty + 2 * blk + 1);
+        umma_commit(bars.pair_empty + RG::pair_slot(jt, blk));
       }
-      umma_commit(bars.kv_empty + 8);
+      if (!C::kRing) umma_commit(bars.rope_empty + RG::rope_slot(jt));  // P lived in the RoPE slot
+      MLA_TR(kTrMmaODone, jt);
       if (j == te - 1) umma_commit(bars.o_full);
     }
     ++seg;
@@ -265,7 +356,9 @@ template <int R>
 __device__ void gather_fp8(const DecodeParams& p, const Segments& sg, uint8_t* kv, const Bars& bars,
                            const Watchdog& wd) {
   using C = Cfg<R, true>;
-  const int tid = threadIdx.x - 256;
+  using RG = Ring<C>;
+  const int tid = threadIdx.x - 32 * C::kGatherWarp0;
+  const bool leader = (threadIdx.x & 31) == 0;
   const uint32_t row_addr = smem_u32(kv) + tid * 128;
   const uint32_t sw = tid & 7;
   int jt = 0;
@@ -279,6 +372,7 @@ __device__ void gather_fp8(const DecodeParams& p, const Segments& sg, uint8_t* k
     const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
     int t_next = (tb * kTileTokens + tid < p.topk) ? idx_row[tb * kTileTokens + tid] : -1;
     for (int j = tb; j < te; ++j, ++jt) {
+      if (tid == 0) MLA_TR(kTrGatherStart, jt);
       const int t = t_next;
       {
         const int kn = (j + 1) * kTileTokens + tid;
@@ -299,10 +393,13 @@ __device__ void gather_fp8(const DecodeParams& p, const Segments& sg, uint8_t* k
       uint4 rope[8];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        if (jt > 0 && !warp_wait(bars.kv_empty + c, (jt - 1) & 1, wd)) return;
+        if ((c & 1) == 0) {
+          const uint32_t use = RG::pair_use(jt, c >> 1);
+          if (use > 0 && !warp_wait(bars.pair_empty + RG::pair_slot(jt, c >> 1), (use - 1) & 1, wd)) return;
+        }
         const uint32_t sw_word = (c >> 1) == 0 ? cs[32].x : ((c >> 1) == 1 ? cs[32].y : ((c >> 1) == 2 ? cs[32].z : cs[32].w));
         const float scale = __uint_as_float(sw_word);
-        const uint32_t base = row_addr + c * C::kKvChunkBytes;
+        const uint32_t base = row_addr + RG::chunk_off(jt, c);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const uint4 v = cs[4 * c + (q >> 1)];
@@ -312,19 +409,25 @@ __device__ void gather_fp8(const DecodeParams& p, const Segments& sg, uint8_t* k
                        dequant2(w1 & 0xffffu, scale), dequant2(w1 >> 16, scale));
         }
         fence_proxy_async_smem();
-        mbar_arrive(bars.kv_full + c);
+        __syncwarp();
+        if (leader) mbar_arrive(bars.full + RG::full_index(jt, c));  // one arrival per gather warp
         if (c == 1) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) rope[i] = ok ? ld_global_nc_v4(src + 528 + 16 * i) : make_uint4(0, 0, 0, 0);
         }
       }
-      if (jt > 0 && !warp_wait(bars.kv_empty + 8, (jt - 1) & 1, wd)) return;
       {
-        const uint32_t base = row_addr + 8 * C::kKvChunkBytes;
+        const uint32_t use = RG::rope_use(jt);
+        if (use > 0 && !warp_wait(bars.rope_empty + RG::rope_slot(jt), (use - 1) & 1, wd)) return;
+      }
+      {
+        const uint32_t base = row_addr + RG::chunk_off(jt, 8);
 #pragma unroll
         for (int q = 0; q < 8; ++q) st_shared_v4(base + ((q ^ sw) << 4), rope[q].x, rope[q].y, rope[q].z, rope[q].w);
         fence_proxy_async_smem();
-        mbar_arrive(bars.kv_full + 8);
+        __syncwarp();
+        if (leader) mbar_arrive(bars.full + RG::full_index(jt, 8));
+        if (tid == 0) MLA_TR(kTrGatherDone, jt);
       }
     }
   }
@@ -333,25 +436,71 @@ __device__ void gather_fp8(const DecodeParams& p, const Segments& sg, uint8_t* k
 // ---------------------------------------------------------------------------
 // softmax + epilogue (128 threads; thread t -> token t of the tile, TMEM lane t)
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float warp_max(float v) {
+// Reduce-scatter of N per-lane values over the 32 lanes of a warp (N a power
+// of two, 16..64): at each step a lane keeps one half of its values, sends the
+// other half to its partner and combines.  Afterwards lane l holds the
+// reduction of values [k*l, k*l + k) in out[0..k) with k = max(N/32, 1) (for
+// N < 32 lanes l and l ^ (32/N)... share a value).  Writes the results to
+// dst[k*l + i] for the lanes that own distinct values.
+template <int N, bool MAX>
+__device__ __forceinline__ void warp_reduce_scatter(const float (&v)[N], float* dst, int lane) {
+  constexpr int K = N >= 32 ? N / 32 : 1;
+  float t[N / 2];
+  // first step reads v directly (no copy of the N inputs)
+  {
+    const bool up = (lane & 16) != 0;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
+    for (int i = 0; i < N / 2; ++i) {
+      const float send = up ? v[i] : v[i + N / 2];
+      const float keep = up ? v[i + N / 2] : v[i];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+      t[i] = MAX ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  int n = N / 2;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+  for (int o = 8; o >= 1; o >>= 1) {
+    if (n > K) {
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < N / 4; ++i) {
+        if (i < n / 2) {
+          const float send = up ? t[i] : t[i + n / 2];
+          const float keep = up ? t[i + n / 2] : t[i];
+          const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+          t[i] = MAX ? fmaxf(keep, recv) : keep + recv;
+        }
+      }
+      n >>= 1;
+    } else {
+      // fewer values than lanes left: plain butterfly on the remaining value
+      const float recv = __shfl_xor_sync(0xffffffffu, t[0], o);
+      t[0] = MAX ? fmaxf(t[0], recv) : t[0] + recv;
+    }
+  }
+  // lane l now holds values [base, base + K) with base = (N >= 32 ? K * l : (l >> (5 - log2 N)) ...)
+  if (N >= 32) {
+#pragma unroll
+    for (int i = 0; i < K; ++i) dst[K * lane + i] = t[i];
+  } else {
+    // N values over 32 lanes: after log2(N) keep-half steps lane l owns value (l >> (5 - log2N))
+    constexpr int kShift = (N == 16) ? 1 : 0;
+    if ((lane & ((1 << kShift) - 1)) == 0) dst[lane >> kShift] = t[0];
+  }
 }
 
 template <int R, bool SPARSE>
 __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int g, int split0, uint32_t tmem,
-                                 uint8_t* kv, const Bars& bars, float* aux, int* vote, const Watchdog& wd) {
+                                 uint8_t* kv, const Bars& bars, float* aux, const Watchdog& wd) {
   using C = Cfg<R, SPARSE>;
-  const int tid = threadIdx.x - 128;
+  constexpr int RW = R / C::kSmWG;  // rows owned by this warpgroup
+  const int wg = (threadIdx.x - 128) >> 7;
+  const int rb = wg * RW;           // first row of this warpgroup
+  const int tid = (threadIdx.x - 128) & 127;  // token of the tile = TMEM lane
   const int warp_q = (threadIdx.x >> 5) & 3;
   const int lane = threadIdx.x & 31;
   const uint32_t lane_base = static_cast<uint32_t>(warp_q * 32) << 16;
+  const uint32_t bar_id = kSoftmaxBar + wg;
   float* m_s = aux;            // running row max (log2 units)
   float* alpha_s = aux + R;    // rescale factors
   float* inv_s = aux + 2 * R;  // 1 / row sum
@@ -360,13 +509,24 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
   const uint32_t p_base = smem_u32(kv) + C::kPOff;
   const uint32_t p_row_off = (tid >> 6) * C::kPHalfBytes + (tid & 7) * 2;
   const uint32_t p_chunk = (tid & 63) >> 3;
-  uint32_t gphase = 0;
+  // The 128 threads of a softmax warpgroup synchronise on their own hardware
+  // named barrier.  Every bounded mbarrier wait is followed by a barrier AND
+  // of its result, so on a timeout all four warps leave together and none is
+  // left at a barrier.  Warpgroups own disjoint rows and never wait on each
+  // other; consumers are signalled with one arrival per warp.
+  auto group_ok = [&](bool ok) { return named_bar_and(bar_id, 128, ok); };
+  auto gsync = [&]() { named_bar_sync(bar_id, 128); };
+  auto warp_arrive = [&](uint64_t* b) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(b);
+  };
+  const bool tracer = (wg == 0 && tid == 0);
   int jt = 0, seg = 0;
-  float l[R];
+  float l[RW];
   if (p.debug_stall) {
     // Watchdog test: mma_done only completes after this role has finished, so
     // this wait can only end by the watchdog limit.
-    if (!warp_wait(bars.mma_done, 0, wd)) return;
+    if (!group_ok(mbar_wait(bars.mma_done, 0, wd))) return;
   }
 
   for (int prob = sg.p0; prob <= sg.last(); ++prob) {
@@ -380,13 +540,13 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
     // causal limit per row: query token i sees keys <= L - s_q + i (dense only)
     int lim_min = L - 1;
     if (!SPARSE && p.is_causal) {
-      const int i_first = (g * R) / p.h_q;
+      const int i_first = (g * R + rb) / p.h_q;
       lim_min = min(L - 1, L - p.s_q + i_first);
     }
-    if (tid < R) m_s[tid] = kNegInf;
+    if (tid < RW) m_s[rb + tid] = kNegInf;
 #pragma unroll
-    for (int r = 0; r < R; ++r) l[r] = 0.f;
-    if (!group_sync(bars.grp, gphase, wd)) return;
+    for (int r = 0; r < RW; ++r) l[r] = 0.f;
+    gsync();
 
     for (int j = tb; j < te; ++j, ++jt) {
       const int sb = jt & 1;
@@ -409,79 +569,74 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
           tok_ok = pg >= 0 && pg < p.num_pages;
         }
       }
-      if (!warp_wait(bars.s_full + sb, (jt >> 1) & 1, wd)) return;
+      if (!group_ok(mbar_wait(bars.s_full + sb, (jt >> 1) & 1, wd))) return;
       tc_fence_after();
-      // Logits are read from TMEM 16 columns at a time (twice: once for the
-      // max test, once for P), which keeps the per-thread state to l[R].
-      const bool all_rows = tok_ok && (SPARSE || pos <= lim_min);
-      const uint32_t s_addr = tmem + lane_base + C::kSCol + sb * R;
-      auto load16 = [&](int q, float (&v)[16]) {
-        tmem_ld_x16(s_addr + 16 * q, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          bool ok = all_rows;
-          if (!SPARSE && !all_rows && tok_ok) {
-            const int fr = g * R + 16 * q + e;
-            const int lim = p.is_causal ? L - p.s_q + fr / p.h_q : L - 1;
-            ok = pos <= lim;
-          }
-          v[e] = ok ? v[e] * p.scale_log2 : kNegInf;  // log2 units, masked -> -inf
-        }
-      };
+      if (tracer) MLA_TR(kTrSmSFull, jt);
 
-      // lazy max update: only when some logit exceeds the running max by the threshold
+      // this thread's token, this warpgroup's rows of S^T: all loads in flight, one wait
+      float x[RW];
+      {
+        const uint32_t s_addr = tmem + lane_base + C::kSCol + sb * R + rb;
+#pragma unroll
+        for (int q = 0; q < RW / 16; ++q) tmem_ld_x16(s_addr + 16 * q, *reinterpret_cast<float(*)[16]>(x + 16 * q));
+        tmem_ld_wait();
+      }
+      tc_fence_before();
+      warp_arrive(bars.s_empty + sb);  // S is in registers; the buffer can be rewritten
+
+      // logits in log2 units; masked -> -inf
+      const bool all_rows = tok_ok && (SPARSE || pos <= lim_min);
+#pragma unroll
+      for (int r = 0; r < RW; ++r) {
+        bool ok = all_rows;
+        if (!SPARSE && !all_rows && tok_ok) {
+          const int lim = p.is_causal ? L - p.s_q + (g * R + rb + r) / p.h_q : L - 1;
+          ok = pos <= lim;
+        }
+        x[r] = ok ? x[r] * p.scale_log2 : kNegInf;
+      }
+
+      // lazy max update: raise the running max only when some logit exceeds it
+      // by more than the threshold (always on the first tile of a segment)
       bool need = (j == tb);
       if (!need) {
         float loc = kNegInf;
 #pragma unroll
-        for (int q = 0; q < R / 16; ++q) {
-          float v[16];
-          load16(q, v);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) loc = fmaxf(loc, v[e] - m_s[16 * q + e]);
+        for (int r4 = 0; r4 < RW / 4; ++r4) {
+          const float4 m4 = reinterpret_cast<const float4*>(m_s + rb)[r4];
+          loc = fmaxf(loc, fmaxf(fmaxf(x[4 * r4] - m4.x, x[4 * r4 + 1] - m4.y),
+                                 fmaxf(x[4 * r4 + 2] - m4.z, x[4 * r4 + 3] - m4.w)));
         }
-        const bool w_need = __any_sync(0xffffffffu, loc > kRescaleThreshold);
-        if (lane == 0) vote[(jt & 1) * 4 + warp_q] = w_need ? 1 : 0;
-        if (!group_sync(bars.grp, gphase, wd)) return;
-        const int* vv = vote + (jt & 1) * 4;
-        need = (vv[0] | vv[1] | vv[2] | vv[3]) != 0;
+        need = named_bar_or(bar_id, 128, loc > kRescaleThreshold);
+        if (tracer) MLA_TR(kTrSmVote, jt);
       }
       if (need) {
-#pragma unroll
-        for (int q = 0; q < R / 16; ++q) {
-          float v[16];
-          load16(q, v);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float mx = warp_max(v[e]);
-            if (lane == ((16 * q + e) & 31)) red[warp_q * R + 16 * q + e] = mx;
-          }
-        }
-        if (!group_sync(bars.grp, gphase, wd)) return;
-        if (tid < R) {
-          const float mx = fmaxf(fmaxf(red[tid], red[R + tid]), fmaxf(red[2 * R + tid], red[3 * R + tid]));
-          const float mo = m_s[tid];
+        warp_reduce_scatter<RW, true>(x, red + warp_q * R + rb, lane);
+        gsync();
+        if (tid < RW) {
+          const int r = rb + tid;
+          const float mx = fmaxf(fmaxf(red[r], red[R + r]), fmaxf(red[2 * R + r], red[3 * R + r]));
+          const float mo = m_s[r];
           const float mn = fmaxf(mo, mx);
-          alpha_s[tid] = (mo == kNegInf) ? 0.f : fast_exp2(mo - mn);
-          m_s[tid] = mn;
+          alpha_s[r] = (mo == kNegInf) ? 0.f : fast_exp2(mo - mn);
+          m_s[r] = mn;
         }
-        if (!group_sync(bars.grp, gphase, wd)) return;
+        gsync();
 #pragma unroll
-        for (int r = 0; r < R; ++r) l[r] *= alpha_s[r];
+        for (int r = 0; r < RW; ++r) l[r] *= alpha_s[rb + r];
         if (j != tb) {
           // O^T of the previous tiles is complete (its MMAs precede this tile's S^T);
-          // rescale each row's column by alpha.
+          // rescale this warpgroup's row columns by alpha.
 #pragma unroll 1
           for (int blk = 0; blk < 4; ++blk) {
 #pragma unroll
-            for (int q = 0; q < R / 16; ++q) {
+            for (int q = 0; q < RW / 16; ++q) {
               float v[16];
-              const uint32_t ta = tmem + lane_base + C::kOCol + blk * R + 16 * q;
+              const uint32_t ta = tmem + lane_base + C::kOCol + blk * R + rb + 16 * q;
               tmem_ld_x16(ta, v);
               tmem_ld_wait();
 #pragma unroll
-              for (int e = 0; e < 16; ++e) v[e] *= alpha_s[16 * q + e];
+              for (int e = 0; e < 16; ++e) v[e] *= alpha_s[rb + 16 * q + e];
               tmem_st_x16(ta, v);
             }
           }
@@ -489,55 +644,67 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
         }
       }
 
-      // probabilities -> P (bf16, K-major 128B-swizzled [2][R][64 tokens]) and row sums
+      // probabilities -> P (bf16) and row sums
 #pragma unroll
-      for (int q = 0; q < R / 16; ++q) {
-        float v[16];
-        load16(q, v);
+      for (int r8 = 0; r8 < RW / 8; ++r8) {
+        const float4 ma = reinterpret_cast<const float4*>(m_s + rb)[2 * r8];
+        const float4 mb = reinterpret_cast<const float4*>(m_s + rb)[2 * r8 + 1];
+        const float mr[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+        float pr[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int r = 16 * q + e;
-          const float pr = (v[e] == kNegInf) ? 0.f : fast_exp2(v[e] - m_s[r]);
-          l[r] += pr;
-          const uint32_t addr = p_base + p_row_off + r * 128 + ((p_chunk ^ (r & 7)) << 4);
-          st_shared_u16(addr, __bfloat16_as_ushort(__float2bfloat16_rn(pr)));
+        for (int e = 0; e < 8; ++e) {
+          const int r = 8 * r8 + e;
+          pr[e] = (x[r] == kNegInf) ? 0.f : fast_exp2(x[r] - mr[e]);
+          l[r] += pr[e];
+        }
+        if (C::kPMnMajor) {
+          // P^T as [token][R rows] (MN-major B operand): one 16-byte chunk per 8 rows
+          const uint32_t ch = (rb >> 3) + r8;
+          st_shared_v4(p_base + tid * 128 + ((ch ^ (tid & 7)) << 4), pack_bf16x2(pr[0], pr[1]),
+                       pack_bf16x2(pr[2], pr[3]), pack_bf16x2(pr[4], pr[5]), pack_bf16x2(pr[6], pr[7]));
+        } else {
+          // P as [2][R rows][64 tokens] (K-major B operand)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int r = rb + 8 * r8 + e;
+            const uint32_t addr = p_base + p_row_off + r * 128 + ((p_chunk ^ (r & 7)) << 4);
+            st_shared_u16(addr, __bfloat16_as_ushort(__float2bfloat16_rn(pr[e])));
+          }
         }
       }
-      tc_fence_before();
-      mbar_arrive(bars.s_empty + sb);
       if (!SPARSE && !tok_ok) {
-        // a masked token's V row must be finite (0 * NaN would poison O): zero it
+        // a masked token's V row must be finite (0 * NaN would poison O): zero
+        // it (the warpgroups split the eight value chunks)
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t base = smem_u32(kv) + c * C::kKvChunkBytes + tid * 128;
+        for (int c = wg; c < 8; c += C::kSmWG) {
+          const uint32_t base = smem_u32(kv) + Ring<C>::chunk_off(jt, c) + tid * 128;
 #pragma unroll
           for (int q = 0; q < 8; ++q) st_shared_v4(base + 16 * q, 0u, 0u, 0u, 0u);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bars.p_full);
+      warp_arrive(bars.p_full);
+      if (tracer) MLA_TR(kTrSmPFull, jt);
     }
 
     // ---- epilogue: O / l -> out (single piece) or fp32 partial (split problem)
-    if (!warp_wait(bars.o_full, seg & 1, wd)) return;
+    if (!group_ok(mbar_wait(bars.o_full, seg & 1, wd))) return;
     tc_fence_after();
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const float v = warp_sum(l[r]);
-      if (lane == (r & 31)) red[warp_q * R + r] = v;
+    if (tracer) MLA_TR(kTrEpiStart, seg);
+    warp_reduce_scatter<RW, false>(l, red + warp_q * R + rb, lane);
+    gsync();
+    if (tid < RW) {
+      const int r = rb + tid;
+      const float lt = red[r] + red[R + r] + red[2 * R + r] + red[3 * R + r];
+      inv_s[r] = lt > 0.f ? 1.0f / lt : 0.f;
+      lse_s[r] = lt > 0.f ? m_s[r] + log2f(lt) : kNegInf;
     }
-    if (!group_sync(bars.grp, gphase, wd)) return;
-    if (tid < R) {
-      const float lt = red[tid] + red[R + tid] + red[2 * R + tid] + red[3 * R + tid];
-      inv_s[tid] = lt > 0.f ? 1.0f / lt : 0.f;
-      lse_s[tid] = lt > 0.f ? m_s[tid] + log2f(lt) : kNegInf;
-    }
-    if (!group_sync(bars.grp, gphase, wd)) return;
+    gsync();
     const int nsplit = p.num_splits[prob + 1] - p.num_splits[prob];
     const bool final_out = nsplit == 1;
     int slot = p.num_splits[prob] + (prob == sg.p0 ? split0 : 0);
-    const int row0 = g * R;
+    const int row0 = g * R + rb;
     bool write_ok = true;
     if (!final_out && (slot < 0 || slot >= p.max_slots)) {
       write_ok = false;  // schedule does not match this call: record it, write nothing
@@ -547,15 +714,15 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
     for (int blk = 0; blk < 4; ++blk) {
       const int dv = blk * 128 + tid;
 #pragma unroll
-      for (int q = 0; q < R / 16; ++q) {
+      for (int q = 0; q < RW / 16; ++q) {
         float v[16];
-        tmem_ld_x16(tmem + lane_base + C::kOCol + blk * R + 16 * q, v);
+        tmem_ld_x16(tmem + lane_base + C::kOCol + blk * R + rb + 16 * q, v);
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int r = 16 * q + e;
           if (write_ok && row0 + r < p.rows) {
-            const float o = v[e] * inv_s[r];
+            const float o = v[e] * inv_s[rb + r];
             if (final_out) {
               __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
               out[(static_cast<int64_t>(prob) * p.rows + row0 + r) * kDv + dv] = __float2bfloat16_rn(o);
@@ -566,14 +733,15 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
         }
       }
     }
-    if (write_ok && tid < R && row0 + tid < p.rows) {
+    if (write_ok && tid < RW && row0 + tid < p.rows) {
       if (final_out)
-        p.lse[static_cast<int64_t>(prob) * p.rows + row0 + tid] = lse_s[tid];
+        p.lse[static_cast<int64_t>(prob) * p.rows + row0 + tid] = lse_s[rb + tid];
       else
-        p.lse_accum[static_cast<int64_t>(slot) * p.rows + row0 + tid] = lse_s[tid];
+        p.lse_accum[static_cast<int64_t>(slot) * p.rows + row0 + tid] = lse_s[rb + tid];
     }
     tc_fence_before();
-    mbar_arrive(bars.o_empty);
+    warp_arrive(bars.o_empty);
+    if (tracer) MLA_TR(kTrEpiEnd, seg);
     ++seg;
   }
 }
@@ -599,15 +767,15 @@ __global__ void __launch_bounds__(Cfg<R, SPARSE>::kThreads, 1)
   Bars bars;
   bars.q_full = bar + 0;
   bars.q_empty = bar + 1;
-  bars.kv_full = bar + 2;
-  bars.kv_empty = bar + 2 + kNumChunks;
-  bars.s_full = bar + 2 + 2 * kNumChunks;
+  bars.full = bar + 2;
+  bars.pair_empty = bars.full + C::kNumFull;
+  bars.rope_empty = bars.pair_empty + C::kNA;
+  bars.s_full = bars.rope_empty + C::kNB;
   bars.s_empty = bars.s_full + 2;
   bars.p_full = bars.s_empty + 2;
   bars.o_full = bars.p_full + 1;
   bars.o_empty = bars.o_full + 1;
   bars.mma_done = bars.o_empty + 1;
-  bars.grp = bars.mma_done + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -617,19 +785,17 @@ __global__ void __launch_bounds__(Cfg<R, SPARSE>::kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bars.q_full, 1);
     mbar_init(bars.q_empty, 1);
-    for (int c = 0; c < kNumChunks; ++c) {
-      mbar_init(bars.kv_full + c, SPARSE ? 128 : 1);
-      mbar_init(bars.kv_empty + c, 1);
-    }
+    for (int k = 0; k < C::kNumFull; ++k) mbar_init(bars.full + k, SPARSE ? 4 : 1);  // sparse: one per gather warp
+    for (int k = 0; k < C::kNA; ++k) mbar_init(bars.pair_empty + k, 1);
+    for (int k = 0; k < C::kNB; ++k) mbar_init(bars.rope_empty + k, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars.s_full + i, 1);
-      mbar_init(bars.s_empty + i, 128);
+      mbar_init(bars.s_empty + i, 4 * C::kSmWG);  // one arrival per softmax warp
     }
-    mbar_init(bars.p_full, 128);
+    mbar_init(bars.p_full, 4 * C::kSmWG);
     mbar_init(bars.o_full, 1);
-    mbar_init(bars.o_empty, 128);
+    mbar_init(bars.o_empty, 4 * C::kSmWG);
     mbar_init(bars.mma_done, 1);
-    mbar_init(bars.grp, 128);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -664,13 +830,17 @@ __global__ void __launch_bounds__(Cfg<R, SPARSE>::kThreads, 1)
     sg.p1 = sg.np;
   }
 
-  if (warp == 0) {
-    if (lane == 0) producer<R, SPARSE>(&tm_q, &tm_kv, p, sg, g, kv, qs, bars, wd);
-  } else if (warp == 1) {
-    if (lane == 0) mma_issuer<R, SPARSE>(sg, tmem, kv, qs, bars, wd);
-  } else if (warp >= 4 && warp < 8) {
-    softmax_epilogue<R, SPARSE>(p, sg, g, split0, tmem, kv, bars, aux, vote, wd);
-  } else if (SPARSE && warp >= 8) {
+  if (warp < 4) {
+    if (C::kRegSplit) regs_dec<C::kRegsCtl>();
+    if (warp == 0) {
+      if (lane == 0) producer<R, SPARSE>(&tm_q, &tm_kv, p, sg, g, kv, qs, bars, wd);
+    } else if (warp == 1) {
+      if (lane == 0) mma_issuer<R, SPARSE>(sg, tmem, kv, qs, bars, wd);
+    }
+  } else if (warp < C::kGatherWarp0) {
+    softmax_epilogue<R, SPARSE>(p, sg, g, split0, tmem, kv, bars, aux, wd);
+  } else if (SPARSE) {
+    if (C::kRegSplit) regs_inc<C::kRegsGather>();
     gather_fp8<R>(p, sg, kv, bars, wd);
   }
 
@@ -729,5 +899,17 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, con
   }
   return cudaErrorInvalidValue;
 }
+
+#ifdef MLA_TRACE
+// Copies the trace buffer (kTrNumEvents x kTraceTiles clock64 stamps) to host memory.
+extern "C" int mla_trace_read(unsigned long long* host, size_t n) {
+  if (n > sizeof(g_mla_trace) / sizeof(unsigned long long)) n = sizeof(g_mla_trace) / sizeof(unsigned long long);
+  if (cudaMemcpyFromSymbol(host, g_mla_trace, n * sizeof(unsigned long long)) != cudaSuccess) return -1;
+  unsigned long long z[256] = {};
+  for (size_t i = 0; i < sizeof(g_mla_trace); i += sizeof z)
+    cudaMemcpyToSymbol(g_mla_trace, z, sizeof z, i);
+  return static_cast<int>(n);
+}
+#endif
 
 }  // namespace mla

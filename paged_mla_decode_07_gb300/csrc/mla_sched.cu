@@ -45,6 +45,19 @@ __device__ Pos locate(const long long* pre, int np, long long x, const int32_t* 
   return Pos{lo, t};
 }
 
+// Last part k (0 <= k < num_parts) whose start is at or before x.
+__device__ int part_of(const Pos* starts, int num_parts, Pos x) {
+  int lo = 0, hi = num_parts - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (!pos_less(x, starts[mid]))
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
 // In-place inclusive scan of v[0..n) (long long) by the whole block.
 __device__ void block_inclusive_scan(long long* v, int n, long long* partial) {
   const int tid = threadIdx.x;
@@ -90,41 +103,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long total = pre[np];
 
   // 2. cut the cost line into num_parts equal pieces
+  // Cut points are distinct while k <= total (so equal part starts, i.e. empty
+  // parts, only arise inside a problem's start-up cost, at its tile 0, or at
+  // the very end); with less work than parts the surplus parts are empty.
   for (int k = tid; k <= num_parts; k += kThreads) {
-    long long x = total * static_cast<long long>(k) / num_parts;
+    long long x = total >= num_parts ? total * static_cast<long long>(k) / num_parts
+                                     : (static_cast<long long>(k) < total ? k : total);
     starts[k] = locate(pre, np, x, cache_seqlens, s_q, topk);
   }
   __syncthreads();
 
-  // 3. pieces per problem
+  // 3. pieces per problem.  Parts are contiguous and empty parts can only sit
+  // at a problem's tile 0, so the parts touching problem p are
+  // first(p) .. last(p), where part(x) = the last part starting at or before x.
   for (int p = tid; p < np; p += kThreads) {
     int n = problem_tiles(cache_seqlens, p, s_q, topk);
-    long long c = 0;
-    if (n > 0) {
-      Pos first{p, 0}, end{p, n};
-      for (int k = 0; k < num_parts; ++k) {
-        Pos a = starts[k], b = starts[k + 1];
-        if (pos_less(a, b) && pos_less(a, end) && pos_less(first, b)) ++c;
-      }
-    }
-    cnt[p] = c;
+    cnt[p] = n > 0 ? part_of(starts, num_parts, Pos{p, n - 1}) - part_of(starts, num_parts, Pos{p, 0}) + 1 : 0;
   }
   __syncthreads();
   block_inclusive_scan(cnt, np, partial);
   for (int p = tid; p <= np; p += kThreads) num_splits[p] = p == 0 ? 0 : static_cast<int32_t>(cnt[p - 1]);
 
-  // 4. schedule records
+  // 4. schedule records; a part's split index in its first problem is its
+  // distance from the first part touching that problem
   for (int k = tid; k < num_parts; k += kThreads) {
     Pos a = starts[k], b = starts[k + 1];
     int split0 = 0;
-    if (pos_less(a, b) && a.p < np) {
-      int n = problem_tiles(cache_seqlens, a.p, s_q, topk);
-      Pos first{a.p, 0}, end{a.p, n};
-      for (int j = 0; j < k; ++j) {
-        Pos c = starts[j], d = starts[j + 1];
-        if (pos_less(c, d) && pos_less(c, end) && pos_less(first, d)) ++split0;
-      }
-    }
+    if (pos_less(a, b) && a.p < np) split0 = k - part_of(starts, num_parts, Pos{a.p, 0});
     int32_t* r = sched + static_cast<size_t>(k) * kSchedInts;
     r[kSchedP0] = a.p;
     r[kSchedT0] = a.t;
