@@ -49,7 +49,8 @@ namespace mla {
 // main pipeline events of CTA 0, one slot per (event, tile).
 enum TraceEvent {
   kTrProdChunk0 = 0, kTrProdChunk8, kTrMmaKv0, kTrMmaKv8, kTrMmaSDone, kTrSmSFull, kTrSmVote, kTrSmPFull,
-  kTrMmaPFull, kTrMmaODone, kTrGatherStart, kTrGatherDone, kTrEpiStart, kTrEpiEnd, kTrNumEvents
+  kTrMmaPFull, kTrMmaODone, kTrGatherStart, kTrGatherDone, kTrEpiStart, kTrEpiEnd, kTrSmLoaded, kTrSmPStored,
+  kTrMmaO1, kTrNumEvents
 };
 #ifdef MLA_TRACE
 constexpr int kTraceTiles = 1024;
@@ -112,8 +113,9 @@ struct Cfg {
   // rounded to 128 bytes so the row statistics after the barriers are 16-byte
   // aligned (they are read with 16-byte vector loads)
   static constexpr int kBarBytes = (kNumBars * 8 + 127) / 128 * 128;
-  // aux floats: m[R], alpha[R], inv_l[R], lse[R], red[4][R]; ints: vote[2][4], abort, tmem
-  static constexpr int kAuxBytes = kBarBytes + 8 * R * 4 + 64;
+  // aux: floats m[R], alpha[R], inv_l[R], lse[R], red[4][R]; 16 ints (abort flag,
+  // TMEM base); 256 bytes of per-tile token validity flags (two tiles in flight)
+  static constexpr int kAuxBytes = kBarBytes + 8 * R * 4 + 64 + 256;
   static constexpr int kSmemBytes = kAuxOff + kAuxBytes + 1024;  // + alignment slack
   static constexpr int kOCol = 0;
   static constexpr int kSCol = 4 * R;
@@ -191,7 +193,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 template <int R, bool SPARSE>
 __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, const DecodeParams& p,
                          const Segments& sg, int g, uint8_t* kv, uint8_t* qs, const Bars& bars,
-                         const Watchdog& wd) {
+                         volatile uint8_t* flags, const Watchdog& wd) {
   using C = Cfg<R, SPARSE>;
   const uint64_t pol_kv = p.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
   const uint64_t pol_q = l2_policy_evict_normal();
@@ -235,6 +237,12 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, cons
           if (item < 4) {
             const uint32_t use = RG::pair_use(jt, item);
             if (use > 0 && !mbar_wait(bars.pair_empty + RG::pair_slot(jt, item), (use - 1) & 1, wd)) goto drain;
+            if (item == 0) {
+              // page flags of this tile for the softmax (its readers of two
+              // tiles ago are done: their PV released this pair slot)
+              flags[(jt & 1) * 128 + 0] = ok_a ? 1 : 0;
+              flags[(jt & 1) * 128 + 1] = ok_b ? 1 : 0;
+            }
             c0 = 2 * item;
             nc = 2;
           } else {
@@ -330,6 +338,7 @@ __device__ void mma_issuer(const Segments& sg, uint32_t tmem, uint8_t* kv, uint8
           umma_bf16_ss(tmem + C::kOCol + blk * R, a, b, kIdO, !(j == tb && kk == 0));
         }
         umma_commit(bars.pair_empty + RG::pair_slot(jt, blk));
+        if (blk == 0) MLA_TR(kTrMmaO1, jt);
       }
       if (!C::kRing) umma_commit(bars.rope_empty + RG::rope_slot(jt));  // P lived in the RoPE slot
       MLA_TR(kTrMmaODone, jt);
@@ -354,7 +363,7 @@ __device__ __forceinline__ uint32_t dequant2(uint32_t codes16, float scale) {
 
 template <int R>
 __device__ void gather_fp8(const DecodeParams& p, const Segments& sg, uint8_t* kv, const Bars& bars,
-                           const Watchdog& wd) {
+                           volatile uint8_t* flags, const Watchdog& wd) {
   using C = Cfg<R, true>;
   using RG = Ring<C>;
   const int tid = threadIdx.x - 32 * C::kGatherWarp0;
@@ -396,6 +405,7 @@ __device__ void gather_fp8(const DecodeParams& p, const Segments& sg, uint8_t* k
         if ((c & 1) == 0) {
           const uint32_t use = RG::pair_use(jt, c >> 1);
           if (use > 0 && !warp_wait(bars.pair_empty + RG::pair_slot(jt, c >> 1), (use - 1) & 1, wd)) return;
+          if (c == 0) flags[(jt & 1) * 128 + tid] = ok ? 1 : 0;  // token validity for the softmax
         }
         const uint32_t sw_word = (c >> 1) == 0 ? cs[32].x : ((c >> 1) == 1 ? cs[32].y : ((c >> 1) == 2 ? cs[32].z : cs[32].w));
         const float scale = __uint_as_float(sw_word);
@@ -491,7 +501,8 @@ __device__ __forceinline__ void warp_reduce_scatter(const float (&v)[N], float* 
 
 template <int R, bool SPARSE>
 __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int g, int split0, uint32_t tmem,
-                                 uint8_t* kv, const Bars& bars, float* aux, const Watchdog& wd) {
+                                 uint8_t* kv, const Bars& bars, float* aux, volatile uint8_t* flags,
+                                 const Watchdog& wd) {
   using C = Cfg<R, SPARSE>;
   constexpr int RW = R / C::kSmWG;  // rows owned by this warpgroup
   const int wg = (threadIdx.x - 128) >> 7;
@@ -535,8 +546,6 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
     if (tb >= te) continue;
     const int b = SPARSE ? prob / p.s_q : prob;
     const int L = sg.seqlens[b];
-    const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
-    const int32_t* idx_row = SPARSE ? p.indices + static_cast<int64_t>(prob) * p.topk : nullptr;
     // causal limit per row: query token i sees keys <= L - s_q + i (dense only)
     int lim_min = L - 1;
     if (!SPARSE && p.is_causal) {
@@ -550,27 +559,17 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
 
     for (int j = tb; j < te; ++j, ++jt) {
       const int sb = jt & 1;
-      // token validity (loads issued before the wait for S)
-      int pos;
-      bool tok_ok;
-      if (SPARSE) {
-        const int k = j * kTileTokens + tid;
-        pos = k < p.topk ? idx_row[k] : -1;
-        tok_ok = pos >= 0 && pos < L && (pos >> 6) < p.block_table_stride;
-        if (tok_ok) {
-          const int pg = bt[pos >> 6];
-          tok_ok = pg >= 0 && pg < p.num_pages;
-        }
-      } else {
-        pos = j * kTileTokens + tid;
-        tok_ok = pos < L && (pos >> 6) < p.block_table_stride;
-        if (tok_ok) {
-          const int pg = bt[pos >> 6];
-          tok_ok = pg >= 0 && pg < p.num_pages;
-        }
+      // S^T of this tile is complete; the wait on the tile's chunk-7 barrier
+      // (already complete) orders the loader's validity flags before our reads
+      {
+        bool ok = mbar_wait(bars.s_full + sb, (jt >> 1) & 1, wd);
+        ok = ok && mbar_wait(bars.full + Ring<C>::full_index(jt, 7), Ring<C>::full_use(jt, 7) & 1, wd);
+        if (!group_ok(ok)) return;
       }
-      if (!group_ok(mbar_wait(bars.s_full + sb, (jt >> 1) & 1, wd))) return;
       tc_fence_after();
+      const int pos = j * kTileTokens + tid;  // dense: logical token of this thread
+      const bool tok_ok = SPARSE ? flags[(jt & 1) * 128 + tid] != 0
+                                 : (pos < L && flags[(jt & 1) * 128 + (tid >> 6)] != 0);
       if (tracer) MLA_TR(kTrSmSFull, jt);
 
       // this thread's token, this warpgroup's rows of S^T: all loads in flight, one wait
@@ -583,6 +582,7 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
       }
       tc_fence_before();
       warp_arrive(bars.s_empty + sb);  // S is in registers; the buffer can be rewritten
+      if (tracer) MLA_TR(kTrSmLoaded, jt);
 
       // logits in log2 units; masked -> -inf
       const bool all_rows = tok_ok && (SPARSE || pos <= lim_min);
@@ -682,6 +682,7 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
           for (int q = 0; q < 8; ++q) st_shared_v4(base + 16 * q, 0u, 0u, 0u, 0u);
         }
       }
+      if (tracer) MLA_TR(kTrSmPStored, jt);
       fence_proxy_async_smem();
       tc_fence_before();
       warp_arrive(bars.p_full);
@@ -760,9 +761,13 @@ __global__ void __launch_bounds__(Cfg<R, SPARSE>::kThreads, 1)
   uint8_t* qs = smem + C::kQOff;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kAuxOff);
   float* aux = reinterpret_cast<float*>(smem + C::kAuxOff + C::kBarBytes);
-  int* vote = reinterpret_cast<int*>(aux + 8 * R);
-  volatile int* abort_flag = vote + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vote + 9);
+  int* ints = reinterpret_cast<int*>(aux + 8 * R);
+  volatile int* abort_flag = ints + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ints + 9);
+  // flags[(jt & 1) * 128 + t]: sparse: token t of tile jt is valid (written by
+  // the gather warps); dense: [0], [1] = the tile's two pages are usable
+  // (written by the producer)
+  volatile uint8_t* flags = reinterpret_cast<volatile uint8_t*>(ints + 16);
 
   Bars bars;
   bars.q_full = bar + 0;
@@ -833,15 +838,15 @@ __global__ void __launch_bounds__(Cfg<R, SPARSE>::kThreads, 1)
   if (warp < 4) {
     if (C::kRegSplit) regs_dec<C::kRegsCtl>();
     if (warp == 0) {
-      if (lane == 0) producer<R, SPARSE>(&tm_q, &tm_kv, p, sg, g, kv, qs, bars, wd);
+      if (lane == 0) producer<R, SPARSE>(&tm_q, &tm_kv, p, sg, g, kv, qs, bars, flags, wd);
     } else if (warp == 1) {
       if (lane == 0) mma_issuer<R, SPARSE>(sg, tmem, kv, qs, bars, wd);
     }
   } else if (warp < C::kGatherWarp0) {
-    softmax_epilogue<R, SPARSE>(p, sg, g, split0, tmem, kv, bars, aux, wd);
+    softmax_epilogue<R, SPARSE>(p, sg, g, split0, tmem, kv, bars, aux, flags, wd);
   } else if (SPARSE) {
     if (C::kRegSplit) regs_inc<C::kRegsGather>();
-    gather_fp8<R>(p, sg, kv, bars, wd);
+    gather_fp8<R>(p, sg, kv, bars, flags, wd);
   }
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -26,8 +26,9 @@ struct Pos {
 
 __device__ __forceinline__ bool pos_less(Pos a, Pos b) { return a.p < b.p || (a.p == b.p && a.t < b.t); }
 
-// Cost-line position x -> (problem, tile).  pre[q] = cost of problems < q.
-__device__ Pos locate(const long long* pre, int np, long long x, const int32_t* seqlens, int s_q, int topk) {
+// Cost-line position x -> (problem, tile).  pre[q] = cost of problems < q,
+// tiles[q] = tiles of problem q.
+__device__ Pos locate(const long long* pre, const int* tiles, int np, long long x) {
   if (x >= pre[np]) return Pos{np, 0};
   // largest p with pre[p] <= x (problems of zero cost share a prefix value; take the last)
   int lo = 0, hi = np - 1;
@@ -39,9 +40,8 @@ __device__ Pos locate(const long long* pre, int np, long long x, const int32_t* 
       hi = mid - 1;
   }
   long long o = x - pre[lo] - kCostOverheadTiles;
-  int n = problem_tiles(seqlens, lo, s_q, topk);
   int t = o > 0 ? static_cast<int>(o) : 0;
-  if (t >= n) return Pos{lo + 1, 0};
+  if (t >= tiles[lo]) return Pos{lo + 1, 0};
   return Pos{lo, t};
 }
 
@@ -58,9 +58,11 @@ __device__ int part_of(const Pos* starts, int num_parts, Pos x) {
   return lo;
 }
 
-// In-place inclusive scan of v[0..n) (long long) by the whole block.
-__device__ void block_inclusive_scan(long long* v, int n, long long* partial) {
-  const int tid = threadIdx.x;
+// In-place inclusive scan of v[0..n) by the whole block: each thread scans a
+// contiguous run, warps scan their run totals with shuffles, one warp scans
+// the warp totals.  warp_tot holds kThreads / 32 entries.
+__device__ void block_inclusive_scan(long long* v, int n, long long* warp_tot) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int per = (n + kThreads - 1) / kThreads;
   const int b = tid * per;
   const int e = min(n, b + per);
@@ -69,15 +71,25 @@ __device__ void block_inclusive_scan(long long* v, int n, long long* partial) {
     s += v[i];
     v[i] = s;
   }
-  partial[tid] = s;
-  __syncthreads();
-  for (int off = 1; off < kThreads; off <<= 1) {
-    long long add = tid >= off ? partial[tid - off] : 0;
-    __syncthreads();
-    partial[tid] += add;
-    __syncthreads();
+  long long x = s;  // inclusive scan of run totals within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  long long base = tid > 0 ? partial[tid - 1] : 0;
+  if (lane == 31) warp_tot[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    long long t = lane < kThreads / 32 ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    if (lane < kThreads / 32) warp_tot[lane] = t;
+  }
+  __syncthreads();
+  const long long base = (x - s) + (w > 0 ? warp_tot[w - 1] : 0);
   for (int i = b; i < e; ++i) v[i] += base;
   __syncthreads();
 }
@@ -87,29 +99,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     int32_t* __restrict__ sched, int32_t* __restrict__ num_splits, uint32_t* status) {
   extern __shared__ __align__(16) unsigned char smem[];
   long long* pre = reinterpret_cast<long long*>(smem);             // [np + 1]
-  long long* partial = pre + (np + 1);                             // [kThreads]
+  long long* warp_tot = pre + (np + 1);                            // [kThreads / 32]
   long long* cnt = pre;                                            // [np], reuses pre after step 2
-  Pos* starts = reinterpret_cast<Pos*>(partial + kThreads);        // [num_parts + 1]
+  Pos* starts = reinterpret_cast<Pos*>(warp_tot + kThreads / 32);  // [num_parts + 1]
+  int* tiles = reinterpret_cast<int*>(starts + num_parts + 1);     // [np]
   const int tid = threadIdx.x;
 
-  // 1. problem costs and their prefix sums
+  // 1. problem tiles (one read of cache_seqlens), costs and their prefix sums
   for (int p = tid; p < np; p += kThreads) {
-    int n = problem_tiles(cache_seqlens, p, s_q, topk);
+    const int n = problem_tiles(cache_seqlens, p, s_q, topk);
+    tiles[p] = n;
     pre[p + 1] = n > 0 ? static_cast<long long>(n) + kCostOverheadTiles : 0;
   }
   if (tid == 0) pre[0] = 0;
   __syncthreads();
-  block_inclusive_scan(pre + 1, np, partial);
+  block_inclusive_scan(pre + 1, np, warp_tot);
   const long long total = pre[np];
 
-  // 2. cut the cost line into num_parts equal pieces
-  // Cut points are distinct while k <= total (so equal part starts, i.e. empty
-  // parts, only arise inside a problem's start-up cost, at its tile 0, or at
-  // the very end); with less work than parts the surplus parts are empty.
+  // 2. cut the cost line into num_parts equal pieces.  Cut points are distinct
+  // while k <= total (so equal part starts, i.e. empty parts, only arise inside
+  // a problem's start-up cost, at its tile 0, or at the very end); with less
+  // work than parts the surplus parts are empty.
   for (int k = tid; k <= num_parts; k += kThreads) {
     long long x = total >= num_parts ? total * static_cast<long long>(k) / num_parts
                                      : (static_cast<long long>(k) < total ? k : total);
-    starts[k] = locate(pre, np, x, cache_seqlens, s_q, topk);
+    starts[k] = locate(pre, tiles, np, x);
   }
   __syncthreads();
 
@@ -117,11 +131,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // at a problem's tile 0, so the parts touching problem p are
   // first(p) .. last(p), where part(x) = the last part starting at or before x.
   for (int p = tid; p < np; p += kThreads) {
-    int n = problem_tiles(cache_seqlens, p, s_q, topk);
+    const int n = tiles[p];
     cnt[p] = n > 0 ? part_of(starts, num_parts, Pos{p, n - 1}) - part_of(starts, num_parts, Pos{p, 0}) + 1 : 0;
   }
   __syncthreads();
-  block_inclusive_scan(cnt, np, partial);
+  block_inclusive_scan(cnt, np, warp_tot);
   for (int p = tid; p <= np; p += kThreads) num_splits[p] = p == 0 ? 0 : static_cast<int32_t>(cnt[p - 1]);
 
   // 4. schedule records; a part's split index in its first problem is its
@@ -146,7 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 size_t metadata_smem_bytes(int np, int num_parts) {
-  return sizeof(long long) * (np + 1) + sizeof(long long) * kThreads + sizeof(int) * 2 * (num_parts + 1);
+  return sizeof(long long) * (np + 1) + sizeof(long long) * (kThreads / 32) + sizeof(int) * 2 * (num_parts + 1) +
+         sizeof(int) * np;
 }
 
 cudaError_t launch_metadata(const int32_t* cache_seqlens, int batch, int s_q, int h_q, int topk,
