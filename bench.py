@@ -71,6 +71,36 @@ def algorithmic(inp) -> dict:
                 bytes=kv_bytes + q_bytes + out_bytes + tab)
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one mla_decode_kernel launch per
+# workload, from one `ncu --set full --clock-control none` capture of the bench command with
+# --workload <name> --no-extras --steps 3 --warmup 3.  Each figure holds only for the kernel
+# sources it was taken with: their SHA-256 prefix is stored beside it and the bench reports
+# null once the sources differ.
+NCU_TRAFFIC = {
+    "dense_membound": (652.04e6, "faa1f53445854f41"),
+    "dense_computebound": (360.77e6, "faa1f53445854f41"),
+    "sparse_fp8_long": (385.49e6, "faa1f53445854f41"),
+}
+KERNEL_SOURCES = ("mla_decode.cu", "mla_device.cuh", "mla_internal.h")
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_mla_decode_07_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """Bytes per launch of the dominant kernel from the stored capture, or None if stale/absent."""
+    entry = NCU_TRAFFIC.get(workload)
+    if entry is None or entry[1] != kernel_source_hash():
+        return None
+    return entry[0]
+
+
 def load_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -247,7 +277,8 @@ def run_mla(args):
     peaks = load_peaks()
 
     # ---- headline workload: full steps
-    inp = W.make_inputs(HEADLINE, device=device)
+    wname = args.workload
+    inp = W.make_inputs(wname, device=device)
     a = algorithmic(inp)
     step = DecodeStep(inp, device)
     for _ in range(args.warmup):
@@ -279,21 +310,31 @@ def run_mla(args):
     step.metadata()
     dts = time_events(step.decode, max(10, args.steps))
     dec_ms = statistics.mean(dts)
-    achieved = a["bytes"] / (dec_ms * 1e-3) / 1e9
+    wl = inp.workload
+    if wname in ("dense_membound", "tiny"):
+        roof = {"bound": "hbm", "achieved": round(a["bytes"] / (dec_ms * 1e-3) / 1e9, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": round(a["flops"] / (dec_ms * 1e-3) / 1e12, 2),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = measured_traffic(wname)
+    roof["algorithmic_bytes"] = a["bytes"] if roof["bound"] == "hbm" else None
+    rows = 16 if wl.s_q * wl.h_q <= 16 else (32 if wl.s_q * wl.h_q <= 32 else 64)
+    roof["kernel"] = f"mla_decode_kernel<{rows},{'sparse' if wl.mode == 'sparse' else 'dense'}> + combine (one decode call)"
+    roof["peak_source"] = peaks["source"]
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 q/KV, random page permutation)",
-        "config": {"workload": HEADLINE, "batch": inp.workload.batch, "h_q": inp.workload.h_q,
-                   "s_q": inp.workload.s_q, "seqlens": "uniform int [1024, 8192], seed 1002",
-                   "page_size": 64, "mode": "dense bf16 cache", "parallelism": f"replicas x{world}",
+        "config": {"workload": wname, "batch": wl.batch, "h_q": wl.h_q, "s_q": wl.s_q,
+                   "seqlens": W.describe_lengths(wl), "page_size": 64,
+                   "mode": "dense bf16 cache" if wl.mode == "dense" else f"sparse top-{wl.topk} fp8 cache",
+                   "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (KV %.0f MB > 129 MB), no flush" % (a["kv_bytes"] / 1e6)},
         "tflops": round(a["flops"] * world / (ms * 1e-3) / 1e12, 2),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
-                     "kernel": "mla_decode_kernel<16,dense> + combine (one decode call)",
-                     "peak_source": peaks["source"]},
+        "roofline": roof,
         "gpu_launches": 3 * args.steps,
         "device_status": flags,
         "clocks": clk.summary(),
@@ -301,7 +342,7 @@ def run_mla(args):
     del step
     torch.cuda.empty_cache()
 
-    if rank == 0 and world == 1 and not args.no_extras:
+    if rank == 0 and world == 1 and not args.no_extras and wname == HEADLINE:
         # ---- end to end through the public API with host buffers
         estep, h2d, d2h = e2e_step_factory(inp, device)
         for _ in range(2):
@@ -416,6 +457,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["mla", "reference"], default="mla")
     ap.add_argument("--no-extras", action="store_true", help="headline workload only")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(W.WORKLOADS),
+                    help="workload timed as the step (default: the memory-bound dense mix)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:

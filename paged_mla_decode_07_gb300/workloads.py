@@ -97,6 +97,16 @@ class Inputs:
                       dict(self.meta))
 
 
+def describe_lengths(w: Workload) -> str:
+    """The length rule of a workload, in words (for reports)."""
+    seed = SEEDS.get(w.name)
+    if w.seqlens is not None:
+        return f"fixed {list(w.seqlens)}"
+    if w.seqlen is not None:
+        return f"all {w.seqlen}"
+    return f"uniform int [{w.seqlen_range[0]}, {w.seqlen_range[1]}], seed {seed}"
+
+
 def draw_seqlens(w: Workload, rng: np.random.Generator) -> np.ndarray:
     if w.seqlens is not None:
         lens = np.asarray(w.seqlens, dtype=np.int64)
