@@ -263,6 +263,26 @@ def measure_workload(name, device, reps=20, warmup=3):
     return inp, a, ms, st
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest x over all ranks of the default process group (x itself without one)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(name: str, rank: int) -> int:
+    """Each rank decodes its own batch (weak scaling): rank r draws with the workload's seed + 100000*r."""
+    return W.SEEDS[name] + 100000 * rank
+
+
+def job_throughput(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time (per second)."""
+    return units_per_rank * world / (ms_max * 1e-3)
+
+
 def run_mla(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -278,7 +298,7 @@ def run_mla(args):
 
     # ---- headline workload: full steps
     wname = args.workload
-    inp = W.make_inputs(wname, device=device)
+    inp = W.make_inputs(wname, seed=rank_seed(wname, rank), device=device)
     a = algorithmic(inp)
     step = DecodeStep(inp, device)
     for _ in range(args.warmup):
@@ -297,14 +317,10 @@ def run_mla(args):
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    total_ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(t0.elapsed_time(t1), device)
     ms = total_ms / args.steps
     flags = mla.device_status()
-    value = a["bytes"] * world / (ms * 1e-3) / 1e9  # GB/s over all ranks
+    value = job_throughput(a["bytes"], world, ms) / 1e9  # GB/s over all ranks
 
     # ---- dominant kernel: decode call (split-KV kernel + combine), same workload
     step.metadata()

@@ -150,6 +150,23 @@ mla_status encode_rows_map(CUtensorMap* map, const void* base, long long nrows, 
   return MLA_OK;
 }
 
+// The FP8 cache as [rows][656] bytes (row = page * 64 + slot).  A box is 128
+// bytes of one row (the map's box is one row high, as row gathers require);
+// no swizzle: the gathered rows land as plain 128-byte rows.
+mla_status encode_fp8_rows_map(CUtensorMap* map, const void* base, long long nrows) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kFp8RowBytes), static_cast<cuuint64_t>(nrows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kFp8RowBytes)};
+  cuuint32_t box[2] = {128, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled(fp8 kvcache) failed with CUresult %d", (int)r);
+  return MLA_OK;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 uint64_t watchdog_ns() {
@@ -270,7 +287,8 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
                          "kvcache");
     if (st != MLA_OK) return st;
   } else {
-    tm_kv = tm_q;  // unused in sparse mode (the FP8 rows are gathered with plain loads)
+    st = encode_fp8_rows_map(&tm_kv, a->kvcache, static_cast<long long>(a->num_pages) * kPageSize);
+    if (st != MLA_OK) return st;
   }
 
   DecodeParams p;

@@ -50,7 +50,8 @@ namespace mla {
 enum TraceEvent {
   kTrProdChunk0 = 0, kTrProdChunk8, kTrMmaKv0, kTrMmaKv8, kTrMmaSDone, kTrSmSFull, kTrSmVote, kTrSmPFull,
   kTrMmaPFull, kTrMmaODone, kTrGatherStart, kTrGatherDone, kTrEpiStart, kTrEpiEnd, kTrSmLoaded, kTrSmPStored,
-  kTrMmaO1, kTrNumEvents
+  kTrMmaO1, kTrSmWaitS, kTrW1Loaded, kTrW2Loaded, kTrW3Loaded, kTrW0PreVote, kTrW1PreVote, kTrW2PreVote,
+  kTrW3PreVote, kTrNumEvents
 };
 #ifdef MLA_TRACE
 constexpr int kTraceTiles = 1024;
@@ -77,11 +78,16 @@ struct Cfg {
   static constexpr int kSmWG = (R == 64) ? 2 : 1;
   static constexpr int kGatherWarp0 = 4 + 4 * kSmWG;  // sparse: first FP8 gather warp
   static constexpr int kWarps = kGatherWarp0 + (SPARSE ? 4 : 0);
-  // sparse with two softmax warpgroups: 512 threads at 128 registers; the
-  // producer/MMA warpgroup gives 72 registers per thread to the gather
-  // warpgroup (128*56 + 2*128*128 + 128*200 = 65536 = the launch's total)
-  static constexpr bool kRegSplit = SPARSE && kSmWG == 2;
-  static constexpr uint32_t kRegsCtl = 56, kRegsGather = 200;
+  // With two softmax warpgroups the producer/MMA warpgroup hands registers to
+  // the others (setmaxnreg).  Sparse: 512 threads launched at 128 registers,
+  // 128*40 + 2*128*168 + 128*136 = 65536.  Dense: 384 threads at 168,
+  // 128*56 + 2*128*224 = 64512.  The host checks the compiled register count
+  // against kRegBudget before launching (an increase beyond the launch's total
+  // would never be granted).
+  static constexpr bool kRegSplit = kSmWG == 2;
+  static constexpr uint32_t kRegsCtl = SPARSE ? 40 : 56, kRegsSoftmax = SPARSE ? 168 : 224, kRegsGather = 136;
+  static constexpr int kRegBudget = 128 * kRegsCtl + 256 * kRegsSoftmax + (SPARSE ? 128 * kRegsGather : 0);
+  static_assert(!kRegSplit || kRegBudget <= 65536, "register split exceeds the register file");
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kKvChunkBytes = kTileTokens * 128;  // 16 KB: [128 tokens][64 dims] bf16
   static constexpr int kPairBytes = 2 * kKvChunkBytes;    // chunks 2b, 2b+1: one 128-dv block of V
@@ -109,13 +115,18 @@ struct Cfg {
   // barriers: q_full, q_empty, chunk_full[2*kNA + kNB], pair_empty[kNA], rope_empty[kNB],
   // s_full[2], s_empty[2], p_full, o_full, o_empty, mma_done
   static constexpr int kNumFull = 2 * kNA + kNB;
-  static constexpr int kNumBars = 2 + kNumFull + kNA + kNB + 4 + 3 + 1;
+  // sparse: raw FP8 rows of a tile land by row gathers in the upper half of
+  // each pair slot (codes) and in the RoPE slot; raw_full[b] (b = 0..3 pairs,
+  // 4 = RoPE) completes when they have arrived
+  static constexpr int kNumRaw = SPARSE ? 5 : 0;
+  static constexpr int kNumBars = 2 + kNumFull + kNA + kNB + 4 + 3 + 1 + kNumRaw;
   // rounded to 128 bytes so the row statistics after the barriers are 16-byte
   // aligned (they are read with 16-byte vector loads)
   static constexpr int kBarBytes = (kNumBars * 8 + 127) / 128 * 128;
   // aux: floats m[R], alpha[R], inv_l[R], lse[R], red[4][R]; 16 ints (abort flag,
-  // TMEM base); 256 bytes of per-tile token validity flags (two tiles in flight)
-  static constexpr int kAuxBytes = kBarBytes + 8 * R * 4 + 64 + 256;
+  // TMEM base); 256 bytes of per-tile token validity flags (two tiles in flight);
+  // ints lim[R] (last visible key per row)
+  static constexpr int kAuxBytes = kBarBytes + 8 * R * 4 + 64 + 256 + 4 * R;
   static constexpr int kSmemBytes = kAuxOff + kAuxBytes + 1024;  // + alignment slack
   static constexpr int kOCol = 0;
   static constexpr int kSCol = 4 * R;
@@ -138,6 +149,7 @@ struct Bars {
   uint64_t* o_full;
   uint64_t* o_empty;
   uint64_t* mma_done;
+  uint64_t* raw_full;  // sparse: [5]
 };
 
 // Segment iterator shared by all roles: the part walks problems p0..p1 and,
@@ -362,14 +374,18 @@ __device__ __forceinline__ uint32_t dequant2(uint32_t codes16, float scale) {
 }
 
 template <int R>
-__device__ void gather_fp8(const DecodeParams& p, const Segments& sg, uint8_t* kv, const Bars& bars,
-                           volatile uint8_t* flags, const Watchdog& wd) {
+__device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, const Segments& sg, uint8_t* kv,
+                           const Bars& bars, volatile uint8_t* flags, const Watchdog& wd) {
   using C = Cfg<R, true>;
   using RG = Ring<C>;
-  const int tid = threadIdx.x - 32 * C::kGatherWarp0;
-  const bool leader = (threadIdx.x & 31) == 0;
-  const uint32_t row_addr = smem_u32(kv) + tid * 128;
-  const uint32_t sw = tid & 7;
+  static_assert(!C::kRing, "the sparse path stages one tile (4 pair slots + 1 RoPE slot)");
+  const int tid = threadIdx.x - 32 * C::kGatherWarp0;  // token of the tile
+  const int lane = tid & 31;
+  const int wbase = tid & ~31;                          // first token of this warp
+  const uint32_t tsw = tid & 7;
+  const uint32_t kv_base = smem_u32(kv);
+  const uint64_t pol = l2_policy_evict_normal();
+  int armed[5] = {0, 0, 0, 0, 0};  // phases of raw_full armed by this warp (drained on exit)
   int jt = 0;
   for (int prob = sg.p0; prob <= sg.last(); ++prob) {
     int tb, te;
@@ -387,60 +403,110 @@ __device__ void gather_fp8(const DecodeParams& p, const Segments& sg, uint8_t* k
         const int kn = (j + 1) * kTileTokens + tid;
         t_next = (j + 1 < te && kn < p.topk) ? idx_row[kn] : -1;
       }
+      // token -> cache row (page * 64 + slot); invalid tokens read row 0 and
+      // are written as zeros below
       bool ok = t >= 0 && t < L;
       const bool in_table = ok && (t >> 6) < p.block_table_stride;
       int page = in_table ? bt[t >> 6] : -1;
       if (ok && (page < 0 || page >= p.num_pages)) {
         ok = false;
-        page = 0;
         atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
       }
-      const uint8_t* src = p.kv_fp8 + (static_cast<int64_t>(page) * kPageSize + (t & 63)) * kFp8RowBytes;
-      uint4 cs[33];  // 512 codes + 4 scales
-#pragma unroll
-      for (int i = 0; i < 33; ++i) cs[i] = ok ? ld_global_nc_v4(src + 16 * i) : make_uint4(0, 0, 0, 0);
-      uint4 rope[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        if ((c & 1) == 0) {
-          const uint32_t use = RG::pair_use(jt, c >> 1);
-          if (use > 0 && !warp_wait(bars.pair_empty + RG::pair_slot(jt, c >> 1), (use - 1) & 1, wd)) return;
-          if (c == 0) flags[(jt & 1) * 128 + tid] = ok ? 1 : 0;  // token validity for the softmax
-        }
-        const uint32_t sw_word = (c >> 1) == 0 ? cs[32].x : ((c >> 1) == 1 ? cs[32].y : ((c >> 1) == 2 ? cs[32].z : cs[32].w));
-        const float scale = __uint_as_float(sw_word);
-        const uint32_t base = row_addr + RG::chunk_off(jt, c);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint4 v = cs[4 * c + (q >> 1)];
-          const uint32_t w0 = (q & 1) ? v.z : v.x;
-          const uint32_t w1 = (q & 1) ? v.w : v.y;
-          st_shared_v4(base + ((q ^ sw) << 4), dequant2(w0 & 0xffffu, scale), dequant2(w0 >> 16, scale),
-                       dequant2(w1 & 0xffffu, scale), dequant2(w1 >> 16, scale));
-        }
-        fence_proxy_async_smem();
+      const int row = ok ? page * kPageSize + (t & 63) : 0;
+      const uint4 sc = ok ? ld_global_nc_v4(p.kv_fp8 + static_cast<int64_t>(row) * kFp8RowBytes + 512)
+                          : make_uint4(0, 0, 0, 0);
+      // rows of this lane's group of four tokens (lanes 0..7 issue the gathers)
+      const int g4 = wbase + 4 * (lane & 7);
+      const int r0 = __shfl_sync(0xffffffffu, row, (4 * lane) & 31);
+      const int r1 = __shfl_sync(0xffffffffu, row, (4 * lane + 1) & 31);
+      const int r2 = __shfl_sync(0xffffffffu, row, (4 * lane + 2) & 31);
+      const int r3 = __shfl_sync(0xffffffffu, row, (4 * lane + 3) & 31);
+
+      // issue: the codes of value block b (dims 128b..128b+127) into the upper
+      // half of pair slot b once its previous tile's PV is done; then the RoPE
+      // bytes into the RoPE slot
+#pragma unroll 1
+      for (int blk = 0; blk < 4; ++blk) {
+        const uint32_t use = RG::pair_use(jt, blk);
+        if (use > 0 && !warp_wait(bars.pair_empty + RG::pair_slot(jt, blk), (use - 1) & 1, wd)) goto drain;
+        if (blk == 0) flags[(jt & 1) * 128 + tid] = ok ? 1 : 0;  // token validity for the softmax
+        if (lane == 0) mbar_arrive_expect_tx(bars.raw_full + blk, 32 * 128);
+        ++armed[blk];
         __syncwarp();
-        if (leader) mbar_arrive(bars.full + RG::full_index(jt, c));  // one arrival per gather warp
-        if (c == 1) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) rope[i] = ok ? ld_global_nc_v4(src + 528 + 16 * i) : make_uint4(0, 0, 0, 0);
+        if (lane < 8) {
+          uint8_t* dst = kv + RG::chunk_off(jt, 2 * blk + 1) + g4 * 128;
+          tma_gather4(dst, tm_rows, bars.raw_full + blk, 128 * blk, r0, r1, r2, r3, pol);
         }
       }
       {
         const uint32_t use = RG::rope_use(jt);
-        if (use > 0 && !warp_wait(bars.rope_empty + RG::rope_slot(jt), (use - 1) & 1, wd)) return;
+        if (use > 0 && !warp_wait(bars.rope_empty + RG::rope_slot(jt), (use - 1) & 1, wd)) goto drain;
+        if (lane == 0) mbar_arrive_expect_tx(bars.raw_full + 4, 32 * 128);
+        ++armed[4];
+        __syncwarp();
+        if (lane < 8) {
+          uint8_t* dst = kv + RG::chunk_off(jt, 8) + g4 * 128;
+          tma_gather4(dst, tm_rows, bars.raw_full + 4, 528, r0, r1, r2, r3, pol);
+        }
       }
-      {
-        const uint32_t base = row_addr + RG::chunk_off(jt, 8);
+
+      // dequantise in place: token tid's 128 code bytes of block b sit at row
+      // tid of chunk 2b+1; they become row tid of chunks 2b and 2b+1 (bf16,
+      // 128-byte swizzle).  Units are read in a per-thread rotated order.
+#pragma unroll 1
+      for (int blk = 0; blk < 4; ++blk) {
+        if (!warp_wait(bars.raw_full + blk, jt & 1, wd)) goto drain;
+        const float scale = __uint_as_float(blk == 0 ? sc.x : (blk == 1 ? sc.y : (blk == 2 ? sc.z : sc.w)));
+        const uint32_t lo = kv_base + RG::chunk_off(jt, 2 * blk) + tid * 128;
+        const uint32_t hi = kv_base + RG::chunk_off(jt, 2 * blk + 1) + tid * 128;
+        uint4 raw[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) st_shared_v4(base + ((q ^ sw) << 4), rope[q].x, rope[q].y, rope[q].z, rope[q].w);
+        for (int i = 0; i < 8; ++i) raw[i] = ld_shared_v4(hi + ((i ^ tsw) << 4));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t u = i ^ tsw;  // raw unit: codes 16u..16u+15 of the block
+          const uint32_t dst = ((u & 4) ? hi : lo);
+          const uint32_t k0 = (2 * (u & 3)) ^ tsw, k1 = (2 * (u & 3) + 1) ^ tsw;
+          uint4 v = raw[i];
+          if (!ok) v = make_uint4(0, 0, 0, 0);
+          st_shared_v4(dst + (k0 << 4), dequant2(v.x & 0xffffu, scale), dequant2(v.x >> 16, scale),
+                       dequant2(v.y & 0xffffu, scale), dequant2(v.y >> 16, scale));
+          st_shared_v4(dst + (k1 << 4), dequant2(v.z & 0xffffu, scale), dequant2(v.z >> 16, scale),
+                       dequant2(v.w & 0xffffu, scale), dequant2(v.w >> 16, scale));
+        }
         fence_proxy_async_smem();
         __syncwarp();
-        if (leader) mbar_arrive(bars.full + RG::full_index(jt, 8));
+        if (lane == 0) {
+          mbar_arrive(bars.full + RG::full_index(jt, 2 * blk));
+          mbar_arrive(bars.full + RG::full_index(jt, 2 * blk + 1));
+        }
+      }
+      {
+        // RoPE: already bf16; permute the 16-byte units into the swizzled order
+        if (!warp_wait(bars.raw_full + 4, jt & 1, wd)) goto drain;
+        const uint32_t base = kv_base + RG::chunk_off(jt, 8) + tid * 128;
+        uint4 raw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) raw[i] = ld_shared_v4(base + ((i ^ tsw) << 4));
+        // raw[i] holds unit i ^ tsw, whose swizzled position is (i ^ tsw) ^ tsw = i
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = ok ? raw[i] : make_uint4(0, 0, 0, 0);
+          st_shared_v4(base + (i << 4), v.x, v.y, v.z, v.w);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.full + RG::full_index(jt, 8));
         if (tid == 0) MLA_TR(kTrGatherDone, jt);
       }
     }
   }
+  return;
+drain:
+  // abort: wait (bounded) for this warp's row gathers still in flight
+#pragma unroll 1
+  for (int k = 0; k < 5; ++k)
+    if (armed[k] > 0) mbar_wait_drain(bars.raw_full + k, (armed[k] - 1) & 1, wd.limit_ns);
 }
 
 // ---------------------------------------------------------------------------
@@ -517,6 +583,8 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
   float* inv_s = aux + 2 * R;  // 1 / row sum
   float* lse_s = aux + 3 * R;  // row lse
   float* red = aux + 4 * R;    // [4][R] cross-warp reduction
+  // last visible key per row (causal), after the 16 ints and the 256 flag bytes
+  int* lim_s = reinterpret_cast<int*>(aux + 8 * R) + 16 + 64;
   const uint32_t p_base = smem_u32(kv) + C::kPOff;
   const uint32_t p_row_off = (tid >> 6) * C::kPHalfBytes + (tid & 7) * 2;
   const uint32_t p_chunk = (tid & 63) >> 3;
@@ -552,13 +620,17 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
       const int i_first = (g * R + rb) / p.h_q;
       lim_min = min(L - 1, L - p.s_q + i_first);
     }
-    if (tid < RW) m_s[rb + tid] = kNegInf;
+    if (tid < RW) {
+      m_s[rb + tid] = kNegInf;
+      lim_s[rb + tid] = (!SPARSE && p.is_causal) ? L - p.s_q + (g * R + rb + tid) / p.h_q : L - 1;
+    }
 #pragma unroll
     for (int r = 0; r < RW; ++r) l[r] = 0.f;
     gsync();
 
     for (int j = tb; j < te; ++j, ++jt) {
       const int sb = jt & 1;
+      if (tracer) MLA_TR(kTrSmWaitS, jt);
       // S^T of this tile is complete; the wait on the tile's chunk-7 barrier
       // (already complete) orders the loader's validity flags before our reads
       {
@@ -583,17 +655,27 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
       tc_fence_before();
       warp_arrive(bars.s_empty + sb);  // S is in registers; the buffer can be rewritten
       if (tracer) MLA_TR(kTrSmLoaded, jt);
+      if (wg == 0 && lane == 0 && warp_q > 0) MLA_TR(kTrW1Loaded + warp_q - 1, jt);
 
-      // logits in log2 units; masked -> -inf
+      // logits in log2 units; masked -> -inf.  Rows differ only where a causal
+      // limit falls inside the tile: their limits come from shared memory.
       const bool all_rows = tok_ok && (SPARSE || pos <= lim_min);
+      const float sc = p.scale_log2;
+      if (all_rows) {
 #pragma unroll
-      for (int r = 0; r < RW; ++r) {
-        bool ok = all_rows;
-        if (!SPARSE && !all_rows && tok_ok) {
-          const int lim = p.is_causal ? L - p.s_q + (g * R + rb + r) / p.h_q : L - 1;
-          ok = pos <= lim;
+        for (int r = 0; r < RW; ++r) x[r] *= sc;
+      } else if (SPARSE || !tok_ok) {
+#pragma unroll
+        for (int r = 0; r < RW; ++r) x[r] = kNegInf;
+      } else {
+#pragma unroll
+        for (int r4 = 0; r4 < RW / 4; ++r4) {
+          const int4 l4 = reinterpret_cast<const int4*>(lim_s + rb)[r4];
+          x[4 * r4] = pos <= l4.x ? x[4 * r4] * sc : kNegInf;
+          x[4 * r4 + 1] = pos <= l4.y ? x[4 * r4 + 1] * sc : kNegInf;
+          x[4 * r4 + 2] = pos <= l4.z ? x[4 * r4 + 2] * sc : kNegInf;
+          x[4 * r4 + 3] = pos <= l4.w ? x[4 * r4 + 3] * sc : kNegInf;
         }
-        x[r] = ok ? x[r] * p.scale_log2 : kNegInf;
       }
 
       // lazy max update: raise the running max only when some logit exceeds it
@@ -607,6 +689,7 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
           loc = fmaxf(loc, fmaxf(fmaxf(x[4 * r4] - m4.x, x[4 * r4 + 1] - m4.y),
                                  fmaxf(x[4 * r4 + 2] - m4.z, x[4 * r4 + 3] - m4.w)));
         }
+        if (wg == 0 && lane == 0) MLA_TR(kTrW0PreVote + warp_q, jt);
         need = named_bar_or(bar_id, 128, loc > kRescaleThreshold);
         if (tracer) MLA_TR(kTrSmVote, jt);
       }
@@ -781,6 +864,7 @@ __global__ void __launch_bounds__(Cfg<R, SPARSE>::kThreads, 1)
   bars.o_full = bars.p_full + 1;
   bars.o_empty = bars.o_full + 1;
   bars.mma_done = bars.o_empty + 1;
+  bars.raw_full = bars.mma_done + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -801,12 +885,13 @@ __global__ void __launch_bounds__(Cfg<R, SPARSE>::kThreads, 1)
     mbar_init(bars.o_full, 1);
     mbar_init(bars.o_empty, 4 * C::kSmWG);
     mbar_init(bars.mma_done, 1);
+    for (int k = 0; k < C::kNumRaw; ++k) mbar_init(bars.raw_full + k, 4);  // one arrive_expect_tx per gather warp
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_q);
-    if (!SPARSE) tma_prefetch_desc(&tm_kv);
+    tma_prefetch_desc(&tm_kv);
   }
   if (warp == 2) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -843,10 +928,11 @@ __global__ void __launch_bounds__(Cfg<R, SPARSE>::kThreads, 1)
       if (lane == 0) mma_issuer<R, SPARSE>(sg, tmem, kv, qs, bars, wd);
     }
   } else if (warp < C::kGatherWarp0) {
+    if (C::kRegSplit) regs_inc<C::kRegsSoftmax>();
     softmax_epilogue<R, SPARSE>(p, sg, g, split0, tmem, kv, bars, aux, flags, wd);
   } else if (SPARSE) {
     if (C::kRegSplit) regs_inc<C::kRegsGather>();
-    gather_fp8<R>(p, sg, kv, bars, flags, wd);
+    gather_fp8<R>(&tm_kv, p, sg, kv, bars, flags, wd);
   }
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -865,6 +951,12 @@ cudaError_t launch_one(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const 
   auto kern = mla_decode_kernel<R, SPARSE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
+  if (C::kRegSplit) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * C::kThreads < C::kRegBudget) return cudaErrorInvalidConfiguration;
+  }
   const int grid = p.num_parts * p.row_groups;
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_kv, p);
   return cudaGetLastError();
