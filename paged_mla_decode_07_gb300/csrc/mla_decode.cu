@@ -4,7 +4,7 @@
 // What is computed (per query row r of a problem and a range of its keys):
 // out = softmax(q K^T * sm_scale) V with V = K[:, :512] — the MQA form of MLA
 // (Modular design-doc overview, section 9 "Multi-Head Latent Attention") —
-// with online softmax across 128-token tiles (overview, section 6 "Matmul to
+// with online softmax across 64-token tiles (overview, section 6 "Matmul to
 // Flash Attention": running row max, exp(old_max - new_max) correction of
 // the running sum and output).  A CTA covering only part of a problem's keys
 // writes an fp32 partial and its log-sum-exp for the combine kernel
@@ -12,25 +12,35 @@
 //
 // Formulation: the MMAs run transposed, as proposed in the overview's section
 // 8 "U/WGMMA Flash Decoding" (option 0: P goes back through shared memory):
-//     S^T[tok, row] = K[tok, :] . Q[row, :]^T      M = 128 tokens, N = rows, K = 576
-//     O^T[dv, row] += V^T[dv, tok] . P^T[tok, row]  M = 128 dv (x4),  N = rows, K = 128 tokens
-// so every tcgen05.mma has M = 128 whatever the head count, and the fp32
-// accumulator O^T (4*rows TMEM columns) fits beside S^T in 512 columns.
-// The same shared-memory K tile is the K-major A operand of the first MMA and
-// (dims 0..511) the MN-major A operand of the second; no separate V load.
+//     S^T[tok, row] = K[tok, :] . Q[row, :]^T      M = 64 tokens, N = rows, K = 576
+//     O^T[dv, row] += V^T[dv, tok] . P^T[tok, row]  M = 128 dv (x4), N = rows, K = 64 tokens
+// A KV tile is one 64-token page.  An M = 64 MMA costs as many cycles as an
+// M = 128 one at these N, but halving the tile lets shared memory hold two
+// tiles beside Q, so the next tile loads while the current one is in the
+// softmax and PV stages.  The fp32 accumulator O^T (4*rows TMEM columns) fits
+// beside the two S^T buffers in 512 columns.  The same shared-memory K tile is
+// the K-major A operand of the first MMA and (dims 0..511) the MN-major A
+// operand of the second; no separate V load.
 //
 // Shared memory (1024-byte aligned):
-//   KV tile : 9 chunks x [128 tokens][64 dims] bf16, 128-byte swizzle  (144 KB)
-//   Q       : 9 chunks x [rows][64 dims] bf16, 128-byte swizzle        (rows*1152 B)
-//   P       : [2][rows][64 tokens] bf16, aliases KV chunk 8 (RoPE dims),
-//             which is dead once S^T of the tile is computed
+//   KV ring : kNA pair slots (2 chunks of [64 tokens][64 dims] bf16, 128-byte
+//             swizzle = one 128-dv block of V) + kNB RoPE-chunk slots
+//   Q       : 9 chunks x [rows][64 dims] bf16, 128-byte swizzle  (rows*1152 B)
+//   P       : per tile, bf16; in the tile's RoPE slot with 64 rows (dead once
+//             S^T is computed), else a separate double buffer
 //   barriers, row statistics
-// TMEM: O^T at columns [0, 4*rows), S^T double buffer at [4*rows, 6*rows).
+// TMEM: O^T at columns [0, 4*rows), S^T double buffer at [4*rows, 6*rows)
+// (an M = 64 result fills lanes 0..15 of each 32-lane quarter).
+//
+// Pipeline: the MMA warp issues S^T of tile j+1 before the PV MMAs of tile j,
+// so the tensor pipe computes scores while the softmax warps turn the
+// previous scores into P; loads run up to two tiles ahead.
 //
 // Warp roles: warp 0 = TMA producer (Q; dense KV pages), warp 1 = MMA
-// issuer, warp 2 = TMEM allocator, warps 4-7 = softmax + epilogue (thread t
-// owns token t of the tile and TMEM lane t), sparse only: warps 8-11 = FP8
-// gather + dequantisation (thread t fills token t of the tile).
+// issuer, warp 2 = TMEM allocator, warps 4.. = softmax + epilogue (one or two
+// warpgroups; lane l < 16 of warp q owns token 16q + l of the tile, and every
+// lane a dv row of O^T in the epilogue), sparse only: four more warps gather
+// the FP8 rows with TMA row gathers and dequantise them (two threads per token).
 //
 // The FP8 row (FlashMLA article, Design 2): 512 e4m3 codes, 4 fp32 scales
 // (one per 128 dims), 64 bf16 RoPE values; dequantised value =
@@ -51,7 +61,7 @@ enum TraceEvent {
   kTrProdChunk0 = 0, kTrProdChunk8, kTrMmaKv0, kTrMmaKv8, kTrMmaSDone, kTrSmSFull, kTrSmVote, kTrSmPFull,
   kTrMmaPFull, kTrMmaODone, kTrGatherStart, kTrGatherDone, kTrEpiStart, kTrEpiEnd, kTrSmLoaded, kTrSmPStored,
   kTrMmaO1, kTrSmWaitS, kTrW1Loaded, kTrW2Loaded, kTrW3Loaded, kTrW0PreVote, kTrW1PreVote, kTrW2PreVote,
-  kTrW3PreVote, kTrNumEvents
+  kTrW3PreVote, kTrProdC = kTrW3PreVote + 1, kTrMmaC = kTrProdC + 9, kTrFine = kTrMmaC + 9, kTrNumEvents = kTrFine + 8
 };
 #ifdef MLA_TRACE
 constexpr int kTraceTiles = 1024;
@@ -80,46 +90,47 @@ struct Cfg {
   static constexpr int kWarps = kGatherWarp0 + (SPARSE ? 4 : 0);
   // With two softmax warpgroups the producer/MMA warpgroup hands registers to
   // the others (setmaxnreg).  Sparse: 512 threads launched at 128 registers,
-  // 128*40 + 2*128*168 + 128*136 = 65536.  Dense: 384 threads at 168,
-  // 128*56 + 2*128*224 = 64512.  The host checks the compiled register count
+  // 128*64 + 2*128*160 + 128*128 = 65536.  Dense: 384 threads at 168,
+  // 128*88 + 2*128*208 = 64512.  The host checks the compiled register count
   // against kRegBudget before launching (an increase beyond the launch's total
   // would never be granted).
   static constexpr bool kRegSplit = kSmWG == 2;
-  static constexpr uint32_t kRegsCtl = SPARSE ? 40 : 56, kRegsSoftmax = SPARSE ? 168 : 224, kRegsGather = 136;
+  static constexpr uint32_t kRegsCtl = SPARSE ? 64 : 88, kRegsSoftmax = SPARSE ? 160 : 208, kRegsGather = 128;
   static constexpr int kRegBudget = 128 * kRegsCtl + 256 * kRegsSoftmax + (SPARSE ? 128 * kRegsGather : 0);
   static_assert(!kRegSplit || kRegBudget <= 65536, "register split exceeds the register file");
   static constexpr int kThreads = kWarps * 32;
-  static constexpr int kKvChunkBytes = kTileTokens * 128;  // 16 KB: [128 tokens][64 dims] bf16
+  static constexpr int kKvChunkBytes = kTileTokens * 128;  // 8 KB: [64 tokens][64 dims] bf16
   static constexpr int kPairBytes = 2 * kKvChunkBytes;    // chunks 2b, 2b+1: one 128-dv block of V
   static constexpr int kQChunkBytes = R * 128;
   static constexpr int kQBytes = kNumChunks * kQChunkBytes;
-  static constexpr int kPHalfBytes = R * 128;  // [R rows][64 tokens] bf16 (K-major P)
-  // KV staging ring: kNA pair slots + kNB RoPE-chunk slots.  A tile occupies
-  // 4 pair slots and 1 RoPE slot.  With 16 or 32 rows Q is small enough for a
-  // spare pair slot, an extra RoPE slot and a separate P buffer, so the next
-  // tile starts loading while this one is in the softmax and PV stages
-  // (kRing).  With 64 rows the ring is exactly one tile and P reuses the RoPE
-  // slot once S^T is done.
-  static constexpr bool kRing = !SPARSE && R <= 32;
-  static constexpr int kNA = kRing ? 5 : 4;
-  static constexpr int kNB = kRing ? (R == 16 ? 2 : 1) : 1;
+  static constexpr int kPBytes = R * kTileTokens * 2;     // P of one tile, bf16
+  // KV staging ring: kNA pair slots + kNB RoPE-chunk slots; a tile occupies 4
+  // pair slots and 1 RoPE slot.  The ring is sized to what shared memory holds
+  // beside Q: with 64 rows exactly two tiles, P of a tile then living in its
+  // RoPE slot once S^T has consumed the RoPE dims (kPAlias); with 16 or 32
+  // rows 2.5-2.75 tiles plus a separate double-buffered P.
+  static constexpr bool kPAlias = (R == 64);
+  static constexpr int kNA = R == 64 ? 8 : (R == 32 ? 10 : 11);
+  static constexpr int kNB = R == 64 ? 2 : (R == 32 ? 2 : 3);
   static constexpr int kPairOff = 0;
   static constexpr int kRopeOff = kNA * kPairBytes;
   static constexpr int kQOff = kRopeOff + kNB * kKvChunkBytes;
-  static constexpr int kPOff = kRing ? kQOff + kQBytes : kRopeOff;
-  static constexpr int kPBytes = kRing ? 2 * kPHalfBytes : 0;  // separate P buffer (ring only)
-  // With 64 rows P is stored MN-major ([128 tokens][64 rows], one 128-byte
+  static constexpr int kPOff = kQOff + kQBytes;                // separate P buffers (not kPAlias)
+  static constexpr int kPBufBytes = kPAlias ? 0 : 2 * kPBytes;
+  // With 64 rows P is stored MN-major ([64 tokens][64 rows], one 128-byte
   // swizzle atom per token): eight 16-byte stores per thread.
   static constexpr bool kPMnMajor = (R == 64);
-  static constexpr int kAuxOff = (kQOff + kQBytes + kPBytes + 1023) / 1024 * 1024;
+  static constexpr int kAuxOff = (kPOff + kPBufBytes + 1023) / 1024 * 1024;
   // barriers: q_full, q_empty, chunk_full[2*kNA + kNB], pair_empty[kNA], rope_empty[kNB],
-  // s_full[2], s_empty[2], p_full, o_full, o_empty, mma_done
-  static constexpr int kNumFull = 2 * kNA + kNB;
-  // sparse: raw FP8 rows of a tile land by row gathers in the upper half of
+  // s_full[2], s_empty[2], p_full[2], o_full, o_empty, mma_done, o_done[2], raw_full[kNumRaw]
+  // one "tile full" barrier per tile in flight (at most three: the ring
+  // holds under three tiles), used round robin: tile jt -> jt % 3, phase jt / 3
+  static constexpr int kNumFull = 3;
+  // sparse: raw FP8 rows of a tile land by row gathers in the upper chunk of
   // each pair slot (codes) and in the RoPE slot; raw_full[b] (b = 0..3 pairs,
   // 4 = RoPE) completes when they have arrived
   static constexpr int kNumRaw = SPARSE ? 5 : 0;
-  static constexpr int kNumBars = 2 + kNumFull + kNA + kNB + 4 + 3 + 1 + kNumRaw;
+  static constexpr int kNumBars = 2 + kNumFull + kNA + kNB + 4 + 2 + 5 + kNumRaw;
   // rounded to 128 bytes so the row statistics after the barriers are 16-byte
   // aligned (they are read with 16-byte vector loads)
   static constexpr int kBarBytes = (kNumBars * 8 + 127) / 128 * 128;
@@ -131,24 +142,30 @@ struct Cfg {
   static constexpr int kOCol = 0;
   static constexpr int kSCol = 4 * R;
   static constexpr int kTmemCols = (6 * R <= 128) ? 128 : ((6 * R <= 256) ? 256 : 512);
-  static_assert(2 * kPHalfBytes <= kKvChunkBytes, "P must fit in the RoPE chunk");
+
+  // arrivals on a tile's full barrier: dense 1 (the producer, + the tile's
+  // TMA bytes); sparse 4 (each gather warp once it has written its part)
+  static constexpr int kFullArrivals = SPARSE ? 4 : 1;
+  static_assert(kPBytes <= kKvChunkBytes || !kPAlias, "P must fit in the RoPE chunk");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(R == 16 || R == 32 || R == 64, "rows per CTA");
   static_assert((kAuxOff + kBarBytes) % 16 == 0, "row statistics must be 16-byte aligned");
+  static_assert(kTileTokens == kPageSize, "one KV tile is one page");
 };
 
 struct Bars {
   uint64_t* q_full;
   uint64_t* q_empty;
-  uint64_t* full;        // [kNumFull]: pair slot s chunk h -> 2s+h; RoPE slot t -> 2*kNA+t
+  uint64_t* full;        // [3]: tile jt's nine chunks are in shared memory (barrier jt % 3)
   uint64_t* pair_empty;  // [kNA]
   uint64_t* rope_empty;  // [kNB]
   uint64_t* s_full;    // [2]
   uint64_t* s_empty;   // [2]
-  uint64_t* p_full;
+  uint64_t* p_full;    // [2]: tile jt's P is ready (barrier jt & 1)
   uint64_t* o_full;
   uint64_t* o_empty;
   uint64_t* mma_done;
+  uint64_t* o_done;    // [2]: tile jt's PV MMAs are done (barrier jt & 1)
   uint64_t* raw_full;  // sparse: [5]
 };
 
@@ -181,8 +198,12 @@ struct Ring {
     return c < 8 ? C::kPairOff + pair_slot(jt, c >> 1) * C::kPairBytes + (c & 1) * C::kKvChunkBytes
                  : C::kRopeOff + rope_slot(jt) * C::kKvChunkBytes;
   }
-  __device__ static int full_index(int jt, int c) { return c < 8 ? 2 * pair_slot(jt, c >> 1) + (c & 1) : 2 * C::kNA + rope_slot(jt); }
-  __device__ static uint32_t full_use(int jt, int c) { return c < 8 ? pair_use(jt, c >> 1) : rope_use(jt); }
+  __device__ static int full_index(int jt) { return jt % 3; }
+  __device__ static uint32_t full_parity(int jt) { return static_cast<uint32_t>(jt / 3) & 1u; }
+  // byte offset of the P buffer of tile jt
+  __device__ static uint32_t p_off(int jt) {
+    return C::kPAlias ? C::kRopeOff + rope_slot(jt) * C::kKvChunkBytes : C::kPOff + (jt & 1) * C::kPBytes;
+  }
 };
 
 // Bounded wait that ignores the abort flag (used to drain own async work).
@@ -206,165 +227,300 @@ template <int R, bool SPARSE>
 __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, const DecodeParams& p,
                          const Segments& sg, int g, uint8_t* kv, uint8_t* qs, const Bars& bars,
                          volatile uint8_t* flags, const Watchdog& wd) {
+  // The whole producer warp runs this code converged; each copy is issued by
+  // one elected lane (as for the MMAs, a lane issuing alone while its warp
+  // waits elsewhere issues far more slowly).
   using C = Cfg<R, SPARSE>;
+
   const uint64_t pol_kv = p.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
   const uint64_t pol_q = l2_policy_evict_normal();
+  const int lane = threadIdx.x & 31;
   using RG = Ring<C>;
-  int armed[C::kNumFull];  // phases armed per full barrier (for the drain)
-#pragma unroll
-  for (int k = 0; k < C::kNumFull; ++k) armed[k] = 0;
+  // full barriers armed so far (bit per barrier) and the parity of each one's
+  // next phase, for the drain
+  uint32_t armed = 0, next_par = 0;
+  int fidx = 0;  // this tile's full barrier (jt % 3)
   int q_armed = 0, jt = 0;
   for (int prob = sg.p0; prob <= sg.last(); ++prob) {
     int tb, te;
     sg.range(prob, tb, te);
     if (tb >= te) continue;
-    if (q_armed > 0 && !mbar_wait(bars.q_empty, (q_armed - 1) & 1, wd)) goto drain;
+    if (q_armed > 0 && !warp_wait(bars.q_empty, (q_armed - 1) & 1, wd)) goto drain;
     {
       const int row0 = prob * p.rows + g * R;
-      mbar_arrive_expect_tx(bars.q_full, kNumChunks * C::kQChunkBytes);
+      if (elect_one()) {
+        mbar_arrive_expect_tx(bars.q_full, kNumChunks * C::kQChunkBytes);
 #pragma unroll 1
-      for (int c = 0; c < kNumChunks; ++c)
-        tma_load_3d(qs + c * C::kQChunkBytes, tm_q, bars.q_full, 0, c, row0, pol_q);
+        for (int c = 0; c < kNumChunks; ++c)
+          tma_load_3d(qs + c * C::kQChunkBytes, tm_q, bars.q_full, 0, c, row0, pol_q);
+      }
+      __syncwarp();
       ++q_armed;
     }
     if (!SPARSE) {
       const int b = prob;
-      const int L = sg.seqlens[b];
       const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
       for (int j = tb; j < te; ++j, ++jt) {
-        const bool in_a = 2 * j < p.block_table_stride;
-        const bool has_b = kTileTokens * j + kPageSize < L;
-        const bool in_b = has_b && 2 * j + 1 < p.block_table_stride;
-        const int pa = in_a ? bt[2 * j] : -1;
-        const int pb = in_b ? bt[2 * j + 1] : -1;
-        const bool ok_a = pa >= 0 && pa < p.num_pages;
-        const bool ok_b = has_b && pb >= 0 && pb < p.num_pages;
-        if (!ok_a || (has_b && !ok_b)) atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
-        const uint32_t bytes = (ok_a ? 8192u : 0u) + (ok_b ? 8192u : 0u);
-        // ring: the RoPE chunk first (its slot frees early); one-tile ring: pairs first
+        // tile j is page j of the element
+        const int pg = j < p.block_table_stride ? bt[j] : -1;
+        const bool ok = pg >= 0 && pg < p.num_pages;
+        if (!ok && lane == 0) atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
+        uint64_t* fb = bars.full + fidx;
+        bool tile_armed = false;
+        // RoPE chunk first when its slot frees at S^T (separate P); pairs first
+        // when P lives in the RoPE slot until the PV MMAs are done
 #pragma unroll 1
         for (int step = 0; step < 5; ++step) {
-          const int item = C::kRing ? (step == 0 ? 4 : step - 1) : step;  // 0..3 pairs, 4 RoPE
+          const int item = C::kPAlias ? step : (step == 0 ? 4 : step - 1);  // 0..3 pairs, 4 RoPE
           int c0, nc;
           if (item < 4) {
             const uint32_t use = RG::pair_use(jt, item);
-            if (use > 0 && !mbar_wait(bars.pair_empty + RG::pair_slot(jt, item), (use - 1) & 1, wd)) goto drain;
-            if (item == 0) {
-              // page flags of this tile for the softmax (its readers of two
+            if (use > 0 && !warp_wait(bars.pair_empty + RG::pair_slot(jt, item), (use - 1) & 1, wd)) goto drain;
+            if (item == 0 && lane == 0) {
+              // page flag of this tile for the softmax (its readers of two
               // tiles ago are done: their PV released this pair slot)
-              flags[(jt & 1) * 128 + 0] = ok_a ? 1 : 0;
-              flags[(jt & 1) * 128 + 1] = ok_b ? 1 : 0;
+              flags[(jt & 1) * 128] = ok ? 1 : 0;
             }
             c0 = 2 * item;
             nc = 2;
           } else {
             const uint32_t use = RG::rope_use(jt);
-            if (use > 0 && !mbar_wait(bars.rope_empty + RG::rope_slot(jt), (use - 1) & 1, wd)) goto drain;
+            if (use > 0 && !warp_wait(bars.rope_empty + RG::rope_slot(jt), (use - 1) & 1, wd)) goto drain;
             c0 = 8;
             nc = 1;
           }
-          for (int c = c0; c < c0 + nc; ++c) {
-            const int fi = RG::full_index(jt, c);
-            uint64_t* fb = bars.full + fi;
-            mbar_arrive_expect_tx(fb, bytes);
-            ++armed[fi];
-            if (c == 0) MLA_TR(kTrProdChunk0, jt);
-            if (c == 8) MLA_TR(kTrProdChunk8, jt);
-            uint8_t* dst = kv + RG::chunk_off(jt, c);
-            if (ok_a) tma_load_3d(dst, tm_kv, fb, 0, c, pa * kPageSize, pol_kv);
-            if (ok_b) tma_load_3d(dst + 8192, tm_kv, fb, 0, c, pb * kPageSize, pol_kv);
+          // the tile's full barrier is armed with all its bytes before its first
+          // copy, after that copy's slot wait (which implies the barrier's
+          // previous phase, three tiles back, has completed)
+          if (elect_one()) {
+            if (!tile_armed) mbar_arrive_expect_tx(fb, ok ? static_cast<uint32_t>(kNumChunks * C::kKvChunkBytes) : 0u);
+            if (ok)
+              for (int c = c0; c < c0 + nc; ++c)
+                tma_load_3d(kv + RG::chunk_off(jt, c), tm_kv, fb, 0, c, pg * kPageSize, pol_kv);
+          }
+          __syncwarp();
+          if (!tile_armed) {
+            tile_armed = true;
+            armed |= 1u << fidx;
+            next_par ^= 1u << fidx;
+          }
+          if (lane == 0) {
+            if (c0 == 0) MLA_TR(kTrProdChunk0, jt);
+            if (c0 == 8) MLA_TR(kTrProdChunk8, jt);
+            MLA_TR(kTrProdC + c0, jt);
           }
         }
+        if (++fidx == 3) fidx = 0;
       }
     }
   }
 drain:
-  // wait (bounded) for this thread's own copies still in flight
-  if (!SPARSE) {
+  // wait (bounded) for this warp's own copies still in flight: the latest
+  // armed phase of every full barrier (earlier phases of a barrier completed
+  // before it was re-armed)
+  if (lane == 0) {
+    if (!SPARSE) {
 #pragma unroll 1
-    for (int k = 0; k < C::kNumFull; ++k)
-      if (armed[k] > 0) mbar_wait_drain(bars.full + k, (armed[k] - 1) & 1, wd.limit_ns);
+      for (int k = 0; k < C::kNumFull; ++k)
+        if ((armed >> k) & 1u) mbar_wait_drain(bars.full + k, ((next_par >> k) & 1u) ^ 1u, wd.limit_ns);
+    }
+    if (q_armed > 0) mbar_wait_drain(bars.q_full, (q_armed - 1) & 1, wd.limit_ns);
   }
-  if (q_armed > 0) mbar_wait_drain(bars.q_full, (q_armed - 1) & 1, wd.limit_ns);
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
-// MMA issuer (one thread)
+// MMA issuers: warp 1 issues S^T, warp 3 issues PV
 // ---------------------------------------------------------------------------
+// Two warps feed the tensor pipe: one issues S^T(jt) as soon as tile jt is in
+// shared memory, the other issues PV(jt) as soon as P(jt) is ready, so
+// neither waits for the other's operands and the pipe receives both streams.
+// Their MMAs write disjoint TMEM columns (S^T buffers, O^T).  Each warp runs
+// converged and issues every MMA and commit from one elected lane (a lane
+// issuing alone while its warp waits elsewhere feeds the pipe at well under
+// half the rate).  Shared-memory addresses are 32-bit values in registers,
+// ring positions advance by counters, descriptors are built once per pair
+// slot and advanced by additions, and barrier tests are warp-uniform.
+
+// Ring position of one tile: slot and use count of its first pair item and
+// of its RoPE item.
+template <class C>
+struct RingPos {
+  int pbase, puse, rslot, ruse;
+  __device__ void advance() {
+    pbase += 4;
+    if (pbase >= C::kNA) {
+      pbase -= C::kNA;
+      ++puse;
+    }
+    if (++rslot == C::kNB) {
+      rslot = 0;
+      ++ruse;
+    }
+  }
+  __device__ int pair_slot(int b) const { return pbase + b >= C::kNA ? pbase + b - C::kNA : pbase + b; }
+};
+
+// Warp-uniform barrier test (lane 0's result).
+__device__ __forceinline__ bool warp_test_u32(uint32_t bar, uint32_t parity) {
+  return __shfl_sync(0xffffffffu, mbar_test_wait_u32(bar, parity) ? 1 : 0, 0) != 0;
+}
+
+// Warp-uniform bounded wait.
+__device__ __forceinline__ bool mbar_wait_u32(uint32_t bar, uint32_t parity, const Watchdog& wd) {
+  uint64_t t0 = 0;
+  while (!warp_test_u32(bar, parity)) {
+    if (t0 == 0) {
+      t0 = global_timer_ns();
+    } else if (__shfl_sync(0xffffffffu, wd.aborted() ? 1 : 0, 0)) {
+      return false;
+    } else if (__shfl_sync(0xffffffffu, global_timer_ns() - t0 > wd.limit_ns ? 1 : 0, 0)) {
+      if ((threadIdx.x & 31) == 0) wd.trip(MLA_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Commit from this warp's elected lane: arrive on `bar` when the MMAs this
+// warp issued so far are done; then the drain of the CTA's end.
+__device__ __forceinline__ void warp_commit(uint32_t bar) {
+  if (elect_one()) umma_commit_u32(bar);
+  __syncwarp();
+}
+
 template <int R, bool SPARSE>
-__device__ void mma_issuer(const Segments& sg, uint32_t tmem, uint8_t* kv, uint8_t* qs, const Bars& bars,
-                           const Watchdog& wd) {
+__device__ void s_issuer(const Segments& sg, uint32_t tmem, uint8_t* kv, uint8_t* qs, const Bars& bars,
+                         const Watchdog& wd) {
   using C = Cfg<R, SPARSE>;
-  using RG = Ring<C>;
-  constexpr uint32_t kIdS = idesc_bf16_f32(128, R, 0, 0);  // A = K tile (K-major), B = Q (K-major)
+  constexpr uint32_t kIdS = idesc_bf16_f32(kTileTokens, R, 0, 0);  // A = K tile (K-major), B = Q (K-major)
+  constexpr uint64_t kHiK = smem_desc_hi(16, 1024);
+  const int lane = threadIdx.x & 31;
+  const uint32_t kvb = smem_u32(kv), qb = smem_u32(qs);
+  const uint32_t full = smem_u32(bars.full), s_full = smem_u32(bars.s_full), s_empty = smem_u32(bars.s_empty);
+  const uint32_t rope_empty = smem_u32(bars.rope_empty);
+  const uint32_t q_full = smem_u32(bars.q_full), q_empty = smem_u32(bars.q_empty);
+  RingPos<C> cur{0, 0, 0, 0};
+  int jt = 0, seg = 0;
+  int fidx = 0, fphase = 0;  // full barrier of the next tile (jt % 3) and its phase (jt / 3)
+  for (int prob = sg.p0; prob <= sg.last(); ++prob) {
+    int tb, te;
+    sg.range(prob, tb, te);
+    if (tb >= te) continue;
+    if (!mbar_wait_u32(q_full, seg & 1, wd)) goto done;
+    tc_fence_after();
+    for (int j = tb; j < te; ++j, ++jt) {
+      const int sb = jt & 1;
+      // the softmax has read S^T of tile jt-2 from this buffer
+      if (jt >= 2 && !mbar_wait_u32(s_empty + 8 * sb, ((jt >> 1) - 1) & 1, wd)) goto done;
+      tc_fence_after();
+      if (!mbar_wait_u32(full + 8 * fidx, static_cast<uint32_t>(fphase) & 1u, wd)) goto done;
+      if (++fidx == 3) {
+        fidx = 0;
+        ++fphase;
+      }
+      if (lane == 0) MLA_TR(kTrMmaKv0, jt);
+      const uint32_t d_s = tmem + C::kSCol + sb * R;
+      // S^T = K Q^T over the nine chunks, 36 MMAs back to back (pairs of
+      // chunks sit together in a pair slot)
+#pragma unroll 1
+      for (int pb = 0; pb < 5; ++pb) {
+        const uint32_t pa = pb < 4 ? kvb + C::kPairOff + cur.pair_slot(pb) * C::kPairBytes
+                                   : kvb + C::kRopeOff + cur.rslot * C::kKvChunkBytes;
+        const uint64_t a0 = kHiK | (pa >> 4);
+        const uint64_t b0 = kHiK | ((qb + 2 * pb * C::kQChunkBytes) >> 4);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (pb == 4 && i >= 4) break;
+          const int h = i >> 2, kk = i & 3;  // chunk 2pb+h, k step kk
+          if (elect_one())
+            umma_bf16_ss_fast(d_s, a0 + h * (C::kKvChunkBytes >> 4) + 2 * kk,
+                              b0 + h * (C::kQChunkBytes >> 4) + 2 * kk, kIdS, (pb | i) != 0);
+          __syncwarp();
+        }
+      }
+      if (elect_one()) {
+        umma_commit_u32(s_full + 8 * sb);
+        // with a separate P buffer the RoPE chunk is free once S^T is done
+        if (!C::kPAlias) umma_commit_u32(rope_empty + 8 * cur.rslot);
+        if (j == te - 1) umma_commit_u32(q_empty);
+      }
+      __syncwarp();
+      if (lane == 0) MLA_TR(kTrMmaSDone, jt);
+      cur.advance();
+    }
+    ++seg;
+  }
+done:
+  warp_commit(smem_u32(bars.mma_done));
+  if (lane == 0) mbar_wait_drain(bars.mma_done, 0, wd.limit_ns);
+  __syncwarp();
+}
+
+template <int R, bool SPARSE>
+__device__ void pv_issuer(const Segments& sg, uint32_t tmem, uint8_t* kv, const Bars& bars, const Watchdog& wd) {
+  using C = Cfg<R, SPARSE>;
   constexpr uint32_t kIdO = idesc_bf16_f32(128, R, 1, C::kPMnMajor ? 1 : 0);  // A = V^T (MN-major), B = P
-  const uint32_t kv_base = smem_u32(kv);
-  const uint32_t q_base = smem_u32(qs);
-  const uint32_t p_base = kv_base + C::kPOff;
+  constexpr uint64_t kHiV = smem_desc_hi(C::kKvChunkBytes, 1024);
+  constexpr uint64_t kHiP = smem_desc_hi(16, 1024);
+  constexpr uint32_t kPStep = C::kPMnMajor ? (2048 >> 4) : (32 >> 4);  // 16 tokens of P
+  const int lane = threadIdx.x & 31;
+  const uint32_t kvb = smem_u32(kv);
+  const uint32_t p_full = smem_u32(bars.p_full), o_empty = smem_u32(bars.o_empty), o_done = smem_u32(bars.o_done);
+  const uint32_t o_full = smem_u32(bars.o_full), pair_empty = smem_u32(bars.pair_empty);
+  const uint32_t rope_empty = smem_u32(bars.rope_empty);
+  RingPos<C> cur{0, 0, 0, 0};
   int jt = 0, seg = 0;
   for (int prob = sg.p0; prob <= sg.last(); ++prob) {
     int tb, te;
     sg.range(prob, tb, te);
     if (tb >= te) continue;
-    if (!mbar_wait(bars.q_full, seg & 1, wd)) goto done;
-    tc_fence_after();
     for (int j = tb; j < te; ++j, ++jt) {
-      const int sb = jt & 1;
-      if (jt >= 2 && !mbar_wait(bars.s_empty + sb, ((jt >> 1) - 1) & 1, wd)) goto done;
+      const bool first = (j == tb), last = (j == te - 1);
+      if (!mbar_wait_u32(p_full + 8 * (jt & 1), (jt >> 1) & 1, wd)) goto done;
       tc_fence_after();
-      const uint32_t d_s = tmem + C::kSCol + sb * R;
-#pragma unroll 1
-      for (int c = 0; c < kNumChunks; ++c) {
-        if (!mbar_wait(bars.full + RG::full_index(jt, c), RG::full_use(jt, c) & 1, wd)) goto done;
+      if (lane == 0) MLA_TR(kTrMmaPFull, jt);
+      if (first && seg > 0) {
+        // the epilogue of the previous segment has read O^T
+        if (!mbar_wait_u32(o_empty, (seg - 1) & 1, wd)) goto done;
         tc_fence_after();
-        if (c == 0) MLA_TR(kTrMmaKv0, jt);
-        if (c == 8) MLA_TR(kTrMmaKv8, jt);
-        const uint32_t chunk = kv_base + RG::chunk_off(jt, c);
+      }
+      const uint32_t p_addr = C::kPAlias ? kvb + C::kRopeOff + cur.rslot * C::kKvChunkBytes
+                                         : kvb + C::kPOff + (jt & 1) * C::kPBytes;
+      const uint64_t b0 = kHiP | (p_addr >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t a = smem_desc(chunk + kk * 32, 16, 1024);
-          const uint64_t b = smem_desc(q_base + c * C::kQChunkBytes + kk * 32, 16, 1024);
-          umma_bf16_ss(d_s, a, b, kIdS, (c | kk) != 0);
-        }
-      }
-      umma_commit(bars.s_full + sb);
-      // with a separate P buffer the RoPE chunk is free once S^T is done
-      if (C::kRing) umma_commit(bars.rope_empty + RG::rope_slot(jt));
-      MLA_TR(kTrMmaSDone, jt);
-      if (j == te - 1) umma_commit(bars.q_empty);
-      if (!mbar_wait(bars.p_full, jt & 1, wd)) goto done;
-      tc_fence_after();
-      MLA_TR(kTrMmaPFull, jt);
-      if (j == tb && seg > 0) {
-        if (!mbar_wait(bars.o_empty, (seg - 1) & 1, wd)) goto done;
-        tc_fence_after();
-      }
-#pragma unroll 1
       for (int blk = 0; blk < 4; ++blk) {
-        const uint32_t pair = kv_base + C::kPairOff + RG::pair_slot(jt, blk) * C::kPairBytes;
+        const int s = cur.pair_slot(blk);
+        const uint64_t a0 = kHiV | ((kvb + C::kPairOff + s * C::kPairBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = smem_desc(pair + kk * 2048, C::kKvChunkBytes, 1024);
-          const uint64_t b = C::kPMnMajor ? smem_desc(p_base + kk * 2048, 16, 1024)
-                                          : smem_desc(p_base + (kk >> 2) * C::kPHalfBytes + (kk & 3) * 32, 16, 1024);
-          umma_bf16_ss(tmem + C::kOCol + blk * R, a, b, kIdO, !(j == tb && kk == 0));
+        for (int kk = 0; kk < kTileTokens / 16; ++kk) {
+          if (elect_one())
+            umma_bf16_ss_fast(tmem + C::kOCol + blk * R, a0 + kk * (2048 >> 4), b0 + kk * kPStep, kIdO,
+                              !(first && kk == 0));
+          __syncwarp();
         }
-        umma_commit(bars.pair_empty + RG::pair_slot(jt, blk));
-        if (blk == 0) MLA_TR(kTrMmaO1, jt);
+        warp_commit(pair_empty + 8 * s);
+        if (blk == 0 && lane == 0) MLA_TR(kTrMmaO1, jt);
       }
-      if (!C::kRing) umma_commit(bars.rope_empty + RG::rope_slot(jt));  // P lived in the RoPE slot
-      MLA_TR(kTrMmaODone, jt);
-      if (j == te - 1) umma_commit(bars.o_full);
+      if (elect_one()) {
+        if (C::kPAlias) umma_commit_u32(rope_empty + 8 * cur.rslot);  // P lived in the RoPE slot
+        umma_commit_u32(o_done + 8 * (jt & 1));
+        if (last) umma_commit_u32(o_full);
+      }
+      __syncwarp();
+      if (lane == 0) MLA_TR(kTrMmaODone, jt);
+      cur.advance();
     }
     ++seg;
   }
 done:
-  umma_commit(bars.mma_done);
-  mbar_wait_drain(bars.mma_done, 0, wd.limit_ns);
+  warp_commit(smem_u32(bars.mma_done));
+  if (lane == 0) mbar_wait_drain(bars.mma_done, 0, wd.limit_ns);
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
-// FP8 gather + dequantisation (sparse, 128 threads; thread t -> token t)
+// FP8 gather + dequantisation (sparse, 128 threads, two per token)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t dequant2(uint32_t codes16, float scale) {
   const uint32_t h2 = e4m3x2_to_f16x2(static_cast<uint16_t>(codes16));
@@ -378,11 +534,14 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
                            const Bars& bars, volatile uint8_t* flags, const Watchdog& wd) {
   using C = Cfg<R, true>;
   using RG = Ring<C>;
-  static_assert(!C::kRing, "the sparse path stages one tile (4 pair slots + 1 RoPE slot)");
-  const int tid = threadIdx.x - 32 * C::kGatherWarp0;  // token of the tile
+  // 128 threads, two per token: half h = 0 (warps 0, 1) converts value blocks
+  // 0 and 1 and the RoPE dims, half 1 (warps 2, 3) value blocks 2 and 3.
+  const int tid = threadIdx.x - 32 * C::kGatherWarp0;
   const int lane = tid & 31;
-  const int wbase = tid & ~31;                          // first token of this warp
-  const uint32_t tsw = tid & 7;
+  const int h = tid >> 6;
+  const int tok = tid & 63;           // token of the tile
+  const int wtok = tok & ~31;         // first token of this warp
+  const uint32_t tsw = tok & 7;
   const uint32_t kv_base = smem_u32(kv);
   const uint64_t pol = l2_policy_evict_normal();
   int armed[5] = {0, 0, 0, 0, 0};  // phases of raw_full armed by this warp (drained on exit)
@@ -395,12 +554,12 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
     const int L = sg.seqlens[b];
     const int32_t* idx_row = p.indices + static_cast<int64_t>(prob) * p.topk;
     const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
-    int t_next = (tb * kTileTokens + tid < p.topk) ? idx_row[tb * kTileTokens + tid] : -1;
+    int t_next = (tb * kTileTokens + tok < p.topk) ? idx_row[tb * kTileTokens + tok] : -1;
     for (int j = tb; j < te; ++j, ++jt) {
       if (tid == 0) MLA_TR(kTrGatherStart, jt);
       const int t = t_next;
       {
-        const int kn = (j + 1) * kTileTokens + tid;
+        const int kn = (j + 1) * kTileTokens + tok;
         t_next = (j + 1 < te && kn < p.topk) ? idx_row[kn] : -1;
       }
       // token -> cache row (page * 64 + slot); invalid tokens read row 0 and
@@ -410,26 +569,29 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
       int page = in_table ? bt[t >> 6] : -1;
       if (ok && (page < 0 || page >= p.num_pages)) {
         ok = false;
-        atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
+        if (h == 0) atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
       }
       const int row = ok ? page * kPageSize + (t & 63) : 0;
-      const uint4 sc = ok ? ld_global_nc_v4(p.kv_fp8 + static_cast<int64_t>(row) * kFp8RowBytes + 512)
-                          : make_uint4(0, 0, 0, 0);
+      // this half's two scales (value blocks 2h, 2h+1)
+      const uint2 sc = ok ? __ldg(reinterpret_cast<const uint2*>(p.kv_fp8 + static_cast<int64_t>(row) * kFp8RowBytes +
+                                                             kFp8ScaleOffset + 8 * h))
+                          : make_uint2(0, 0);
       // rows of this lane's group of four tokens (lanes 0..7 issue the gathers)
-      const int g4 = wbase + 4 * (lane & 7);
+      const int g4 = wtok + 4 * (lane & 7);
       const int r0 = __shfl_sync(0xffffffffu, row, (4 * lane) & 31);
       const int r1 = __shfl_sync(0xffffffffu, row, (4 * lane + 1) & 31);
       const int r2 = __shfl_sync(0xffffffffu, row, (4 * lane + 2) & 31);
       const int r3 = __shfl_sync(0xffffffffu, row, (4 * lane + 3) & 31);
 
       // issue: the codes of value block b (dims 128b..128b+127) into the upper
-      // half of pair slot b once its previous tile's PV is done; then the RoPE
-      // bytes into the RoPE slot
+      // chunk of pair slot b once its previous tile's PV is done; half 0 then
+      // the RoPE bytes into the RoPE slot
 #pragma unroll 1
-      for (int blk = 0; blk < 4; ++blk) {
+      for (int i = 0; i < 2; ++i) {
+        const int blk = 2 * h + i;
         const uint32_t use = RG::pair_use(jt, blk);
         if (use > 0 && !warp_wait(bars.pair_empty + RG::pair_slot(jt, blk), (use - 1) & 1, wd)) goto drain;
-        if (blk == 0) flags[(jt & 1) * 128 + tid] = ok ? 1 : 0;  // token validity for the softmax
+        if (blk == 0) flags[(jt & 1) * 128 + tok] = ok ? 1 : 0;  // token validity for the softmax
         if (lane == 0) mbar_arrive_expect_tx(bars.raw_full + blk, 32 * 128);
         ++armed[blk];
         __syncwarp();
@@ -438,7 +600,7 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
           tma_gather4(dst, tm_rows, bars.raw_full + blk, 128 * blk, r0, r1, r2, r3, pol);
         }
       }
-      {
+      if (h == 0) {
         const uint32_t use = RG::rope_use(jt);
         if (use > 0 && !warp_wait(bars.rope_empty + RG::rope_slot(jt), (use - 1) & 1, wd)) goto drain;
         if (lane == 0) mbar_arrive_expect_tx(bars.raw_full + 4, 32 * 128);
@@ -446,59 +608,56 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
         __syncwarp();
         if (lane < 8) {
           uint8_t* dst = kv + RG::chunk_off(jt, 8) + g4 * 128;
-          tma_gather4(dst, tm_rows, bars.raw_full + 4, 528, r0, r1, r2, r3, pol);
+          tma_gather4(dst, tm_rows, bars.raw_full + 4, kFp8RopeOffset, r0, r1, r2, r3, pol);
         }
       }
 
-      // dequantise in place: token tid's 128 code bytes of block b sit at row
-      // tid of chunk 2b+1; they become row tid of chunks 2b and 2b+1 (bf16,
+      // dequantise in place: token tok's 128 code bytes of block b sit at row
+      // tok of chunk 2b+1; they become row tok of chunks 2b and 2b+1 (bf16,
       // 128-byte swizzle).  Units are read in a per-thread rotated order.
 #pragma unroll 1
-      for (int blk = 0; blk < 4; ++blk) {
-        if (!warp_wait(bars.raw_full + blk, jt & 1, wd)) goto drain;
-        const float scale = __uint_as_float(blk == 0 ? sc.x : (blk == 1 ? sc.y : (blk == 2 ? sc.z : sc.w)));
-        const uint32_t lo = kv_base + RG::chunk_off(jt, 2 * blk) + tid * 128;
-        const uint32_t hi = kv_base + RG::chunk_off(jt, 2 * blk + 1) + tid * 128;
+      for (int i = 0; i < 2; ++i) {
+        const int blk = 2 * h + i;
+        if (!warp_wait(bars.raw_full + blk, armed[blk] == 0 ? 0 : (armed[blk] - 1) & 1, wd)) goto drain;
+        const float scale = __uint_as_float(i == 0 ? sc.x : sc.y);
+        const uint32_t lo = kv_base + RG::chunk_off(jt, 2 * blk) + tok * 128;
+        const uint32_t hi = kv_base + RG::chunk_off(jt, 2 * blk + 1) + tok * 128;
         uint4 raw[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) raw[i] = ld_shared_v4(hi + ((i ^ tsw) << 4));
+        for (int k = 0; k < 8; ++k) raw[k] = ld_shared_v4(hi + ((k ^ tsw) << 4));
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t u = i ^ tsw;  // raw unit: codes 16u..16u+15 of the block
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t u = k ^ tsw;  // raw unit: codes 16u..16u+15 of the block
           const uint32_t dst = ((u & 4) ? hi : lo);
           const uint32_t k0 = (2 * (u & 3)) ^ tsw, k1 = (2 * (u & 3) + 1) ^ tsw;
-          uint4 v = raw[i];
+          uint4 v = raw[k];
           if (!ok) v = make_uint4(0, 0, 0, 0);
           st_shared_v4(dst + (k0 << 4), dequant2(v.x & 0xffffu, scale), dequant2(v.x >> 16, scale),
                        dequant2(v.y & 0xffffu, scale), dequant2(v.y >> 16, scale));
           st_shared_v4(dst + (k1 << 4), dequant2(v.z & 0xffffu, scale), dequant2(v.z >> 16, scale),
                        dequant2(v.w & 0xffffu, scale), dequant2(v.w >> 16, scale));
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bars.full + RG::full_index(jt, 2 * blk));
-          mbar_arrive(bars.full + RG::full_index(jt, 2 * blk + 1));
-        }
       }
-      {
+      if (h == 0) {
         // RoPE: already bf16; permute the 16-byte units into the swizzled order
-        if (!warp_wait(bars.raw_full + 4, jt & 1, wd)) goto drain;
-        const uint32_t base = kv_base + RG::chunk_off(jt, 8) + tid * 128;
+        if (!warp_wait(bars.raw_full + 4, (armed[4] - 1) & 1, wd)) goto drain;
+        const uint32_t base = kv_base + RG::chunk_off(jt, 8) + tok * 128;
         uint4 raw[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) raw[i] = ld_shared_v4(base + ((i ^ tsw) << 4));
-        // raw[i] holds unit i ^ tsw, whose swizzled position is (i ^ tsw) ^ tsw = i
+        for (int k = 0; k < 8; ++k) raw[k] = ld_shared_v4(base + ((k ^ tsw) << 4));
+        // raw[k] holds unit k ^ tsw, whose swizzled position is (k ^ tsw) ^ tsw = k
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = ok ? raw[i] : make_uint4(0, 0, 0, 0);
-          st_shared_v4(base + (i << 4), v.x, v.y, v.z, v.w);
+        for (int k = 0; k < 8; ++k) {
+          const uint4 v = ok ? raw[k] : make_uint4(0, 0, 0, 0);
+          st_shared_v4(base + (k << 4), v.x, v.y, v.z, v.w);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.full + RG::full_index(jt, 8));
-        if (tid == 0) MLA_TR(kTrGatherDone, jt);
       }
+      // this warp's part of the tile is written: one arrival on the tile's
+      // full barrier (after the proxy fence that orders it for the MMAs)
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.full + RG::full_index(jt));
+      if (tid == 0) MLA_TR(kTrGatherDone, jt);
     }
   }
   return;
@@ -573,9 +732,13 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
   constexpr int RW = R / C::kSmWG;  // rows owned by this warpgroup
   const int wg = (threadIdx.x - 128) >> 7;
   const int rb = wg * RW;           // first row of this warpgroup
-  const int tid = (threadIdx.x - 128) & 127;  // token of the tile = TMEM lane
+  const int tid = (threadIdx.x - 128) & 127;  // TMEM lane (O^T: dv row of a block)
   const int warp_q = (threadIdx.x >> 5) & 3;
   const int lane = threadIdx.x & 31;
+  // S^T of a 64-token tile (M = 64) occupies lanes 0..15 of each warp's
+  // quarter of TMEM: lane l < 16 of warp q holds token 16q + l
+  const bool active = lane < 16;
+  const int tl = 16 * warp_q + (lane & 15);  // token of the tile (active lanes)
   const uint32_t lane_base = static_cast<uint32_t>(warp_q * 32) << 16;
   const uint32_t bar_id = kSoftmaxBar + wg;
   float* m_s = aux;            // running row max (log2 units)
@@ -585,9 +748,9 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
   float* red = aux + 4 * R;    // [4][R] cross-warp reduction
   // last visible key per row (causal), after the 16 ints and the 256 flag bytes
   int* lim_s = reinterpret_cast<int*>(aux + 8 * R) + 16 + 64;
-  const uint32_t p_base = smem_u32(kv) + C::kPOff;
-  const uint32_t p_row_off = (tid >> 6) * C::kPHalfBytes + (tid & 7) * 2;
-  const uint32_t p_chunk = (tid & 63) >> 3;
+  const uint32_t kv_base = smem_u32(kv);
+  const uint32_t p_row_off = (tl & 7) * 2;  // K-major P: byte of this token inside its 16-byte unit
+  const uint32_t p_chunk = tl >> 3;         // K-major P: 16-byte unit of this token
   // The 128 threads of a softmax warpgroup synchronise on their own hardware
   // named barrier.  Every bounded mbarrier wait is followed by a barrier AND
   // of its result, so on a timeout all four warps leave together and none is
@@ -631,17 +794,17 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
     for (int j = tb; j < te; ++j, ++jt) {
       const int sb = jt & 1;
       if (tracer) MLA_TR(kTrSmWaitS, jt);
-      // S^T of this tile is complete; the wait on the tile's chunk-7 barrier
+      // S^T of this tile is complete; the wait on the tile's full barrier
       // (already complete) orders the loader's validity flags before our reads
       {
         bool ok = mbar_wait(bars.s_full + sb, (jt >> 1) & 1, wd);
-        ok = ok && mbar_wait(bars.full + Ring<C>::full_index(jt, 7), Ring<C>::full_use(jt, 7) & 1, wd);
+        ok = ok && mbar_wait(bars.full + Ring<C>::full_index(jt), Ring<C>::full_parity(jt), wd);
         if (!group_ok(ok)) return;
       }
       tc_fence_after();
-      const int pos = j * kTileTokens + tid;  // dense: logical token of this thread
-      const bool tok_ok = SPARSE ? flags[(jt & 1) * 128 + tid] != 0
-                                 : (pos < L && flags[(jt & 1) * 128 + (tid >> 6)] != 0);
+      const int pos = j * kTileTokens + tl;  // dense: logical token of this thread
+      const bool tok_ok = active && (SPARSE ? flags[(jt & 1) * 128 + tl] != 0
+                                            : (pos < L && flags[(jt & 1) * 128] != 0));
       if (tracer) MLA_TR(kTrSmSFull, jt);
 
       // this thread's token, this warpgroup's rows of S^T: all loads in flight, one wait
@@ -655,7 +818,7 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
       tc_fence_before();
       warp_arrive(bars.s_empty + sb);  // S is in registers; the buffer can be rewritten
       if (tracer) MLA_TR(kTrSmLoaded, jt);
-      if (wg == 0 && lane == 0 && warp_q > 0) MLA_TR(kTrW1Loaded + warp_q - 1, jt);
+      if (wg == 0 && lane == 0 && warp_q == 1) MLA_TR(kTrW1Loaded, jt);
 
       // logits in log2 units; masked -> -inf.  Rows differ only where a causal
       // limit falls inside the tile: their limits come from shared memory.
@@ -689,7 +852,7 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
           loc = fmaxf(loc, fmaxf(fmaxf(x[4 * r4] - m4.x, x[4 * r4 + 1] - m4.y),
                                  fmaxf(x[4 * r4 + 2] - m4.z, x[4 * r4 + 3] - m4.w)));
         }
-        if (wg == 0 && lane == 0) MLA_TR(kTrW0PreVote + warp_q, jt);
+        if (wg == 0 && lane == 0 && warp_q > 0) MLA_TR(kTrW0PreVote + warp_q, jt);
         need = named_bar_or(bar_id, 128, loc > kRescaleThreshold);
         if (tracer) MLA_TR(kTrSmVote, jt);
       }
@@ -708,8 +871,11 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
 #pragma unroll
         for (int r = 0; r < RW; ++r) l[r] *= alpha_s[rb + r];
         if (j != tb) {
-          // O^T of the previous tiles is complete (its MMAs precede this tile's S^T);
-          // rescale this warpgroup's row columns by alpha.
+          // rescale this warpgroup's row columns of O^T by alpha once the PV
+          // MMAs of the previous tile are done (those of earlier tiles are:
+          // this tile's loads reused slots they released)
+          if (!group_ok(mbar_wait(bars.o_done + ((jt - 1) & 1), ((jt - 1) >> 1) & 1, wd))) return;
+          tc_fence_after();
 #pragma unroll 1
           for (int blk = 0; blk < 4; ++blk) {
 #pragma unroll
@@ -727,7 +893,13 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
         }
       }
 
-      // probabilities -> P (bf16) and row sums
+      // probabilities -> P (bf16) and row sums.  A separate P buffer was last
+      // read by the PV of tile jt-2: wait for it (P in the RoPE slot needs no
+      // wait: this tile's RoPE chunk was loaded there after that PV).
+      if (!C::kPAlias && jt >= 2) {
+        if (!group_ok(mbar_wait(bars.o_done + (jt & 1), ((jt - 2) >> 1) & 1, wd))) return;
+      }
+      const uint32_t p_base = kv_base + Ring<C>::p_off(jt);
 #pragma unroll
       for (int r8 = 0; r8 < RW / 8; ++r8) {
         const float4 ma = reinterpret_cast<const float4*>(m_s + rb)[2 * r8];
@@ -740,13 +912,14 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
           pr[e] = (x[r] == kNegInf) ? 0.f : fast_exp2(x[r] - mr[e]);
           l[r] += pr[e];
         }
+        if (!active) continue;
         if (C::kPMnMajor) {
           // P^T as [token][R rows] (MN-major B operand): one 16-byte chunk per 8 rows
           const uint32_t ch = (rb >> 3) + r8;
-          st_shared_v4(p_base + tid * 128 + ((ch ^ (tid & 7)) << 4), pack_bf16x2(pr[0], pr[1]),
+          st_shared_v4(p_base + tl * 128 + ((ch ^ (tl & 7)) << 4), pack_bf16x2(pr[0], pr[1]),
                        pack_bf16x2(pr[2], pr[3]), pack_bf16x2(pr[4], pr[5]), pack_bf16x2(pr[6], pr[7]));
         } else {
-          // P as [2][R rows][64 tokens] (K-major B operand)
+          // P as [R rows][64 tokens] (K-major B operand)
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int r = rb + 8 * r8 + e;
@@ -755,12 +928,12 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
           }
         }
       }
-      if (!SPARSE && !tok_ok) {
+      if (!SPARSE && active && !tok_ok) {
         // a masked token's V row must be finite (0 * NaN would poison O): zero
         // it (the warpgroups split the eight value chunks)
 #pragma unroll 1
         for (int c = wg; c < 8; c += C::kSmWG) {
-          const uint32_t base = smem_u32(kv) + Ring<C>::chunk_off(jt, c) + tid * 128;
+          const uint32_t base = kv_base + Ring<C>::chunk_off(jt, c) + tl * 128;
 #pragma unroll
           for (int q = 0; q < 8; ++q) st_shared_v4(base + 16 * q, 0u, 0u, 0u, 0u);
         }
@@ -768,8 +941,9 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
       if (tracer) MLA_TR(kTrSmPStored, jt);
       fence_proxy_async_smem();
       tc_fence_before();
-      warp_arrive(bars.p_full);
+      warp_arrive(bars.p_full + (jt & 1));
       if (tracer) MLA_TR(kTrSmPFull, jt);
+      if (wg == C::kSmWG - 1 && tid == 96) MLA_TR(kTrW0PreVote, jt);  // last warp's arrival
     }
 
     // ---- epilogue: O / l -> out (single piece) or fp32 partial (split problem)
@@ -861,10 +1035,11 @@ __global__ void __launch_bounds__(Cfg<R, SPARSE>::kThreads, 1)
   bars.s_full = bars.rope_empty + C::kNB;
   bars.s_empty = bars.s_full + 2;
   bars.p_full = bars.s_empty + 2;
-  bars.o_full = bars.p_full + 1;
+  bars.o_full = bars.p_full + 2;
   bars.o_empty = bars.o_full + 1;
   bars.mma_done = bars.o_empty + 1;
-  bars.raw_full = bars.mma_done + 1;
+  bars.o_done = bars.mma_done + 1;
+  bars.raw_full = bars.o_done + 2;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -874,18 +1049,20 @@ __global__ void __launch_bounds__(Cfg<R, SPARSE>::kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bars.q_full, 1);
     mbar_init(bars.q_empty, 1);
-    for (int k = 0; k < C::kNumFull; ++k) mbar_init(bars.full + k, SPARSE ? 4 : 1);  // sparse: one per gather warp
+    for (int k = 0; k < C::kNumFull; ++k) mbar_init(bars.full + k, C::kFullArrivals);
     for (int k = 0; k < C::kNA; ++k) mbar_init(bars.pair_empty + k, 1);
     for (int k = 0; k < C::kNB; ++k) mbar_init(bars.rope_empty + k, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars.s_full + i, 1);
       mbar_init(bars.s_empty + i, 4 * C::kSmWG);  // one arrival per softmax warp
+      mbar_init(bars.p_full + i, 4 * C::kSmWG);
     }
-    mbar_init(bars.p_full, 4 * C::kSmWG);
+    mbar_init(bars.o_done, 1);
+    mbar_init(bars.o_done + 1, 1);
     mbar_init(bars.o_full, 1);
     mbar_init(bars.o_empty, 4 * C::kSmWG);
-    mbar_init(bars.mma_done, 1);
-    for (int k = 0; k < C::kNumRaw; ++k) mbar_init(bars.raw_full + k, 4);  // one arrive_expect_tx per gather warp
+    mbar_init(bars.mma_done, 2);  // one commit per MMA-issuing warp
+    for (int k = 0; k < C::kNumRaw; ++k) mbar_init(bars.raw_full + k, 2);  // one arrive_expect_tx per issuing warp
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -923,9 +1100,11 @@ __global__ void __launch_bounds__(Cfg<R, SPARSE>::kThreads, 1)
   if (warp < 4) {
     if (C::kRegSplit) regs_dec<C::kRegsCtl>();
     if (warp == 0) {
-      if (lane == 0) producer<R, SPARSE>(&tm_q, &tm_kv, p, sg, g, kv, qs, bars, flags, wd);
+      producer<R, SPARSE>(&tm_q, &tm_kv, p, sg, g, kv, qs, bars, flags, wd);  // the whole warp, converged
     } else if (warp == 1) {
-      if (lane == 0) mma_issuer<R, SPARSE>(sg, tmem, kv, qs, bars, wd);
+      s_issuer<R, SPARSE>(sg, tmem, kv, qs, bars, wd);  // the whole warp, converged
+    } else if (warp == 3) {
+      pv_issuer<R, SPARSE>(sg, tmem, kv, bars, wd);
     }
   } else if (warp < C::kGatherWarp0) {
     if (C::kRegSplit) regs_inc<C::kRegsSoftmax>();

@@ -18,7 +18,7 @@ constexpr int kDv = 512;           // value dims = first 512 key dims
 constexpr int kChunk = 64;         // dims per 128-byte swizzle atom row (bf16)
 constexpr int kNumChunks = 9;      // 576 / 64
 constexpr int kPageSize = 64;      // tokens per page
-constexpr int kTileTokens = 128;   // tokens per KV tile = MMA M of S^T = K Q^T
+constexpr int kTileTokens = 64;    // tokens per KV tile (one page) = MMA M of S^T = K Q^T
 constexpr int kFp8RowBytes = 656;  // 512 e4m3 + 4 fp32 scales + 64 bf16
 constexpr int kFp8ScaleOffset = 512;
 constexpr int kFp8RopeOffset = 528;
@@ -34,7 +34,7 @@ enum SchedField { kSchedP0 = 0, kSchedT0 = 1, kSchedP1 = 2, kSchedT1 = 3, kSched
 
 constexpr int kMaxProblems = 16384;    // metadata kernel keeps per-problem prefix sums in smem
 
-// Number of 128-token tiles of problem p: dense covers the cached tokens
+// Number of 64-token tiles of problem p: dense covers the cached tokens
 // [0, seqlen), sparse covers the topk index slots of the query token.
 __host__ __device__ inline int problem_tiles(const int32_t* cache_seqlens, int p, int s_q, int topk) {
   if (topk > 0) return (topk + kTileTokens - 1) / kTileTokens;

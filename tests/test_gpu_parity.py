@@ -85,7 +85,7 @@ def test_rescale_path_increasing_logits():
     """Logits that grow along the sequence force an O rescale on every tile.
 
     Key j is pushed along head 0's query direction by 0.15*j*24/|q|, so head 0's logit grows by
-    about 19 (28 in log2 units, above the threshold of 8) per 128-token tile and ends near 165:
+    about 9.6 (13.9 in log2 units, above the threshold of 8) per 64-token tile and ends near 165:
     large enough to exercise the rescale, small enough for fp32 accumulation to meet the
     absolute lse bound."""
     w = W.custom(name="ramp", batch=1, h_q=32, s_q=1, mode="dense", seqlens=(1100,))
@@ -168,7 +168,7 @@ def test_schedule_covers_every_tile_once(topk, lens):
     sched = sched.view(-1, 8).cpu().numpy()
     ns = ns.cpu().numpy()
     np_ = len(lens) * (s_q if topk else 1)
-    tiles = [math.ceil(topk / 128) if topk else math.ceil(L / 128) for L in
+    tiles = [math.ceil(topk / 64) if topk else math.ceil(L / 64) for L in
              ([lens[p // s_q] for p in range(np_)] if topk else lens)]
     seen = {}
     count = np.zeros(np_, int)

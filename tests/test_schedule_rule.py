@@ -88,7 +88,7 @@ def test_every_tile_once_and_split_bookkeeping(seed):
 def test_balance_on_a_ragged_mix():
     rng = np.random.default_rng(1002)
     lens = rng.integers(1024, 8193, size=128)
-    tiles = [int((L + 127) // 128) for L in lens]
+    tiles = [int((L + 63) // 64) for L in lens]
     parts = 152
     starts, counts, _ = schedule(tiles, parts)
     load = np.zeros(parts)
