@@ -248,12 +248,9 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, cons
     if (q_armed > 0 && !warp_wait(bars.q_empty, (q_armed - 1) & 1, wd)) goto drain;
     {
       const int row0 = prob * p.rows + g * R;
-      if (elect_one()) {
-        mbar_arrive_expect_tx(bars.q_full, kNumChunks * C::kQChunkBytes);
-#pragma unroll 1
-        for (int c = 0; c < kNumChunks; ++c)
-          tma_load_3d(qs + c * C::kQChunkBytes, tm_q, bars.q_full, 0, c, row0, pol_q);
-      }
+      if (lane == 0) mbar_arrive_expect_tx(bars.q_full, kNumChunks * C::kQChunkBytes);
+      __syncwarp();
+      if (lane < kNumChunks) tma_load_3d(qs + lane * C::kQChunkBytes, tm_q, bars.q_full, 0, lane, row0, pol_q);
       __syncwarp();
       ++q_armed;
     }
@@ -291,23 +288,21 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, cons
           }
           // the tile's full barrier is armed with all its bytes before its first
           // copy, after that copy's slot wait (which implies the barrier's
-          // previous phase, three tiles back, has completed)
-          if (elect_one()) {
-            if (!tile_armed) mbar_arrive_expect_tx(fb, ok ? static_cast<uint32_t>(kNumChunks * C::kKvChunkBytes) : 0u);
-            if (ok)
-              for (int c = c0; c < c0 + nc; ++c)
-                tma_load_3d(kv + RG::chunk_off(jt, c), tm_kv, fb, 0, c, pg * kPageSize, pol_kv);
-          }
-          __syncwarp();
+          // previous phase, three tiles back, has completed); the item's
+          // chunks are issued by one lane each
           if (!tile_armed) {
+            if (lane == 0) mbar_arrive_expect_tx(fb, ok ? static_cast<uint32_t>(kNumChunks * C::kKvChunkBytes) : 0u);
+            __syncwarp();
             tile_armed = true;
             armed |= 1u << fidx;
             next_par ^= 1u << fidx;
           }
+          if (ok && lane < nc)
+            tma_load_3d(kv + RG::chunk_off(jt, c0 + lane), tm_kv, fb, 0, c0 + lane, pg * kPageSize, pol_kv);
+          __syncwarp();
           if (lane == 0) {
             if (c0 == 0) MLA_TR(kTrProdChunk0, jt);
             if (c0 == 8) MLA_TR(kTrProdChunk8, jt);
-            MLA_TR(kTrProdC + c0, jt);
           }
         }
         if (++fidx == 3) fidx = 0;
