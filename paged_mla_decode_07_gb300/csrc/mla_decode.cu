@@ -719,6 +719,51 @@ __device__ __forceinline__ void warp_reduce_scatter(const float (&v)[N], float* 
   }
 }
 
+// The same over the 16 lanes of each half warp (xor offsets 8..1; the two
+// halves reduce independently).  N = 16: lane l of a half ends with value
+// l & 15; N = 8: lanes 2k, 2k+1 of a half both hold value k.  Writes dst[i]
+// for the lanes that own value i.
+template <int N, bool MAX>
+__device__ __forceinline__ void half_reduce_scatter(const float (&v)[N], float* dst, int lane) {
+  static_assert(N == 8 || N == 16, "values per thread");
+  float t[N / 2];
+  {
+    const bool up = (lane & 8) != 0;
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      const float send = up ? v[i] : v[i + N / 2];
+      const float keep = up ? v[i + N / 2] : v[i];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, 8);
+      t[i] = MAX ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  int n = N / 2;
+#pragma unroll
+  for (int o = 4; o >= 1; o >>= 1) {
+    if (n > 1) {
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < N / 4; ++i) {
+        if (i < n / 2) {
+          const float send = up ? t[i] : t[i + n / 2];
+          const float keep = up ? t[i + n / 2] : t[i];
+          const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+          t[i] = MAX ? fmaxf(keep, recv) : keep + recv;
+        }
+      }
+      n >>= 1;
+    } else {
+      const float recv = __shfl_xor_sync(0xffffffffu, t[0], o);
+      t[0] = MAX ? fmaxf(t[0], recv) : t[0] + recv;
+    }
+  }
+  if (N == 16) {
+    dst[lane & 15] = t[0];
+  } else if ((lane & 1) == 0) {
+    dst[(lane >> 1) & 7] = t[0];
+  }
+}
+
 template <int R, bool SPARSE>
 __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int g, int split0, uint32_t tmem,
                                  uint8_t* kv, const Bars& bars, float* aux, volatile uint8_t* flags,
@@ -731,9 +776,13 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
   const int warp_q = (threadIdx.x >> 5) & 3;
   const int lane = threadIdx.x & 31;
   // S^T of a 64-token tile (M = 64) occupies lanes 0..15 of each warp's
-  // quarter of TMEM: lane l < 16 of warp q holds token 16q + l
-  const bool active = lane < 16;
-  const int tl = 16 * warp_q + (lane & 15);  // token of the tile (active lanes)
+  // quarter of TMEM, token 16q + l in lane l of quarter q.  Both halves of a
+  // warp work on the same 16 tokens: half hh = lane / 16 takes rows
+  // [rb + hh*RH, rb + hh*RH + RH) of this warpgroup's RW rows.
+  constexpr int RH = RW / 2;
+  const int hh = lane >> 4;
+  const int tl = 16 * warp_q + (lane & 15);  // token of the tile
+  const int rh = rb + hh * RH;               // first row of this thread
   const uint32_t lane_base = static_cast<uint32_t>(warp_q * 32) << 16;
   const uint32_t bar_id = kSoftmaxBar + wg;
   float* m_s = aux;            // running row max (log2 units)
@@ -759,7 +808,7 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
   };
   const bool tracer = (wg == 0 && tid == 0);
   int jt = 0, seg = 0;
-  float l[RW];
+  float l[RH];
   if (p.debug_stall) {
     // Watchdog test: mma_done only completes after this role has finished, so
     // this wait can only end by the watchdog limit.
@@ -783,7 +832,7 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
       lim_s[rb + tid] = (!SPARSE && p.is_causal) ? L - p.s_q + (g * R + rb + tid) / p.h_q : L - 1;
     }
 #pragma unroll
-    for (int r = 0; r < RW; ++r) l[r] = 0.f;
+    for (int r = 0; r < RH; ++r) l[r] = 0.f;
     gsync();
 
     for (int j = tb; j < te; ++j, ++jt) {
@@ -798,16 +847,18 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
       }
       tc_fence_after();
       const int pos = j * kTileTokens + tl;  // dense: logical token of this thread
-      const bool tok_ok = active && (SPARSE ? flags[(jt & 1) * 128 + tl] != 0
-                                            : (pos < L && flags[(jt & 1) * 128] != 0));
+      const bool tok_ok = SPARSE ? flags[(jt & 1) * 128 + tl] != 0 : (pos < L && flags[(jt & 1) * 128] != 0);
       if (tracer) MLA_TR(kTrSmSFull, jt);
 
-      // this thread's token, this warpgroup's rows of S^T: all loads in flight, one wait
-      float x[RW];
+      // this thread's token, its RH rows of S^T (the two halves of the warp
+      // read the two halves of the warpgroup's columns)
+      float x[RH];
       {
         const uint32_t s_addr = tmem + lane_base + C::kSCol + sb * R + rb;
-#pragma unroll
-        for (int q = 0; q < RW / 16; ++q) tmem_ld_x16(s_addr + 16 * q, *reinterpret_cast<float(*)[16]>(x + 16 * q));
+        if constexpr (RH == 16)
+          tmem_ld_16x32bx2_x16<RH>(s_addr, x);
+        else
+          tmem_ld_16x32bx2_x8<RH>(s_addr, x);
         tmem_ld_wait();
       }
       tc_fence_before();
@@ -821,14 +872,14 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
       const float sc = p.scale_log2;
       if (all_rows) {
 #pragma unroll
-        for (int r = 0; r < RW; ++r) x[r] *= sc;
+        for (int r = 0; r < RH; ++r) x[r] *= sc;
       } else if (SPARSE || !tok_ok) {
 #pragma unroll
-        for (int r = 0; r < RW; ++r) x[r] = kNegInf;
+        for (int r = 0; r < RH; ++r) x[r] = kNegInf;
       } else {
 #pragma unroll
-        for (int r4 = 0; r4 < RW / 4; ++r4) {
-          const int4 l4 = reinterpret_cast<const int4*>(lim_s + rb)[r4];
+        for (int r4 = 0; r4 < RH / 4; ++r4) {
+          const int4 l4 = reinterpret_cast<const int4*>(lim_s + rh)[r4];
           x[4 * r4] = pos <= l4.x ? x[4 * r4] * sc : kNegInf;
           x[4 * r4 + 1] = pos <= l4.y ? x[4 * r4 + 1] * sc : kNegInf;
           x[4 * r4 + 2] = pos <= l4.z ? x[4 * r4 + 2] * sc : kNegInf;
@@ -842,8 +893,8 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
       if (!need) {
         float loc = kNegInf;
 #pragma unroll
-        for (int r4 = 0; r4 < RW / 4; ++r4) {
-          const float4 m4 = reinterpret_cast<const float4*>(m_s + rb)[r4];
+        for (int r4 = 0; r4 < RH / 4; ++r4) {
+          const float4 m4 = reinterpret_cast<const float4*>(m_s + rh)[r4];
           loc = fmaxf(loc, fmaxf(fmaxf(x[4 * r4] - m4.x, x[4 * r4 + 1] - m4.y),
                                  fmaxf(x[4 * r4 + 2] - m4.z, x[4 * r4 + 3] - m4.w)));
         }
@@ -852,7 +903,7 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
         if (tracer) MLA_TR(kTrSmVote, jt);
       }
       if (need) {
-        warp_reduce_scatter<RW, true>(x, red + warp_q * R + rb, lane);
+        half_reduce_scatter<RH, true>(x, red + warp_q * R + rh, lane);
         gsync();
         if (tid < RW) {
           const int r = rb + tid;
@@ -864,7 +915,7 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
         }
         gsync();
 #pragma unroll
-        for (int r = 0; r < RW; ++r) l[r] *= alpha_s[rb + r];
+        for (int r = 0; r < RH; ++r) l[r] *= alpha_s[rh + r];
         if (j != tb) {
           // rescale this warpgroup's row columns of O^T by alpha once the PV
           // MMAs of the previous tile are done (those of earlier tiles are:
@@ -896,9 +947,9 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
       }
       const uint32_t p_base = kv_base + Ring<C>::p_off(jt);
 #pragma unroll
-      for (int r8 = 0; r8 < RW / 8; ++r8) {
-        const float4 ma = reinterpret_cast<const float4*>(m_s + rb)[2 * r8];
-        const float4 mb = reinterpret_cast<const float4*>(m_s + rb)[2 * r8 + 1];
+      for (int r8 = 0; r8 < RH / 8; ++r8) {
+        const float4 ma = reinterpret_cast<const float4*>(m_s + rh)[2 * r8];
+        const float4 mb = reinterpret_cast<const float4*>(m_s + rh)[2 * r8 + 1];
         const float mr[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
         float pr[8];
 #pragma unroll
@@ -907,27 +958,26 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
           pr[e] = (x[r] == kNegInf) ? 0.f : fast_exp2(x[r] - mr[e]);
           l[r] += pr[e];
         }
-        if (!active) continue;
         if (C::kPMnMajor) {
           // P^T as [token][R rows] (MN-major B operand): one 16-byte chunk per 8 rows
-          const uint32_t ch = (rb >> 3) + r8;
+          const uint32_t ch = (rh >> 3) + r8;
           st_shared_v4(p_base + tl * 128 + ((ch ^ (tl & 7)) << 4), pack_bf16x2(pr[0], pr[1]),
                        pack_bf16x2(pr[2], pr[3]), pack_bf16x2(pr[4], pr[5]), pack_bf16x2(pr[6], pr[7]));
         } else {
           // P as [R rows][64 tokens] (K-major B operand)
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const int r = rb + 8 * r8 + e;
+            const int r = rh + 8 * r8 + e;
             const uint32_t addr = p_base + p_row_off + r * 128 + ((p_chunk ^ (r & 7)) << 4);
             st_shared_u16(addr, __bfloat16_as_ushort(__float2bfloat16_rn(pr[e])));
           }
         }
       }
-      if (!SPARSE && active && !tok_ok) {
+      if (!SPARSE && !tok_ok) {
         // a masked token's V row must be finite (0 * NaN would poison O): zero
-        // it (the warpgroups split the eight value chunks)
+        // it (the warpgroups and warp halves split the eight value chunks)
 #pragma unroll 1
-        for (int c = wg; c < 8; c += C::kSmWG) {
+        for (int c = 2 * wg + hh; c < 8; c += 2 * C::kSmWG) {
           const uint32_t base = kv_base + Ring<C>::chunk_off(jt, c) + tl * 128;
 #pragma unroll
           for (int q = 0; q < 8; ++q) st_shared_v4(base + 16 * q, 0u, 0u, 0u, 0u);
@@ -945,7 +995,7 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
     if (!group_ok(mbar_wait(bars.o_full, seg & 1, wd))) return;
     tc_fence_after();
     if (tracer) MLA_TR(kTrEpiStart, seg);
-    warp_reduce_scatter<RW, false>(l, red + warp_q * R + rb, lane);
+    half_reduce_scatter<RH, false>(l, red + warp_q * R + rh, lane);
     gsync();
     if (tid < RW) {
       const int r = rb + tid;

@@ -325,6 +325,33 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 // tcgen05: TMEM <-> registers (32 lanes x 32-bit shape: thread t of the warp
 // reads/writes TMEM lane (warp's lane quarter base + t), N consecutive columns)
 // ---------------------------------------------------------------------------
+// 16 lanes x 32 bits, two halves: threads 0..15 read lanes base+t, columns
+// [col, col+N); threads 16..31 read lanes base+t-16, columns [col+OFF, col+OFF+N)
+// (for an M = 64 result, which fills lanes 0..15 of each 32-lane quarter).
+template <int OFF>
+__device__ __forceinline__ void tmem_ld_16x32bx2_x16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], %17;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr), "n"(OFF));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+template <int OFF>
+__device__ __forceinline__ void tmem_ld_16x32bx2_x8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr), "n"(OFF));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile(
