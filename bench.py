@@ -187,6 +187,7 @@ class DecodeStep:
         ns, nn = mla.metadata_size(b, s, h, self.topk)
         self.sched = torch.empty(ns, dtype=torch.int32, device=device)
         self.nsplit = torch.empty(nn, dtype=torch.int32, device=device)
+        self.g_step = self.g_decode = None
 
     def metadata(self):
         self.mla.get_metadata(self.d.cache_seqlens, self.w.s_q, self.w.h_q, self.topk, sched=self.sched,
@@ -201,6 +202,41 @@ class DecodeStep:
     def __call__(self):
         self.metadata()
         self.decode()
+
+    def capture(self):
+        """Record one step (and one decode call) as CUDA graphs, so a timed step is the device work
+        alone, not the host-side argument marshalling of each call.  Returns False (eager steps)
+        if capture is unavailable."""
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                self()
+            torch.cuda.current_stream().wait_stream(side)
+            self.g_step = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.g_step):
+                self()
+            self.g_decode = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(self.g_decode):
+                self.decode()
+            torch.cuda.synchronize()
+            return True
+        except Exception as e:  # capture unsupported in this environment: time eager calls
+            print(f"CUDA graph capture unavailable ({e}); timing eager calls", file=sys.stderr)
+            self.g_step = self.g_decode = None
+            return False
+
+    def replay_step(self):
+        if self.g_step is not None:
+            self.g_step.replay()
+        else:
+            self()
+
+    def replay_decode(self):
+        if self.g_decode is not None:
+            self.g_decode.replay()
+        else:
+            self.decode()
 
 
 def time_events(fn, n: int):
@@ -254,10 +290,11 @@ def measure_workload(name, device, reps=20, warmup=3):
     """Kernel-level measurement of one workload (decode call = split-KV kernel + combine)."""
     inp = W.make_inputs(name, device=device)
     st = DecodeStep(inp, device)
+    st.capture()
     st.metadata()
     for _ in range(warmup):
-        st.decode()
-    times = time_events(st.decode, reps)
+        st.replay_decode()
+    times = time_events(st.replay_decode, reps)
     a = algorithmic(inp)
     ms = statistics.median(times)
     return inp, a, ms, st
@@ -301,8 +338,9 @@ def run_mla(args):
     inp = W.make_inputs(wname, seed=rank_seed(wname, rank), device=device)
     a = algorithmic(inp)
     step = DecodeStep(inp, device)
+    graphs = step.capture()
     for _ in range(args.warmup):
-        step()
+        step.replay_step()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -312,7 +350,7 @@ def run_mla(args):
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record()
         for _ in range(args.steps):
-            step()
+            step.replay_step()
         t1.record()
         torch.cuda.synchronize()
     if world > 1:
@@ -324,7 +362,7 @@ def run_mla(args):
 
     # ---- dominant kernel: decode call (split-KV kernel + combine), same workload
     step.metadata()
-    dts = time_events(step.decode, max(10, args.steps))
+    dts = time_events(step.replay_decode, max(10, args.steps))
     dec_ms = statistics.mean(dts)
     wl = inp.workload
     if wname in ("dense_membound", "tiny"):
@@ -348,7 +386,8 @@ def run_mla(args):
                    "seqlens": W.describe_lengths(wl), "page_size": 64,
                    "mode": "dense bf16 cache" if wl.mode == "dense" else f"sparse top-{wl.topk} fp8 cache",
                    "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (KV %.0f MB > 129 MB), no flush" % (a["kv_bytes"] / 1e6)},
+                   "l2": "inputs larger than L2 (KV %.0f MB > 129 MB), no flush" % (a["kv_bytes"] / 1e6),
+                   "step_launch": "CUDA graph of schedule + decode + combine" if graphs else "eager calls"},
         "tflops": round(a["flops"] * world / (ms * 1e-3) / 1e12, 2),
         "roofline": roof,
         "gpu_launches": 3 * args.steps,
