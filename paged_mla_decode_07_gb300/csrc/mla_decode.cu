@@ -127,9 +127,9 @@ struct Cfg {
   // holds under three tiles), used round robin: tile jt -> jt % 3, phase jt / 3
   static constexpr int kNumFull = 3;
   // sparse: raw FP8 rows of a tile land by row gathers in the upper chunk of
-  // each pair slot (codes) and in the RoPE slot; raw_full[b] (b = 0..3 pairs,
-  // 4 = RoPE) completes when they have arrived
-  static constexpr int kNumRaw = SPARSE ? 5 : 0;
+  // each pair slot (codes) and in the RoPE slot; raw_full[5 * (jt & 1) + b]
+  // (b = 0..3 pairs, 4 = RoPE) completes when tile jt's have arrived
+  static constexpr int kNumRaw = SPARSE ? 10 : 0;  // two sets (tile parity) of five
   static constexpr int kNumBars = 2 + kNumFull + kNA + kNB + 4 + 2 + 5 + kNumRaw;
   // rounded to 128 bytes so the row statistics after the barriers are 16-byte
   // aligned (they are read with 16-byte vector loads)
@@ -166,7 +166,7 @@ struct Bars {
   uint64_t* o_empty;
   uint64_t* mma_done;
   uint64_t* o_done;    // [2]: tile jt's PV MMAs are done (barrier jt & 1)
-  uint64_t* raw_full;  // sparse: [5]
+  uint64_t* raw_full;  // sparse: [10]
 };
 
 // Segment iterator shared by all roles: the part walks problems p0..p1 and,
@@ -531,6 +531,11 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
   using RG = Ring<C>;
   // 128 threads, two per token: half h = 0 (warps 0, 1) converts value blocks
   // 0 and 1 and the RoPE dims, half 1 (warps 2, 3) value blocks 2 and 3.
+  // Software-pipelined: the rows of tile jt+1 are looked up (dependent index
+  // and block-table loads) before tile jt is dequantised, and tile jt+1's row
+  // gathers are issued right after, so lookups overlap conversion and gather
+  // latency overlaps the next lookup.  The raw barriers come in two sets
+  // (tile parity) so two tiles' copies never share a phase.
   const int tid = threadIdx.x - 32 * C::kGatherWarp0;
   const int lane = tid & 31;
   const int h = tid >> 6;
@@ -539,82 +544,111 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
   const uint32_t tsw = tok & 7;
   const uint32_t kv_base = smem_u32(kv);
   const uint64_t pol = l2_policy_evict_normal();
-  int armed[5] = {0, 0, 0, 0, 0};  // phases of raw_full armed by this warp (drained on exit)
-  int jt = 0;
-  for (int prob = sg.p0; prob <= sg.last(); ++prob) {
-    int tb, te;
-    sg.range(prob, tb, te);
-    if (tb >= te) continue;
-    const int b = prob / p.s_q;
+  uint32_t armed = 0, next_par = 0;  // raw barriers armed by this warp (bit per barrier), next phase parity
+
+  // tile iterator over the CTA's segments
+  struct It {
+    int prob, j, te;
+    bool valid;
+  };
+  auto first_from = [&](int prob) -> It {
+    for (; prob <= sg.last(); ++prob) {
+      int tb, te;
+      sg.range(prob, tb, te);
+      if (tb < te) return It{prob, tb, te, true};
+    }
+    return It{0, 0, 0, false};
+  };
+  auto next_of = [&](const It& it) -> It {
+    if (it.j + 1 < it.te) return It{it.prob, it.j + 1, it.te, true};
+    return first_from(it.prob + 1);
+  };
+  // look up this thread's token of tile `it`: cache row (invalid -> row 0,
+  // zeros written later), validity, this half's two scales
+  auto lookup = [&](const It& it, int& row, bool& ok, uint2& sc) {
+    const int b = it.prob / p.s_q;
     const int L = sg.seqlens[b];
-    const int32_t* idx_row = p.indices + static_cast<int64_t>(prob) * p.topk;
+    const int k = it.j * kTileTokens + tok;
+    const int t = k < p.topk ? p.indices[static_cast<int64_t>(it.prob) * p.topk + k] : -1;
+    ok = t >= 0 && t < L;
     const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
-    int t_next = (tb * kTileTokens + tok < p.topk) ? idx_row[tb * kTileTokens + tok] : -1;
-    for (int j = tb; j < te; ++j, ++jt) {
-      if (tid == 0) MLA_TR(kTrGatherStart, jt);
-      const int t = t_next;
-      {
-        const int kn = (j + 1) * kTileTokens + tok;
-        t_next = (j + 1 < te && kn < p.topk) ? idx_row[kn] : -1;
+    const int page = (ok && (t >> 6) < p.block_table_stride) ? bt[t >> 6] : -1;
+    if (ok && (page < 0 || page >= p.num_pages)) {
+      ok = false;
+      if (h == 0) atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
+    }
+    row = ok ? page * kPageSize + (t & 63) : 0;
+    sc = ok ? __ldg(reinterpret_cast<const uint2*>(p.kv_fp8 + static_cast<int64_t>(row) * kFp8RowBytes +
+                                                   kFp8ScaleOffset + 8 * h))
+            : make_uint2(0, 0);
+  };
+  // issue the row gathers of tile jt (codes of this half's blocks into the
+  // upper chunks of their pair slots; half 0 also the RoPE bytes)
+  auto issue = [&](int jt, int row, bool ok) -> bool {
+    const int g4 = wtok + 4 * (lane & 7);
+    const int r0 = __shfl_sync(0xffffffffu, row, (4 * lane) & 31);
+    const int r1 = __shfl_sync(0xffffffffu, row, (4 * lane + 1) & 31);
+    const int r2 = __shfl_sync(0xffffffffu, row, (4 * lane + 2) & 31);
+    const int r3 = __shfl_sync(0xffffffffu, row, (4 * lane + 3) & 31);
+    const int set = 5 * (jt & 1);
+#pragma unroll 1
+    for (int i = 0; i < 2; ++i) {
+      const int blk = 2 * h + i;
+      const uint32_t use = RG::pair_use(jt, blk);
+      if (use > 0 && !warp_wait(bars.pair_empty + RG::pair_slot(jt, blk), (use - 1) & 1, wd)) return false;
+      if (blk == 0) flags[(jt & 1) * 128 + tok] = ok ? 1 : 0;  // token validity for the softmax
+      if (lane == 0) mbar_arrive_expect_tx(bars.raw_full + set + blk, 32 * 128);
+      armed |= 1u << (set + blk);
+      next_par ^= 1u << (set + blk);
+      __syncwarp();
+      if (lane < 8) {
+        uint8_t* dst = kv + RG::chunk_off(jt, 2 * blk + 1) + g4 * 128;
+        tma_gather4(dst, tm_rows, bars.raw_full + set + blk, 128 * blk, r0, r1, r2, r3, pol);
       }
-      // token -> cache row (page * 64 + slot); invalid tokens read row 0 and
-      // are written as zeros below
-      bool ok = t >= 0 && t < L;
-      const bool in_table = ok && (t >> 6) < p.block_table_stride;
-      int page = in_table ? bt[t >> 6] : -1;
-      if (ok && (page < 0 || page >= p.num_pages)) {
-        ok = false;
-        if (h == 0) atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
+    }
+    if (h == 0) {
+      const uint32_t use = RG::rope_use(jt);
+      if (use > 0 && !warp_wait(bars.rope_empty + RG::rope_slot(jt), (use - 1) & 1, wd)) return false;
+      if (lane == 0) mbar_arrive_expect_tx(bars.raw_full + set + 4, 32 * 128);
+      armed |= 1u << (set + 4);
+      next_par ^= 1u << (set + 4);
+      __syncwarp();
+      if (lane < 8) {
+        uint8_t* dst = kv + RG::chunk_off(jt, 8) + g4 * 128;
+        tma_gather4(dst, tm_rows, bars.raw_full + set + 4, kFp8RopeOffset, r0, r1, r2, r3, pol);
       }
-      const int row = ok ? page * kPageSize + (t & 63) : 0;
-      // this half's two scales (value blocks 2h, 2h+1)
-      const uint2 sc = ok ? __ldg(reinterpret_cast<const uint2*>(p.kv_fp8 + static_cast<int64_t>(row) * kFp8RowBytes +
-                                                             kFp8ScaleOffset + 8 * h))
-                          : make_uint2(0, 0);
-      // rows of this lane's group of four tokens (lanes 0..7 issue the gathers)
-      const int g4 = wtok + 4 * (lane & 7);
-      const int r0 = __shfl_sync(0xffffffffu, row, (4 * lane) & 31);
-      const int r1 = __shfl_sync(0xffffffffu, row, (4 * lane + 1) & 31);
-      const int r2 = __shfl_sync(0xffffffffu, row, (4 * lane + 2) & 31);
-      const int r3 = __shfl_sync(0xffffffffu, row, (4 * lane + 3) & 31);
+    }
+    return true;
+  };
 
-      // issue: the codes of value block b (dims 128b..128b+127) into the upper
-      // chunk of pair slot b once its previous tile's PV is done; half 0 then
-      // the RoPE bytes into the RoPE slot
+  It cur = first_from(sg.p0);
+  int row_c = 0;
+  bool ok_c = false;
+  uint2 sc_c = make_uint2(0, 0);
+  int jt = 0;
+  if (cur.valid) {
+    lookup(cur, row_c, ok_c, sc_c);
+    if (!issue(0, row_c, ok_c)) goto drain;
+  }
+  for (; cur.valid; ++jt) {
+    if (tid == 0) MLA_TR(kTrGatherStart, jt);
+    // tile jt+1: look up its rows first (the loads overlap the conversion)
+    const It nxt = next_of(cur);
+    int row_n = 0;
+    bool ok_n = false;
+    uint2 sc_n = make_uint2(0, 0);
+    if (nxt.valid) lookup(nxt, row_n, ok_n, sc_n);
+    // dequantise tile jt in place: token tok's 128 code bytes of block b sit
+    // at row tok of chunk 2b+1; they become row tok of chunks 2b and 2b+1
+    // (bf16, 128-byte swizzle).  Units are read in a per-thread rotated order.
+    {
+      const int set = 5 * (jt & 1);
+      const uint32_t par = static_cast<uint32_t>(jt >> 1) & 1u;  // phase of set (jt & 1) for tile jt
 #pragma unroll 1
       for (int i = 0; i < 2; ++i) {
         const int blk = 2 * h + i;
-        const uint32_t use = RG::pair_use(jt, blk);
-        if (use > 0 && !warp_wait(bars.pair_empty + RG::pair_slot(jt, blk), (use - 1) & 1, wd)) goto drain;
-        if (blk == 0) flags[(jt & 1) * 128 + tok] = ok ? 1 : 0;  // token validity for the softmax
-        if (lane == 0) mbar_arrive_expect_tx(bars.raw_full + blk, 32 * 128);
-        ++armed[blk];
-        __syncwarp();
-        if (lane < 8) {
-          uint8_t* dst = kv + RG::chunk_off(jt, 2 * blk + 1) + g4 * 128;
-          tma_gather4(dst, tm_rows, bars.raw_full + blk, 128 * blk, r0, r1, r2, r3, pol);
-        }
-      }
-      if (h == 0) {
-        const uint32_t use = RG::rope_use(jt);
-        if (use > 0 && !warp_wait(bars.rope_empty + RG::rope_slot(jt), (use - 1) & 1, wd)) goto drain;
-        if (lane == 0) mbar_arrive_expect_tx(bars.raw_full + 4, 32 * 128);
-        ++armed[4];
-        __syncwarp();
-        if (lane < 8) {
-          uint8_t* dst = kv + RG::chunk_off(jt, 8) + g4 * 128;
-          tma_gather4(dst, tm_rows, bars.raw_full + 4, kFp8RopeOffset, r0, r1, r2, r3, pol);
-        }
-      }
-
-      // dequantise in place: token tok's 128 code bytes of block b sit at row
-      // tok of chunk 2b+1; they become row tok of chunks 2b and 2b+1 (bf16,
-      // 128-byte swizzle).  Units are read in a per-thread rotated order.
-#pragma unroll 1
-      for (int i = 0; i < 2; ++i) {
-        const int blk = 2 * h + i;
-        if (!warp_wait(bars.raw_full + blk, armed[blk] == 0 ? 0 : (armed[blk] - 1) & 1, wd)) goto drain;
-        const float scale = __uint_as_float(i == 0 ? sc.x : sc.y);
+        if (!warp_wait(bars.raw_full + set + blk, par, wd)) goto drain;
+        const float scale = __uint_as_float(i == 0 ? sc_c.x : sc_c.y);
         const uint32_t lo = kv_base + RG::chunk_off(jt, 2 * blk) + tok * 128;
         const uint32_t hi = kv_base + RG::chunk_off(jt, 2 * blk + 1) + tok * 128;
         uint4 raw[8];
@@ -626,7 +660,7 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
           const uint32_t dst = ((u & 4) ? hi : lo);
           const uint32_t k0 = (2 * (u & 3)) ^ tsw, k1 = (2 * (u & 3) + 1) ^ tsw;
           uint4 v = raw[k];
-          if (!ok) v = make_uint4(0, 0, 0, 0);
+          if (!ok_c) v = make_uint4(0, 0, 0, 0);
           st_shared_v4(dst + (k0 << 4), dequant2(v.x & 0xffffu, scale), dequant2(v.x >> 16, scale),
                        dequant2(v.y & 0xffffu, scale), dequant2(v.y >> 16, scale));
           st_shared_v4(dst + (k1 << 4), dequant2(v.z & 0xffffu, scale), dequant2(v.z >> 16, scale),
@@ -635,7 +669,7 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
       }
       if (h == 0) {
         // RoPE: already bf16; permute the 16-byte units into the swizzled order
-        if (!warp_wait(bars.raw_full + 4, (armed[4] - 1) & 1, wd)) goto drain;
+        if (!warp_wait(bars.raw_full + set + 4, par, wd)) goto drain;
         const uint32_t base = kv_base + RG::chunk_off(jt, 8) + tok * 128;
         uint4 raw[8];
 #pragma unroll
@@ -643,24 +677,34 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
         // raw[k] holds unit k ^ tsw, whose swizzled position is (k ^ tsw) ^ tsw = k
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint4 v = ok ? raw[k] : make_uint4(0, 0, 0, 0);
+          const uint4 v = ok_c ? raw[k] : make_uint4(0, 0, 0, 0);
           st_shared_v4(base + (k << 4), v.x, v.y, v.z, v.w);
         }
       }
-      // this warp's part of the tile is written: one arrival on the tile's
-      // full barrier (after the proxy fence that orders it for the MMAs)
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars.full + RG::full_index(jt));
-      if (tid == 0) MLA_TR(kTrGatherDone, jt);
     }
+    // this warp's part of the tile is written: one arrival on the tile's full
+    // barrier (after the proxy fence that orders it for the MMAs)
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars.full + RG::full_index(jt));
+    if (tid == 0) MLA_TR(kTrGatherDone, jt);
+    // then tile jt+1's row gathers (their slots free once the PV of tile jt-1 is done)
+    if (nxt.valid && !issue(jt + 1, row_n, ok_n)) goto drain;
+    cur = nxt;
+    row_c = row_n;
+    ok_c = ok_n;
+    sc_c = sc_n;
   }
   return;
 drain:
-  // abort: wait (bounded) for this warp's row gathers still in flight
+  // abort: wait (bounded) for this warp's row gathers still in flight (the
+  // latest armed phase of each raw barrier)
+  if (lane == 0) {
 #pragma unroll 1
-  for (int k = 0; k < 5; ++k)
-    if (armed[k] > 0) mbar_wait_drain(bars.raw_full + k, (armed[k] - 1) & 1, wd.limit_ns);
+    for (int k = 0; k < C::kNumRaw; ++k)
+      if ((armed >> k) & 1u) mbar_wait_drain(bars.raw_full + k, ((next_par >> k) & 1u) ^ 1u, wd.limit_ns);
+  }
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
@@ -1125,6 +1169,10 @@ __global__ void __launch_bounds__(Cfg<R, SPARSE>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   Watchdog wd{abort_flag, p.status, p.timeout_ns};
+  // launched as a programmatic dependent of the schedule kernel: everything
+  // above overlapped it; its results (and any earlier kernel's) are visible
+  // from here on
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   Segments sg;
   const int32_t* sr = p.sched + static_cast<int64_t>(part) * kSchedInts;
   sg.p0 = sr[kSchedP0];
@@ -1181,9 +1229,17 @@ cudaError_t launch_one(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const 
     if (e != cudaSuccess) return e;
     if (fa.numRegs * C::kThreads < C::kRegBudget) return cudaErrorInvalidConfiguration;
   }
-  const int grid = p.num_parts * p.row_groups;
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_kv, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_parts * p.row_groups);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tm_q, tm_kv, p);
 }
 
 }  // namespace

@@ -104,6 +104,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   Pos* starts = reinterpret_cast<Pos*>(warp_tot + kThreads / 32);  // [num_parts + 1]
   int* tiles = reinterpret_cast<int*>(starts + num_parts + 1);     // [np]
   const int tid = threadIdx.x;
+  // the decode kernel may launch now (its prologue overlaps this kernel; it
+  // waits for this kernel's results before reading the schedule)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // 1. problem tiles (one read of cache_seqlens), costs and their prefix sums
   for (int p = tid; p < np; p += kThreads) {
