@@ -74,6 +74,13 @@ def _load():
             lib.oracle_e4m3_to_double.restype = D
             lib.oracle_dequant_row.argtypes = [P, P]
             lib.oracle_dequant_row.restype = None
+            lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
+            lib.oracle_fp8_quantize_row.argtypes = [P, P]
+            lib.oracle_fp8_quantize_row.restype = None
+            lib.oracle_fp8_cache_store.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_int, P]
+            lib.oracle_fp8_cache_store.restype = ctypes.c_int64
             _libs[path] = lib
     return lib
 
@@ -189,3 +196,31 @@ def dequant_row(row656) -> np.ndarray:
     k = np.zeros((D_QK,), np.float64)
     _load().oracle_dequant_row(_ptr(r), _ptr(k))
     return k
+
+
+def e4m3_from_float(q: float) -> int:
+    """float32 value -> E4M3 code: nearest value, ties to the even code, saturating at 448."""
+    return int(_load().oracle_e4m3_from_float(ctypes.c_float(q)))
+
+
+def fp8_quantize_row(x576) -> np.ndarray:
+    """One token (576 bf16 values, torch bf16 tensor) -> its 656-byte FP8 cache row."""
+    xb = np.ascontiguousarray(_np(x576, np.uint16).reshape(-1))
+    assert xb.size == 576
+    row = np.zeros(656, dtype=np.uint8)
+    _load().oracle_fp8_quantize_row(_ptr(xb), _ptr(row))
+    return row
+
+
+def fp8_cache_store(x, input_row_offsets, cache_lengths, block_table, kvcache):
+    """Ragged FP8 cache write into a copy of `kvcache` (uint8 [pages, page_size, 1, 656]).
+    Returns (new cache as a numpy array, number of skipped tokens)."""
+    xb = np.ascontiguousarray(_np(x, np.uint16))
+    offs = np.ascontiguousarray(_np(input_row_offsets, np.int32))
+    lens = np.ascontiguousarray(_np(cache_lengths, np.int32))
+    bt = np.ascontiguousarray(_np(block_table, np.int32))
+    cache = np.array(_np(kvcache, np.uint8), copy=True)
+    batch = int(lens.shape[0])
+    skipped = _load().oracle_fp8_cache_store(_ptr(xb), _ptr(offs), _ptr(lens), _ptr(bt), int(bt.shape[1]), batch,
+                                              int(cache.shape[0]), int(cache.shape[1]), _ptr(cache))
+    return cache, int(skipped)

@@ -327,3 +327,94 @@ void oracle_lse_merge(int n, const double* outs, const double* lses, double* out
   }
   *lse = L;
 }
+
+/* ------------------------------------------------------------------------
+ * FP8 cache write ("Why FlashMLA's decode kernel reaches 660 TFLOPS",
+ * Design 2: per token, the 512 NoPE dims are quantised to float8_e4m3 in
+ * 1 x 128 tiles with one float32 scale per tile, the 64 RoPE dims stay
+ * bf16; the MAX kernels summary, KV-cache store section: new tokens of a
+ * ragged batch are written at the end of each sequence through the page
+ * lookup table).
+ *
+ * Reading of the quantiser (the pages name only amax / 448 and E4M3):
+ *   amax  = max |x| over the tile's 128 values (exact),
+ *   scale = amax / 448 in float32 (round to nearest), 1 if amax == 0,
+ *   code  = e4m3 of x / scale (float32 division, round to nearest), rounded
+ *           to the nearest E4M3 value, ties to the even code, magnitudes
+ *           above 448 saturated to 448 ("satfinite"); NaN -> 0x7F.
+ * ------------------------------------------------------------------------ */
+
+/* The 127 non-negative finite E4M3 values, by code 0x00 .. 0x7E (ascending). */
+static double e4m3_pos_value(int code) { return oracle_e4m3_to_double((uint8_t)code); }
+
+/* float -> E4M3 code: nearest value, ties to the even code, saturating. */
+uint8_t oracle_e4m3_from_float(float q) {
+  if (isnan(q)) return 0x7F;
+  const uint8_t sign = signbit(q) ? 0x80 : 0x00;
+  const double a = fabs((double)q);
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+  /* largest code lo with value(lo) <= a (binary search over the ascending grid) */
+  int lo = 0, hi = 0x7E;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) / 2;
+    if (e4m3_pos_value(mid) <= a)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  if (e4m3_pos_value(lo) == a) return (uint8_t)(sign | lo);
+  /* a lies strictly between value(lo) and value(lo + 1) */
+  const double d_lo = a - e4m3_pos_value(lo), d_hi = e4m3_pos_value(lo + 1) - a;
+  int code;
+  if (d_lo < d_hi)
+    code = lo;
+  else if (d_hi < d_lo)
+    code = lo + 1;
+  else
+    code = (lo % 2 == 0) ? lo : lo + 1; /* tie: the even code */
+  return (uint8_t)(sign | code);
+}
+
+/* One token: 576 bf16 values (bits) -> one 656-byte cache row. */
+void oracle_fp8_quantize_row(const uint16_t* x, uint8_t* row) {
+  for (int t = 0; t < 4; ++t) {
+    float amax = 0.0f;
+    for (int d = 128 * t; d < 128 * t + 128; ++d) {
+      float v = (float)bf16_bits_to_double(x[d]);
+      if (fabsf(v) > amax) amax = fabsf(v);
+    }
+    const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int d = 128 * t; d < 128 * t + 128; ++d) {
+      const float v = (float)bf16_bits_to_double(x[d]);
+      row[d] = oracle_e4m3_from_float(v / scale);
+    }
+    memcpy(row + FP8_SCALE_OFFSET + 4 * t, &scale, sizeof scale);
+  }
+  memcpy(row + FP8_ROPE_OFFSET, x + D_V, 2 * (D_QK - D_V));
+}
+
+/* Ragged store: token i of element b (row input_row_offsets[b] + i of x)
+ * goes to logical position cache_lengths[b] + i of element b, i.e. page
+ * block_table[b][pos / page_size], slot pos % page_size.  Tokens whose page
+ * entry lies outside the table or the pool are skipped.  Returns the number
+ * of skipped tokens. */
+int64_t oracle_fp8_cache_store(const uint16_t* x, const int32_t* input_row_offsets,
+                               const int32_t* cache_lengths, const int32_t* block_table,
+                               int block_table_stride, int batch, int num_pages, int page_size,
+                               uint8_t* kvcache) {
+  int64_t skipped = 0;
+  for (int b = 0; b < batch; ++b) {
+    for (int32_t r = input_row_offsets[b]; r < input_row_offsets[b + 1]; ++r) {
+      const int64_t pos = (int64_t)cache_lengths[b] + (r - input_row_offsets[b]);
+      const int64_t blk = pos / page_size;
+      const int32_t page = blk < block_table_stride ? block_table[(int64_t)b * block_table_stride + blk] : -1;
+      if (page < 0 || page >= num_pages) {
+        ++skipped;
+        continue;
+      }
+      uint8_t* dst = kvcache + ((int64_t)page * page_size + pos % page_size) * FP8_ROW_BYTES;
+      oracle_fp8_quantize_row(x + (int64_t)r * D_QK, dst);
+    }
+  }
+  return skipped;
+}
