@@ -300,6 +300,27 @@ def measure_workload(name, device, reps=20, warmup=3):
     return inp, a, ms, st
 
 
+def measure_store(device, peaks, batch=32, new_tokens=4096, reps=20):
+    """FP8 cache write (mla_fp8_cache_store) of a prefill-sized chunk: batch x new_tokens bf16 tokens
+    quantised into fresh pages.  Bytes = 1152 read + 656 written per token (larger than L2)."""
+    import paged_mla_decode_07_gb300 as mla
+    g = torch.Generator(device=device).manual_seed(1006)
+    n = batch * new_tokens
+    x = torch.randn((n, D_QK), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    offs = torch.arange(0, n + 1, new_tokens, dtype=torch.int32, device=device)
+    lens = torch.zeros(batch, dtype=torch.int32, device=device)
+    per = new_tokens // 64
+    table = torch.randperm(batch * per, generator=g, device=device).int().reshape(batch, per)
+    cache = torch.empty((batch * per, 64, 1, FP8_ROW), dtype=torch.uint8, device=device)
+    fn = lambda: mla.fp8_cache_store(x, offs, lens, table, cache)
+    for _ in range(3):
+        fn()
+    ms = statistics.median(time_events(fn, reps))
+    gbs = n * (D_QK * 2 + FP8_ROW) / (ms * 1e-3) / 1e9
+    return {"ms": round(ms, 5), "tokens": n, "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+            "bytes_per_token": D_QK * 2 + FP8_ROW}
+
+
 def max_over_ranks(x: float, device) -> float:
     """The largest x over all ranks of the default process group (x itself without one)."""
     import torch.distributed as dist
@@ -424,6 +445,7 @@ def run_mla(args):
             extra[name] = e
             del st, winp
             torch.cuda.empty_cache()
+        extra["fp8_cache_store"] = measure_store(device, peaks)
         result["workloads"] = extra
         # ---- the oracle on the host cores, bounded sample
         result["cpu_baseline"] = cpu_baseline(inp, target_s=args.cpu_seconds)

@@ -137,6 +137,34 @@ mla_status mla_decode(const mla_decode_args* args, mla_stream_t stream);
  * the array needs to start at zero. */
 mla_status mla_decode_noalloc(const mla_decode_args* args, mla_stream_t stream);
 
+/* FP8 cache write: quantise new tokens into the 656-byte FP8 cache row and
+ * store them through the block table (the step before a sparse FP8 decode).
+ *
+ * Row format ("Why FlashMLA's decode kernel reaches 660 TFLOPS", Design 2):
+ * dims 0..511 as float8_e4m3 codes in four 1 x 128 tiles, each tile with one
+ * float32 scale = amax / 448 (1 for an all-zero tile), code = E4M3 of
+ * x / scale (float32 division) rounded to nearest even and saturated at 448;
+ * bytes [512, 528) the four scales; bytes [528, 656) dims 512..575 as bf16.
+ * Placement (MAX kernels summary, KV-cache store section): the new tokens of
+ * batch element b are rows input_row_offsets[b] .. input_row_offsets[b+1]-1
+ * of x and go to positions cache_lengths[b] + i of element b, i.e. page
+ * block_table[b * block_table_stride + pos / 64], slot pos % 64.
+ *
+ *   x                 bf16 [num_tokens, 576], device, 16-byte aligned
+ *   input_row_offsets int32 [batch + 1], device, non-decreasing, from 0 to num_tokens
+ *   cache_lengths     int32 [batch], device: tokens already cached per element
+ *   block_table       int32 [batch, block_table_stride], device
+ *   kvcache           uint8 [num_pages, 64, 1, 656], device, 16-byte aligned; written
+ * The caller owns all memory; the call is asynchronous on `stream`.  A token
+ * whose page entry lies past block_table_stride or outside [0, num_pages) is
+ * not written and sets MLA_DEVICE_BAD_PAGE in the device status word.  Host-
+ * side argument errors return MLA_ERR_INVALID_ARG / MLA_ERR_UNSUPPORTED
+ * (page_size != 64) without launching.  num_tokens == 0 launches nothing. */
+mla_status mla_fp8_cache_store(const void* x, int num_tokens, const int32_t* input_row_offsets,
+                               const int32_t* cache_lengths, int batch, const int32_t* block_table,
+                               int block_table_stride, void* kvcache, int num_pages, int page_size,
+                               mla_stream_t stream);
+
 /* Synchronises `stream`, returns the device status bits accumulated since the
  * last call in *flags (0 = clean) and clears them.  Returns
  * MLA_ERR_DEVICE_TIMEOUT / MLA_ERR_DEVICE_BOUNDS when the matching bit is set. */

@@ -82,6 +82,8 @@ def lib():
             L.mla_decode.argtypes = [ctypes.POINTER(DecodeArgs), P]
             L.mla_decode.restype = I
             L.mla_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+            L.mla_fp8_cache_store.argtypes = [P, I, P, P, I, P, I, P, I, I, P]
+            L.mla_fp8_cache_store.restype = I
             L.mla_get_device_status.restype = I
             _lib = L
     return _lib
@@ -215,6 +217,34 @@ def decode(q: torch.Tensor, kvcache: torch.Tensor, block_table: torch.Tensor, ca
     a.lse = lse.data_ptr()
     _check(lib().mla_decode(ctypes.byref(a), _stream(stream)))
     return out.view(batch, s_q, h_q, D_V), lse.view(batch, s_q, h_q)
+
+
+def fp8_cache_store(x: torch.Tensor, input_row_offsets: torch.Tensor, cache_lengths: torch.Tensor,
+                    block_table: torch.Tensor, kvcache: torch.Tensor, stream=None) -> None:
+    """Quantise new tokens into the FP8 cache rows (mla_fp8_cache_store).
+
+    x bf16 [num_tokens, 576]; input_row_offsets int32 [batch + 1]; cache_lengths int32 [batch];
+    block_table int32 [batch, stride]; kvcache uint8 [num_pages, 64, 1, 656] (written in place).
+    """
+    if not torch.is_tensor(x) or x.device.type != "cuda":
+        raise ValueError("x must be a CUDA tensor")
+    dev = x.device
+    _need(x, "x", torch.bfloat16, dev, 2)
+    if x.shape[1] != 576:
+        raise ValueError(f"x must be [num_tokens, 576] (got {tuple(x.shape)})")
+    _need(input_row_offsets, "input_row_offsets", torch.int32, dev, 1)
+    _need(cache_lengths, "cache_lengths", torch.int32, dev, 1)
+    _need(block_table, "block_table", torch.int32, dev, 2)
+    _need(kvcache, "kvcache", torch.uint8, dev, 4)
+    batch = cache_lengths.shape[0]
+    if input_row_offsets.shape[0] != batch + 1 or block_table.shape[0] != batch:
+        raise ValueError("input_row_offsets must have batch + 1 entries and block_table batch rows")
+    if kvcache.shape[2] != 1 or kvcache.shape[3] != 656:
+        raise ValueError(f"kvcache must be [num_pages, page_size, 1, 656] (got {tuple(kvcache.shape)})")
+    _check(lib().mla_fp8_cache_store(x.data_ptr(), x.shape[0], input_row_offsets.data_ptr(),
+                                     cache_lengths.data_ptr(), batch, block_table.data_ptr(),
+                                     block_table.shape[1], kvcache.data_ptr(), kvcache.shape[0], kvcache.shape[1],
+                                     _stream(stream)))
 
 
 def device_status(stream=None, raise_on_error: bool = False) -> int:

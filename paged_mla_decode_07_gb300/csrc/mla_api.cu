@@ -343,6 +343,34 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
   return ok();
 }
 
+mla_status mla_fp8_cache_store(const void* x, int num_tokens, const int32_t* input_row_offsets,
+                               const int32_t* cache_lengths, int batch, const int32_t* block_table,
+                               int block_table_stride, void* kvcache, int num_pages, int page_size,
+                               mla_stream_t stream) {
+  if (batch < 1) return fail(MLA_ERR_INVALID_ARG, "batch = %d must be >= 1", batch);
+  if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens = %d must be >= 0", num_tokens);
+  if (page_size != kPageSize) return fail(MLA_ERR_UNSUPPORTED, "page_size must be 64 (got %d)", page_size);
+  if (num_pages < 1) return fail(MLA_ERR_INVALID_ARG, "num_pages = %d must be >= 1", num_pages);
+  if (block_table_stride < 1)
+    return fail(MLA_ERR_INVALID_ARG, "block_table_stride = %d must be >= 1", block_table_stride);
+  if (num_tokens > 0 && !x) return fail(MLA_ERR_INVALID_ARG, "x is NULL");
+  if (!input_row_offsets) return fail(MLA_ERR_INVALID_ARG, "input_row_offsets is NULL");
+  if (!cache_lengths) return fail(MLA_ERR_INVALID_ARG, "cache_lengths is NULL");
+  if (!block_table) return fail(MLA_ERR_INVALID_ARG, "block_table is NULL");
+  if (!kvcache) return fail(MLA_ERR_INVALID_ARG, "kvcache is NULL");
+  if (x && !aligned(x, 16)) return fail(MLA_ERR_INVALID_ARG, "x is not 16-byte aligned");
+  if (!aligned(kvcache, 16)) return fail(MLA_ERR_INVALID_ARG, "kvcache is not 16-byte aligned");
+  uint32_t* status = nullptr;
+  int sms = 0;
+  mla_status st = device_info(&status, &sms);
+  if (st != MLA_OK) return st;
+  cudaError_t e = launch_fp8_cache_store(static_cast<const uint16_t*>(x), num_tokens, input_row_offsets,
+                                         cache_lengths, batch, block_table, block_table_stride,
+                                         static_cast<uint8_t*>(kvcache), num_pages, status, sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "fp8 cache store launch");
+  return ok();
+}
+
 mla_status mla_get_device_status(mla_stream_t stream, uint32_t* flags) {
   if (!flags) return fail(MLA_ERR_INVALID_ARG, "flags is NULL");
   uint32_t* status = nullptr;

@@ -97,6 +97,10 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, con
                           bool sparse, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
 size_t decode_smem_bytes(int rpc, bool sparse);
+cudaError_t launch_fp8_cache_store(const uint16_t* x, int num_tokens, const int32_t* row_offsets,
+                                   const int32_t* cache_lengths, int batch, const int32_t* block_table,
+                                   int block_table_stride, uint8_t* kvcache, int num_pages, uint32_t* status,
+                                   int sm_count, cudaStream_t stream);
 // Sets the thread-local message returned by mla_last_error().
 void set_error_message(const std::string& msg);
 
