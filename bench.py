@@ -59,7 +59,7 @@ def algorithmic(inp) -> dict:
         vflops = 2.0 * w.h_q * valid * (D_QK + D_V)
         tab = idx.numel() * 4 + inp.block_table.numel() * 4
     else:
-        kv_bytes = int(lens.sum()) * D_QK * 2
+        kv_bytes = int(lens.sum()) * (FP8_ROW if w.is_fp8 else D_QK * 2)  # dense over bf16 or FP8 rows
         flops = 2.0 * w.h_q * w.s_q * float(lens.sum()) * (D_QK + D_V)
         if w.causal:
             vk = sum(max(0, min(L, L - w.s_q + i + 1)) for L in lens for i in range(w.s_q))
@@ -386,7 +386,7 @@ def run_mla(args):
     dts = time_events(step.replay_decode, max(10, args.steps))
     dec_ms = statistics.mean(dts)
     wl = inp.workload
-    if wname in ("dense_membound", "tiny"):
+    if wname in ("dense_membound", "tiny", "dense_membound_fp8"):
         roof = {"bound": "hbm", "achieved": round(a["bytes"] / (dec_ms * 1e-3) / 1e9, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     else:
@@ -396,7 +396,8 @@ def run_mla(args):
     roof["traffic"] = measured_traffic(wname)
     roof["algorithmic_bytes"] = a["bytes"] if roof["bound"] == "hbm" else None
     rows = 16 if wl.s_q * wl.h_q <= 16 else (32 if wl.s_q * wl.h_q <= 32 else 64)
-    roof["kernel"] = f"mla_decode_kernel<{rows},{'sparse' if wl.mode == 'sparse' else 'dense'}> + combine (one decode call)"
+    kmode = "sparse" if wl.mode == "sparse" else ("dense_fp8" if wl.is_fp8 else "dense")
+    roof["kernel"] = f"mla_decode_kernel<{rows},{kmode}> + combine (one decode call)"
     roof["peak_source"] = peaks["source"]
 
     result = {
@@ -405,7 +406,8 @@ def run_mla(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 q/KV, random page permutation)",
         "config": {"workload": wname, "batch": wl.batch, "h_q": wl.h_q, "s_q": wl.s_q,
                    "seqlens": W.describe_lengths(wl), "page_size": 64,
-                   "mode": "dense bf16 cache" if wl.mode == "dense" else f"sparse top-{wl.topk} fp8 cache",
+                   "mode": ("dense fp8 cache" if wl.is_fp8 else "dense bf16 cache") if wl.mode == "dense"
+                           else f"sparse top-{wl.topk} fp8 cache",
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (KV %.0f MB > 129 MB), no flush" % (a["kv_bytes"] / 1e6),
                    "step_launch": "CUDA graph of schedule + decode + combine" if graphs else "eager calls"},
@@ -432,9 +434,9 @@ def run_mla(args):
         torch.cuda.empty_cache()
         # ---- the other workloads (kernel level)
         extra = {}
-        for name in ("tiny", "dense_computebound", "sparse_fp8", "sparse_fp8_long"):
+        for name in ("tiny", "dense_computebound", "sparse_fp8", "sparse_fp8_long", "dense_membound_fp8"):
             winp, wa, wms, st = measure_workload(name, device)
-            bound = "hbm" if name == "tiny" else "tensor"
+            bound = "hbm" if name in ("tiny", "dense_membound_fp8") else "tensor"
             e = {"ms": round(wms, 5), "tflops": round(wa["flops"] / (wms * 1e-3) / 1e12, 2),
                  "tflops_valid": round(wa["valid_flops"] / (wms * 1e-3) / 1e12, 2),
                  "kv_gbs": round(wa["bytes"] / (wms * 1e-3) / 1e9, 1)}

@@ -151,14 +151,15 @@ mla_status encode_rows_map(CUtensorMap* map, const void* base, long long nrows, 
 }
 
 // The FP8 cache as [rows][656] bytes (row = page * 64 + slot).  A box is 128
-// bytes of one row (the map's box is one row high, as row gathers require);
-// no swizzle: the gathered rows land as plain 128-byte rows.
-mla_status encode_fp8_rows_map(CUtensorMap* map, const void* base, long long nrows) {
+// bytes of box_rows rows: one row for the sparse row gathers (as row gathers
+// require), 32 consecutive rows of a page for dense decode over the FP8
+// cache; no swizzle: the rows land as plain 128-byte rows.
+mla_status encode_fp8_rows_map(CUtensorMap* map, const void* base, long long nrows, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(kFp8RowBytes), static_cast<cuuint64_t>(nrows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(kFp8RowBytes)};
-  cuuint32_t box[2] = {128, 1};
+  cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -252,8 +253,6 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
     return fail(MLA_ERR_UNSUPPORTED, "num_pages = %d exceeds 2^31 tokens", a->num_pages);
   if (a->block_table_stride < 1)
     return fail(MLA_ERR_INVALID_ARG, "block_table_stride must be >= 1 (got %d)", a->block_table_stride);
-  if (a->is_fp8 && !sparse)
-    return fail(MLA_ERR_UNSUPPORTED, "is_fp8 = 1 requires sparse mode (topk > 0): dense decode reads a bf16 cache");
   if (!a->is_fp8 && sparse)
     return fail(MLA_ERR_UNSUPPORTED, "sparse mode (topk > 0) requires the FP8 cache (is_fp8 = 1)");
   if (a->is_causal && sparse) return fail(MLA_ERR_UNSUPPORTED, "is_causal applies to dense mode only");
@@ -282,12 +281,16 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
   const long long qrows = static_cast<long long>(a->batch) * a->s_q * a->h_q;
   st = encode_rows_map(&tm_q, a->q, qrows, g.rpc, "q");
   if (st != MLA_OK) return st;
-  if (!sparse) {
+  // kernel mode: 0 dense over the bf16 cache, 1 sparse over the FP8 cache,
+  // 2 dense over the FP8 cache
+  const int mode = sparse ? 1 : (a->is_fp8 ? 2 : 0);
+  if (mode == 0) {
     st = encode_rows_map(&tm_kv, a->kvcache, static_cast<long long>(a->num_pages) * kPageSize, kPageSize,
                          "kvcache");
     if (st != MLA_OK) return st;
   } else {
-    st = encode_fp8_rows_map(&tm_kv, a->kvcache, static_cast<long long>(a->num_pages) * kPageSize);
+    st = encode_fp8_rows_map(&tm_kv, a->kvcache, static_cast<long long>(a->num_pages) * kPageSize,
+                             mode == 1 ? 1 : 32);
     if (st != MLA_OK) return st;
   }
 
@@ -325,7 +328,7 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
   p.scale_log2 = a->sm_scale * 1.4426950408889634f;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_decode(tm_q, tm_kv, p, g.rpc, sparse, s);
+  cudaError_t e = launch_decode(tm_q, tm_kv, p, g.rpc, mode, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
 
   CombineParams cp;

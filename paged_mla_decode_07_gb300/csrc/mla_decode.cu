@@ -82,12 +82,20 @@ constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 before a max update is forced
 constexpr uint32_t kSoftmaxBar = 1;        // named barrier of the 128 softmax threads
 
-template <int R, bool SPARSE>
+// Kernel modes: dense decode over the bf16 cache, sparse (top-k) decode over
+// the FP8 cache, dense decode over the FP8 cache.
+constexpr int kModeDense = 0, kModeSparse = 1, kModeDenseFp8 = 2;
+
+template <int R, int MODE>
 struct Cfg {
+  // FP8 rows are gathered and dequantised by four extra warps; sparse
+  // problems are (batch element, query token) pairs with their own indices
+  static constexpr bool kGather = MODE != kModeDense;
+  static constexpr bool kIndexed = MODE == kModeSparse;
   // softmax warpgroups: with 64 rows two warpgroups split the rows
   static constexpr int kSmWG = (R == 64) ? 2 : 1;
   static constexpr int kGatherWarp0 = 4 + 4 * kSmWG;  // sparse: first FP8 gather warp
-  static constexpr int kWarps = kGatherWarp0 + (SPARSE ? 4 : 0);
+  static constexpr int kWarps = kGatherWarp0 + (kGather ? 4 : 0);
   // With two softmax warpgroups the producer/MMA warpgroup hands registers to
   // the others (setmaxnreg).  Sparse: 512 threads launched at 128 registers,
   // 128*64 + 2*128*160 + 128*128 = 65536.  Dense: 384 threads at 168,
@@ -95,8 +103,8 @@ struct Cfg {
   // against kRegBudget before launching (an increase beyond the launch's total
   // would never be granted).
   static constexpr bool kRegSplit = kSmWG == 2;
-  static constexpr uint32_t kRegsCtl = SPARSE ? 64 : 88, kRegsSoftmax = SPARSE ? 160 : 208, kRegsGather = 128;
-  static constexpr int kRegBudget = 128 * kRegsCtl + 256 * kRegsSoftmax + (SPARSE ? 128 * kRegsGather : 0);
+  static constexpr uint32_t kRegsCtl = kGather ? 64 : 88, kRegsSoftmax = kGather ? 160 : 208, kRegsGather = 128;
+  static constexpr int kRegBudget = 128 * kRegsCtl + 256 * kRegsSoftmax + (kGather ? 128 * kRegsGather : 0);
   static_assert(!kRegSplit || kRegBudget <= 65536, "register split exceeds the register file");
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kKvChunkBytes = kTileTokens * 128;  // 8 KB: [64 tokens][64 dims] bf16
@@ -129,7 +137,7 @@ struct Cfg {
   // sparse: raw FP8 rows of a tile land by row gathers in the upper chunk of
   // each pair slot (codes) and in the RoPE slot; raw_full[5 * (jt & 1) + b]
   // (b = 0..3 pairs, 4 = RoPE) completes when tile jt's have arrived
-  static constexpr int kNumRaw = SPARSE ? 10 : 0;  // two sets (tile parity) of five
+  static constexpr int kNumRaw = kGather ? 10 : 0;  // two sets (tile parity) of five
   static constexpr int kNumBars = 2 + kNumFull + kNA + kNB + 4 + 2 + 5 + kNumRaw;
   // rounded to 128 bytes so the row statistics after the barriers are 16-byte
   // aligned (they are read with 16-byte vector loads)
@@ -145,7 +153,7 @@ struct Cfg {
 
   // arrivals on a tile's full barrier: dense 1 (the producer, + the tile's
   // TMA bytes); sparse 4 (each gather warp once it has written its part)
-  static constexpr int kFullArrivals = SPARSE ? 4 : 1;
+  static constexpr int kFullArrivals = kGather ? 4 : 1;
   static_assert(kPBytes <= kKvChunkBytes || !kPAlias, "P must fit in the RoPE chunk");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(R == 16 || R == 32 || R == 64, "rows per CTA");
@@ -223,14 +231,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 // ---------------------------------------------------------------------------
 // producer: Q (always) and dense KV pages by TMA
 // ---------------------------------------------------------------------------
-template <int R, bool SPARSE>
+template <int R, int MODE>
 __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, const DecodeParams& p,
                          const Segments& sg, int g, uint8_t* kv, uint8_t* qs, const Bars& bars,
                          volatile uint8_t* flags, const Watchdog& wd) {
   // The whole producer warp runs this code converged; each copy is issued by
   // one elected lane (as for the MMAs, a lane issuing alone while its warp
   // waits elsewhere issues far more slowly).
-  using C = Cfg<R, SPARSE>;
+  using C = Cfg<R, MODE>;
 
   const uint64_t pol_kv = p.evict_first ? l2_policy_evict_first() : l2_policy_evict_normal();
   const uint64_t pol_q = l2_policy_evict_normal();
@@ -254,7 +262,7 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, cons
       __syncwarp();
       ++q_armed;
     }
-    if (!SPARSE) {
+    if (!C::kGather) {
       const int b = prob;
       const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
       for (int j = tb; j < te; ++j, ++jt) {
@@ -314,7 +322,7 @@ drain:
   // armed phase of every full barrier (earlier phases of a barrier completed
   // before it was re-armed)
   if (lane == 0) {
-    if (!SPARSE) {
+    if (!C::kGather) {
 #pragma unroll 1
       for (int k = 0; k < C::kNumFull; ++k)
         if ((armed >> k) & 1u) mbar_wait_drain(bars.full + k, ((next_par >> k) & 1u) ^ 1u, wd.limit_ns);
@@ -384,10 +392,10 @@ __device__ __forceinline__ void warp_commit(uint32_t bar) {
   __syncwarp();
 }
 
-template <int R, bool SPARSE>
+template <int R, int MODE>
 __device__ void s_issuer(const Segments& sg, uint32_t tmem, uint8_t* kv, uint8_t* qs, const Bars& bars,
                          const Watchdog& wd) {
-  using C = Cfg<R, SPARSE>;
+  using C = Cfg<R, MODE>;
   constexpr uint32_t kIdS = idesc_bf16_f32(kTileTokens, R, 0, 0);  // A = K tile (K-major), B = Q (K-major)
   constexpr uint64_t kHiK = smem_desc_hi(16, 1024);
   const int lane = threadIdx.x & 31;
@@ -452,9 +460,9 @@ done:
   __syncwarp();
 }
 
-template <int R, bool SPARSE>
+template <int R, int MODE>
 __device__ void pv_issuer(const Segments& sg, uint32_t tmem, uint8_t* kv, const Bars& bars, const Watchdog& wd) {
-  using C = Cfg<R, SPARSE>;
+  using C = Cfg<R, MODE>;
   constexpr uint32_t kIdO = idesc_bf16_f32(128, R, 1, C::kPMnMajor ? 1 : 0);  // A = V^T (MN-major), B = P
   constexpr uint64_t kHiV = smem_desc_hi(C::kKvChunkBytes, 1024);
   constexpr uint64_t kHiP = smem_desc_hi(16, 1024);
@@ -524,10 +532,10 @@ __device__ __forceinline__ uint32_t dequant2(uint32_t codes16, float scale) {
   return pack_bf16x2(lo * scale, hi * scale);
 }
 
-template <int R>
+template <int R, int MODE>
 __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, const Segments& sg, uint8_t* kv,
                            const Bars& bars, volatile uint8_t* flags, const Watchdog& wd) {
-  using C = Cfg<R, true>;
+  using C = Cfg<R, MODE>;
   using RG = Ring<C>;
   // 128 threads, two per token: half h = 0 (warps 0, 1) converts value blocks
   // 0 and 1 and the RoPE dims, half 1 (warps 2, 3) value blocks 2 and 3.
@@ -566,18 +574,30 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
   // look up this thread's token of tile `it`: cache row (invalid -> row 0,
   // zeros written later), validity, this half's two scales
   auto lookup = [&](const It& it, int& row, bool& ok, uint2& sc) {
-    const int b = it.prob / p.s_q;
-    const int L = sg.seqlens[b];
-    const int k = it.j * kTileTokens + tok;
-    const int t = k < p.topk ? p.indices[static_cast<int64_t>(it.prob) * p.topk + k] : -1;
-    ok = t >= 0 && t < L;
-    const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
-    const int page = (ok && (t >> 6) < p.block_table_stride) ? bt[t >> 6] : -1;
-    if (ok && (page < 0 || page >= p.num_pages)) {
-      ok = false;
-      if (h == 0) atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
+    if (C::kIndexed) {
+      const int b = it.prob / p.s_q;
+      const int L = sg.seqlens[b];
+      const int k = it.j * kTileTokens + tok;
+      const int t = k < p.topk ? p.indices[static_cast<int64_t>(it.prob) * p.topk + k] : -1;
+      ok = t >= 0 && t < L;
+      const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
+      const int page = (ok && (t >> 6) < p.block_table_stride) ? bt[t >> 6] : -1;
+      if (ok && (page < 0 || page >= p.num_pages)) {
+        ok = false;
+        if (h == 0) atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
+      }
+      row = ok ? page * kPageSize + (t & 63) : 0;
+    } else {
+      // dense: tile j is page j of the element; row = page * 64 + token, with
+      // page 0 standing in for an unusable page (its tokens are written as zeros)
+      const int b = it.prob;
+      const int L = sg.seqlens[b];
+      const int page = it.j < p.block_table_stride ? p.block_table[static_cast<int64_t>(b) * p.block_table_stride + it.j] : -1;
+      const bool page_ok = page >= 0 && page < p.num_pages;
+      if (!page_ok && tok == 0 && h == 0) atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
+      ok = page_ok && it.j * kTileTokens + tok < L;
+      row = (page_ok ? page : 0) * kPageSize + tok;
     }
-    row = ok ? page * kPageSize + (t & 63) : 0;
     sc = ok ? __ldg(reinterpret_cast<const uint2*>(p.kv_fp8 + static_cast<int64_t>(row) * kFp8RowBytes +
                                                    kFp8ScaleOffset + 8 * h))
             : make_uint2(0, 0);
@@ -601,9 +621,15 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
       armed |= 1u << (set + blk);
       next_par ^= 1u << (set + blk);
       __syncwarp();
-      if (lane < 8) {
-        uint8_t* dst = kv + RG::chunk_off(jt, 2 * blk + 1) + g4 * 128;
-        tma_gather4(dst, tm_rows, bars.raw_full + set + blk, 128 * blk, r0, r1, r2, r3, pol);
+      if (C::kIndexed) {
+        if (lane < 8) {
+          uint8_t* dst = kv + RG::chunk_off(jt, 2 * blk + 1) + g4 * 128;
+          tma_gather4(dst, tm_rows, bars.raw_full + set + blk, 128 * blk, r0, r1, r2, r3, pol);
+        }
+      } else if (lane == 0) {
+        // dense: this warp's 32 consecutive rows of the page in one box
+        tma_load_2d(kv + RG::chunk_off(jt, 2 * blk + 1) + wtok * 128, tm_rows, bars.raw_full + set + blk,
+                    128 * blk, row, pol);
       }
     }
     if (h == 0) {
@@ -613,9 +639,14 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
       armed |= 1u << (set + 4);
       next_par ^= 1u << (set + 4);
       __syncwarp();
-      if (lane < 8) {
-        uint8_t* dst = kv + RG::chunk_off(jt, 8) + g4 * 128;
-        tma_gather4(dst, tm_rows, bars.raw_full + set + 4, kFp8RopeOffset, r0, r1, r2, r3, pol);
+      if (C::kIndexed) {
+        if (lane < 8) {
+          uint8_t* dst = kv + RG::chunk_off(jt, 8) + g4 * 128;
+          tma_gather4(dst, tm_rows, bars.raw_full + set + 4, kFp8RopeOffset, r0, r1, r2, r3, pol);
+        }
+      } else if (lane == 0) {
+        tma_load_2d(kv + RG::chunk_off(jt, 8) + wtok * 128, tm_rows, bars.raw_full + set + 4, kFp8RopeOffset, row,
+                    pol);
       }
     }
     return true;
@@ -808,11 +839,11 @@ __device__ __forceinline__ void half_reduce_scatter(const float (&v)[N], float* 
   }
 }
 
-template <int R, bool SPARSE>
+template <int R, int MODE>
 __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int g, int split0, uint32_t tmem,
                                  uint8_t* kv, const Bars& bars, float* aux, volatile uint8_t* flags,
                                  const Watchdog& wd) {
-  using C = Cfg<R, SPARSE>;
+  using C = Cfg<R, MODE>;
   constexpr int RW = R / C::kSmWG;  // rows owned by this warpgroup
   const int wg = (threadIdx.x - 128) >> 7;
   const int rb = wg * RW;           // first row of this warpgroup
@@ -863,17 +894,17 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
     int tb, te;
     sg.range(prob, tb, te);
     if (tb >= te) continue;
-    const int b = SPARSE ? prob / p.s_q : prob;
+    const int b = C::kIndexed ? prob / p.s_q : prob;
     const int L = sg.seqlens[b];
     // causal limit per row: query token i sees keys <= L - s_q + i (dense only)
     int lim_min = L - 1;
-    if (!SPARSE && p.is_causal) {
+    if (!C::kIndexed && p.is_causal) {
       const int i_first = (g * R + rb) / p.h_q;
       lim_min = min(L - 1, L - p.s_q + i_first);
     }
     if (tid < RW) {
       m_s[rb + tid] = kNegInf;
-      lim_s[rb + tid] = (!SPARSE && p.is_causal) ? L - p.s_q + (g * R + rb + tid) / p.h_q : L - 1;
+      lim_s[rb + tid] = (!C::kIndexed && p.is_causal) ? L - p.s_q + (g * R + rb + tid) / p.h_q : L - 1;
     }
 #pragma unroll
     for (int r = 0; r < RH; ++r) l[r] = 0.f;
@@ -891,7 +922,9 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
       }
       tc_fence_after();
       const int pos = j * kTileTokens + tl;  // dense: logical token of this thread
-      const bool tok_ok = SPARSE ? flags[(jt & 1) * 128 + tl] != 0 : (pos < L && flags[(jt & 1) * 128] != 0);
+      // gathered modes: the gather warps' per-token flag (dense FP8: position
+      // below the length and page usable); dense bf16: length and page flag
+      const bool tok_ok = C::kGather ? flags[(jt & 1) * 128 + tl] != 0 : (pos < L && flags[(jt & 1) * 128] != 0);
       if (tracer) MLA_TR(kTrSmSFull, jt);
 
       // this thread's token, its RH rows of S^T (the two halves of the warp
@@ -912,12 +945,12 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
 
       // logits in log2 units; masked -> -inf.  Rows differ only where a causal
       // limit falls inside the tile: their limits come from shared memory.
-      const bool all_rows = tok_ok && (SPARSE || pos <= lim_min);
+      const bool all_rows = tok_ok && (C::kIndexed || pos <= lim_min);
       const float sc = p.scale_log2;
       if (all_rows) {
 #pragma unroll
         for (int r = 0; r < RH; ++r) x[r] *= sc;
-      } else if (SPARSE || !tok_ok) {
+      } else if (C::kIndexed || !tok_ok) {
 #pragma unroll
         for (int r = 0; r < RH; ++r) x[r] = kNegInf;
       } else {
@@ -1017,7 +1050,7 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
           }
         }
       }
-      if (!SPARSE && !tok_ok) {
+      if (!C::kGather && !tok_ok) {
         // a masked token's V row must be finite (0 * NaN would poison O): zero
         // it (the warpgroups and warp halves split the eight value chunks)
 #pragma unroll 1
@@ -1096,11 +1129,11 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
 // ---------------------------------------------------------------------------
 // kernel
 // ---------------------------------------------------------------------------
-template <int R, bool SPARSE>
-__global__ void __launch_bounds__(Cfg<R, SPARSE>::kThreads, 1)
+template <int R, int MODE>
+__global__ void __launch_bounds__(Cfg<R, MODE>::kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                       const DecodeParams p) {
-  using C = Cfg<R, SPARSE>;
+  using C = Cfg<R, MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* kv = smem;
@@ -1193,18 +1226,18 @@ __global__ void __launch_bounds__(Cfg<R, SPARSE>::kThreads, 1)
   if (warp < 4) {
     if (C::kRegSplit) regs_dec<C::kRegsCtl>();
     if (warp == 0) {
-      producer<R, SPARSE>(&tm_q, &tm_kv, p, sg, g, kv, qs, bars, flags, wd);  // the whole warp, converged
+      producer<R, MODE>(&tm_q, &tm_kv, p, sg, g, kv, qs, bars, flags, wd);  // the whole warp, converged
     } else if (warp == 1) {
-      s_issuer<R, SPARSE>(sg, tmem, kv, qs, bars, wd);  // the whole warp, converged
+      s_issuer<R, MODE>(sg, tmem, kv, qs, bars, wd);  // the whole warp, converged
     } else if (warp == 3) {
-      pv_issuer<R, SPARSE>(sg, tmem, kv, bars, wd);
+      pv_issuer<R, MODE>(sg, tmem, kv, bars, wd);
     }
   } else if (warp < C::kGatherWarp0) {
     if (C::kRegSplit) regs_inc<C::kRegsSoftmax>();
-    softmax_epilogue<R, SPARSE>(p, sg, g, split0, tmem, kv, bars, aux, flags, wd);
-  } else if (SPARSE) {
+    softmax_epilogue<R, MODE>(p, sg, g, split0, tmem, kv, bars, aux, flags, wd);
+  } else if (C::kGather) {
     if (C::kRegSplit) regs_inc<C::kRegsGather>();
-    gather_fp8<R>(&tm_kv, p, sg, kv, bars, flags, wd);
+    gather_fp8<R, MODE>(&tm_kv, p, sg, kv, bars, flags, wd);
   }
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1216,11 +1249,11 @@ __global__ void __launch_bounds__(Cfg<R, SPARSE>::kThreads, 1)
   }
 }
 
-template <int R, bool SPARSE>
+template <int R, int MODE>
 cudaError_t launch_one(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const DecodeParams& p,
                        cudaStream_t stream) {
-  using C = Cfg<R, SPARSE>;
-  auto kern = mla_decode_kernel<R, SPARSE>;
+  using C = Cfg<R, MODE>;
+  auto kern = mla_decode_kernel<R, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   if (C::kRegSplit) {
@@ -1244,35 +1277,33 @@ cudaError_t launch_one(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const 
 
 }  // namespace
 
-size_t decode_smem_bytes(int rpc, bool sparse) {
-  if (sparse) {
-    switch (rpc) {
-      case 16: return Cfg<16, true>::kSmemBytes;
-      case 32: return Cfg<32, true>::kSmemBytes;
-      default: return Cfg<64, true>::kSmemBytes;
-    }
+size_t decode_smem_bytes(int rpc, int mode) {
+  switch (mode * 100 + rpc) {
+    case 16: return Cfg<16, kModeDense>::kSmemBytes;
+    case 32: return Cfg<32, kModeDense>::kSmemBytes;
+    case 64: return Cfg<64, kModeDense>::kSmemBytes;
+    case 116: return Cfg<16, kModeSparse>::kSmemBytes;
+    case 132: return Cfg<32, kModeSparse>::kSmemBytes;
+    case 164: return Cfg<64, kModeSparse>::kSmemBytes;
+    case 216: return Cfg<16, kModeDenseFp8>::kSmemBytes;
+    case 232: return Cfg<32, kModeDenseFp8>::kSmemBytes;
+    case 264: return Cfg<64, kModeDenseFp8>::kSmemBytes;
   }
-  switch (rpc) {
-    case 16: return Cfg<16, false>::kSmemBytes;
-    case 32: return Cfg<32, false>::kSmemBytes;
-    default: return Cfg<64, false>::kSmemBytes;
-  }
+  return 0;
 }
 
 cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const DecodeParams& p, int rpc,
-                          bool sparse, cudaStream_t stream) {
-  if (sparse) {
-    switch (rpc) {
-      case 16: return launch_one<16, true>(tm_q, tm_kv, p, stream);
-      case 32: return launch_one<32, true>(tm_q, tm_kv, p, stream);
-      case 64: return launch_one<64, true>(tm_q, tm_kv, p, stream);
-    }
-  } else {
-    switch (rpc) {
-      case 16: return launch_one<16, false>(tm_q, tm_kv, p, stream);
-      case 32: return launch_one<32, false>(tm_q, tm_kv, p, stream);
-      case 64: return launch_one<64, false>(tm_q, tm_kv, p, stream);
-    }
+                          int mode, cudaStream_t stream) {
+  switch (mode * 100 + rpc) {
+    case 16: return launch_one<16, kModeDense>(tm_q, tm_kv, p, stream);
+    case 32: return launch_one<32, kModeDense>(tm_q, tm_kv, p, stream);
+    case 64: return launch_one<64, kModeDense>(tm_q, tm_kv, p, stream);
+    case 116: return launch_one<16, kModeSparse>(tm_q, tm_kv, p, stream);
+    case 132: return launch_one<32, kModeSparse>(tm_q, tm_kv, p, stream);
+    case 164: return launch_one<64, kModeSparse>(tm_q, tm_kv, p, stream);
+    case 216: return launch_one<16, kModeDenseFp8>(tm_q, tm_kv, p, stream);
+    case 232: return launch_one<32, kModeDenseFp8>(tm_q, tm_kv, p, stream);
+    case 264: return launch_one<64, kModeDenseFp8>(tm_q, tm_kv, p, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -93,10 +93,11 @@ struct CombineParams {
 cudaError_t launch_metadata(const int32_t* cache_seqlens, int batch, int s_q, int h_q, int topk,
                             const Geometry& g, int32_t* sched, int32_t* num_splits, uint32_t* status,
                             cudaStream_t stream);
+// mode: 0 dense bf16 cache, 1 sparse FP8 cache, 2 dense FP8 cache
 cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const DecodeParams& p, int rpc,
-                          bool sparse, cudaStream_t stream);
+                          int mode, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
-size_t decode_smem_bytes(int rpc, bool sparse);
+size_t decode_smem_bytes(int rpc, int mode);
 cudaError_t launch_fp8_cache_store(const uint16_t* x, int num_tokens, const int32_t* row_offsets,
                                    const int32_t* cache_lengths, int batch, const int32_t* block_table,
                                    int block_table_stride, uint8_t* kvcache, int num_pages, uint32_t* status,

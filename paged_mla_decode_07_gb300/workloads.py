@@ -53,10 +53,11 @@ class Workload:
     invalid_frac: float = 0.05                  # sparse: trailing fraction of each index row set to -1
     page_size: int = PAGE_SIZE
     sm_scale: Optional[float] = None            # default 1/sqrt(576)
+    fp8: bool = False                           # dense mode over the FP8 cache
 
     @property
     def is_fp8(self) -> bool:
-        return self.mode == "sparse"
+        return self.mode == "sparse" or self.fp8
 
     @property
     def scale(self) -> float:
@@ -73,6 +74,9 @@ WORKLOADS = {
                            topk=2048),
     "sparse_fp8_long": Workload("sparse_fp8_long", batch=16, h_q=128, s_q=1, mode="sparse",
                                 seqlen_range=(65536, 131072), topk=32768),
+    # mode variant: the memory-bound dense mix over the FP8 cache (656 bytes per token)
+    "dense_membound_fp8": Workload("dense_membound_fp8", batch=128, h_q=16, s_q=1, mode="dense",
+                                   seqlen_range=(1024, 8192), fp8=True),
 }
 # Seed per named workload: 1000 + its position (1-based) in the list above.
 SEEDS = {name: 1000 + i for i, name in enumerate(WORKLOADS, start=1)}

@@ -77,7 +77,6 @@ def _args(**kw):
     ("page_size", 32, 2, "page_size must be 64"),
     ("num_pages", 0, 1, "num_pages"),
     ("block_table_stride", 0, 1, "block_table_stride"),
-    ("is_fp8", 1, 2, "requires sparse mode"),
     ("q", 18, 1, "q is not 16-byte aligned"),
     ("sm_scale", float("nan"), 1, "sm_scale"),
 ])

@@ -226,3 +226,53 @@ def test_full_size_workload(name, n_problems):
     if inp.workload.mode == "dense":
         vmax = float(inp.kvcache[..., :512].float().nan_to_num(0.0).abs().max())
         assert float(np.abs(out).max()) <= vmax * (1 + 1e-2)
+
+
+# ---------------------------------------------------------------- dense over the FP8 cache
+@pytest.mark.parametrize("L", [1, 63, 64, 65, 200, 1000])
+def test_dense_fp8_lengths(L):
+    check(W.custom(name=f"dfp8_{L}", batch=2, h_q=16, s_q=1, mode="dense", fp8=True, seqlens=(L, max(1, L // 3))),
+          700 + L)
+
+
+@pytest.mark.parametrize("h_q,s_q,causal", [(32, 1, False), (64, 1, False), (128, 2, True), (16, 4, True),
+                                            (40, 3, False)])
+def test_dense_fp8_row_shapes_and_causal(h_q, s_q, causal):
+    check(W.custom(name=f"dfp8h{h_q}s{s_q}", batch=3, h_q=h_q, s_q=s_q, mode="dense", fp8=True,
+                   seqlens=(200, 77, 513), causal=causal), 800 + h_q + s_q)
+
+
+@pytest.mark.parametrize("parts", [1, 7, 300])
+def test_dense_fp8_forced_splits_and_empty(parts):
+    w = W.custom(name=f"dfp8p{parts}", batch=4, h_q=64, s_q=2, mode="dense", fp8=True,
+                 seqlens=(1000, 0, 130, 2049), causal=True)
+    out, lse, _, _ = check(w, 900 + parts, parts=parts)
+    assert np.all(out[1] == 0) and np.all(np.isneginf(lse[1]))
+
+
+def test_dense_fp8_equals_dense_over_dequantised_cache():
+    """Dense decode over an FP8 cache equals dense decode over its dequantised bf16 copy."""
+    w = W.custom(name="dfp8eq", batch=2, h_q=64, s_q=1, mode="dense", fp8=True, seqlens=(700, 129))
+    inp = W.make_inputs(w, seed=33, poison_tail=False)
+    out_f, lse_f, _ = run_cuda(inp)
+    flat = inp.kvcache.reshape(-1, 656)
+    n = flat.shape[0]
+    codes = flat[:, :512].contiguous().view(torch.float8_e4m3fn).float().reshape(n, 4, 128)
+    scales = flat[:, 512:528].contiguous().view(torch.float32).reshape(n, 4)
+    nope = (codes * scales[:, :, None]).reshape(n, 512).to(torch.bfloat16)
+    rope = flat[:, 528:].contiguous().view(torch.bfloat16)
+    kvb = torch.cat([nope, rope], 1).reshape(inp.kvcache.shape[0], 64, 1, 576)
+    dense = W.Inputs(W.custom(name="d", batch=2, h_q=64, s_q=1, mode="dense", seqlens=(700, 129)), inp.q, kvb,
+                     inp.block_table, inp.cache_seqlens, None, inp.sm_scale, 0)
+    out_d, lse_d, _ = run_cuda(dense)
+    compare(out_f, lse_f, out_d, lse_d, "dense-fp8-vs-dense")
+
+
+def test_dense_fp8_full_size_workload():
+    inp = W.make_inputs("dense_membound_fp8")
+    out, lse, flags = run_cuda(inp)
+    assert flags == 0
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+    rows = _sample_rows(inp, 12, np.random.default_rng(8))
+    ref_out, ref_lse = run_oracle(inp, rows=rows)
+    compare(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, "dense_membound_fp8")
