@@ -81,6 +81,8 @@ def _load():
             lib.oracle_fp8_cache_store.argtypes = [P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                    ctypes.c_int, P]
             lib.oracle_fp8_cache_store.restype = ctypes.c_int64
+            lib.oracle_sparse_prefill.argtypes = [P, P, I64, P, I, I, D, P, I64, P, P, I]
+            lib.oracle_sparse_prefill.restype = None
             _libs[path] = lib
     return lib
 
@@ -224,3 +226,28 @@ def fp8_cache_store(x, input_row_offsets, cache_lengths, block_table, kvcache):
     skipped = _load().oracle_fp8_cache_store(_ptr(xb), _ptr(offs), _ptr(lens), _ptr(bt), int(bt.shape[1]), batch,
                                               int(cache.shape[0]), int(cache.shape[1]), _ptr(cache))
     return cache, int(skipped)
+
+
+def sparse_prefill(q, kv, indices, sm_scale, rows=None, n_threads=None):
+    """Oracle sparse prefill: q [s_q, h_q, 576] bf16, kv [s_kv, 576] (or [s_kv, 1, 576]) bf16,
+    indices [s_q, topk] (or [s_q, 1, topk]) int32.  Returns (out float64, lse float64):
+    [s_q, h_q, 512] and [s_q, h_q] for all rows, else [n, 512] and [n] for the listed
+    flat rows (i * h_q + h)."""
+    lib = _load()
+    qn = _np(q, np.uint16)
+    s_q, h_q, d = qn.shape
+    assert d == D_QK
+    kvn = _np(kv, np.uint16).reshape(-1, D_QK)
+    idx = _np(indices, np.int32).reshape(s_q, -1)
+    topk = idx.shape[1]
+    all_rows = rows is None
+    r = None if all_rows else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = s_q * h_q if all_rows else r.shape[0]
+    out = np.zeros((n, D_V), np.float64)
+    lse = np.zeros((n,), np.float64)
+    nt = n_threads or os.cpu_count() or 1
+    lib.oracle_sparse_prefill(_ptr(qn), _ptr(kvn), int(kvn.shape[0]), _ptr(idx), int(topk), int(h_q),
+                              float(sm_scale), _ptr(r), int(n), _ptr(out), _ptr(lse), int(nt))
+    if all_rows:
+        return out.reshape(s_q, h_q, D_V), lse.reshape(s_q, h_q)
+    return out, lse

@@ -418,3 +418,115 @@ int64_t oracle_fp8_cache_store(const uint16_t* x, const int32_t* input_row_offse
   }
   return skipped;
 }
+
+/* ------------------------------------------------------------------------
+ * Sparse prefill ("Why FlashMLA's decode kernel reaches 660 TFLOPS", usage
+ * section: flash_mla_sparse_fwd(q, kv, indices, sm_scale)).  No batch and no
+ * paging: the single KV head is squeezed out, so kv is [s_kv, 576] bf16 and
+ * indices is [s_q, topk].  For query token i and head h, in the order the
+ * article states the computation:
+ *   1. gather: the focused rows K_k = kv[indices[i, k]], k = 0 .. topk-1;
+ *      ids outside [0, s_kv) are skipped and a repeated id counts once per
+ *      occurrence (the reading taken for sparse decode),
+ *   2. logits P_k = sm_scale * q[i, h] . K_k                    (fp64),
+ *   3. lse = log2 sum_k e^{P_k}, the base-2 log-sum-exp of the natural
+ *      logits (the article's base-2 exponentials read with the factor
+ *      log2(e) folded into the scale, as for decode),
+ *   4. S_k = e^{P_k} / sum_k' e^{P_k'}, out = sum_k S_k K_k[0:512] (V is the
+ *      first 512 dims of the gathered row, the MQA form of MLA).
+ *   No valid id: out = 0, lse = -inf.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  const uint16_t* q;
+  const uint16_t* kv;
+  int64_t s_kv;
+  const int32_t* indices;
+  int topk;
+  int h_q;
+  double sm_scale;
+  const int64_t* rows;
+  int64_t n_rows;
+  double* out;
+  double* lse;
+  int64_t next;
+  pthread_mutex_t mu;
+} prefill_job;
+
+/* Output row `row` = i * h_q + h.  p: topk logits scratch. */
+static void prefill_row(const prefill_job* j, int64_t row, double* out, double* lse, double* p) {
+  const int64_t i = row / j->h_q;
+  const uint16_t* q = j->q + row * D_QK;
+  const int32_t* idx = j->indices + i * j->topk;
+  /* steps 1-2: logits of the valid gathered rows */
+  double m = -INFINITY;
+  for (int k = 0; k < j->topk; ++k) {
+    p[k] = -INFINITY;
+    if (idx[k] < 0 || idx[k] >= j->s_kv) continue;
+    const uint16_t* kr = j->kv + (int64_t)idx[k] * D_QK;
+    double acc = 0.0;
+    for (int d = 0; d < D_QK; ++d) acc += bf16_bits_to_double(q[d]) * bf16_bits_to_double(kr[d]);
+    p[k] = j->sm_scale * acc;
+    if (p[k] > m) m = p[k];
+  }
+  for (int d = 0; d < D_V; ++d) out[d] = 0.0;
+  if (m == -INFINITY) {
+    *lse = -INFINITY;
+    return;
+  }
+  /* step 3: log-sum-exp */
+  double z = 0.0;
+  for (int k = 0; k < j->topk; ++k)
+    if (p[k] != -INFINITY) z += exp(p[k] - m);
+  *lse = (m + log(z)) / log(2.0);
+  /* step 4: softmax weights times the value dims of the gathered rows */
+  for (int k = 0; k < j->topk; ++k) {
+    if (p[k] == -INFINITY) continue;
+    const double w = exp(p[k] - m) / z;
+    const uint16_t* kr = j->kv + (int64_t)idx[k] * D_QK;
+    for (int d = 0; d < D_V; ++d) out[d] += w * bf16_bits_to_double(kr[d]);
+  }
+}
+
+static void* prefill_worker(void* arg) {
+  prefill_job* j = (prefill_job*)arg;
+  double* p = (double*)malloc(sizeof(double) * (j->topk > 0 ? j->topk : 1));
+  for (;;) {
+    pthread_mutex_lock(&j->mu);
+    int64_t r = j->next++;
+    pthread_mutex_unlock(&j->mu);
+    if (r >= j->n_rows) break;
+    const int64_t row = j->rows ? j->rows[r] : r;
+    prefill_row(j, row, j->out + r * D_V, j->lse + r, p);
+  }
+  free(p);
+  return NULL;
+}
+
+/* q [s_q, h_q, 576] bf16 bits, kv [s_kv, 576] bf16 bits, indices [s_q, topk].
+ * Computes the listed flat rows (i * h_q + h; rows == NULL: all n_rows rows
+ * in order) into out [n_rows, 512] and lse [n_rows]. */
+void oracle_sparse_prefill(const uint16_t* q, const uint16_t* kv, int64_t s_kv, const int32_t* indices,
+                           int topk, int h_q, double sm_scale, const int64_t* rows, int64_t n_rows,
+                           double* out, double* lse, int n_threads) {
+  prefill_job j;
+  memset(&j, 0, sizeof j);
+  j.q = q;
+  j.kv = kv;
+  j.s_kv = s_kv;
+  j.indices = indices;
+  j.topk = topk;
+  j.h_q = h_q;
+  j.sm_scale = sm_scale;
+  j.rows = rows;
+  j.n_rows = n_rows;
+  j.out = out;
+  j.lse = lse;
+  pthread_mutex_init(&j.mu, NULL);
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads > 256) n_threads = 256;
+  pthread_t tid[256];
+  for (int t = 1; t < n_threads; ++t) pthread_create(&tid[t], NULL, prefill_worker, &j);
+  prefill_worker(&j);
+  for (int t = 1; t < n_threads; ++t) pthread_join(tid[t], NULL);
+  pthread_mutex_destroy(&j.mu);
+}

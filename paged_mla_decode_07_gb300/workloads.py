@@ -53,11 +53,11 @@ class Workload:
     invalid_frac: float = 0.05                  # sparse: trailing fraction of each index row set to -1
     page_size: int = PAGE_SIZE
     sm_scale: Optional[float] = None            # default 1/sqrt(576)
-    fp8: bool = False                           # dense mode over the FP8 cache
+    fp8: Optional[bool] = None                  # cache format; None: FP8 for sparse, bf16 for dense
 
     @property
     def is_fp8(self) -> bool:
-        return self.mode == "sparse" or self.fp8
+        return self.fp8 if self.fp8 is not None else self.mode == "sparse"
 
     @property
     def scale(self) -> float:
@@ -80,6 +80,70 @@ WORKLOADS = {
 }
 # Seed per named workload: 1000 + its position (1-based) in the list above.
 SEEDS = {name: 1000 + i for i, name in enumerate(WORKLOADS, start=1)}
+
+
+@dataclass(frozen=True)
+class PrefillWorkload:
+    """Sparse prefill: s_q query tokens, each attending to topk rows of one
+    unpaged bf16 KV of s_kv rows (no batch dimension)."""
+    name: str
+    s_q: int
+    s_kv: int
+    h_q: int
+    topk: int
+    invalid_frac: float = 0.0                   # trailing fraction of each index row set to -1
+    sm_scale: Optional[float] = None            # default 1/sqrt(576)
+
+    @property
+    def scale(self) -> float:
+        return self.sm_scale if self.sm_scale is not None else 1.0 / math.sqrt(D_QK)
+
+
+# The prefill shape the FlashMLA article's sparse-prefill kernel is quoted on
+# is not printed; 128 heads and top-k 2048 follow its sparse decode numbers,
+# a 4096-token prefill chunk attends into a 32768-row KV.
+PREFILL_WORKLOADS = {
+    "prefill_tiny": PrefillWorkload("prefill_tiny", s_q=5, s_kv=300, h_q=16, topk=100, invalid_frac=0.1),
+    "sparse_prefill": PrefillWorkload("sparse_prefill", s_q=4096, s_kv=32768, h_q=128, topk=2048),
+}
+PREFILL_SEEDS = {name: 1100 + i for i, name in enumerate(PREFILL_WORKLOADS, start=1)}
+
+
+@dataclass
+class PrefillInputs:
+    workload: PrefillWorkload
+    q: torch.Tensor        # bf16 [s_q, h_q, 576]
+    kv: torch.Tensor       # bf16 [s_kv, 576]
+    indices: torch.Tensor  # int32 [s_q, topk]
+    sm_scale: float
+    seed: int
+
+    def to(self, device) -> "PrefillInputs":
+        return PrefillInputs(self.workload, self.q.to(device), self.kv.to(device), self.indices.to(device),
+                             self.sm_scale, self.seed)
+
+
+def make_prefill_inputs(w, seed: Optional[int] = None, device="cpu") -> PrefillInputs:
+    """q and kv ~ N(0, 1) in bf16 (torch generator on ``device``); each query
+    token's index row holds distinct ids drawn uniformly from [0, s_kv) (numpy
+    PCG64), its trailing ``invalid_frac`` part set to -1."""
+    if isinstance(w, str):
+        if seed is None:
+            seed = PREFILL_SEEDS[w]
+        w = PREFILL_WORKLOADS[w]
+    if seed is None:
+        seed = 4321
+    rng = np.random.default_rng(seed)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    q = torch.randn((w.s_q, w.h_q, D_QK), generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+    kv = torch.randn((w.s_kv, D_QK), generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+    idx = np.full((w.s_q, w.topk), -1, dtype=np.int32)
+    n_valid = min(w.topk - int(math.floor(w.invalid_frac * w.topk)), w.s_kv)
+    for i in range(w.s_q):
+        if n_valid > 0:
+            idx[i, :n_valid] = rng.choice(w.s_kv, size=n_valid, replace=False).astype(np.int32)
+    return PrefillInputs(w, q, kv, torch.from_numpy(idx).to(device), w.scale, seed)
 
 
 @dataclass

@@ -354,9 +354,9 @@ def test_named_workload_shapes():
 # mutation tests: each planted mistake must be caught by a pin above
 # ----------------------------------------------------------------------------
 MUTATIONS = {
-    "rope_dims_dropped_from_logits": ("for (int d = 0; d < D_QK; ++d) acc +=",
-                                      "for (int d = 0; d < D_V; ++d) acc +="),
-    "natural_log_lse": ("*lse = (m + log(z)) / log(2.0);", "*lse = (m + log(z));"),
+    "rope_dims_dropped_from_logits": ("for (int d = 0; d < D_QK; ++d) acc += bf16_bits_to_double(q[d]) * kbuf[d];",
+                                      "for (int d = 0; d < D_V; ++d) acc += bf16_bits_to_double(q[d]) * kbuf[d];"),
+    "natural_log_lse": ("  *lse = (m + log(z)) / log(2.0);\n  return 1;", "  *lse = (m + log(z));\n  return 1;"),
     "page_slot_swapped": ("int slot = j % p->page_size;", "int slot = (j + 1) % p->page_size;"),
     "wrong_scale_tile": ("4 * (d / 128)", "4 * (d / 256)"),
     "causal_off_by_one": ("last = L - p->s_q + i;", "last = L - p->s_q + i - 1;"),
