@@ -54,7 +54,7 @@ def algorithmic(inp) -> dict:
     if w.mode == "sparse":
         idx = inp.indices
         valid = ((idx >= 0) & (idx < inp.cache_seqlens.view(-1, 1, 1))).sum().item()
-        kv_bytes = valid * FP8_ROW
+        kv_bytes = valid * (FP8_ROW if w.is_fp8 else D_QK * 2)
         flops = 2.0 * w.h_q * w.s_q * w.topk * w.batch * (D_QK + D_V)
         vflops = 2.0 * w.h_q * valid * (D_QK + D_V)
         tab = idx.numel() * 4 + inp.block_table.numel() * 4
@@ -321,6 +321,28 @@ def measure_store(device, peaks, batch=32, new_tokens=4096, reps=20):
             "bytes_per_token": D_QK * 2 + FP8_ROW}
 
 
+def measure_prefill(device, peaks, reps=10):
+    """Sparse prefill (mla_sparse_prefill) on the named prefill workload: TFLOPS nominal
+    (2 * h_q * s_q * topk * 1088) and valid-only, fraction of the measured bf16 peak."""
+    import paged_mla_decode_07_gb300 as mla
+    inp = W.make_prefill_inputs("sparse_prefill", device=device)
+    w = inp.workload
+    out = torch.empty((w.s_q, w.h_q, D_V), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((w.s_q, w.h_q), dtype=torch.float32, device=device)
+    ws = torch.empty(mla.sparse_prefill_workspace_size(w.s_q, w.h_q, w.topk), dtype=torch.uint8, device=device)
+    fn = lambda: mla.sparse_prefill(inp.q, inp.kv, inp.indices, inp.sm_scale, out=out, lse=lse, workspace=ws)
+    for _ in range(3):
+        fn()
+    ms = statistics.median(time_events(fn, reps))
+    valid = int(((inp.indices >= 0) & (inp.indices < w.s_kv)).sum().item())
+    flops = 2.0 * w.h_q * w.s_q * w.topk * (D_QK + D_V)
+    vflops = 2.0 * w.h_q * valid * (D_QK + D_V)
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"ms": round(ms, 4), "tflops": round(tf, 2), "tflops_valid": round(vflops / (ms * 1e-3) / 1e12, 2),
+            "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+            "shape": f"s_q {w.s_q}, s_kv {w.s_kv}, h_q {w.h_q}, topk {w.topk}"}
+
+
 def max_over_ranks(x: float, device) -> float:
     """The largest x over all ranks of the default process group (x itself without one)."""
     import torch.distributed as dist
@@ -434,7 +456,8 @@ def run_mla(args):
         torch.cuda.empty_cache()
         # ---- the other workloads (kernel level)
         extra = {}
-        for name in ("tiny", "dense_computebound", "sparse_fp8", "sparse_fp8_long", "dense_membound_fp8"):
+        for name in ("tiny", "dense_computebound", "sparse_fp8", "sparse_fp8_long", "dense_membound_fp8",
+                     "sparse_bf16"):
             winp, wa, wms, st = measure_workload(name, device)
             bound = "hbm" if name in ("tiny", "dense_membound_fp8") else "tensor"
             e = {"ms": round(wms, 5), "tflops": round(wa["flops"] / (wms * 1e-3) / 1e12, 2),
@@ -448,6 +471,7 @@ def run_mla(args):
             del st, winp
             torch.cuda.empty_cache()
         extra["fp8_cache_store"] = measure_store(device, peaks)
+        extra["sparse_prefill"] = measure_prefill(device, peaks)
         result["workloads"] = extra
         # ---- the oracle on the host cores, bounded sample
         result["cpu_baseline"] = cpu_baseline(inp, target_s=args.cpu_seconds)

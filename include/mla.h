@@ -82,16 +82,20 @@ mla_status mla_metadata_size(int batch, int s_q, int h_q, int topk, int* sched_e
                              int* num_splits_elems);
 
 /* Scratch bytes that mla_decode needs for split-KV partial results
- * (fp32 partial outputs and their log-sum-exps). */
+ * (fp32 partial outputs and their log-sum-exps): min(2 * parts,
+ * problems + parts) slots of rows x 513 floats, bounded by the part count
+ * whatever the batch size. */
 mla_status mla_workspace_size(int batch, int s_q, int h_q, int topk, size_t* bytes);
 
 /* (1) Tile schedule for one decode step ("get_mla_metadata").
  * cache_seqlens: device int32 [batch]; sched, num_splits: device int32
  * buffers of the sizes above, written on `stream`.  The work of all problems
- * (128-token tiles of their key ranges) is divided into contiguous ranges of
+ * (64-token tiles of their key ranges) is divided into contiguous ranges of
  * near-equal cost, one per part; num_splits holds the exclusive prefix sum of
- * the number of parts that touch each problem.  Reusable by every layer of
- * the step as long as cache_seqlens, batch, s_q, h_q and topk are unchanged. */
+ * the split-KV partial-result slots of each problem: as many as the parts
+ * touching it when there are two or more, none when one part covers it
+ * (that part writes the output directly).  Reusable by every layer of the
+ * step as long as cache_seqlens, batch, s_q, h_q and topk are unchanged. */
 mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, int h_q, int topk,
                             int32_t* sched, int32_t* num_splits, mla_stream_t stream);
 
@@ -106,7 +110,7 @@ typedef struct {
   const int32_t* cache_seqlens;   /* int32 [batch] */
   float sm_scale;                 /* softmax scale applied to q.k */
   int is_causal;                  /* dense only: query token i sees keys <= seqlen - s_q + i */
-  int is_fp8;                     /* 1: FP8 656-byte cache (sparse mode only) */
+  int is_fp8;                     /* 1: FP8 656-byte cache rows, 0: bf16 576-value rows (either mode) */
   const int32_t* indices;         /* sparse: int32 [batch, s_q, topk]; NULL for dense */
   int topk;                       /* 0 for dense */
   const int32_t* sched;           /* from mla_get_metadata with the same batch/s_q/h_q/topk */
@@ -164,6 +168,40 @@ mla_status mla_fp8_cache_store(const void* x, int num_tokens, const int32_t* inp
                                const int32_t* cache_lengths, int batch, const int32_t* block_table,
                                int block_table_stride, void* kvcache, int num_pages, int page_size,
                                mla_stream_t stream);
+
+/* Sparse prefill ("flash_mla_sparse_fwd(q, kv, indices, sm_scale)" of the
+ * FlashMLA article's usage section): token-level sparse attention with no
+ * batch dimension and an unpaged bf16 KV with one head.  For query token i
+ * and head h the rows kv[indices[i, k]] are gathered (ids outside [0, s_kv)
+ * are skipped, a repeated id counts once per occurrence), logits
+ * s_k = sm_scale * q[i, h] . kv[id_k], and
+ *   out[i, h] = sum_k softmax(s)_k kv[id_k][0:512],   lse[i, h] = log2 sum_k e^{s_k}
+ * (base-2 log-sum-exp of the natural logits; no valid id: out = 0,
+ * lse = -inf).  The same computation as sparse decode with one batch element
+ * whose cache is the KV itself; the library runs its decode kernels on
+ * chunks of at most 16384 query tokens. */
+typedef struct {
+  const void* q;                  /* bf16 [s_q, h_q, 576], 16-byte aligned */
+  int s_q, h_q;                   /* h_q <= 1024 */
+  const void* kv;                 /* bf16 [s_kv, 576] (the single KV head squeezed out), 16-byte aligned */
+  int s_kv;
+  const int32_t* indices;         /* int32 [s_q, topk] */
+  int topk;                       /* >= 1 */
+  float sm_scale;
+  void* workspace;                /* >= mla_sparse_prefill_workspace_size() bytes, 256-byte aligned */
+  size_t workspace_bytes;
+  void* out;                      /* bf16 [s_q, h_q, 512], 16-byte aligned */
+  float* lse;                     /* fp32 [s_q, h_q] */
+} mla_sparse_prefill_args;
+
+/* Scratch bytes for mla_sparse_prefill: one chunk's schedule and split-KV
+ * partials (independent of s_q beyond the first 16384 tokens). */
+mla_status mla_sparse_prefill_workspace_size(int s_q, int h_q, int topk, size_t* bytes);
+
+/* Asynchronous on `stream`; all pointers are device pointers owned by the
+ * caller.  Host-side argument errors return without launching; device-side
+ * problems set bits in the device status word (mla_get_device_status). */
+mla_status mla_sparse_prefill(const mla_sparse_prefill_args* args, mla_stream_t stream);
 
 /* Synchronises `stream`, returns the device status bits accumulated since the
  * last call in *flags (0 = clean) and clears them.  Returns

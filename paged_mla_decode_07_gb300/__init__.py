@@ -10,6 +10,7 @@ code path.  If ``libmla.so`` has not been built, every call raises.
     sched, num_splits = get_metadata(cache_seqlens, s_q, h_q, topk)
     out, lse = decode(q, kvcache, block_table, cache_seqlens, sm_scale,
                       sched, num_splits, is_causal=..., indices=...)
+    out, lse = sparse_prefill(q, kv, indices, sm_scale)
 """
 from __future__ import annotations
 
@@ -57,6 +58,17 @@ class DecodeArgs(ctypes.Structure):
     ]
 
 
+class SparsePrefillArgs(ctypes.Structure):
+    """Mirror of ``mla_sparse_prefill_args`` in include/mla.h."""
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("s_q", ctypes.c_int), ("h_q", ctypes.c_int),
+        ("kv", ctypes.c_void_p), ("s_kv", ctypes.c_int),
+        ("indices", ctypes.c_void_p), ("topk", ctypes.c_int), ("sm_scale", ctypes.c_float),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+    ]
+
+
 def library_path() -> str:
     return _build.LIB
 
@@ -85,6 +97,10 @@ def lib():
             L.mla_fp8_cache_store.argtypes = [P, I, P, P, I, P, I, P, I, I, P]
             L.mla_fp8_cache_store.restype = I
             L.mla_get_device_status.restype = I
+            L.mla_sparse_prefill_workspace_size.argtypes = [I, I, I, ctypes.POINTER(S)]
+            L.mla_sparse_prefill_workspace_size.restype = I
+            L.mla_sparse_prefill.argtypes = [ctypes.POINTER(SparsePrefillArgs), P]
+            L.mla_sparse_prefill.restype = I
             _lib = L
     return _lib
 
@@ -245,6 +261,66 @@ def fp8_cache_store(x: torch.Tensor, input_row_offsets: torch.Tensor, cache_leng
                                      cache_lengths.data_ptr(), batch, block_table.data_ptr(),
                                      block_table.shape[1], kvcache.data_ptr(), kvcache.shape[0], kvcache.shape[1],
                                      _stream(stream)))
+
+
+def sparse_prefill_workspace_size(s_q: int, h_q: int, topk: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().mla_sparse_prefill_workspace_size(s_q, h_q, topk, ctypes.byref(n)))
+    return n.value
+
+
+def sparse_prefill(q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor, sm_scale: float,
+                   out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None, stream=None):
+    """Sparse prefill (mla_sparse_prefill).  q bf16 [s_q, h_q, 576]; kv bf16 [s_kv, 576] or
+    [s_kv, 1, 576]; indices int32 [s_q, topk] or [s_q, 1, topk].  Returns (out bf16
+    [s_q, h_q, 512], lse fp32 [s_q, h_q], base 2)."""
+    if not torch.is_tensor(q) or q.device.type != "cuda":
+        raise ValueError("q must be a CUDA tensor")
+    dev = q.device
+    _need(q, "q", torch.bfloat16, dev, 3)
+    s_q, h_q, d = q.shape
+    if d != D_QK:
+        raise ValueError(f"q must have last dimension {D_QK} (got {d})")
+    _need(kv, "kv", torch.bfloat16, dev)
+    if kv.dim() == 3:
+        if kv.shape[1] != 1:
+            raise ValueError(f"kv must have one KV head (got {tuple(kv.shape)})")
+        kv = kv.view(kv.shape[0], kv.shape[2])
+    if kv.dim() != 2 or kv.shape[1] != D_QK:
+        raise ValueError(f"kv must be [s_kv, {D_QK}] (got {tuple(kv.shape)})")
+    _need(indices, "indices", torch.int32, dev)
+    if indices.dim() == 3:
+        if indices.shape[1] != 1:
+            raise ValueError(f"indices must have one KV head (got {tuple(indices.shape)})")
+        indices = indices.view(indices.shape[0], indices.shape[2])
+    if indices.dim() != 2 or indices.shape[0] != s_q:
+        raise ValueError(f"indices must be [s_q, topk] (got {tuple(indices.shape)})")
+    topk = indices.shape[1]
+    if out is None:
+        out = torch.empty((s_q, h_q, D_V), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((s_q, h_q), dtype=torch.float32, device=dev)
+    _need(out, "out", torch.bfloat16, dev)
+    _need(lse, "lse", torch.float32, dev)
+    if out.numel() != s_q * h_q * D_V or lse.numel() != s_q * h_q:
+        raise ValueError("out / lse have the wrong size")
+    if workspace is None:
+        workspace = torch.empty(sparse_prefill_workspace_size(s_q, h_q, topk), dtype=torch.uint8, device=dev)
+    a = SparsePrefillArgs()
+    a.q = q.data_ptr()
+    a.s_q, a.h_q = s_q, h_q
+    a.kv = kv.data_ptr()
+    a.s_kv = kv.shape[0]
+    a.indices = indices.data_ptr()
+    a.topk = topk
+    a.sm_scale = float(sm_scale)
+    a.workspace = workspace.data_ptr()
+    a.workspace_bytes = workspace.numel() * workspace.element_size()
+    a.out = out.data_ptr()
+    a.lse = lse.data_ptr()
+    _check(lib().mla_sparse_prefill(ctypes.byref(a), _stream(stream)))
+    return out.view(s_q, h_q, D_V), lse.view(s_q, h_q)
 
 
 def device_status(stream=None, raise_on_error: bool = False) -> int:

@@ -111,8 +111,15 @@ mla_status geometry(int batch, int s_q, int h_q, int topk, Geometry* g) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Partial-result slots: only split problems take slots, at most two per part
+// (see the metadata kernel), independent of the number of problems.
+int max_slots(const Geometry& g) {
+  // also at most one piece per problem plus one per part boundary
+  return g.num_problems + g.num_parts < 2 * g.num_parts ? g.num_problems + g.num_parts : 2 * g.num_parts;
+}
+
 void workspace_layout(const Geometry& g, size_t* o_bytes, size_t* lse_bytes) {
-  const size_t slots = static_cast<size_t>(g.num_problems) + g.num_parts;
+  const size_t slots = static_cast<size_t>(max_slots(g));
   *o_bytes = align256(slots * g.rows * kDv * sizeof(float));
   *lse_bytes = align256(slots * g.rows * sizeof(float));
 }
@@ -150,21 +157,22 @@ mla_status encode_rows_map(CUtensorMap* map, const void* base, long long nrows, 
   return MLA_OK;
 }
 
-// The FP8 cache as [rows][656] bytes (row = page * 64 + slot).  A box is 128
-// bytes of box_rows rows: one row for the sparse row gathers (as row gathers
-// require), 32 consecutive rows of a page for dense decode over the FP8
-// cache; no swizzle: the rows land as plain 128-byte rows.
-mla_status encode_fp8_rows_map(CUtensorMap* map, const void* base, long long nrows, int box_rows) {
+// Cache rows as raw bytes, [rows][row_bytes] (row = page * 64 + slot, or the
+// row of an unpaged KV): FP8 rows (656 bytes) or bf16 rows (1152 bytes).  A
+// box is 128 bytes of box_rows rows: one row for the sparse row gathers (as
+// row gathers require), 32 consecutive rows of a page for dense decode over
+// the FP8 cache; no swizzle: the rows land as plain 128-byte rows.
+mla_status encode_byte_rows_map(CUtensorMap* map, const void* base, long long nrows, int row_bytes, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kFp8RowBytes), static_cast<cuuint64_t>(nrows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kFp8RowBytes)};
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(nrows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
   cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled(fp8 kvcache) failed with CUresult %d", (int)r);
+  if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled(kv rows) failed with CUresult %d", (int)r);
   return MLA_OK;
 }
 
@@ -186,6 +194,28 @@ void set_error_message(const std::string& msg) { g_error = msg; }
 }  // namespace mla
 
 using namespace mla;
+
+// Sparse prefill runs the decode pipeline (schedule, attention, combine) on
+// chunks of at most kMaxProblems query tokens; the workspace holds one
+// chunk's schedule, slot prefix sums and split-KV partials.
+namespace {
+struct PrefillLayout {
+  size_t sched, num_splits, o_accum, lse_accum, total;
+};
+mla_status prefill_layout(int s_q, int h_q, int topk, Geometry* g, PrefillLayout* L) {
+  const int chunk = s_q < kMaxProblems ? s_q : kMaxProblems;
+  mla_status st = geometry(1, chunk, h_q, topk, g);
+  if (st != MLA_OK) return st;
+  size_t ob, lb;
+  workspace_layout(*g, &ob, &lb);
+  L->sched = 0;
+  L->num_splits = align256(static_cast<size_t>(g->num_parts) * kSchedInts * sizeof(int32_t));
+  L->o_accum = L->num_splits + align256(static_cast<size_t>(chunk + 1) * sizeof(int32_t));
+  L->lse_accum = L->o_accum + ob;
+  L->total = L->lse_accum + lb;
+  return MLA_OK;
+}
+}  // namespace
 
 extern "C" {
 
@@ -253,8 +283,6 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
     return fail(MLA_ERR_UNSUPPORTED, "num_pages = %d exceeds 2^31 tokens", a->num_pages);
   if (a->block_table_stride < 1)
     return fail(MLA_ERR_INVALID_ARG, "block_table_stride must be >= 1 (got %d)", a->block_table_stride);
-  if (!a->is_fp8 && sparse)
-    return fail(MLA_ERR_UNSUPPORTED, "sparse mode (topk > 0) requires the FP8 cache (is_fp8 = 1)");
   if (a->is_causal && sparse) return fail(MLA_ERR_UNSUPPORTED, "is_causal applies to dense mode only");
   if (!std::isfinite(a->sm_scale)) return fail(MLA_ERR_INVALID_ARG, "sm_scale is not finite");
   if (!aligned(a->q, 16)) return fail(MLA_ERR_INVALID_ARG, "q is not 16-byte aligned");
@@ -282,17 +310,16 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
   st = encode_rows_map(&tm_q, a->q, qrows, g.rpc, "q");
   if (st != MLA_OK) return st;
   // kernel mode: 0 dense over the bf16 cache, 1 sparse over the FP8 cache,
-  // 2 dense over the FP8 cache
-  const int mode = sparse ? 1 : (a->is_fp8 ? 2 : 0);
-  if (mode == 0) {
-    st = encode_rows_map(&tm_kv, a->kvcache, static_cast<long long>(a->num_pages) * kPageSize, kPageSize,
-                         "kvcache");
-    if (st != MLA_OK) return st;
-  } else {
-    st = encode_fp8_rows_map(&tm_kv, a->kvcache, static_cast<long long>(a->num_pages) * kPageSize,
-                             mode == 1 ? 1 : 32);
-    if (st != MLA_OK) return st;
-  }
+  // 2 dense over the FP8 cache, 3 sparse over the bf16 cache
+  const int mode = sparse ? (a->is_fp8 ? 1 : 3) : (a->is_fp8 ? 2 : 0);
+  const long long cache_rows = static_cast<long long>(a->num_pages) * kPageSize;
+  if (mode == 0)
+    st = encode_rows_map(&tm_kv, a->kvcache, cache_rows, kPageSize, "kvcache");
+  else if (mode == 3)
+    st = encode_byte_rows_map(&tm_kv, a->kvcache, cache_rows, 2 * kDqk, 1);
+  else
+    st = encode_byte_rows_map(&tm_kv, a->kvcache, cache_rows, kFp8RowBytes, mode == 1 ? 1 : 32);
+  if (st != MLA_OK) return st;
 
   DecodeParams p;
   memset(&p, 0, sizeof p);
@@ -318,7 +345,7 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
   p.rows = g.rows;
   p.row_groups = g.row_groups;
   p.num_parts = g.num_parts;
-  p.max_slots = g.num_problems + g.num_parts;
+  p.max_slots = max_slots(g);
   p.is_causal = a->is_causal ? 1 : 0;
   p.evict_first = g.row_groups == 1 ? 1 : 0;
   {
@@ -333,6 +360,9 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
 
   CombineParams cp;
   cp.num_splits = a->num_splits;
+  cp.cache_seqlens = a->cache_seqlens;
+  cp.s_q = a->s_q;
+  cp.topk = a->topk;
   cp.o_accum = p.o_accum;
   cp.lse_accum = p.lse_accum;
   cp.out = a->out;
@@ -371,6 +401,112 @@ mla_status mla_fp8_cache_store(const void* x, int num_tokens, const int32_t* inp
                                          cache_lengths, batch, block_table, block_table_stride,
                                          static_cast<uint8_t*>(kvcache), num_pages, status, sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "fp8 cache store launch");
+  return ok();
+}
+
+mla_status mla_sparse_prefill_workspace_size(int s_q, int h_q, int topk, size_t* bytes) {
+  if (!bytes) return fail(MLA_ERR_INVALID_ARG, "bytes is NULL");
+  if (topk < 1) return fail(MLA_ERR_INVALID_ARG, "topk must be >= 1 (got %d)", topk);
+  Geometry g{};
+  PrefillLayout L{};
+  mla_status st = prefill_layout(s_q, h_q, topk, &g, &L);
+  if (st != MLA_OK) return st;
+  *bytes = L.total;
+  return ok();
+}
+
+mla_status mla_sparse_prefill(const mla_sparse_prefill_args* a, mla_stream_t stream) {
+  if (!a) return fail(MLA_ERR_INVALID_ARG, "args is NULL");
+  if (!a->q) return fail(MLA_ERR_INVALID_ARG, "q is NULL");
+  if (!a->kv) return fail(MLA_ERR_INVALID_ARG, "kv is NULL");
+  if (!a->indices) return fail(MLA_ERR_INVALID_ARG, "indices is NULL");
+  if (!a->out) return fail(MLA_ERR_INVALID_ARG, "out is NULL");
+  if (!a->lse) return fail(MLA_ERR_INVALID_ARG, "lse is NULL");
+  if (a->s_q < 1) return fail(MLA_ERR_INVALID_ARG, "s_q must be >= 1 (got %d)", a->s_q);
+  if (a->s_kv < 1) return fail(MLA_ERR_INVALID_ARG, "s_kv must be >= 1 (got %d)", a->s_kv);
+  if (a->topk < 1) return fail(MLA_ERR_INVALID_ARG, "topk must be >= 1 (got %d)", a->topk);
+  if (!std::isfinite(a->sm_scale)) return fail(MLA_ERR_INVALID_ARG, "sm_scale is not finite");
+  if (!aligned(a->q, 16)) return fail(MLA_ERR_INVALID_ARG, "q is not 16-byte aligned");
+  if (!aligned(a->kv, 16)) return fail(MLA_ERR_INVALID_ARG, "kv is not 16-byte aligned");
+  if (!aligned(a->out, 16)) return fail(MLA_ERR_INVALID_ARG, "out is not 16-byte aligned");
+  if (!aligned(a->lse, 4)) return fail(MLA_ERR_INVALID_ARG, "lse is not 4-byte aligned");
+  if (!aligned(a->indices, 4)) return fail(MLA_ERR_INVALID_ARG, "indices is not 4-byte aligned");
+  Geometry g{};
+  PrefillLayout L{};
+  mla_status st = prefill_layout(a->s_q, a->h_q, a->topk, &g, &L);
+  if (st != MLA_OK) return st;
+  if (!a->workspace) return fail(MLA_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", L.total);
+  if (a->workspace_bytes < L.total)
+    return fail(MLA_ERR_WORKSPACE, "workspace_bytes = %zu < %zu needed", a->workspace_bytes, L.total);
+  if (!aligned(a->workspace, 256)) return fail(MLA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  uint32_t* status = nullptr;
+  st = device_info(&status, nullptr);
+  if (st != MLA_OK) return st;
+
+  char* ws = static_cast<char*>(a->workspace);
+  int32_t* sched = reinterpret_cast<int32_t*>(ws + L.sched);
+  int32_t* num_splits = reinterpret_cast<int32_t*>(ws + L.num_splits);
+  CUtensorMap tm_kv;
+  st = encode_byte_rows_map(&tm_kv, a->kv, a->s_kv, 2 * kDqk, 1);
+  if (st != MLA_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint64_t timeout = watchdog_ns();
+  for (int c0 = 0; c0 < a->s_q; c0 += kMaxProblems) {
+    const int chunk = a->s_q - c0 < kMaxProblems ? a->s_q - c0 : kMaxProblems;
+    Geometry gc{};
+    st = geometry(1, chunk, a->h_q, a->topk, &gc);
+    if (st != MLA_OK) return st;
+    const char* q = static_cast<const char*>(a->q) + static_cast<size_t>(c0) * a->h_q * kDqk * 2;
+    CUtensorMap tm_q;
+    st = encode_rows_map(&tm_q, q, static_cast<long long>(chunk) * a->h_q, gc.rpc, "q");
+    if (st != MLA_OK) return st;
+    cudaError_t e = launch_metadata(nullptr, 1, chunk, a->h_q, a->topk, gc, sched, num_splits, status, s);
+    if (e != cudaSuccess) return cuda_fail(e, "metadata kernel launch");
+
+    DecodeParams p;
+    memset(&p, 0, sizeof p);
+    p.indices = a->indices + static_cast<size_t>(c0) * a->topk;
+    p.sched = sched;
+    p.num_splits = num_splits;
+    p.kv_fp8 = static_cast<const uint8_t*>(a->kv);
+    p.out = static_cast<char*>(a->out) + static_cast<size_t>(c0) * a->h_q * kDv * 2;
+    p.lse = a->lse + static_cast<size_t>(c0) * a->h_q;
+    p.o_accum = reinterpret_cast<float*>(ws + L.o_accum);
+    p.lse_accum = reinterpret_cast<float*>(ws + L.lse_accum);
+    p.status = status;
+    p.timeout_ns = timeout;
+    p.batch = 1;
+    p.s_q = chunk;
+    p.h_q = a->h_q;
+    p.topk = a->topk;
+    p.num_pages = 1;
+    p.block_table_stride = 1;
+    p.num_problems = gc.num_problems;
+    p.rows = gc.rows;
+    p.row_groups = gc.row_groups;
+    p.num_parts = gc.num_parts;
+    p.max_slots = max_slots(gc);
+    p.evict_first = gc.row_groups == 1 ? 1 : 0;
+    p.flat_rows = a->s_kv;
+    p.scale_log2 = a->sm_scale * 1.4426950408889634f;
+    e = launch_decode(tm_q, tm_kv, p, gc.rpc, 3, s);
+    if (e != cudaSuccess) return cuda_fail(e, "sparse prefill attention kernel launch");
+    CombineParams cp;
+    cp.num_splits = num_splits;
+    cp.cache_seqlens = nullptr;
+    cp.s_q = chunk;
+    cp.topk = a->topk;
+    cp.o_accum = p.o_accum;
+    cp.lse_accum = p.lse_accum;
+    cp.out = p.out;
+    cp.lse = p.lse;
+    cp.num_problems = gc.num_problems;
+    cp.rows = gc.rows;
+    cp.max_slots = p.max_slots;
+    cp.status = status;
+    e = launch_combine(cp, s, true);
+    if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
+  }
   return ok();
 }
 

@@ -28,8 +28,18 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) combine_kernel(const Combi
   const int r = static_cast<int>(grow % p.rows);
   const int base = p.num_splits[prob];
   const int n = p.num_splits[prob + 1] - base;
-  if (n == 1) return;  // written directly by the decode kernel
-  if (base < 0 || n < 0 || base + n > p.max_slots) {
+  if (n == 0) {
+    // a single piece wrote the output directly; a problem without any tile
+    // (no keys) was touched by no part: its output is 0, its lse -inf
+    if (problem_tiles(p.cache_seqlens, prob, p.s_q, p.topk) > 0) return;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + grow * kDv + lane * 16;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(out)[0] = z;
+    reinterpret_cast<uint4*>(out)[1] = z;
+    if (lane == 0) p.lse[grow] = -__int_as_float(0x7f800000);
+    return;
+  }
+  if (base < 0 || n < 2 || base + n > p.max_slots) {
     if (lane == 0) atomicOr(p.status, MLA_DEVICE_BAD_SCHEDULE);
     return;
   }

@@ -83,15 +83,18 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 2^8 before a max 
 constexpr uint32_t kSoftmaxBar = 1;        // named barrier of the 128 softmax threads
 
 // Kernel modes: dense decode over the bf16 cache, sparse (top-k) decode over
-// the FP8 cache, dense decode over the FP8 cache.
-constexpr int kModeDense = 0, kModeSparse = 1, kModeDenseFp8 = 2;
+// the FP8 cache, dense decode over the FP8 cache, sparse over bf16 rows (the
+// paged bf16 cache, or an unpaged KV for sparse prefill).
+constexpr int kModeDense = 0, kModeSparse = 1, kModeDenseFp8 = 2, kModeSparseBf16 = 3;
 
 template <int R, int MODE>
 struct Cfg {
-  // FP8 rows are gathered and dequantised by four extra warps; sparse
+  // Rows other than whole bf16 pages are gathered by four extra warps (FP8
+  // rows dequantised, bf16 rows put into the swizzled operand layout); sparse
   // problems are (batch element, query token) pairs with their own indices
   static constexpr bool kGather = MODE != kModeDense;
-  static constexpr bool kIndexed = MODE == kModeSparse;
+  static constexpr bool kIndexed = MODE == kModeSparse || MODE == kModeSparseBf16;
+  static constexpr bool kFp8 = MODE == kModeSparse || MODE == kModeDenseFp8;
   // softmax warpgroups: with 64 rows two warpgroups split the rows
   static constexpr int kSmWG = (R == 64) ? 2 : 1;
   static constexpr int kGatherWarp0 = 4 + 4 * kSmWG;  // sparse: first FP8 gather warp
@@ -523,7 +526,8 @@ done:
 }
 
 // ---------------------------------------------------------------------------
-// FP8 gather + dequantisation (sparse, 128 threads, two per token)
+// row gathers (128 threads, two per token): FP8 rows are dequantised, bf16
+// rows only put into the swizzled operand layout
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t dequant2(uint32_t codes16, float scale) {
   const uint32_t h2 = e4m3x2_to_f16x2(static_cast<uint16_t>(codes16));
@@ -532,13 +536,31 @@ __device__ __forceinline__ uint32_t dequant2(uint32_t codes16, float scale) {
   return pack_bf16x2(lo * scale, hi * scale);
 }
 
+// Permute one 128-byte row of a chunk, copied in plain order, into the
+// 128-byte swizzle (unit u of row t goes to unit u ^ (t & 7)) in place; an
+// invalid token's row becomes zeros.
+__device__ __forceinline__ void swizzle_row_in_place(uint32_t row_addr, uint32_t tsw, bool ok) {
+  uint4 raw[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) raw[k] = ld_shared_v4(row_addr + ((k ^ tsw) << 4));
+  // raw[k] holds unit k ^ tsw, whose swizzled position is (k ^ tsw) ^ tsw = k
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint4 v = ok ? raw[k] : make_uint4(0, 0, 0, 0);
+    st_shared_v4(row_addr + (k << 4), v.x, v.y, v.z, v.w);
+  }
+}
+
 template <int R, int MODE>
-__device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, const Segments& sg, uint8_t* kv,
-                           const Bars& bars, volatile uint8_t* flags, const Watchdog& wd) {
+__device__ void gather_rows(const CUtensorMap* tm_rows, const DecodeParams& p, const Segments& sg, uint8_t* kv,
+                            const Bars& bars, volatile uint8_t* flags, const Watchdog& wd) {
   using C = Cfg<R, MODE>;
   using RG = Ring<C>;
   // 128 threads, two per token: half h = 0 (warps 0, 1) converts value blocks
   // 0 and 1 and the RoPE dims, half 1 (warps 2, 3) value blocks 2 and 3.
+  // FP8 rows: a block's 128 codes land in the upper chunk of its pair slot
+  // and are dequantised into both chunks.  bf16 rows: both chunks of a block
+  // are copied as plain 128-byte rows and permuted into the swizzle in place.
   // Software-pipelined: the rows of tile jt+1 are looked up (dependent index
   // and block-table loads) before tile jt is dequantised, and tile jt+1's row
   // gathers are issued right after, so lookups overlap conversion and gather
@@ -576,17 +598,21 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
   auto lookup = [&](const It& it, int& row, bool& ok, uint2& sc) {
     if (C::kIndexed) {
       const int b = it.prob / p.s_q;
-      const int L = sg.seqlens[b];
+      const int L = p.flat_rows > 0 ? p.flat_rows : sg.seqlens[b];
       const int k = it.j * kTileTokens + tok;
       const int t = k < p.topk ? p.indices[static_cast<int64_t>(it.prob) * p.topk + k] : -1;
       ok = t >= 0 && t < L;
-      const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
-      const int page = (ok && (t >> 6) < p.block_table_stride) ? bt[t >> 6] : -1;
-      if (ok && (page < 0 || page >= p.num_pages)) {
-        ok = false;
-        if (h == 0) atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
+      if (p.flat_rows > 0) {
+        row = ok ? t : 0;  // unpaged KV: the index is the row
+      } else {
+        const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
+        const int page = (ok && (t >> 6) < p.block_table_stride) ? bt[t >> 6] : -1;
+        if (ok && (page < 0 || page >= p.num_pages)) {
+          ok = false;
+          if (h == 0) atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
+        }
+        row = ok ? page * kPageSize + (t & 63) : 0;
       }
-      row = ok ? page * kPageSize + (t & 63) : 0;
     } else {
       // dense: tile j is page j of the element; row = page * 64 + token, with
       // page 0 standing in for an unusable page (its tokens are written as zeros)
@@ -598,18 +624,23 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
       ok = page_ok && it.j * kTileTokens + tok < L;
       row = (page_ok ? page : 0) * kPageSize + tok;
     }
-    sc = ok ? __ldg(reinterpret_cast<const uint2*>(p.kv_fp8 + static_cast<int64_t>(row) * kFp8RowBytes +
-                                                   kFp8ScaleOffset + 8 * h))
-            : make_uint2(0, 0);
+    if (C::kFp8)
+      sc = ok ? __ldg(reinterpret_cast<const uint2*>(p.kv_fp8 + static_cast<int64_t>(row) * kFp8RowBytes +
+                                                     kFp8ScaleOffset + 8 * h))
+              : make_uint2(0, 0);
+    else
+      sc = make_uint2(0, 0);
   };
-  // issue the row gathers of tile jt (codes of this half's blocks into the
-  // upper chunks of their pair slots; half 0 also the RoPE bytes)
+  // issue the row gathers of tile jt (FP8: codes of this half's blocks into
+  // the upper chunks of their pair slots; bf16: both chunks of each block;
+  // half 0 also the RoPE bytes).  A 4-row gather covers tokens g4 .. g4 + 3.
   auto issue = [&](int jt, int row, bool ok) -> bool {
-    const int g4 = wtok + 4 * (lane & 7);
-    const int r0 = __shfl_sync(0xffffffffu, row, (4 * lane) & 31);
-    const int r1 = __shfl_sync(0xffffffffu, row, (4 * lane + 1) & 31);
-    const int r2 = __shfl_sync(0xffffffffu, row, (4 * lane + 2) & 31);
-    const int r3 = __shfl_sync(0xffffffffu, row, (4 * lane + 3) & 31);
+    const int gl = lane & 7;
+    const int g4 = wtok + 4 * gl;
+    const int r0 = __shfl_sync(0xffffffffu, row, 4 * gl);
+    const int r1 = __shfl_sync(0xffffffffu, row, 4 * gl + 1);
+    const int r2 = __shfl_sync(0xffffffffu, row, 4 * gl + 2);
+    const int r3 = __shfl_sync(0xffffffffu, row, 4 * gl + 3);
     const int set = 5 * (jt & 1);
 #pragma unroll 1
     for (int i = 0; i < 2; ++i) {
@@ -617,11 +648,18 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
       const uint32_t use = RG::pair_use(jt, blk);
       if (use > 0 && !warp_wait(bars.pair_empty + RG::pair_slot(jt, blk), (use - 1) & 1, wd)) return false;
       if (blk == 0) flags[(jt & 1) * 128 + tok] = ok ? 1 : 0;  // token validity for the softmax
-      if (lane == 0) mbar_arrive_expect_tx(bars.raw_full + set + blk, 32 * 128);
+      if (lane == 0) mbar_arrive_expect_tx(bars.raw_full + set + blk, (C::kFp8 ? 1 : 2) * 32 * 128);
       armed |= 1u << (set + blk);
       next_par ^= 1u << (set + blk);
       __syncwarp();
-      if (C::kIndexed) {
+      if (!C::kFp8) {
+        // bf16 rows: lanes 0..7 chunk 2 blk, lanes 8..15 chunk 2 blk + 1
+        if (lane < 16) {
+          const int c = 2 * blk + (lane >> 3);
+          uint8_t* dst = kv + RG::chunk_off(jt, c) + g4 * 128;
+          tma_gather4(dst, tm_rows, bars.raw_full + set + blk, 128 * c, r0, r1, r2, r3, pol);
+        }
+      } else if (C::kIndexed) {
         if (lane < 8) {
           uint8_t* dst = kv + RG::chunk_off(jt, 2 * blk + 1) + g4 * 128;
           tma_gather4(dst, tm_rows, bars.raw_full + set + blk, 128 * blk, r0, r1, r2, r3, pol);
@@ -642,7 +680,8 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
       if (C::kIndexed) {
         if (lane < 8) {
           uint8_t* dst = kv + RG::chunk_off(jt, 8) + g4 * 128;
-          tma_gather4(dst, tm_rows, bars.raw_full + set + 4, kFp8RopeOffset, r0, r1, r2, r3, pol);
+          tma_gather4(dst, tm_rows, bars.raw_full + set + 4, C::kFp8 ? kFp8RopeOffset : 2 * kDv, r0, r1, r2, r3,
+                      pol);
         }
       } else if (lane == 0) {
         tma_load_2d(kv + RG::chunk_off(jt, 8) + wtok * 128, tm_rows, bars.raw_full + set + 4, kFp8RopeOffset, row,
@@ -679,6 +718,11 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
       for (int i = 0; i < 2; ++i) {
         const int blk = 2 * h + i;
         if (!warp_wait(bars.raw_full + set + blk, par, wd)) goto drain;
+        if (!C::kFp8) {
+          swizzle_row_in_place(kv_base + RG::chunk_off(jt, 2 * blk) + tok * 128, tsw, ok_c);
+          swizzle_row_in_place(kv_base + RG::chunk_off(jt, 2 * blk + 1) + tok * 128, tsw, ok_c);
+          continue;
+        }
         const float scale = __uint_as_float(i == 0 ? sc_c.x : sc_c.y);
         const uint32_t lo = kv_base + RG::chunk_off(jt, 2 * blk) + tok * 128;
         const uint32_t hi = kv_base + RG::chunk_off(jt, 2 * blk + 1) + tok * 128;
@@ -701,16 +745,7 @@ __device__ void gather_fp8(const CUtensorMap* tm_rows, const DecodeParams& p, co
       if (h == 0) {
         // RoPE: already bf16; permute the 16-byte units into the swizzled order
         if (!warp_wait(bars.raw_full + set + 4, par, wd)) goto drain;
-        const uint32_t base = kv_base + RG::chunk_off(jt, 8) + tok * 128;
-        uint4 raw[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) raw[k] = ld_shared_v4(base + ((k ^ tsw) << 4));
-        // raw[k] holds unit k ^ tsw, whose swizzled position is (k ^ tsw) ^ tsw = k
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint4 v = ok_c ? raw[k] : make_uint4(0, 0, 0, 0);
-          st_shared_v4(base + (k << 4), v.x, v.y, v.z, v.w);
-        }
+        swizzle_row_in_place(kv_base + RG::chunk_off(jt, 8) + tok * 128, tsw, ok_c);
       }
     }
     // this warp's part of the tile is written: one arrival on the tile's full
@@ -895,7 +930,7 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
     sg.range(prob, tb, te);
     if (tb >= te) continue;
     const int b = C::kIndexed ? prob / p.s_q : prob;
-    const int L = sg.seqlens[b];
+    const int L = p.flat_rows > 0 ? p.flat_rows : sg.seqlens[b];
     // causal limit per row: query token i sees keys <= L - s_q + i (dense only)
     int lim_min = L - 1;
     if (!C::kIndexed && p.is_causal) {
@@ -1081,8 +1116,9 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
       lse_s[r] = lt > 0.f ? m_s[r] + log2f(lt) : kNegInf;
     }
     gsync();
+    // partial-result slots of this problem: none when this piece is the whole problem
     const int nsplit = p.num_splits[prob + 1] - p.num_splits[prob];
-    const bool final_out = nsplit == 1;
+    const bool final_out = nsplit <= 1;
     int slot = p.num_splits[prob] + (prob == sg.p0 ? split0 : 0);
     const int row0 = g * R + rb;
     bool write_ok = true;
@@ -1237,7 +1273,7 @@ __global__ void __launch_bounds__(Cfg<R, MODE>::kThreads, 1)
     softmax_epilogue<R, MODE>(p, sg, g, split0, tmem, kv, bars, aux, flags, wd);
   } else if (C::kGather) {
     if (C::kRegSplit) regs_inc<C::kRegsGather>();
-    gather_fp8<R, MODE>(&tm_kv, p, sg, kv, bars, flags, wd);
+    gather_rows<R, MODE>(&tm_kv, p, sg, kv, bars, flags, wd);
   }
 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1288,6 +1324,9 @@ size_t decode_smem_bytes(int rpc, int mode) {
     case 216: return Cfg<16, kModeDenseFp8>::kSmemBytes;
     case 232: return Cfg<32, kModeDenseFp8>::kSmemBytes;
     case 264: return Cfg<64, kModeDenseFp8>::kSmemBytes;
+    case 316: return Cfg<16, kModeSparseBf16>::kSmemBytes;
+    case 332: return Cfg<32, kModeSparseBf16>::kSmemBytes;
+    case 364: return Cfg<64, kModeSparseBf16>::kSmemBytes;
   }
   return 0;
 }
@@ -1304,6 +1343,9 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, con
     case 216: return launch_one<16, kModeDenseFp8>(tm_q, tm_kv, p, stream);
     case 232: return launch_one<32, kModeDenseFp8>(tm_q, tm_kv, p, stream);
     case 264: return launch_one<64, kModeDenseFp8>(tm_q, tm_kv, p, stream);
+    case 316: return launch_one<16, kModeSparseBf16>(tm_q, tm_kv, p, stream);
+    case 332: return launch_one<32, kModeSparseBf16>(tm_q, tm_kv, p, stream);
+    case 364: return launch_one<64, kModeSparseBf16>(tm_q, tm_kv, p, stream);
   }
   return cudaErrorInvalidValue;
 }

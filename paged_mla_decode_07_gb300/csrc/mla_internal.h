@@ -74,12 +74,16 @@ struct DecodeParams {
   int is_causal;
   int evict_first;
   int debug_stall;            // test hook: the softmax role waits on a barrier nothing completes
+  int flat_rows;              // > 0: sparse over an unpaged KV of this many rows (index = row; no
+                              // block table or cache_seqlens); 0: paged cache
 
   float scale_log2;           // sm_scale * log2(e)
 };
 
 struct CombineParams {
   const int32_t* num_splits;
+  const int32_t* cache_seqlens;  // problems without tiles get out = 0, lse = -inf (sparse: unused)
+  int s_q, topk;
   const float* o_accum;
   const float* lse_accum;
   void* out;
@@ -93,7 +97,7 @@ struct CombineParams {
 cudaError_t launch_metadata(const int32_t* cache_seqlens, int batch, int s_q, int h_q, int topk,
                             const Geometry& g, int32_t* sched, int32_t* num_splits, uint32_t* status,
                             cudaStream_t stream);
-// mode: 0 dense bf16 cache, 1 sparse FP8 cache, 2 dense FP8 cache
+// mode: 0 dense bf16 cache, 1 sparse FP8 cache, 2 dense FP8 cache, 3 sparse bf16 rows
 cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const DecodeParams& p, int rpc,
                           int mode, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);

@@ -8,8 +8,13 @@
 // a fixed start-up cost; the concatenated cost line is cut into num_parts
 // contiguous pieces of equal cost.  A piece may start or end inside a
 // problem; such a problem is then split and its pieces are merged by the
-// combine kernel.  num_splits is the exclusive prefix sum of the number of
-// pieces per problem, which doubles as the partial-result slot base.
+// combine kernel.  num_splits is the exclusive prefix sum of the partial-result
+// slots per problem: a split problem takes one slot per piece, a problem
+// covered by a single piece takes none (its piece writes the output
+// directly).  Split problems' part ranges overlap only at their end parts,
+// so all problems together take at most 2 * num_parts slots, whatever the
+// number of problems (and at most num_problems + num_parts: each part
+// boundary adds one piece).
 //
 // One CTA of 1024 threads; per-problem prefix sums live in shared memory.
 #include "mla_device.cuh"
@@ -133,9 +138,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 3. pieces per problem.  Parts are contiguous and empty parts can only sit
   // at a problem's tile 0, so the parts touching problem p are
   // first(p) .. last(p), where part(x) = the last part starting at or before x.
+  // Slots: the piece count of a split problem, 0 for a single piece.
   for (int p = tid; p < np; p += kThreads) {
     const int n = tiles[p];
-    cnt[p] = n > 0 ? part_of(starts, num_parts, Pos{p, n - 1}) - part_of(starts, num_parts, Pos{p, 0}) + 1 : 0;
+    const int pieces =
+        n > 0 ? part_of(starts, num_parts, Pos{p, n - 1}) - part_of(starts, num_parts, Pos{p, 0}) + 1 : 0;
+    cnt[p] = pieces > 1 ? pieces : 0;
   }
   __syncthreads();
   block_inclusive_scan(cnt, np, warp_tot);

@@ -77,6 +77,9 @@ WORKLOADS = {
     # mode variant: the memory-bound dense mix over the FP8 cache (656 bytes per token)
     "dense_membound_fp8": Workload("dense_membound_fp8", batch=128, h_q=16, s_q=1, mode="dense",
                                    seqlen_range=(1024, 8192), fp8=True),
+    # mode variant: the sparse FP8 shape over the bf16 cache (1152 bytes per gathered row)
+    "sparse_bf16": Workload("sparse_bf16", batch=128, h_q=128, s_q=2, mode="sparse", seqlen=32768, topk=2048,
+                            fp8=False),
 }
 # Seed per named workload: 1000 + its position (1-based) in the list above.
 SEEDS = {name: 1000 + i for i, name in enumerate(WORKLOADS, start=1)}

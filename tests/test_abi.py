@@ -28,7 +28,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["mla_metadata_size", "mla_workspace_size", "mla_get_metadata", "mla_decode",
-              "mla_get_device_status", "mla_last_error", "mla_abi_version"]:
+              "mla_get_device_status", "mla_last_error", "mla_abi_version", "mla_fp8_cache_store",
+              "mla_sparse_prefill_workspace_size", "mla_sparse_prefill"]:
         assert n in names
 
 
@@ -38,10 +39,12 @@ def test_library_exports_every_declared_symbol(lib):
     assert lib.mla_abi_version() == 1
 
 
-def test_decode_args_struct_matches_header():
-    # field order and count of mla_decode_args
+@pytest.mark.parametrize("struct,cls", [("mla_decode_args", mla.DecodeArgs),
+                                        ("mla_sparse_prefill_args", mla.SparsePrefillArgs)])
+def test_args_structs_match_header(struct, cls):
+    # field order and count of the argument structs
     text = open(HEADER).read()
-    body = re.search(r"typedef struct \{(.*?)\} mla_decode_args;", text, flags=re.S).group(1)
+    body = re.search(r"typedef struct \{((?:(?!typedef struct).)*?)\} " + struct + ";", text, flags=re.S).group(1)
     body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
     fields = []
     for decl in body.split(";"):
@@ -50,7 +53,7 @@ def test_decode_args_struct_matches_header():
             continue
         names = [n.strip().lstrip("*") for n in re.sub(r"^(const\s+)?[\w]+\s*\*?", "", decl).split(",")]
         fields += [n for n in names if n]
-    assert fields == [f for f, _ in mla.DecodeArgs._fields_]
+    assert fields == [f for f, _ in cls._fields_]
 
 
 def test_null_args_rejected(lib):
@@ -89,8 +92,8 @@ def test_host_validation(lib, field, value, status, needle):
 def test_sparse_mode_rules(lib):
     a = _args(topk=64, indices=None, is_fp8=1)
     assert lib.mla_decode(ctypes.byref(a), None) == 1 and "indices is NULL" in mla.last_error()
-    a = _args(topk=64, indices=16, is_fp8=0)
-    assert lib.mla_decode(ctypes.byref(a), None) == 2 and "FP8 cache" in mla.last_error()
+    a = _args(topk=64, indices=16, is_fp8=0)  # sparse over the bf16 cache is a supported mode
+    assert lib.mla_decode(ctypes.byref(a), None) not in (1, 2)
     a = _args(topk=64, indices=16, is_fp8=1, is_causal=1)
     assert lib.mla_decode(ctypes.byref(a), None) == 2 and "dense mode only" in mla.last_error()
     a = _args(topk=0, indices=16)
@@ -116,3 +119,39 @@ def test_python_binding_rejects_bad_tensors():
     q = torch.zeros(1, 1, 16, 576, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         mla.decode(q, q, q, q, 0.1, q, q)
+
+
+def _prefill_args(**kw):
+    a = mla.SparsePrefillArgs()
+    for f, v in dict(q=16, s_q=4, h_q=16, kv=16, s_kv=100, indices=16, topk=64, sm_scale=0.1,
+                     workspace=256, workspace_bytes=1 << 30, out=16, lse=16).items():
+        setattr(a, f, v)
+    for f, v in kw.items():
+        setattr(a, f, v)
+    return a
+
+
+@pytest.mark.parametrize("field,value,status,needle", [
+    ("q", None, 1, "q is NULL"),
+    ("kv", None, 1, "kv is NULL"),
+    ("indices", None, 1, "indices is NULL"),
+    ("out", None, 1, "out is NULL"),
+    ("lse", None, 1, "lse is NULL"),
+    ("s_q", 0, 1, "s_q"),
+    ("s_kv", 0, 1, "s_kv"),
+    ("topk", 0, 1, "topk"),
+    ("kv", 24, 1, "kv is not 16-byte aligned"),
+    ("sm_scale", float("inf"), 1, "sm_scale"),
+])
+def test_sparse_prefill_host_validation(lib, field, value, status, needle):
+    a = _prefill_args(**{field: value})
+    assert lib.mla_sparse_prefill(ctypes.byref(a), None) == status
+    assert needle in mla.last_error()
+    assert lib.mla_sparse_prefill(None, None) == 1
+
+
+def test_sparse_prefill_binding_rejects_bad_tensors():
+    import torch
+    q = torch.zeros(4, 16, 576, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        mla.sparse_prefill(q, q, q, 0.1)

@@ -3,8 +3,10 @@ kernel implements): cut the concatenated cost line of all problems (tiles +
 a fixed start-up cost each) into `parts` equal pieces; a piece may start or
 end inside a problem.  For any workload every tile must belong to exactly one
 piece, the per-problem piece counts must equal last_part - first_part + 1 (the
-closed form the kernel uses), and each piece's split index must be its rank
-among the pieces touching its first problem.  The GPU test
+closed form the kernel uses), each piece's split index must be its rank
+among the pieces touching its first problem, and the partial-result slots
+(the piece count of each split problem) must total at most
+min(2 * parts, problems + parts).  The GPU test
 test_schedule_covers_every_tile_once checks the kernel's own output."""
 import numpy as np
 import pytest
@@ -83,6 +85,9 @@ def test_every_tile_once_and_split_bookkeeping(seed):
             for rank, k in enumerate(ks):
                 if starts[k][0] == p:
                     assert split0[k] == rank
+        # partial-result slots: split problems only, at most two per part
+        slots = [c if c > 1 else 0 for c in counts]
+        assert sum(slots) <= min(2 * parts, np_ + parts)
 
 
 def test_balance_on_a_ragged_mix():
