@@ -83,6 +83,11 @@ def _load():
             lib.oracle_fp8_cache_store.restype = ctypes.c_int64
             lib.oracle_sparse_prefill.argtypes = [P, P, I64, P, I, I, D, P, I64, P, P, I]
             lib.oracle_sparse_prefill.restype = None
+            idx_common = [P, P, P, I, P, I, P, P, I, I, P, I, P, I]
+            lib.oracle_index_scores.argtypes = idx_common + [I64, P]
+            lib.oracle_index_scores.restype = I
+            lib.oracle_index_topk.argtypes = idx_common + [I, P]
+            lib.oracle_index_topk.restype = I
             _libs[path] = lib
     return lib
 
@@ -251,3 +256,45 @@ def sparse_prefill(q, kv, indices, sm_scale, rows=None, n_threads=None):
     if all_rows:
         return out.reshape(s_q, h_q, D_V), lse.reshape(s_q, h_q)
     return out, lse
+
+
+def _index_args(inp):
+    qc = _np(inp.q_codes, np.uint8)
+    qs = _np(inp.q_scales, np.float32)
+    w = _np(inp.weights, np.float32)
+    offs = _np(inp.row_offsets, np.int32)
+    kc = _np(inp.k_codes, np.uint8)
+    ks = _np(inp.k_scales, np.float32)
+    bt = _np(inp.block_table, np.int32)
+    sl = _np(inp.cache_seqlens, np.int32)
+    h_idx = qc.shape[1]
+    assert qc.shape[-1] == 128 and kc.shape[-1] == 128
+    keep = (qc, qs, w, offs, kc, ks, bt, sl)
+    a = [_ptr(qc), _ptr(qs), _ptr(w), h_idx, _ptr(offs), int(sl.shape[0]), _ptr(kc), _ptr(ks),
+         int(kc.shape[0]), int(kc.shape[1]), _ptr(bt), int(bt.shape[1]), _ptr(sl), int(bool(inp.relu))]
+    return a, keep, int(offs[-1])
+
+
+def index_scores(inp, width=None):
+    """Indexer scores [num_tokens, width] float64 (-inf where a key is not visible)."""
+    lib = _load()
+    a, keep, n = _index_args(inp)
+    if width is None:
+        width = max(1, int(_np(inp.cache_seqlens, np.int32).max()))
+    out = np.zeros((n, width), np.float64)
+    if lib.oracle_index_scores(*a, int(width), _ptr(out)) != 0:
+        raise ValueError("oracle: block_table holds an entry outside [0, num_pages)")
+    del keep
+    return out
+
+
+def index_topk(inp, topk=None):
+    """Indexer top-k key ids [num_tokens, topk] int32 (descending score, ties to the smaller id, -1 fill)."""
+    lib = _load()
+    a, keep, n = _index_args(inp)
+    k = int(inp.topk if topk is None else topk)
+    out = np.zeros((n, k), np.int32)
+    if lib.oracle_index_topk(*a, k, _ptr(out)) != 0:
+        raise ValueError("oracle: block_table holds an entry outside [0, num_pages)")
+    del keep
+    return out

@@ -530,3 +530,135 @@ void oracle_sparse_prefill(const uint16_t* q, const uint16_t* kv, int64_t s_kv, 
   for (int t = 1; t < n_threads; ++t) pthread_join(tid[t], NULL);
   pthread_mutex_destroy(&j.mu);
 }
+
+/* ------------------------------------------------------------------------
+ * FP8 top-k indexer (MAX kernels summary, MLA indexing kernels:
+ * mla_fp8_index_top_k — FP8 scores of FP8 queries against a quantised,
+ * paged key cache with their scales, aggregated over the index heads,
+ * masked, reduced to the top-k key ids per query token as int32 with -1 in
+ * the unused slots).  The pages give no formula; the readings taken:
+ *
+ *   query token t (ragged: rows row_offsets[b] .. row_offsets[b+1]-1 belong
+ *   to element b, n_b of them, the last n_b tokens of its cache of L_b):
+ *   position L_b - n_b + j for its j-th row, so it sees keys
+ *   s <= L_b - n_b + j (and s < L_b);
+ *   index heads h < h_idx, head dim 128; q codes / k codes are E4M3 with one
+ *   float32 scale per (token, head) and per cached key;
+ *   score(t, s) = sum_h w[t,h] * f(qs[t,h] * ks[s] * sum_d q[t,h,d] k[s,d])
+ *   with f = ReLU when `relu` is set, else the identity (fp64 from the
+ *   exactly decoded codes);
+ *   top-k: the k visible keys of largest score, in descending score order,
+ *   ties to the smaller key id; slots beyond the visible keys hold -1.
+ * Key s of element b is row block_table[b][s / page_size] * page_size +
+ * s % page_size of the key cache (codes [rows][128], scales [rows]).
+ * ------------------------------------------------------------------------ */
+#define IDX_DIM 128
+
+typedef struct {
+  const uint8_t* q_codes;
+  const float* q_scales;
+  const float* weights;
+  int h_idx;
+  const int32_t* row_offsets;
+  int batch;
+  const uint8_t* k_codes;
+  const float* k_scales;
+  int num_pages, page_size;
+  const int32_t* block_table;
+  int block_table_stride;
+  const int32_t* cache_seqlens;
+  int relu;
+} index_problem;
+
+/* Element of query row t (row_offsets is non-decreasing). */
+static int index_element(const index_problem* p, int64_t t) {
+  int b = 0;
+  while (b + 1 < p->batch && p->row_offsets[b + 1] <= t) ++b;
+  return b;
+}
+
+/* Scores of query row t against keys 0 .. width-1 into sc (-inf where not
+ * visible).  Returns the number of visible keys, or -1 on a bad page id. */
+static int64_t index_row_scores(const index_problem* p, int64_t t, int64_t width, double* sc) {
+  const int b = index_element(p, t);
+  const int64_t n_b = p->row_offsets[b + 1] - p->row_offsets[b];
+  const int64_t j = t - p->row_offsets[b];
+  const int64_t L = p->cache_seqlens[b];
+  int64_t last = L - n_b + j;
+  if (last > L - 1) last = L - 1;
+  int64_t visible = 0;
+  for (int64_t s = 0; s < width; ++s) {
+    sc[s] = -INFINITY;
+    if (s > last) continue;
+    const int64_t blk = s / p->page_size;
+    const int32_t page = blk < p->block_table_stride ? p->block_table[(int64_t)b * p->block_table_stride + blk] : -1;
+    if (page < 0 || page >= p->num_pages) return -1;
+    const int64_t row = (int64_t)page * p->page_size + s % p->page_size;
+    const uint8_t* kc = p->k_codes + row * IDX_DIM;
+    double acc = 0.0;
+    for (int h = 0; h < p->h_idx; ++h) {
+      const uint8_t* qc = p->q_codes + (t * p->h_idx + h) * IDX_DIM;
+      double dot = 0.0;
+      for (int d = 0; d < IDX_DIM; ++d) dot += oracle_e4m3_to_double(qc[d]) * oracle_e4m3_to_double(kc[d]);
+      double v = (double)p->q_scales[t * p->h_idx + h] * (double)p->k_scales[row] * dot;
+      if (p->relu && v < 0.0) v = 0.0;
+      acc += (double)p->weights[t * p->h_idx + h] * v;
+    }
+    sc[s] = acc;
+    ++visible;
+  }
+  return visible;
+}
+
+/* All scores: out [num_tokens, width] (-inf where not visible).  Returns 0,
+ * or 1 on a bad page id. */
+int oracle_index_scores(const uint8_t* q_codes, const float* q_scales, const float* weights, int h_idx,
+                        const int32_t* row_offsets, int batch, const uint8_t* k_codes, const float* k_scales,
+                        int num_pages, int page_size, const int32_t* block_table, int block_table_stride,
+                        const int32_t* cache_seqlens, int relu, int64_t width, double* out) {
+  index_problem p = {q_codes, q_scales, weights, h_idx, row_offsets, batch, k_codes, k_scales, num_pages,
+                     page_size, block_table, block_table_stride, cache_seqlens, relu};
+  const int64_t n = row_offsets[batch];
+  for (int64_t t = 0; t < n; ++t)
+    if (index_row_scores(&p, t, width, out + t * width) < 0) return 1;
+  return 0;
+}
+
+/* Top-k ids per query row: out [num_tokens, topk].  Selection by repeated
+ * scans for the best remaining key (largest score, then smallest id).
+ * Returns 0, or 1 on a bad page id. */
+int oracle_index_topk(const uint8_t* q_codes, const float* q_scales, const float* weights, int h_idx,
+                      const int32_t* row_offsets, int batch, const uint8_t* k_codes, const float* k_scales,
+                      int num_pages, int page_size, const int32_t* block_table, int block_table_stride,
+                      const int32_t* cache_seqlens, int relu, int topk, int32_t* out) {
+  index_problem p = {q_codes, q_scales, weights, h_idx, row_offsets, batch, k_codes, k_scales, num_pages,
+                     page_size, block_table, block_table_stride, cache_seqlens, relu};
+  const int64_t n = row_offsets[batch];
+  int64_t width = 1;
+  for (int b = 0; b < batch; ++b)
+    if (cache_seqlens[b] > width) width = cache_seqlens[b];
+  double* sc = (double*)malloc(sizeof(double) * width);
+  char* taken = (char*)malloc(width);
+  int bad = 0;
+  for (int64_t t = 0; t < n && !bad; ++t) {
+    const int64_t visible = index_row_scores(&p, t, width, sc);
+    if (visible < 0) {
+      bad = 1;
+      break;
+    }
+    memset(taken, 0, width);
+    for (int k = 0; k < topk; ++k) {
+      int64_t best = -1;
+      if (k < visible)
+        for (int64_t s = 0; s < width; ++s) {
+          if (taken[s] || sc[s] == -INFINITY) continue;
+          if (best < 0 || sc[s] > sc[best]) best = s; /* strict: the smaller id wins a tie */
+        }
+      out[t * topk + k] = (int32_t)best;
+      if (best >= 0) taken[best] = 1;
+    }
+  }
+  free(sc);
+  free(taken);
+  return bad;
+}

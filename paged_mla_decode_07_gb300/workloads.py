@@ -302,3 +302,94 @@ def custom(name="custom", **kw) -> Workload:
 def with_fields(w: Workload, **kw) -> Workload:
     return replace(w, **kw)
 
+
+
+# ----------------------------------------------------------------------------
+# FP8 top-k indexer inputs
+# ----------------------------------------------------------------------------
+IDX_DIM = 128
+
+
+@dataclass(frozen=True)
+class IndexWorkload:
+    """Index queries of n_new tokens per element (ragged rows, the last n_new
+    positions of each element's cache) scored against a paged FP8 key cache."""
+    name: str
+    batch: int
+    n_new: int                                  # query tokens per element
+    h_idx: int                                  # index heads
+    topk: int
+    seqlens: Optional[Tuple[int, ...]] = None
+    seqlen: Optional[int] = None
+    seqlen_range: Optional[Tuple[int, int]] = None
+    relu: bool = False
+
+
+# 64 index heads of dimension 128 and top-k 2048 are the shapes the sparse
+# decode workloads consume (the pages give the indexer no shapes).
+INDEX_WORKLOADS = {
+    "index_tiny": IndexWorkload("index_tiny", batch=2, n_new=2, h_idx=8, topk=64, seqlens=(300, 90)),
+    "index_decode": IndexWorkload("index_decode", batch=128, n_new=2, h_idx=64, topk=2048, seqlen=32768),
+}
+INDEX_SEEDS = {name: 1200 + i for i, name in enumerate(INDEX_WORKLOADS, start=1)}
+
+
+@dataclass
+class IndexInputs:
+    workload: IndexWorkload
+    q_codes: torch.Tensor       # uint8 [num_tokens, h_idx, 128] E4M3 codes
+    q_scales: torch.Tensor      # fp32 [num_tokens, h_idx]
+    weights: torch.Tensor       # fp32 [num_tokens, h_idx]
+    row_offsets: torch.Tensor   # int32 [batch + 1]
+    k_codes: torch.Tensor       # uint8 [num_pages, 64, 128]
+    k_scales: torch.Tensor      # fp32 [num_pages, 64]
+    block_table: torch.Tensor   # int32 [batch, max_blocks]
+    cache_seqlens: torch.Tensor  # int32 [batch]
+    topk: int
+    relu: bool
+    seed: int
+
+    def to(self, device) -> "IndexInputs":
+        f = lambda t: t.to(device)
+        return IndexInputs(self.workload, f(self.q_codes), f(self.q_scales), f(self.weights), f(self.row_offsets),
+                           f(self.k_codes), f(self.k_scales), f(self.block_table), f(self.cache_seqlens),
+                           self.topk, self.relu, self.seed)
+
+
+def quantize_e4m3_rows(x: torch.Tensor):
+    """[..., 128] float32 -> (E4M3 codes uint8 [..., 128], fp32 scales [...]): scale = amax / 448
+    (1 for an all-zero row), codes = torch's float8_e4m3fn cast of x / scale."""
+    amax = x.abs().amax(dim=-1)
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    codes = (x / scale[..., None]).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, scale
+
+
+def make_index_inputs(w, seed: Optional[int] = None, device="cpu") -> IndexInputs:
+    """Keys and queries ~ N(0, 1) quantised per 128-dim row; weights ~ N(0, 1) / sqrt(h_idx);
+    lengths and a random page permutation as for decode (numpy PCG64 with ``seed``)."""
+    if isinstance(w, str):
+        if seed is None:
+            seed = INDEX_SEEDS[w]
+        w = INDEX_WORKLOADS[w]
+    if seed is None:
+        seed = 2468
+    rng = np.random.default_rng(seed)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    dw = Workload(w.name, batch=w.batch, h_q=1, s_q=1, mode="dense", seqlens=w.seqlens, seqlen=w.seqlen,
+                  seqlen_range=w.seqlen_range)
+    lens = draw_seqlens(dw, rng)
+    assert np.all(lens >= 0)
+    table, num_pages = _paging(lens, PAGE_SIZE, rng)
+    n = w.batch * w.n_new
+    qx = torch.randn((n, w.h_idx, IDX_DIM), generator=gen, device=device, dtype=torch.float32)
+    q_codes, q_scales = quantize_e4m3_rows(qx)
+    weights = torch.randn((n, w.h_idx), generator=gen, device=device, dtype=torch.float32) / math.sqrt(w.h_idx)
+    kx = torch.randn((num_pages * PAGE_SIZE, IDX_DIM), generator=gen, device=device, dtype=torch.float32)
+    k_codes, k_scales = quantize_e4m3_rows(kx)
+    offs = torch.arange(0, n + 1, w.n_new, dtype=torch.int32)
+    return IndexInputs(w, q_codes.contiguous(), q_scales.contiguous(), weights.contiguous(), offs.to(device),
+                       k_codes.reshape(num_pages, PAGE_SIZE, IDX_DIM).contiguous(),
+                       k_scales.reshape(num_pages, PAGE_SIZE).contiguous(), torch.from_numpy(table).to(device),
+                       torch.from_numpy(lens.astype(np.int32)).to(device), w.topk, w.relu, seed)
