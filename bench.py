@@ -343,6 +343,31 @@ def measure_prefill(device, peaks, reps=10):
             "shape": f"s_q {w.s_q}, s_kv {w.s_kv}, h_q {w.h_q}, topk {w.topk}"}
 
 
+def measure_index(device, peaks, reps=10):
+    """FP8 top-k indexer (mla_index_topk) on the named indexer workload.  Algorithmic bytes: every
+    cached key once per element (128 code bytes + a 4-byte scale) + the query codes, scales and
+    weights + the int32 ids written; FLOPs of the head dots 2 * 128 * h_idx per (query row, key)."""
+    import paged_mla_decode_07_gb300 as mla
+    inp = W.make_index_inputs("index_decode", device=device)
+    w = inp.workload
+    T = int(inp.row_offsets[-1])
+    idx = torch.empty((T, w.topk), dtype=torch.int32, device=device)
+    ws = torch.empty(mla.index_topk_workspace_size(T, inp.block_table.shape[1]), dtype=torch.uint8, device=device)
+    fn = lambda: mla.index_topk(inp.q_codes, inp.q_scales, inp.weights, inp.row_offsets, inp.k_codes, inp.k_scales,
+                                inp.block_table, inp.cache_seqlens, w.topk, relu=w.relu, max_new_tokens=w.n_new,
+                                indices=idx, workspace=ws)
+    for _ in range(3):
+        fn()
+    ms = statistics.median(time_events(fn, reps))
+    lens = inp.cache_seqlens.cpu().numpy().astype(np.int64)
+    nbytes = int(lens.sum()) * 132 + T * w.h_idx * (128 + 8) + T * w.topk * 4
+    flops = 2.0 * 128 * w.h_idx * float(np.sum(lens * w.n_new))
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+            "tflops_fp8": round(flops / (ms * 1e-3) / 1e12, 1),
+            "shape": f"batch {w.batch}, {w.n_new} query tokens each, {w.h_idx} heads x 128, L {w.seqlen}, topk {w.topk}"}
+
+
 def max_over_ranks(x: float, device) -> float:
     """The largest x over all ranks of the default process group (x itself without one)."""
     import torch.distributed as dist
@@ -472,6 +497,7 @@ def run_mla(args):
             torch.cuda.empty_cache()
         extra["fp8_cache_store"] = measure_store(device, peaks)
         extra["sparse_prefill"] = measure_prefill(device, peaks)
+        extra["fp8_index_topk"] = measure_index(device, peaks)
         result["workloads"] = extra
         # ---- the oracle on the host cores, bounded sample
         result["cpu_baseline"] = cpu_baseline(inp, target_s=args.cpu_seconds)

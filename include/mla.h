@@ -203,6 +203,53 @@ mla_status mla_sparse_prefill_workspace_size(int s_q, int h_q, int topk, size_t*
  * problems set bits in the device status word (mla_get_device_status). */
 mla_status mla_sparse_prefill(const mla_sparse_prefill_args* args, mla_stream_t stream);
 
+/* FP8 top-k indexer (MAX kernels summary, MLA indexing kernels:
+ * mla_fp8_index_top_k): picks, per query token, the topk cached keys that
+ * sparse attention will read.  The pages name its steps (FP8 scores with
+ * scales, aggregation over the index heads, masking, int32 top-k with -1
+ * fill) but give no formula; this library computes, for query row t of
+ * element b (rows row_offsets[b] .. row_offsets[b+1]-1, the last n_b
+ * positions of a cache of cache_seqlens[b] keys, so row j sees keys
+ * s <= seqlen - n_b + j):
+ *   score(t, s) = sum_h weights[t,h] * f(q_scales[t,h] * k_scales[s] * sum_d q[t,h,d] * k[s,d])
+ * with E4M3 codes q, k (head dim 128), f = ReLU if relu != 0 else identity,
+ * and writes the ids of the topk visible keys of largest score, in
+ * descending score order (ties to the smaller id), -1 after the last visible
+ * key.  Scores are computed in fp32 from the exact E4M3 products; keys whose
+ * scores differ by less than that rounding may be ordered either way.  Key s
+ * of element b is row block_table[b * block_table_stride + s / 64] * 64 + s % 64
+ * of the key cache. */
+typedef struct {
+  const void* q_codes;            /* uint8 E4M3 [num_tokens, h_idx, 128], 16-byte aligned */
+  const float* q_scales;          /* fp32 [num_tokens, h_idx] */
+  const float* weights;           /* fp32 [num_tokens, h_idx] */
+  int num_tokens, h_idx;          /* h_idx a multiple of 8, at most 256 */
+  const int32_t* row_offsets;     /* int32 [batch + 1], non-decreasing, row_offsets[batch] = num_tokens */
+  int batch;
+  int max_new_tokens;             /* >= every element's row count; max_new_tokens * h_idx <= 256 */
+  const void* k_codes;            /* uint8 E4M3 [num_pages, 64, 128], 16-byte aligned */
+  const float* k_scales;          /* fp32 [num_pages, 64] */
+  int num_pages, page_size;       /* page_size must be 64 */
+  const int32_t* block_table;     /* int32 [batch, block_table_stride] */
+  int block_table_stride;
+  const int32_t* cache_seqlens;   /* int32 [batch], each <= block_table_stride * 64 */
+  int relu;
+  int topk;                       /* 1 .. 16384 */
+  void* workspace;                /* >= mla_index_topk_workspace_size() bytes (fp32 scores) */
+  size_t workspace_bytes;
+  int32_t* indices;               /* out: int32 [num_tokens, topk] */
+} mla_index_topk_args;
+
+/* Scratch bytes for mla_index_topk: num_tokens x block_table_stride x 64 fp32 scores. */
+mla_status mla_index_topk_workspace_size(int num_tokens, int block_table_stride, size_t* bytes);
+
+/* Asynchronous on `stream`; device pointers owned by the caller.  Host-side
+ * argument errors return without launching.  On the device, a block-table
+ * entry outside [0, num_pages) sets MLA_DEVICE_BAD_PAGE (its keys are not
+ * selected) and an element with more than max_new_tokens rows sets
+ * MLA_DEVICE_BAD_SCHEDULE (its rows get -1). */
+mla_status mla_index_topk(const mla_index_topk_args* args, mla_stream_t stream);
+
 /* Synchronises `stream`, returns the device status bits accumulated since the
  * last call in *flags (0 = clean) and clears them.  Returns
  * MLA_ERR_DEVICE_TIMEOUT / MLA_ERR_DEVICE_BOUNDS when the matching bit is set. */

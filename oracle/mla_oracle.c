@@ -586,6 +586,8 @@ static int64_t index_row_scores(const index_problem* p, int64_t t, int64_t width
   const int64_t L = p->cache_seqlens[b];
   int64_t last = L - n_b + j;
   if (last > L - 1) last = L - 1;
+  double dec[256]; /* the E4M3 values by code */
+  for (int c = 0; c < 256; ++c) dec[c] = oracle_e4m3_to_double((uint8_t)c);
   int64_t visible = 0;
   for (int64_t s = 0; s < width; ++s) {
     sc[s] = -INFINITY;
@@ -599,7 +601,7 @@ static int64_t index_row_scores(const index_problem* p, int64_t t, int64_t width
     for (int h = 0; h < p->h_idx; ++h) {
       const uint8_t* qc = p->q_codes + (t * p->h_idx + h) * IDX_DIM;
       double dot = 0.0;
-      for (int d = 0; d < IDX_DIM; ++d) dot += oracle_e4m3_to_double(qc[d]) * oracle_e4m3_to_double(kc[d]);
+      for (int d = 0; d < IDX_DIM; ++d) dot += dec[qc[d]] * dec[kc[d]];
       double v = (double)p->q_scales[t * p->h_idx + h] * (double)p->k_scales[row] * dot;
       if (p->relu && v < 0.0) v = 0.0;
       acc += (double)p->weights[t * p->h_idx + h] * v;

@@ -69,6 +69,19 @@ class SparsePrefillArgs(ctypes.Structure):
     ]
 
 
+class IndexTopkArgs(ctypes.Structure):
+    """Mirror of ``mla_index_topk_args`` in include/mla.h."""
+    _fields_ = [
+        ("q_codes", ctypes.c_void_p), ("q_scales", ctypes.c_void_p), ("weights", ctypes.c_void_p),
+        ("num_tokens", ctypes.c_int), ("h_idx", ctypes.c_int), ("row_offsets", ctypes.c_void_p),
+        ("batch", ctypes.c_int), ("max_new_tokens", ctypes.c_int), ("k_codes", ctypes.c_void_p),
+        ("k_scales", ctypes.c_void_p), ("num_pages", ctypes.c_int), ("page_size", ctypes.c_int),
+        ("block_table", ctypes.c_void_p), ("block_table_stride", ctypes.c_int),
+        ("cache_seqlens", ctypes.c_void_p), ("relu", ctypes.c_int), ("topk", ctypes.c_int),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t), ("indices", ctypes.c_void_p),
+    ]
+
+
 def library_path() -> str:
     return _build.LIB
 
@@ -101,6 +114,10 @@ def lib():
             L.mla_sparse_prefill_workspace_size.restype = I
             L.mla_sparse_prefill.argtypes = [ctypes.POINTER(SparsePrefillArgs), P]
             L.mla_sparse_prefill.restype = I
+            L.mla_index_topk_workspace_size.argtypes = [I, I, ctypes.POINTER(S)]
+            L.mla_index_topk_workspace_size.restype = I
+            L.mla_index_topk.argtypes = [ctypes.POINTER(IndexTopkArgs), P]
+            L.mla_index_topk.restype = I
             _lib = L
     return _lib
 
@@ -321,6 +338,70 @@ def sparse_prefill(q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor, sm_
     a.lse = lse.data_ptr()
     _check(lib().mla_sparse_prefill(ctypes.byref(a), _stream(stream)))
     return out.view(s_q, h_q, D_V), lse.view(s_q, h_q)
+
+
+def index_topk_workspace_size(num_tokens: int, block_table_stride: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().mla_index_topk_workspace_size(num_tokens, block_table_stride, ctypes.byref(n)))
+    return n.value
+
+
+def index_topk(q_codes: torch.Tensor, q_scales: torch.Tensor, weights: torch.Tensor, row_offsets: torch.Tensor,
+               k_codes: torch.Tensor, k_scales: torch.Tensor, block_table: torch.Tensor, cache_seqlens: torch.Tensor,
+               topk: int, relu: bool = False, max_new_tokens: Optional[int] = None,
+               indices: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """FP8 top-k indexer (mla_index_topk).  q_codes uint8 [T, h_idx, 128] (E4M3 codes), q_scales and
+    weights fp32 [T, h_idx], row_offsets int32 [batch + 1], k_codes uint8 [num_pages, 64, 128],
+    k_scales fp32 [num_pages, 64], block_table int32 [batch, stride], cache_seqlens int32 [batch].
+    Returns int32 [T, topk] key ids (descending score, -1 fill).  Without max_new_tokens the
+    largest row count is read from row_offsets (one device-to-host copy)."""
+    if not torch.is_tensor(q_codes) or q_codes.device.type != "cuda":
+        raise ValueError("q_codes must be a CUDA tensor")
+    dev = q_codes.device
+    _need(q_codes, "q_codes", torch.uint8, dev, 3)
+    T, h_idx, d = q_codes.shape
+    if d != 128:
+        raise ValueError(f"q_codes must be [num_tokens, h_idx, 128] (got {tuple(q_codes.shape)})")
+    _need(q_scales, "q_scales", torch.float32, dev, 2)
+    _need(weights, "weights", torch.float32, dev, 2)
+    if tuple(q_scales.shape) != (T, h_idx) or tuple(weights.shape) != (T, h_idx):
+        raise ValueError("q_scales and weights must be [num_tokens, h_idx]")
+    _need(row_offsets, "row_offsets", torch.int32, dev, 1)
+    _need(k_codes, "k_codes", torch.uint8, dev, 3)
+    if k_codes.shape[2] != 128:
+        raise ValueError(f"k_codes must be [num_pages, page_size, 128] (got {tuple(k_codes.shape)})")
+    _need(k_scales, "k_scales", torch.float32, dev, 2)
+    if tuple(k_scales.shape) != tuple(k_codes.shape[:2]):
+        raise ValueError("k_scales must be [num_pages, page_size]")
+    _need(block_table, "block_table", torch.int32, dev, 2)
+    _need(cache_seqlens, "cache_seqlens", torch.int32, dev, 1)
+    batch = cache_seqlens.shape[0]
+    if row_offsets.shape[0] != batch + 1 or block_table.shape[0] != batch:
+        raise ValueError("row_offsets must have batch + 1 entries and block_table batch rows")
+    if max_new_tokens is None:
+        max_new_tokens = max(1, int(torch.diff(row_offsets).max().item())) if batch > 0 else 1
+    if indices is None:
+        indices = torch.empty((T, topk), dtype=torch.int32, device=dev)
+    _need(indices, "indices", torch.int32, dev)
+    if indices.numel() != T * topk:
+        raise ValueError("indices has the wrong size")
+    if workspace is None:
+        workspace = torch.empty(max(16, index_topk_workspace_size(T, block_table.shape[1])), dtype=torch.uint8,
+                                device=dev)
+    a = IndexTopkArgs()
+    a.q_codes, a.q_scales, a.weights = q_codes.data_ptr(), q_scales.data_ptr(), weights.data_ptr()
+    a.num_tokens, a.h_idx = T, h_idx
+    a.row_offsets, a.batch, a.max_new_tokens = row_offsets.data_ptr(), batch, int(max_new_tokens)
+    a.k_codes, a.k_scales = k_codes.data_ptr(), k_scales.data_ptr()
+    a.num_pages, a.page_size = k_codes.shape[0], k_codes.shape[1]
+    a.block_table, a.block_table_stride = block_table.data_ptr(), block_table.shape[1]
+    a.cache_seqlens = cache_seqlens.data_ptr()
+    a.relu, a.topk = int(bool(relu)), int(topk)
+    a.workspace = workspace.data_ptr()
+    a.workspace_bytes = workspace.numel() * workspace.element_size()
+    a.indices = indices.data_ptr()
+    _check(lib().mla_index_topk(ctypes.byref(a), _stream(stream)))
+    return indices.view(T, topk)
 
 
 def device_status(stream=None, raise_on_error: bool = False) -> int:

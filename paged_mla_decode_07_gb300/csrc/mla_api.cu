@@ -176,6 +176,22 @@ mla_status encode_byte_rows_map(CUtensorMap* map, const void* base, long long nr
   return MLA_OK;
 }
 
+// E4M3 rows of 128 bytes, [rows][128], 128-byte swizzle: a box of box_rows
+// rows lands as the canonical K-major operand of a kind::f8f6f4 MMA.
+mla_status encode_e4m3_rows_map(CUtensorMap* map, const void* base, long long nrows, int box_rows, const char* what) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(nrows)};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what, (int)r);
+  return MLA_OK;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 uint64_t watchdog_ns() {
@@ -507,6 +523,89 @@ mla_status mla_sparse_prefill(const mla_sparse_prefill_args* a, mla_stream_t str
     e = launch_combine(cp, s, true);
     if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
   }
+  return ok();
+}
+
+mla_status mla_index_topk_workspace_size(int num_tokens, int block_table_stride, size_t* bytes) {
+  if (!bytes) return fail(MLA_ERR_INVALID_ARG, "bytes is NULL");
+  if (num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0 (got %d)", num_tokens);
+  if (block_table_stride < 1)
+    return fail(MLA_ERR_INVALID_ARG, "block_table_stride must be >= 1 (got %d)", block_table_stride);
+  *bytes = align256(static_cast<size_t>(num_tokens) * block_table_stride * kPageSize * sizeof(float));
+  return ok();
+}
+
+mla_status mla_index_topk(const mla_index_topk_args* a, mla_stream_t stream) {
+  if (!a) return fail(MLA_ERR_INVALID_ARG, "args is NULL");
+  if (a->batch < 1) return fail(MLA_ERR_INVALID_ARG, "batch must be >= 1 (got %d)", a->batch);
+  if (a->num_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "num_tokens must be >= 0 (got %d)", a->num_tokens);
+  if (a->h_idx < 8 || a->h_idx % 8 != 0 || a->h_idx > 256)
+    return fail(MLA_ERR_UNSUPPORTED, "h_idx must be a multiple of 8 in [8, 256] (got %d)", a->h_idx);
+  if (a->max_new_tokens < 1) return fail(MLA_ERR_INVALID_ARG, "max_new_tokens must be >= 1 (got %d)", a->max_new_tokens);
+  if (static_cast<long long>(a->max_new_tokens) * a->h_idx > 256)
+    return fail(MLA_ERR_UNSUPPORTED, "max_new_tokens * h_idx = %lld exceeds 256 rows per element",
+                static_cast<long long>(a->max_new_tokens) * a->h_idx);
+  if (a->topk < 1 || a->topk > 16384) return fail(MLA_ERR_UNSUPPORTED, "topk must be in [1, 16384] (got %d)", a->topk);
+  if (a->page_size != kPageSize) return fail(MLA_ERR_UNSUPPORTED, "page_size must be 64 (got %d)", a->page_size);
+  if (a->num_pages < 1) return fail(MLA_ERR_INVALID_ARG, "num_pages must be >= 1 (got %d)", a->num_pages);
+  if (a->block_table_stride < 1)
+    return fail(MLA_ERR_INVALID_ARG, "block_table_stride must be >= 1 (got %d)", a->block_table_stride);
+  if (static_cast<long long>(a->block_table_stride) * kPageSize > (1ll << 31) - 1)
+    return fail(MLA_ERR_UNSUPPORTED, "block_table_stride = %d exceeds 2^31 keys", a->block_table_stride);
+  if (!a->q_codes) return fail(MLA_ERR_INVALID_ARG, "q_codes is NULL");
+  if (!a->q_scales) return fail(MLA_ERR_INVALID_ARG, "q_scales is NULL");
+  if (!a->weights) return fail(MLA_ERR_INVALID_ARG, "weights is NULL");
+  if (!a->row_offsets) return fail(MLA_ERR_INVALID_ARG, "row_offsets is NULL");
+  if (!a->k_codes) return fail(MLA_ERR_INVALID_ARG, "k_codes is NULL");
+  if (!a->k_scales) return fail(MLA_ERR_INVALID_ARG, "k_scales is NULL");
+  if (!a->block_table) return fail(MLA_ERR_INVALID_ARG, "block_table is NULL");
+  if (!a->cache_seqlens) return fail(MLA_ERR_INVALID_ARG, "cache_seqlens is NULL");
+  if (!a->indices) return fail(MLA_ERR_INVALID_ARG, "indices is NULL");
+  if (!aligned(a->q_codes, 16)) return fail(MLA_ERR_INVALID_ARG, "q_codes is not 16-byte aligned");
+  if (!aligned(a->k_codes, 16)) return fail(MLA_ERR_INVALID_ARG, "k_codes is not 16-byte aligned");
+  size_t need = 0;
+  mla_status st = mla_index_topk_workspace_size(a->num_tokens, a->block_table_stride, &need);
+  if (st != MLA_OK) return st;
+  if (a->num_tokens == 0) return ok();
+  if (!a->workspace) return fail(MLA_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
+  if (a->workspace_bytes < need) return fail(MLA_ERR_WORKSPACE, "workspace_bytes = %zu < %zu needed", a->workspace_bytes, need);
+  if (!aligned(a->workspace, 16)) return fail(MLA_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  uint32_t* status = nullptr;
+  st = device_info(&status, nullptr);
+  if (st != MLA_OK) return st;
+
+  IndexParams p;
+  memset(&p, 0, sizeof p);
+  const int rows = a->max_new_tokens * a->h_idx;
+  p.n_box = (rows + 15) & ~15;
+  uint32_t cols = 32;
+  while (cols < static_cast<uint32_t>(p.n_box)) cols <<= 1;
+  p.tmem_cols = 2 * cols;
+  CUtensorMap tm_q, tm_k;
+  st = encode_e4m3_rows_map(&tm_q, a->q_codes, static_cast<long long>(a->num_tokens) * a->h_idx, p.n_box, "q_codes");
+  if (st != MLA_OK) return st;
+  st = encode_e4m3_rows_map(&tm_k, a->k_codes, static_cast<long long>(a->num_pages) * kPageSize, kPageSize, "k_codes");
+  if (st != MLA_OK) return st;
+  p.q_scales = a->q_scales;
+  p.weights = a->weights;
+  p.row_offsets = a->row_offsets;
+  p.k_scales = a->k_scales;
+  p.block_table = a->block_table;
+  p.cache_seqlens = a->cache_seqlens;
+  p.scores = static_cast<float*>(a->workspace);
+  p.status = status;
+  p.timeout_ns = watchdog_ns();
+  p.width = static_cast<int64_t>(a->block_table_stride) * kPageSize;
+  p.batch = a->batch;
+  p.num_tokens = a->num_tokens;
+  p.h_idx = a->h_idx;
+  p.max_new = a->max_new_tokens;
+  p.num_pages = a->num_pages;
+  p.block_table_stride = a->block_table_stride;
+  p.relu = a->relu ? 1 : 0;
+  p.tiles_per_cta = 8;
+  cudaError_t e = launch_index(tm_q, tm_k, p, a->topk, a->indices, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "indexer kernel launch");
   return ok();
 }
 

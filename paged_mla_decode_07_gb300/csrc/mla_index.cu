@@ -1,0 +1,429 @@
+// K4 + K5 — FP8 top-k indexer (MAX kernels summary, MLA indexing kernels:
+// mla_fp8_index_top_k scores FP8 queries against a quantised, paged key
+// cache with their scales, aggregates over the index heads, masks, and keeps
+// the top-k key ids per query token as int32, -1 in unused slots).
+//
+//   score(t, s) = sum_h w[t,h] * f(qs[t,h] * ks[s] * sum_d q[t,h,d] k[s,d])
+//   f = ReLU or identity; query row j of element b (n_b new rows, the last
+//   n_b positions of a cache of L_b) sees keys s <= L_b - n_b + j.
+//
+// K4 index_score_kernel: one CTA per (element, run of 128-key tiles).  The
+// head dots of a tile are one tcgen05 kind::f8f6f4 contraction
+//     D[key, row] = K[key, :] . Q[row, :]    M = 128 keys, N = n_b * h rows, K = 128
+// with E4M3 operands in shared memory (128-byte rows, 128-byte swizzle,
+// loaded by TMA) and the fp32 accumulator in TMEM (two buffers, so the
+// epilogue of one tile overlaps the MMAs of the next).  The epilogue (one
+// thread per key) applies the scales, f and the head weights and writes one
+// fp32 score per (query row, key).  The contraction streams the key cache
+// once per element; its arithmetic intensity (2 * N FLOP per 132-byte key)
+// stays under the FP8 ridge, so the kernel is bounded by HBM.
+//
+// K5 index_topk_kernel: one CTA of 1024 threads per query row: radix select
+// (four 8-bit passes over order-preserving integer images of the scores)
+// finds the k-th largest score, the keys above it and the first ties in key
+// order are collected, and a bitonic sort orders them by (score desc, id asc).
+//
+// Every mbarrier wait is bounded (watchdog); on expiry the CTA records
+// MLA_DEVICE_TIMEOUT, drains its own copies and MMAs and frees TMEM.
+#include "mla_device.cuh"
+#include "mla_internal.h"
+
+namespace mla {
+namespace {
+
+constexpr int kIdxDim = 128;                          // index head dimension (bytes per E4M3 row)
+constexpr int kKeysPerTile = 128;                     // M of the MMA: two pages
+constexpr int kStages = 4;                            // key tiles in flight
+constexpr int kTileBytes = kKeysPerTile * kIdxDim;    // 16 KB
+constexpr int kMaxRows = 256;                         // N of the MMA (query rows x heads of one element)
+constexpr int kScoreThreads = 256;                    // warp 0 TMA, 1 MMA, 2 TMEM, 4..7 epilogue
+constexpr int kQOff = kStages * kTileBytes;
+constexpr int kBarOff = kQOff + kMaxRows * kIdxDim;
+constexpr int kNumBars = 2 * kStages + 4 + 2;         // full, empty, d_full[2], d_empty[2], q_full, done
+constexpr int kAuxOff = kBarOff + kNumBars * 8;       // qs[kMaxRows], w[kMaxRows], ints
+constexpr int kScoreSmem = kAuxOff + 2 * kMaxRows * 4 + 64 + 1024;
+
+// kind::f8f6f4 instruction descriptor: D f32 (bits 4-5 = 1), A and B E4M3
+// (format 0 in bits 7-9 and 10-12), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__device__ __forceinline__ uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Warp-uniform bounded wait: if any lane fails, every lane sees failure.
+__device__ __forceinline__ bool warp_wait_any(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
+  const bool ok = mbar_wait(bar, parity, wd);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded wait that ignores the abort flag (used to drain own async work).
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
+__global__ void __launch_bounds__(kScoreThreads, 1)
+    index_score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const IndexParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint8_t* qs = smem + kQOff;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kBarOff);
+  uint64_t* full = bar;
+  uint64_t* empty = bar + kStages;
+  uint64_t* d_full = bar + 2 * kStages;
+  uint64_t* d_empty = d_full + 2;
+  uint64_t* q_full = d_empty + 2;
+  uint64_t* done = q_full + 1;
+  float* qscale = reinterpret_cast<float*>(smem + kAuxOff);
+  float* wgt = qscale + kMaxRows;
+  int* ints = reinterpret_cast<int*>(wgt + kMaxRows);
+  volatile int* abort_flag = ints;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ints + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.y;
+  const int r0 = p.row_offsets[b];
+  const int n_b = p.row_offsets[b + 1] - r0;
+  const int L = p.cache_seqlens[b];
+  const int nrows = n_b * p.h_idx;
+  if (n_b <= 0 || L <= 0) return;
+  if (n_b > p.max_new) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.status, MLA_DEVICE_BAD_SCHEDULE);
+    return;
+  }
+  const int ntiles = (L + kKeysPerTile - 1) / kKeysPerTile;
+  const int tb = blockIdx.x * p.tiles_per_cta;
+  const int te = min(ntiles, tb + p.tiles_per_cta);
+  if (tb >= te) return;
+  const int N = (nrows + 15) & ~15;  // MMA N: a multiple of 16 (rows past nrows are ignored)
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(d_full + i, 1);
+      mbar_init(d_empty + i, 4);  // one arrival per epilogue warp
+    }
+    mbar_init(q_full, 1);
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  for (int i = threadIdx.x; i < nrows; i += kScoreThreads) {
+    qscale[i] = p.q_scales[static_cast<int64_t>(r0) * p.h_idx + i];
+    wgt[i] = p.weights[static_cast<int64_t>(r0) * p.h_idx + i];
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t dcols = p.tmem_cols / 2;  // columns of one accumulator buffer
+  Watchdog wd{abort_flag, p.status, p.timeout_ns};
+  const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
+
+  if (warp == 0) {
+    // ---- producer: Q rows of the element once, then the key tiles
+    const uint64_t pol = l2_policy_evict_first();
+    int uses[kStages] = {0, 0, 0, 0};
+    bool q_armed = false;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(p.n_box) * kIdxDim);
+      tma_load_2d(qs, &tm_q, q_full, 0, r0 * p.h_idx, l2_policy_evict_normal());
+    }
+    q_armed = true;
+    __syncwarp();
+    for (int t = tb, i = 0; t < te; ++t, ++i) {
+      const int st = i % kStages;
+      if (i >= kStages && !warp_wait_any(empty + st, static_cast<uint32_t>((i / kStages) - 1) & 1u, wd)) break;
+      int pages[2];
+      uint32_t bytes = 0;
+      for (int pg = 0; pg < 2; ++pg) {
+        const int jp = 2 * t + pg;
+        pages[pg] = -1;
+        if (jp * kPageSize < L && jp < p.block_table_stride) {
+          const int id = bt[jp];
+          if (id >= 0 && id < p.num_pages) {
+            pages[pg] = id;
+            bytes += kPageSize * kIdxDim;
+          } else if (lane == 0) {
+            atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
+          }
+        }
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full + st, bytes);
+        for (int pg = 0; pg < 2; ++pg)
+          if (pages[pg] >= 0)
+            tma_load_2d(ring + st * kTileBytes + pg * (kPageSize * kIdxDim), &tm_k, full + st, 0,
+                        pages[pg] * kPageSize, pol);
+      }
+      ++uses[st];
+      __syncwarp();
+    }
+    // drain (bounded): the latest armed phase of every stage and Q
+    if (lane == 0) {
+      for (int st = 0; st < kStages; ++st)
+        if (uses[st] > 0) mbar_wait_drain(full + st, static_cast<uint32_t>(uses[st] - 1) & 1u, wd.limit_ns);
+      if (q_armed) mbar_wait_drain(q_full, 0, wd.limit_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---- MMA issuer (converged warp, elected lane)
+    const uint32_t idesc = idesc_e4m3_f32(kKeysPerTile, N);
+    const uint64_t hi = smem_desc_hi(16, 1024);
+    const uint32_t ringb = smem_u32(ring), qb = smem_u32(qs);
+    bool ok = warp_wait_any(q_full, 0, wd);
+    tc_fence_after();
+    for (int t = tb, i = 0; ok && t < te; ++t, ++i) {
+      const int st = i % kStages, db = i & 1;
+      if (i >= 2 && !warp_wait_any(d_empty + db, static_cast<uint32_t>((i >> 1) - 1) & 1u, wd)) break;
+      if (!warp_wait_any(full + st, static_cast<uint32_t>(i / kStages) & 1u, wd)) break;
+      tc_fence_after();
+      const uint64_t a0 = hi | ((ringb + st * kTileBytes) >> 4);
+      const uint64_t b0 = hi | (qb >> 4);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {  // K = 32 E4M3 values (32 bytes) per MMA
+        if (elect_one()) umma_e4m3_ss(tmem + db * dcols, a0 + 2 * kk, b0 + 2 * kk, idesc, kk != 0);
+        __syncwarp();
+      }
+      if (elect_one()) {
+        umma_commit(empty + st);
+        umma_commit(d_full + db);
+      }
+      __syncwarp();
+    }
+    // drain: every MMA issued by this warp has completed
+    if (elect_one()) umma_commit(done);
+    __syncwarp();
+    if (lane == 0) mbar_wait_drain(done, 0, wd.limit_ns);
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---- epilogue: thread = key of the tile (TMEM lane)
+    const int q4 = warp & 3;
+    const int kt = 32 * q4 + lane;  // key within the tile
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    for (int t = tb, i = 0; t < te; ++t, ++i) {
+      const int db = i & 1;
+      if (!warp_wait_any(d_full + db, static_cast<uint32_t>(i >> 1) & 1u, wd)) break;
+      tc_fence_after();
+      const int key = t * kKeysPerTile + kt;
+      const int jp = key >> 6;
+      int page = -1;
+      if (key < L && jp < p.block_table_stride) {
+        page = bt[jp];
+        if (page < 0 || page >= p.num_pages) page = -1;
+      }
+      const float ks = page >= 0 ? p.k_scales[static_cast<int64_t>(page) * kPageSize + (key & 63)] : 0.f;
+      const uint32_t dbase = tmem + lane_base + db * dcols;
+      for (int j = 0; j < n_b; ++j) {
+        float acc = 0.f;
+        for (int h0 = 0; h0 < p.h_idx; h0 += 8) {
+          float v[8];
+          tmem_ld_x8(dbase + j * p.h_idx + h0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int r = j * p.h_idx + h0 + e;
+            float x = qscale[r] * ks * v[e];
+            if (p.relu) x = fmaxf(x, 0.f);
+            acc = fmaf(wgt[r], x, acc);
+          }
+        }
+        const bool visible = page >= 0 && key <= L - n_b + j;
+        if (key < p.width)
+          p.scores[static_cast<int64_t>(r0 + j) * p.width + key] = visible ? acc : -__int_as_float(0x7f800000);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(d_empty + db);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, p.tmem_cols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// K5: top-k per query row
+// ---------------------------------------------------------------------------
+constexpr int kTopkThreads = 1024;
+
+// Order-preserving image of a finite float (larger float -> larger unsigned);
+// -0 is taken as +0.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Sort key: score image in the high word, 0xFFFFFFFF - id in the low word,
+// so a descending sort puts larger scores first and, among equal scores,
+// smaller ids first.  0 = padding (sorts last).
+__device__ __forceinline__ unsigned long long pack_key(uint32_t u, int id) {
+  return (static_cast<unsigned long long>(u) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(id));
+}
+
+__global__ void __launch_bounds__(kTopkThreads, 1)
+    index_topk_kernel(const IndexParams p, int topk, int sort_cap, int32_t* __restrict__ out) {
+  extern __shared__ unsigned long long keys[];  // [sort_cap]
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t warp_cnt[32];
+  __shared__ uint32_t sh_prefix, sh_mask, sh_remaining, sh_gt, sh_eq_taken;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t t = blockIdx.x;
+  // element of row t: the last b with row_offsets[b] <= t
+  int lo = 0, hi = p.batch - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.row_offsets[mid] <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int b = lo;
+  const int n_b = p.row_offsets[b + 1] - p.row_offsets[b];
+  const int j = static_cast<int>(t - p.row_offsets[b]);
+  const int L = p.cache_seqlens[b];
+  int vis = min(L - n_b + j + 1, L);
+  if (vis < 0 || n_b > p.max_new) vis = 0;
+  if (vis > p.width) vis = static_cast<int>(p.width);
+  const float* sc = p.scores + t * p.width;
+  int32_t* o = out + t * topk;
+
+  if (vis <= topk) {
+    for (int i = tid; i < sort_cap; i += kTopkThreads) keys[i] = i < vis ? pack_key(order_key(sc[i]), i) : 0ull;
+  } else {
+    // radix select of the topk-th largest image, 8 bits per pass from the top
+    if (tid == 0) {
+      sh_prefix = 0;
+      sh_mask = 0;
+      sh_remaining = static_cast<uint32_t>(topk);
+    }
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
+      __syncthreads();
+      const uint32_t prefix = sh_prefix, mask = sh_mask;
+      for (int i = tid; i < vis; i += kTopkThreads) {
+        const uint32_t u = order_key(sc[i]);
+        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        uint32_t above = 0, rem = sh_remaining;
+        int d = 255;
+        for (; d > 0; --d) {
+          if (above + hist[d] >= rem) break;
+          above += hist[d];
+        }
+        sh_remaining = rem - above;
+        sh_prefix = prefix | (static_cast<uint32_t>(d) << shift);
+        sh_mask = mask | (255u << shift);
+      }
+      __syncthreads();
+    }
+    const uint32_t T = sh_prefix;
+    const uint32_t need_eq = sh_remaining;             // ties at T to take, in key order
+    const uint32_t n_gt = static_cast<uint32_t>(topk) - need_eq;
+    if (tid == 0) {
+      sh_gt = 0;
+      sh_eq_taken = 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < vis; base += kTopkThreads) {
+      const int i = base + tid;
+      const uint32_t u = i < vis ? order_key(sc[i]) : 0u;
+      if (i < vis && u > T) keys[atomicAdd(&sh_gt, 1u)] = pack_key(u, i);
+      const bool eq = i < vis && u == T;
+      const uint32_t bal = __ballot_sync(0xffffffffu, eq);
+      if (lane == 0) warp_cnt[warp] = __popc(bal);
+      const uint32_t taken_before = sh_eq_taken;
+      __syncthreads();
+      uint32_t before = 0;
+      for (int w = 0; w < warp; ++w) before += warp_cnt[w];
+      const uint32_t rank = taken_before + before + __popc(bal & ((1u << lane) - 1u));
+      if (eq && rank < need_eq) keys[n_gt + rank] = pack_key(u, i);
+      __syncthreads();
+      if (tid == 0) {
+        uint32_t tot = 0;
+        for (int w = 0; w < kTopkThreads / 32; ++w) tot += warp_cnt[w];
+        sh_eq_taken = taken_before + tot;
+      }
+      __syncthreads();
+    }
+    for (int i = topk + tid; i < sort_cap; i += kTopkThreads) keys[i] = 0ull;
+  }
+  __syncthreads();
+  // bitonic sort, descending
+  for (int size = 2; size <= sort_cap; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < sort_cap / 2; i += kTopkThreads) {
+        const int a = 2 * i - (i & (stride - 1));
+        const int c = a + stride;
+        const bool desc = (a & size) == 0;
+        const unsigned long long x = keys[a], y = keys[c];
+        if ((x < y) == desc) {
+          keys[a] = y;
+          keys[c] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // keys of unusable pages carry -inf: sorted last, reported as unused slots
+  const int n_out = min(vis, topk);
+  const unsigned long long ninf = static_cast<unsigned long long>(order_key(-__int_as_float(0x7f800000)));
+  for (int k = tid; k < topk; k += kTopkThreads)
+    o[k] = (k < n_out && (keys[k] >> 32) != ninf)
+               ? static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(keys[k] & 0xFFFFFFFFull))
+               : -1;
+}
+
+}  // namespace
+
+size_t index_score_smem_bytes() { return kScoreSmem; }
+
+cudaError_t launch_index(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const IndexParams& p, int topk,
+                         int32_t* out, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(index_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
+  if (e != cudaSuccess) return e;
+  const int max_tiles = static_cast<int>((p.width + kKeysPerTile - 1) / kKeysPerTile);
+  dim3 grid((max_tiles + p.tiles_per_cta - 1) / p.tiles_per_cta, p.batch);
+  index_score_kernel<<<grid, kScoreThreads, kScoreSmem, stream>>>(tm_q, tm_k, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  int cap = 1;
+  while (cap < topk) cap <<= 1;
+  const size_t smem = static_cast<size_t>(cap) * sizeof(unsigned long long);
+  e = cudaFuncSetAttribute(index_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  index_topk_kernel<<<p.num_tokens, kTopkThreads, smem, stream>>>(p, topk, cap, out);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

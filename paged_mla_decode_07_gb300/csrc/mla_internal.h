@@ -93,6 +93,21 @@ struct CombineParams {
   uint32_t* status;
 };
 
+struct IndexParams {
+  const float* q_scales;      // [num_tokens, h_idx]
+  const float* weights;       // [num_tokens, h_idx]
+  const int32_t* row_offsets; // [batch + 1]
+  const float* k_scales;      // [num_pages * 64]
+  const int32_t* block_table;
+  const int32_t* cache_seqlens;
+  float* scores;              // [num_tokens, width]
+  uint32_t* status;
+  uint64_t timeout_ns;
+  int64_t width;              // block_table_stride * 64: the longest possible key range
+  int batch, num_tokens, h_idx, max_new, n_box, num_pages, block_table_stride, relu, tiles_per_cta;
+  uint32_t tmem_cols;         // two accumulator buffers of tmem_cols / 2 >= n_box columns
+};
+
 // Kernel launchers (defined in the .cu files); return a CUDA error code.
 cudaError_t launch_metadata(const int32_t* cache_seqlens, int batch, int s_q, int h_q, int topk,
                             const Geometry& g, int32_t* sched, int32_t* num_splits, uint32_t* status,
@@ -106,6 +121,8 @@ cudaError_t launch_fp8_cache_store(const uint16_t* x, int num_tokens, const int3
                                    const int32_t* cache_lengths, int batch, const int32_t* block_table,
                                    int block_table_stride, uint8_t* kvcache, int num_pages, uint32_t* status,
                                    int sm_count, cudaStream_t stream);
+cudaError_t launch_index(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const IndexParams& p, int topk,
+                         int32_t* out, cudaStream_t stream);
 // Sets the thread-local message returned by mla_last_error().
 void set_error_message(const std::string& msg);
 

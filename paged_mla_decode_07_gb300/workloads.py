@@ -323,6 +323,7 @@ class IndexWorkload:
     seqlen: Optional[int] = None
     seqlen_range: Optional[Tuple[int, int]] = None
     relu: bool = False
+    rows: Optional[Tuple[int, ...]] = None      # ragged: query tokens per element (overrides n_new)
 
 
 # 64 index heads of dimension 128 and top-k 2048 are the shapes the sparse
@@ -382,13 +383,15 @@ def make_index_inputs(w, seed: Optional[int] = None, device="cpu") -> IndexInput
     lens = draw_seqlens(dw, rng)
     assert np.all(lens >= 0)
     table, num_pages = _paging(lens, PAGE_SIZE, rng)
-    n = w.batch * w.n_new
+    counts = np.asarray(w.rows if w.rows is not None else [w.n_new] * w.batch, dtype=np.int64)
+    assert counts.shape == (w.batch,)
+    n = int(counts.sum())
     qx = torch.randn((n, w.h_idx, IDX_DIM), generator=gen, device=device, dtype=torch.float32)
     q_codes, q_scales = quantize_e4m3_rows(qx)
     weights = torch.randn((n, w.h_idx), generator=gen, device=device, dtype=torch.float32) / math.sqrt(w.h_idx)
     kx = torch.randn((num_pages * PAGE_SIZE, IDX_DIM), generator=gen, device=device, dtype=torch.float32)
     k_codes, k_scales = quantize_e4m3_rows(kx)
-    offs = torch.arange(0, n + 1, w.n_new, dtype=torch.int32)
+    offs = torch.from_numpy(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32))
     return IndexInputs(w, q_codes.contiguous(), q_scales.contiguous(), weights.contiguous(), offs.to(device),
                        k_codes.reshape(num_pages, PAGE_SIZE, IDX_DIM).contiguous(),
                        k_scales.reshape(num_pages, PAGE_SIZE).contiguous(), torch.from_numpy(table).to(device),

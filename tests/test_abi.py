@@ -29,7 +29,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ["mla_metadata_size", "mla_workspace_size", "mla_get_metadata", "mla_decode",
               "mla_get_device_status", "mla_last_error", "mla_abi_version", "mla_fp8_cache_store",
-              "mla_sparse_prefill_workspace_size", "mla_sparse_prefill"]:
+              "mla_sparse_prefill_workspace_size", "mla_sparse_prefill", "mla_index_topk_workspace_size",
+              "mla_index_topk"]:
         assert n in names
 
 
@@ -40,7 +41,8 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 @pytest.mark.parametrize("struct,cls", [("mla_decode_args", mla.DecodeArgs),
-                                        ("mla_sparse_prefill_args", mla.SparsePrefillArgs)])
+                                        ("mla_sparse_prefill_args", mla.SparsePrefillArgs),
+                                        ("mla_index_topk_args", mla.IndexTopkArgs)])
 def test_args_structs_match_header(struct, cls):
     # field order and count of the argument structs
     text = open(HEADER).read()
@@ -155,3 +157,34 @@ def test_sparse_prefill_binding_rejects_bad_tensors():
     q = torch.zeros(4, 16, 576, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         mla.sparse_prefill(q, q, q, 0.1)
+
+
+def _index_args(**kw):
+    a = mla.IndexTopkArgs()
+    for f, v in dict(q_codes=16, q_scales=16, weights=16, num_tokens=4, h_idx=64, row_offsets=16, batch=2,
+                     max_new_tokens=2, k_codes=16, k_scales=16, num_pages=4, page_size=64, block_table=16,
+                     block_table_stride=4, cache_seqlens=16, relu=0, topk=64, workspace=16,
+                     workspace_bytes=1 << 20, indices=16).items():
+        setattr(a, f, v)
+    for f, v in kw.items():
+        setattr(a, f, v)
+    return a
+
+
+@pytest.mark.parametrize("field,value,status,needle", [
+    ("q_codes", None, 1, "q_codes is NULL"),
+    ("k_scales", None, 1, "k_scales is NULL"),
+    ("indices", None, 1, "indices is NULL"),
+    ("h_idx", 12, 2, "multiple of 8"),
+    ("max_new_tokens", 5, 2, "exceeds 256"),
+    ("topk", 0, 2, "topk"),
+    ("topk", 20000, 2, "topk"),
+    ("page_size", 32, 2, "page_size"),
+    ("k_codes", 8, 1, "k_codes is not 16-byte aligned"),
+    ("workspace_bytes", 100, 3, "workspace_bytes"),
+])
+def test_index_topk_host_validation(lib, field, value, status, needle):
+    a = _index_args(**{field: value})
+    assert lib.mla_index_topk(ctypes.byref(a), None) == status
+    assert needle in mla.last_error()
+    assert lib.mla_index_topk(None, None) == 1
