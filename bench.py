@@ -589,9 +589,18 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(W.WORKLOADS),
                     help="workload timed as the step (default: the memory-bound dense mix)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--extra", choices=["sparse_prefill", "fp8_index_topk", "fp8_cache_store"],
+                    help="time only this entry point (one JSON line; used for profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.extra:
+        device = "cuda"
+        peaks = load_peaks()
+        fn = {"sparse_prefill": measure_prefill, "fp8_index_topk": measure_index,
+              "fp8_cache_store": measure_store}[args.extra]
+        print(json.dumps({"extra": args.extra, **fn(device, peaks)}), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

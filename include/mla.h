@@ -213,6 +213,7 @@ mla_status mla_sparse_prefill(const mla_sparse_prefill_args* args, mla_stream_t 
  * s <= seqlen - n_b + j):
  *   score(t, s) = sum_h weights[t,h] * f(q_scales[t,h] * k_scales[s] * sum_d q[t,h,d] * k[s,d])
  * with E4M3 codes q, k (head dim 128), f = ReLU if relu != 0 else identity,
+ * (q_scales and k_scales positive, as the amax / 448 quantiser makes them)
  * and writes the ids of the topk visible keys of largest score, in
  * descending score order (ties to the smaller id), -1 after the last visible
  * key.  Scores are computed in fp32 from the exact E4M3 products; keys whose

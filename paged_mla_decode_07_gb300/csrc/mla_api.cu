@@ -603,7 +603,16 @@ mla_status mla_index_topk(const mla_index_topk_args* a, mla_stream_t stream) {
   p.num_pages = a->num_pages;
   p.block_table_stride = a->block_table_stride;
   p.relu = a->relu ? 1 : 0;
-  p.tiles_per_cta = 8;
+  // key tiles per CTA: about four waves of two CTAs per SM when every element
+  // has the longest possible length (fewer, longer CTAs amortise the set-up)
+  {
+    int sms = 0;
+    st = device_info(nullptr, &sms);
+    if (st != MLA_OK) return st;
+    const long long max_tiles = (p.width + 127) / 128;
+    long long tpc = (static_cast<long long>(a->batch) * max_tiles + 8ll * sms - 1) / (8ll * sms);
+    p.tiles_per_cta = static_cast<int>(tpc < 4 ? 4 : (tpc > 64 ? 64 : tpc));
+  }
   cudaError_t e = launch_index(tm_q, tm_k, p, a->topk, a->indices, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "indexer kernel launch");
   return ok();

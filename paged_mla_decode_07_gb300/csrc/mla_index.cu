@@ -36,12 +36,14 @@ constexpr int kKeysPerTile = 128;                     // M of the MMA: two pages
 constexpr int kStages = 4;                            // key tiles in flight
 constexpr int kTileBytes = kKeysPerTile * kIdxDim;    // 16 KB
 constexpr int kMaxRows = 256;                         // N of the MMA (query rows x heads of one element)
-constexpr int kScoreThreads = 256;                    // warp 0 TMA, 1 MMA, 2 TMEM, 4..7 epilogue
+constexpr int kScoreThreads = 384;                    // warp 0 TMA, 1 MMA, 2 TMEM, 4..11 epilogue
+constexpr int kEpiWarps = 8;                          // two per TMEM lane quarter: they split the query rows
 constexpr int kQOff = kStages * kTileBytes;
 constexpr int kBarOff = kQOff + kMaxRows * kIdxDim;
 constexpr int kNumBars = 2 * kStages + 4 + 2;         // full, empty, d_full[2], d_empty[2], q_full, done
 constexpr int kAuxOff = kBarOff + kNumBars * 8;       // qs[kMaxRows], w[kMaxRows], ints
 constexpr int kScoreSmem = kAuxOff + 2 * kMaxRows * 4 + 64 + 1024;
+static_assert(kAuxOff % 16 == 0, "w * qs must be 16-byte aligned for vector loads");
 
 // kind::f8f6f4 instruction descriptor: D f32 (bits 4-5 = 1), A and B E4M3
 // (format 0 in bits 7-9 and 10-12), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
@@ -73,7 +75,12 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
   return true;
 }
 
-__global__ void __launch_bounds__(kScoreThreads, 1)
+// With positive scales (the quantiser's amax / 448, or 1) a head's term is
+// w * f(qs * ks * dot) = ks * (w * qs) * f(dot), f = ReLU or identity: the
+// epilogue multiplies each dot by the per-row factor w * qs (kept in shared
+// memory) and the sum by the key's scale once.
+template <bool RELU>
+__global__ void __launch_bounds__(kScoreThreads, 2)
     index_score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const IndexParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -87,9 +94,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
   uint64_t* d_empty = d_full + 2;
   uint64_t* q_full = d_empty + 2;
   uint64_t* done = q_full + 1;
-  float* qscale = reinterpret_cast<float*>(smem + kAuxOff);
-  float* wgt = qscale + kMaxRows;
-  int* ints = reinterpret_cast<int*>(wgt + kMaxRows);
+  float* wq = reinterpret_cast<float*>(smem + kAuxOff);  // w * qs per query row x head (16-byte aligned)
+  int* ints = reinterpret_cast<int*>(wq + 2 * kMaxRows);
   volatile int* abort_flag = ints;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ints + 1);
 
@@ -117,7 +123,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(d_full + i, 1);
-      mbar_init(d_empty + i, 4);  // one arrival per epilogue warp
+      mbar_init(d_empty + i, kEpiWarps);  // one arrival per epilogue warp
     }
     mbar_init(q_full, 1);
     mbar_init(done, 1);
@@ -125,8 +131,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     fence_barrier_init();
   }
   for (int i = threadIdx.x; i < nrows; i += kScoreThreads) {
-    qscale[i] = p.q_scales[static_cast<int64_t>(r0) * p.h_idx + i];
-    wgt[i] = p.weights[static_cast<int64_t>(r0) * p.h_idx + i];
+    wq[i] = p.weights[static_cast<int64_t>(r0) * p.h_idx + i] * p.q_scales[static_cast<int64_t>(r0) * p.h_idx + i];
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_q);
@@ -221,8 +226,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     if (lane == 0) mbar_wait_drain(done, 0, wd.limit_ns);
     __syncwarp();
   } else if (warp >= 4) {
-    // ---- epilogue: thread = key of the tile (TMEM lane)
+    // ---- epilogue: thread = key of the tile (TMEM lane); the two warps of a
+    // lane quarter take alternate query rows
     const int q4 = warp & 3;
+    const int eg = (warp - 4) >> 2;
     const int kt = 32 * q4 + lane;  // key within the tile
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     for (int t = tb, i = 0; t < te; ++t, ++i) {
@@ -238,20 +245,30 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
       }
       const float ks = page >= 0 ? p.k_scales[static_cast<int64_t>(page) * kPageSize + (key & 63)] : 0.f;
       const uint32_t dbase = tmem + lane_base + db * dcols;
-      for (int j = 0; j < n_b; ++j) {
+      for (int j = eg; j < n_b; j += 2) {
         float acc = 0.f;
-        for (int h0 = 0; h0 < p.h_idx; h0 += 8) {
-          float v[8];
-          tmem_ld_x8(dbase + j * p.h_idx + h0, v);
+        for (int h0 = 0; h0 < p.h_idx; h0 += 32) {
+          // up to 32 columns per wait (h_idx is a multiple of 8)
+          const int nc = min(32, p.h_idx - h0);
+          float v[32];
+          tmem_ld_x8(dbase + j * p.h_idx + h0, *reinterpret_cast<float(*)[8]>(v));
+          if (nc > 8) tmem_ld_x8(dbase + j * p.h_idx + h0 + 8, *reinterpret_cast<float(*)[8]>(v + 8));
+          if (nc > 16) tmem_ld_x8(dbase + j * p.h_idx + h0 + 16, *reinterpret_cast<float(*)[8]>(v + 16));
+          if (nc > 24) tmem_ld_x8(dbase + j * p.h_idx + h0 + 24, *reinterpret_cast<float(*)[8]>(v + 24));
           tmem_ld_wait();
+          const float4* w4 = reinterpret_cast<const float4*>(wq + j * p.h_idx + h0);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int r = j * p.h_idx + h0 + e;
-            float x = qscale[r] * ks * v[e];
-            if (p.relu) x = fmaxf(x, 0.f);
-            acc = fmaf(wgt[r], x, acc);
+          for (int e = 0; e < 32; e += 4) {
+            if (e < nc) {
+              const float4 w = w4[e >> 2];
+              acc = fmaf(w.x, RELU ? fmaxf(v[e], 0.f) : v[e], acc);
+              acc = fmaf(w.y, RELU ? fmaxf(v[e + 1], 0.f) : v[e + 1], acc);
+              acc = fmaf(w.z, RELU ? fmaxf(v[e + 2], 0.f) : v[e + 2], acc);
+              acc = fmaf(w.w, RELU ? fmaxf(v[e + 3], 0.f) : v[e + 3], acc);
+            }
           }
         }
+        acc *= ks;
         const bool visible = page >= 0 && key <= L - n_b + j;
         if (key < p.width)
           p.scores[static_cast<int64_t>(r0 + j) * p.width + key] = visible ? acc : -__int_as_float(0x7f800000);
@@ -274,6 +291,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 // K5: top-k per query row
 // ---------------------------------------------------------------------------
 constexpr int kTopkThreads = 1024;
+constexpr int kBatch = 8;  // score loads in flight per thread
 
 // Order-preserving image of a finite float (larger float -> larger unsigned);
 // -0 is taken as +0.
@@ -292,9 +310,9 @@ __device__ __forceinline__ unsigned long long pack_key(uint32_t u, int id) {
 __global__ void __launch_bounds__(kTopkThreads, 1)
     index_topk_kernel(const IndexParams p, int topk, int sort_cap, int32_t* __restrict__ out) {
   extern __shared__ unsigned long long keys[];  // [sort_cap]
-  __shared__ uint32_t hist[256];
+  __shared__ uint32_t hist[4096];
   __shared__ uint32_t warp_cnt[32];
-  __shared__ uint32_t sh_prefix, sh_mask, sh_remaining, sh_gt, sh_eq_taken;
+  __shared__ uint32_t sh_prefix, sh_mask, sh_remaining, sh_gt, sh_eq_taken, sh_eq_total;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t t = blockIdx.x;
   // element of row t: the last b with row_offsets[b] <= t
@@ -319,31 +337,64 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   if (vis <= topk) {
     for (int i = tid; i < sort_cap; i += kTopkThreads) keys[i] = i < vis ? pack_key(order_key(sc[i]), i) : 0ull;
   } else {
-    // radix select of the topk-th largest image, 8 bits per pass from the top
+    // radix select of the topk-th largest image: digits of 12, 12 and 8 bits
+    // from the top.  Twelve-bit leading digits (sign, exponent and three
+    // mantissa bits) spread nearby scores over many bins, so plain shared
+    // atomics rarely collide.
     if (tid == 0) {
       sh_prefix = 0;
       sh_mask = 0;
       sh_remaining = static_cast<uint32_t>(topk);
     }
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = pass == 0 ? 20 : (pass == 1 ? 8 : 0);
+      const uint32_t dmask = pass == 2 ? 255u : 4095u;
+      for (int i = tid; i < 4096; i += kTopkThreads) hist[i] = 0;
       __syncthreads();
-      const uint32_t prefix = sh_prefix, mask = sh_mask;
-      for (int i = tid; i < vis; i += kTopkThreads) {
-        const uint32_t u = order_key(sc[i]);
-        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+      // read before any thread can update them (the digit search below)
+      const uint32_t prefix = sh_prefix, mask = sh_mask, rem = sh_remaining;
+      // loads in batches of kBatch per thread (independent, so they are all
+      // in flight together), then the histogram updates
+      for (int i0 = 0; i0 < vis; i0 += kBatch * kTopkThreads) {
+        uint32_t u[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          const int i = i0 + k * kTopkThreads + tid;
+          u[k] = i < vis ? order_key(__ldcg(sc + i)) : 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          const int i = i0 + k * kTopkThreads + tid;
+          if (i < vis && (u[k] & mask) == prefix) atomicAdd(&hist[(u[k] >> shift) & dmask], 1u);
+        }
       }
       __syncthreads();
-      if (tid == 0) {
-        uint32_t above = 0, rem = sh_remaining;
-        int d = 255;
-        for (; d > 0; --d) {
-          if (above + hist[d] >= rem) break;
-          above += hist[d];
+      // the digit holding the remaining-th largest: thread t owns bins
+      // 4t .. 4t+3; an exclusive suffix sum over threads gives the count of
+      // keys in higher bins
+      const uint32_t c = hist[4 * tid] + hist[4 * tid + 1] + hist[4 * tid + 2] + hist[4 * tid + 3];
+      uint32_t x = c;  // inclusive suffix sum within the warp (lanes above)
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xffffffffu, x, o);
+        if (lane + o < 32) x += y;
+      }
+      if (lane == 0) warp_cnt[warp] = x;  // warp total
+      __syncthreads();
+      uint32_t above = x - c;  // bins of higher lanes in this warp
+      for (int w = warp + 1; w < kTopkThreads / 32; ++w) above += warp_cnt[w];
+      if (above < rem && above + c >= rem) {
+        uint32_t acc = above;
+        int d = 4 * tid + 3;
+        for (; d > 4 * tid; --d) {
+          if (acc + hist[d] >= rem) break;
+          acc += hist[d];
         }
-        sh_remaining = rem - above;
+        sh_remaining = rem - acc;
+        sh_eq_total = hist[d];  // after the last pass: the number of keys equal to T
         sh_prefix = prefix | (static_cast<uint32_t>(d) << shift);
-        sh_mask = mask | (255u << shift);
+        sh_mask = mask | (dmask << shift);
       }
       __syncthreads();
     }
@@ -355,26 +406,46 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
       sh_eq_taken = 0;
     }
     __syncthreads();
-    for (int base = 0; base < vis; base += kTopkThreads) {
-      const int i = base + tid;
-      const uint32_t u = i < vis ? order_key(sc[i]) : 0u;
-      if (i < vis && u > T) keys[atomicAdd(&sh_gt, 1u)] = pack_key(u, i);
-      const bool eq = i < vis && u == T;
-      const uint32_t bal = __ballot_sync(0xffffffffu, eq);
-      if (lane == 0) warp_cnt[warp] = __popc(bal);
-      const uint32_t taken_before = sh_eq_taken;
-      __syncthreads();
-      uint32_t before = 0;
-      for (int w = 0; w < warp; ++w) before += warp_cnt[w];
-      const uint32_t rank = taken_before + before + __popc(bal & ((1u << lane) - 1u));
-      if (eq && rank < need_eq) keys[n_gt + rank] = pack_key(u, i);
-      __syncthreads();
-      if (tid == 0) {
-        uint32_t tot = 0;
-        for (int w = 0; w < kTopkThreads / 32; ++w) tot += warp_cnt[w];
-        sh_eq_taken = taken_before + tot;
+    // when every key equal to T is taken their order does not matter: they
+    // are appended like the larger ones; otherwise the first need_eq in key
+    // order are taken (block-wide ordered compaction, chunk by chunk)
+    const bool all_eq = sh_eq_total == need_eq;
+    for (int i0 = 0; i0 < vis; i0 += kBatch * kTopkThreads) {
+      uint32_t ub[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int i = i0 + k * kTopkThreads + tid;
+        ub[k] = i < vis ? order_key(__ldcg(sc + i)) : 0u;
       }
-      __syncthreads();
+#pragma unroll 1
+      for (int k = 0; k < kBatch; ++k) {
+        if (i0 + k * kTopkThreads >= vis) break;  // uniform across the block
+        const int i = i0 + k * kTopkThreads + tid;
+        const uint32_t u = ub[k];
+        const bool gt = i < vis && (u > T || (all_eq && u == T));
+        const uint32_t gbal = __ballot_sync(0xffffffffu, gt);
+        uint32_t gbase = 0;
+        if (lane == 0 && gbal) gbase = atomicAdd(&sh_gt, static_cast<uint32_t>(__popc(gbal)));
+        gbase = __shfl_sync(0xffffffffu, gbase, 0);
+        if (gt) keys[gbase + __popc(gbal & ((1u << lane) - 1u))] = pack_key(u, i);
+        if (all_eq) continue;
+        const bool eq = i < vis && u == T;
+        const uint32_t bal = __ballot_sync(0xffffffffu, eq);
+        if (lane == 0) warp_cnt[warp] = __popc(bal);
+        const uint32_t taken_before = sh_eq_taken;
+        __syncthreads();
+        uint32_t before = 0;
+        for (int w = 0; w < warp; ++w) before += warp_cnt[w];
+        const uint32_t rank = taken_before + before + __popc(bal & ((1u << lane) - 1u));
+        if (eq && rank < need_eq) keys[n_gt + rank] = pack_key(u, i);
+        __syncthreads();
+        if (tid == 0) {
+          uint32_t tot = 0;
+          for (int w = 0; w < kTopkThreads / 32; ++w) tot += warp_cnt[w];
+          sh_eq_taken = taken_before + tot;
+        }
+        __syncthreads();
+      }
     }
     for (int i = topk + tid; i < sort_cap; i += kTopkThreads) keys[i] = 0ull;
   }
@@ -410,11 +481,12 @@ size_t index_score_smem_bytes() { return kScoreSmem; }
 
 cudaError_t launch_index(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const IndexParams& p, int topk,
                          int32_t* out, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(index_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
+  auto kern = p.relu ? index_score_kernel<true> : index_score_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
   if (e != cudaSuccess) return e;
   const int max_tiles = static_cast<int>((p.width + kKeysPerTile - 1) / kKeysPerTile);
   dim3 grid((max_tiles + p.tiles_per_cta - 1) / p.tiles_per_cta, p.batch);
-  index_score_kernel<<<grid, kScoreThreads, kScoreSmem, stream>>>(tm_q, tm_k, p);
+  kern<<<grid, kScoreThreads, kScoreSmem, stream>>>(tm_q, tm_k, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   int cap = 1;
