@@ -100,14 +100,18 @@ struct Cfg {
   static constexpr int kGatherWarp0 = 4 + 4 * kSmWG;  // sparse: first FP8 gather warp
   static constexpr int kWarps = kGatherWarp0 + (kGather ? 4 : 0);
   // With two softmax warpgroups the producer/MMA warpgroup hands registers to
-  // the others (setmaxnreg).  Sparse: 512 threads launched at 128 registers,
-  // 128*64 + 2*128*160 + 128*128 = 65536.  Dense: 384 threads at 168,
-  // 128*88 + 2*128*208 = 64512.  The host checks the compiled register count
+  // the others (setmaxnreg).  Gathered modes: 512 threads launched at 128
+  // registers, 128*64 + 2*128*168 + 128*112 = 65536 (the softmax needs 168
+  // to run without spilling).  Dense: 384 threads at 168, 128*88 + 2*128*208 = 64512.  The host checks the compiled register count
   // against kRegBudget before launching (an increase beyond the launch's total
   // would never be granted).
   static constexpr bool kRegSplit = kSmWG == 2;
-  static constexpr uint32_t kRegsCtl = kGather ? 64 : 88, kRegsSoftmax = kGather ? 160 : 208, kRegsGather = 128;
+  static constexpr uint32_t kRegsCtl = kGather ? 64 : 88, kRegsSoftmax = kGather ? 168 : 208, kRegsGather = 112;
   static constexpr int kRegBudget = 128 * kRegsCtl + 256 * kRegsSoftmax + (kGather ? 128 * kRegsGather : 0);
+  // registers per thread at launch: a kernel that uses setmaxnreg is compiled
+  // to the whole per-thread share of the register file (checked on the host);
+  // each role then moves from this count to its own with .inc or .dec
+  static constexpr uint32_t kLaunchRegs = (65536 / (kGatherWarp0 * 32 + (kGather ? 128 : 0))) & ~7u;
   static_assert(!kRegSplit || kRegBudget <= 65536, "register split exceeds the register file");
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kKvChunkBytes = kTileTokens * 128;  // 8 KB: [64 tokens][64 dims] bf16
@@ -1260,7 +1264,7 @@ __global__ void __launch_bounds__(Cfg<R, MODE>::kThreads, 1)
   }
 
   if (warp < 4) {
-    if (C::kRegSplit) regs_dec<C::kRegsCtl>();
+    if (C::kRegSplit) regs_to<C::kRegsCtl, C::kLaunchRegs>();
     if (warp == 0) {
       producer<R, MODE>(&tm_q, &tm_kv, p, sg, g, kv, qs, bars, flags, wd);  // the whole warp, converged
     } else if (warp == 1) {
@@ -1269,10 +1273,10 @@ __global__ void __launch_bounds__(Cfg<R, MODE>::kThreads, 1)
       pv_issuer<R, MODE>(sg, tmem, kv, bars, wd);
     }
   } else if (warp < C::kGatherWarp0) {
-    if (C::kRegSplit) regs_inc<C::kRegsSoftmax>();
+    if (C::kRegSplit) regs_to<C::kRegsSoftmax, C::kLaunchRegs>();
     softmax_epilogue<R, MODE>(p, sg, g, split0, tmem, kv, bars, aux, flags, wd);
   } else if (C::kGather) {
-    if (C::kRegSplit) regs_inc<C::kRegsGather>();
+    if (C::kRegSplit) regs_to<C::kRegsGather, C::kLaunchRegs>();
     gather_rows<R, MODE>(&tm_kv, p, sg, kv, bars, flags, wd);
   }
 
@@ -1296,7 +1300,8 @@ cudaError_t launch_one(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const 
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
-    if (fa.numRegs * C::kThreads < C::kRegBudget) return cudaErrorInvalidConfiguration;
+    if (fa.numRegs * C::kThreads < C::kRegBudget || fa.numRegs != static_cast<int>(C::kLaunchRegs))
+      return cudaErrorInvalidConfiguration;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.num_parts * p.row_groups);

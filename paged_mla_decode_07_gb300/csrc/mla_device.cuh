@@ -152,6 +152,16 @@ template <uint32_t N>
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
 template <uint32_t N>
 __device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+// Move a warpgroup from FROM registers per thread to TO: .inc only raises and
+// .dec only lowers the count (the other direction is an illegal instruction).
+template <uint32_t TO, uint32_t FROM>
+__device__ __forceinline__ void regs_to() {
+  static_assert(TO % 8 == 0 && TO >= 24 && TO <= 256, "setmaxnreg counts are multiples of 8 in [24, 256]");
+  if constexpr (TO > FROM)
+    regs_inc<TO>();
+  else if constexpr (TO < FROM)
+    regs_dec<TO>();
+}
 
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA / tensor core) before it signals a consumer.
