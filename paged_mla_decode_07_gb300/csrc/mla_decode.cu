@@ -599,19 +599,12 @@ __device__ void gather_rows(const CUtensorMap* tm_rows, const DecodeParams& p, c
   };
   // look up this thread's token of tile `it`: cache row (invalid -> row 0,
   // zeros written later), validity, this half's two scales
-  // sparse: this thread's index of tile `it`, loaded two tiles ahead of its
-  // conversion (the first link of the dependent index -> page -> scale chain)
-  auto fetch_index = [&](const It& it) -> int {
-    if (!C::kIndexed || !it.valid) return -1;
-    const int k = it.j * kTileTokens + tok;
-    return k < p.topk ? __ldg(p.indices + static_cast<int64_t>(it.prob) * p.topk + k) : -1;
-  };
-  // one tile ahead: cache row, validity and this half's scales of tile `it`
-  // (t: the token's index, sparse only)
-  auto lookup = [&](const It& it, int t, int& row, bool& ok, uint2& sc) {
+  auto lookup = [&](const It& it, int& row, bool& ok, uint2& sc) {
     if (C::kIndexed) {
       const int b = it.prob / p.s_q;
       const int L = p.flat_rows > 0 ? p.flat_rows : sg.seqlens[b];
+      const int k = it.j * kTileTokens + tok;
+      const int t = k < p.topk ? p.indices[static_cast<int64_t>(it.prob) * p.topk + k] : -1;
       ok = t >= 0 && t < L;
       if (p.flat_rows > 0) {
         row = ok ? t : 0;  // unpaged KV: the index is the row
@@ -702,29 +695,23 @@ __device__ void gather_rows(const CUtensorMap* tm_rows, const DecodeParams& p, c
     return true;
   };
 
-  const It none{0, 0, 0, false};
   It cur = first_from(sg.p0);
-  It nxt = cur.valid ? next_of(cur) : none;
-  int t_n = fetch_index(nxt);  // index of tile 1
   int row_c = 0;
   bool ok_c = false;
   uint2 sc_c = make_uint2(0, 0);
   int jt = 0;
   if (cur.valid) {
-    lookup(cur, fetch_index(cur), row_c, ok_c, sc_c);
+    lookup(cur, row_c, ok_c, sc_c);
     if (!issue(0, row_c, ok_c)) goto drain;
   }
   for (; cur.valid; ++jt) {
     if (tid == 0) MLA_TR(kTrGatherStart, jt);
-    // tile jt+2: load its indices (used an iteration later); tile jt+1: look
-    // up its rows from the indices loaded an iteration ago (these loads
-    // overlap the conversion of tile jt)
-    const It nn = nxt.valid ? next_of(nxt) : none;
-    const int t_nn = fetch_index(nn);
+    // tile jt+1: look up its rows first (the loads overlap the conversion)
+    const It nxt = next_of(cur);
     int row_n = 0;
     bool ok_n = false;
     uint2 sc_n = make_uint2(0, 0);
-    if (nxt.valid) lookup(nxt, t_n, row_n, ok_n, sc_n);
+    if (nxt.valid) lookup(nxt, row_n, ok_n, sc_n);
     // dequantise tile jt in place: token tok's 128 code bytes of block b sit
     // at row tok of chunk 2b+1; they become row tok of chunks 2b and 2b+1
     // (bf16, 128-byte swizzle).  Units are read in a per-thread rotated order.
@@ -774,8 +761,6 @@ __device__ void gather_rows(const CUtensorMap* tm_rows, const DecodeParams& p, c
     // then tile jt+1's row gathers (their slots free once the PV of tile jt-1 is done)
     if (nxt.valid && !issue(jt + 1, row_n, ok_n)) goto drain;
     cur = nxt;
-    nxt = nn;
-    t_n = t_nn;
     row_c = row_n;
     ok_c = ok_n;
     sc_c = sc_n;
