@@ -63,7 +63,7 @@ def _load():
             I = ctypes.c_int
             I64 = ctypes.c_int64
             D = ctypes.c_double
-            common = [P, P, I, I, I, P, I, P, I, I, I, P, I, D, I, P, I64]
+            common = [P, P, I, I, I, P, I, P, I, I, I, P, I, D, I, P, P, P, I64]
             lib.oracle_mla_decode.argtypes = common + [P, P, I]
             lib.oracle_mla_decode.restype = I
             lib.oracle_mla_partial.argtypes = common + [I64, I64, P, P, I]
@@ -74,6 +74,8 @@ def _load():
             lib.oracle_e4m3_to_double.restype = D
             lib.oracle_dequant_row.argtypes = [P, P]
             lib.oracle_dequant_row.restype = None
+            lib.oracle_dequant_row_token_scale.argtypes = [P, ctypes.c_float, P]
+            lib.oracle_dequant_row_token_scale.restype = None
             lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
             lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
             lib.oracle_fp8_quantize_row.argtypes = [P, P]
@@ -114,12 +116,19 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
-def _args(q, kvcache, block_table, cache_seqlens, sm_scale, is_causal, indices):
+def _args(q, kvcache, block_table, cache_seqlens, sm_scale, is_causal, indices, topk_lengths=None,
+          kv_scales=None):
     qn = _np(q, np.uint16)
     batch, s_q, h_q, d = qn.shape
     assert d == D_QK
     kv = kvcache
-    if hasattr(kv, "dtype") and str(kv.dtype) in ("torch.uint8", "uint8"):
+    scales = None if kv_scales is None else np.ascontiguousarray(_np(kv_scales, np.float32))
+    lens = None if topk_lengths is None else np.ascontiguousarray(_np(topk_lengths, np.int32))
+    if hasattr(kv, "dtype") and str(kv.dtype) in ("torch.uint8", "uint8") and scales is not None:
+        kvn = _np(kv, np.uint8)
+        is_fp8 = 2
+        assert kvn.shape[-1] == 640
+    elif hasattr(kv, "dtype") and str(kv.dtype) in ("torch.uint8", "uint8"):
         kvn = _np(kv, np.uint8)
         is_fp8 = 1
         assert kvn.shape[-1] == 656
@@ -132,14 +141,14 @@ def _args(q, kvcache, block_table, cache_seqlens, sm_scale, is_causal, indices):
     sl = _np(cache_seqlens, np.int32)
     idx = _np(indices, np.int32)
     topk = 0 if idx is None else idx.shape[-1]
-    keep = (qn, kvn, bt, sl, idx)
+    keep = (qn, kvn, bt, sl, idx, scales, lens)
     a = [_ptr(qn), _ptr(kvn), is_fp8, num_pages, page_size, _ptr(bt), bt.shape[1], _ptr(sl), batch,
-         s_q, h_q, _ptr(idx), topk, float(sm_scale), int(bool(is_causal))]
+         s_q, h_q, _ptr(idx), topk, float(sm_scale), int(bool(is_causal)), _ptr(lens), _ptr(scales)]
     return a, keep, (batch, s_q, h_q)
 
 
 def mla_decode(q, kvcache, block_table, cache_seqlens, sm_scale, is_causal=False, indices=None,
-               rows=None, n_threads=None):
+               rows=None, n_threads=None, topk_lengths=None, kv_scales=None):
     """Oracle decode.  Returns (out float64 [n_rows, 512], lse float64 [n_rows]).
 
     ``rows`` selects flat output rows ((b*s_q + i)*h_q + h); None = all rows
@@ -147,7 +156,7 @@ def mla_decode(q, kvcache, block_table, cache_seqlens, sm_scale, is_causal=False
     """
     lib = _load()
     a, keep, (batch, s_q, h_q) = _args(q, kvcache, block_table, cache_seqlens, sm_scale, is_causal,
-                                       indices)
+                                       indices, topk_lengths, kv_scales)
     all_rows = rows is None
     r = None if all_rows else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     n = batch * s_q * h_q if all_rows else r.shape[0]
@@ -164,11 +173,11 @@ def mla_decode(q, kvcache, block_table, cache_seqlens, sm_scale, is_causal=False
 
 
 def mla_partial(q, kvcache, block_table, cache_seqlens, sm_scale, k0, k1, is_causal=False,
-                indices=None, rows=None, n_threads=None):
+                indices=None, rows=None, n_threads=None, topk_lengths=None, kv_scales=None):
     """Oracle restricted to key-set positions [k0, k1) of every row (flat rows)."""
     lib = _load()
     a, keep, (batch, s_q, h_q) = _args(q, kvcache, block_table, cache_seqlens, sm_scale, is_causal,
-                                       indices)
+                                       indices, topk_lengths, kv_scales)
     r = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     n = batch * s_q * h_q if r is None else r.shape[0]
     out = np.zeros((n, D_V), np.float64)
@@ -298,3 +307,12 @@ def index_topk(inp, topk=None):
         raise ValueError("oracle: block_table holds an entry outside [0, num_pages)")
     del keep
     return out
+
+
+def dequant_row_token_scale(row640, scale) -> np.ndarray:
+    """Dequantise one 640-byte per-token-scale FP8 row into 576 float64 (bf16-valued) numbers."""
+    r = np.ascontiguousarray(np.asarray(row640, np.uint8))
+    assert r.shape == (640,)
+    k = np.zeros((D_QK,), np.float64)
+    _load().oracle_dequant_row_token_scale(_ptr(r), ctypes.c_float(float(scale)), _ptr(k))
+    return k

@@ -106,10 +106,30 @@ void oracle_dequant_row(const uint8_t* row, double* k) {
   }
 }
 
+/* Per-token-scale FP8 row (MAX kernels summary, MLA section: the scaled
+ * decode takes explicit per-token KV scales [num_blocks, ..., page_size, ...]
+ * and an FP8 + BF16 layout whose row is 640 bytes): bytes [0, 512) the E4M3
+ * codes of dims 0..511, bytes [512, 640) dims 512..575 as bf16; one float32
+ * scale per token.  K[d] = bf16_rn(fp32_rn(e4m3 * scale)) for d < 512. */
+void oracle_dequant_row_token_scale(const uint8_t* row, float scale, double* k) {
+  for (int d = 0; d < D_V; ++d) {
+    float prod = (float)(oracle_e4m3_to_double(row[d]) * (double)scale);
+    k[d] = bf16_bits_to_double(float_to_bf16_rne(prod));
+  }
+  for (int d = D_V; d < D_QK; ++d) {
+    uint16_t h;
+    memcpy(&h, row + D_V + 2 * (d - D_V), sizeof h);
+    k[d] = bf16_bits_to_double(h);
+  }
+}
+
 typedef struct {
   const uint16_t* q;        /* bf16 bits [batch, s_q, h_q, 576] */
-  const void* kvcache;      /* bf16 [pages, page_size, 576] or uint8 [pages, page_size, 656] */
+  const void* kvcache;      /* bf16 [pages, page_size, 576], uint8 [pages, page_size, 656] (is_fp8 1)
+                               or uint8 [pages, page_size, 640] with per-token scales (is_fp8 2) */
   int is_fp8;
+  const float* kv_scales;   /* is_fp8 2: float32 [pages, page_size] */
+  const int32_t* topk_lengths; /* sparse, optional: int32 [batch, s_q], valid index slots per row */
   int num_pages;
   int page_size;
   const int32_t* block_table;
@@ -129,7 +149,9 @@ static int fetch_token(const oracle_problem* p, int b, int j, double* k) {
   int slot = j % p->page_size;
   if (page < 0 || page >= p->num_pages) return 0;
   int64_t token = (int64_t)page * p->page_size + slot;
-  if (p->is_fp8) {
+  if (p->is_fp8 == 2) {
+    oracle_dequant_row_token_scale((const uint8_t*)p->kvcache + token * 640, p->kv_scales[token], k);
+  } else if (p->is_fp8) {
     oracle_dequant_row((const uint8_t*)p->kvcache + token * FP8_ROW_BYTES, k);
   } else {
     const uint16_t* row = (const uint16_t*)p->kvcache + token * D_QK;
@@ -145,7 +167,14 @@ static int64_t key_set(const oracle_problem* p, int b, int i, int32_t* keys) {
   int64_t n = 0;
   if (p->indices) {
     const int32_t* idx = p->indices + ((int64_t)b * p->s_q + i) * p->topk;
-    for (int k = 0; k < p->topk; ++k)
+    /* with topk_lengths, only the first topk_lengths[b, i] slots hold ids (the
+       MAX kernels summary names sparse_topk_lengths beside sparse_indices) */
+    int n_slots = p->topk;
+    if (p->topk_lengths) {
+      const int32_t len = p->topk_lengths[(int64_t)b * p->s_q + i];
+      n_slots = len < 0 ? 0 : (len < p->topk ? len : p->topk);
+    }
+    for (int k = 0; k < n_slots; ++k)
       if (idx[k] >= 0 && idx[k] < L) keys[n++] = idx[k];
   } else {
     int last = L - 1;
@@ -260,7 +289,10 @@ static int run(const oracle_problem* p, const int64_t* rows, int64_t n_rows, int
 static void fill_problem(oracle_problem* p, const uint16_t* q, const void* kvcache, int is_fp8,
                          int num_pages, int page_size, const int32_t* block_table,
                          int block_table_stride, const int32_t* cache_seqlens, int batch, int s_q,
-                         int h_q, const int32_t* indices, int topk, double sm_scale, int is_causal) {
+                         int h_q, const int32_t* indices, int topk, double sm_scale, int is_causal,
+                         const int32_t* topk_lengths, const float* kv_scales) {
+  p->topk_lengths = topk_lengths;
+  p->kv_scales = kv_scales;
   p->q = q;
   p->kvcache = kvcache;
   p->is_fp8 = is_fp8;
@@ -285,11 +317,12 @@ int oracle_mla_decode(const uint16_t* q, const void* kvcache, int is_fp8, int nu
                       int page_size, const int32_t* block_table, int block_table_stride,
                       const int32_t* cache_seqlens, int batch, int s_q, int h_q,
                       const int32_t* indices, int topk, double sm_scale, int is_causal,
+                      const int32_t* topk_lengths, const float* kv_scales,
                       const int64_t* rows, int64_t n_rows, double* out, double* lse,
                       int n_threads) {
   oracle_problem p;
   fill_problem(&p, q, kvcache, is_fp8, num_pages, page_size, block_table, block_table_stride,
-               cache_seqlens, batch, s_q, h_q, indices, topk, sm_scale, is_causal);
+               cache_seqlens, batch, s_q, h_q, indices, topk, sm_scale, is_causal, topk_lengths, kv_scales);
   return run(&p, rows, n_rows, 0, -1, out, lse, n_threads);
 }
 
@@ -298,11 +331,12 @@ int oracle_mla_partial(const uint16_t* q, const void* kvcache, int is_fp8, int n
                        int page_size, const int32_t* block_table, int block_table_stride,
                        const int32_t* cache_seqlens, int batch, int s_q, int h_q,
                        const int32_t* indices, int topk, double sm_scale, int is_causal,
+                       const int32_t* topk_lengths, const float* kv_scales,
                        const int64_t* rows, int64_t n_rows, int64_t k0, int64_t k1, double* out,
                        double* lse, int n_threads) {
   oracle_problem p;
   fill_problem(&p, q, kvcache, is_fp8, num_pages, page_size, block_table, block_table_stride,
-               cache_seqlens, batch, s_q, h_q, indices, topk, sm_scale, is_causal);
+               cache_seqlens, batch, s_q, h_q, indices, topk, sm_scale, is_causal, topk_lengths, kv_scales);
   return run(&p, rows, n_rows, k0, k1, out, lse, n_threads);
 }
 

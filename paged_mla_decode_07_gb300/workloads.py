@@ -54,6 +54,9 @@ class Workload:
     page_size: int = PAGE_SIZE
     sm_scale: Optional[float] = None            # default 1/sqrt(576)
     fp8: Optional[bool] = None                  # cache format; None: FP8 for sparse, bf16 for dense
+    fp8_scales: str = "tile"                    # FP8 rows: "tile" = 656 B, four scales in the row;
+                                                # "token" = 640 B rows + one fp32 scale per token
+    ragged_topk: bool = False                   # sparse: per-row topk_lengths; slots past them hold ids
 
     @property
     def is_fp8(self) -> bool:
@@ -160,12 +163,14 @@ class Inputs:
     sm_scale: float
     seed: int
     meta: dict = field(default_factory=dict)
+    kv_scales: Optional[torch.Tensor] = None      # fp32 [num_pages, page_size] ("token" FP8 rows)
+    topk_lengths: Optional[torch.Tensor] = None   # int32 [batch, s_q] (ragged top-k)
 
     def to(self, device) -> "Inputs":
         mv = lambda t: None if t is None else t.to(device)
         return Inputs(self.workload, mv(self.q), mv(self.kvcache), mv(self.block_table),
                       mv(self.cache_seqlens), mv(self.indices), self.sm_scale, self.seed,
-                      dict(self.meta))
+                      dict(self.meta), mv(self.kv_scales), mv(self.topk_lengths))
 
 
 def describe_lengths(w: Workload) -> str:
@@ -227,6 +232,21 @@ def encode_fp8_rows(x: torch.Tensor) -> torch.Tensor:
     return row
 
 
+def encode_fp8_token_rows(x: torch.Tensor):
+    """Source values [n, 576] float32 -> ([n, 640] uint8 rows, [n] fp32 scales): one scale per
+    token, amax of dims 0..511 / 448 (1 for an all-zero token), codes = float8_e4m3fn(x / scale)
+    via torch's cast in bytes [0, 512), dims 512..575 as bf16 in bytes [512, 640)."""
+    n = x.shape[0]
+    nope = x[:, :D_V].float()
+    amax = nope.abs().amax(dim=1)
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    codes = (nope / scale[:, None]).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    row = torch.empty((n, 640), dtype=torch.uint8, device=x.device)
+    row[:, :D_V] = codes.view(torch.uint8)
+    row[:, D_V:] = x[:, D_V:].to(torch.bfloat16).contiguous().view(torch.uint8).reshape(n, 2 * D_ROPE)
+    return row, scale.contiguous()
+
+
 def make_inputs(w, seed: Optional[int] = None, device="cpu", poison_tail: bool = True,
                 chunk_pages: int = 2048) -> Inputs:
     """Draw one batch of inputs for workload ``w`` (a Workload or a name in WORKLOADS).
@@ -251,15 +271,21 @@ def make_inputs(w, seed: Optional[int] = None, device="cpu", poison_tail: bool =
     q = torch.randn((w.batch, w.s_q, w.h_q, D_QK), generator=gen, device=device,
                     dtype=torch.float32).to(torch.bfloat16)
     ntok = num_pages * w.page_size
+    per_token = w.is_fp8 and w.fp8_scales == "token"
+    row_bytes = 640 if per_token else FP8_ROW_BYTES
+    kv_scales = torch.empty((ntok,), dtype=torch.float32, device=device) if per_token else None
     if w.is_fp8:
-        kv = torch.empty((ntok, FP8_ROW_BYTES), dtype=torch.uint8, device=device)
+        kv = torch.empty((ntok, row_bytes), dtype=torch.uint8, device=device)
     else:
         kv = torch.empty((ntok, D_QK), dtype=torch.bfloat16, device=device)
     step = chunk_pages * w.page_size
     for t0 in range(0, ntok, step):
         t1 = min(ntok, t0 + step)
         x = torch.randn((t1 - t0, D_QK), generator=gen, device=device, dtype=torch.float32)
-        kv[t0:t1] = encode_fp8_rows(x) if w.is_fp8 else x.to(torch.bfloat16)
+        if per_token:
+            kv[t0:t1], kv_scales[t0:t1] = encode_fp8_token_rows(x)
+        else:
+            kv[t0:t1] = encode_fp8_rows(x) if w.is_fp8 else x.to(torch.bfloat16)
 
     if poison_tail:
         for b, L in enumerate(lens.tolist()):
@@ -272,6 +298,8 @@ def make_inputs(w, seed: Optional[int] = None, device="cpu", poison_tail: bool =
             s1 = (page + 1) * w.page_size
             if w.is_fp8:
                 kv[s0:s1] = 0x7F  # e4m3 NaN codes; scale / RoPE bytes 0x7F7F.. are NaN too
+                if per_token:
+                    kv_scales[s0:s1] = float("nan")
             else:
                 kv[s0:s1] = float("nan")
 
@@ -288,10 +316,26 @@ def make_inputs(w, seed: Optional[int] = None, device="cpu", poison_tail: bool =
                     indices_np[b, i, :k] = rng.choice(L, size=k, replace=False).astype(np.int32)
         indices = torch.from_numpy(indices_np).to(device)
 
-    kv = kv.reshape(num_pages, w.page_size, 1, FP8_ROW_BYTES if w.is_fp8 else D_QK)
+    topk_lengths = None
+    if w.mode == "sparse" and w.ragged_topk:
+        # per row a length uniform in [0, topk]; the slots past it hold ids that
+        # would be valid (they must be ignored, not merely skipped as -1)
+        tl = rng.integers(0, w.topk + 1, size=(w.batch, w.s_q)).astype(np.int32)
+        idx_np = indices.cpu().numpy()
+        for b in range(w.batch):
+            L = int(lens[b])
+            for i in range(w.s_q):
+                if L > 0:
+                    idx_np[b, i, tl[b, i]:] = rng.integers(0, L, size=w.topk - tl[b, i])
+        indices = torch.from_numpy(idx_np).to(device)
+        topk_lengths = torch.from_numpy(tl).to(device)
+
+    kv = kv.reshape(num_pages, w.page_size, 1, (row_bytes if w.is_fp8 else D_QK))
     return Inputs(w, q, kv, torch.from_numpy(table).to(device),
                   torch.from_numpy(lens.astype(np.int32)).to(device), indices, w.scale, seed,
-                  meta={"num_pages": num_pages})
+                  meta={"num_pages": num_pages},
+                  kv_scales=None if kv_scales is None else kv_scales.reshape(num_pages, w.page_size),
+                  topk_lengths=topk_lengths)
 
 
 def custom(name="custom", **kw) -> Workload:

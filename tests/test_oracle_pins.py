@@ -364,6 +364,9 @@ MUTATIONS = {
     "invalid_index_kept": ("if (idx[k] >= 0 && idx[k] < L)", "if (idx[k] >= 0)"),
     "v_from_rope_end": ("out[d] += w * kbuf[d];", "out[d] += w * kbuf[d + 64];"),
     "merge_sign": ("double w = exp2(lses[i] - L);", "double w = exp2(L - lses[i]);"),
+    "topk_lengths_ignored": ("n_slots = len < 0 ? 0 : (len < p->topk ? len : p->topk);", "n_slots = p->topk;"),
+    "token_scale_rope_offset": ("memcpy(&h, row + D_V + 2 * (d - D_V), sizeof h);",
+                                "memcpy(&h, row + D_V + 16 + 2 * (d - D_V), sizeof h);"),
 }
 
 
@@ -385,6 +388,8 @@ def _mutant_checks():
         o, l = run_oracle(inp)
         assert_close(o, o_ref)
         test_split_merge_invariant("dense")
+        test_token_scale_dequant_matches_torch()
+        test_topk_lengths_ignore_the_slots_past_them()
         return True
     except AssertionError:
         return False
@@ -401,3 +406,59 @@ def test_planted_mistake_is_caught(name, tmp_path):
     with oracle.use_library(lib):
         assert not _mutant_checks(), f"planted mistake '{name}' went unnoticed"
     assert _mutant_checks()
+
+
+# ----------------------------------------------------------------------------
+# per-token-scale FP8 rows and ragged top-k lengths
+# ----------------------------------------------------------------------------
+def test_token_scale_dequant_matches_torch():
+    """640-byte rows with one fp32 scale per token, against torch's E4M3 cast and fp32 multiply."""
+    g = torch.Generator().manual_seed(12)
+    x = torch.randn(40, 576, generator=g) * torch.rand(40, 1, generator=g) * 5
+    rows, scales = W.encode_fp8_token_rows(x)
+    for n in range(40):
+        k = oracle.dequant_row_token_scale(rows[n].numpy(), float(scales[n]))
+        codes = rows[n, :512].contiguous().view(torch.float8_e4m3fn).float()
+        ref = (codes * scales[n]).to(torch.bfloat16).double().numpy()
+        np.testing.assert_array_equal(k[:512], ref)
+        np.testing.assert_array_equal(k[512:], x[n, 512:].to(torch.bfloat16).double().numpy())
+
+
+def test_token_scale_cache_equals_its_dequantised_bf16_cache():
+    w = W.custom(name="tok", batch=2, h_q=4, s_q=2, mode="sparse", seqlens=(150, 90), topk=48,
+                 fp8_scales="token")
+    inp = W.make_inputs(w, seed=13, poison_tail=False)
+    assert inp.kvcache.shape[-1] == 640 and inp.kv_scales.shape == inp.kvcache.shape[:2]
+    flat = inp.kvcache.reshape(-1, 640)
+    sc = inp.kv_scales.reshape(-1)
+    kb = np.stack([oracle.dequant_row_token_scale(flat[n].numpy(), float(sc[n])) for n in range(flat.shape[0])])
+    kvb = torch.from_numpy(kb).float().to(torch.bfloat16).reshape(inp.kvcache.shape[0], 64, 1, 576)
+    o1, l1 = oracle.mla_decode(inp.q, inp.kvcache, inp.block_table, inp.cache_seqlens, inp.sm_scale,
+                               indices=inp.indices, kv_scales=inp.kv_scales)
+    o2, l2 = oracle.mla_decode(inp.q, kvb, inp.block_table, inp.cache_seqlens, inp.sm_scale, indices=inp.indices)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_topk_lengths_ignore_the_slots_past_them():
+    """Ragged top-k: slots past topk_lengths hold valid-looking ids that must not count; the result
+    equals the same rows with those slots set to -1, and a zero length gives an empty row."""
+    w = W.custom(name="rag", batch=3, h_q=2, s_q=2, mode="sparse", seqlens=(200, 90, 130), topk=40,
+                 ragged_topk=True)
+    inp = W.make_inputs(w, seed=14)
+    tl = inp.topk_lengths.clone()
+    tl[1, 1] = 0
+    tl[2, 0] = 40
+    o, l = oracle.mla_decode(inp.q, inp.kvcache, inp.block_table, inp.cache_seqlens, inp.sm_scale,
+                             indices=inp.indices, topk_lengths=tl)
+    masked = inp.indices.clone()
+    for b in range(3):
+        for i in range(2):
+            masked[b, i, int(tl[b, i]):] = -1
+    o2, l2 = oracle.mla_decode(inp.q, inp.kvcache, inp.block_table, inp.cache_seqlens, inp.sm_scale, indices=masked)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(l, l2)
+    assert np.all(o[1, 1] == 0) and np.all(l[1, 1] == -np.inf)
+    o3, _ = oracle.mla_decode(inp.q, inp.kvcache, inp.block_table, inp.cache_seqlens, inp.sm_scale,
+                              indices=inp.indices)
+    assert not np.array_equal(o3, o)   # the ids past the lengths would have changed the result
