@@ -54,7 +54,8 @@ def algorithmic(inp) -> dict:
     if w.mode == "sparse":
         idx = inp.indices
         valid = ((idx >= 0) & (idx < inp.cache_seqlens.view(-1, 1, 1))).sum().item()
-        kv_bytes = valid * (FP8_ROW if w.is_fp8 else D_QK * 2)
+        row = (644 if w.fp8_scales == "token" else FP8_ROW) if w.is_fp8 else D_QK * 2  # 640 B + a 4-byte scale
+        kv_bytes = valid * row
         flops = 2.0 * w.h_q * w.s_q * w.topk * w.batch * (D_QK + D_V)
         vflops = 2.0 * w.h_q * valid * (D_QK + D_V)
         tab = idx.numel() * 4 + inp.block_table.numel() * 4
@@ -197,7 +198,7 @@ class DecodeStep:
         d = self.d
         self.mla.decode(d.q, d.kvcache, d.block_table, d.cache_seqlens, d.sm_scale, self.sched, self.nsplit,
                         is_causal=self.w.causal, indices=d.indices, out=self.out, lse=self.lse,
-                        workspace=self.ws)
+                        workspace=self.ws, kv_scales=d.kv_scales, topk_lengths=d.topk_lengths)
 
     def __call__(self):
         self.metadata()
@@ -482,7 +483,7 @@ def run_mla(args):
         # ---- the other workloads (kernel level)
         extra = {}
         for name in ("tiny", "dense_computebound", "sparse_fp8", "sparse_fp8_long", "dense_membound_fp8",
-                     "sparse_bf16"):
+                     "sparse_bf16", "sparse_fp8_token"):
             winp, wa, wms, st = measure_workload(name, device)
             bound = "hbm" if name in ("tiny", "dense_membound_fp8") else "tensor"
             e = {"ms": round(wms, 5), "tflops": round(wa["flops"] / (wms * 1e-3) / 1e12, 2),

@@ -70,7 +70,7 @@ typedef enum {
 #define MLA_DEVICE_BAD_SCHEDULE 0x4u /* the schedule did not match the arguments; results invalid */
 
 /* ABI version of this header (incremented on incompatible change). */
-#define MLA_ABI_VERSION 1
+#define MLA_ABI_VERSION 2
 int mla_abi_version(void);
 
 /* Sizes of the two metadata arrays for a decode configuration on the
@@ -119,6 +119,15 @@ typedef struct {
   size_t workspace_bytes;
   void* out;                      /* bf16 [batch, s_q, h_q, 512] */
   float* lse;                     /* fp32 [batch, s_q, h_q] */
+  /* ABI version 2 (zero when unused): */
+  const float* kv_scales;         /* FP8 cache with one scale per token (MAX kernels summary, MLA section:
+                                     the scaled decode's per-token KV scales and 640-byte FP8 + BF16 rows):
+                                     fp32 [num_pages, 64]; the cache rows are then uint8 [.., 640] = 512
+                                     E4M3 codes + 64 bf16 RoPE values, K[d] = bf16_rn(e4m3 * scale) for
+                                     d < 512.  NULL: 656-byte rows with four scales each. */
+  const int32_t* topk_lengths;    /* sparse, optional: int32 [batch, s_q]; row (b, i) reads only its first
+                                     topk_lengths[b, i] index slots (clamped to [0, topk]); NULL: all topk
+                                     slots, -1 marking unused ones */
 } mla_decode_args;
 
 /* (2) Decode ("flash_mla_with_kvcache"): split-KV attention kernel followed

@@ -55,6 +55,7 @@ class DecodeArgs(ctypes.Structure):
         ("is_fp8", ctypes.c_int), ("indices", ctypes.c_void_p), ("topk", ctypes.c_int),
         ("sched", ctypes.c_void_p), ("num_splits", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("kv_scales", ctypes.c_void_p), ("topk_lengths", ctypes.c_void_p),
     ]
 
 
@@ -189,8 +190,11 @@ def get_metadata(cache_seqlens: torch.Tensor, s_q: int, h_q: int, topk: int = 0,
 def decode(q: torch.Tensor, kvcache: torch.Tensor, block_table: torch.Tensor, cache_seqlens: torch.Tensor,
            sm_scale: float, sched: torch.Tensor, num_splits: torch.Tensor, is_causal: bool = False,
            indices: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
-           lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
-    """Paged MLA decode.  Returns (out bf16 [b, s_q, h_q, 512], lse fp32 [b, s_q, h_q], base 2)."""
+           lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None,
+           kv_scales: Optional[torch.Tensor] = None, topk_lengths: Optional[torch.Tensor] = None):
+    """Paged MLA decode.  Returns (out bf16 [b, s_q, h_q, 512], lse fp32 [b, s_q, h_q], base 2).
+    kv_scales (fp32 [num_pages, 64]) selects the FP8 cache with one scale per token (640-byte rows);
+    topk_lengths (int32 [b, s_q]) limits each sparse row to its first index slots."""
     _need(q, "q", torch.bfloat16, ndim=4)
     if not q.is_cuda:
         raise ValueError("q must be a CUDA tensor")
@@ -201,8 +205,13 @@ def decode(q: torch.Tensor, kvcache: torch.Tensor, block_table: torch.Tensor, ca
     is_fp8 = kvcache.dtype == torch.uint8
     if is_fp8:
         _need(kvcache, "kvcache", torch.uint8, dev, 4)
-        if kvcache.shape[-1] != FP8_ROW_BYTES or kvcache.shape[2] != 1:
-            raise ValueError(f"FP8 kvcache must be [pages, page_size, 1, {FP8_ROW_BYTES}]")
+        row = 640 if kv_scales is not None else FP8_ROW_BYTES
+        if kvcache.shape[-1] != row or kvcache.shape[2] != 1:
+            raise ValueError(f"FP8 kvcache must be [pages, page_size, 1, {row}]")
+        if kv_scales is not None:
+            _need(kv_scales, "kv_scales", torch.float32, dev)
+            if kv_scales.numel() != kvcache.shape[0] * kvcache.shape[1]:
+                raise ValueError("kv_scales must hold one scale per cached token")
     else:
         _need(kvcache, "kvcache", torch.bfloat16, dev, 4)
         if kvcache.shape[-1] != D_QK or kvcache.shape[2] != 1:
@@ -217,6 +226,10 @@ def decode(q: torch.Tensor, kvcache: torch.Tensor, block_table: torch.Tensor, ca
         if tuple(indices.shape[:2]) != (batch, s_q):
             raise ValueError(f"indices must be [batch, s_q, topk] (got {tuple(indices.shape)})")
         topk = indices.shape[2]
+    if topk_lengths is not None:
+        _need(topk_lengths, "topk_lengths", torch.int32, dev)
+        if topk_lengths.numel() != batch * s_q:
+            raise ValueError("topk_lengths must be [batch, s_q]")
     _need(sched, "sched", torch.int32, dev)
     _need(num_splits, "num_splits", torch.int32, dev)
     if out is None:
@@ -248,6 +261,8 @@ def decode(q: torch.Tensor, kvcache: torch.Tensor, block_table: torch.Tensor, ca
     a.workspace_bytes = workspace.numel() * workspace.element_size()
     a.out = out.data_ptr()
     a.lse = lse.data_ptr()
+    a.kv_scales = kv_scales.data_ptr() if kv_scales is not None else None
+    a.topk_lengths = topk_lengths.data_ptr() if topk_lengths is not None else None
     _check(lib().mla_decode(ctypes.byref(a), _stream(stream)))
     return out.view(batch, s_q, h_q, D_V), lse.view(batch, s_q, h_q)
 

@@ -300,6 +300,9 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
   if (a->block_table_stride < 1)
     return fail(MLA_ERR_INVALID_ARG, "block_table_stride must be >= 1 (got %d)", a->block_table_stride);
   if (a->is_causal && sparse) return fail(MLA_ERR_UNSUPPORTED, "is_causal applies to dense mode only");
+  if (a->kv_scales && !a->is_fp8) return fail(MLA_ERR_INVALID_ARG, "kv_scales given with a bf16 cache (is_fp8 = 0)");
+  if (a->topk_lengths && !sparse) return fail(MLA_ERR_INVALID_ARG, "topk_lengths given with topk = 0");
+  if (a->kv_scales && !aligned(a->kv_scales, 4)) return fail(MLA_ERR_INVALID_ARG, "kv_scales is not 4-byte aligned");
   if (!std::isfinite(a->sm_scale)) return fail(MLA_ERR_INVALID_ARG, "sm_scale is not finite");
   if (!aligned(a->q, 16)) return fail(MLA_ERR_INVALID_ARG, "q is not 16-byte aligned");
   if (!aligned(a->kvcache, 16)) return fail(MLA_ERR_INVALID_ARG, "kvcache is not 16-byte aligned");
@@ -334,7 +337,7 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
   else if (mode == 3)
     st = encode_byte_rows_map(&tm_kv, a->kvcache, cache_rows, 2 * kDqk, 1);
   else
-    st = encode_byte_rows_map(&tm_kv, a->kvcache, cache_rows, kFp8RowBytes, mode == 1 ? 1 : 32);
+    st = encode_byte_rows_map(&tm_kv, a->kvcache, cache_rows, a->kv_scales ? 640 : kFp8RowBytes, mode == 1 ? 1 : 32);
   if (st != MLA_OK) return st;
 
   DecodeParams p;
@@ -369,6 +372,9 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
     p.debug_stall = (s && atoi(s) != 0) ? 1 : 0;
   }
   p.scale_log2 = a->sm_scale * 1.4426950408889634f;
+  p.kv_scales = a->kv_scales;
+  p.topk_lengths = a->topk_lengths;
+  p.fp8_rope_off = a->kv_scales ? kDv : kFp8RopeOffset;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = launch_decode(tm_q, tm_kv, p, g.rpc, mode, s);

@@ -604,7 +604,12 @@ __device__ void gather_rows(const CUtensorMap* tm_rows, const DecodeParams& p, c
       const int b = it.prob / p.s_q;
       const int L = p.flat_rows > 0 ? p.flat_rows : sg.seqlens[b];
       const int k = it.j * kTileTokens + tok;
-      const int t = k < p.topk ? p.indices[static_cast<int64_t>(it.prob) * p.topk + k] : -1;
+      int tk = p.topk;  // index slots of this problem
+      if (p.topk_lengths) {
+        const int len = p.topk_lengths[it.prob];
+        tk = len < 0 ? 0 : (len < p.topk ? len : p.topk);
+      }
+      const int t = k < tk ? p.indices[static_cast<int64_t>(it.prob) * p.topk + k] : -1;
       ok = t >= 0 && t < L;
       if (p.flat_rows > 0) {
         row = ok ? t : 0;  // unpaged KV: the index is the row
@@ -628,12 +633,17 @@ __device__ void gather_rows(const CUtensorMap* tm_rows, const DecodeParams& p, c
       ok = page_ok && it.j * kTileTokens + tok < L;
       row = (page_ok ? page : 0) * kPageSize + tok;
     }
-    if (C::kFp8)
+    if (C::kFp8 && p.kv_scales) {
+      // one scale per token for all four blocks
+      const uint32_t s1 = ok ? __float_as_uint(__ldg(p.kv_scales + row)) : 0u;
+      sc = make_uint2(s1, s1);
+    } else if (C::kFp8) {
       sc = ok ? __ldg(reinterpret_cast<const uint2*>(p.kv_fp8 + static_cast<int64_t>(row) * kFp8RowBytes +
                                                      kFp8ScaleOffset + 8 * h))
               : make_uint2(0, 0);
-    else
+    } else {
       sc = make_uint2(0, 0);
+    }
   };
   // issue the row gathers of tile jt (FP8: codes of this half's blocks into
   // the upper chunks of their pair slots; bf16: both chunks of each block;
@@ -684,11 +694,11 @@ __device__ void gather_rows(const CUtensorMap* tm_rows, const DecodeParams& p, c
       if (C::kIndexed) {
         if (lane < 8) {
           uint8_t* dst = kv + RG::chunk_off(jt, 8) + g4 * 128;
-          tma_gather4(dst, tm_rows, bars.raw_full + set + 4, C::kFp8 ? kFp8RopeOffset : 2 * kDv, r0, r1, r2, r3,
+          tma_gather4(dst, tm_rows, bars.raw_full + set + 4, C::kFp8 ? p.fp8_rope_off : 2 * kDv, r0, r1, r2, r3,
                       pol);
         }
       } else if (lane == 0) {
-        tma_load_2d(kv + RG::chunk_off(jt, 8) + wtok * 128, tm_rows, bars.raw_full + set + 4, kFp8RopeOffset, row,
+        tma_load_2d(kv + RG::chunk_off(jt, 8) + wtok * 128, tm_rows, bars.raw_full + set + 4, p.fp8_rope_off, row,
                     pol);
       }
     }

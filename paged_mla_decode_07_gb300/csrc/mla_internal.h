@@ -76,6 +76,9 @@ struct DecodeParams {
   int debug_stall;            // test hook: the softmax role waits on a barrier nothing completes
   int flat_rows;              // > 0: sparse over an unpaged KV of this many rows (index = row; no
                               // block table or cache_seqlens); 0: paged cache
+  const float* kv_scales;     // FP8 rows with one scale per token ([rows] fp32), else NULL
+  const int32_t* topk_lengths;  // sparse: valid index slots per problem, else NULL
+  int fp8_rope_off;           // byte offset of the RoPE dims in an FP8 row (528, or 512 with kv_scales)
 
   float scale_log2;           // sm_scale * log2(e)
 };

@@ -83,6 +83,9 @@ WORKLOADS = {
     # mode variant: the sparse FP8 shape over the bf16 cache (1152 bytes per gathered row)
     "sparse_bf16": Workload("sparse_bf16", batch=128, h_q=128, s_q=2, mode="sparse", seqlen=32768, topk=2048,
                             fp8=False),
+    # mode variant: the sparse FP8 shape over 640-byte rows with one scale per token
+    "sparse_fp8_token": Workload("sparse_fp8_token", batch=128, h_q=128, s_q=2, mode="sparse", seqlen=32768,
+                                 topk=2048, fp8_scales="token"),
 }
 # Seed per named workload: 1000 + its position (1-based) in the list above.
 SEEDS = {name: 1000 + i for i, name in enumerate(WORKLOADS, start=1)}

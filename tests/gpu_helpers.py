@@ -41,14 +41,16 @@ def run_cuda(inp, device="cuda"):
     topk = 0 if d.indices is None else d.indices.shape[-1]
     sched, ns = mla.get_metadata(d.cache_seqlens, w.s_q, w.h_q, topk)
     out, lse = mla.decode(d.q, d.kvcache, d.block_table, d.cache_seqlens, d.sm_scale, sched, ns,
-                          is_causal=w.causal, indices=d.indices)
+                          is_causal=w.causal, indices=d.indices, kv_scales=d.kv_scales,
+                          topk_lengths=d.topk_lengths)
     flags = mla.device_status()
     return out.double().cpu().numpy(), lse.double().cpu().numpy(), flags
 
 
 def run_oracle(inp, rows=None):
     return oracle.mla_decode(inp.q, inp.kvcache, inp.block_table, inp.cache_seqlens, inp.sm_scale,
-                             is_causal=inp.workload.causal, indices=inp.indices, rows=rows)
+                             is_causal=inp.workload.causal, indices=inp.indices, rows=rows,
+                             kv_scales=inp.kv_scales, topk_lengths=inp.topk_lengths)
 
 
 def compare(out, lse, ref_out, ref_lse, what=""):

@@ -37,7 +37,7 @@ def test_header_declares_the_boundary():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"libmla.so does not export {name}"
-    assert lib.mla_abi_version() == 1
+    assert lib.mla_abi_version() == 2
 
 
 @pytest.mark.parametrize("struct,cls", [("mla_decode_args", mla.DecodeArgs),

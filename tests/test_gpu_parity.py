@@ -278,3 +278,47 @@ def test_dense_fp8_full_size_workload():
     rows = _sample_rows(inp, 12, np.random.default_rng(8))
     ref_out, ref_lse = run_oracle(inp, rows=rows)
     compare(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, "dense_membound_fp8")
+
+
+# ---------------------------------------------------------------- per-token-scale FP8 rows, ragged top-k
+@pytest.mark.parametrize("h_q,s_q", [(16, 1), (64, 2), (128, 1)])
+def test_sparse_token_scale_cache(h_q, s_q):
+    """640-byte FP8 rows with one scale per token (16/64-row CTAs, two row groups)."""
+    check(W.custom(name=f"stok{h_q}", batch=3, h_q=h_q, s_q=s_q, mode="sparse", seqlens=(2000, 300, 5000),
+                   topk=384, fp8_scales="token"), 1100 + h_q)
+
+
+@pytest.mark.parametrize("h_q,s_q,causal", [(16, 1, False), (64, 1, False), (128, 2, True)])
+def test_dense_token_scale_cache(h_q, s_q, causal):
+    check(W.custom(name=f"dtok{h_q}", batch=3, h_q=h_q, s_q=s_q, mode="dense", fp8=True, fp8_scales="token",
+                   seqlens=(200, 77, 513), causal=causal), 1200 + h_q)
+
+
+@pytest.mark.parametrize("fp8", [True, False])
+@pytest.mark.parametrize("h_q", [16, 64])
+def test_sparse_topk_lengths(h_q, fp8):
+    """Ragged top-k: the slots past each row's length hold valid-looking ids that must be ignored."""
+    w = W.custom(name=f"rag{h_q}{int(fp8)}", batch=3, h_q=h_q, s_q=2, mode="sparse", fp8=fp8,
+                 seqlens=(1500, 200, 3000), topk=320, ragged_topk=True)
+    inp = W.make_inputs(w, seed=1300 + h_q)
+    tl = inp.topk_lengths.clone()
+    tl[0, 0] = 0          # empty row
+    tl[1, 1] = 320        # every slot
+    tl[2, 0] = -5         # negative: empty
+    inp.topk_lengths = tl
+    out, lse, flags = run_cuda(inp)
+    assert flags == 0
+    ref_out, ref_lse = run_oracle(inp)
+    compare(out, lse, ref_out, ref_lse, w.name)
+    assert np.all(out[0, 0] == 0) and np.all(lse[0, 0] == -np.inf)
+
+
+def test_sparse_token_scale_full_size_sampled():
+    """The sparse FP8 decode shape over 640-byte rows with per-token scales, sampled rows."""
+    inp = W.make_inputs("sparse_fp8_token")
+    w = inp.workload
+    out, lse, flags = run_cuda(inp)
+    assert flags == 0
+    rows = _sample_rows(inp, 4, np.random.default_rng(9))
+    ref_out, ref_lse = run_oracle(inp, rows=rows)
+    compare(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, w.name)
