@@ -66,6 +66,8 @@ enum TraceEvent {
 #ifdef MLA_TRACE
 constexpr int kTraceTiles = 1024;
 __device__ unsigned long long g_mla_trace[kTrNumEvents * kTraceTiles];
+// per CTA (up to 1024): %globaltimer when its work starts and when it ends
+__device__ unsigned long long g_mla_cta[2 * 1024];
 #define MLA_TR(ev, idx)                                                                      \
   do {                                                                                       \
     if (blockIdx.x == 0 && (idx) < kTraceTiles) g_mla_trace[(ev) * kTraceTiles + (idx)] = clock64(); \
@@ -1256,6 +1258,13 @@ __global__ void __launch_bounds__(Cfg<R, MODE>::kThreads, 1)
   // above overlapped it; its results (and any earlier kernel's) are visible
   // from here on
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the combine kernel (a programmatic dependent of this one) may be
+  // scheduled from now on: its blocks wait (griddepcontrol.wait) for this
+  // grid to complete, but are resident when it does
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#ifdef MLA_TRACE
+  if (threadIdx.x == 0 && blockIdx.x < 1024) g_mla_cta[2 * blockIdx.x] = global_timer_ns();
+#endif
   Segments sg;
   const int32_t* sr = p.sched + static_cast<int64_t>(part) * kSchedInts;
   sg.p0 = sr[kSchedP0];
@@ -1290,9 +1299,11 @@ __global__ void __launch_bounds__(Cfg<R, MODE>::kThreads, 1)
     gather_rows<R, MODE>(&tm_kv, p, sg, kv, bars, flags, wd);
   }
 
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   tc_fence_before();
   __syncthreads();
+#ifdef MLA_TRACE
+  if (threadIdx.x == 0 && blockIdx.x < 1024) g_mla_cta[2 * blockIdx.x + 1] = global_timer_ns();
+#endif
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
@@ -1374,6 +1385,10 @@ extern "C" int mla_trace_read(unsigned long long* host, size_t n) {
   for (size_t i = 0; i < sizeof(g_mla_trace); i += sizeof z)
     cudaMemcpyToSymbol(g_mla_trace, z, sizeof z, i);
   return static_cast<int>(n);
+}
+// Copies the per-CTA start/end stamps (2 x 1024 %globaltimer values).
+extern "C" int mla_trace_cta_read(unsigned long long* host) {
+  return cudaMemcpyFromSymbol(host, g_mla_cta, sizeof(g_mla_cta)) == cudaSuccess ? 0 : -1;
 }
 #endif
 
