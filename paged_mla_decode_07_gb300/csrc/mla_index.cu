@@ -290,8 +290,41 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
 // ---------------------------------------------------------------------------
 // K5: top-k per query row
 // ---------------------------------------------------------------------------
-constexpr int kTopkThreads = 1024;
-constexpr int kBatch = 8;  // score loads in flight per thread
+constexpr int kTopkThreads = 512;                   // two CTAs per SM
+constexpr int kBinsPerThread = 4096 / kTopkThreads;  // of the 12-bit digit histogram
+constexpr int kBatch = 8;      // score loads in flight per thread
+constexpr int kCandCap = 4096;  // keys of the threshold's leading-digit bin kept in shared memory
+
+// Descending bitonic sort of n (a power of two) keys in shared memory by the
+// whole block.
+__device__ void bitonic_desc(unsigned long long* a, int n) {
+  for (int size = 2; size <= n; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < n / 2; i += kTopkThreads) {
+        const int x0 = 2 * i - (i & (stride - 1));
+        const int x1 = x0 + stride;
+        const bool desc = (x0 & size) == 0;
+        const unsigned long long x = a[x0], y = a[x1];
+        if ((x < y) == desc) {
+          a[x0] = y;
+          a[x1] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Append the keys of the lanes with `take` at *counter (one shared atomic per warp).
+__device__ __forceinline__ void warp_append(unsigned long long* dst, uint32_t* counter, bool take,
+                                            unsigned long long key) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t bal = __ballot_sync(0xffffffffu, take);
+  uint32_t base = 0;
+  if (lane == 0 && bal) base = atomicAdd(counter, static_cast<uint32_t>(__popc(bal)));
+  base = __shfl_sync(0xffffffffu, base, 0);
+  if (take) dst[base + __popc(bal & ((1u << lane) - 1u))] = key;
+}
 
 // Order-preserving image of a finite float (larger float -> larger unsigned);
 // -0 is taken as +0.
@@ -307,11 +340,12 @@ __device__ __forceinline__ unsigned long long pack_key(uint32_t u, int id) {
   return (static_cast<unsigned long long>(u) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(id));
 }
 
-__global__ void __launch_bounds__(kTopkThreads, 1)
+__global__ void __launch_bounds__(kTopkThreads, 2)
     index_topk_kernel(const IndexParams p, int topk, int sort_cap, int32_t* __restrict__ out) {
-  extern __shared__ unsigned long long keys[];  // [sort_cap]
+  extern __shared__ unsigned long long keys[];  // [sort_cap], then candidates [kCandCap]
+  unsigned long long* cand = keys + sort_cap;
   __shared__ uint32_t hist[4096];
-  __shared__ uint32_t warp_cnt[32];
+  __shared__ uint32_t warp_cnt[kTopkThreads / 32];
   __shared__ uint32_t sh_prefix, sh_mask, sh_remaining, sh_gt, sh_eq_taken, sh_eq_total;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t t = blockIdx.x;
@@ -371,9 +405,11 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
       }
       __syncthreads();
       // the digit holding the remaining-th largest: thread t owns bins
-      // 4t .. 4t+3; an exclusive suffix sum over threads gives the count of
-      // keys in higher bins
-      const uint32_t c = hist[4 * tid] + hist[4 * tid + 1] + hist[4 * tid + 2] + hist[4 * tid + 3];
+      // [kBinsPerThread * t, kBinsPerThread * (t + 1)); an exclusive suffix sum
+      // over threads gives the count of keys in higher bins
+      uint32_t c = 0;
+#pragma unroll
+      for (int q = 0; q < kBinsPerThread; ++q) c += hist[kBinsPerThread * tid + q];
       uint32_t x = c;  // inclusive suffix sum within the warp (lanes above)
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -386,17 +422,65 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
       for (int w = warp + 1; w < kTopkThreads / 32; ++w) above += warp_cnt[w];
       if (above < rem && above + c >= rem) {
         uint32_t acc = above;
-        int d = 4 * tid + 3;
-        for (; d > 4 * tid; --d) {
+        int d = kBinsPerThread * tid + kBinsPerThread - 1;
+        for (; d > kBinsPerThread * tid; --d) {
           if (acc + hist[d] >= rem) break;
           acc += hist[d];
         }
         sh_remaining = rem - acc;
-        sh_eq_total = hist[d];  // after the last pass: the number of keys equal to T
+        sh_eq_total = hist[d];  // keys in the chosen bin (after the last pass: equal to T)
         sh_prefix = prefix | (static_cast<uint32_t>(d) << shift);
         sh_mask = mask | (dmask << shift);
       }
       __syncthreads();
+      if (pass == 0 && sh_eq_total <= static_cast<uint32_t>(kCandCap)) break;  // uniform
+    }
+    if (sh_mask == (4095u << 20)) {
+      // the bin of the leading digit holds few keys: one more pass over the
+      // scores takes every key of a higher bin and copies that bin's keys to
+      // shared memory, where a sort picks the rest (larger first, ties to the
+      // smaller id)
+      const uint32_t d1 = sh_prefix >> 20;
+      const uint32_t rem1 = sh_remaining;
+      const uint32_t n_cand = sh_eq_total;
+      __syncthreads();
+      if (tid == 0) {
+        sh_gt = 0;
+        sh_eq_taken = 0;
+      }
+      __syncthreads();
+      for (int i0 = 0; i0 < vis; i0 += kBatch * kTopkThreads) {
+        uint32_t ub[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          const int i = i0 + k * kTopkThreads + tid;
+          ub[k] = i < vis ? order_key(__ldcg(sc + i)) : 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          const int i = i0 + k * kTopkThreads + tid;
+          const uint32_t dig = ub[k] >> 20;
+          warp_append(keys, &sh_gt, i < vis && dig > d1, pack_key(ub[k], i));
+          warp_append(cand, &sh_eq_taken, i < vis && dig == d1, pack_key(ub[k], i));
+        }
+      }
+      int c2 = 1;
+      while (c2 < static_cast<int>(n_cand)) c2 <<= 1;
+      for (int i = static_cast<int>(n_cand) + tid; i < c2; i += kTopkThreads) cand[i] = 0ull;
+      __syncthreads();
+      bitonic_desc(cand, c2);
+      const uint32_t n_gt1 = static_cast<uint32_t>(topk) - rem1;
+      for (uint32_t k = tid; k < rem1; k += kTopkThreads) keys[n_gt1 + k] = cand[k];
+      for (int i = topk + tid; i < sort_cap; i += kTopkThreads) keys[i] = 0ull;
+      __syncthreads();
+      bitonic_desc(keys, sort_cap);
+      const int n_out1 = min(vis, topk);
+      const unsigned long long ninf1 = static_cast<unsigned long long>(order_key(-__int_as_float(0x7f800000)));
+      for (int k = tid; k < topk; k += kTopkThreads)
+        o[k] = (k < n_out1 && (keys[k] >> 32) != ninf1)
+                   ? static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(keys[k] & 0xFFFFFFFFull))
+                   : -1;
+      return;
     }
     const uint32_t T = sh_prefix;
     const uint32_t need_eq = sh_remaining;             // ties at T to take, in key order
@@ -450,22 +534,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
     for (int i = topk + tid; i < sort_cap; i += kTopkThreads) keys[i] = 0ull;
   }
   __syncthreads();
-  // bitonic sort, descending
-  for (int size = 2; size <= sort_cap; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < sort_cap / 2; i += kTopkThreads) {
-        const int a = 2 * i - (i & (stride - 1));
-        const int c = a + stride;
-        const bool desc = (a & size) == 0;
-        const unsigned long long x = keys[a], y = keys[c];
-        if ((x < y) == desc) {
-          keys[a] = y;
-          keys[c] = x;
-        }
-      }
-      __syncthreads();
-    }
-  }
+  bitonic_desc(keys, sort_cap);
   // keys of unusable pages carry -inf: sorted last, reported as unused slots
   const int n_out = min(vis, topk);
   const unsigned long long ninf = static_cast<unsigned long long>(order_key(-__int_as_float(0x7f800000)));
@@ -491,7 +560,7 @@ cudaError_t launch_index(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const
   if (e != cudaSuccess) return e;
   int cap = 1;
   while (cap < topk) cap <<= 1;
-  const size_t smem = static_cast<size_t>(cap) * sizeof(unsigned long long);
+  const size_t smem = static_cast<size_t>(cap + kCandCap) * sizeof(unsigned long long);
   e = cudaFuncSetAttribute(index_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   index_topk_kernel<<<p.num_tokens, kTopkThreads, smem, stream>>>(p, topk, cap, out);
