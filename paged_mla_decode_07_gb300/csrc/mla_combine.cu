@@ -18,6 +18,7 @@ namespace mla {
 namespace {
 
 constexpr int kRowsPerBlock = 4;
+constexpr int kFastSplits = 4;  // pieces merged with all loads in flight at once
 
 __global__ void __launch_bounds__(kRowsPerBlock * 32) combine_kernel(const CombineParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -44,6 +45,65 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) combine_kernel(const Combi
     return;
   }
   __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + grow * kDv + lane * 16;
+
+  if (n <= kFastSplits) {
+    // few pieces (the common case): every load is issued before any is used,
+    // so the merge costs two memory round trips instead of one per piece
+    float l[kFastSplits];
+#pragma unroll
+    for (int i = 0; i < kFastSplits; ++i)
+      l[i] = i < n ? p.lse_accum[static_cast<int64_t>(base + i) * p.rows + r] : -__int_as_float(0x7f800000);
+    float4 x[kFastSplits][4];
+#pragma unroll
+    for (int i = 0; i < kFastSplits; ++i) {
+      if (i < n) {
+        const float4* src = reinterpret_cast<const float4*>(p.o_accum + (static_cast<int64_t>(base + i) * p.rows + r) * kDv +
+                                                            lane * 16);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) x[i][v] = src[v];
+      }
+    }
+    float mxf = l[0];
+#pragma unroll
+    for (int i = 1; i < kFastSplits; ++i) mxf = fmaxf(mxf, l[i]);
+    float acc[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+    float Lf = -__int_as_float(0x7f800000);
+    if (mxf != -__int_as_float(0x7f800000)) {
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < kFastSplits; ++i)
+        if (i < n) sum += exp2f(l[i] - mxf);
+      Lf = mxf + log2f(sum);
+#pragma unroll
+      for (int i = 0; i < kFastSplits; ++i) {
+        if (i < n) {
+          const float w = exp2f(l[i] - Lf);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            acc[4 * v + 0] += w * x[i][v].x;
+            acc[4 * v + 1] += w * x[i][v].y;
+            acc[4 * v + 2] += w * x[i][v].z;
+            acc[4 * v + 3] += w * x[i][v].w;
+          }
+        }
+      }
+    }
+    uint4 o0, o1;
+    o0.x = pack_bf16x2(acc[0], acc[1]);
+    o0.y = pack_bf16x2(acc[2], acc[3]);
+    o0.z = pack_bf16x2(acc[4], acc[5]);
+    o0.w = pack_bf16x2(acc[6], acc[7]);
+    o1.x = pack_bf16x2(acc[8], acc[9]);
+    o1.y = pack_bf16x2(acc[10], acc[11]);
+    o1.z = pack_bf16x2(acc[12], acc[13]);
+    o1.w = pack_bf16x2(acc[14], acc[15]);
+    reinterpret_cast<uint4*>(out)[0] = o0;
+    reinterpret_cast<uint4*>(out)[1] = o1;
+    if (lane == 0) p.lse[grow] = Lf;
+    return;
+  }
 
   float mx = -__int_as_float(0x7f800000);
   for (int i = lane; i < n; i += 32) mx = fmaxf(mx, p.lse_accum[static_cast<int64_t>(base + i) * p.rows + r]);
