@@ -152,9 +152,11 @@ struct Cfg {
   // aligned (they are read with 16-byte vector loads)
   static constexpr int kBarBytes = (kNumBars * 8 + 127) / 128 * 128;
   // aux: floats m[R], alpha[R], inv_l[R], lse[R], red[4][R]; 16 ints (abort flag,
-  // TMEM base); 256 bytes of per-tile token validity flags (two tiles in flight);
+  // TMEM base); 512 bytes of per-tile token validity flags (a ring of four
+  // tiles: a tile's flags are written once the slots of a tile at least two
+  // back are free, when the softmax of the tile three back is surely done);
   // ints lim[R] (last visible key per row)
-  static constexpr int kAuxBytes = kBarBytes + 8 * R * 4 + 64 + 256 + 4 * R;
+  static constexpr int kAuxBytes = kBarBytes + 8 * R * 4 + 64 + 512 + 4 * R;
   static constexpr int kSmemBytes = kAuxOff + kAuxBytes + 1024;  // + alignment slack
   static constexpr int kOCol = 0;
   static constexpr int kSCol = 4 * R;
@@ -293,7 +295,7 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, cons
             if (item == 0 && lane == 0) {
               // page flag of this tile for the softmax (its readers of two
               // tiles ago are done: their PV released this pair slot)
-              flags[(jt & 1) * 128] = ok ? 1 : 0;
+              flags[(jt & 3) * 128] = ok ? 1 : 0;
             }
             c0 = 2 * item;
             nc = 2;
@@ -663,7 +665,7 @@ __device__ void gather_rows(const CUtensorMap* tm_rows, const DecodeParams& p, c
       const int blk = 2 * h + i;
       const uint32_t use = RG::pair_use(jt, blk);
       if (use > 0 && !warp_wait(bars.pair_empty + RG::pair_slot(jt, blk), (use - 1) & 1, wd)) return false;
-      if (blk == 0) flags[(jt & 1) * 128 + tok] = ok ? 1 : 0;  // token validity for the softmax
+      if (blk == 0) flags[(jt & 3) * 128 + tok] = ok ? 1 : 0;  // token validity for the softmax
       if (lane == 0) mbar_arrive_expect_tx(bars.raw_full + set + blk, (C::kFp8 ? 1 : 2) * 32 * 128);
       armed |= 1u << (set + blk);
       next_par ^= 1u << (set + blk);
@@ -917,7 +919,7 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
   float* lse_s = aux + 3 * R;  // row lse
   float* red = aux + 4 * R;    // [4][R] cross-warp reduction
   // last visible key per row (causal), after the 16 ints and the 256 flag bytes
-  int* lim_s = reinterpret_cast<int*>(aux + 8 * R) + 16 + 64;
+  int* lim_s = reinterpret_cast<int*>(aux + 8 * R) + 16 + 128;
   const uint32_t kv_base = smem_u32(kv);
   const uint32_t p_row_off = (tl & 7) * 2;  // K-major P: byte of this token inside its 16-byte unit
   const uint32_t p_chunk = tl >> 3;         // K-major P: 16-byte unit of this token
@@ -975,7 +977,7 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
       const int pos = j * kTileTokens + tl;  // dense: logical token of this thread
       // gathered modes: the gather warps' per-token flag (dense FP8: position
       // below the length and page usable); dense bf16: length and page flag
-      const bool tok_ok = C::kGather ? flags[(jt & 1) * 128 + tl] != 0 : (pos < L && flags[(jt & 1) * 128] != 0);
+      const bool tok_ok = C::kGather ? flags[(jt & 3) * 128 + tl] != 0 : (pos < L && flags[(jt & 3) * 128] != 0);
       if (tracer) MLA_TR(kTrSmSFull, jt);
 
       // this thread's token, its RH rows of S^T (the two halves of the warp
@@ -1195,9 +1197,9 @@ __global__ void __launch_bounds__(Cfg<R, MODE>::kThreads, 1)
   int* ints = reinterpret_cast<int*>(aux + 8 * R);
   volatile int* abort_flag = ints + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ints + 9);
-  // flags[(jt & 1) * 128 + t]: sparse: token t of tile jt is valid (written by
-  // the gather warps); dense: [0], [1] = the tile's two pages are usable
-  // (written by the producer)
+  // flags[(jt & 3) * 128 + t]: sparse: token t of tile jt is valid (written by
+  // the gather warps); dense: [0] = the tile's page is usable (written by the
+  // producer)
   volatile uint8_t* flags = reinterpret_cast<volatile uint8_t*>(ints + 16);
 
   Bars bars;
