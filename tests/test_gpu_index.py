@@ -183,3 +183,13 @@ def test_indexer_feeds_sparse_decode():
     assert mla.device_status() == 0
     ref_out, ref_lse = run_oracle(dinp)
     compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse, "indexer->decode")
+
+
+@pytest.mark.parametrize("L", [12000, 20000])
+def test_index_largest_topk(L):
+    """top-k 16384 (the largest supported): every visible key when there are fewer, else a selection."""
+    w = W.IndexWorkload(f"imax{L}", batch=1, n_new=1, h_idx=16, topk=16384, seqlens=(L,))
+    inp = W.make_index_inputs(w, seed=L)
+    idx, flags = run_index(inp)
+    assert flags == 0
+    check_selection(idx, inp)

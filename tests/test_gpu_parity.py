@@ -322,3 +322,14 @@ def test_sparse_token_scale_full_size_sampled():
     rows = _sample_rows(inp, 4, np.random.default_rng(9))
     ref_out, ref_lse = run_oracle(inp, rows=rows)
     compare(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, w.name)
+
+
+# ---------------------------------------------------------------- largest supported shapes
+def test_dense_max_rows_per_problem():
+    """1024 query rows per problem (s_q 8 x 128 heads): 16 row groups, causal."""
+    check(W.custom(name="rows1024", batch=2, h_q=128, s_q=8, mode="dense", seqlens=(300, 70), causal=True), 1401)
+
+
+def test_sparse_max_heads():
+    """1024 heads of one sparse query token: 16 row groups reading the same gathered rows."""
+    check(W.custom(name="heads1024", batch=1, h_q=1024, s_q=1, mode="sparse", seqlens=(900,), topk=200), 1402)

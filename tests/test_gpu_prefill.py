@@ -154,3 +154,9 @@ def test_prefill_with_parts_forced_small_splits_problems():
     inp = W.make_prefill_inputs(w, seed=4)
     with env(MLA_NUM_PARTS=7):
         check_prefill(inp)
+
+
+def test_prefill_many_heads():
+    """512 heads: eight row groups of 64 per query token."""
+    w = W.PrefillWorkload("p512", s_q=7, s_kv=900, h_q=512, topk=130, invalid_frac=0.05)
+    check_prefill(W.make_prefill_inputs(w, seed=512))
