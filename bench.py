@@ -369,6 +369,78 @@ def measure_index(device, peaks, reps=10):
             "shape": f"batch {w.batch}, {w.n_new} query tokens each, {w.h_idx} heads x 128, L {w.seqlen}, topk {w.topk}"}
 
 
+# ----------------------------------------------------------------------------
+# the oracle beside each workload: a bounded sample timed on the host cores
+# ----------------------------------------------------------------------------
+def _cpu(sample: str, seconds: float, value: float, unit: str, threads: int = 0) -> dict:
+    threads = threads or os.cpu_count()
+    return {"value": round(value, 6), "unit": unit, "cores": threads, "kind": "oracle",
+            "sample": f"{sample}, {seconds:.2f} s, fp64, {threads} thread{'s' if threads > 1 else ''}"}
+
+
+def oracle_decode_rate(inp, max_rows=32) -> dict:
+    """Oracle decode of the first rows of the first problem; TFLOPS counted as the GPU line counts them
+    (2 * s_k * 1088 per row, s_k = the element's length, or topk in sparse mode)."""
+    import oracle
+    oracle.build()
+    w = inp.workload
+    cpu = inp.to("cpu")
+    rows_per = w.h_q if w.mode == "sparse" else w.s_q * w.h_q
+    rows = np.arange(min(rows_per, max_rows), dtype=np.int64)
+    s_k = w.topk if w.mode == "sparse" else int(cpu.cache_seqlens[0])
+    t = time.perf_counter()
+    oracle.mla_decode(cpu.q, cpu.kvcache, cpu.block_table, cpu.cache_seqlens, cpu.sm_scale, is_causal=w.causal,
+                      indices=cpu.indices, rows=rows, kv_scales=cpu.kv_scales, topk_lengths=cpu.topk_lengths)
+    dt = time.perf_counter() - t
+    flops = 2.0 * len(rows) * s_k * (D_QK + D_V)
+    return _cpu(f"{len(rows)} rows of the first problem (s_k {s_k})", dt, flops / dt / 1e12, "TFLOPS")
+
+
+def oracle_prefill_rate(inp, max_rows=32) -> dict:
+    import oracle
+    oracle.build()
+    w = inp.workload
+    rows = np.arange(min(w.h_q, max_rows), dtype=np.int64)
+    t = time.perf_counter()
+    oracle.sparse_prefill(inp.q.cpu(), inp.kv.cpu(), inp.indices.cpu(), inp.sm_scale, rows=rows)
+    dt = time.perf_counter() - t
+    flops = 2.0 * len(rows) * w.topk * (D_QK + D_V)
+    return _cpu(f"{len(rows)} rows of the first query token", dt, flops / dt / 1e12, "TFLOPS")
+
+
+def oracle_index_rate(inp) -> dict:
+    """Oracle top-k of the first element's query rows; GB/s of that element's algorithmic bytes."""
+    import oracle
+    oracle.build()
+    w = inp.workload
+    r1 = int(inp.row_offsets[1])
+    sub = W.IndexInputs(w, inp.q_codes[:r1].cpu(), inp.q_scales[:r1].cpu(), inp.weights[:r1].cpu(),
+                        torch.tensor([0, r1], dtype=torch.int32), inp.k_codes.cpu(), inp.k_scales.cpu(),
+                        inp.block_table[:1].cpu(), inp.cache_seqlens[:1].cpu(), w.topk, w.relu, inp.seed)
+    t = time.perf_counter()
+    oracle.index_topk(sub)
+    dt = time.perf_counter() - t
+    L = int(sub.cache_seqlens[0])
+    nbytes = L * 132 + r1 * w.h_idx * (128 + 8) + r1 * w.topk * 4
+    return _cpu(f"the first element ({r1} query rows x {L} keys)", dt, nbytes / dt / 1e9, "GB/s", threads=1)
+
+
+def oracle_store_rate(n_tokens=2048) -> dict:
+    import oracle
+    oracle.build()
+    g = torch.Generator().manual_seed(1006)
+    x = torch.randn((n_tokens, D_QK), generator=g).to(torch.bfloat16)
+    per = n_tokens // 64
+    offs = torch.tensor([0, n_tokens], dtype=torch.int32)
+    lens = torch.zeros(1, dtype=torch.int32)
+    table = torch.randperm(per, generator=g).int().reshape(1, per)
+    cache = torch.zeros((per, 64, 1, FP8_ROW), dtype=torch.uint8)
+    t = time.perf_counter()
+    oracle.fp8_cache_store(x, offs, lens, table, cache)
+    dt = time.perf_counter() - t
+    return _cpu(f"{n_tokens} tokens", dt, n_tokens * (D_QK * 2 + FP8_ROW) / dt / 1e9, "GB/s", threads=1)
+
+
 def max_over_ranks(x: float, device) -> float:
     """The largest x over all ranks of the default process group (x itself without one)."""
     import torch.distributed as dist
@@ -493,12 +565,16 @@ def run_mla(args):
                 e["frac_of_bf16_peak"] = round(e["tflops"] / peaks["bf16_tflops"], 4)
             else:
                 e["frac_of_hbm"] = round(e["kv_gbs"] / peaks["hbm_gbs"], 4)
+            e["cpu_oracle"] = oracle_decode_rate(winp)
             extra[name] = e
             del st, winp
             torch.cuda.empty_cache()
         extra["fp8_cache_store"] = measure_store(device, peaks)
+        extra["fp8_cache_store"]["cpu_oracle"] = oracle_store_rate()
         extra["sparse_prefill"] = measure_prefill(device, peaks)
+        extra["sparse_prefill"]["cpu_oracle"] = oracle_prefill_rate(W.make_prefill_inputs("sparse_prefill"))
         extra["fp8_index_topk"] = measure_index(device, peaks)
+        extra["fp8_index_topk"]["cpu_oracle"] = oracle_index_rate(W.make_index_inputs("index_decode"))
         result["workloads"] = extra
         # ---- the oracle on the host cores, bounded sample
         result["cpu_baseline"] = cpu_baseline(inp, target_s=args.cpu_seconds)
