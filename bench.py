@@ -372,6 +372,18 @@ def measure_index(device, peaks, reps=10):
 # ----------------------------------------------------------------------------
 # the oracle beside each workload: a bounded sample timed on the host cores
 # ----------------------------------------------------------------------------
+def _repeat(fn, min_s=1.0, max_reps=50):
+    """Run fn until at least min_s seconds have passed; returns (seconds per run, runs)."""
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        fn()
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_s or n >= max_reps:
+            return dt / n, n
+
+
 def _cpu(sample: str, seconds: float, value: float, unit: str, threads: int = 0) -> dict:
     threads = threads or os.cpu_count()
     return {"value": round(value, 6), "unit": unit, "cores": threads, "kind": "oracle",
@@ -388,12 +400,11 @@ def oracle_decode_rate(inp, max_rows=32) -> dict:
     rows_per = w.h_q if w.mode == "sparse" else w.s_q * w.h_q
     rows = np.arange(min(rows_per, max_rows), dtype=np.int64)
     s_k = w.topk if w.mode == "sparse" else int(cpu.cache_seqlens[0])
-    t = time.perf_counter()
-    oracle.mla_decode(cpu.q, cpu.kvcache, cpu.block_table, cpu.cache_seqlens, cpu.sm_scale, is_causal=w.causal,
-                      indices=cpu.indices, rows=rows, kv_scales=cpu.kv_scales, topk_lengths=cpu.topk_lengths)
-    dt = time.perf_counter() - t
+    dt, n = _repeat(lambda: oracle.mla_decode(cpu.q, cpu.kvcache, cpu.block_table, cpu.cache_seqlens, cpu.sm_scale,
+                                              is_causal=w.causal, indices=cpu.indices, rows=rows,
+                                              kv_scales=cpu.kv_scales, topk_lengths=cpu.topk_lengths))
     flops = 2.0 * len(rows) * s_k * (D_QK + D_V)
-    return _cpu(f"{len(rows)} rows of the first problem (s_k {s_k})", dt, flops / dt / 1e12, "TFLOPS")
+    return _cpu(f"{len(rows)} rows of the first problem (s_k {s_k}) x{n}", dt * n, flops / dt / 1e12, "TFLOPS")
 
 
 def oracle_prefill_rate(inp, max_rows=32) -> dict:
@@ -401,11 +412,10 @@ def oracle_prefill_rate(inp, max_rows=32) -> dict:
     oracle.build()
     w = inp.workload
     rows = np.arange(min(w.h_q, max_rows), dtype=np.int64)
-    t = time.perf_counter()
-    oracle.sparse_prefill(inp.q.cpu(), inp.kv.cpu(), inp.indices.cpu(), inp.sm_scale, rows=rows)
-    dt = time.perf_counter() - t
+    q, kv, idx = inp.q.cpu(), inp.kv.cpu(), inp.indices.cpu()
+    dt, n = _repeat(lambda: oracle.sparse_prefill(q, kv, idx, inp.sm_scale, rows=rows))
     flops = 2.0 * len(rows) * w.topk * (D_QK + D_V)
-    return _cpu(f"{len(rows)} rows of the first query token", dt, flops / dt / 1e12, "TFLOPS")
+    return _cpu(f"{len(rows)} rows of the first query token x{n}", dt * n, flops / dt / 1e12, "TFLOPS")
 
 
 def oracle_index_rate(inp) -> dict:
@@ -417,12 +427,10 @@ def oracle_index_rate(inp) -> dict:
     sub = W.IndexInputs(w, inp.q_codes[:r1].cpu(), inp.q_scales[:r1].cpu(), inp.weights[:r1].cpu(),
                         torch.tensor([0, r1], dtype=torch.int32), inp.k_codes.cpu(), inp.k_scales.cpu(),
                         inp.block_table[:1].cpu(), inp.cache_seqlens[:1].cpu(), w.topk, w.relu, inp.seed)
-    t = time.perf_counter()
-    oracle.index_topk(sub)
-    dt = time.perf_counter() - t
+    dt, n = _repeat(lambda: oracle.index_topk(sub))
     L = int(sub.cache_seqlens[0])
     nbytes = L * 132 + r1 * w.h_idx * (128 + 8) + r1 * w.topk * 4
-    return _cpu(f"the first element ({r1} query rows x {L} keys)", dt, nbytes / dt / 1e9, "GB/s", threads=1)
+    return _cpu(f"the first element ({r1} query rows x {L} keys) x{n}", dt * n, nbytes / dt / 1e9, "GB/s", threads=1)
 
 
 def oracle_store_rate(n_tokens=2048) -> dict:
@@ -435,10 +443,8 @@ def oracle_store_rate(n_tokens=2048) -> dict:
     lens = torch.zeros(1, dtype=torch.int32)
     table = torch.randperm(per, generator=g).int().reshape(1, per)
     cache = torch.zeros((per, 64, 1, FP8_ROW), dtype=torch.uint8)
-    t = time.perf_counter()
-    oracle.fp8_cache_store(x, offs, lens, table, cache)
-    dt = time.perf_counter() - t
-    return _cpu(f"{n_tokens} tokens", dt, n_tokens * (D_QK * 2 + FP8_ROW) / dt / 1e9, "GB/s", threads=1)
+    dt, n = _repeat(lambda: oracle.fp8_cache_store(x, offs, lens, table, cache))
+    return _cpu(f"{n_tokens} tokens x{n}", dt * n, n_tokens * (D_QK * 2 + FP8_ROW) / dt / 1e9, "GB/s", threads=1)
 
 
 def max_over_ranks(x: float, device) -> float:
