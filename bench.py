@@ -81,6 +81,8 @@ NCU_TRAFFIC = {
     "dense_membound": (651.43e6, "e0eed748ba35c440"),
     "dense_computebound": (357.02e6, "e0eed748ba35c440"),
     "sparse_fp8_long": (387.84e6, "e0eed748ba35c440"),
+    "sparse_fp8": (466.70e6, "e0eed748ba35c440"),
+    "dense_membound_fp8": (395.97e6, "e0eed748ba35c440"),
 }
 KERNEL_SOURCES = ("mla_decode.cu", "mla_device.cuh", "mla_internal.h")
 

@@ -105,3 +105,51 @@ def test_store_then_sparse_decode_reads_the_rows():
     from gpu_helpers import compare
     compare(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out.reshape(out.shape),
             ref_lse.reshape(lse.shape), "store+decode")
+
+
+def _boundary_tokens(n_tokens, seed):
+    """Tokens whose tiles put quotients x / scale on and next to E4M3 rounding
+    boundaries: each tile holds its amax (a bf16 value) and values x with
+    448 x / amax equal to a midpoint between two E4M3 values.  With a scale
+    amax / 448 that rounds in float32, the quotient lands within a float32
+    ulp of the midpoint, on either side; with an exact scale, on it (a tie)."""
+    rng = np.random.default_rng(seed)
+    vals = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    mids = (vals[:-1] + vals[1:]) / 2
+    amaxes = [1.0, 1.5, 2.5, 0.75, 100.0, 3e-3, 448.0, 1344.0, 5.0, 0.3]
+    x = np.zeros((n_tokens, 576))
+    near = ties = 0
+    for t in range(n_tokens):
+        for tile in range(4):
+            amax = float(torch.tensor(amaxes[(4 * t + tile) % len(amaxes)] * (1 + 0.01 * rng.integers(0, 8)))
+                         .to(torch.bfloat16))
+            scale = np.float32(amax) / np.float32(448.0)
+            cand = amax * mids / 448.0
+            exact = torch.tensor(cand).to(torch.bfloat16).double().numpy() == cand
+            pick = cand[exact & (cand <= amax)]
+            row = rng.uniform(-amax, amax, 128)
+            row[0] = amax
+            k = min(len(pick), 127)
+            row[1:1 + k] = pick[rng.permutation(len(pick))[:k]] * rng.choice([-1.0, 1.0], k)
+            x[t, 128 * tile:128 * tile + 128] = row
+            q = np.abs(np.float32(row[1:1 + k]) / scale).astype(np.float64)
+            m = np.abs(row[1:1 + k]) * 448.0 / amax
+            near += int(np.sum((q != m) & (np.abs(q - m) <= m * 2.0 ** -21)))
+            ties += int(np.sum(q == m))
+        x[t, 512:] = rng.standard_normal(64)
+    return torch.tensor(x).to(torch.bfloat16), near, ties
+
+
+def test_store_values_at_e4m3_rounding_boundaries():
+    """Quotients on (ties to the even code) and within a float32 ulp of E4M3
+    rounding boundaries quantise exactly as the float32 division decides."""
+    n = 256
+    x, near, ties = _boundary_tokens(n, seed=11)
+    assert near > 100 and ties > 1000         # the data does reach both kinds of boundary case
+    offs = torch.tensor([0, n], dtype=torch.int32)
+    lens = torch.tensor([0], dtype=torch.int32)
+    table = torch.arange(n // 64, dtype=torch.int32)[None]
+    cache = torch.zeros((n // 64, 64, 1, 656), dtype=torch.uint8)
+    got, ref, skipped, flags = _run(x, offs, lens, table, cache)
+    assert skipped == 0 and flags == 0
+    assert np.array_equal(got, ref)
