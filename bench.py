@@ -83,6 +83,8 @@ NCU_TRAFFIC = {
     "sparse_fp8_long": (387.84e6, "e0eed748ba35c440"),
     "sparse_fp8": (466.70e6, "e0eed748ba35c440"),
     "dense_membound_fp8": (395.97e6, "e0eed748ba35c440"),
+    "sparse_bf16": (663.87e6, "e0eed748ba35c440"),
+    "sparse_fp8_token": (432.76e6, "e0eed748ba35c440"),
 }
 KERNEL_SOURCES = ("mla_decode.cu", "mla_device.cuh", "mla_internal.h")
 
