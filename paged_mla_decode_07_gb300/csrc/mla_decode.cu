@@ -140,9 +140,16 @@ struct Cfg {
   static constexpr int kAuxOff = (kPOff + kPBufBytes + 1023) / 1024 * 1024;
   // barriers: q_full, q_empty, chunk_full[2*kNA + kNB], pair_empty[kNA], rope_empty[kNB],
   // s_full[2], s_empty[2], p_full[2], o_full, o_empty, mma_done, o_done[2], raw_full[kNumRaw]
-  // one "tile full" barrier per tile in flight (at most three: the ring
-  // holds under three tiles), used round robin: tile jt -> jt % 3, phase jt / 3
-  static constexpr int kNumFull = 3;
+  // "tile full" barriers for the tiles in flight (at most three: the ring
+  // holds under three tiles), used round robin: tile jt -> jt % 3, phase
+  // jt / 3.  One per tile, or one per item of a tile (pairs 0..3, RoPE) where
+  // the S MMAs start on each item as it is written: dense with 64 rows (the
+  // tile loads are the chain there) and bf16 row gathers (the in-place
+  // swizzle); both measured faster that way, the 16-row dense path and the
+  // FP8 gathers slower.
+  static constexpr bool kItemFull = (MODE == kModeSparseBf16) || (MODE == kModeDense && R == 64);
+  static constexpr int kFullItems = kItemFull ? 5 : 1;
+  static constexpr int kNumFull = 3 * kFullItems;
   // sparse: raw FP8 rows of a tile land by row gathers in the upper chunk of
   // each pair slot (codes) and in the RoPE slot; raw_full[5 * (jt & 1) + b]
   // (b = 0..3 pairs, 4 = RoPE) completes when tile jt's have arrived
@@ -162,9 +169,10 @@ struct Cfg {
   static constexpr int kSCol = 4 * R;
   static constexpr int kTmemCols = (6 * R <= 128) ? 128 : ((6 * R <= 256) ? 256 : 512);
 
-  // arrivals on a tile's full barrier: dense 1 (the producer, + the tile's
-  // TMA bytes); sparse 4 (each gather warp once it has written its part)
-  static constexpr int kFullArrivals = kGather ? 4 : 1;
+  // arrivals on a full barrier: dense 1 (the producer, + the TMA bytes);
+  // gathered 4 per tile (each gather warp once it has written its part) or 2
+  // per item (the two warps writing it)
+  static constexpr int kFullArrivals = kGather ? (kItemFull ? 2 : 4) : 1;
   static_assert(kPBytes <= kKvChunkBytes || !kPAlias, "P must fit in the RoPE chunk");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(R == 16 || R == 32 || R == 64, "rows per CTA");
@@ -175,7 +183,7 @@ struct Cfg {
 struct Bars {
   uint64_t* q_full;
   uint64_t* q_empty;
-  uint64_t* full;        // [3]: tile jt's nine chunks are in shared memory (barrier jt % 3)
+  uint64_t* full;        // [3 * kFullItems]: tile jt's chunks (or one item of them) are in shared memory
   uint64_t* pair_empty;  // [kNA]
   uint64_t* rope_empty;  // [kNB]
   uint64_t* s_full;    // [2]
@@ -281,7 +289,7 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, cons
         const int pg = j < p.block_table_stride ? bt[j] : -1;
         const bool ok = pg >= 0 && pg < p.num_pages;
         if (!ok && lane == 0) atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
-        uint64_t* fb = bars.full + fidx;
+        uint64_t* fb = bars.full + C::kFullItems * fidx;
         bool tile_armed = false;
         // RoPE chunk first when its slot frees at S^T (separate P); pairs first
         // when P lives in the RoPE slot until the PV MMAs are done
@@ -306,10 +314,19 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, cons
             nc = 1;
           }
           // the tile's full barrier is armed with all its bytes before its first
-          // copy, after that copy's slot wait (which implies the barrier's
-          // previous phase, three tiles back, has completed); the item's
-          // chunks are issued by one lane each
-          if (!tile_armed) {
+          // copy (per item: the item's barrier with the item's bytes), after
+          // that copy's slot wait (which implies the barrier's previous phase,
+          // three tiles back, has completed); the item's chunks are issued by
+          // one lane each
+          uint64_t* ib = fb;
+          if (C::kItemFull) {
+            const int bi = C::kFullItems * fidx + item;
+            ib = bars.full + bi;
+            if (lane == 0) mbar_arrive_expect_tx(ib, ok ? static_cast<uint32_t>(nc * C::kKvChunkBytes) : 0u);
+            __syncwarp();
+            armed |= 1u << bi;
+            next_par ^= 1u << bi;
+          } else if (!tile_armed) {
             if (lane == 0) mbar_arrive_expect_tx(fb, ok ? static_cast<uint32_t>(kNumChunks * C::kKvChunkBytes) : 0u);
             __syncwarp();
             tile_armed = true;
@@ -317,7 +334,7 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, cons
             next_par ^= 1u << fidx;
           }
           if (ok && lane < nc)
-            tma_load_3d(kv + RG::chunk_off(jt, c0 + lane), tm_kv, fb, 0, c0 + lane, pg * kPageSize, pol_kv);
+            tma_load_3d(kv + RG::chunk_off(jt, c0 + lane), tm_kv, ib, 0, c0 + lane, pg * kPageSize, pol_kv);
           __syncwarp();
           if (lane == 0) {
             if (c0 == 0) MLA_TR(kTrProdChunk0, jt);
@@ -428,17 +445,23 @@ __device__ void s_issuer(const Segments& sg, uint32_t tmem, uint8_t* kv, uint8_t
       // the softmax has read S^T of tile jt-2 from this buffer
       if (jt >= 2 && !mbar_wait_u32(s_empty + 8 * sb, ((jt >> 1) - 1) & 1, wd)) goto done;
       tc_fence_after();
-      if (!mbar_wait_u32(full + 8 * fidx, static_cast<uint32_t>(fphase) & 1u, wd)) goto done;
+      const uint32_t fpar = static_cast<uint32_t>(fphase) & 1u;
+      const uint32_t fbar = full + 8 * C::kFullItems * fidx;
+      if (!C::kItemFull && !mbar_wait_u32(fbar, fpar, wd)) goto done;
       if (++fidx == 3) {
         fidx = 0;
         ++fphase;
       }
-      if (lane == 0) MLA_TR(kTrMmaKv0, jt);
       const uint32_t d_s = tmem + C::kSCol + sb * R;
-      // S^T = K Q^T over the nine chunks, 36 MMAs back to back (pairs of
-      // chunks sit together in a pair slot)
+      // S^T = K Q^T over the nine chunks, 36 MMAs (pairs of chunks sit
+      // together in a pair slot): back to back once the tile is in, or item
+      // by item as each is written, in the order they are written (row
+      // gathers: blocks 0 and 2, then 1 and 3, then RoPE)
 #pragma unroll 1
-      for (int pb = 0; pb < 5; ++pb) {
+      for (int q = 0; q < 5; ++q) {
+        const int pb = (C::kGather && C::kItemFull) ? (q < 4 ? ((q & 1) << 1) | (q >> 1) : 4) : q;
+        if (C::kItemFull && !mbar_wait_u32(fbar + 8 * pb, fpar, wd)) goto done;
+        if (q == 0 && lane == 0) MLA_TR(kTrMmaKv0, jt);
         const uint32_t pa = pb < 4 ? kvb + C::kPairOff + cur.pair_slot(pb) * C::kPairBytes
                                    : kvb + C::kRopeOff + cur.rslot * C::kKvChunkBytes;
         const uint64_t a0 = kHiK | (pa >> 4);
@@ -449,7 +472,7 @@ __device__ void s_issuer(const Segments& sg, uint32_t tmem, uint8_t* kv, uint8_t
           const int h = i >> 2, kk = i & 3;  // chunk 2pb+h, k step kk
           if (elect_one())
             umma_bf16_ss_fast(d_s, a0 + h * (C::kKvChunkBytes >> 4) + 2 * kk,
-                              b0 + h * (C::kQChunkBytes >> 4) + 2 * kk, kIdS, (pb | i) != 0);
+                              b0 + h * (C::kQChunkBytes >> 4) + 2 * kk, kIdS, (q | i) != 0);
           __syncwarp();
         }
       }
@@ -729,9 +752,12 @@ __device__ void gather_rows(const CUtensorMap* tm_rows, const DecodeParams& p, c
     // dequantise tile jt in place: token tok's 128 code bytes of block b sit
     // at row tok of chunk 2b+1; they become row tok of chunks 2b and 2b+1
     // (bf16, 128-byte swizzle).  Units are read in a per-thread rotated order.
+    // bf16 rows: each permuted block gets this warp's arrival on the block's
+    // full barrier (after the proxy fence that orders it for the MMAs).
     {
       const int set = 5 * (jt & 1);
       const uint32_t par = static_cast<uint32_t>(jt >> 1) & 1u;  // phase of set (jt & 1) for tile jt
+      uint64_t* fb = bars.full + C::kFullItems * RG::full_index(jt);
 #pragma unroll 1
       for (int i = 0; i < 2; ++i) {
         const int blk = 2 * h + i;
@@ -739,6 +765,11 @@ __device__ void gather_rows(const CUtensorMap* tm_rows, const DecodeParams& p, c
         if (!C::kFp8) {
           swizzle_row_in_place(kv_base + RG::chunk_off(jt, 2 * blk) + tok * 128, tsw, ok_c);
           swizzle_row_in_place(kv_base + RG::chunk_off(jt, 2 * blk + 1) + tok * 128, tsw, ok_c);
+          if (C::kItemFull) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(fb + blk);
+          }
           continue;
         }
         const float scale = __uint_as_float(i == 0 ? sc_c.x : sc_c.y);
@@ -764,13 +795,20 @@ __device__ void gather_rows(const CUtensorMap* tm_rows, const DecodeParams& p, c
         // RoPE: already bf16; permute the 16-byte units into the swizzled order
         if (!warp_wait(bars.raw_full + set + 4, par, wd)) goto drain;
         swizzle_row_in_place(kv_base + RG::chunk_off(jt, 8) + tok * 128, tsw, ok_c);
+        if (C::kItemFull) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(fb + 4);
+        }
+      }
+      if (!C::kItemFull) {
+        // this warp's part of the tile is written: one arrival on the tile's
+        // full barrier (after the proxy fence that orders it for the MMAs)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(fb);
       }
     }
-    // this warp's part of the tile is written: one arrival on the tile's full
-    // barrier (after the proxy fence that orders it for the MMAs)
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bars.full + RG::full_index(jt));
     if (tid == 0) MLA_TR(kTrGatherDone, jt);
     // then tile jt+1's row gathers (their slots free once the PV of tile jt-1 is done)
     if (nxt.valid && !issue(jt + 1, row_n, ok_n)) goto drain;
@@ -966,11 +1004,12 @@ __device__ void softmax_epilogue(const DecodeParams& p, const Segments& sg, int 
     for (int j = tb; j < te; ++j, ++jt) {
       const int sb = jt & 1;
       if (tracer) MLA_TR(kTrSmWaitS, jt);
-      // S^T of this tile is complete; the wait on the tile's full barrier
-      // (already complete) orders the loader's validity flags before our reads
+      // S^T of this tile is complete; the wait on the tile's (first) full
+      // barrier (already complete) orders the loader's validity flags before
+      // our reads
       {
         bool ok = mbar_wait(bars.s_full + sb, (jt >> 1) & 1, wd);
-        ok = ok && mbar_wait(bars.full + Ring<C>::full_index(jt), Ring<C>::full_parity(jt), wd);
+        ok = ok && mbar_wait(bars.full + C::kFullItems * Ring<C>::full_index(jt), Ring<C>::full_parity(jt), wd);
         if (!group_ok(ok)) return;
       }
       tc_fence_after();
