@@ -193,8 +193,10 @@ def test_schedule_covers_every_tile_once(topk, lens):
 
 
 # ---------------------------------------------------------------- device status
-def test_bad_page_is_flagged_not_faulted():
-    w = W.custom(name="badpage", batch=2, h_q=16, s_q=1, mode="dense", seqlens=(200, 100))
+@pytest.mark.parametrize("h_q", [16, 64])
+def test_bad_page_is_flagged_not_faulted(h_q):
+    """16 rows: one full barrier per tile; 64 rows: one per ring item, armed with no bytes for a bad page."""
+    w = W.custom(name="badpage", batch=2, h_q=h_q, s_q=1, mode="dense", seqlens=(200, 100))
     inp = W.make_inputs(w, seed=3)
     bt = inp.block_table.clone()
     bt[0, 1] = inp.kvcache.shape[0] + 5

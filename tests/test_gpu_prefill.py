@@ -45,6 +45,26 @@ def test_sparse_decode_over_bf16_cache(h_q):
     assert np.all(out[2, 0] == 0) and np.all(lse[2, 0] == -np.inf)
 
 
+def test_sparse_bf16_bad_page_skips_its_tokens():
+    """A block-table entry outside the pool: flagged, and its tokens count as invalid ids."""
+    w = W.custom(name="sbbad", batch=2, h_q=64, s_q=1, mode="sparse", fp8=False, seqlens=(700, 300), topk=256)
+    inp = W.make_inputs(w, seed=5)
+    good_table = inp.block_table
+    bt = good_table.clone()
+    bt[0, 3] = inp.kvcache.shape[0] + 7          # tokens 192..255 of element 0 sit on no page
+    inp.block_table = bt
+    out, lse, flags = run_cuda(inp)
+    assert flags & mla.DEVICE_BAD_PAGE
+    idx = inp.indices.clone()
+    e0 = idx[0]
+    e0[(e0 >= 192) & (e0 < 256)] = -1
+    assert int(((inp.indices[0] >= 192) & (inp.indices[0] < 256)).sum()) > 0
+    inp.indices = idx
+    inp.block_table = good_table
+    ref_out, ref_lse = run_oracle(inp)
+    compare(out, lse, ref_out, ref_lse, w.name)
+
+
 def test_sparse_bf16_and_fp8_caches_agree_on_dequantised_values():
     """The same keys as FP8 rows and as their dequantised bf16 values give the same result."""
     w = W.custom(name="sx", batch=2, h_q=64, s_q=1, mode="sparse", seqlens=(1500, 600), topk=256)
