@@ -38,8 +38,10 @@
  * query token i), sparse mode = the valid ids of indices[b, i, :].  A row
  * with an empty key set gets out = 0 and lse = -inf.
  *
- * Supported modes: dense over a bf16 cache and sparse (top-k) over an FP8
- * cache, page_size 64.  Other combinations return MLA_ERR_UNSUPPORTED.
+ * Supported modes (page_size 64): dense or sparse (top-k), each over a bf16
+ * cache or an FP8 cache (is_fp8 selects the format); an FP8 cache may also
+ * hold 640-byte rows (codes + RoPE) with one float32 scale per token in a
+ * separate array (kv_scales).  Other page sizes return MLA_ERR_UNSUPPORTED.
  */
 #ifndef MLA_H_
 #define MLA_H_
