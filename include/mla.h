@@ -105,14 +105,16 @@ mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, in
 typedef struct {
   const void* q;                  /* bf16 [batch, s_q, h_q, 576] */
   int batch, s_q, h_q;
-  const void* kvcache;            /* bf16 [num_pages,64,1,576] or uint8 [num_pages,64,1,656] */
+  const void* kvcache;            /* bf16 [num_pages,64,1,576], uint8 [num_pages,64,1,656], or with
+                                     kv_scales uint8 [num_pages,64,1,640] */
   int num_pages, page_size;       /* page_size must be 64 */
   const int32_t* block_table;     /* int32 [batch, block_table_stride] */
   int block_table_stride;         /* >= ceil(max seqlen / page_size) */
   const int32_t* cache_seqlens;   /* int32 [batch] */
   float sm_scale;                 /* softmax scale applied to q.k */
   int is_causal;                  /* dense only: query token i sees keys <= seqlen - s_q + i */
-  int is_fp8;                     /* 1: FP8 656-byte cache rows, 0: bf16 576-value rows (either mode) */
+  int is_fp8;                     /* 1: FP8 cache rows (656 bytes; 640 with kv_scales), 0: bf16
+                                     576-value rows (either mode) */
   const int32_t* indices;         /* sparse: int32 [batch, s_q, topk]; NULL for dense */
   int topk;                       /* 0 for dense */
   const int32_t* sched;           /* from mla_get_metadata with the same batch/s_q/h_q/topk */
