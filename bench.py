@@ -186,17 +186,18 @@ class DecodeStep:
         self.d = inp.to(device) if inp.q.device != torch.device(device) else inp
         self.topk = 0 if self.d.indices is None else self.d.indices.shape[-1]
         b, s, h = self.w.batch, self.w.s_q, self.w.h_q
+        self.is_fp8 = self.d.kvcache.dtype == torch.uint8
+        self.cfg = dict(h_q=h, s_q=s, topk=self.topk, is_fp8=self.is_fp8)
         self.out = torch.empty((b, s, h, D_V), dtype=torch.bfloat16, device=device)
         self.lse = torch.empty((b, s, h), dtype=torch.float32, device=device)
-        self.ws = torch.empty(max(256, mla.workspace_size(b, s, h, self.topk)), dtype=torch.uint8, device=device)
-        ns, nn = mla.metadata_size(b, s, h, self.topk)
+        self.ws = torch.empty(max(256, mla.workspace_size(b, **self.cfg)), dtype=torch.uint8, device=device)
+        ns, nn = mla.metadata_size(b, **self.cfg)
         self.sched = torch.empty(ns, dtype=torch.int32, device=device)
         self.nsplit = torch.empty(nn, dtype=torch.int32, device=device)
         self.g_step = self.g_decode = None
 
     def metadata(self):
-        self.mla.get_metadata(self.d.cache_seqlens, self.w.s_q, self.w.h_q, self.topk, sched=self.sched,
-                              num_splits=self.nsplit)
+        self.mla.get_metadata(self.d.cache_seqlens, **self.cfg, sched=self.sched, num_splits=self.nsplit)
 
     def decode(self):
         d = self.d
@@ -257,23 +258,29 @@ def time_events(fn, n: int):
     return [a.elapsed_time(b) for a, b in ev]
 
 
-def e2e_step_factory(inp, device):
+def e2e_step_factory(inp, device, resident_cache=False):
     """End to end through the public API: pinned host inputs -> H2D copies -> schedule + decode ->
-    D2H of out and lse, every step."""
+    D2H of out and lse, every step.  With resident_cache the KV cache stays in device memory (as it
+    does in a serving loop) and only q, the block table and the lengths cross the link."""
     import paged_mla_decode_07_gb300 as mla
     w = inp.workload
-    host = {k: getattr(inp, k).cpu().pin_memory() for k in ("q", "kvcache", "block_table", "cache_seqlens")}
+    names = ("q", "block_table", "cache_seqlens") if resident_cache else ("q", "kvcache", "block_table",
+                                                                          "cache_seqlens")
+    host = {k: getattr(inp, k).cpu().pin_memory() for k in names}
     if inp.indices is not None:
         host["indices"] = inp.indices.cpu().pin_memory()
     dev = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    if resident_cache:
+        dev["kvcache"] = inp.kvcache.to(device)
     topk = 0 if inp.indices is None else inp.indices.shape[-1]
     b, s, h = w.batch, w.s_q, w.h_q
+    cfg = dict(h_q=h, s_q=s, topk=topk, is_fp8=inp.kvcache.dtype == torch.uint8)
     out = torch.empty((b, s, h, D_V), dtype=torch.bfloat16, device=device)
     lse = torch.empty((b, s, h), dtype=torch.float32, device=device)
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    ws = torch.empty(max(256, mla.workspace_size(b, s, h, topk)), dtype=torch.uint8, device=device)
-    ns, nn = mla.metadata_size(b, s, h, topk)
+    ws = torch.empty(max(256, mla.workspace_size(b, **cfg)), dtype=torch.uint8, device=device)
+    ns, nn = mla.metadata_size(b, **cfg)
     sched = torch.empty(ns, dtype=torch.int32, device=device)
     nsplit = torch.empty(nn, dtype=torch.int32, device=device)
     h2d = sum(v.numel() * v.element_size() for v in host.values())
@@ -282,7 +289,7 @@ def e2e_step_factory(inp, device):
     def step():
         for k, v in host.items():
             dev[k].copy_(v, non_blocking=True)
-        mla.get_metadata(dev["cache_seqlens"], s, h, topk, sched=sched, num_splits=nsplit)
+        mla.get_metadata(dev["cache_seqlens"], **cfg, sched=sched, num_splits=nsplit)
         mla.decode(dev["q"], dev["kvcache"], dev["block_table"], dev["cache_seqlens"], inp.sm_scale, sched, nsplit,
                    is_causal=w.causal, indices=dev.get("indices"), out=out, lse=lse, workspace=ws)
         out_h.copy_(out, non_blocking=True)
@@ -291,8 +298,9 @@ def e2e_step_factory(inp, device):
     return step, h2d, d2h
 
 
-def measure_workload(name, device, reps=20, warmup=3):
-    """Kernel-level measurement of one workload (decode call = split-KV kernel + combine)."""
+def measure_workload(name, device, reps=50, warmup=10):
+    """Kernel-level measurement of one workload (decode call = split-KV kernel + combine): the
+    median of `reps` calls after `warmup` untimed ones."""
     inp = W.make_inputs(name, device=device)
     st = DecodeStep(inp, device)
     st.capture()
@@ -511,10 +519,10 @@ def run_mla(args):
     flags = mla.device_status()
     value = job_throughput(a["bytes"], world, ms) / 1e9  # GB/s over all ranks
 
-    # ---- dominant kernel: decode call (split-KV kernel + combine), same workload
+    # ---- dominant kernel: decode call (split-KV kernel + combine), same workload: median of >= 50
     step.metadata()
-    dts = time_events(step.replay_decode, max(10, args.steps))
-    dec_ms = statistics.mean(dts)
+    dts = time_events(step.replay_decode, max(50, args.steps))
+    dec_ms = statistics.median(dts)
     wl = inp.workload
     if wname in ("dense_membound", "tiny", "dense_membound_fp8"):
         roof = {"bound": "hbm", "achieved": round(a["bytes"] / (dec_ms * 1e-3) / 1e9, 1), "peak": peaks["hbm_gbs"],
@@ -551,17 +559,22 @@ def run_mla(args):
     torch.cuda.empty_cache()
 
     if rank == 0 and world == 1 and not args.no_extras and wname == HEADLINE:
-        # ---- end to end through the public API with host buffers
-        estep, h2d, d2h = e2e_step_factory(inp, device)
-        for _ in range(2):
-            estep()
-        et = time_events(estep, max(3, min(args.steps, 10)))
-        ems = statistics.mean(et)
-        result["e2e"] = {"value": round(a["bytes"] / (ems * 1e-3) / 1e9, 1), "unit": "GB/s",
-                         "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                         "ms_per_step": round(ems, 4), "note": "inputs incl. the whole KV cache copied from pinned host memory each step"}
-        del estep
-        torch.cuda.empty_cache()
+        # ---- end to end through the public API with host buffers: every input (the whole KV
+        # cache included) copied in each step, and beside it the same with the cache resident
+        for key, resident in (("e2e", False), ("e2e_resident_cache", True)):
+            estep, h2d, d2h = e2e_step_factory(inp, device, resident_cache=resident)
+            for _ in range(3):
+                estep()
+            et = time_events(estep, max(5, min(args.steps, 20)))
+            ems = statistics.median(et)
+            result[key] = {"value": round(a["bytes"] / (ems * 1e-3) / 1e9, 1), "unit": "GB/s",
+                           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                           "ms_per_step": round(ems, 4),
+                           "note": "KV cache resident in device memory; q, block table and lengths copied "
+                                   "from pinned host memory each step, out and lse copied back" if resident else
+                                   "inputs incl. the whole KV cache copied from pinned host memory each step"}
+            del estep
+            torch.cuda.empty_cache()
         # ---- the other workloads (kernel level)
         extra = {}
         for name in ("tiny", "dense_computebound", "sparse_fp8", "sparse_fp8_long", "dense_membound_fp8",

@@ -72,33 +72,47 @@ typedef enum {
 #define MLA_DEVICE_BAD_SCHEDULE 0x4u /* the schedule did not match the arguments; results invalid */
 
 /* ABI version of this header (incremented on incompatible change). */
-#define MLA_ABI_VERSION 2
+#define MLA_ABI_VERSION 3
 int mla_abi_version(void);
 
+/* A decode configuration is the tuple (batch, h_q, s_q, topk, is_fp8), in the
+ * order of the FlashMLA article's get_mla_metadata(cache_seqlens, ..., h_q,
+ * is_fp8, topk) (usage section); topk = 0 selects dense mode, is_fp8 = 1 an
+ * FP8 cache.  The three calls below and mla_decode must see the same tuple:
+ * the schedule depends on it (rows per CTA, the kernel mode and the cost of a
+ * tile in that mode) and on the current device's SM count, so a schedule
+ * belongs to one configuration on one device. */
+
 /* Sizes of the two metadata arrays for a decode configuration on the
- * current device (int32 element counts).  topk = 0 selects dense mode.
- * sched has one 8-int record per scheduled work part; num_splits has one
- * entry per problem plus one (problem = batch element in dense mode,
- * (batch element, query token) pair in sparse mode). */
-mla_status mla_metadata_size(int batch, int s_q, int h_q, int topk, int* sched_elems,
+ * current device (int32 element counts).  sched has one 8-int record per
+ * scheduled work part; num_splits has one entry per problem plus one
+ * (problem = batch element in dense mode, (batch element, query token) pair
+ * in sparse mode). */
+mla_status mla_metadata_size(int batch, int h_q, int s_q, int topk, int is_fp8, int* sched_elems,
                              int* num_splits_elems);
 
 /* Scratch bytes that mla_decode needs for split-KV partial results
  * (fp32 partial outputs and their log-sum-exps): min(2 * parts,
  * problems + parts) slots of rows x 513 floats, bounded by the part count
  * whatever the batch size. */
-mla_status mla_workspace_size(int batch, int s_q, int h_q, int topk, size_t* bytes);
+mla_status mla_workspace_size(int batch, int h_q, int s_q, int topk, int is_fp8, size_t* bytes);
 
 /* (1) Tile schedule for one decode step ("get_mla_metadata").
  * cache_seqlens: device int32 [batch]; sched, num_splits: device int32
  * buffers of the sizes above, written on `stream`.  The work of all problems
- * (64-token tiles of their key ranges) is divided into contiguous ranges of
- * near-equal cost, one per part; num_splits holds the exclusive prefix sum of
- * the split-KV partial-result slots of each problem: as many as the parts
- * touching it when there are two or more, none when one part covers it
- * (that part writes the output directly).  Reusable by every layer of the
- * step as long as cache_seqlens, batch, s_q, h_q and topk are unchanged. */
-mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, int h_q, int topk,
+ * (64-token tiles of their key ranges, each tile weighted by the cost of its
+ * mode, FP8 tiles 1.5 times a bf16 tile, plus a fixed start-up cost per
+ * problem segment) is divided into contiguous ranges of near-equal cost,
+ * one per part; num_splits holds the exclusive prefix sum of the split-KV
+ * partial-result slots of each problem: as many as the parts touching it
+ * when there are two or more, none when one part covers it (that part writes
+ * the output directly).  Every sched record also holds the part count and a
+ * tag of the configuration; mla_decode checks both on the device against its
+ * own and, on a mismatch, sets MLA_DEVICE_BAD_SCHEDULE and computes nothing
+ * (it reads only the first record before that check).  Reusable by every
+ * layer of the step as long as cache_seqlens and the configuration are
+ * unchanged. */
+mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int h_q, int s_q, int topk, int is_fp8,
                             int32_t* sched, int32_t* num_splits, mla_stream_t stream);
 
 /* Arguments of mla_decode.  Pointers are device pointers unless noted. */
@@ -117,7 +131,7 @@ typedef struct {
                                      576-value rows (either mode) */
   const int32_t* indices;         /* sparse: int32 [batch, s_q, topk]; NULL for dense */
   int topk;                       /* 0 for dense */
-  const int32_t* sched;           /* from mla_get_metadata with the same batch/s_q/h_q/topk */
+  const int32_t* sched;           /* from mla_get_metadata with the same batch/h_q/s_q/topk/is_fp8 */
   const int32_t* num_splits;
   void* workspace;                /* >= mla_workspace_size() bytes, 256-byte aligned */
   size_t workspace_bytes;
@@ -136,7 +150,11 @@ typedef struct {
 
 /* (2) Decode ("flash_mla_with_kvcache"): split-KV attention kernel followed
  * by a log-sum-exp combine of the split partials, both on `stream`.
- * Alignment: q, kvcache, out, lse, workspace 16-byte aligned. */
+ * Alignment: q, kvcache and out 16-byte aligned, lse, block_table and
+ * kv_scales 4-byte aligned, workspace 256-byte aligned.  Every wait inside
+ * the kernels is bounded (2 s by default; the environment variable
+ * MLA_WATCHDOG_NS sets another limit in nanoseconds): a wait that runs out
+ * sets MLA_DEVICE_TIMEOUT and the kernel returns. */
 mla_status mla_decode(const mla_decode_args* args, mla_stream_t stream);
 
 /* Decode without any caller scratch, for callers that cannot allocate device
@@ -263,6 +281,16 @@ mla_status mla_index_topk_workspace_size(int num_tokens, int block_table_stride,
  * selected) and an element with more than max_new_tokens rows sets
  * MLA_DEVICE_BAD_SCHEDULE (its rows get -1). */
 mla_status mla_index_topk(const mla_index_topk_args* args, mla_stream_t stream);
+
+/* Test hooks, process-wide, for the library's own tests; production callers
+ * never need them.  num_parts > 0 makes every later schedule (metadata,
+ * workspace and decode geometry) use that many parts instead of the count
+ * the SM count gives, to exercise split-KV paths on small inputs; 0 restores
+ * the default.  debug_stall != 0 makes the decode kernel's softmax role wait
+ * on a barrier that nothing completes, so that its bounded wait runs out and
+ * MLA_DEVICE_TIMEOUT is reported; 0 restores normal operation.  The pages
+ * describe no such call.  Returns MLA_ERR_INVALID_ARG for num_parts < 0. */
+mla_status mla_test_hooks(int num_parts, int debug_stall);
 
 /* Synchronises `stream`, returns the device status bits accumulated since the
  * last call in *flags (0 = clean) and clears them.  Returns

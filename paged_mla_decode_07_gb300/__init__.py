@@ -7,7 +7,7 @@ not pass them, and calls the C entry points on the current CUDA stream.
 Every step of decode runs in the library's CUDA kernels; there is no other
 code path.  If ``libmla.so`` has not been built, every call raises.
 
-    sched, num_splits = get_metadata(cache_seqlens, s_q, h_q, topk)
+    sched, num_splits = get_metadata(cache_seqlens, h_q=..., s_q=..., topk=..., is_fp8=...)
     out, lse = decode(q, kvcache, block_table, cache_seqlens, sm_scale,
                       sched, num_splits, is_causal=..., indices=...)
     out, lse = sparse_prefill(q, kv, indices, sm_scale)
@@ -99,12 +99,14 @@ def lib():
             I, P, S = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
             L.mla_abi_version.restype = I
             L.mla_last_error.restype = ctypes.c_char_p
-            L.mla_metadata_size.argtypes = [I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)]
+            L.mla_metadata_size.argtypes = [I, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)]
             L.mla_metadata_size.restype = I
-            L.mla_workspace_size.argtypes = [I, I, I, I, ctypes.POINTER(S)]
+            L.mla_workspace_size.argtypes = [I, I, I, I, I, ctypes.POINTER(S)]
             L.mla_workspace_size.restype = I
-            L.mla_get_metadata.argtypes = [P, I, I, I, I, P, P, P]
+            L.mla_get_metadata.argtypes = [P, I, I, I, I, I, P, P, P]
             L.mla_get_metadata.restype = I
+            L.mla_test_hooks.argtypes = [I, I]
+            L.mla_test_hooks.restype = I
             L.mla_decode.argtypes = [ctypes.POINTER(DecodeArgs), P]
             L.mla_decode.restype = I
             L.mla_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
@@ -154,37 +156,46 @@ def _need(t, name, dtype, device=None, ndim=None):
         raise ValueError(f"{name} must be contiguous")
 
 
-def metadata_size(batch: int, s_q: int, h_q: int, topk: int = 0) -> Tuple[int, int]:
+def metadata_size(batch: int, *, h_q: int, s_q: int, topk: int, is_fp8: bool) -> Tuple[int, int]:
+    """(sched int32 elements, num_splits int32 elements) for one decode configuration."""
     a, b = ctypes.c_int(), ctypes.c_int()
-    _check(lib().mla_metadata_size(batch, s_q, h_q, topk, ctypes.byref(a), ctypes.byref(b)))
+    _check(lib().mla_metadata_size(batch, h_q, s_q, topk, int(bool(is_fp8)), ctypes.byref(a), ctypes.byref(b)))
     return a.value, b.value
 
 
-def workspace_size(batch: int, s_q: int, h_q: int, topk: int = 0) -> int:
+def workspace_size(batch: int, *, h_q: int, s_q: int, topk: int, is_fp8: bool) -> int:
+    """Scratch bytes mla_decode needs for one decode configuration."""
     n = ctypes.c_size_t()
-    _check(lib().mla_workspace_size(batch, s_q, h_q, topk, ctypes.byref(n)))
+    _check(lib().mla_workspace_size(batch, h_q, s_q, topk, int(bool(is_fp8)), ctypes.byref(n)))
     return n.value
 
 
-def get_metadata(cache_seqlens: torch.Tensor, s_q: int, h_q: int, topk: int = 0, stream=None,
+def get_metadata(cache_seqlens: torch.Tensor, *, h_q: int, s_q: int, topk: int, is_fp8: bool, stream=None,
                  sched: Optional[torch.Tensor] = None, num_splits: Optional[torch.Tensor] = None):
-    """Tile schedule for one decode step; reuse it for every layer of the step."""
+    """Tile schedule for one decode step; reuse it for every layer of the step.  The keywords name
+    the decode configuration (topk = 0: dense; is_fp8: the cache format) that decode() will run."""
     _need(cache_seqlens, "cache_seqlens", torch.int32, ndim=1)
     if not cache_seqlens.is_cuda:
         raise ValueError("cache_seqlens must be a CUDA tensor")
     dev = cache_seqlens.device
     batch = cache_seqlens.shape[0]
-    ns, nn = metadata_size(batch, s_q, h_q, topk)
+    ns, nn = metadata_size(batch, h_q=h_q, s_q=s_q, topk=topk, is_fp8=is_fp8)
     if sched is None:
         sched = torch.empty(ns, dtype=torch.int32, device=dev)
     if num_splits is None:
         num_splits = torch.empty(nn, dtype=torch.int32, device=dev)
     if sched.numel() < ns or num_splits.numel() < nn:
         raise ValueError("sched / num_splits buffers are too small")
-    _check(lib().mla_get_metadata(ctypes.c_void_p(cache_seqlens.data_ptr()), batch, s_q, h_q, topk,
-                                  ctypes.c_void_p(sched.data_ptr()), ctypes.c_void_p(num_splits.data_ptr()),
-                                  _stream(stream)))
+    _check(lib().mla_get_metadata(ctypes.c_void_p(cache_seqlens.data_ptr()), batch, h_q, s_q, topk,
+                                  int(bool(is_fp8)), ctypes.c_void_p(sched.data_ptr()),
+                                  ctypes.c_void_p(num_splits.data_ptr()), _stream(stream)))
     return sched, num_splits
+
+
+def set_test_hooks(num_parts: int = 0, debug_stall: bool = False) -> None:
+    """Library test hooks (mla_test_hooks): force the schedule's part count (0 = default) and make
+    the decode kernel's softmax role stall so that its bounded wait runs out."""
+    _check(lib().mla_test_hooks(int(num_parts), int(bool(debug_stall))))
 
 
 def decode(q: torch.Tensor, kvcache: torch.Tensor, block_table: torch.Tensor, cache_seqlens: torch.Tensor,
@@ -241,7 +252,8 @@ def decode(q: torch.Tensor, kvcache: torch.Tensor, block_table: torch.Tensor, ca
     if out.numel() != batch * s_q * h_q * D_V or lse.numel() != batch * s_q * h_q:
         raise ValueError("out / lse have the wrong size")
     if workspace is None:
-        workspace = torch.empty(max(workspace_size(batch, s_q, h_q, topk), 256), dtype=torch.uint8, device=dev)
+        workspace = torch.empty(max(workspace_size(batch, h_q=h_q, s_q=s_q, topk=topk, is_fp8=is_fp8), 256),
+                                dtype=torch.uint8, device=dev)
     a = DecodeArgs()
     a.q = q.data_ptr()
     a.batch, a.s_q, a.h_q = batch, s_q, h_q

@@ -16,7 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmla.so")
-SOURCES = ["mla_api.cu", "mla_sched.cu", "mla_decode.cu", "mla_combine.cu", "mla_noalloc.cu", "mla_store.cu", "mla_index.cu"]
+SOURCES = ["mla_api.cu", "mla_sched.cu", "mla_decode.cu", "mla_decode_pair.cu", "mla_combine.cu", "mla_noalloc.cu",
+           "mla_store.cu", "mla_index.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr"]

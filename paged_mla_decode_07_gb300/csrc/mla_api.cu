@@ -9,6 +9,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -75,12 +76,19 @@ mla_status device_info(uint32_t** status, int* sm_count) {
   return MLA_OK;
 }
 
-int sm_count_override() {
-  const char* s = getenv("MLA_NUM_PARTS");
-  return s ? atoi(s) : 0;
-}
+// The CTA-pair decode kernel for problems of more than 64 rows over the bf16
+// cache (mla_decode_pair.cu).
+constexpr bool kPairDecode = false;
 
-mla_status geometry(int batch, int s_q, int h_q, int topk, Geometry* g) {
+// Test hooks (mla_test_hooks): a forced part count and a stalled softmax role.
+std::atomic<int> g_test_num_parts{0};
+std::atomic<int> g_test_debug_stall{0};
+
+// Kernel mode of a decode: 0 dense over the bf16 cache, 1 sparse over the FP8
+// cache, 2 dense over the FP8 cache, 3 sparse over bf16 rows.
+int decode_mode(int topk, int is_fp8) { return topk > 0 ? (is_fp8 ? 1 : 3) : (is_fp8 ? 2 : 0); }
+
+mla_status geometry(int batch, int h_q, int s_q, int topk, int is_fp8, Geometry* g) {
   if (batch < 1) return fail(MLA_ERR_INVALID_ARG, "batch must be >= 1 (got %d)", batch);
   if (s_q < 1) return fail(MLA_ERR_INVALID_ARG, "s_q must be >= 1 (got %d)", s_q);
   if (h_q < 1) return fail(MLA_ERR_INVALID_ARG, "h_q must be >= 1 (got %d)", h_q);
@@ -94,18 +102,30 @@ mla_status geometry(int batch, int s_q, int h_q, int topk, Geometry* g) {
     return fail(MLA_ERR_UNSUPPORTED, "%s = %lld query rows per problem exceeds 1024",
                 topk > 0 ? "h_q" : "s_q*h_q", rows);
   if (topk > (1 << 24)) return fail(MLA_ERR_UNSUPPORTED, "topk = %d too large", topk);
+  if (is_fp8 != 0 && is_fp8 != 1) return fail(MLA_ERR_INVALID_ARG, "is_fp8 must be 0 or 1 (got %d)", is_fp8);
   int sms = 0;
   mla_status st = device_info(nullptr, &sms);
   if (st != MLA_OK) return st;
-  const int ov = sm_count_override();
-  if (ov > 0) sms = ov;
   g->num_problems = static_cast<int>(np);
   g->rows = static_cast<int>(rows);
-  g->rpc = rows_per_cta(g->rows);
-  g->row_groups = (g->rows + g->rpc - 1) / g->rpc;
+  g->mode = decode_mode(topk, is_fp8);
   g->sm_count = sms;
-  g->num_parts = sms / g->row_groups;
+  // problems of more than 64 rows over the bf16 cache run on CTA pairs (128
+  // rows and 128-token tiles per pair); everything else on single CTAs
+  g->pair = (kPairDecode && g->mode == 0 && g->rows > 64) ? 1 : 0;
+  g->rpc = g->pair ? 128 : rows_per_cta(g->rows);
+  g->tile_tokens = g->pair ? 128 : kTileTokens;
+  g->row_groups = (g->rows + g->rpc - 1) / g->rpc;
+  g->num_parts = (g->pair ? sms / 2 : sms) / g->row_groups;
+  const int forced = g_test_num_parts.load();
+  if (forced > 0) g->num_parts = forced;
   if (g->num_parts < 1) g->num_parts = 1;
+  // schedule costs in quarters of a 64-token bf16 tile: FP8 rows are
+  // dequantised before their MMAs, so their tiles weigh more against the
+  // fixed start-up of a segment
+  g->tile_cost = (is_fp8 ? 6 : 4) * (g->tile_tokens / kTileTokens);
+  g->overhead = 8;
+  g->tag = g->rpc | (g->mode << 8) | ((g->tile_tokens / kTileTokens) << 12) | (g->pair << 15);
   return MLA_OK;
 }
 
@@ -220,7 +240,7 @@ struct PrefillLayout {
 };
 mla_status prefill_layout(int s_q, int h_q, int topk, Geometry* g, PrefillLayout* L) {
   const int chunk = s_q < kMaxProblems ? s_q : kMaxProblems;
-  mla_status st = geometry(1, chunk, h_q, topk, g);
+  mla_status st = geometry(1, h_q, chunk, topk, 0, g);
   if (st != MLA_OK) return st;
   size_t ob, lb;
   workspace_layout(*g, &ob, &lb);
@@ -239,21 +259,29 @@ int mla_abi_version(void) { return MLA_ABI_VERSION; }
 
 const char* mla_last_error(void) { return g_error.c_str(); }
 
-mla_status mla_metadata_size(int batch, int s_q, int h_q, int topk, int* sched_elems, int* num_splits_elems) {
+mla_status mla_test_hooks(int num_parts, int debug_stall) {
+  if (num_parts < 0) return fail(MLA_ERR_INVALID_ARG, "num_parts must be >= 0 (got %d)", num_parts);
+  g_test_num_parts.store(num_parts);
+  g_test_debug_stall.store(debug_stall != 0 ? 1 : 0);
+  return ok();
+}
+
+mla_status mla_metadata_size(int batch, int h_q, int s_q, int topk, int is_fp8, int* sched_elems,
+                             int* num_splits_elems) {
   if (!sched_elems) return fail(MLA_ERR_INVALID_ARG, "sched_elems is NULL");
   if (!num_splits_elems) return fail(MLA_ERR_INVALID_ARG, "num_splits_elems is NULL");
   Geometry g{};
-  mla_status st = geometry(batch, s_q, h_q, topk, &g);
+  mla_status st = geometry(batch, h_q, s_q, topk, is_fp8, &g);
   if (st != MLA_OK) return st;
   *sched_elems = g.num_parts * kSchedInts;
   *num_splits_elems = g.num_problems + 1;
   return ok();
 }
 
-mla_status mla_workspace_size(int batch, int s_q, int h_q, int topk, size_t* bytes) {
+mla_status mla_workspace_size(int batch, int h_q, int s_q, int topk, int is_fp8, size_t* bytes) {
   if (!bytes) return fail(MLA_ERR_INVALID_ARG, "bytes is NULL");
   Geometry g{};
-  mla_status st = geometry(batch, s_q, h_q, topk, &g);
+  mla_status st = geometry(batch, h_q, s_q, topk, is_fp8, &g);
   if (st != MLA_OK) return st;
   size_t ob, lb;
   workspace_layout(g, &ob, &lb);
@@ -261,18 +289,15 @@ mla_status mla_workspace_size(int batch, int s_q, int h_q, int topk, size_t* byt
   return ok();
 }
 
-mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int s_q, int h_q, int topk, int32_t* sched,
-                            int32_t* num_splits, mla_stream_t stream) {
+mla_status mla_get_metadata(const int32_t* cache_seqlens, int batch, int h_q, int s_q, int topk, int is_fp8,
+                            int32_t* sched, int32_t* num_splits, mla_stream_t stream) {
   if (!cache_seqlens) return fail(MLA_ERR_INVALID_ARG, "cache_seqlens is NULL");
   if (!sched) return fail(MLA_ERR_INVALID_ARG, "sched is NULL");
   if (!num_splits) return fail(MLA_ERR_INVALID_ARG, "num_splits is NULL");
   Geometry g{};
-  mla_status st = geometry(batch, s_q, h_q, topk, &g);
+  mla_status st = geometry(batch, h_q, s_q, topk, is_fp8, &g);
   if (st != MLA_OK) return st;
-  uint32_t* status = nullptr;
-  st = device_info(&status, nullptr);
-  if (st != MLA_OK) return st;
-  cudaError_t e = launch_metadata(cache_seqlens, batch, s_q, h_q, topk, g, sched, num_splits, status,
+  cudaError_t e = launch_metadata(cache_seqlens, s_q, topk, g, sched, num_splits,
                                   reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "metadata kernel launch");
   return ok();
@@ -310,8 +335,9 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
   if (!aligned(a->lse, 4)) return fail(MLA_ERR_INVALID_ARG, "lse is not 4-byte aligned");
   if (!aligned(a->block_table, 4)) return fail(MLA_ERR_INVALID_ARG, "block_table is not 4-byte aligned");
 
+  if (a->is_fp8 != 0 && a->is_fp8 != 1) return fail(MLA_ERR_INVALID_ARG, "is_fp8 must be 0 or 1 (got %d)", a->is_fp8);
   Geometry g{};
-  mla_status st = geometry(a->batch, a->s_q, a->h_q, a->topk, &g);
+  mla_status st = geometry(a->batch, a->h_q, a->s_q, a->topk, a->is_fp8, &g);
   if (st != MLA_OK) return st;
   size_t ob, lb;
   workspace_layout(g, &ob, &lb);
@@ -326,11 +352,9 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
 
   CUtensorMap tm_q, tm_kv;
   const long long qrows = static_cast<long long>(a->batch) * a->s_q * a->h_q;
-  st = encode_rows_map(&tm_q, a->q, qrows, g.rpc, "q");
+  st = encode_rows_map(&tm_q, a->q, qrows, g.pair ? g.rpc / 2 : g.rpc, "q");
   if (st != MLA_OK) return st;
-  // kernel mode: 0 dense over the bf16 cache, 1 sparse over the FP8 cache,
-  // 2 dense over the FP8 cache, 3 sparse over the bf16 cache
-  const int mode = sparse ? (a->is_fp8 ? 1 : 3) : (a->is_fp8 ? 2 : 0);
+  const int mode = g.mode;
   const long long cache_rows = static_cast<long long>(a->num_pages) * kPageSize;
   if (mode == 0)
     st = encode_rows_map(&tm_kv, a->kvcache, cache_rows, kPageSize, "kvcache");
@@ -366,18 +390,16 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
   p.num_parts = g.num_parts;
   p.max_slots = max_slots(g);
   p.is_causal = a->is_causal ? 1 : 0;
-  p.evict_first = g.row_groups == 1 ? 1 : 0;
-  {
-    const char* s = getenv("MLA_DEBUG_STALL");  // watchdog test hook (tests only)
-    p.debug_stall = (s && atoi(s) != 0) ? 1 : 0;
-  }
+  p.evict_first = (g.row_groups == 1 && !g.pair) ? 1 : 0;
+  p.sched_tag = g.tag;
+  p.debug_stall = g_test_debug_stall.load();
   p.scale_log2 = a->sm_scale * 1.4426950408889634f;
   p.kv_scales = a->kv_scales;
   p.topk_lengths = a->topk_lengths;
   p.fp8_rope_off = a->kv_scales ? kDv : kFp8RopeOffset;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_decode(tm_q, tm_kv, p, g.rpc, mode, s);
+  cudaError_t e = g.pair ? launch_decode_pair(tm_q, tm_kv, p, s) : launch_decode(tm_q, tm_kv, p, g.rpc, mode, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
 
   CombineParams cp;
@@ -476,13 +498,13 @@ mla_status mla_sparse_prefill(const mla_sparse_prefill_args* a, mla_stream_t str
   for (int c0 = 0; c0 < a->s_q; c0 += kMaxProblems) {
     const int chunk = a->s_q - c0 < kMaxProblems ? a->s_q - c0 : kMaxProblems;
     Geometry gc{};
-    st = geometry(1, chunk, a->h_q, a->topk, &gc);
+    st = geometry(1, a->h_q, chunk, a->topk, 0, &gc);
     if (st != MLA_OK) return st;
     const char* q = static_cast<const char*>(a->q) + static_cast<size_t>(c0) * a->h_q * kDqk * 2;
     CUtensorMap tm_q;
     st = encode_rows_map(&tm_q, q, static_cast<long long>(chunk) * a->h_q, gc.rpc, "q");
     if (st != MLA_OK) return st;
-    cudaError_t e = launch_metadata(nullptr, 1, chunk, a->h_q, a->topk, gc, sched, num_splits, status, s);
+    cudaError_t e = launch_metadata(nullptr, chunk, a->topk, gc, sched, num_splits, s);
     if (e != cudaSuccess) return cuda_fail(e, "metadata kernel launch");
 
     DecodeParams p;
@@ -509,6 +531,7 @@ mla_status mla_sparse_prefill(const mla_sparse_prefill_args* a, mla_stream_t str
     p.num_parts = gc.num_parts;
     p.max_slots = max_slots(gc);
     p.evict_first = gc.row_groups == 1 ? 1 : 0;
+    p.sched_tag = gc.tag;
     p.flat_rows = a->s_kv;
     p.scale_log2 = a->sm_scale * 1.4426950408889634f;
     e = launch_decode(tm_q, tm_kv, p, gc.rpc, 3, s);

@@ -1307,12 +1307,20 @@ __global__ void __launch_bounds__(Cfg<R, MODE>::kThreads, 1)
   if (threadIdx.x == 0 && blockIdx.x < 1024) g_mla_cta[2 * blockIdx.x] = global_timer_ns();
 #endif
   Segments sg;
-  const int32_t* sr = p.sched + static_cast<int64_t>(part) * kSchedInts;
-  sg.p0 = sr[kSchedP0];
-  sg.t0 = sr[kSchedT0];
-  sg.p1 = sr[kSchedP1];
-  sg.t1 = sr[kSchedT1];
-  const int split0 = sr[kSchedSplit0];
+  int split0 = 0;
+  // record 0 names the part count and geometry the schedule was made for;
+  // only a matching schedule is read further
+  if (p.sched[kSchedParts] == p.num_parts && p.sched[kSchedTag] == p.sched_tag) {
+    const int32_t* sr = p.sched + static_cast<int64_t>(part) * kSchedInts;
+    sg.p0 = sr[kSchedP0];
+    sg.t0 = sr[kSchedT0];
+    sg.p1 = sr[kSchedP1];
+    sg.t1 = sr[kSchedT1];
+    split0 = sr[kSchedSplit0];
+  } else {
+    sg.p0 = -1;  // reported and skipped below
+    sg.t0 = sg.p1 = sg.t1 = 0;
+  }
   sg.np = p.num_problems;
   sg.s_q = p.s_q;
   sg.topk = p.topk;

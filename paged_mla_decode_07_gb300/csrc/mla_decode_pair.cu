@@ -1,0 +1,717 @@
+// K1p — paged MLA decode on CTA pairs (tcgen05 cta_group::2), dense over the
+// bf16 cache, for problems of more than 64 query rows.
+//
+// What is computed is the same as in the single-CTA kernel (mla_decode.cu):
+// per query row, softmax(q K^T * sm_scale) V over the row's keys with
+// V = K[:, :512] (the MQA form of MLA, Modular design-doc overview, section 9
+// "Multi-Head Latent Attention"), with online softmax across tiles (overview,
+// section 6 "Matmul to Flash Attention"), and a split-KV partial with its
+// log-sum-exp where a part covers only some of a problem's tiles (FlashMLA
+// article, Design 5; merged by the combine kernel).
+//
+// Formulation.  The two CTAs of a cluster (one TPC) work together on 128
+// query rows of a problem, 64 rows each, and on 128-token tiles, one 64-token
+// page each.  Both matrix products are pair MMAs issued by one thread of the
+// even CTA: each CTA supplies half of A's rows and half of B's columns from
+// its own shared memory and receives its half of the result rows in its own
+// TMEM.  For an M = 128 pair result a CTA's row r lies in TMEM lane r for the
+// first half of the columns and in lane 64 + r for the second half.
+//     S[row, tok]  = Q[row, :] . K[tok, :]      M = 128 rows, N = 128 tokens, K = 576
+//                    A: the CTA's 64 query rows, B: the CTA's own page
+//     O[row, dv]  += P[row, tok] . V[tok, dv]    M = 128 rows, N = 256 dv (twice), K = 128 tokens
+//                    A: the CTA's P rows, B: the CTA's share of the 256 dv
+// An N = 256 pair MMA runs at the tensor pipe's full rate and an N = 128 one
+// at 57 %, where a single-CTA M = 64 score MMA runs at 28 %.  Each CTA loads
+// one page per tile for the scores, and it keeps the running O of its own
+// rows for all 512 value dims (64 rows x 512 fp32 = 256 TMEM columns), so
+// the online-softmax rescale and the epilogue stay inside the CTA.
+//
+// The value dims a CTA supplies to the PV product must sit at the same
+// shared-memory address in both CTAs while holding different dims (dv 0-127
+// and 256-383 for the even CTA, 128-255 and 384-511 for the odd one), so
+// those dims of both pages of a tile are loaded into a separate set of slots.
+//
+// Shared memory (1024-byte aligned, identical in both CTAs):
+//   Q    9 chunks [64 rows][64 dims] bf16, 128-byte swizzle         72 KB
+//   KS   9 slots: chunk k of the CTA's own page (score operand)      72 KB
+//   KV   8 slots: page t of the tile, share s at slot 4t + s          64 KB
+//   P    2 chunks [64 rows][64 tokens] bf16 (PV operand)             16 KB
+//   barriers, row statistics
+// TMEM (512 columns, allocated for the pair): O at [0, 256) (block m of 256
+// dv at [128m, 128m + 128)), S double buffer at [256, 320) and [320, 384).
+//
+// Synchronisation.  Only the even CTA issues MMAs.  Its producer arms its
+// own barriers with its own bytes; the odd CTA's copies complete on the odd
+// CTA's barriers and its idle MMA-issuer warp forwards each completion to the
+// even CTA with a remote arrive, so every CTA can drain its own copies.  The
+// MMA warps commit to the barriers of both CTAs at once (multicast); the odd
+// CTA's softmax warps arrive remotely on the even CTA's barriers.  Every wait
+// is bounded by the watchdog; a CTA that gives up records MLA_DEVICE_TIMEOUT
+// and unwinds, and its partner's waits then run out too.
+//
+// Roles (384 threads):
+//   warp 0      Q + score-operand producer (TMA), both CTAs
+//   warp 1      score MMA issuer (even CTA) / completion forwarder (odd CTA)
+//   warp 2      TMEM allocation, then value-operand producer (TMA), both CTAs
+//   warp 3      PV MMA issuer (even CTA)
+//   warps 4-11  softmax + epilogue: warp w reads TMEM lane quarter w % 4, so
+//               a thread owns one row and one half of the tile (page), and
+//               the two warpgroups split that half's 64 tokens
+#include "mla_device.cuh"
+#include "mla_internal.h"
+
+namespace mla {
+namespace {
+
+constexpr int kPairRows = 64;            // query rows per CTA
+constexpr int kPairTile = 128;           // tokens per tile (one page per CTA)
+constexpr int kPairChunk = 8192;         // [64 rows or tokens][64 dims] bf16
+constexpr int kPairThreads = 384;
+constexpr int kPairQOff = 0;
+constexpr int kPairKsOff = 9 * kPairChunk;
+constexpr int kPairKvOff = 18 * kPairChunk;
+constexpr int kPairPOff = 26 * kPairChunk;
+constexpr int kPairAuxOff = 28 * kPairChunk;  // 229376
+constexpr int kPairBarBytes = 256;
+// aux: barriers, m[64], red[4][64] (partial row maxima / sums), ints (abort flag, TMEM base)
+constexpr int kPairAuxBytes = kPairBarBytes + 64 * 4 + 4 * 64 * 4 + 64;
+constexpr int kPairSmemBytes = kPairAuxOff + kPairAuxBytes + 1024;  // + alignment slack
+static_assert(kPairSmemBytes <= 232448, "shared memory budget");
+constexpr uint32_t kPairOCol = 0;
+constexpr uint32_t kPairSCol = 256;
+constexpr uint32_t kPairTmemCols = 512;
+constexpr float kPairNegInf = -__builtin_huge_valf();
+constexpr float kPairRescale = 8.0f;     // log2 units: P <= 2^8 before a max update is forced
+constexpr uint32_t kPairSmBar = 1;       // named barrier of the 256 softmax threads
+constexpr uint32_t kPairRegsCtl = 88, kPairRegsSm = 208, kPairLaunchRegs = 168;
+static_assert(128 * kPairRegsCtl + 256 * kPairRegsSm <= 65536, "register split");
+
+enum PairBar {
+  kBQFull = 0,    // Q of the segment loaded (even: both CTAs, odd: own)
+  kBQEmpty = 1,   // the segment's last score MMAs are done (Q reusable)
+  kBKsFull = 2,   // [9] own page chunk k loaded (even: both CTAs, odd: own)
+  kBKsEmpty = 11, // [9] the score MMAs have read chunk slot k
+  kBKvFull = 20,  // the tile's value-operand slots are loaded (own CTA)
+  kBKvEmpty = 21, // the tile's PV MMAs are done (value slots reusable)
+  kBSFull = 22,   // [2] S of a tile is in TMEM
+  kBSEmpty = 24,  // [2] (even) both CTAs' softmax warps have read an S buffer
+  kBPFull = 26,   // (even) both CTAs' P of the tile is written, O rescaled
+  kBPEmpty = 27,  // the tile's PV MMAs are done (P reusable, O current)
+  kBOFull = 28,   // the segment's last PV MMAs are done
+  kBOEmpty = 29,  // (even) both CTAs' epilogues have read O
+  kBMmaDone = 30, // (even) drain of the MMA issuers
+  kBCount = 31
+};
+static_assert(kBCount * 8 <= kPairBarBytes, "barrier area");
+
+// Segment iterator over the part's problems (128-token tiles); every role
+// derives the identical sequence.
+struct PairSeg {
+  int p0, t0, p1, t1, np, s_q;
+  const int32_t* seqlens;
+  __device__ int last() const { return p1 < np ? p1 : np - 1; }
+  __device__ void range(int p, int& tb, int& te) const {
+    const int n = problem_tiles(seqlens, p, s_q, 0, kPairTile);
+    tb = (p == p0) ? t0 : 0;
+    te = (p == p1) ? t1 : n;
+    if (te > n) te = n;
+  }
+};
+
+// Page of half h (0, 1) of tile j of element b: its id, or -1 when it holds
+// no cached token or its block-table entry is unusable (flagged).
+__device__ __forceinline__ int tile_page(const DecodeParams& p, int b, int L, int j, int h, bool flag) {
+  const int pi = 2 * j + h;
+  if (pi * kPageSize >= L) return -1;
+  const int pg = pi < p.block_table_stride ? p.block_table[static_cast<int64_t>(b) * p.block_table_stride + pi] : -1;
+  if (pg < 0 || pg >= p.num_pages) {
+    if (flag) atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
+    return -1;
+  }
+  return pg;
+}
+
+__device__ __forceinline__ void tma3(uint32_t dst, const void* map, uint32_t bar, int c0, int c1, int c2,
+                                     uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+
+// Warp-uniform bounded wait on a barrier of this CTA.
+__device__ __forceinline__ bool pair_wait(uint32_t bar, uint32_t parity, const Watchdog& wd) {
+  uint64_t t0 = 0;
+  while (__shfl_sync(0xffffffffu, mbar_test_wait_u32(bar, parity) ? 1 : 0, 0) == 0) {
+    if (t0 == 0) {
+      t0 = global_timer_ns();
+    } else if (__shfl_sync(0xffffffffu, wd.aborted() ? 1 : 0, 0)) {
+      return false;
+    } else if (__shfl_sync(0xffffffffu, global_timer_ns() - t0 > wd.limit_ns ? 1 : 0, 0)) {
+      if ((threadIdx.x & 31) == 0) wd.trip(MLA_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Bounded wait that ignores the abort flag (drain of own asynchronous work).
+__device__ __forceinline__ void pair_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test_wait_u32(bar, parity))
+    if (global_timer_ns() - t0 > limit_ns) return;
+}
+
+// ---------------------------------------------------------------------------
+// warp 0: Q and the score operand (the CTA's own page of each tile)
+// ---------------------------------------------------------------------------
+__device__ void pair_producer_ks(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, const DecodeParams& p,
+                                 const PairSeg& sg, int g, int rank, uint32_t smem, uint32_t bars,
+                                 const Watchdog& wd) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t pol = l2_policy_evict_normal();
+  uint32_t armed = 0, next_par = 0;  // ks_full barriers armed (bit k), parity of their next phase
+  int q_armed = 0, jt = 0;
+  for (int prob = sg.p0; prob <= sg.last(); ++prob) {
+    int tb, te;
+    sg.range(prob, tb, te);
+    if (tb >= te) continue;
+    if (q_armed > 0 && !pair_wait(bars + 8 * kBQEmpty, (q_armed - 1) & 1, wd)) goto drain;
+    {
+      const int row0 = prob * p.rows + g * 2 * kPairRows + rank * kPairRows;
+      if (lane == 0) mbar_arrive_expect_tx_u32(bars + 8 * kBQFull, kNumChunks * kPairChunk);
+      __syncwarp();
+      if (lane < kNumChunks)
+        tma3(smem + kPairQOff + lane * kPairChunk, tm_q, bars + 8 * kBQFull, 0, lane, row0, pol);
+      __syncwarp();
+      ++q_armed;
+    }
+    {
+      const int b = prob;
+      const int L = sg.seqlens[b];
+      for (int j = tb; j < te; ++j, ++jt) {
+        const int pg = tile_page(p, b, L, j, rank, lane == 0);
+#pragma unroll 1
+        for (int k = 0; k < kNumChunks; ++k) {
+          const uint32_t fb = bars + 8 * (kBKsFull + k);
+          if (jt > 0 && !pair_wait(bars + 8 * (kBKsEmpty + k), (jt - 1) & 1, wd)) goto drain;
+          if (lane == 0) mbar_arrive_expect_tx_u32(fb, pg >= 0 ? kPairChunk : 0u);
+          __syncwarp();
+          armed |= 1u << k;
+          next_par ^= 1u << k;
+          if (pg >= 0 && lane == 0) tma3(smem + kPairKsOff + k * kPairChunk, tm_kv, fb, 0, k, pg * kPageSize, pol);
+          __syncwarp();
+        }
+      }
+    }
+  }
+drain:
+  if (lane == 0) {
+#pragma unroll 1
+    for (int k = 0; k < kNumChunks; ++k)
+      if ((armed >> k) & 1u) pair_drain(bars + 8 * (kBKsFull + k), ((next_par >> k) & 1u) ^ 1u, wd.limit_ns);
+    if (q_armed > 0) pair_drain(bars + 8 * kBQFull, (q_armed - 1) & 1, wd.limit_ns);
+  }
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// warp 2 (after the TMEM allocation): the value operand — for both pages of
+// each tile, the two 128-dv blocks this CTA supplies (chunks 4m + 2 rank and
+// 4m + 2 rank + 1 for m = 0, 1), into slots 4t + s
+// ---------------------------------------------------------------------------
+__device__ void pair_producer_kv(const CUtensorMap* tm_kv, const DecodeParams& p, const PairSeg& sg, int rank,
+                                 uint32_t smem, uint32_t bars, const Watchdog& wd) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t pol = l2_policy_evict_normal();
+  const uint32_t fb = bars + 8 * kBKvFull;
+  int jt = 0;
+  bool armed = false;
+  for (int prob = sg.p0; prob <= sg.last(); ++prob) {
+    int tb, te;
+    sg.range(prob, tb, te);
+    if (tb >= te) continue;
+    const int b = prob;
+    const int L = sg.seqlens[b];
+    for (int j = tb; j < te; ++j, ++jt) {
+      const int pg0 = tile_page(p, b, L, j, 0, false);
+      const int pg1 = tile_page(p, b, L, j, 1, false);
+      if (jt > 0 && !pair_wait(bars + 8 * kBKvEmpty, (jt - 1) & 1, wd)) goto drain;
+      const uint32_t bytes = static_cast<uint32_t>(((pg0 >= 0) + (pg1 >= 0)) * 4 * kPairChunk);
+      if (lane == 0) mbar_arrive_expect_tx_u32(fb, bytes);
+      __syncwarp();
+      armed = true;
+      if (lane < 8) {
+        const int t = lane >> 2, s = lane & 3;
+        const int pg = t ? pg1 : pg0;
+        const int c = 4 * (s >> 1) + 2 * rank + (s & 1);
+        if (pg >= 0) tma3(smem + kPairKvOff + (4 * t + s) * kPairChunk, tm_kv, fb, 0, c, pg * kPageSize, pol);
+      }
+      __syncwarp();
+    }
+  }
+drain:
+  if (lane == 0 && armed) pair_drain(fb, (jt - 1) & 1, wd.limit_ns);
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// warp 1 of the odd CTA: forwards the completion of its Q and score-operand
+// copies to the even CTA's barriers (which count one arrival per CTA)
+// ---------------------------------------------------------------------------
+__device__ void pair_forwarder(const PairSeg& sg, uint32_t bars, uint32_t bars_even, const Watchdog& wd) {
+  const int lane = threadIdx.x & 31;
+  int seg = 0, jt = 0;
+  for (int prob = sg.p0; prob <= sg.last(); ++prob) {
+    int tb, te;
+    sg.range(prob, tb, te);
+    if (tb >= te) continue;
+    if (!pair_wait(bars + 8 * kBQFull, seg & 1, wd)) return;
+    if (lane == 0) mbar_arrive_cluster(bars_even + 8 * kBQFull);
+    __syncwarp();
+    for (int j = tb; j < te; ++j, ++jt) {
+#pragma unroll 1
+      for (int k = 0; k < kNumChunks; ++k) {
+        if (!pair_wait(bars + 8 * (kBKsFull + k), jt & 1, wd)) return;
+        if (lane == 0) mbar_arrive_cluster(bars_even + 8 * (kBKsFull + k));
+        __syncwarp();
+      }
+    }
+    ++seg;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// warp 1 of the even CTA: score MMAs, S = Q K^T over the pair
+// ---------------------------------------------------------------------------
+__device__ void pair_s_issuer(const PairSeg& sg, uint32_t tmem, uint32_t smem, uint32_t bars, const Watchdog& wd) {
+  constexpr uint32_t kIdS = idesc_bf16_f32(128, kPairTile, 0, 0);
+  constexpr uint64_t kHiK = smem_desc_hi(16, 1024);
+  const int lane = threadIdx.x & 31;
+  int jt = 0, seg = 0;
+  for (int prob = sg.p0; prob <= sg.last(); ++prob) {
+    int tb, te;
+    sg.range(prob, tb, te);
+    if (tb >= te) continue;
+    if (!pair_wait(bars + 8 * kBQFull, seg & 1, wd)) goto done;
+    tc_fence_after();
+    for (int j = tb; j < te; ++j, ++jt) {
+      const int sb = jt & 1;
+      if (jt >= 2 && !pair_wait(bars + 8 * (kBSEmpty + sb), ((jt >> 1) - 1) & 1, wd)) goto done;
+      tc_fence_after();
+      const uint32_t d = tmem + kPairSCol + sb * (kPairTile / 2);
+#pragma unroll 1
+      for (int k = 0; k < kNumChunks; ++k) {
+        if (!pair_wait(bars + 8 * (kBKsFull + k), jt & 1, wd)) goto done;
+        tc_fence_after();
+        const uint64_t a0 = kHiK | ((smem + kPairQOff + k * kPairChunk) >> 4);
+        const uint64_t b0 = kHiK | ((smem + kPairKsOff + k * kPairChunk) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          if (elect_one()) umma2_bf16_ss(d, a0 + 2 * kk, b0 + 2 * kk, kIdS, (k | kk) != 0);
+          __syncwarp();
+        }
+        if (elect_one()) umma2_commit_both(bars + 8 * (kBKsEmpty + k));
+        __syncwarp();
+      }
+      if (elect_one()) {
+        umma2_commit_both(bars + 8 * (kBSFull + sb));
+        if (j == te - 1) umma2_commit_both(bars + 8 * kBQEmpty);
+      }
+      __syncwarp();
+    }
+    ++seg;
+  }
+done:
+  if (elect_one()) umma2_commit_own(bars + 8 * kBMmaDone);
+  __syncwarp();
+  if (lane == 0) pair_drain(bars + 8 * kBMmaDone, 0, wd.limit_ns);
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// warp 3 of the even CTA: PV MMAs, O += P V over the pair
+// ---------------------------------------------------------------------------
+__device__ void pair_pv_issuer(const PairSeg& sg, uint32_t tmem, uint32_t smem, uint32_t bars, const Watchdog& wd) {
+  constexpr uint32_t kIdO = idesc_bf16_f32(128, 256, 0, 1);  // A = P (K-major), B = V (MN-major)
+  constexpr uint64_t kHiP = smem_desc_hi(16, 1024);
+  constexpr uint64_t kHiV = smem_desc_hi(kPairChunk, 1024);
+  const int lane = threadIdx.x & 31;
+  int jt = 0, seg = 0;
+  for (int prob = sg.p0; prob <= sg.last(); ++prob) {
+    int tb, te;
+    sg.range(prob, tb, te);
+    if (tb >= te) continue;
+    for (int j = tb; j < te; ++j, ++jt) {
+      const bool first = (j == tb), last = (j == te - 1);
+      if (!pair_wait(bars + 8 * kBPFull, jt & 1, wd)) goto done;
+      tc_fence_after();
+      if (first && seg > 0) {
+        if (!pair_wait(bars + 8 * kBOEmpty, (seg - 1) & 1, wd)) goto done;
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+#pragma unroll
+        for (int kk = 0; kk < kPairTile / 16; ++kk) {
+          const int t = kk >> 2;
+          const uint64_t a = kHiP | ((smem + kPairPOff + t * kPairChunk + 32 * (kk & 3)) >> 4);
+          const uint64_t bdesc =
+              kHiV | ((smem + kPairKvOff + (4 * t + 2 * m) * kPairChunk + 2048 * (kk & 3)) >> 4);
+          if (elect_one()) umma2_bf16_ss(tmem + kPairOCol + 128 * m, a, bdesc, kIdO, !(first && kk == 0));
+          __syncwarp();
+        }
+      }
+      if (elect_one()) {
+        umma2_commit_both(bars + 8 * kBPEmpty);
+        umma2_commit_both(bars + 8 * kBKvEmpty);
+        if (last) umma2_commit_both(bars + 8 * kBOFull);
+      }
+      __syncwarp();
+    }
+    ++seg;
+  }
+done:
+  if (elect_one()) umma2_commit_own(bars + 8 * kBMmaDone);
+  __syncwarp();
+  if (lane == 0) pair_drain(bars + 8 * kBMmaDone, 0, wd.limit_ns);
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// warps 4-11: online softmax and epilogue
+// ---------------------------------------------------------------------------
+__device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, int rank, int split0, uint32_t tmem,
+                             uint32_t smem, uint32_t bars, uint32_t bars_even, float* m_s, float* red,
+                             const Watchdog& wd) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int q = warp & 3;           // TMEM lane quarter
+  const int h = q >> 1;             // half of the tile (page) this thread's columns cover
+  const int w = (warp - 4) >> 2;    // warpgroup: tokens [32w, 32w + 32) of the half
+  const int r = (q & 1) * 32 + lane;  // row of this CTA (0..63)
+  const int hw = 2 * h + w;         // which of the row's four partial statistics
+  const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+  const int row0 = g * 2 * kPairRows + rank * kPairRows;
+  const int grow = row0 + r;        // row within the problem
+  const float sc = p.scale_log2;
+  // arrivals of this warp on the even CTA's barriers (remote from the odd CTA)
+  auto arrive_even = [&](int bar) {
+    __syncwarp();
+    if (lane == 0) {
+      if (rank == 0)
+        mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + 8 * bar)));
+      else
+        mbar_arrive_cluster(bars_even + 8 * bar);
+    }
+  };
+  auto all_ok = [&](bool ok) { return named_bar_and(kPairSmBar, 256, ok); };
+  auto wait_all = [&](int bar, uint32_t parity) { return all_ok(mbar_wait(
+      reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + 8 * bar)), parity, wd)); };
+  if (p.debug_stall) {
+    // watchdog test: this barrier's first phase only completes when this role has finished
+    if (!wait_all(kBMmaDone, 0)) return;
+  }
+
+  int jt = 0, seg = 0;
+  for (int prob = sg.p0; prob <= sg.last(); ++prob) {
+    int tb, te;
+    sg.range(prob, tb, te);
+    if (tb >= te) continue;
+    const int b = prob;
+    const int L = sg.seqlens[b];
+    // last visible key of this row (bottom-right causal alignment)
+    const int lim = p.is_causal ? L - p.s_q + grow / p.h_q : L - 1;
+    float l_part = 0.f;
+    for (int j = tb; j < te; ++j, ++jt) {
+      const int sb = jt & 1;
+      if (!wait_all(kBSFull + sb, (jt >> 1) & 1)) return;
+      tc_fence_after();
+      float x[32];
+      tmem_ld_x32(tmem + lane_base + kPairSCol + sb * (kPairTile / 2) + 32 * w, x);
+      tmem_ld_wait();
+      tc_fence_before();
+      arrive_even(kBSEmpty + sb);
+      // mask and scale (log2 units); tokens of this thread: h * 64 + 32 w + i
+      const bool page_ok = tile_page(p, b, L, j, h, false) >= 0;
+      const int pos0 = j * kPairTile + h * 64 + 32 * w;
+      float mx = kPairNegInf;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int pos = pos0 + i;
+        x[i] = (page_ok && pos <= lim) ? x[i] * sc : kPairNegInf;
+        mx = fmaxf(mx, x[i]);
+      }
+      red[hw * 64 + r] = mx;
+      named_bar_sync(kPairSmBar, 256);
+      const float rmax = fmaxf(fmaxf(red[r], red[64 + r]), fmaxf(red[128 + r], red[192 + r]));
+      const float m_old = (j == tb) ? kPairNegInf : m_s[r];
+      const bool raise = (j == tb) || (rmax > m_old + kPairRescale);
+      const float m_new = raise ? fmaxf(m_old, rmax) : m_old;
+      // any row of either warpgroup raised its max (after the first tile): O needs a rescale
+      const bool any = named_bar_or(kPairSmBar, 256, raise && j != tb);
+      if (raise && hw == 0) m_s[r] = m_new;
+      const float alpha = (m_old == kPairNegInf) ? 0.f : fast_exp2(m_old - m_new);
+      if (raise) l_part *= alpha;
+      float pr[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        pr[i] = (x[i] == kPairNegInf) ? 0.f : fast_exp2(x[i] - m_new);
+        l_part += pr[i];
+      }
+      // P and O of the previous tile are free once its PV MMAs are done
+      if (jt > 0 && !wait_all(kBPEmpty, (jt - 1) & 1)) return;
+      tc_fence_after();
+      if (any) {
+        // rescale this thread's row of O (its lane's 128 columns of block w) by alpha
+        const float a = raise ? alpha : 1.0f;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 16) {
+          float v[16];
+          const uint32_t ta = tmem + lane_base + kPairOCol + 128 * w + c;
+          tmem_ld_x16(ta, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] *= a;
+          tmem_st_x16(ta, v);
+        }
+        tmem_st_wait();
+      }
+      // P (bf16, K-major, 128-byte swizzle): row r, tokens 32w .. 32w + 31 of chunk h
+      {
+        const uint32_t prow = smem + kPairPOff + h * kPairChunk + r * 128;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int unit = 4 * w + u;
+          st_shared_v4(prow + ((unit ^ (r & 7)) << 4), pack_bf16x2(pr[8 * u], pr[8 * u + 1]),
+                       pack_bf16x2(pr[8 * u + 2], pr[8 * u + 3]), pack_bf16x2(pr[8 * u + 4], pr[8 * u + 5]),
+                       pack_bf16x2(pr[8 * u + 6], pr[8 * u + 7]));
+        }
+      }
+      // the tile's value slots are loaded; tokens past the length or on an
+      // unusable page get zero value rows (their P is 0, but the slot may
+      // hold NaN, and 0 * NaN would poison O)
+      if (!wait_all(kBKvFull, jt & 1)) return;
+      {
+        const int tl = (q & 1) * 32 + lane;  // token of page h zeroed by this thread
+        if (!page_ok || j * kPairTile + h * 64 + tl >= L) {
+#pragma unroll
+          for (int s2 = 0; s2 < 2; ++s2) {
+            const uint32_t rowa = smem + kPairKvOff + (4 * h + 2 * w + s2) * kPairChunk + tl * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) st_shared_v4(rowa + 16 * u, 0u, 0u, 0u, 0u);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      arrive_even(kBPFull);
+    }
+
+    // ---- epilogue: O / l -> out (single piece) or fp32 partial (split problem)
+    if (!wait_all(kBOFull, seg & 1)) return;
+    tc_fence_after();
+    red[hw * 64 + r] = l_part;
+    named_bar_sync(kPairSmBar, 256);
+    const float lt = red[r] + red[64 + r] + red[128 + r] + red[192 + r];
+    const float m_fin = m_s[r];
+    named_bar_sync(kPairSmBar, 256);  // red and m_s are reused by the next segment
+    const float inv = lt > 0.f ? 1.0f / lt : 0.f;
+    const float lse = lt > 0.f ? m_fin + log2f(lt) : kPairNegInf;
+    const int nsplit = p.num_splits[prob + 1] - p.num_splits[prob];
+    const bool final_out = nsplit <= 1;
+    const int slot = p.num_splits[prob] + (prob == sg.p0 ? split0 : 0);
+    bool write_ok = grow < p.rows;
+    if (!final_out && (slot < 0 || slot >= p.max_slots)) {
+      write_ok = false;
+      if (r == 0 && hw == 0) atomicOr(p.status, MLA_DEVICE_BAD_SCHEDULE);
+    }
+    const int dv0 = 256 * w + 128 * h;
+    const int64_t orow = final_out ? static_cast<int64_t>(prob) * p.rows + grow
+                                   : static_cast<int64_t>(slot) * p.rows + grow;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 16) {
+      float v[16];
+      tmem_ld_x16(tmem + lane_base + kPairOCol + 128 * w + c, v);
+      tmem_ld_wait();
+      if (write_ok) {
+        if (final_out) {
+          uint4 lo, hi;
+          lo.x = pack_bf16x2(v[0] * inv, v[1] * inv);
+          lo.y = pack_bf16x2(v[2] * inv, v[3] * inv);
+          lo.z = pack_bf16x2(v[4] * inv, v[5] * inv);
+          lo.w = pack_bf16x2(v[6] * inv, v[7] * inv);
+          hi.x = pack_bf16x2(v[8] * inv, v[9] * inv);
+          hi.y = pack_bf16x2(v[10] * inv, v[11] * inv);
+          hi.z = pack_bf16x2(v[12] * inv, v[13] * inv);
+          hi.w = pack_bf16x2(v[14] * inv, v[15] * inv);
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kDv + dv0 + c);
+          dst[0] = lo;
+          dst[1] = hi;
+        } else {
+          float4* dst = reinterpret_cast<float4*>(p.o_accum + orow * kDv + dv0 + c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_float4(v[4 * e] * inv, v[4 * e + 1] * inv, v[4 * e + 2] * inv, v[4 * e + 3] * inv);
+        }
+      }
+    }
+    if (write_ok && hw == 0) {
+      if (final_out)
+        p.lse[orow] = lse;
+      else
+        p.lse_accum[orow] = lse;
+    }
+    tc_fence_before();
+    arrive_even(kBOEmpty);
+    ++seg;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kPairThreads, 1)
+    mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
+                           const DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t smem = smem_u32(base);
+  const uint32_t bars = smem + kPairAuxOff;
+  float* m_s = reinterpret_cast<float*>(base + kPairAuxOff + kPairBarBytes);
+  float* red = m_s + 64;
+  int* ints = reinterpret_cast<int*>(red + 256);
+  volatile int* abort_flag = ints;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ints + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int pair_id = blockIdx.x >> 1;
+  const int part = pair_id / p.row_groups;
+  const int g = pair_id % p.row_groups;
+
+  if (threadIdx.x == 0) {
+    uint64_t* bp = reinterpret_cast<uint64_t*>(base + kPairAuxOff);
+    // the even CTA's Q / score-operand barriers also count the odd CTA's forwarded arrival
+    const uint32_t fwd = rank == 0 ? 2 : 1;
+    mbar_init(bp + kBQFull, fwd);
+    mbar_init(bp + kBQEmpty, 1);
+    for (int k = 0; k < kNumChunks; ++k) {
+      mbar_init(bp + kBKsFull + k, fwd);
+      mbar_init(bp + kBKsEmpty + k, 1);
+    }
+    mbar_init(bp + kBKvFull, 1);
+    mbar_init(bp + kBKvEmpty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bp + kBSFull + i, 1);
+      mbar_init(bp + kBSEmpty + i, 16);  // 8 softmax warps in each CTA
+    }
+    mbar_init(bp + kBPFull, 16);
+    mbar_init(bp + kBPEmpty, 1);
+    mbar_init(bp + kBOFull, 1);
+    mbar_init(bp + kBOEmpty, 16);
+    mbar_init(bp + kBMmaDone, 2);  // one commit per MMA-issuing warp
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kv);
+  }
+  if (warp == 2) {
+    tmem_alloc_pair(tmem_slot, kPairTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  // both CTAs' barriers are initialised before any remote arrival or commit
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t bars_even = mapa_shared(bars, 0);
+
+  Watchdog wd{abort_flag, p.status, p.timeout_ns};
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  PairSeg sg;
+  int split0 = 0;
+  if (p.sched[kSchedParts] == p.num_parts && p.sched[kSchedTag] == p.sched_tag) {
+    const int32_t* sr = p.sched + static_cast<int64_t>(part) * kSchedInts;
+    sg.p0 = sr[kSchedP0];
+    sg.t0 = sr[kSchedT0];
+    sg.p1 = sr[kSchedP1];
+    sg.t1 = sr[kSchedT1];
+    split0 = sr[kSchedSplit0];
+  } else {
+    sg.p0 = -1;
+    sg.t0 = sg.p1 = sg.t1 = 0;
+  }
+  sg.np = p.num_problems;
+  sg.s_q = p.s_q;
+  sg.seqlens = p.cache_seqlens;
+  if (sg.p0 < 0 || sg.p0 > sg.np || sg.p1 < sg.p0 || sg.p1 > sg.np || sg.t0 < 0 || sg.t1 < 0) {
+    if (threadIdx.x == 0) atomicOr(p.status, MLA_DEVICE_BAD_SCHEDULE);
+    sg.p0 = sg.np;
+    sg.p1 = sg.np;
+  }
+
+  if (warp < 4) {
+    regs_to<kPairRegsCtl, kPairLaunchRegs>();
+    if (warp == 0) {
+      pair_producer_ks(&tm_q, &tm_kv, p, sg, g, rank, smem, bars, wd);
+    } else if (warp == 1) {
+      if (rank == 0)
+        pair_s_issuer(sg, tmem, smem, bars, wd);
+      else
+        pair_forwarder(sg, bars, bars_even, wd);
+    } else if (warp == 2) {
+      pair_producer_kv(&tm_kv, p, sg, rank, smem, bars, wd);
+    } else if (rank == 0) {
+      pair_pv_issuer(sg, tmem, smem, bars, wd);
+    }
+  } else {
+    regs_to<kPairRegsSm, kPairLaunchRegs>();
+    pair_softmax(p, sg, g, rank, split0, tmem, smem, bars, bars_even, m_s, red, wd);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  // neither CTA leaves while its partner may still read its shared memory,
+  // arrive on its barriers or run MMAs on its TMEM
+  cluster_sync_all();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kPairTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_pair(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const DecodeParams& p,
+                               cudaStream_t stream) {
+  auto kern = mla_decode_pair_kernel;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != static_cast<int>(kPairLaunchRegs)) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * p.num_parts * p.row_groups);
+  cfg.blockDim = dim3(kPairThreads);
+  cfg.dynamicSmemBytes = kPairSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, tm_q, tm_kv, p);
+}
+
+}  // namespace mla

@@ -23,23 +23,30 @@ constexpr int kFp8RowBytes = 656;  // 512 e4m3 + 4 fp32 scales + 64 bf16
 constexpr int kFp8ScaleOffset = 512;
 constexpr int kFp8RopeOffset = 528;
 constexpr int kSchedInts = 8;      // ints per schedule record
-constexpr int kCostOverheadTiles = 2;  // fixed cost of starting a problem segment, in tiles
 
 // Schedule record of one part (a group of `row_groups` CTAs that walk the
 // same tiles, one CTA per row group):
 //   [0] first problem  [1] first tile in it  [2] last problem (inclusive bound)
 //   [3] end tile in the last problem (exclusive)  [4] split index of the
-//   part's piece of its first problem  [5..7] unused (0)
-enum SchedField { kSchedP0 = 0, kSchedT0 = 1, kSchedP1 = 2, kSchedT1 = 3, kSchedSplit0 = 4 };
+//   part's piece of its first problem  [5] number of parts the schedule was
+//   cut into  [6] geometry tag of the decode it was made for  [7] unused (0)
+// The decode kernel compares [5] and [6] of record 0 with its own launch
+// before it reads any other record, so a schedule made for another
+// configuration (or another device) is reported, never followed.
+enum SchedField { kSchedP0 = 0, kSchedT0 = 1, kSchedP1 = 2, kSchedT1 = 3, kSchedSplit0 = 4, kSchedParts = 5,
+                  kSchedTag = 6 };
 
 constexpr int kMaxProblems = 16384;    // metadata kernel keeps per-problem prefix sums in smem
 
-// Number of 64-token tiles of problem p: dense covers the cached tokens
-// [0, seqlen), sparse covers the topk index slots of the query token.
-__host__ __device__ inline int problem_tiles(const int32_t* cache_seqlens, int p, int s_q, int topk) {
-  if (topk > 0) return (topk + kTileTokens - 1) / kTileTokens;
+// Number of tiles of problem p: dense covers the cached tokens [0, seqlen),
+// sparse covers the topk index slots of the query token.  Tiles are 64
+// tokens (one page) for the single-CTA kernel and 128 (two pages, one per
+// CTA) for the CTA-pair kernel.
+__host__ __device__ inline int problem_tiles(const int32_t* cache_seqlens, int p, int s_q, int topk,
+                                             int tile_tokens = kTileTokens) {
+  if (topk > 0) return (topk + tile_tokens - 1) / tile_tokens;
   int L = cache_seqlens[p];
-  return L > 0 ? (L + kTileTokens - 1) / kTileTokens : 0;
+  return L > 0 ? (L + tile_tokens - 1) / tile_tokens : 0;
 }
 
 // Rows per CTA for a problem with `rows` query rows sharing one key set.
@@ -52,6 +59,12 @@ struct Geometry {
   int row_groups;    // ceil(rows / rpc)
   int num_parts;     // schedule parts (each = row_groups CTAs)
   int sm_count;
+  int mode;          // decode kernel mode: 0 dense bf16, 1 sparse FP8, 2 dense FP8, 3 sparse bf16 rows
+  int pair;          // 1: CTA-pair kernel (128 rows and 128-token tiles per pair), 0: one CTA per row group
+  int tile_tokens;   // tokens per schedule tile (64, or 128 for the pair kernel)
+  int tile_cost;     // schedule cost of one tile (quarter units of a 64-token bf16 tile)
+  int overhead;      // schedule cost of starting a problem segment (same units)
+  int tag;           // geometry tag written into the schedule records
 };
 
 struct DecodeParams {
@@ -73,6 +86,7 @@ struct DecodeParams {
   int max_slots;              // partial-result slots the workspace holds
   int is_causal;
   int evict_first;
+  int sched_tag;              // expected kSchedTag of the schedule records
   int debug_stall;            // test hook: the softmax role waits on a barrier nothing completes
   int flat_rows;              // > 0: sparse over an unpaged KV of this many rows (index = row; no
                               // block table or cache_seqlens); 0: paged cache
@@ -112,12 +126,14 @@ struct IndexParams {
 };
 
 // Kernel launchers (defined in the .cu files); return a CUDA error code.
-cudaError_t launch_metadata(const int32_t* cache_seqlens, int batch, int s_q, int h_q, int topk,
-                            const Geometry& g, int32_t* sched, int32_t* num_splits, uint32_t* status,
-                            cudaStream_t stream);
+cudaError_t launch_metadata(const int32_t* cache_seqlens, int s_q, int topk, const Geometry& g, int32_t* sched,
+                            int32_t* num_splits, cudaStream_t stream);
 // mode: 0 dense bf16 cache, 1 sparse FP8 cache, 2 dense FP8 cache, 3 sparse bf16 rows
 cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const DecodeParams& p, int rpc,
                           int mode, cudaStream_t stream);
+// CTA-pair decode (dense over the bf16 cache, problems of more than 64 rows)
+cudaError_t launch_decode_pair(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const DecodeParams& p,
+                               cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
 size_t decode_smem_bytes(int rpc, int mode);
 cudaError_t launch_fp8_cache_store(const uint16_t* x, int num_tokens, const int32_t* row_offsets,

@@ -65,7 +65,7 @@ extern "C" mla_status mla_decode_noalloc(const mla_decode_args* args, mla_stream
   using namespace mla;
   if (!args) return mla_decode(args, stream);  // same argument error as the allocating entry point
   size_t need = 0;
-  mla_status st = mla_workspace_size(args->batch, args->s_q, args->h_q, args->topk, &need);
+  mla_status st = mla_workspace_size(args->batch, args->h_q, args->s_q, args->topk, args->is_fp8, &need);
   if (st != MLA_OK) return st;
   if (need > kNoallocScratchBytes) {
     set_error_message("mla_decode_noalloc: this decode needs " + std::to_string(need) +

@@ -30,14 +30,14 @@ def test_header_declares_the_boundary():
     for n in ["mla_metadata_size", "mla_workspace_size", "mla_get_metadata", "mla_decode",
               "mla_get_device_status", "mla_last_error", "mla_abi_version", "mla_fp8_cache_store",
               "mla_sparse_prefill_workspace_size", "mla_sparse_prefill", "mla_index_topk_workspace_size",
-              "mla_index_topk"]:
+              "mla_index_topk", "mla_test_hooks", "mla_decode_noalloc"]:
         assert n in names
 
 
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"libmla.so does not export {name}"
-    assert lib.mla_abi_version() == 2
+    assert lib.mla_abi_version() == 3
 
 
 @pytest.mark.parametrize("struct,cls", [("mla_decode_args", mla.DecodeArgs),
@@ -91,6 +91,11 @@ def test_host_validation(lib, field, value, status, needle):
     assert needle in mla.last_error()
 
 
+def test_decode_rejects_a_bad_is_fp8(lib):
+    a = _args(is_fp8=3)
+    assert lib.mla_decode(ctypes.byref(a), None) == 1 and "is_fp8" in mla.last_error()
+
+
 def test_sparse_mode_rules(lib):
     a = _args(topk=64, indices=None, is_fp8=1)
     assert lib.mla_decode(ctypes.byref(a), None) == 1 and "indices is NULL" in mla.last_error()
@@ -103,14 +108,32 @@ def test_sparse_mode_rules(lib):
 
 
 def test_size_queries_validate_before_touching_a_device(lib):
+    # argument order (batch, h_q, s_q, topk, is_fp8)
     a, b = ctypes.c_int(), ctypes.c_int()
-    assert lib.mla_metadata_size(0, 1, 16, 0, ctypes.byref(a), ctypes.byref(b)) == 1
+    assert lib.mla_metadata_size(0, 16, 1, 0, 0, ctypes.byref(a), ctypes.byref(b)) == 1
     assert "batch" in mla.last_error()
     n = ctypes.c_size_t()
-    assert lib.mla_workspace_size(1, 0, 16, 0, ctypes.byref(n)) == 1
+    assert lib.mla_workspace_size(1, 16, 0, 0, 0, ctypes.byref(n)) == 1
     assert "s_q" in mla.last_error()
-    assert lib.mla_workspace_size(1, 1, 2048, 0, ctypes.byref(n)) in (2, 4)
-    assert lib.mla_get_metadata(None, 1, 1, 16, 0, None, None, None) == 1
+    assert lib.mla_workspace_size(1, 0, 1, 0, 0, ctypes.byref(n)) == 1
+    assert "h_q" in mla.last_error()
+    assert lib.mla_workspace_size(1, 2048, 1, 0, 0, ctypes.byref(n)) in (2, 4)
+    assert lib.mla_workspace_size(1, 16, 1, 0, 2, ctypes.byref(n)) == 1
+    assert "is_fp8" in mla.last_error()
+    assert lib.mla_get_metadata(None, 1, 16, 1, 0, 0, None, None, None) == 1
+
+
+def test_test_hooks_validate(lib):
+    assert lib.mla_test_hooks(-1, 0) == 1 and "num_parts" in mla.last_error()
+    assert lib.mla_test_hooks(0, 0) == 0
+
+
+def test_binding_takes_the_configuration_by_keyword():
+    # h_q and s_q are both ints: positional use could swap them silently, so it is refused
+    with pytest.raises(TypeError):
+        mla.workspace_size(1, 1, 16, 0, False)
+    with pytest.raises(TypeError):
+        mla.get_metadata(None, 1, 16, 0)
 
 
 def test_python_binding_rejects_bad_tensors():

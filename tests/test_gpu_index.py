@@ -22,7 +22,7 @@ import oracle
 import paged_mla_decode_07_gb300 as mla
 from paged_mla_decode_07_gb300 import workloads as W
 
-from gpu_helpers import compare, run_oracle
+from gpu_helpers import Guarded, check_guards, compare, guarded_tensor, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -63,10 +63,15 @@ def abs_bound(inp, width):
 
 
 def run_index(inp):
+    """Indexer into guarded ids / workspace buffers (guards checked after the call)."""
     d = inp.to("cuda")
+    T = int(inp.row_offsets[-1])
+    g_idx, idx = guarded_tensor((T, inp.topk), torch.int32)
+    g_ws = Guarded(max(16, mla.index_topk_workspace_size(T, d.block_table.shape[1])))
     out = mla.index_topk(d.q_codes, d.q_scales, d.weights, d.row_offsets, d.k_codes, d.k_scales, d.block_table,
-                         d.cache_seqlens, inp.topk, relu=inp.relu)
+                         d.cache_seqlens, inp.topk, relu=inp.relu, indices=idx, workspace=g_ws.body)
     flags = mla.device_status()
+    check_guards({"indices": g_idx, "workspace": g_ws}, inp.workload.name)
     return out.cpu().numpy(), flags
 
 
@@ -178,7 +183,7 @@ def test_indexer_feeds_sparse_decode():
     dinp = W.make_inputs(dw, seed=6)
     dinp.indices = torch.from_numpy(idx.reshape(3, 2, 256).copy())
     d = dinp.to("cuda")
-    sched, ns = mla.get_metadata(d.cache_seqlens, 2, 64, 256)
+    sched, ns = mla.get_metadata(d.cache_seqlens, h_q=64, s_q=2, topk=256, is_fp8=True)
     out, lse = mla.decode(d.q, d.kvcache, d.block_table, d.cache_seqlens, d.sm_scale, sched, ns, indices=d.indices)
     assert mla.device_status() == 0
     ref_out, ref_lse = run_oracle(dinp)

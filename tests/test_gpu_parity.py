@@ -1,8 +1,9 @@
 """Parity of the CUDA decode path (through the C ABI) with the fp64 oracle.
 
-Small cases compare every output element; the five named workloads run at
-full size in the benchmark's launch configuration and are compared on
-sampled rows the oracle computes one by one, plus whole-output properties.
+Small cases and the named workloads at full size (in the benchmark's launch
+configuration) compare every output element with the oracle run over all
+rows; whole-output properties are checked beside them.  Every output and
+scratch buffer sits between guard regions that must survive each call.
 """
 import math
 
@@ -13,7 +14,7 @@ import torch
 import paged_mla_decode_07_gb300 as mla
 from paged_mla_decode_07_gb300 import workloads as W
 
-from gpu_helpers import compare, env, run_cuda, run_oracle
+from gpu_helpers import compare, metadata, overrides, run_cuda, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -28,7 +29,7 @@ def _built():
 
 def check(w, seed, parts=None, poison=True, **mk):
     inp = W.make_inputs(w, seed=seed, poison_tail=poison, **mk)
-    with env(MLA_NUM_PARTS=parts):
+    with overrides(num_parts=parts):
         out, lse, flags = run_cuda(inp)
     ref_out, ref_lse = run_oracle(inp)
     assert flags == 0, f"device status 0x{flags:x}"
@@ -98,7 +99,7 @@ def test_rescale_path_increasing_logits():
         page, slot = int(inp.block_table[0, j // 64]), j % 64
         kv[page, slot, 0] = kv[page, slot, 0] * 0.1 + unit * (0.15 * j * 24.0 / qn)
     inp.kvcache = kv.to(torch.bfloat16)
-    with env(MLA_NUM_PARTS=1):
+    with overrides(num_parts=1):
         out, lse, flags = run_cuda(inp)
     ref_out, ref_lse = run_oracle(inp)
     assert flags == 0
@@ -164,7 +165,7 @@ def test_sparse_equals_dense_over_all_tokens():
 def test_schedule_covers_every_tile_once(topk, lens):
     s_q, h_q = 2, 128
     sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
-    sched, ns = mla.get_metadata(sl, s_q, h_q, topk)
+    sched, ns = mla.get_metadata(sl, h_q=h_q, s_q=s_q, topk=topk, is_fp8=topk > 0)
     sched = sched.view(-1, 8).cpu().numpy()
     ns = ns.cpu().numpy()
     np_ = len(lens) * (s_q if topk else 1)
@@ -193,6 +194,27 @@ def test_schedule_covers_every_tile_once(topk, lens):
 
 
 # ---------------------------------------------------------------- device status
+@pytest.mark.parametrize("case", ["parts", "mode"])
+def test_schedule_of_another_configuration_is_flagged(case):
+    """A schedule made for another part count or another cache format is reported by the decode
+    (it checks the first record's part count and configuration tag) and nothing else is read."""
+    w = W.custom(name="mismatch", batch=2, h_q=64, s_q=1, mode="dense", seqlens=(300, 100))
+    d = W.make_inputs(w, seed=8).to("cuda")
+    mla.device_status()
+    if case == "parts":
+        with overrides(num_parts=5):
+            sched, ns = metadata(d, w)
+    else:
+        sched, ns = mla.get_metadata(d.cache_seqlens, h_q=w.h_q, s_q=w.s_q, topk=0, is_fp8=True)
+    out, lse = mla.decode(d.q, d.kvcache, d.block_table, d.cache_seqlens, d.sm_scale, sched, ns)
+    flags = mla.device_status()
+    assert flags & mla.DEVICE_BAD_SCHEDULE
+    # the same inputs with a matching schedule still decode correctly
+    out, lse, flags = run_cuda(W.make_inputs(w, seed=8))
+    assert flags == 0
+
+
+
 @pytest.mark.parametrize("h_q", [16, 64])
 def test_bad_page_is_flagged_not_faulted(h_q):
     """16 rows: one full barrier per tile; 64 rows: one per ring item, armed with no bytes for a bad page."""
@@ -208,26 +230,22 @@ def test_bad_page_is_flagged_not_faulted(h_q):
 
 
 # ---------------------------------------------------------------- full-size workloads
-def _sample_rows(inp, n_problems, rng):
-    w = inp.workload
-    rows_per_problem = w.h_q if w.mode == "sparse" else w.s_q * w.h_q
-    n_total_problems = w.batch * (w.s_q if w.mode == "sparse" else 1)
-    probs = rng.choice(n_total_problems, size=min(n_problems, n_total_problems), replace=False)
-    return np.sort(np.concatenate([p * rows_per_problem + np.arange(rows_per_problem) for p in probs]))
+FULL_SIZE = ["tiny", "dense_membound", "dense_computebound", "sparse_fp8", "sparse_fp8_long", "sparse_bf16",
+             "sparse_fp8_token", "dense_membound_fp8"]
 
 
-@pytest.mark.parametrize("name,n_problems", [("tiny", 2), ("dense_membound", 12), ("dense_computebound", 3),
-                                             ("sparse_fp8", 6), ("sparse_fp8_long", 2), ("sparse_bf16", 4)])
-def test_full_size_workload(name, n_problems):
+@pytest.mark.parametrize("name", FULL_SIZE)
+def test_full_size_workload(name):
+    """Every output row of a named workload, in the launch configuration the benchmark times,
+    against the oracle run over all rows (all host threads)."""
     inp = W.make_inputs(name)
     out, lse, flags = run_cuda(inp)
     assert flags == 0
-    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
-    rows = _sample_rows(inp, n_problems, np.random.default_rng(7))
-    ref_out, ref_lse = run_oracle(inp, rows=rows)
-    compare(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, name)
+    assert np.all(np.isfinite(out))
+    ref_out, ref_lse = run_oracle(inp)
+    compare(out, lse, ref_out, ref_lse, name)
     # property at any size: each output row is a convex combination of value rows
-    if inp.workload.mode == "dense":
+    if inp.workload.mode == "dense" and not inp.workload.is_fp8:
         vmax = float(inp.kvcache[..., :512].float().nan_to_num(0.0).abs().max())
         assert float(np.abs(out).max()) <= vmax * (1 + 1e-2)
 
@@ -272,16 +290,6 @@ def test_dense_fp8_equals_dense_over_dequantised_cache():
     compare(out_f, lse_f, out_d, lse_d, "dense-fp8-vs-dense")
 
 
-def test_dense_fp8_full_size_workload():
-    inp = W.make_inputs("dense_membound_fp8")
-    out, lse, flags = run_cuda(inp)
-    assert flags == 0
-    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
-    rows = _sample_rows(inp, 12, np.random.default_rng(8))
-    ref_out, ref_lse = run_oracle(inp, rows=rows)
-    compare(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, "dense_membound_fp8")
-
-
 # ---------------------------------------------------------------- per-token-scale FP8 rows, ragged top-k
 @pytest.mark.parametrize("h_q,s_q", [(16, 1), (64, 2), (128, 1)])
 def test_sparse_token_scale_cache(h_q, s_q):
@@ -313,17 +321,6 @@ def test_sparse_topk_lengths(h_q, fp8):
     ref_out, ref_lse = run_oracle(inp)
     compare(out, lse, ref_out, ref_lse, w.name)
     assert np.all(out[0, 0] == 0) and np.all(lse[0, 0] == -np.inf)
-
-
-def test_sparse_token_scale_full_size_sampled():
-    """The sparse FP8 decode shape over 640-byte rows with per-token scales, sampled rows."""
-    inp = W.make_inputs("sparse_fp8_token")
-    w = inp.workload
-    out, lse, flags = run_cuda(inp)
-    assert flags == 0
-    rows = _sample_rows(inp, 4, np.random.default_rng(9))
-    ref_out, ref_lse = run_oracle(inp, rows=rows)
-    compare(out.reshape(-1, 512)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, w.name)
 
 
 # ---------------------------------------------------------------- largest supported shapes

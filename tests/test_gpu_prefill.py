@@ -14,7 +14,7 @@ import oracle
 import paged_mla_decode_07_gb300 as mla
 from paged_mla_decode_07_gb300 import workloads as W
 
-from gpu_helpers import compare, env, run_cuda, run_oracle
+from gpu_helpers import Guarded, check_guards, compare, guarded_tensor, metadata, overrides, run_cuda, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -86,9 +86,15 @@ def test_sparse_bf16_and_fp8_caches_agree_on_dequantised_values():
 
 # ---------------------------------------------------------------- sparse prefill
 def run_prefill(inp, rows=None):
+    """Prefill into guarded out / lse / workspace buffers (guards checked after the call)."""
     d = inp.to("cuda")
-    out, lse = mla.sparse_prefill(d.q, d.kv, d.indices, d.sm_scale)
+    w = inp.workload
+    g_out, out = guarded_tensor((w.s_q, w.h_q, 512), torch.bfloat16)
+    g_lse, lse = guarded_tensor((w.s_q, w.h_q), torch.float32)
+    g_ws = Guarded(mla.sparse_prefill_workspace_size(w.s_q, w.h_q, w.topk))
+    out, lse = mla.sparse_prefill(d.q, d.kv, d.indices, d.sm_scale, out=out, lse=lse, workspace=g_ws.body)
     flags = mla.device_status()
+    check_guards({"out": g_out, "lse": g_lse, "workspace": g_ws}, w.name)
     out = out.reshape(-1, 512)
     lse = lse.reshape(-1)
     if rows is not None:
@@ -142,7 +148,7 @@ def test_prefill_is_sparse_decode_on_one_element():
     cache = d.kv.reshape(10, 64, 1, 576)
     table = torch.arange(10, dtype=torch.int32, device="cuda")[None]
     lens = torch.tensor([640], dtype=torch.int32, device="cuda")
-    sched, ns = mla.get_metadata(lens, 20, 64, 200)
+    sched, ns = mla.get_metadata(lens, h_q=64, s_q=20, topk=200, is_fp8=False)
     out_d, lse_d = mla.decode(d.q[None], cache, table, lens, d.sm_scale, sched, ns, indices=d.indices[None])
     np.testing.assert_array_equal(out_p, out_d.reshape(-1, 512).double().cpu().numpy())
     np.testing.assert_array_equal(lse_p, lse_d.reshape(-1).double().cpu().numpy())
@@ -172,7 +178,7 @@ def test_prefill_with_parts_forced_small_splits_problems():
     """Few parts: every part covers several query tokens and splits some; the combine merges them."""
     w = W.PrefillWorkload("p_split", s_q=9, s_kv=4000, h_q=64, topk=1024)
     inp = W.make_prefill_inputs(w, seed=4)
-    with env(MLA_NUM_PARTS=7):
+    with overrides(num_parts=7):
         check_prefill(inp)
 
 

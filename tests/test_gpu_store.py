@@ -98,7 +98,7 @@ def test_store_then_sparse_decode_reads_the_rows():
     mla.fp8_cache_store(x.cuda(), offs.cuda(), lens.cuda(), inp.block_table.cuda(), c)
     inp.kvcache = c.cpu()
     d = inp.to("cuda")
-    sched, ns = mla.get_metadata(d.cache_seqlens, w.s_q, w.h_q, 256)
+    sched, ns = mla.get_metadata(d.cache_seqlens, h_q=w.h_q, s_q=w.s_q, topk=256, is_fp8=True)
     out, lse = mla.decode(d.q, d.kvcache, d.block_table, d.cache_seqlens, d.sm_scale, sched, ns, indices=d.indices)
     ref_out, ref_lse = oracle.mla_decode(inp.q, inp.kvcache, inp.block_table, inp.cache_seqlens, inp.sm_scale,
                                          indices=inp.indices)

@@ -1,13 +1,15 @@
 """Failure detection without a GPU fault: a wait that nothing completes runs out
 its (short) watchdog limit, the kernel unwinds and reports MLA_DEVICE_TIMEOUT
-through the device status word, and the context stays usable."""
+through the device status word, and the context stays usable.  The stall is
+switched on through the library's test-hook entry point (mla_test_hooks), not
+an environment variable, so production decodes cannot be stalled by accident."""
 import pytest
 import torch
 
 import paged_mla_decode_07_gb300 as mla
 from paged_mla_decode_07_gb300 import workloads as W
 
-from gpu_helpers import compare, env, run_cuda, run_oracle
+from gpu_helpers import compare, env, metadata, overrides, run_cuda, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -23,15 +25,15 @@ def test_watchdog_timeout_is_reported_and_context_survives(mode):
         inp = W.make_inputs(W.custom(name="wd_sparse", batch=2, h_q=64, s_q=2, mode="sparse",
                                      seqlens=(900, 300), topk=256), seed=5)
     mla.device_status()  # clear
-    with env(MLA_WATCHDOG_NS=200_000_000, MLA_DEBUG_STALL=1):
+    with env(MLA_WATCHDOG_NS=200_000_000), overrides(debug_stall=True):
         _, _, flags = run_cuda(inp)
     assert flags & mla.DEVICE_TIMEOUT
     # the status call itself reports MLA_ERR_DEVICE_TIMEOUT
     w = inp.workload
     d = inp.to("cuda")
     topk = 0 if d.indices is None else d.indices.shape[-1]
-    with env(MLA_WATCHDOG_NS=200_000_000, MLA_DEBUG_STALL=1):
-        sched, ns = mla.get_metadata(d.cache_seqlens, w.s_q, w.h_q, topk)
+    with env(MLA_WATCHDOG_NS=200_000_000), overrides(debug_stall=True):
+        sched, ns = metadata(d, w)
         mla.decode(d.q, d.kvcache, d.block_table, d.cache_seqlens, d.sm_scale, sched, ns,
                    is_causal=w.causal, indices=d.indices)
     with pytest.raises(mla.MLAError) as ei:

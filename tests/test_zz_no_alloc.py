@@ -19,7 +19,7 @@ import torch
 import paged_mla_decode_07_gb300 as mla
 from paged_mla_decode_07_gb300 import workloads as W
 
-from gpu_helpers import compare
+from gpu_helpers import compare, metadata
 
 pytestmark = pytest.mark.gpu
 
@@ -72,8 +72,7 @@ def test_noalloc_matches_the_allocating_entry_point_on_two_calls(name):
     L = _lib()
     d = CASES[name]().to("cuda")
     w = d.workload
-    topk = 0 if d.indices is None else d.indices.shape[-1]
-    sched, ns = mla.get_metadata(d.cache_seqlens, w.s_q, w.h_q, topk)
+    sched, ns = metadata(d, w)
     ref_out, ref_lse = mla.decode(d.q, d.kvcache, d.block_table, d.cache_seqlens, d.sm_scale, sched, ns,
                                   is_causal=w.causal, indices=d.indices)
     ref_out = ref_out.double().cpu().numpy()
@@ -91,18 +90,26 @@ def test_noalloc_matches_the_allocating_entry_point_on_two_calls(name):
 
 
 def test_noalloc_rejects_scratch_beyond_its_fixed_size():
+    """A decode whose split-KV scratch exceeds the fixed array is refused before any launch: the
+    call gets real buffers of a small decode (so nothing could go wrong even if it launched) with
+    the large configuration's sizes, returns MLA_ERR_WORKSPACE and leaves the outputs untouched."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     mla.build()
     L = _lib()
     w = W.WORKLOADS["sparse_fp8"]  # its split-KV scratch exceeds the fixed 32 MiB
-    assert mla.workspace_size(w.batch, w.s_q, w.h_q, w.topk) > 32 << 20
+    assert mla.workspace_size(w.batch, h_q=w.h_q, s_q=w.s_q, topk=w.topk, is_fp8=True) > 32 << 20
     small = W.make_inputs(W.custom(name="tiny_sparse", batch=2, h_q=16, s_q=1, mode="sparse", seqlens=(100, 50),
                                    topk=64), seed=3).to("cuda")
-    a = _args(small, small.block_table, small.cache_seqlens, torch.empty(1, device="cuda"),
-              torch.empty(1, device="cuda"))
+    sched, ns = metadata(small, small.workload)
+    out = torch.full((2, 1, 16, 512), 7.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((2, 1, 16), 7.0, dtype=torch.float32, device="cuda")
+    a = _args(small, sched, ns, out, lse)
     a.batch, a.s_q, a.h_q, a.topk = w.batch, w.s_q, w.h_q, w.topk
     st = L.mla_decode_noalloc(ctypes.byref(a), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == MLA_ERR_WORKSPACE
     assert "32" in mla.last_error() or "33554432" in mla.last_error()
     assert "scratch" in mla.last_error()
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all()) and bool((lse == 7.0).all())
+    assert mla.device_status() == 0
