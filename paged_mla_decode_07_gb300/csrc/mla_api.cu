@@ -53,9 +53,10 @@ __device__ uint32_t g_device_status;
 constexpr int kMaxDevices = 64;
 uint32_t* g_status_ptr[kMaxDevices];
 int g_sm_count[kMaxDevices];
+int g_pair_capacity[kMaxDevices];  // co-resident CTA pairs of the pair decode kernel
 std::mutex g_mu;
 
-mla_status device_info(uint32_t** status, int* sm_count) {
+mla_status device_info(uint32_t** status, int* sm_count, int* pair_capacity = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -70,15 +71,18 @@ mla_status device_info(uint32_t** status, int* sm_count) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
     g_status_ptr[dev] = static_cast<uint32_t*>(ptr);
     g_sm_count[dev] = sms;
+    const int cap = pair_cluster_capacity();
+    g_pair_capacity[dev] = (cap > 0 && cap < sms / 2) ? cap : sms / 2;
   }
   if (status) *status = g_status_ptr[dev];
   if (sm_count) *sm_count = g_sm_count[dev];
+  if (pair_capacity) *pair_capacity = g_pair_capacity[dev];
   return MLA_OK;
 }
 
 // The CTA-pair decode kernel for problems of more than 64 rows over the bf16
 // cache (mla_decode_pair.cu).
-constexpr bool kPairDecode = false;
+constexpr bool kPairDecode = true;
 
 // Test hooks (mla_test_hooks): a forced part count and a stalled softmax role.
 std::atomic<int> g_test_num_parts{0};
@@ -103,8 +107,8 @@ mla_status geometry(int batch, int h_q, int s_q, int topk, int is_fp8, Geometry*
                 topk > 0 ? "h_q" : "s_q*h_q", rows);
   if (topk > (1 << 24)) return fail(MLA_ERR_UNSUPPORTED, "topk = %d too large", topk);
   if (is_fp8 != 0 && is_fp8 != 1) return fail(MLA_ERR_INVALID_ARG, "is_fp8 must be 0 or 1 (got %d)", is_fp8);
-  int sms = 0;
-  mla_status st = device_info(nullptr, &sms);
+  int sms = 0, pairs = 0;
+  mla_status st = device_info(nullptr, &sms, &pairs);
   if (st != MLA_OK) return st;
   g->num_problems = static_cast<int>(np);
   g->rows = static_cast<int>(rows);
@@ -116,7 +120,9 @@ mla_status geometry(int batch, int h_q, int s_q, int topk, int is_fp8, Geometry*
   g->rpc = g->pair ? 128 : rows_per_cta(g->rows);
   g->tile_tokens = g->pair ? 128 : kTileTokens;
   g->row_groups = (g->rows + g->rpc - 1) / g->rpc;
-  g->num_parts = (g->pair ? sms / 2 : sms) / g->row_groups;
+  // persistent grids: one CTA (or CTA pair) per SM (or per pair of SMs that
+  // can hold one) for every row group of a part
+  g->num_parts = (g->pair ? pairs : sms) / g->row_groups;
   const int forced = g_test_num_parts.load();
   if (forced > 0) g->num_parts = forced;
   if (g->num_parts < 1) g->num_parts = 1;
@@ -169,6 +175,26 @@ mla_status encode_rows_map(CUtensorMap* map, const void* base, long long nrows, 
   cuuint64_t dims[3] = {64, 9, static_cast<cuuint64_t>(nrows)};
   cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(kDqk * 2)};
   cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", what, (int)r);
+  return MLA_OK;
+}
+
+// The same 576-wide bf16 rows viewed chunk-major: dim0 = 64 elements of a
+// chunk, dim1 = row (stride 1152 B), dim2 = chunk (stride 128 B).  A box of
+// {64, 64, n} copies n chunks of 64 consecutive rows in one instruction and
+// lands as n x [64 rows][128 B] with the 128-byte swizzle: n consecutive
+// K-major operand tiles of the tcgen05 MMAs.
+mla_status encode_chunk_major_map(CUtensorMap* map, const void* base, long long nrows, int box_chunks,
+                                  const char* what) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(nrows), 9};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDqk * 2), 128};
+  cuuint32_t box[3] = {64, 64, static_cast<cuuint32_t>(box_chunks)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -350,13 +376,24 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
   st = device_info(&status, nullptr);
   if (st != MLA_OK) return st;
 
-  CUtensorMap tm_q, tm_kv;
+  CUtensorMap tm_q, tm_kv, tm_kv2;
   const long long qrows = static_cast<long long>(a->batch) * a->s_q * a->h_q;
-  st = encode_rows_map(&tm_q, a->q, qrows, g.pair ? g.rpc / 2 : g.rpc, "q");
+  const long long cache_rows = static_cast<long long>(a->num_pages) * kPageSize;
+  if (g.pair) {
+    // chunk-major boxes: Q of a CTA in one copy, a page's score operand in three
+    // copies of three chunks, its value shares in copies of two chunks
+    st = encode_chunk_major_map(&tm_q, a->q, qrows, kNumChunks, "q");
+    if (st == MLA_OK) st = encode_chunk_major_map(&tm_kv, a->kvcache, cache_rows, 3, "kvcache");
+    if (st == MLA_OK) st = encode_chunk_major_map(&tm_kv2, a->kvcache, cache_rows, 2, "kvcache");
+    if (st != MLA_OK) return st;
+  } else {
+    st = encode_rows_map(&tm_q, a->q, qrows, g.rpc, "q");
+  }
   if (st != MLA_OK) return st;
   const int mode = g.mode;
-  const long long cache_rows = static_cast<long long>(a->num_pages) * kPageSize;
-  if (mode == 0)
+  if (g.pair)
+    ;  // maps encoded above
+  else if (mode == 0)
     st = encode_rows_map(&tm_kv, a->kvcache, cache_rows, kPageSize, "kvcache");
   else if (mode == 3)
     st = encode_byte_rows_map(&tm_kv, a->kvcache, cache_rows, 2 * kDqk, 1);
@@ -399,7 +436,7 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
   p.fp8_rope_off = a->kv_scales ? kDv : kFp8RopeOffset;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = g.pair ? launch_decode_pair(tm_q, tm_kv, p, s) : launch_decode(tm_q, tm_kv, p, g.rpc, mode, s);
+  cudaError_t e = g.pair ? launch_decode_pair(tm_q, tm_kv, tm_kv2, p, s) : launch_decode(tm_q, tm_kv, p, g.rpc, mode, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
 
   CombineParams cp;

@@ -33,7 +33,8 @@
 //
 // Shared memory (1024-byte aligned, identical in both CTAs):
 //   Q    9 chunks [64 rows][64 dims] bf16, 128-byte swizzle         72 KB
-//   KS   9 slots: chunk k of the CTA's own page (score operand)      72 KB
+//   KS   9 slots: chunk k of the CTA's own page (score operand,      72 KB
+//        three copies of three chunks, released a group at a time)
 //   KV   8 slots: page t of the tile, share s at slot 4t + s          64 KB
 //   P    2 chunks [64 rows][64 tokens] bf16 (PV operand)             16 KB
 //   barriers, row statistics
@@ -61,6 +62,28 @@
 #include "mla_internal.h"
 
 namespace mla {
+
+// Pipeline tracing (built only with -DMLA_TRACE): clock64() stamps of the
+// pipeline events of the first CTA pair, per (CTA, event, tile).
+#ifdef MLA_TRACE
+constexpr int kPairTrTiles = 256, kPairTrEvents = 16;
+__device__ unsigned long long g_pair_trace[2 * kPairTrEvents * kPairTrTiles];
+#define PAIR_TR(rank, ev, idx)                                                                      \
+  do {                                                                                              \
+    if (blockIdx.x < 2 && (idx) < kPairTrTiles) g_pair_trace[((rank) * kPairTrEvents + (ev)) * kPairTrTiles + (idx)] = clock64(); \
+  } while (0)
+extern "C" int mla_pair_trace_read(unsigned long long* host, size_t n) {
+  const size_t total = sizeof(g_pair_trace) / sizeof(unsigned long long);
+  if (n > total) n = total;
+  if (cudaMemcpyFromSymbol(host, g_pair_trace, n * sizeof(unsigned long long)) != cudaSuccess) return -1;
+  return static_cast<int>(n);
+}
+#else
+#define PAIR_TR(rank, ev, idx) \
+  do {                         \
+  } while (0)
+#endif
+
 namespace {
 
 constexpr int kPairRows = 64;            // query rows per CTA
@@ -86,21 +109,22 @@ constexpr uint32_t kPairSmBar = 1;       // named barrier of the 256 softmax thr
 constexpr uint32_t kPairRegsCtl = 88, kPairRegsSm = 208, kPairLaunchRegs = 168;
 static_assert(128 * kPairRegsCtl + 256 * kPairRegsSm <= 65536, "register split");
 
+constexpr int kKsGroups = 3;             // a page's score operand arrives in three copies of three chunks
 enum PairBar {
   kBQFull = 0,    // Q of the segment loaded (even: both CTAs, odd: own)
   kBQEmpty = 1,   // the segment's last score MMAs are done (Q reusable)
-  kBKsFull = 2,   // [9] own page chunk k loaded (even: both CTAs, odd: own)
-  kBKsEmpty = 11, // [9] the score MMAs have read chunk slot k
-  kBKvFull = 20,  // the tile's value-operand slots are loaded (own CTA)
-  kBKvEmpty = 21, // the tile's PV MMAs are done (value slots reusable)
-  kBSFull = 22,   // [2] S of a tile is in TMEM
-  kBSEmpty = 24,  // [2] (even) both CTAs' softmax warps have read an S buffer
-  kBPFull = 26,   // (even) both CTAs' P of the tile is written, O rescaled
-  kBPEmpty = 27,  // the tile's PV MMAs are done (P reusable, O current)
-  kBOFull = 28,   // the segment's last PV MMAs are done
-  kBOEmpty = 29,  // (even) both CTAs' epilogues have read O
-  kBMmaDone = 30, // (even) drain of the MMA issuers
-  kBCount = 31
+  kBKsFull = 2,   // [3] own page chunks 3g..3g+2 loaded (even: both CTAs, odd: own)
+  kBKsEmpty = 5,  // [3] the score MMAs have read chunk slots 3g..3g+2
+  kBKvFull = 8,   // the tile's value-operand slots are loaded (own CTA)
+  kBKvEmpty = 9,  // the tile's PV MMAs are done (value slots reusable)
+  kBSFull = 10,   // [2] S of a tile is in TMEM
+  kBSEmpty = 12,  // [2] (even) both CTAs' softmax warps have read an S buffer
+  kBPFull = 14,   // (even) both CTAs' P of the tile is written, O rescaled
+  kBPEmpty = 15,  // the tile's PV MMAs are done (P reusable, O current)
+  kBOFull = 16,   // the segment's last PV MMAs are done
+  kBOEmpty = 17,  // (even) both CTAs' epilogues have read O
+  kBMmaDone = 18, // (even) drain of the MMA issuers
+  kBCount = 19
 };
 static_assert(kBCount * 8 <= kPairBarBytes, "barrier area");
 
@@ -166,12 +190,12 @@ __device__ __forceinline__ void pair_drain(uint32_t bar, uint32_t parity, uint64
 // ---------------------------------------------------------------------------
 // warp 0: Q and the score operand (the CTA's own page of each tile)
 // ---------------------------------------------------------------------------
-__device__ void pair_producer_ks(const CUtensorMap* tm_q, const CUtensorMap* tm_kv, const DecodeParams& p,
+__device__ void pair_producer_ks(const CUtensorMap* tm_q, const CUtensorMap* tm_ks, const DecodeParams& p,
                                  const PairSeg& sg, int g, int rank, uint32_t smem, uint32_t bars,
                                  const Watchdog& wd) {
   const int lane = threadIdx.x & 31;
   const uint64_t pol = l2_policy_evict_normal();
-  uint32_t armed = 0, next_par = 0;  // ks_full barriers armed (bit k), parity of their next phase
+  uint32_t armed = 0, next_par = 0;  // ks_full barriers armed (bit per group), parity of their next phase
   int q_armed = 0, jt = 0;
   for (int prob = sg.p0; prob <= sg.last(); ++prob) {
     int tb, te;
@@ -179,11 +203,12 @@ __device__ void pair_producer_ks(const CUtensorMap* tm_q, const CUtensorMap* tm_
     if (tb >= te) continue;
     if (q_armed > 0 && !pair_wait(bars + 8 * kBQEmpty, (q_armed - 1) & 1, wd)) goto drain;
     {
+      // this CTA's 64 query rows, all nine chunks, in one copy
       const int row0 = prob * p.rows + g * 2 * kPairRows + rank * kPairRows;
-      if (lane == 0) mbar_arrive_expect_tx_u32(bars + 8 * kBQFull, kNumChunks * kPairChunk);
-      __syncwarp();
-      if (lane < kNumChunks)
-        tma3(smem + kPairQOff + lane * kPairChunk, tm_q, bars + 8 * kBQFull, 0, lane, row0, pol);
+      if (lane == 0) {
+        mbar_arrive_expect_tx_u32(bars + 8 * kBQFull, kNumChunks * kPairChunk);
+        tma3(smem + kPairQOff, tm_q, bars + 8 * kBQFull, 0, row0, 0, pol);
+      }
       __syncwarp();
       ++q_armed;
     }
@@ -192,16 +217,20 @@ __device__ void pair_producer_ks(const CUtensorMap* tm_q, const CUtensorMap* tm_
       const int L = sg.seqlens[b];
       for (int j = tb; j < te; ++j, ++jt) {
         const int pg = tile_page(p, b, L, j, rank, lane == 0);
+        if (lane == 0) PAIR_TR(rank, 0, jt);
 #pragma unroll 1
-        for (int k = 0; k < kNumChunks; ++k) {
-          const uint32_t fb = bars + 8 * (kBKsFull + k);
-          if (jt > 0 && !pair_wait(bars + 8 * (kBKsEmpty + k), (jt - 1) & 1, wd)) goto drain;
-          if (lane == 0) mbar_arrive_expect_tx_u32(fb, pg >= 0 ? kPairChunk : 0u);
+        for (int gr = 0; gr < kKsGroups; ++gr) {
+          const uint32_t fb = bars + 8 * (kBKsFull + gr);
+          if (jt > 0 && !pair_wait(bars + 8 * (kBKsEmpty + gr), (jt - 1) & 1, wd)) goto drain;
+          if (lane == 0) {
+            mbar_arrive_expect_tx_u32(fb, pg >= 0 ? 3 * kPairChunk : 0u);
+            if (pg >= 0) tma3(smem + kPairKsOff + 3 * gr * kPairChunk, tm_ks, fb, 0, pg * kPageSize, 3 * gr, pol);
+          }
           __syncwarp();
-          armed |= 1u << k;
-          next_par ^= 1u << k;
-          if (pg >= 0 && lane == 0) tma3(smem + kPairKsOff + k * kPairChunk, tm_kv, fb, 0, k, pg * kPageSize, pol);
-          __syncwarp();
+          armed |= 1u << gr;
+          next_par ^= 1u << gr;
+          if (lane == 0 && gr == 0) PAIR_TR(rank, 1, jt);
+          if (lane == 0 && gr == kKsGroups - 1) PAIR_TR(rank, 2, jt);
         }
       }
     }
@@ -209,8 +238,8 @@ __device__ void pair_producer_ks(const CUtensorMap* tm_q, const CUtensorMap* tm_
 drain:
   if (lane == 0) {
 #pragma unroll 1
-    for (int k = 0; k < kNumChunks; ++k)
-      if ((armed >> k) & 1u) pair_drain(bars + 8 * (kBKsFull + k), ((next_par >> k) & 1u) ^ 1u, wd.limit_ns);
+    for (int gr = 0; gr < kKsGroups; ++gr)
+      if ((armed >> gr) & 1u) pair_drain(bars + 8 * (kBKsFull + gr), ((next_par >> gr) & 1u) ^ 1u, wd.limit_ns);
     if (q_armed > 0) pair_drain(bars + 8 * kBQFull, (q_armed - 1) & 1, wd.limit_ns);
   }
   __syncwarp();
@@ -238,15 +267,17 @@ __device__ void pair_producer_kv(const CUtensorMap* tm_kv, const DecodeParams& p
       const int pg0 = tile_page(p, b, L, j, 0, false);
       const int pg1 = tile_page(p, b, L, j, 1, false);
       if (jt > 0 && !pair_wait(bars + 8 * kBKvEmpty, (jt - 1) & 1, wd)) goto drain;
+      if (lane == 0) PAIR_TR(rank, 12, jt);
       const uint32_t bytes = static_cast<uint32_t>(((pg0 >= 0) + (pg1 >= 0)) * 4 * kPairChunk);
       if (lane == 0) mbar_arrive_expect_tx_u32(fb, bytes);
       __syncwarp();
       armed = true;
-      if (lane < 8) {
-        const int t = lane >> 2, s = lane & 3;
+      if (lane < 4) {
+        // page t, value block m: chunks 4m + 2 rank and 4m + 2 rank + 1 into slots 4t + 2m, 4t + 2m + 1
+        const int t = lane >> 1, m = lane & 1;
         const int pg = t ? pg1 : pg0;
-        const int c = 4 * (s >> 1) + 2 * rank + (s & 1);
-        if (pg >= 0) tma3(smem + kPairKvOff + (4 * t + s) * kPairChunk, tm_kv, fb, 0, c, pg * kPageSize, pol);
+        if (pg >= 0)
+          tma3(smem + kPairKvOff + (4 * t + 2 * m) * kPairChunk, tm_kv, fb, 0, pg * kPageSize, 4 * m + 2 * rank, pol);
       }
       __syncwarp();
     }
@@ -272,10 +303,12 @@ __device__ void pair_forwarder(const PairSeg& sg, uint32_t bars, uint32_t bars_e
     __syncwarp();
     for (int j = tb; j < te; ++j, ++jt) {
 #pragma unroll 1
-      for (int k = 0; k < kNumChunks; ++k) {
-        if (!pair_wait(bars + 8 * (kBKsFull + k), jt & 1, wd)) return;
-        if (lane == 0) mbar_arrive_cluster(bars_even + 8 * (kBKsFull + k));
+      for (int gr = 0; gr < kKsGroups; ++gr) {
+        if (!pair_wait(bars + 8 * (kBKsFull + gr), jt & 1, wd)) return;
+        if (lane == 0) mbar_arrive_cluster(bars_even + 8 * (kBKsFull + gr));
         __syncwarp();
+        if (lane == 0 && gr == 0) PAIR_TR(1, 3, jt);
+        if (lane == 0 && gr == kKsGroups - 1) PAIR_TR(1, 4, jt);
       }
     }
     ++seg;
@@ -302,17 +335,23 @@ __device__ void pair_s_issuer(const PairSeg& sg, uint32_t tmem, uint32_t smem, u
       tc_fence_after();
       const uint32_t d = tmem + kPairSCol + sb * (kPairTile / 2);
 #pragma unroll 1
-      for (int k = 0; k < kNumChunks; ++k) {
-        if (!pair_wait(bars + 8 * (kBKsFull + k), jt & 1, wd)) goto done;
+      for (int gr = 0; gr < kKsGroups; ++gr) {
+        if (!pair_wait(bars + 8 * (kBKsFull + gr), jt & 1, wd)) goto done;
         tc_fence_after();
-        const uint64_t a0 = kHiK | ((smem + kPairQOff + k * kPairChunk) >> 4);
-        const uint64_t b0 = kHiK | ((smem + kPairKsOff + k * kPairChunk) >> 4);
+        if (lane == 0 && gr == 0) PAIR_TR(0, 3, jt);
+        if (lane == 0 && gr == kKsGroups - 1) PAIR_TR(0, 4, jt);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          if (elect_one()) umma2_bf16_ss(d, a0 + 2 * kk, b0 + 2 * kk, kIdS, (k | kk) != 0);
-          __syncwarp();
+        for (int kc = 0; kc < 3; ++kc) {
+          const int k = 3 * gr + kc;
+          const uint64_t a0 = kHiK | ((smem + kPairQOff + k * kPairChunk) >> 4);
+          const uint64_t b0 = kHiK | ((smem + kPairKsOff + k * kPairChunk) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            if (elect_one()) umma2_bf16_ss(d, a0 + 2 * kk, b0 + 2 * kk, kIdS, (k | kk) != 0);
+            __syncwarp();
+          }
         }
-        if (elect_one()) umma2_commit_both(bars + 8 * (kBKsEmpty + k));
+        if (elect_one()) umma2_commit_both(bars + 8 * (kBKsEmpty + gr));
         __syncwarp();
       }
       if (elect_one()) {
@@ -347,6 +386,7 @@ __device__ void pair_pv_issuer(const PairSeg& sg, uint32_t tmem, uint32_t smem, 
       const bool first = (j == tb), last = (j == te - 1);
       if (!pair_wait(bars + 8 * kBPFull, jt & 1, wd)) goto done;
       tc_fence_after();
+      if (lane == 0) PAIR_TR(0, 10, jt);
       if (first && seg > 0) {
         if (!pair_wait(bars + 8 * kBOEmpty, (seg - 1) & 1, wd)) goto done;
         tc_fence_after();
@@ -369,6 +409,7 @@ __device__ void pair_pv_issuer(const PairSeg& sg, uint32_t tmem, uint32_t smem, 
         if (last) umma2_commit_both(bars + 8 * kBOFull);
       }
       __syncwarp();
+      if (lane == 0) PAIR_TR(0, 11, jt);
     }
     ++seg;
   }
@@ -428,6 +469,8 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
       const int sb = jt & 1;
       if (!wait_all(kBSFull + sb, (jt >> 1) & 1)) return;
       tc_fence_after();
+      const bool tr = (warp == 4 && lane == 0);
+      if (tr) PAIR_TR(rank, 5, jt);
       float x[32];
       tmem_ld_x32(tmem + lane_base + kPairSCol + sb * (kPairTile / 2) + 32 * w, x);
       tmem_ld_wait();
@@ -451,6 +494,7 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
       const float m_new = raise ? fmaxf(m_old, rmax) : m_old;
       // any row of either warpgroup raised its max (after the first tile): O needs a rescale
       const bool any = named_bar_or(kPairSmBar, 256, raise && j != tb);
+      if (tr) PAIR_TR(rank, 6, jt);
       if (raise && hw == 0) m_s[r] = m_new;
       const float alpha = (m_old == kPairNegInf) ? 0.f : fast_exp2(m_old - m_new);
       if (raise) l_part *= alpha;
@@ -463,6 +507,7 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
       // P and O of the previous tile are free once its PV MMAs are done
       if (jt > 0 && !wait_all(kBPEmpty, (jt - 1) & 1)) return;
       tc_fence_after();
+      if (tr) PAIR_TR(rank, 7, jt);
       if (any) {
         // rescale this thread's row of O (its lane's 128 columns of block w) by alpha
         const float a = raise ? alpha : 1.0f;
@@ -493,6 +538,7 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
       // unusable page get zero value rows (their P is 0, but the slot may
       // hold NaN, and 0 * NaN would poison O)
       if (!wait_all(kBKvFull, jt & 1)) return;
+      if (tr) PAIR_TR(rank, 8, jt);
       {
         const int tl = (q & 1) * 32 + lane;  // token of page h zeroed by this thread
         if (!page_ok || j * kPairTile + h * 64 + tl >= L) {
@@ -507,6 +553,7 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
       fence_proxy_async_smem();
       tc_fence_before();
       arrive_even(kBPFull);
+      if (tr) PAIR_TR(rank, 9, jt);
     }
 
     // ---- epilogue: O / l -> out (single piece) or fp32 partial (split problem)
@@ -573,8 +620,8 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
 // kernel
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kPairThreads, 1)
-    mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-                           const DecodeParams p) {
+    mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_ks,
+                           const __grid_constant__ CUtensorMap tm_kv, const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t smem = smem_u32(base);
@@ -598,9 +645,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     const uint32_t fwd = rank == 0 ? 2 : 1;
     mbar_init(bp + kBQFull, fwd);
     mbar_init(bp + kBQEmpty, 1);
-    for (int k = 0; k < kNumChunks; ++k) {
-      mbar_init(bp + kBKsFull + k, fwd);
-      mbar_init(bp + kBKsEmpty + k, 1);
+    for (int gr = 0; gr < kKsGroups; ++gr) {
+      mbar_init(bp + kBKsFull + gr, fwd);
+      mbar_init(bp + kBKsEmpty + gr, 1);
     }
     mbar_init(bp + kBKvFull, 1);
     mbar_init(bp + kBKvEmpty, 1);
@@ -618,6 +665,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_ks);
     tma_prefetch_desc(&tm_kv);
   }
   if (warp == 2) {
@@ -659,7 +707,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   if (warp < 4) {
     regs_to<kPairRegsCtl, kPairLaunchRegs>();
     if (warp == 0) {
-      pair_producer_ks(&tm_q, &tm_kv, p, sg, g, rank, smem, bars, wd);
+      pair_producer_ks(&tm_q, &tm_ks, p, sg, g, rank, smem, bars, wd);
     } else if (warp == 1) {
       if (rank == 0)
         pair_s_issuer(sg, tmem, smem, bars, wd);
@@ -688,8 +736,27 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_decode_pair(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const DecodeParams& p,
-                               cudaStream_t stream) {
+int pair_cluster_capacity() {
+  auto kern = mla_decode_pair_kernel;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kPairThreads);
+  cfg.dynamicSmemBytes = kPairSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+  return n;
+}
+
+cudaError_t launch_decode_pair(const CUtensorMap& tm_q, const CUtensorMap& tm_ks, const CUtensorMap& tm_kv,
+                               const DecodeParams& p, cudaStream_t stream) {
   auto kern = mla_decode_pair_kernel;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
   if (e != cudaSuccess) return e;
@@ -711,7 +778,7 @@ cudaError_t launch_decode_pair(const CUtensorMap& tm_q, const CUtensorMap& tm_kv
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, tm_q, tm_kv, p);
+  return cudaLaunchKernelEx(&cfg, kern, tm_q, tm_ks, tm_kv, p);
 }
 
 }  // namespace mla

@@ -131,9 +131,13 @@ cudaError_t launch_metadata(const int32_t* cache_seqlens, int s_q, int topk, con
 // mode: 0 dense bf16 cache, 1 sparse FP8 cache, 2 dense FP8 cache, 3 sparse bf16 rows
 cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const DecodeParams& p, int rpc,
                           int mode, cudaStream_t stream);
+// CTA pairs the pair decode kernel can keep resident at once on the current
+// device (0 if the query fails)
+int pair_cluster_capacity();
 // CTA-pair decode (dense over the bf16 cache, problems of more than 64 rows)
-cudaError_t launch_decode_pair(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const DecodeParams& p,
-                               cudaStream_t stream);
+// tm_q, tm_ks, tm_kv: chunk-major maps with boxes of 9 chunks (Q), 3 and 2 chunks (cache)
+cudaError_t launch_decode_pair(const CUtensorMap& tm_q, const CUtensorMap& tm_ks, const CUtensorMap& tm_kv,
+                               const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
 size_t decode_smem_bytes(int rpc, int mode);
 cudaError_t launch_fp8_cache_store(const uint16_t* x, int num_tokens, const int32_t* row_offsets,

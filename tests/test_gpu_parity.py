@@ -106,6 +106,46 @@ def test_rescale_path_increasing_logits():
     compare(out, lse, ref_out, ref_lse, "ramp")
 
 
+# ---------------------------------------------------------------- CTA-pair kernel (more than 64 rows, bf16 cache)
+@pytest.mark.parametrize("L", [1, 63, 64, 65, 127, 128, 129, 200, 256, 257, 1000])
+def test_pair_lengths(L):
+    """128-token tiles of two pages: a tile whose second page holds no token, ragged last pages."""
+    check(W.custom(name=f"pl{L}", batch=2, h_q=128, s_q=1, mode="dense", seqlens=(L, max(1, L // 3))), 1500 + L)
+
+
+@pytest.mark.parametrize("h_q,s_q", [(96, 1), (80, 2), (128, 3), (65, 1), (256, 1)])
+def test_pair_row_shapes(h_q, s_q):
+    """Ghost rows in the odd CTA or the second pair, several pairs per problem."""
+    check(W.custom(name=f"ph{h_q}s{s_q}", batch=3, h_q=h_q, s_q=s_q, mode="dense", seqlens=(300, 77, 700)),
+          1600 + h_q + s_q)
+
+
+@pytest.mark.parametrize("parts", [1, 3, 38, 200])
+def test_pair_forced_splits_causal(parts):
+    w = W.custom(name=f"pp{parts}", batch=4, h_q=128, s_q=2, mode="dense", seqlens=(1000, 0, 130, 2049),
+                 causal=True)
+    out, lse, _, _ = check(w, 1700 + parts, parts=parts)
+    assert np.all(out[1] == 0) and np.all(np.isneginf(lse[1]))
+
+
+def test_pair_bad_page_is_flagged_not_faulted():
+    w = W.custom(name="pbad", batch=2, h_q=128, s_q=1, mode="dense", seqlens=(300, 100))
+    inp = W.make_inputs(w, seed=19)
+    bt = inp.block_table.clone()
+    bt[0, 1] = inp.kvcache.shape[0] + 9   # the odd CTA's page of tile 0
+    bt[0, 2] = -3                         # the even CTA's page of tile 1
+    inp.block_table = bt
+    out, lse, flags = run_cuda(inp)
+    assert flags & mla.DEVICE_BAD_PAGE
+    assert np.all(np.isfinite(out))
+
+
+def test_pair_rescale_path():
+    """A large scale makes later tiles raise the running max by far more than the threshold."""
+    check(W.custom(name="pbig", batch=2, h_q=128, s_q=1, mode="dense", seqlens=(1500, 800), sm_scale=0.6), 1801,
+          parts=1)
+
+
 # ---------------------------------------------------------------- sparse mode
 @pytest.mark.parametrize("h_q,topk", [(16, 64), (16, 200), (64, 128), (128, 300), (32, 1000), (48, 129)])
 def test_sparse_small(h_q, topk):
