@@ -41,18 +41,18 @@
 // TMEM (512 columns, allocated for the pair): O at [0, 256) (block m of 256
 // dv at [128m, 128m + 128)), S double buffer at [256, 320) and [320, 384).
 //
-// Synchronisation.  Only the even CTA issues MMAs.  Its producer arms its
-// own barriers with its own bytes; the odd CTA's copies complete on the odd
-// CTA's barriers and its idle MMA-issuer warp forwards each completion to the
-// even CTA with a remote arrive, so every CTA can drain its own copies.  The
-// MMA warps commit to the barriers of both CTAs at once (multicast); the odd
+// Synchronisation.  Only the even CTA issues MMAs.  Its producers arm its
+// barriers with the bytes of both CTAs, and the odd CTA's copies (cta_group::2
+// TMA) complete on them directly; pages without tokens or with an unusable
+// block-table entry are read past the end of the cache, as zeros.  The MMA
+// warps commit to the barriers of both CTAs at once (multicast); the odd
 // CTA's softmax warps arrive remotely on the even CTA's barriers.  Every wait
 // is bounded by the watchdog; a CTA that gives up records MLA_DEVICE_TIMEOUT
 // and unwinds, and its partner's waits then run out too.
 //
 // Roles (384 threads):
 //   warp 0      Q + score-operand producer (TMA), both CTAs
-//   warp 1      score MMA issuer (even CTA) / completion forwarder (odd CTA)
+//   warp 1      score MMA issuer (even CTA)
 //   warp 2      TMEM allocation, then value-operand producer (TMA), both CTAs
 //   warp 3      PV MMA issuer (even CTA)
 //   warps 4-11  softmax + epilogue: warp w reads TMEM lane quarter w % 4, so
@@ -68,10 +68,15 @@ namespace mla {
 #ifdef MLA_TRACE
 constexpr int kPairTrTiles = 256, kPairTrEvents = 16;
 __device__ unsigned long long g_pair_trace[2 * kPairTrEvents * kPairTrTiles];
+// per CTA (up to 1024): %globaltimer at the start of its work, at its end, and its tile count
+__device__ unsigned long long g_pair_cta[3 * 1024];
 #define PAIR_TR(rank, ev, idx)                                                                      \
   do {                                                                                              \
     if (blockIdx.x < 2 && (idx) < kPairTrTiles) g_pair_trace[((rank) * kPairTrEvents + (ev)) * kPairTrTiles + (idx)] = clock64(); \
   } while (0)
+extern "C" int mla_pair_cta_read(unsigned long long* host) {
+  return cudaMemcpyFromSymbol(host, g_pair_cta, sizeof(g_pair_cta)) == cudaSuccess ? 0 : -1;
+}
 extern "C" int mla_pair_trace_read(unsigned long long* host, size_t n) {
   const size_t total = sizeof(g_pair_trace) / sizeof(unsigned long long);
   if (n > total) n = total;
@@ -164,6 +169,31 @@ __device__ __forceinline__ void tma3(uint32_t dst, const void* map, uint32_t bar
       : "memory");
 }
 
+// The same copy, completing on an mbarrier of the even CTA (shared::cluster address).
+__device__ __forceinline__ void tma3_to_even(uint32_t dst, const void* map, uint32_t bar_cluster, int c0, int c1, int c2,
+                                             uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+
+// Tile j of a problem of L tokens holds a page that straddles the length:
+// its slots past the length may hold anything (e.g. NaN), so the value rows
+// of those tokens are zeroed after the copy lands, before the PV MMAs.
+__device__ __forceinline__ bool tail_tile(int L, int j) {
+  return L > 0 && (L & (kPageSize - 1)) != 0 && j == (L - 1) / kPairTile;
+}
+
+// Prefetch a box of a tensor map into L2 (no shared memory involved).
+__device__ __forceinline__ void tma_prefetch3(const void* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 // Warp-uniform bounded wait on a barrier of this CTA.
 __device__ __forceinline__ bool pair_wait(uint32_t bar, uint32_t parity, const Watchdog& wd) {
   uint64_t t0 = 0;
@@ -191,10 +221,15 @@ __device__ __forceinline__ void pair_drain(uint32_t bar, uint32_t parity, uint64
 // warp 0: Q and the score operand (the CTA's own page of each tile)
 // ---------------------------------------------------------------------------
 __device__ void pair_producer_ks(const CUtensorMap* tm_q, const CUtensorMap* tm_ks, const DecodeParams& p,
-                                 const PairSeg& sg, int g, int rank, uint32_t smem, uint32_t bars,
+                                 const PairSeg& sg, int g, int rank, uint32_t smem, uint32_t bars, uint32_t bars_even,
                                  const Watchdog& wd) {
+  // The even CTA arms its Q and score-operand barriers with the bytes of
+  // both CTAs; the odd CTA's copies complete on them directly.  A page that
+  // holds no token or whose block-table entry is unusable is read at a row
+  // past the end of the cache, which the copy fills with zeros.
   const int lane = threadIdx.x & 31;
   const uint64_t pol = l2_policy_evict_normal();
+  const int oob_row = p.num_pages * kPageSize;
   uint32_t armed = 0, next_par = 0;  // ks_full barriers armed (bit per group), parity of their next phase
   int q_armed = 0, jt = 0;
   for (int prob = sg.p0; prob <= sg.last(); ++prob) {
@@ -206,8 +241,12 @@ __device__ void pair_producer_ks(const CUtensorMap* tm_q, const CUtensorMap* tm_
       // this CTA's 64 query rows, all nine chunks, in one copy
       const int row0 = prob * p.rows + g * 2 * kPairRows + rank * kPairRows;
       if (lane == 0) {
-        mbar_arrive_expect_tx_u32(bars + 8 * kBQFull, kNumChunks * kPairChunk);
-        tma3(smem + kPairQOff, tm_q, bars + 8 * kBQFull, 0, row0, 0, pol);
+        if (rank == 0) {
+          mbar_arrive_expect_tx_u32(bars + 8 * kBQFull, 2 * kNumChunks * kPairChunk);
+          tma3(smem + kPairQOff, tm_q, bars + 8 * kBQFull, 0, row0, 0, pol);
+        } else {
+          tma3_to_even(smem + kPairQOff, tm_q, bars_even + 8 * kBQFull, 0, row0, 0, pol);
+        }
       }
       __syncwarp();
       ++q_armed;
@@ -217,14 +256,26 @@ __device__ void pair_producer_ks(const CUtensorMap* tm_q, const CUtensorMap* tm_
       const int L = sg.seqlens[b];
       for (int j = tb; j < te; ++j, ++jt) {
         const int pg = tile_page(p, b, L, j, rank, lane == 0);
+        const int row = pg >= 0 ? pg * kPageSize : oob_row;
         if (lane == 0) PAIR_TR(rank, 0, jt);
+        // the page two tiles ahead goes to L2 now, so that its copy into shared
+        // memory (which must wait for this tile's score MMAs) hits L2
+        if (j + 2 < te) {
+          const int pg2 = tile_page(p, b, L, j + 2, rank, false);
+          if (pg2 >= 0 && lane < kKsGroups) tma_prefetch3(tm_ks, 0, pg2 * kPageSize, 3 * lane);
+        }
 #pragma unroll 1
         for (int gr = 0; gr < kKsGroups; ++gr) {
           const uint32_t fb = bars + 8 * (kBKsFull + gr);
           if (jt > 0 && !pair_wait(bars + 8 * (kBKsEmpty + gr), (jt - 1) & 1, wd)) goto drain;
           if (lane == 0) {
-            mbar_arrive_expect_tx_u32(fb, pg >= 0 ? 3 * kPairChunk : 0u);
-            if (pg >= 0) tma3(smem + kPairKsOff + 3 * gr * kPairChunk, tm_ks, fb, 0, pg * kPageSize, 3 * gr, pol);
+            if (rank == 0) {
+              mbar_arrive_expect_tx_u32(fb, 2 * 3 * kPairChunk);
+              tma3(smem + kPairKsOff + 3 * gr * kPairChunk, tm_ks, fb, 0, row, 3 * gr, pol);
+            } else {
+              tma3_to_even(smem + kPairKsOff + 3 * gr * kPairChunk, tm_ks, bars_even + 8 * (kBKsFull + gr), 0, row,
+                           3 * gr, pol);
+            }
           }
           __syncwarp();
           armed |= 1u << gr;
@@ -236,7 +287,9 @@ __device__ void pair_producer_ks(const CUtensorMap* tm_q, const CUtensorMap* tm_
     }
   }
 drain:
-  if (lane == 0) {
+  // the even CTA waits (bounded) for the copies of both CTAs it armed; the
+  // odd CTA's copies are covered by that wait and by the pause before exit
+  if (lane == 0 && rank == 0) {
 #pragma unroll 1
     for (int gr = 0; gr < kKsGroups; ++gr)
       if ((armed >> gr) & 1u) pair_drain(bars + 8 * (kBKsFull + gr), ((next_par >> gr) & 1u) ^ 1u, wd.limit_ns);
@@ -251,10 +304,16 @@ drain:
 // 4m + 2 rank + 1 for m = 0, 1), into slots 4t + s
 // ---------------------------------------------------------------------------
 __device__ void pair_producer_kv(const CUtensorMap* tm_kv, const DecodeParams& p, const PairSeg& sg, int rank,
-                                 uint32_t smem, uint32_t bars, const Watchdog& wd) {
+                                 uint32_t smem, uint32_t bars, uint32_t bars_even, const Watchdog& wd) {
+  // Every tile's value slots complete on the even CTA's kv_full (armed with
+  // both CTAs' bytes), except on a tail tile, where each CTA's copies
+  // complete on its own kv_full so that its softmax warps can zero the rows
+  // past the length before they report P ready.  Each CTA arms its own
+  // kv_full once per tile (the odd CTA with no bytes outside tail tiles).
   const int lane = threadIdx.x & 31;
   const uint64_t pol = l2_policy_evict_normal();
   const uint32_t fb = bars + 8 * kBKvFull;
+  const int oob_row = p.num_pages * kPageSize;
   int jt = 0;
   bool armed = false;
   for (int prob = sg.p0; prob <= sg.last(); ++prob) {
@@ -266,18 +325,28 @@ __device__ void pair_producer_kv(const CUtensorMap* tm_kv, const DecodeParams& p
     for (int j = tb; j < te; ++j, ++jt) {
       const int pg0 = tile_page(p, b, L, j, 0, false);
       const int pg1 = tile_page(p, b, L, j, 1, false);
+      const bool tail = tail_tile(L, j);
       if (jt > 0 && !pair_wait(bars + 8 * kBKvEmpty, (jt - 1) & 1, wd)) goto drain;
-      if (lane == 0) PAIR_TR(rank, 12, jt);
-      const uint32_t bytes = static_cast<uint32_t>(((pg0 >= 0) + (pg1 >= 0)) * 4 * kPairChunk);
-      if (lane == 0) mbar_arrive_expect_tx_u32(fb, bytes);
+      if (lane == 0) {
+        PAIR_TR(rank, 12, jt);
+        const uint32_t own = 4 * kPairChunk * 2;  // two pages x two copies of two chunks
+        if (rank == 0)
+          mbar_arrive_expect_tx_u32(fb, tail ? own : 2 * own);
+        else
+          mbar_arrive_expect_tx_u32(fb, tail ? own : 0u);
+      }
       __syncwarp();
       armed = true;
       if (lane < 4) {
         // page t, value block m: chunks 4m + 2 rank and 4m + 2 rank + 1 into slots 4t + 2m, 4t + 2m + 1
         const int t = lane >> 1, m = lane & 1;
         const int pg = t ? pg1 : pg0;
-        if (pg >= 0)
-          tma3(smem + kPairKvOff + (4 * t + 2 * m) * kPairChunk, tm_kv, fb, 0, pg * kPageSize, 4 * m + 2 * rank, pol);
+        const int row = pg >= 0 ? pg * kPageSize : oob_row;
+        const uint32_t dst = smem + kPairKvOff + (4 * t + 2 * m) * kPairChunk;
+        if (rank == 0 || tail)
+          tma3(dst, tm_kv, fb, 0, row, 4 * m + 2 * rank, pol);
+        else
+          tma3_to_even(dst, tm_kv, bars_even + 8 * kBKvFull, 0, row, 4 * m + 2 * rank, pol);
       }
       __syncwarp();
     }
@@ -285,34 +354,6 @@ __device__ void pair_producer_kv(const CUtensorMap* tm_kv, const DecodeParams& p
 drain:
   if (lane == 0 && armed) pair_drain(fb, (jt - 1) & 1, wd.limit_ns);
   __syncwarp();
-}
-
-// ---------------------------------------------------------------------------
-// warp 1 of the odd CTA: forwards the completion of its Q and score-operand
-// copies to the even CTA's barriers (which count one arrival per CTA)
-// ---------------------------------------------------------------------------
-__device__ void pair_forwarder(const PairSeg& sg, uint32_t bars, uint32_t bars_even, const Watchdog& wd) {
-  const int lane = threadIdx.x & 31;
-  int seg = 0, jt = 0;
-  for (int prob = sg.p0; prob <= sg.last(); ++prob) {
-    int tb, te;
-    sg.range(prob, tb, te);
-    if (tb >= te) continue;
-    if (!pair_wait(bars + 8 * kBQFull, seg & 1, wd)) return;
-    if (lane == 0) mbar_arrive_cluster(bars_even + 8 * kBQFull);
-    __syncwarp();
-    for (int j = tb; j < te; ++j, ++jt) {
-#pragma unroll 1
-      for (int gr = 0; gr < kKsGroups; ++gr) {
-        if (!pair_wait(bars + 8 * (kBKsFull + gr), jt & 1, wd)) return;
-        if (lane == 0) mbar_arrive_cluster(bars_even + 8 * (kBKsFull + gr));
-        __syncwarp();
-        if (lane == 0 && gr == 0) PAIR_TR(1, 3, jt);
-        if (lane == 0 && gr == kKsGroups - 1) PAIR_TR(1, 4, jt);
-      }
-    }
-    ++seg;
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -385,6 +426,7 @@ __device__ void pair_pv_issuer(const PairSeg& sg, uint32_t tmem, uint32_t smem, 
     for (int j = tb; j < te; ++j, ++jt) {
       const bool first = (j == tb), last = (j == te - 1);
       if (!pair_wait(bars + 8 * kBPFull, jt & 1, wd)) goto done;
+      if (!pair_wait(bars + 8 * kBKvFull, jt & 1, wd)) goto done;
       tc_fence_after();
       if (lane == 0) PAIR_TR(0, 10, jt);
       if (first && seg > 0) {
@@ -534,14 +576,15 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
                        pack_bf16x2(pr[8 * u + 6], pr[8 * u + 7]));
         }
       }
-      // the tile's value slots are loaded; tokens past the length or on an
-      // unusable page get zero value rows (their P is 0, but the slot may
-      // hold NaN, and 0 * NaN would poison O)
-      if (!wait_all(kBKvFull, jt & 1)) return;
-      if (tr) PAIR_TR(rank, 8, jt);
-      {
+      // tail tile: this CTA's value slots are loaded (on its own barrier); the
+      // rows of tokens past the length are zeroed (their P is 0, but a slot
+      // may hold NaN, and 0 * NaN would poison O).  Unusable pages were read
+      // as zeros.
+      if (tail_tile(L, j)) {
+        if (!wait_all(kBKvFull, jt & 1)) return;
+        if (tr) PAIR_TR(rank, 8, jt);
         const int tl = (q & 1) * 32 + lane;  // token of page h zeroed by this thread
-        if (!page_ok || j * kPairTile + h * 64 + tl >= L) {
+        if (page_ok && j * kPairTile + h * 64 + tl >= L) {
 #pragma unroll
           for (int s2 = 0; s2 < 2; ++s2) {
             const uint32_t rowa = smem + kPairKvOff + (4 * h + 2 * w + s2) * kPairChunk + tl * 128;
@@ -641,12 +684,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
   if (threadIdx.x == 0) {
     uint64_t* bp = reinterpret_cast<uint64_t*>(base + kPairAuxOff);
-    // the even CTA's Q / score-operand barriers also count the odd CTA's forwarded arrival
-    const uint32_t fwd = rank == 0 ? 2 : 1;
-    mbar_init(bp + kBQFull, fwd);
+    mbar_init(bp + kBQFull, 1);
     mbar_init(bp + kBQEmpty, 1);
     for (int gr = 0; gr < kKsGroups; ++gr) {
-      mbar_init(bp + kBKsFull + gr, fwd);
+      mbar_init(bp + kBKsFull + gr, 1);
       mbar_init(bp + kBKsEmpty + gr, 1);
     }
     mbar_init(bp + kBKvFull, 1);
@@ -704,17 +745,26 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     sg.p1 = sg.np;
   }
 
+#ifdef MLA_TRACE
+  if (threadIdx.x == 0 && blockIdx.x < 1024) {
+    g_pair_cta[3 * blockIdx.x] = global_timer_ns();
+    int n = 0;
+    for (int pr = sg.p0; pr <= sg.last(); ++pr) {
+      int tb, te;
+      sg.range(pr, tb, te);
+      if (te > tb) n += te - tb;
+    }
+    g_pair_cta[3 * blockIdx.x + 2] = n;
+  }
+#endif
   if (warp < 4) {
     regs_to<kPairRegsCtl, kPairLaunchRegs>();
     if (warp == 0) {
-      pair_producer_ks(&tm_q, &tm_ks, p, sg, g, rank, smem, bars, wd);
+      pair_producer_ks(&tm_q, &tm_ks, p, sg, g, rank, smem, bars, bars_even, wd);
     } else if (warp == 1) {
-      if (rank == 0)
-        pair_s_issuer(sg, tmem, smem, bars, wd);
-      else
-        pair_forwarder(sg, bars, bars_even, wd);
+      if (rank == 0) pair_s_issuer(sg, tmem, smem, bars, wd);
     } else if (warp == 2) {
-      pair_producer_kv(&tm_kv, p, sg, rank, smem, bars, wd);
+      pair_producer_kv(&tm_kv, p, sg, rank, smem, bars, bars_even, wd);
     } else if (rank == 0) {
       pair_pv_issuer(sg, tmem, smem, bars, wd);
     }
@@ -725,6 +775,16 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+#ifdef MLA_TRACE
+  if (threadIdx.x == 0 && blockIdx.x < 1024) g_pair_cta[3 * blockIdx.x + 1] = global_timer_ns();
+#endif
+  if (*abort_flag) {
+    // after a timeout, copies the odd CTA issued may still be landing in its
+    // shared memory (their completions go to the even CTA): give them time
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 50000) {
+    }
+  }
   // neither CTA leaves while its partner may still read its shared memory,
   // arrive on its barriers or run MMAs on its TMEM
   cluster_sync_all();
