@@ -86,7 +86,7 @@ NCU_TRAFFIC = {
     "sparse_bf16": (663.91e6, "34b86f766f6da9f3"),
     "sparse_fp8_token": (432.55e6, "34b86f766f6da9f3"),
 }
-KERNEL_SOURCES = ("mla_decode.cu", "mla_device.cuh", "mla_internal.h")
+KERNEL_SOURCES = ("mla_decode.cu", "mla_decode_pair.cu", "mla_device.cuh", "mla_internal.h")
 
 
 def kernel_source_hash() -> str:
@@ -104,6 +104,18 @@ def measured_traffic(workload: str):
     if entry is None or entry[1] != kernel_source_hash():
         return None
     return entry[0]
+
+
+def kernel_name(w) -> str:
+    """The decode kernel the library runs for workload w: problems of more than 64 rows, dense over
+    the bf16 cache or sparse over the FP8 cache, run on CTA pairs; the rest on single CTAs of 16, 32
+    or 64 rows."""
+    rows = w.h_q if w.mode == "sparse" else w.s_q * w.h_q
+    kmode = ("sparse" if w.is_fp8 else "sparse_bf16") if w.mode == "sparse" else ("dense_fp8" if w.is_fp8 else "dense")
+    if rows > 64 and kmode in ("dense", "sparse"):
+        return f"mla_decode_pair_kernel<{kmode}>"
+    rpc = 16 if rows <= 16 else (32 if rows <= 32 else 64)
+    return f"mla_decode_kernel<{rpc},{kmode}>"
 
 
 def load_peaks() -> dict:
@@ -494,7 +506,13 @@ def run_mla(args):
 
     # ---- headline workload: full steps
     wname = args.workload
-    inp = W.make_inputs(wname, seed=rank_seed(wname, rank), device=device)
+    wdef = W.WORKLOADS[wname]
+    if args.batch:
+        # a reduced batch of the same workload (same per-CTA shape): for profiler captures
+        from dataclasses import replace
+        wdef = replace(wdef, batch=args.batch,
+                       seqlens=wdef.seqlens[:args.batch] if wdef.seqlens is not None else None)
+    inp = W.make_inputs(wdef, seed=rank_seed(wname, rank), device=device)
     a = algorithmic(inp)
     step = DecodeStep(inp, device)
     graphs = step.capture()
@@ -533,9 +551,7 @@ def run_mla(args):
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = measured_traffic(wname)
     roof["algorithmic_bytes"] = a["bytes"] if roof["bound"] == "hbm" else None
-    rows = 16 if wl.s_q * wl.h_q <= 16 else (32 if wl.s_q * wl.h_q <= 32 else 64)
-    kmode = "sparse" if wl.mode == "sparse" else ("dense_fp8" if wl.is_fp8 else "dense")
-    roof["kernel"] = f"mla_decode_kernel<{rows},{kmode}> + combine (one decode call)"
+    roof["kernel"] = kernel_name(wl) + " + combine (one decode call)"
     roof["peak_source"] = peaks["source"]
 
     result = {
@@ -689,11 +705,16 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(W.WORKLOADS),
                     help="workload timed as the step (default: the memory-bound dense mix)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="run the workload with this batch size instead of its own (profiler captures of a "
+                         "reduced case; implies --no-extras)")
     ap.add_argument("--extra", choices=["sparse_prefill", "fp8_index_topk", "fp8_cache_store"],
                     help="time only this entry point (one JSON line; used for profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.batch:
+        args.no_extras = True
     if args.extra:
         device = "cuda"
         peaks = load_peaks()

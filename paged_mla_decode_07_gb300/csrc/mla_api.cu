@@ -80,9 +80,12 @@ mla_status device_info(uint32_t** status, int* sm_count, int* pair_capacity = nu
   return MLA_OK;
 }
 
-// The CTA-pair decode kernel for problems of more than 64 rows over the bf16
-// cache (mla_decode_pair.cu).
+// The CTA-pair decode kernel for problems of more than 64 rows, dense over
+// the bf16 cache or sparse over the FP8 cache (mla_decode_pair.cu).
 constexpr bool kPairDecode = true;
+// Sparse over the FP8 cache on CTA pairs (passes every parity test; slower
+// than the single-CTA kernel so far, so not selected yet).
+constexpr bool kPairSparse = false;
 
 // Test hooks (mla_test_hooks): a forced part count and a stalled softmax role.
 std::atomic<int> g_test_num_parts{0};
@@ -114,9 +117,10 @@ mla_status geometry(int batch, int h_q, int s_q, int topk, int is_fp8, Geometry*
   g->rows = static_cast<int>(rows);
   g->mode = decode_mode(topk, is_fp8);
   g->sm_count = sms;
-  // problems of more than 64 rows over the bf16 cache run on CTA pairs (128
-  // rows and 128-token tiles per pair); everything else on single CTAs
-  g->pair = (kPairDecode && g->mode == 0 && g->rows > 64) ? 1 : 0;
+  // problems of more than 64 rows, dense over the bf16 cache or sparse over
+  // the FP8 cache, run on CTA pairs (128 rows and 128-token tiles per pair);
+  // everything else on single CTAs
+  g->pair = (kPairDecode && (g->mode == 0 || (kPairSparse && g->mode == 1)) && g->rows > 64) ? 1 : 0;
   g->rpc = g->pair ? 128 : rows_per_cta(g->rows);
   g->tile_tokens = g->pair ? 128 : kTileTokens;
   g->row_groups = (g->rows + g->rpc - 1) / g->rpc;
@@ -380,11 +384,16 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
   const long long qrows = static_cast<long long>(a->batch) * a->s_q * a->h_q;
   const long long cache_rows = static_cast<long long>(a->num_pages) * kPageSize;
   if (g.pair) {
-    // chunk-major boxes: Q of a CTA in one copy, a page's score operand in three
-    // copies of three chunks, its value shares in copies of two chunks
+    // chunk-major boxes: Q of a CTA in one copy; dense: a page's score operand
+    // in three copies of three chunks, its value shares in copies of two
+    // chunks; sparse: FP8 rows for the row gathers
     st = encode_chunk_major_map(&tm_q, a->q, qrows, kNumChunks, "q");
-    if (st == MLA_OK) st = encode_chunk_major_map(&tm_kv, a->kvcache, cache_rows, 3, "kvcache");
-    if (st == MLA_OK) st = encode_chunk_major_map(&tm_kv2, a->kvcache, cache_rows, 2, "kvcache");
+    if (st == MLA_OK && g.mode == 0) st = encode_chunk_major_map(&tm_kv, a->kvcache, cache_rows, 3, "kvcache");
+    if (st == MLA_OK && g.mode == 0) st = encode_chunk_major_map(&tm_kv2, a->kvcache, cache_rows, 2, "kvcache");
+    if (st == MLA_OK && g.mode == 1) {
+      st = encode_byte_rows_map(&tm_kv, a->kvcache, cache_rows, a->kv_scales ? 640 : kFp8RowBytes, 1);
+      tm_kv2 = tm_kv;
+    }
     if (st != MLA_OK) return st;
   } else {
     st = encode_rows_map(&tm_q, a->q, qrows, g.rpc, "q");
@@ -436,7 +445,8 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
   p.fp8_rope_off = a->kv_scales ? kDv : kFp8RopeOffset;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = g.pair ? launch_decode_pair(tm_q, tm_kv, tm_kv2, p, s) : launch_decode(tm_q, tm_kv, p, g.rpc, mode, s);
+  cudaError_t e = g.pair ? launch_decode_pair(tm_q, tm_kv, tm_kv2, p, g.mode == 1, s)
+                         : launch_decode(tm_q, tm_kv, p, g.rpc, mode, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
 
   CombineParams cp;

@@ -1,5 +1,6 @@
-// K1p — paged MLA decode on CTA pairs (tcgen05 cta_group::2), dense over the
-// bf16 cache, for problems of more than 64 query rows.
+// K1p — paged MLA decode on CTA pairs (tcgen05 cta_group::2) for problems of
+// more than 64 query rows: dense over the bf16 cache, and sparse (top-k) over
+// the FP8 cache.
 //
 // What is computed is the same as in the single-CTA kernel (mla_decode.cu):
 // per query row, softmax(q K^T * sm_scale) V over the row's keys with
@@ -7,57 +8,67 @@
 // "Multi-Head Latent Attention"), with online softmax across tiles (overview,
 // section 6 "Matmul to Flash Attention"), and a split-KV partial with its
 // log-sum-exp where a part covers only some of a problem's tiles (FlashMLA
-// article, Design 5; merged by the combine kernel).
+// article, Design 5; merged by the combine kernel).  In sparse mode the keys
+// of a query token are the valid ids of its index row and each FP8 row is
+// dequantised as bf16_rn(fp32(e4m3) * scale) before the MMAs (FlashMLA
+// article, Design 2).
 //
 // Formulation.  The two CTAs of a cluster (one TPC) work together on 128
-// query rows of a problem, 64 rows each, and on 128-token tiles, one 64-token
-// page each.  Both matrix products are pair MMAs issued by one thread of the
-// even CTA: each CTA supplies half of A's rows and half of B's columns from
-// its own shared memory and receives its half of the result rows in its own
-// TMEM.  For an M = 128 pair result a CTA's row r lies in TMEM lane r for the
-// first half of the columns and in lane 64 + r for the second half.
+// query rows of a problem, 64 rows each, and on 128-token tiles, 64 tokens
+// each (dense: one page per CTA; sparse: index slots 64c .. 64c + 63 of the
+// tile for CTA c).  Both matrix products are pair MMAs issued by one thread
+// of the even CTA: each CTA supplies half of A's rows and half of B's columns
+// from its own shared memory and receives its half of the result rows in its
+// own TMEM.  For an M = 128 pair result a CTA's row r lies in TMEM lane r for
+// the first half of the columns and in lane 64 + r for the second half.
 //     S[row, tok]  = Q[row, :] . K[tok, :]      M = 128 rows, N = 128 tokens, K = 576
-//                    A: the CTA's 64 query rows, B: the CTA's own page
+//                    A: the CTA's 64 query rows, B: the CTA's 64 tokens
 //     O[row, dv]  += P[row, tok] . V[tok, dv]    M = 128 rows, N = 256 dv (twice), K = 128 tokens
 //                    A: the CTA's P rows, B: the CTA's share of the 256 dv
 // An N = 256 pair MMA runs at the tensor pipe's full rate and an N = 128 one
-// at 57 %, where a single-CTA M = 64 score MMA runs at 28 %.  Each CTA loads
-// one page per tile for the scores, and it keeps the running O of its own
-// rows for all 512 value dims (64 rows x 512 fp32 = 256 TMEM columns), so
-// the online-softmax rescale and the epilogue stay inside the CTA.
+// at 57 %, where a single-CTA M = 64 score MMA runs at 28 %.  Each CTA
+// brings in its own 64 tokens per tile for the scores, and it keeps the
+// running O of its own rows for all 512 value dims (64 rows x 512 fp32 = 256
+// TMEM columns), so the online-softmax rescale and the epilogue stay inside
+// the CTA.
 //
 // The value dims a CTA supplies to the PV product must sit at the same
 // shared-memory address in both CTAs while holding different dims (dv 0-127
 // and 256-383 for the even CTA, 128-255 and 384-511 for the odd one), so
-// those dims of both pages of a tile are loaded into a separate set of slots.
+// those dims of all 128 tokens of a tile live in a separate set of slots:
+// for the CTA's own tokens copied (dense: loaded again, sparse: written a
+// second time by the dequantisation), for its partner's tokens loaded
+// (dense) or gathered and dequantised (sparse).
 //
 // Shared memory (1024-byte aligned, identical in both CTAs):
 //   Q    9 chunks [64 rows][64 dims] bf16, 128-byte swizzle         72 KB
-//   KS   9 slots: chunk k of the CTA's own page (score operand,      72 KB
-//        three copies of three chunks, released a group at a time)
-//   KV   8 slots: page t of the tile, share s at slot 4t + s          64 KB
+//   KS   9 slots: dims chunk k of the CTA's 64 tokens (score operand) 72 KB
+//   KV   8 slots: token half t of the tile, share s at slot 4t + s    64 KB
 //   P    2 chunks [64 rows][64 tokens] bf16 (PV operand)             16 KB
-//   barriers, row statistics
+//   barriers, row statistics, token-validity bits (sparse)
 // TMEM (512 columns, allocated for the pair): O at [0, 256) (block m of 256
 // dv at [128m, 128m + 128)), S double buffer at [256, 320) and [320, 384).
 //
-// Synchronisation.  Only the even CTA issues MMAs.  Its producers arm its
-// barriers with the bytes of both CTAs, and the odd CTA's copies (cta_group::2
-// TMA) complete on them directly; pages without tokens or with an unusable
-// block-table entry are read past the end of the cache, as zeros.  The MMA
-// warps commit to the barriers of both CTAs at once (multicast); the odd
-// CTA's softmax warps arrive remotely on the even CTA's barriers.  Every wait
-// is bounded by the watchdog; a CTA that gives up records MLA_DEVICE_TIMEOUT
-// and unwinds, and its partner's waits then run out too.
+// Synchronisation.  Only the even CTA issues MMAs.  Dense: its producers arm
+// its barriers with the bytes of both CTAs, and the odd CTA's copies
+// (cta_group::2 TMA) complete on them directly; pages without tokens or with
+// an unusable block-table entry are read past the end of the cache, as
+// zeros.  Sparse: the gather warps of both CTAs arrive on the even CTA's
+// barriers once they have dequantised an item.  The MMA warps commit to the
+// barriers of both CTAs at once (multicast); the odd CTA's softmax warps
+// arrive remotely on the even CTA's barriers.  Every wait is bounded by the
+// watchdog; a CTA that gives up records MLA_DEVICE_TIMEOUT and unwinds, and
+// its partner's waits then run out too.
 //
-// Roles (384 threads):
-//   warp 0      Q + score-operand producer (TMA), both CTAs
+// Roles:
+//   warp 0      Q (and, dense, the score operand) producer (TMA), both CTAs
 //   warp 1      score MMA issuer (even CTA)
-//   warp 2      TMEM allocation, then value-operand producer (TMA), both CTAs
+//   warp 2      TMEM allocation, then (dense) the value-operand producer
 //   warp 3      PV MMA issuer (even CTA)
 //   warps 4-11  softmax + epilogue: warp w reads TMEM lane quarter w % 4, so
-//               a thread owns one row and one half of the tile (page), and
-//               the two warpgroups split that half's 64 tokens
+//               a thread owns one row and one half of the tile, and the two
+//               warpgroups split that half's 64 tokens
+//   warps 12-15 (sparse) row lookups, TMA row gathers, dequantisation
 #include "mla_device.cuh"
 #include "mla_internal.h"
 
@@ -92,17 +103,21 @@ extern "C" int mla_pair_trace_read(unsigned long long* host, size_t n) {
 namespace {
 
 constexpr int kPairRows = 64;            // query rows per CTA
-constexpr int kPairTile = 128;           // tokens per tile (one page per CTA)
+constexpr int kPairTile = 128;           // tokens per tile (64 per CTA)
 constexpr int kPairChunk = 8192;         // [64 rows or tokens][64 dims] bf16
-constexpr int kPairThreads = 384;
 constexpr int kPairQOff = 0;
 constexpr int kPairKsOff = 9 * kPairChunk;
 constexpr int kPairKvOff = 18 * kPairChunk;
 constexpr int kPairPOff = 26 * kPairChunk;
 constexpr int kPairAuxOff = 28 * kPairChunk;  // 229376
 constexpr int kPairBarBytes = 256;
-// aux: barriers, m[64], red[4][64] (partial row maxima / sums), ints (abort flag, TMEM base)
-constexpr int kPairAuxBytes = kPairBarBytes + 64 * 4 + 4 * 64 * 4 + 64;
+// aux: barriers, m[64], red[4][64] (partial row maxima / sums), ints (abort
+// flag, TMEM base), token-validity bits of four tiles (sparse)
+constexpr int kPairMOff = kPairBarBytes;
+constexpr int kPairRedOff = kPairMOff + 64 * 4;
+constexpr int kPairIntOff = kPairRedOff + 4 * 64 * 4;
+constexpr int kPairFlagOff = kPairIntOff + 64;
+constexpr int kPairAuxBytes = kPairFlagOff + 4 * 16;
 constexpr int kPairSmemBytes = kPairAuxOff + kPairAuxBytes + 1024;  // + alignment slack
 static_assert(kPairSmemBytes <= 232448, "shared memory budget");
 constexpr uint32_t kPairOCol = 0;
@@ -111,36 +126,55 @@ constexpr uint32_t kPairTmemCols = 512;
 constexpr float kPairNegInf = -__builtin_huge_valf();
 constexpr float kPairRescale = 8.0f;     // log2 units: P <= 2^8 before a max update is forced
 constexpr uint32_t kPairSmBar = 1;       // named barrier of the 256 softmax threads
-constexpr uint32_t kPairRegsCtl = 88, kPairRegsSm = 208, kPairLaunchRegs = 168;
-static_assert(128 * kPairRegsCtl + 256 * kPairRegsSm <= 65536, "register split");
+constexpr int kPairGatherWarp0 = 12;
 
-constexpr int kKsGroups = 3;             // a page's score operand arrives in three copies of three chunks
+// Dense: 384 threads, the score operand arrives in three copies of three
+// chunks.  Sparse: 512 threads (four gather warps), the score operand is
+// released and refilled by value block (chunks 2b, 2b + 1) and RoPE chunk.
+// Registers: a kernel that uses setmaxnreg is compiled to the whole
+// per-thread share of the register file; each role moves from it with .inc
+// or .dec, and the shares add up to at most 65536.
+template <bool SPARSE>
+struct PairCfg {
+  static constexpr int kThreads = SPARSE ? 512 : 384;
+  static constexpr int kItems = SPARSE ? 5 : 3;
+  static constexpr uint32_t kRegsCtl = SPARSE ? 64 : 88;
+  static constexpr uint32_t kRegsSm = SPARSE ? 168 : 208;
+  static constexpr uint32_t kRegsGather = 112;
+  static constexpr uint32_t kLaunchRegs = SPARSE ? 128 : 168;
+  static_assert(128 * kRegsCtl + 256 * kRegsSm + (SPARSE ? 128 * kRegsGather : 0) <= 65536, "register split");
+  __device__ static constexpr int item_chunk0(int i) { return SPARSE ? 2 * i : 3 * i; }
+  __device__ static constexpr int item_chunks(int i) { return SPARSE ? (i < 4 ? 2 : 1) : 3; }
+};
+
 enum PairBar {
-  kBQFull = 0,    // Q of the segment loaded (even: both CTAs, odd: own)
+  kBQFull = 0,    // Q of the segment loaded (both CTAs)
   kBQEmpty = 1,   // the segment's last score MMAs are done (Q reusable)
-  kBKsFull = 2,   // [3] own page chunks 3g..3g+2 loaded (even: both CTAs, odd: own)
-  kBKsEmpty = 5,  // [3] the score MMAs have read chunk slots 3g..3g+2
-  kBKvFull = 8,   // the tile's value-operand slots are loaded (own CTA)
-  kBKvEmpty = 9,  // the tile's PV MMAs are done (value slots reusable)
-  kBSFull = 10,   // [2] S of a tile is in TMEM
-  kBSEmpty = 12,  // [2] (even) both CTAs' softmax warps have read an S buffer
-  kBPFull = 14,   // (even) both CTAs' P of the tile is written, O rescaled
-  kBPEmpty = 15,  // the tile's PV MMAs are done (P reusable, O current)
-  kBOFull = 16,   // the segment's last PV MMAs are done
-  kBOEmpty = 17,  // (even) both CTAs' epilogues have read O
-  kBMmaDone = 18, // (even) drain of the MMA issuers
-  kBCount = 19
+  kBKsFull = 2,   // [5] score-operand item i of both CTAs is in place
+  kBKsEmpty = 7,  // [5] the score MMAs have read item i
+  kBKvFull = 12,  // the tile's value-operand slots are in place
+  kBKvEmpty = 13, // the tile's PV MMAs are done (value slots reusable)
+  kBSFull = 14,   // [2] S of a tile is in TMEM
+  kBSEmpty = 16,  // [2] (even) both CTAs' softmax warps have read an S buffer
+  kBPFull = 18,   // (even) both CTAs' P of the tile is written, O rescaled
+  kBPEmpty = 19,  // the tile's PV MMAs are done (P reusable, O current)
+  kBOFull = 20,   // the segment's last PV MMAs are done
+  kBOEmpty = 21,  // (even) both CTAs' epilogues have read O
+  kBMmaDone = 22, // (even) drain of the MMA issuers
+  kBRaw = 23,     // [7] (sparse) raw rows of an item landed in this CTA
+  kBFlags = 30,   // (sparse) the tile's token-validity bits of this CTA are written
+  kBCount = 31
 };
 static_assert(kBCount * 8 <= kPairBarBytes, "barrier area");
 
 // Segment iterator over the part's problems (128-token tiles); every role
 // derives the identical sequence.
 struct PairSeg {
-  int p0, t0, p1, t1, np, s_q;
+  int p0, t0, p1, t1, np, s_q, topk;
   const int32_t* seqlens;
   __device__ int last() const { return p1 < np ? p1 : np - 1; }
   __device__ void range(int p, int& tb, int& te) const {
-    const int n = problem_tiles(seqlens, p, s_q, 0, kPairTile);
+    const int n = problem_tiles(seqlens, p, s_q, topk, kPairTile);
     tb = (p == p0) ? t0 : 0;
     te = (p == p1) ? t1 : n;
     if (te > n) te = n;
@@ -176,6 +210,17 @@ __device__ __forceinline__ void tma3_to_even(uint32_t dst, const void* map, uint
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+
+// Row gather: four rows r0..r3 of a 2-D byte-row map (box 128 bytes x one
+// row) land back to back at dst; x is the byte column.
+__device__ __forceinline__ void gather4(uint32_t dst, const void* map, uint32_t bar, int x, int r0, int r1, int r2,
+                                        int r3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "l"(policy)
       : "memory");
 }
 
@@ -217,9 +262,22 @@ __device__ __forceinline__ void pair_drain(uint32_t bar, uint32_t parity, uint64
     if (global_timer_ns() - t0 > limit_ns) return;
 }
 
+// One arrival of the calling warp on a barrier of the even CTA (remote from the odd CTA).
+__device__ __forceinline__ void warp_arrive_even(int rank, uint32_t bar_local, uint32_t bar_even) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
+    if (rank == 0)
+      mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bar_local)));
+    else
+      mbar_arrive_cluster(bar_even);
+  }
+}
+
 // ---------------------------------------------------------------------------
-// warp 0: Q and the score operand (the CTA's own page of each tile)
+// warp 0: Q of each segment and (dense) the score operand: the CTA's own
+// page of each tile
 // ---------------------------------------------------------------------------
+template <bool SPARSE>
 __device__ void pair_producer_ks(const CUtensorMap* tm_q, const CUtensorMap* tm_ks, const DecodeParams& p,
                                  const PairSeg& sg, int g, int rank, uint32_t smem, uint32_t bars, uint32_t bars_even,
                                  const Watchdog& wd) {
@@ -251,6 +309,7 @@ __device__ void pair_producer_ks(const CUtensorMap* tm_q, const CUtensorMap* tm_
       __syncwarp();
       ++q_armed;
     }
+    if (SPARSE) continue;  // the gather warps fill the score operand
     {
       const int b = prob;
       const int L = sg.seqlens[b];
@@ -262,10 +321,10 @@ __device__ void pair_producer_ks(const CUtensorMap* tm_q, const CUtensorMap* tm_
         // memory (which must wait for this tile's score MMAs) hits L2
         if (j + 2 < te) {
           const int pg2 = tile_page(p, b, L, j + 2, rank, false);
-          if (pg2 >= 0 && lane < kKsGroups) tma_prefetch3(tm_ks, 0, pg2 * kPageSize, 3 * lane);
+          if (pg2 >= 0 && lane < 3) tma_prefetch3(tm_ks, 0, pg2 * kPageSize, 3 * lane);
         }
 #pragma unroll 1
-        for (int gr = 0; gr < kKsGroups; ++gr) {
+        for (int gr = 0; gr < 3; ++gr) {
           const uint32_t fb = bars + 8 * (kBKsFull + gr);
           if (jt > 0 && !pair_wait(bars + 8 * (kBKsEmpty + gr), (jt - 1) & 1, wd)) goto drain;
           if (lane == 0) {
@@ -281,7 +340,7 @@ __device__ void pair_producer_ks(const CUtensorMap* tm_q, const CUtensorMap* tm_
           armed |= 1u << gr;
           next_par ^= 1u << gr;
           if (lane == 0 && gr == 0) PAIR_TR(rank, 1, jt);
-          if (lane == 0 && gr == kKsGroups - 1) PAIR_TR(rank, 2, jt);
+          if (lane == 0 && gr == 2) PAIR_TR(rank, 2, jt);
         }
       }
     }
@@ -291,7 +350,7 @@ drain:
   // odd CTA's copies are covered by that wait and by the pause before exit
   if (lane == 0 && rank == 0) {
 #pragma unroll 1
-    for (int gr = 0; gr < kKsGroups; ++gr)
+    for (int gr = 0; gr < 3; ++gr)
       if ((armed >> gr) & 1u) pair_drain(bars + 8 * (kBKsFull + gr), ((next_par >> gr) & 1u) ^ 1u, wd.limit_ns);
     if (q_armed > 0) pair_drain(bars + 8 * kBQFull, (q_armed - 1) & 1, wd.limit_ns);
   }
@@ -299,9 +358,9 @@ drain:
 }
 
 // ---------------------------------------------------------------------------
-// warp 2 (after the TMEM allocation): the value operand — for both pages of
-// each tile, the two 128-dv blocks this CTA supplies (chunks 4m + 2 rank and
-// 4m + 2 rank + 1 for m = 0, 1), into slots 4t + s
+// warp 2 (dense, after the TMEM allocation): the value operand — for both
+// pages of each tile, the two 128-dv blocks this CTA supplies (chunks
+// 4m + 2 rank and 4m + 2 rank + 1 for m = 0, 1), into slots 4t + 2m, 4t + 2m + 1
 // ---------------------------------------------------------------------------
 __device__ void pair_producer_kv(const CUtensorMap* tm_kv, const DecodeParams& p, const PairSeg& sg, int rank,
                                  uint32_t smem, uint32_t bars, uint32_t bars_even, const Watchdog& wd) {
@@ -338,7 +397,6 @@ __device__ void pair_producer_kv(const CUtensorMap* tm_kv, const DecodeParams& p
       __syncwarp();
       armed = true;
       if (lane < 4) {
-        // page t, value block m: chunks 4m + 2 rank and 4m + 2 rank + 1 into slots 4t + 2m, 4t + 2m + 1
         const int t = lane >> 1, m = lane & 1;
         const int pg = t ? pg1 : pg0;
         const int row = pg >= 0 ? pg * kPageSize : oob_row;
@@ -357,9 +415,274 @@ drain:
 }
 
 // ---------------------------------------------------------------------------
+// warps 12-15 (sparse): row lookups, row gathers and dequantisation
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t pair_dequant2(uint32_t codes16, float scale) {
+  const uint32_t h2 = e4m3x2_to_f16x2(static_cast<uint16_t>(codes16));
+  const float lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu)));
+  const float hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+  return pack_bf16x2(lo * scale, hi * scale);
+}
+
+// Dequantise one token's 128 codes of a value block in place: the codes sit
+// as a plain 128-byte row at row `tok` of chunk `hi_chunk`; values 0..63 go
+// to row `tok` of `lo_chunk`, 64..127 to row `tok` of `hi_chunk`, in the
+// 128-byte swizzle (16-byte unit u of row t at u ^ (t & 7)).  An invalid
+// token's values become zeros.
+__device__ __forceinline__ void dequant_block_row(uint32_t lo, uint32_t hi, uint32_t tsw, float scale, bool ok) {
+  uint4 raw[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) raw[k] = ld_shared_v4(hi + ((k ^ tsw) << 4));
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t u = k ^ tsw;  // raw unit: codes 16u .. 16u + 15 of the block
+    const uint32_t dst = (u & 4) ? hi : lo;
+    const uint32_t k0 = (2 * (u & 3)) ^ tsw, k1 = (2 * (u & 3) + 1) ^ tsw;
+    uint4 v = raw[k];
+    if (!ok) v = make_uint4(0, 0, 0, 0);
+    st_shared_v4(dst + (k0 << 4), pair_dequant2(v.x & 0xffffu, scale), pair_dequant2(v.x >> 16, scale),
+                 pair_dequant2(v.y & 0xffffu, scale), pair_dequant2(v.y >> 16, scale));
+    st_shared_v4(dst + (k1 << 4), pair_dequant2(v.z & 0xffffu, scale), pair_dequant2(v.z >> 16, scale),
+                 pair_dequant2(v.w & 0xffffu, scale), pair_dequant2(v.w >> 16, scale));
+  }
+}
+
+// Permute one 128-byte row copied in plain order into the 128-byte swizzle
+// in place; an invalid token's row becomes zeros.
+__device__ __forceinline__ void swizzle_row(uint32_t row_addr, uint32_t tsw, bool ok) {
+  uint4 raw[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) raw[k] = ld_shared_v4(row_addr + ((k ^ tsw) << 4));
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint4 v = ok ? raw[k] : make_uint4(0, 0, 0, 0);
+    st_shared_v4(row_addr + (k << 4), v.x, v.y, v.z, v.w);
+  }
+}
+
+__device__ void pair_gather(const CUtensorMap* tm_rows, const DecodeParams& p, const PairSeg& sg, int rank,
+                            uint32_t smem, uint32_t bars, uint32_t bars_even, uint32_t* flags, const Watchdog& wd) {
+  // 128 threads.  Thread tid takes token tok = tid % 64 of each half of the
+  // tile and hh = tid / 64: of its own tokens (index slots 64 rank + tok) it
+  // converts value blocks 2hh and 2hh + 1 (and the RoPE chunk when hh = 0);
+  // of its partner's tokens (slots 64 (1 - rank) + tok) value block
+  // 2hh + rank, one of the two this CTA supplies to the PV product.  Each
+  // warp gathers its 32 tokens' rows with TMA row gathers (four rows each).
+  // Per tile jt, in order: (A) convert own blocks and RoPE, write the tile's
+  // validity bits, report each item to the even CTA; (B) look up the rows of
+  // tile jt + 1; (C) once the PV MMAs of tile jt - 1 are done, gather the
+  // partner blocks of tile jt and copy the own blocks this CTA supplies into
+  // the value slots; (D) gather tile jt + 1's own blocks as the score MMAs of
+  // tile jt free their slots; (E) convert the partner blocks and report the
+  // tile's value slots.
+  const int tid = threadIdx.x - 32 * kPairGatherWarp0;
+  const int lane = tid & 31;
+  const int hh = tid >> 6;
+  const int tok = tid & 63;
+  const int wtok = tok & ~31;  // first token of this warp's 32
+  const uint32_t tsw = tok & 7;
+  const uint64_t pol = l2_policy_evict_normal();
+  const int row_bytes = p.kv_scales ? 640 : kFp8RowBytes;
+  const int tp = 1 - rank;     // the partner's half of the tile
+  const int bp = 2 * hh + rank;  // this thread's partner value block (one this CTA supplies)
+  uint32_t armed = 0, next_par = 0;  // raw barriers armed by this warp (bit per item), parity of their next phase
+
+  struct It {
+    int prob, j, te;
+    bool valid;
+  };
+  auto first_from = [&](int prob) -> It {
+    for (; prob <= sg.last(); ++prob) {
+      int tb, te;
+      sg.range(prob, tb, te);
+      if (tb < te) return It{prob, tb, te, true};
+    }
+    return It{0, 0, 0, false};
+  };
+  auto next_of = [&](const It& it) -> It {
+    if (it.j + 1 < it.te) return It{it.prob, it.j + 1, it.te, true};
+    return first_from(it.prob + 1);
+  };
+  struct Look {
+    int row_o, row_p;
+    bool ok_o, ok_p;
+    uint2 sc_o;   // scales of own blocks 2hh, 2hh + 1
+    float sc_p;   // scale of partner block bp
+  };
+  // row of the token in index slot k of problem prob (0 for an invalid one)
+  auto lookup_row = [&](int prob, int k, bool flag, int& row) -> bool {
+    const int b = prob / p.s_q;
+    const int L = sg.seqlens[b];
+    int tk = p.topk;
+    if (p.topk_lengths) {
+      const int len = p.topk_lengths[prob];
+      tk = len < 0 ? 0 : (len < p.topk ? len : p.topk);
+    }
+    const int t = k < tk ? p.indices[static_cast<int64_t>(prob) * p.topk + k] : -1;
+    bool ok = t >= 0 && t < L;
+    const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
+    const int page = (ok && (t >> 6) < p.block_table_stride) ? bt[t >> 6] : -1;
+    if (ok && (page < 0 || page >= p.num_pages)) {
+      ok = false;
+      if (flag) atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
+    }
+    row = ok ? page * kPageSize + (t & 63) : 0;
+    return ok;
+  };
+  auto lookup = [&](const It& it) -> Look {
+    Look lk;
+    lk.ok_o = lookup_row(it.prob, it.j * kPairTile + 64 * rank + tok, hh == 0, lk.row_o);
+    lk.ok_p = lookup_row(it.prob, it.j * kPairTile + 64 * tp + tok, false, lk.row_p);
+    if (p.kv_scales) {
+      const float s = lk.ok_o ? __ldg(p.kv_scales + lk.row_o) : 0.f;
+      lk.sc_o = make_uint2(__float_as_uint(s), __float_as_uint(s));
+      lk.sc_p = lk.ok_p ? __ldg(p.kv_scales + lk.row_p) : 0.f;
+    } else {
+      lk.sc_o = lk.ok_o ? __ldg(reinterpret_cast<const uint2*>(p.kv_fp8 + static_cast<int64_t>(lk.row_o) * row_bytes +
+                                                              kFp8ScaleOffset + 8 * hh))
+                        : make_uint2(0, 0);
+      lk.sc_p = lk.ok_p ? __ldg(reinterpret_cast<const float*>(p.kv_fp8 + static_cast<int64_t>(lk.row_p) * row_bytes +
+                                                               kFp8ScaleOffset + 4 * bp))
+                        : 0.f;
+    }
+    return lk;
+  };
+  // four consecutive rows of this warp's tokens for the gathers of lane gl
+  auto rows4 = [&](int row, int gl, int& r0, int& r1, int& r2, int& r3) {
+    r0 = __shfl_sync(0xffffffffu, row, 4 * gl);
+    r1 = __shfl_sync(0xffffffffu, row, 4 * gl + 1);
+    r2 = __shfl_sync(0xffffffffu, row, 4 * gl + 2);
+    r3 = __shfl_sync(0xffffffffu, row, 4 * gl + 3);
+  };
+  auto arm = [&](int item, uint32_t bytes) {
+    if (lane == 0) mbar_arrive_expect_tx_u32(bars + 8 * (kBRaw + item), bytes);
+    armed |= 1u << item;
+    next_par ^= 1u << item;
+    __syncwarp();
+  };
+  // (D) own value blocks and RoPE of tile jt into the score-operand slots
+  auto issue_own = [&](int jt, const Look& lk) -> bool {
+    const int gl = lane & 7;
+    int r0, r1, r2, r3;
+    rows4(lk.row_o, gl, r0, r1, r2, r3);
+#pragma unroll 1
+    for (int i = 0; i < 2; ++i) {
+      const int blk = 2 * hh + i;
+      if (jt > 0 && !pair_wait(bars + 8 * (kBKsEmpty + blk), (jt - 1) & 1, wd)) return false;
+      // the slot's previous contents were read by this thread (value copies) before
+      fence_proxy_async_smem();
+      arm(blk, 32 * 128);
+      if (lane < 8)
+        gather4(smem + kPairKsOff + (2 * blk + 1) * kPairChunk + (wtok + 4 * gl) * 128, tm_rows,
+                bars + 8 * (kBRaw + blk), 128 * blk, r0, r1, r2, r3, pol);
+      __syncwarp();
+    }
+    if (hh == 0) {
+      if (jt > 0 && !pair_wait(bars + 8 * (kBKsEmpty + 4), (jt - 1) & 1, wd)) return false;
+      arm(4, 32 * 128);
+      if (lane < 8)
+        gather4(smem + kPairKsOff + 8 * kPairChunk + (wtok + 4 * gl) * 128, tm_rows, bars + 8 * (kBRaw + 4),
+                p.fp8_rope_off, r0, r1, r2, r3, pol);
+      __syncwarp();
+    }
+    return true;
+  };
+
+  It cur = first_from(sg.p0);
+  Look lk_c{}, lk_n{};
+  int jt = 0;
+  if (cur.valid) {
+    lk_c = lookup(cur);
+    if (!issue_own(0, lk_c)) goto drain;
+  }
+  for (; cur.valid; ++jt) {
+    const uint32_t par = static_cast<uint32_t>(jt) & 1u;
+    // (A) validity bits of the tile (warps 0 and 1: own and partner tokens of
+    // their 32), then the own blocks and the RoPE chunk
+    {
+      const uint32_t vo = __ballot_sync(0xffffffffu, lk_c.ok_o);
+      const uint32_t vp = __ballot_sync(0xffffffffu, lk_c.ok_p);
+      if (hh == 0 && lane == 0) {
+        flags[4 * (jt & 3) + 2 * rank + (wtok >> 5)] = vo;
+        flags[4 * (jt & 3) + 2 * tp + (wtok >> 5)] = vp;
+        mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + 8 * kBFlags)));
+      }
+      __syncwarp();
+    }
+#pragma unroll 1
+    for (int i = 0; i < 2; ++i) {
+      const int blk = 2 * hh + i;
+      if (!pair_wait(bars + 8 * (kBRaw + blk), par, wd)) goto drain;
+      dequant_block_row(smem + kPairKsOff + 2 * blk * kPairChunk + tok * 128,
+                        smem + kPairKsOff + (2 * blk + 1) * kPairChunk + tok * 128, tsw,
+                        __uint_as_float(i == 0 ? lk_c.sc_o.x : lk_c.sc_o.y), lk_c.ok_o);
+      fence_proxy_async_smem();
+      warp_arrive_even(rank, bars + 8 * (kBKsFull + blk), bars_even + 8 * (kBKsFull + blk));
+    }
+    if (hh == 0) {
+      if (!pair_wait(bars + 8 * (kBRaw + 4), par, wd)) goto drain;
+      swizzle_row(smem + kPairKsOff + 8 * kPairChunk + tok * 128, tsw, lk_c.ok_o);
+      fence_proxy_async_smem();
+      warp_arrive_even(rank, bars + 8 * (kBKsFull + 4), bars_even + 8 * (kBKsFull + 4));
+    }
+    if (lane == 0 && hh == 0 && (tid >> 5) == 0) PAIR_TR(rank, 3, jt);
+    // (B) the rows of the next tile
+    const It nxt = next_of(cur);
+    if (nxt.valid) lk_n = lookup(nxt);
+    // (C) the partner blocks of this tile, and the own blocks this CTA
+    // supplies (block bp of its own tokens: converted above by this thread)
+    if (jt > 0 && !pair_wait(bars + 8 * kBKvEmpty, (jt - 1) & 1, wd)) goto drain;
+    {
+      const int gl = lane & 7;
+      int r0, r1, r2, r3;
+      rows4(lk_c.row_p, gl, r0, r1, r2, r3);
+      arm(5 + hh, 32 * 128);
+      if (lane < 8)
+        gather4(smem + kPairKvOff + (4 * tp + 2 * hh + 1) * kPairChunk + (wtok + 4 * gl) * 128, tm_rows,
+                bars + 8 * (kBRaw + 5 + hh), 128 * bp, r0, r1, r2, r3, pol);
+      __syncwarp();
+      // own block bp = 2hh + rank sits in score slots 2bp, 2bp + 1; its copy
+      // goes to value slots 4 rank + 2hh, 4 rank + 2hh + 1 (same row layout)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const uint32_t src = smem + kPairKsOff + (2 * bp + e) * kPairChunk + tok * 128;
+        const uint32_t dst = smem + kPairKvOff + (4 * rank + 2 * hh + e) * kPairChunk + tok * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 v = ld_shared_v4(src + 16 * u);
+          st_shared_v4(dst + 16 * u, v.x, v.y, v.z, v.w);
+        }
+      }
+    }
+    // (D) the next tile's own blocks, as the score MMAs free their slots
+    if (nxt.valid && !issue_own(jt + 1, lk_n)) goto drain;
+    // (E) the partner blocks, dequantised in place
+    if (!pair_wait(bars + 8 * (kBRaw + 5 + hh), par, wd)) goto drain;
+    dequant_block_row(smem + kPairKvOff + (4 * tp + 2 * hh) * kPairChunk + tok * 128,
+                      smem + kPairKvOff + (4 * tp + 2 * hh + 1) * kPairChunk + tok * 128, tsw, lk_c.sc_p, lk_c.ok_p);
+    fence_proxy_async_smem();
+    warp_arrive_even(rank, bars + 8 * kBKvFull, bars_even + 8 * kBKvFull);
+    if (lane == 0 && tid == 0) PAIR_TR(rank, 4, jt);
+    cur = nxt;
+    lk_c = lk_n;
+  }
+  return;
+drain:
+  // abort: wait (bounded) for this warp's row gathers still in flight
+  if (lane == 0) {
+#pragma unroll 1
+    for (int k = 0; k < 7; ++k)
+      if ((armed >> k) & 1u) pair_drain(bars + 8 * (kBRaw + k), ((next_par >> k) & 1u) ^ 1u, wd.limit_ns);
+  }
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
 // warp 1 of the even CTA: score MMAs, S = Q K^T over the pair
 // ---------------------------------------------------------------------------
+template <bool SPARSE>
 __device__ void pair_s_issuer(const PairSeg& sg, uint32_t tmem, uint32_t smem, uint32_t bars, const Watchdog& wd) {
+  using C = PairCfg<SPARSE>;
   constexpr uint32_t kIdS = idesc_bf16_f32(128, kPairTile, 0, 0);
   constexpr uint64_t kHiK = smem_desc_hi(16, 1024);
   const int lane = threadIdx.x & 31;
@@ -376,14 +699,15 @@ __device__ void pair_s_issuer(const PairSeg& sg, uint32_t tmem, uint32_t smem, u
       tc_fence_after();
       const uint32_t d = tmem + kPairSCol + sb * (kPairTile / 2);
 #pragma unroll 1
-      for (int gr = 0; gr < kKsGroups; ++gr) {
-        if (!pair_wait(bars + 8 * (kBKsFull + gr), jt & 1, wd)) goto done;
+      for (int it = 0; it < C::kItems; ++it) {
+        if (!pair_wait(bars + 8 * (kBKsFull + it), jt & 1, wd)) goto done;
         tc_fence_after();
-        if (lane == 0 && gr == 0) PAIR_TR(0, 3, jt);
-        if (lane == 0 && gr == kKsGroups - 1) PAIR_TR(0, 4, jt);
-#pragma unroll
-        for (int kc = 0; kc < 3; ++kc) {
-          const int k = 3 * gr + kc;
+        if (lane == 0 && it == 0) PAIR_TR(0, 5, jt);
+        if (lane == 0 && it == C::kItems - 1) PAIR_TR(0, 6, jt);
+        const int k0 = C::item_chunk0(it), nk = C::item_chunks(it);
+#pragma unroll 1
+        for (int kc = 0; kc < nk; ++kc) {
+          const int k = k0 + kc;
           const uint64_t a0 = kHiK | ((smem + kPairQOff + k * kPairChunk) >> 4);
           const uint64_t b0 = kHiK | ((smem + kPairKsOff + k * kPairChunk) >> 4);
 #pragma unroll
@@ -392,7 +716,7 @@ __device__ void pair_s_issuer(const PairSeg& sg, uint32_t tmem, uint32_t smem, u
             __syncwarp();
           }
         }
-        if (elect_one()) umma2_commit_both(bars + 8 * (kBKsEmpty + gr));
+        if (elect_one()) umma2_commit_both(bars + 8 * (kBKsEmpty + it));
         __syncwarp();
       }
       if (elect_one()) {
@@ -465,13 +789,14 @@ done:
 // ---------------------------------------------------------------------------
 // warps 4-11: online softmax and epilogue
 // ---------------------------------------------------------------------------
+template <bool SPARSE>
 __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, int rank, int split0, uint32_t tmem,
                              uint32_t smem, uint32_t bars, uint32_t bars_even, float* m_s, float* red,
-                             const Watchdog& wd) {
+                             const volatile uint32_t* flags, const Watchdog& wd) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int q = warp & 3;           // TMEM lane quarter
-  const int h = q >> 1;             // half of the tile (page) this thread's columns cover
+  const int h = q >> 1;             // half of the tile this thread's columns cover
   const int w = (warp - 4) >> 2;    // warpgroup: tokens [32w, 32w + 32) of the half
   const int r = (q & 1) * 32 + lane;  // row of this CTA (0..63)
   const int hw = 2 * h + w;         // which of the row's four partial statistics
@@ -479,16 +804,7 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
   const int row0 = g * 2 * kPairRows + rank * kPairRows;
   const int grow = row0 + r;        // row within the problem
   const float sc = p.scale_log2;
-  // arrivals of this warp on the even CTA's barriers (remote from the odd CTA)
-  auto arrive_even = [&](int bar) {
-    __syncwarp();
-    if (lane == 0) {
-      if (rank == 0)
-        mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + 8 * bar)));
-      else
-        mbar_arrive_cluster(bars_even + 8 * bar);
-    }
-  };
+  auto arrive_even = [&](int bar) { warp_arrive_even(rank, bars + 8 * bar, bars_even + 8 * bar); };
   auto all_ok = [&](bool ok) { return named_bar_and(kPairSmBar, 256, ok); };
   auto wait_all = [&](int bar, uint32_t parity) { return all_ok(mbar_wait(
       reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + 8 * bar)), parity, wd)); };
@@ -502,30 +818,38 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
     int tb, te;
     sg.range(prob, tb, te);
     if (tb >= te) continue;
-    const int b = prob;
+    const int b = SPARSE ? prob / p.s_q : prob;
     const int L = sg.seqlens[b];
-    // last visible key of this row (bottom-right causal alignment)
-    const int lim = p.is_causal ? L - p.s_q + grow / p.h_q : L - 1;
+    // last visible key of this row (dense: bottom-right causal alignment)
+    const int lim = (!SPARSE && p.is_causal) ? L - p.s_q + grow / p.h_q : L - 1;
     float l_part = 0.f;
     for (int j = tb; j < te; ++j, ++jt) {
       const int sb = jt & 1;
       if (!wait_all(kBSFull + sb, (jt >> 1) & 1)) return;
       tc_fence_after();
       const bool tr = (warp == 4 && lane == 0);
-      if (tr) PAIR_TR(rank, 5, jt);
+      if (tr) PAIR_TR(rank, 7, jt);
       float x[32];
       tmem_ld_x32(tmem + lane_base + kPairSCol + sb * (kPairTile / 2) + 32 * w, x);
       tmem_ld_wait();
       tc_fence_before();
       arrive_even(kBSEmpty + sb);
       // mask and scale (log2 units); tokens of this thread: h * 64 + 32 w + i
-      const bool page_ok = tile_page(p, b, L, j, h, false) >= 0;
+      bool page_ok = true;
+      uint32_t vbits = 0xffffffffu;
+      if (SPARSE) {
+        // the gather warps of this CTA wrote the tile's validity bits
+        if (!wait_all(kBFlags, jt & 1)) return;
+        vbits = flags[4 * (jt & 3) + 2 * h + w];
+      } else {
+        page_ok = tile_page(p, b, L, j, h, false) >= 0;
+      }
       const int pos0 = j * kPairTile + h * 64 + 32 * w;
       float mx = kPairNegInf;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const int pos = pos0 + i;
-        x[i] = (page_ok && pos <= lim) ? x[i] * sc : kPairNegInf;
+        const bool ok = SPARSE ? ((vbits >> i) & 1u) != 0 : (page_ok && pos0 + i <= lim);
+        x[i] = ok ? x[i] * sc : kPairNegInf;
         mx = fmaxf(mx, x[i]);
       }
       red[hw * 64 + r] = mx;
@@ -536,20 +860,18 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
       const float m_new = raise ? fmaxf(m_old, rmax) : m_old;
       // any row of either warpgroup raised its max (after the first tile): O needs a rescale
       const bool any = named_bar_or(kPairSmBar, 256, raise && j != tb);
-      if (tr) PAIR_TR(rank, 6, jt);
       if (raise && hw == 0) m_s[r] = m_new;
       const float alpha = (m_old == kPairNegInf) ? 0.f : fast_exp2(m_old - m_new);
       if (raise) l_part *= alpha;
-      float pr[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        pr[i] = (x[i] == kPairNegInf) ? 0.f : fast_exp2(x[i] - m_new);
-        l_part += pr[i];
+        x[i] = (x[i] == kPairNegInf) ? 0.f : fast_exp2(x[i] - m_new);
+        l_part += x[i];
       }
       // P and O of the previous tile are free once its PV MMAs are done
       if (jt > 0 && !wait_all(kBPEmpty, (jt - 1) & 1)) return;
       tc_fence_after();
-      if (tr) PAIR_TR(rank, 7, jt);
+      if (tr) PAIR_TR(rank, 8, jt);
       if (any) {
         // rescale this thread's row of O (its lane's 128 columns of block w) by alpha
         const float a = raise ? alpha : 1.0f;
@@ -571,18 +893,18 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int unit = 4 * w + u;
-          st_shared_v4(prow + ((unit ^ (r & 7)) << 4), pack_bf16x2(pr[8 * u], pr[8 * u + 1]),
-                       pack_bf16x2(pr[8 * u + 2], pr[8 * u + 3]), pack_bf16x2(pr[8 * u + 4], pr[8 * u + 5]),
-                       pack_bf16x2(pr[8 * u + 6], pr[8 * u + 7]));
+          st_shared_v4(prow + ((unit ^ (r & 7)) << 4), pack_bf16x2(x[8 * u], x[8 * u + 1]),
+                       pack_bf16x2(x[8 * u + 2], x[8 * u + 3]), pack_bf16x2(x[8 * u + 4], x[8 * u + 5]),
+                       pack_bf16x2(x[8 * u + 6], x[8 * u + 7]));
         }
       }
-      // tail tile: this CTA's value slots are loaded (on its own barrier); the
-      // rows of tokens past the length are zeroed (their P is 0, but a slot
-      // may hold NaN, and 0 * NaN would poison O).  Unusable pages were read
-      // as zeros.
-      if (tail_tile(L, j)) {
+      // dense tail tile: this CTA's value slots are loaded (on its own
+      // barrier); the rows of tokens past the length are zeroed (their P is
+      // 0, but a slot may hold NaN, and 0 * NaN would poison O).  Unusable
+      // pages were read as zeros.  (Sparse: invalid tokens were written as
+      // zeros by the gather warps.)
+      if (!SPARSE && tail_tile(L, j)) {
         if (!wait_all(kBKvFull, jt & 1)) return;
-        if (tr) PAIR_TR(rank, 8, jt);
         const int tl = (q & 1) * 32 + lane;  // token of page h zeroed by this thread
         if (page_ok && j * kPairTile + h * 64 + tl >= L) {
 #pragma unroll
@@ -662,16 +984,19 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
 // ---------------------------------------------------------------------------
 // kernel
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kPairThreads, 1)
+template <bool SPARSE>
+__global__ void __launch_bounds__(PairCfg<SPARSE>::kThreads, 1)
     mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_ks,
                            const __grid_constant__ CUtensorMap tm_kv, const DecodeParams p) {
+  using C = PairCfg<SPARSE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t smem = smem_u32(base);
   const uint32_t bars = smem + kPairAuxOff;
-  float* m_s = reinterpret_cast<float*>(base + kPairAuxOff + kPairBarBytes);
-  float* red = m_s + 64;
-  int* ints = reinterpret_cast<int*>(red + 256);
+  float* m_s = reinterpret_cast<float*>(base + kPairAuxOff + kPairMOff);
+  float* red = reinterpret_cast<float*>(base + kPairAuxOff + kPairRedOff);
+  int* ints = reinterpret_cast<int*>(base + kPairAuxOff + kPairIntOff);
+  uint32_t* flags = reinterpret_cast<uint32_t*>(base + kPairAuxOff + kPairFlagOff);
   volatile int* abort_flag = ints;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ints + 1);
 
@@ -686,11 +1011,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     uint64_t* bp = reinterpret_cast<uint64_t*>(base + kPairAuxOff);
     mbar_init(bp + kBQFull, 1);
     mbar_init(bp + kBQEmpty, 1);
-    for (int gr = 0; gr < kKsGroups; ++gr) {
-      mbar_init(bp + kBKsFull + gr, 1);
-      mbar_init(bp + kBKsEmpty + gr, 1);
+    for (int it = 0; it < C::kItems; ++it) {
+      // dense: the even producer's arrival plus both CTAs' bytes; sparse: the
+      // two gather warps converting the item in each CTA
+      mbar_init(bp + kBKsFull + it, SPARSE ? 4 : 1);
+      mbar_init(bp + kBKsEmpty + it, 1);
     }
-    mbar_init(bp + kBKvFull, 1);
+    mbar_init(bp + kBKvFull, SPARSE ? 8 : 1);  // sparse: four gather warps in each CTA
     mbar_init(bp + kBKvEmpty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bp + kBSFull + i, 1);
@@ -701,13 +1028,18 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     mbar_init(bp + kBOFull, 1);
     mbar_init(bp + kBOEmpty, 16);
     mbar_init(bp + kBMmaDone, 2);  // one commit per MMA-issuing warp
+    if (SPARSE) {
+      for (int k = 0; k < 7; ++k) mbar_init(bp + kBRaw + k, 2);  // the two warps gathering the item
+      mbar_init(bp + kBFlags, 2);                                 // the two gather warps writing the bits
+    }
+    for (int k = 0; k < 16; ++k) flags[k] = 0;
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_ks);
-    tma_prefetch_desc(&tm_kv);
+    if (!SPARSE) tma_prefetch_desc(&tm_kv);
   }
   if (warp == 2) {
     tmem_alloc_pair(tmem_slot, kPairTmemCols);
@@ -738,6 +1070,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   }
   sg.np = p.num_problems;
   sg.s_q = p.s_q;
+  sg.topk = SPARSE ? p.topk : 0;
   sg.seqlens = p.cache_seqlens;
   if (sg.p0 < 0 || sg.p0 > sg.np || sg.p1 < sg.p0 || sg.p1 > sg.np || sg.t0 < 0 || sg.t1 < 0) {
     if (threadIdx.x == 0) atomicOr(p.status, MLA_DEVICE_BAD_SCHEDULE);
@@ -758,19 +1091,22 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   }
 #endif
   if (warp < 4) {
-    regs_to<kPairRegsCtl, kPairLaunchRegs>();
+    regs_to<C::kRegsCtl, C::kLaunchRegs>();
     if (warp == 0) {
-      pair_producer_ks(&tm_q, &tm_ks, p, sg, g, rank, smem, bars, bars_even, wd);
+      pair_producer_ks<SPARSE>(&tm_q, &tm_ks, p, sg, g, rank, smem, bars, bars_even, wd);
     } else if (warp == 1) {
-      if (rank == 0) pair_s_issuer(sg, tmem, smem, bars, wd);
+      if (rank == 0) pair_s_issuer<SPARSE>(sg, tmem, smem, bars, wd);
     } else if (warp == 2) {
-      pair_producer_kv(&tm_kv, p, sg, rank, smem, bars, bars_even, wd);
+      if (!SPARSE) pair_producer_kv(&tm_kv, p, sg, rank, smem, bars, bars_even, wd);
     } else if (rank == 0) {
       pair_pv_issuer(sg, tmem, smem, bars, wd);
     }
-  } else {
-    regs_to<kPairRegsSm, kPairLaunchRegs>();
-    pair_softmax(p, sg, g, rank, split0, tmem, smem, bars, bars_even, m_s, red, wd);
+  } else if (warp < kPairGatherWarp0) {
+    regs_to<C::kRegsSm, C::kLaunchRegs>();
+    pair_softmax<SPARSE>(p, sg, g, rank, split0, tmem, smem, bars, bars_even, m_s, red, flags, wd);
+  } else if (SPARSE) {
+    regs_to<C::kRegsGather, C::kLaunchRegs>();
+    pair_gather(&tm_ks, p, sg, rank, smem, bars, bars_even, flags, wd);
   }
 
   tc_fence_before();
@@ -794,14 +1130,42 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   }
 }
 
+template <bool SPARSE>
+cudaError_t launch_pair(const CUtensorMap& tm_q, const CUtensorMap& tm_ks, const CUtensorMap& tm_kv,
+                        const DecodeParams& p, cudaStream_t stream) {
+  using C = PairCfg<SPARSE>;
+  auto kern = mla_decode_pair_kernel<SPARSE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != static_cast<int>(C::kLaunchRegs)) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * p.num_parts * p.row_groups);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = kPairSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, tm_q, tm_ks, tm_kv, p);
+}
+
 }  // namespace
 
 int pair_cluster_capacity() {
-  auto kern = mla_decode_pair_kernel;
+  auto kern = mla_decode_pair_kernel<true>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(kPairThreads);
+  cfg.blockDim = dim3(PairCfg<true>::kThreads);
   cfg.dynamicSmemBytes = kPairSmemBytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -816,29 +1180,8 @@ int pair_cluster_capacity() {
 }
 
 cudaError_t launch_decode_pair(const CUtensorMap& tm_q, const CUtensorMap& tm_ks, const CUtensorMap& tm_kv,
-                               const DecodeParams& p, cudaStream_t stream) {
-  auto kern = mla_decode_pair_kernel;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
-  if (e != cudaSuccess) return e;
-  cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, kern);
-  if (e != cudaSuccess) return e;
-  if (fa.numRegs != static_cast<int>(kPairLaunchRegs)) return cudaErrorInvalidConfiguration;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * p.num_parts * p.row_groups);
-  cfg.blockDim = dim3(kPairThreads);
-  cfg.dynamicSmemBytes = kPairSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, tm_q, tm_ks, tm_kv, p);
+                               const DecodeParams& p, bool sparse, cudaStream_t stream) {
+  return sparse ? launch_pair<true>(tm_q, tm_ks, tm_kv, p, stream) : launch_pair<false>(tm_q, tm_ks, tm_kv, p, stream);
 }
 
 }  // namespace mla

@@ -134,10 +134,12 @@ cudaError_t launch_decode(const CUtensorMap& tm_q, const CUtensorMap& tm_kv, con
 // CTA pairs the pair decode kernel can keep resident at once on the current
 // device (0 if the query fails)
 int pair_cluster_capacity();
-// CTA-pair decode (dense over the bf16 cache, problems of more than 64 rows)
-// tm_q, tm_ks, tm_kv: chunk-major maps with boxes of 9 chunks (Q), 3 and 2 chunks (cache)
+// CTA-pair decode for problems of more than 64 rows: dense over the bf16 cache
+// (tm_q, tm_ks, tm_kv: chunk-major maps with boxes of 9 chunks (Q), 3 and 2
+// chunks (cache)) or sparse over the FP8 cache (tm_q as before, tm_ks: the
+// FP8 rows as 128-byte boxes of one row for row gathers, tm_kv unused)
 cudaError_t launch_decode_pair(const CUtensorMap& tm_q, const CUtensorMap& tm_ks, const CUtensorMap& tm_kv,
-                               const DecodeParams& p, cudaStream_t stream);
+                               const DecodeParams& p, bool sparse, cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream, bool pdl);
 size_t decode_smem_bytes(int rpc, int mode);
 cudaError_t launch_fp8_cache_store(const uint16_t* x, int num_tokens, const int32_t* row_offsets,

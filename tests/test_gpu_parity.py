@@ -146,6 +146,70 @@ def test_pair_rescale_path():
           parts=1)
 
 
+@pytest.mark.parametrize("h_q,topk", [(128, 64), (128, 127), (128, 129), (128, 640), (96, 200), (256, 300)])
+def test_pair_sparse_shapes(h_q, topk):
+    """Sparse FP8 decode on CTA pairs: 128-slot tiles (a partial last tile, a single one), ghost
+    rows, two pairs per query token."""
+    check(W.custom(name=f"ps{h_q}_{topk}", batch=2, h_q=h_q, s_q=2, mode="sparse", seqlens=(3000, 700),
+                   topk=topk), 1900 + h_q + topk)
+
+
+def test_pair_sparse_duplicates_invalid_and_bad_pages():
+    w = W.custom(name="psdup", batch=2, h_q=128, s_q=2, mode="sparse", seqlens=(300, 900), topk=256)
+    inp = W.make_inputs(w, seed=23)
+    idx = inp.indices.clone()
+    idx[0, 0, :40] = 7           # one id forty times
+    idx[0, 1, 70] = 300          # == seqlen: skipped
+    idx[1, 0, 130] = 10 ** 7     # far out of range: skipped
+    idx[1, 1, :] = -1            # empty key set
+    inp.indices = idx
+    out, lse, flags = run_cuda(inp)
+    ref_out, ref_lse = run_oracle(inp)
+    assert flags == 0
+    compare(out, lse, ref_out, ref_lse, "psdup")
+    assert np.all(out[1, 1] == 0) and np.all(np.isneginf(lse[1, 1]))
+    # a page outside the pool: flagged, its tokens count as invalid ids
+    bt = inp.block_table.clone()
+    bt[1, 2] = inp.kvcache.shape[0] + 3
+    inp.block_table = bt
+    out, lse, flags = run_cuda(inp)
+    assert flags & mla.DEVICE_BAD_PAGE
+    idx2 = inp.indices.clone()
+    e1 = idx2[1]
+    e1[(e1 >= 128) & (e1 < 192)] = -1
+    inp.indices = idx2
+    ref_out, ref_lse = run_oracle(inp)
+    compare(out, lse, ref_out, ref_lse, "psbad")
+
+
+@pytest.mark.parametrize("parts", [1, 5, 300])
+def test_pair_sparse_forced_splits(parts):
+    w = W.custom(name=f"psp{parts}", batch=3, h_q=128, s_q=2, mode="sparse", seqlens=(5000, 3000, 700), topk=640)
+    check(w, 2000 + parts, parts=parts)
+
+
+def test_pair_sparse_token_scales_and_ragged_topk():
+    check(W.custom(name="pstok", batch=3, h_q=128, s_q=1, mode="sparse", seqlens=(2000, 300, 5000), topk=384,
+                   fp8_scales="token"), 2101)
+    w = W.custom(name="psrag", batch=3, h_q=128, s_q=2, mode="sparse", seqlens=(1500, 200, 3000), topk=320,
+                 ragged_topk=True)
+    inp = W.make_inputs(w, seed=2102)
+    tl = inp.topk_lengths.clone()
+    tl[0, 0] = 0
+    tl[1, 1] = 320
+    tl[2, 0] = 129
+    inp.topk_lengths = tl
+    out, lse, flags = run_cuda(inp)
+    assert flags == 0
+    ref_out, ref_lse = run_oracle(inp)
+    compare(out, lse, ref_out, ref_lse, w.name)
+
+
+def test_pair_sparse_rescale_path():
+    check(W.custom(name="psbig", batch=2, h_q=128, s_q=1, mode="sparse", seqlens=(4000, 2000), topk=1024,
+                   sm_scale=0.6), 2201, parts=1)
+
+
 # ---------------------------------------------------------------- sparse mode
 @pytest.mark.parametrize("h_q,topk", [(16, 64), (16, 200), (64, 128), (128, 300), (32, 1000), (48, 129)])
 def test_sparse_small(h_q, topk):

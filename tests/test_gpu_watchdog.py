@@ -14,13 +14,16 @@ from gpu_helpers import compare, env, metadata, overrides, run_cuda, run_oracle
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("mode", ["dense", "sparse", "pair"])
+@pytest.mark.parametrize("mode", ["dense", "sparse", "pair", "pair_sparse"])
 def test_watchdog_timeout_is_reported_and_context_survives(mode):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     mla.build()
     if mode == "dense":
         inp = W.make_inputs("tiny")
+    elif mode == "pair_sparse":
+        inp = W.make_inputs(W.custom(name="wd_psparse", batch=2, h_q=128, s_q=1, mode="sparse", seqlens=(900, 300),
+                                     topk=256), seed=7)
     elif mode == "pair":
         inp = W.make_inputs(W.custom(name="wd_pair", batch=2, h_q=128, s_q=1, mode="dense", seqlens=(400, 90)),
                             seed=6)
