@@ -83,9 +83,8 @@ mla_status device_info(uint32_t** status, int* sm_count, int* pair_capacity = nu
 // The CTA-pair decode kernel for problems of more than 64 rows, dense over
 // the bf16 cache or sparse over the FP8 cache (mla_decode_pair.cu).
 constexpr bool kPairDecode = true;
-// Sparse over the FP8 cache on CTA pairs (passes every parity test; slower
-// than the single-CTA kernel so far, so not selected yet).
-constexpr bool kPairSparse = false;
+// Sparse over the FP8 cache on CTA pairs.
+constexpr bool kPairSparse = true;
 
 // Test hooks (mla_test_hooks): a forced part count and a stalled softmax role.
 std::atomic<int> g_test_num_parts{0};
@@ -386,15 +385,13 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
   if (g.pair) {
     // chunk-major boxes: Q of a CTA in one copy; dense: a page's score operand
     // in three copies of three chunks, its value shares in copies of two
-    // chunks; sparse: FP8 rows for the row gathers
+    // chunks.  Sparse: the FP8 rows are copied by the gather warps with
+    // cp.async and the two cache maps go unused.
     st = encode_chunk_major_map(&tm_q, a->q, qrows, kNumChunks, "q");
     if (st == MLA_OK && g.mode == 0) st = encode_chunk_major_map(&tm_kv, a->kvcache, cache_rows, 3, "kvcache");
     if (st == MLA_OK && g.mode == 0) st = encode_chunk_major_map(&tm_kv2, a->kvcache, cache_rows, 2, "kvcache");
-    if (st == MLA_OK && g.mode == 1) {
-      st = encode_byte_rows_map(&tm_kv, a->kvcache, cache_rows, a->kv_scales ? 640 : kFp8RowBytes, 1);
-      tm_kv2 = tm_kv;
-    }
     if (st != MLA_OK) return st;
+    if (g.mode == 1) tm_kv = tm_kv2 = tm_q;
   } else {
     st = encode_rows_map(&tm_q, a->q, qrows, g.rpc, "q");
   }

@@ -36,9 +36,8 @@
 // shared-memory address in both CTAs while holding different dims (dv 0-127
 // and 256-383 for the even CTA, 128-255 and 384-511 for the odd one), so
 // those dims of all 128 tokens of a tile live in a separate set of slots:
-// for the CTA's own tokens copied (dense: loaded again, sparse: written a
-// second time by the dequantisation), for its partner's tokens loaded
-// (dense) or gathered and dequantised (sparse).
+// loaded (dense), or (sparse) bulk-copied from the dequantised score operand
+// of the CTA that owns the token, into its own slots or its partner's.
 //
 // Shared memory (1024-byte aligned, identical in both CTAs):
 //   Q    9 chunks [64 rows][64 dims] bf16, 128-byte swizzle         72 KB
@@ -54,7 +53,11 @@
 // (cta_group::2 TMA) complete on them directly; pages without tokens or with
 // an unusable block-table entry are read past the end of the cache, as
 // zeros.  Sparse: the gather warps of both CTAs arrive on the even CTA's
-// barriers once they have dequantised an item.  The MMA warps commit to the
+// barriers once they have dequantised an item, and each CTA's value-slot
+// copier once its slots of the tile are complete.  Sparse rows are copied with
+// 16-byte cp.async by all lanes of the gather warps rather than with TMA row
+// gathers: a warp issuing row gathers waits about 90 cycles per gather, which
+// at 40 gathers per warp and tile was longer than the tile's MMAs.  The MMA warps commit to the
 // barriers of both CTAs at once (multicast); the odd CTA's softmax warps
 // arrive remotely on the even CTA's barriers.  Every wait is bounded by the
 // watchdog; a CTA that gives up records MLA_DEVICE_TIMEOUT and unwinds, and
@@ -63,12 +66,13 @@
 // Roles:
 //   warp 0      Q (and, dense, the score operand) producer (TMA), both CTAs
 //   warp 1      score MMA issuer (even CTA)
-//   warp 2      TMEM allocation, then (dense) the value-operand producer
+//   warp 2      TMEM allocation, then the value-operand producer (dense: TMA
+//               loads; sparse: bulk copies from the dequantised score slots)
 //   warp 3      PV MMA issuer (even CTA)
 //   warps 4-11  softmax + epilogue: warp w reads TMEM lane quarter w % 4, so
 //               a thread owns one row and one half of the tile, and the two
 //               warpgroups split that half's 64 tokens
-//   warps 12-15 (sparse) row lookups, TMA row gathers, dequantisation
+//   warps 12-15 (sparse) row lookups, row copies, dequantisation, value-slot copies
 #include "mla_device.cuh"
 #include "mla_internal.h"
 
@@ -110,7 +114,7 @@ constexpr int kPairKsOff = 9 * kPairChunk;
 constexpr int kPairKvOff = 18 * kPairChunk;
 constexpr int kPairPOff = 26 * kPairChunk;
 constexpr int kPairAuxOff = 28 * kPairChunk;  // 229376
-constexpr int kPairBarBytes = 256;
+constexpr int kPairBarBytes = 320;
 // aux: barriers, m[64], red[4][64] (partial row maxima / sums), ints (abort
 // flag, TMEM base), token-validity bits of four tiles (sparse)
 constexpr int kPairMOff = kPairBarBytes;
@@ -161,9 +165,14 @@ enum PairBar {
   kBOFull = 20,   // the segment's last PV MMAs are done
   kBOEmpty = 21,  // (even) both CTAs' epilogues have read O
   kBMmaDone = 22, // (even) drain of the MMA issuers
-  kBRaw = 23,     // [7] (sparse) raw rows of an item landed in this CTA
-  kBFlags = 30,   // (sparse) the tile's token-validity bits of this CTA are written
-  kBCount = 31
+  kBRaw = 23,     // [5] (sparse) the codes of item i (block i, 4: RoPE) landed in this CTA
+  kBFlags = 28,   // [4] (sparse) the validity bits of tile jt (barrier jt % 4) are written by the
+                  // gather warps of both CTAs, which can run up to three tiles ahead of the softmax
+  kBKsDone = 32,  // [2] (sparse) block 1 - rank + 2m of the tile's score operand is dequantised
+  kBKsRead = 34,  // [2] (sparse) its copy to the partner's value slots has read it
+  kBKvIn = 36,    // (sparse) this CTA's value slots of the tile are complete: its own share
+                  // written by its gather warps, the partner's copies (transaction bytes)
+  kBCount = 37
 };
 static_assert(kBCount * 8 <= kPairBarBytes, "barrier area");
 
@@ -213,17 +222,6 @@ __device__ __forceinline__ void tma3_to_even(uint32_t dst, const void* map, uint
       : "memory");
 }
 
-// Row gather: four rows r0..r3 of a 2-D byte-row map (box 128 bytes x one
-// row) land back to back at dst; x is the byte column.
-__device__ __forceinline__ void gather4(uint32_t dst, const void* map, uint32_t bar, int x, int r0, int r1, int r2,
-                                        int r3, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "l"(policy)
-      : "memory");
-}
-
 // Tile j of a problem of L tokens holds a page that straddles the length:
 // its slots past the length may hold anything (e.g. NaN), so the value rows
 // of those tokens are zeroed after the copy lands, before the PV MMAs.
@@ -239,10 +237,11 @@ __device__ __forceinline__ void tma_prefetch3(const void* map, int c0, int c1, i
                : "memory");
 }
 
-// Warp-uniform bounded wait on a barrier of this CTA.
+// Warp-uniform bounded wait on a barrier of this CTA (acquire at cluster
+// scope: many phases are completed by the other CTA's arrivals).
 __device__ __forceinline__ bool pair_wait(uint32_t bar, uint32_t parity, const Watchdog& wd) {
   uint64_t t0 = 0;
-  while (__shfl_sync(0xffffffffu, mbar_test_wait_u32(bar, parity) ? 1 : 0, 0) == 0) {
+  while (__shfl_sync(0xffffffffu, mbar_test_wait_cluster_u32(bar, parity) ? 1 : 0, 0) == 0) {
     if (t0 == 0) {
       t0 = global_timer_ns();
     } else if (__shfl_sync(0xffffffffu, wd.aborted() ? 1 : 0, 0)) {
@@ -253,6 +252,22 @@ __device__ __forceinline__ bool pair_wait(uint32_t bar, uint32_t parity, const W
     }
   }
   return true;
+}
+
+// The same for one thread.
+__device__ __forceinline__ bool pair_wait_thread(uint32_t bar, uint32_t parity, const Watchdog& wd) {
+  if (mbar_test_wait_cluster_u32(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_test_wait_cluster_u32(bar, parity)) return true;
+    if (wd.aborted()) return false;
+    if (global_timer_ns() - t0 > wd.limit_ns) {
+      wd.trip(MLA_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
 }
 
 // Bounded wait that ignores the abort flag (drain of own asynchronous work).
@@ -447,233 +462,341 @@ __device__ __forceinline__ void dequant_block_row(uint32_t lo, uint32_t hi, uint
   }
 }
 
-// Permute one 128-byte row copied in plain order into the 128-byte swizzle
-// in place; an invalid token's row becomes zeros.
-__device__ __forceinline__ void swizzle_row(uint32_t row_addr, uint32_t tsw, bool ok) {
+// The same, also writing the values to a second place with the same row layout.
+__device__ __forceinline__ void dequant_block_row2(uint32_t lo, uint32_t hi, uint32_t lo2, uint32_t hi2, uint32_t tsw,
+                                                   float scale, bool ok) {
   uint4 raw[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) raw[k] = ld_shared_v4(row_addr + ((k ^ tsw) << 4));
+  for (int k = 0; k < 8; ++k) raw[k] = ld_shared_v4(hi + ((k ^ tsw) << 4));
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const uint4 v = ok ? raw[k] : make_uint4(0, 0, 0, 0);
-    st_shared_v4(row_addr + (k << 4), v.x, v.y, v.z, v.w);
+    const uint32_t u = k ^ tsw;
+    const uint32_t d1 = (u & 4) ? hi : lo, d2 = (u & 4) ? hi2 : lo2;
+    const uint32_t k0 = ((2 * (u & 3)) ^ tsw) << 4, k1 = ((2 * (u & 3) + 1) ^ tsw) << 4;
+    uint4 v = raw[k];
+    if (!ok) v = make_uint4(0, 0, 0, 0);
+    const uint32_t a0 = pair_dequant2(v.x & 0xffffu, scale), a1 = pair_dequant2(v.x >> 16, scale);
+    const uint32_t a2 = pair_dequant2(v.y & 0xffffu, scale), a3 = pair_dequant2(v.y >> 16, scale);
+    const uint32_t b0 = pair_dequant2(v.z & 0xffffu, scale), b1 = pair_dequant2(v.z >> 16, scale);
+    const uint32_t b2 = pair_dequant2(v.w & 0xffffu, scale), b3 = pair_dequant2(v.w >> 16, scale);
+    st_shared_v4(d1 + k0, a0, a1, a2, a3);
+    st_shared_v4(d1 + k1, b0, b1, b2, b3);
+    st_shared_v4(d2 + k0, a0, a1, a2, a3);
+    st_shared_v4(d2 + k1, b0, b1, b2, b3);
   }
 }
 
-__device__ void pair_gather(const CUtensorMap* tm_rows, const DecodeParams& p, const PairSeg& sg, int rank,
-                            uint32_t smem, uint32_t bars, uint32_t bars_even, uint32_t* flags, const Watchdog& wd) {
-  // 128 threads.  Thread tid takes token tok = tid % 64 of each half of the
-  // tile and hh = tid / 64: of its own tokens (index slots 64 rank + tok) it
-  // converts value blocks 2hh and 2hh + 1 (and the RoPE chunk when hh = 0);
-  // of its partner's tokens (slots 64 (1 - rank) + tok) value block
-  // 2hh + rank, one of the two this CTA supplies to the PV product.  Each
-  // warp gathers its 32 tokens' rows with TMA row gathers (four rows each).
-  // Per tile jt, in order: (A) convert own blocks and RoPE, write the tile's
-  // validity bits, report each item to the even CTA; (B) look up the rows of
-  // tile jt + 1; (C) once the PV MMAs of tile jt - 1 are done, gather the
-  // partner blocks of tile jt and copy the own blocks this CTA supplies into
-  // the value slots; (D) gather tile jt + 1's own blocks as the score MMAs of
-  // tile jt free their slots; (E) convert the partner blocks and report the
-  // tile's value slots.
-  const int tid = threadIdx.x - 32 * kPairGatherWarp0;
-  const int lane = tid & 31;
-  const int hh = tid >> 6;
-  const int tok = tid & 63;
-  const int wtok = tok & ~31;  // first token of this warp's 32
-  const uint32_t tsw = tok & 7;
-  const uint64_t pol = l2_policy_evict_normal();
-  const int row_bytes = p.kv_scales ? 640 : kFp8RowBytes;
-  const int tp = 1 - rank;     // the partner's half of the tile
-  const int bp = 2 * hh + rank;  // this thread's partner value block (one this CTA supplies)
-  uint32_t armed = 0, next_par = 0;  // raw barriers armed by this warp (bit per item), parity of their next phase
+// Tile iterator of a role that runs ahead of the others.
+struct PairIt {
+  int prob, j, te;
+  bool valid;
+};
+__device__ __forceinline__ PairIt pair_first_from(const PairSeg& sg, int prob) {
+  for (; prob <= sg.last(); ++prob) {
+    int tb, te;
+    sg.range(prob, tb, te);
+    if (tb < te) return PairIt{prob, tb, te, true};
+  }
+  return PairIt{0, 0, 0, false};
+}
+__device__ __forceinline__ PairIt pair_next(const PairSeg& sg, const PairIt& it) {
+  if (!it.valid) return it;
+  if (it.j + 1 < it.te) return PairIt{it.prob, it.j + 1, it.te, true};
+  return pair_first_from(sg, it.prob + 1);
+}
 
-  struct It {
-    int prob, j, te;
-    bool valid;
+// Cache row of the token in index slot k of problem prob, or -1 for an
+// invalid id (outside [0, length) or on an unusable page, flagged when asked).
+__device__ __forceinline__ int sparse_row(const DecodeParams& p, const PairSeg& sg, int prob, int k, bool flag) {
+  const int b = prob / p.s_q;
+  const int L = sg.seqlens[b];
+  int tk = p.topk;
+  if (p.topk_lengths) {
+    const int len = p.topk_lengths[prob];
+    tk = len < 0 ? 0 : (len < p.topk ? len : p.topk);
+  }
+  const int t = k < tk ? p.indices[static_cast<int64_t>(prob) * p.topk + k] : -1;
+  if (t < 0 || t >= L) return -1;
+  const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
+  const int page = (t >> 6) < p.block_table_stride ? bt[t >> 6] : -1;
+  if (page < 0 || page >= p.num_pages) {
+    if (flag) atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
+    return -1;
+  }
+  return page * kPageSize + (t & 63);
+}
+
+// fp32 scale of value block blk of cache row `row` (656-byte rows: four scales
+// in the row; 640-byte rows: one scale per token in kv_scales)
+__device__ __forceinline__ float sparse_scale(const DecodeParams& p, int row, int blk) {
+  if (row < 0) return 0.f;
+  if (p.kv_scales) return __ldg(p.kv_scales + row);
+  return __ldg(reinterpret_cast<const float*>(p.kv_fp8 + static_cast<int64_t>(row) * kFp8RowBytes + kFp8ScaleOffset) +
+               blk);
+}
+
+// Prefetch `bytes` (a multiple of 16) from a 16-byte aligned address into L2.
+__device__ __forceinline__ void l2_prefetch_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared (L2 only); src_bytes 0 writes zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)),
+               "r"(src_bytes)
+               : "memory");
+}
+// One arrival on `bar` once every copy this thread has started is complete
+// (the barrier's expected count includes it).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Row copies of a gather warp.  Copy instruction i (0..7) of lane l moves the
+// 16-byte unit l % 8 of warp token 4 i + l / 8, so that each instruction
+// reads four 128-byte row segments whole.  rows[i] is that token's cache row
+// (-1: invalid token).
+struct WarpRows {
+  int r[8];
+  __device__ __forceinline__ void load(int my_row, int lane) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r[i] = __shfl_sync(0xffffffffu, my_row, 4 * i + (lane >> 3));
+  }
+};
+
+// The 128 codes of value block `blk` of the warp's 32 tokens, as plain 128-byte
+// rows at rows wtok .. wtok + 31 of the chunk at `dst_chunk`.  An invalid
+// token's codes are read from row 0 (its values are written as zeros later).
+__device__ __forceinline__ void copy_block_codes(const DecodeParams& p, int row_bytes, const WarpRows& wr, int blk,
+                                                 uint32_t dst_chunk, int wtok, int lane) {
+  const int u = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = wr.r[i] < 0 ? 0 : wr.r[i];
+    const int tk = wtok + 4 * i + (lane >> 3);
+    cp_async16(dst_chunk + tk * 128 + 16 * u, p.kv_fp8 + static_cast<int64_t>(row) * row_bytes + 128 * blk + 16 * u,
+               16);
+  }
+}
+
+// Warps 12-15 (sparse): row copies and dequantisation.  Thread g (0..127)
+// owns token tok = g % 64 of the CTA's half of each tile (index slot
+// 64 rank + tok) and value blocks 2hh and 2hh + 1 (hh = g / 64): block
+// bs = 2hh + rank is in this CTA's share of the value dims, block
+// bp = 2hh + 1 - rank in its partner's.  Per tile:
+//   * its warp copies the codes of those blocks for its 32 tokens into the
+//     score slots (block b as plain rows in chunk 2b + 1) as the score MMAs of
+//     the previous tile release them; the hh = 0 warps also copy the RoPE
+//     parts straight into the 128-byte swizzle of chunk 8 (zeros for invalid
+//     tokens);
+//   * the thread dequantises block bp in place (chunks 2bp, 2bp + 1), for the
+//     score MMAs and for the copier, which moves the block of all 64 tokens
+//     into the partner's value slots (pair_value_copier); then, once the PV
+//     MMAs of the previous tile are done, block bs, in place and into this
+//     CTA's value slots 4 rank + 2hh, 4 rank + 2hh + 1 (an own-share copy
+//     made later, on its own, delayed the next tile's row copies more than
+//     this wait delays the score MMAs);
+//   * the next tile's codes are copied in once the score MMAs, and for bp
+//     the copier, have read the slots.
+// So each token is fetched and dequantised once per pair.  The hh = 0 warps
+// write the tile's validity bits of their tokens to both CTAs, look the rows
+// up three tiles ahead and prefetch them whole into L2, so that the copies
+// on the tile's critical chain hit L2.
+__device__ void pair_gather(const DecodeParams& p, const PairSeg& sg, int rank, uint32_t smem, uint32_t bars,
+                            uint32_t bars_even, uint32_t* flags, const Watchdog& wd) {
+  const int g = threadIdx.x - 32 * kPairGatherWarp0;  // 0..127
+  const int lane = g & 31;
+  const int hh = g >> 6;
+  const int tok = g & 63;
+  const int wtok = tok & ~31;
+  const uint32_t tsw = tok & 7;
+  const int bs = 2 * hh + rank, bp = 2 * hh + 1 - rank;
+  const int row_bytes = p.kv_scales ? 640 : kFp8RowBytes;
+  const uint32_t peer = static_cast<uint32_t>(rank ^ 1);
+  const uint32_t kv_own = smem + kPairKvOff + (4 * rank + 2 * hh) * kPairChunk + tok * 128;
+  const uint32_t flags_here = static_cast<uint32_t>(__cvta_generic_to_shared(flags));
+  const uint32_t flags_peer = mapa_shared(flags_here, peer);
+  const uint32_t bars_peer = mapa_shared(bars, peer);
+  uint32_t armed = 0, next_par = 0;  // raw barriers with copies of this thread (bit per item), parity of their next phase
+  auto row_of = [&](const PairIt& it) {
+    return it.valid ? sparse_row(p, sg, it.prob, it.j * kPairTile + 64 * rank + tok, hh == 0) : -1;
   };
-  auto first_from = [&](int prob) -> It {
-    for (; prob <= sg.last(); ++prob) {
-      int tb, te;
-      sg.range(prob, tb, te);
-      if (tb < te) return It{prob, tb, te, true};
-    }
-    return It{0, 0, 0, false};
+  auto prefetch = [&](int row) {
+    if (hh == 0 && row >= 0) l2_prefetch_bulk(p.kv_fp8 + static_cast<int64_t>(row) * row_bytes, row_bytes);
   };
-  auto next_of = [&](const It& it) -> It {
-    if (it.j + 1 < it.te) return It{it.prob, it.j + 1, it.te, true};
-    return first_from(it.prob + 1);
-  };
-  struct Look {
-    int row_o, row_p;
-    bool ok_o, ok_p;
-    uint2 sc_o;   // scales of own blocks 2hh, 2hh + 1
-    float sc_p;   // scale of partner block bp
-  };
-  // row of the token in index slot k of problem prob (0 for an invalid one)
-  auto lookup_row = [&](int prob, int k, bool flag, int& row) -> bool {
-    const int b = prob / p.s_q;
-    const int L = sg.seqlens[b];
-    int tk = p.topk;
-    if (p.topk_lengths) {
-      const int len = p.topk_lengths[prob];
-      tk = len < 0 ? 0 : (len < p.topk ? len : p.topk);
-    }
-    const int t = k < tk ? p.indices[static_cast<int64_t>(prob) * p.topk + k] : -1;
-    bool ok = t >= 0 && t < L;
-    const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
-    const int page = (ok && (t >> 6) < p.block_table_stride) ? bt[t >> 6] : -1;
-    if (ok && (page < 0 || page >= p.num_pages)) {
-      ok = false;
-      if (flag) atomicOr(p.status, MLA_DEVICE_BAD_PAGE);
-    }
-    row = ok ? page * kPageSize + (t & 63) : 0;
-    return ok;
-  };
-  auto lookup = [&](const It& it) -> Look {
-    Look lk;
-    lk.ok_o = lookup_row(it.prob, it.j * kPairTile + 64 * rank + tok, hh == 0, lk.row_o);
-    lk.ok_p = lookup_row(it.prob, it.j * kPairTile + 64 * tp + tok, false, lk.row_p);
-    if (p.kv_scales) {
-      const float s = lk.ok_o ? __ldg(p.kv_scales + lk.row_o) : 0.f;
-      lk.sc_o = make_uint2(__float_as_uint(s), __float_as_uint(s));
-      lk.sc_p = lk.ok_p ? __ldg(p.kv_scales + lk.row_p) : 0.f;
-    } else {
-      lk.sc_o = lk.ok_o ? __ldg(reinterpret_cast<const uint2*>(p.kv_fp8 + static_cast<int64_t>(lk.row_o) * row_bytes +
-                                                              kFp8ScaleOffset + 8 * hh))
-                        : make_uint2(0, 0);
-      lk.sc_p = lk.ok_p ? __ldg(reinterpret_cast<const float*>(p.kv_fp8 + static_cast<int64_t>(lk.row_p) * row_bytes +
-                                                               kFp8ScaleOffset + 4 * bp))
-                        : 0.f;
-    }
-    return lk;
-  };
-  // four consecutive rows of this warp's tokens for the gathers of lane gl
-  auto rows4 = [&](int row, int gl, int& r0, int& r1, int& r2, int& r3) {
-    r0 = __shfl_sync(0xffffffffu, row, 4 * gl);
-    r1 = __shfl_sync(0xffffffffu, row, 4 * gl + 1);
-    r2 = __shfl_sync(0xffffffffu, row, 4 * gl + 2);
-    r3 = __shfl_sync(0xffffffffu, row, 4 * gl + 3);
-  };
-  auto arm = [&](int item, uint32_t bytes) {
-    if (lane == 0) mbar_arrive_expect_tx_u32(bars + 8 * (kBRaw + item), bytes);
-    armed |= 1u << item;
-    next_par ^= 1u << item;
-    __syncwarp();
-  };
-  // (D) own value blocks and RoPE of tile jt into the score-operand slots
-  auto issue_own = [&](int jt, const Look& lk) -> bool {
-    const int gl = lane & 7;
-    int r0, r1, r2, r3;
-    rows4(lk.row_o, gl, r0, r1, r2, r3);
+  // this warp's items of tile jt into the score slots: bs, bp, (RoPE)
+  auto issue = [&](int jt, int row) -> bool {
+    WarpRows wr;
+    wr.load(row, lane);
 #pragma unroll 1
-    for (int i = 0; i < 2; ++i) {
-      const int blk = 2 * hh + i;
-      if (jt > 0 && !pair_wait(bars + 8 * (kBKsEmpty + blk), (jt - 1) & 1, wd)) return false;
-      // the slot's previous contents were read by this thread (value copies) before
-      fence_proxy_async_smem();
-      arm(blk, 32 * 128);
-      if (lane < 8)
-        gather4(smem + kPairKsOff + (2 * blk + 1) * kPairChunk + (wtok + 4 * gl) * 128, tm_rows,
-                bars + 8 * (kBRaw + blk), 128 * blk, r0, r1, r2, r3, pol);
-      __syncwarp();
+    for (int i = 0; i < (hh == 0 ? 3 : 2); ++i) {
+      const int item = i == 0 ? bs : i == 1 ? bp : 4;
+      if (jt > 0) {
+        if (!pair_wait(bars + 8 * (kBKsEmpty + item), (jt - 1) & 1, wd)) return false;
+        if (i == 1 && !pair_wait(bars + 8 * (kBKsRead + hh), (jt - 1) & 1, wd)) return false;
+      }
+      if (i == 0 && g == 0) PAIR_TR(rank, 0, jt);
+      if (item < 4) {
+        copy_block_codes(p, row_bytes, wr, item, smem + kPairKsOff + (2 * item + 1) * kPairChunk, wtok, lane);
+      } else {
+        const uint32_t u = lane & 7;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int tk = wtok + 4 * k + (lane >> 3);
+          const int r = wr.r[k];
+          cp_async16(smem + kPairKsOff + 8 * kPairChunk + tk * 128 + ((u ^ (tk & 7)) << 4),
+                     p.kv_fp8 + static_cast<int64_t>(r < 0 ? 0 : r) * row_bytes + p.fp8_rope_off + 16 * u,
+                     r < 0 ? 0u : 16u);
+        }
+      }
+      cp_async_arrive(bars + 8 * (kBRaw + item));
+      armed |= 1u << item;
+      next_par ^= 1u << item;
     }
-    if (hh == 0) {
-      if (jt > 0 && !pair_wait(bars + 8 * (kBKsEmpty + 4), (jt - 1) & 1, wd)) return false;
-      arm(4, 32 * 128);
-      if (lane < 8)
-        gather4(smem + kPairKsOff + 8 * kPairChunk + (wtok + 4 * gl) * 128, tm_rows, bars + 8 * (kBRaw + 4),
-                p.fp8_rope_off, r0, r1, r2, r3, pol);
-      __syncwarp();
-    }
+    if (g == 0) PAIR_TR(rank, 1, jt);
     return true;
   };
 
-  It cur = first_from(sg.p0);
-  Look lk_c{}, lk_n{};
+  PairIt it_c = pair_first_from(sg, sg.p0);
+  PairIt it_1 = pair_next(sg, it_c);
+  PairIt it_2 = pair_next(sg, it_1);
+  int row_c = row_of(it_c), row_1 = row_of(it_1), row_2 = row_of(it_2);
+  prefetch(row_1);
+  prefetch(row_2);
   int jt = 0;
-  if (cur.valid) {
-    lk_c = lookup(cur);
-    if (!issue_own(0, lk_c)) goto drain;
-  }
-  for (; cur.valid; ++jt) {
-    const uint32_t par = static_cast<uint32_t>(jt) & 1u;
-    // (A) validity bits of the tile (warps 0 and 1: own and partner tokens of
-    // their 32), then the own blocks and the RoPE chunk
-    {
-      const uint32_t vo = __ballot_sync(0xffffffffu, lk_c.ok_o);
-      const uint32_t vp = __ballot_sync(0xffffffffu, lk_c.ok_p);
-      if (hh == 0 && lane == 0) {
-        flags[4 * (jt & 3) + 2 * rank + (wtok >> 5)] = vo;
-        flags[4 * (jt & 3) + 2 * tp + (wtok >> 5)] = vp;
-        mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + 8 * kBFlags)));
+  if (it_c.valid && !issue(0, row_c)) goto drain;
+  for (; it_c.valid; ++jt) {
+    // rows of the tile three ahead (the loads of the lookup overlap the work below)
+    const PairIt it_3 = pair_next(sg, it_2);
+    const int row_3 = row_of(it_3);
+    const float sc_s = sparse_scale(p, row_c, bs), sc_p = sparse_scale(p, row_c, bp);
+    const bool ok = row_c >= 0;
+    if (hh == 0) {
+      // validity bits of this warp's tokens, to both CTAs
+      const uint32_t v = __ballot_sync(0xffffffffu, ok);
+      if (lane == 0) {
+        const uint32_t word = 4 * (4 * (jt & 3) + 2 * rank + (wtok >> 5));
+        const uint32_t fb = 8 * (kBFlags + (jt & 3));
+        st_shared_u32(flags_here + word, v);
+        st_cluster_u32(flags_peer + word, v);
+        mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + fb)));
+        mbar_arrive_cluster(bars_peer + fb);
       }
       __syncwarp();
     }
-#pragma unroll 1
-    for (int i = 0; i < 2; ++i) {
-      const int blk = 2 * hh + i;
-      if (!pair_wait(bars + 8 * (kBRaw + blk), par, wd)) goto drain;
-      dequant_block_row(smem + kPairKsOff + 2 * blk * kPairChunk + tok * 128,
-                        smem + kPairKsOff + (2 * blk + 1) * kPairChunk + tok * 128, tsw,
-                        __uint_as_float(i == 0 ? lk_c.sc_o.x : lk_c.sc_o.y), lk_c.ok_o);
-      fence_proxy_async_smem();
-      warp_arrive_even(rank, bars + 8 * (kBKsFull + blk), bars_even + 8 * (kBKsFull + blk));
-    }
+    const uint32_t par = static_cast<uint32_t>(jt) & 1u;
+    // block bp: score operand, and source of the copy to the partner
+    if (!pair_wait(bars + 8 * (kBRaw + bp), par, wd)) goto drain;
+    if (g == 0) PAIR_TR(rank, 2, jt);
+    dequant_block_row(smem + kPairKsOff + 2 * bp * kPairChunk + tok * 128,
+                      smem + kPairKsOff + (2 * bp + 1) * kPairChunk + tok * 128, tsw, sc_p, ok);
+    fence_proxy_async_smem();
+    warp_arrive_even(rank, bars + 8 * (kBKsFull + bp), bars_even + 8 * (kBKsFull + bp));
+    if (lane == 0) mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + 8 * (kBKsDone + hh))));
+    // block bs: score operand and, once the PV MMAs of the previous tile are
+    // done, this CTA's value slots
+    if (jt > 0 && !pair_wait(bars + 8 * kBKvEmpty, (jt - 1) & 1, wd)) goto drain;
+    if (!pair_wait(bars + 8 * (kBRaw + bs), par, wd)) goto drain;
+    dequant_block_row2(smem + kPairKsOff + 2 * bs * kPairChunk + tok * 128,
+                       smem + kPairKsOff + (2 * bs + 1) * kPairChunk + tok * 128, kv_own, kv_own + kPairChunk, tsw,
+                       sc_s, ok);
+    fence_proxy_async_smem();
+    warp_arrive_even(rank, bars + 8 * (kBKsFull + bs), bars_even + 8 * (kBKsFull + bs));
+    if (lane == 0) mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + 8 * kBKvIn)));
     if (hh == 0) {
       if (!pair_wait(bars + 8 * (kBRaw + 4), par, wd)) goto drain;
-      swizzle_row(smem + kPairKsOff + 8 * kPairChunk + tok * 128, tsw, lk_c.ok_o);
       fence_proxy_async_smem();
       warp_arrive_even(rank, bars + 8 * (kBKsFull + 4), bars_even + 8 * (kBKsFull + 4));
     }
-    if (lane == 0 && hh == 0 && (tid >> 5) == 0) PAIR_TR(rank, 3, jt);
-    // (B) the rows of the next tile
-    const It nxt = next_of(cur);
-    if (nxt.valid) lk_n = lookup(nxt);
-    // (C) the partner blocks of this tile, and the own blocks this CTA
-    // supplies (block bp of its own tokens: converted above by this thread)
-    if (jt > 0 && !pair_wait(bars + 8 * kBKvEmpty, (jt - 1) & 1, wd)) goto drain;
-    {
-      const int gl = lane & 7;
-      int r0, r1, r2, r3;
-      rows4(lk_c.row_p, gl, r0, r1, r2, r3);
-      arm(5 + hh, 32 * 128);
-      if (lane < 8)
-        gather4(smem + kPairKvOff + (4 * tp + 2 * hh + 1) * kPairChunk + (wtok + 4 * gl) * 128, tm_rows,
-                bars + 8 * (kBRaw + 5 + hh), 128 * bp, r0, r1, r2, r3, pol);
-      __syncwarp();
-      // own block bp = 2hh + rank sits in score slots 2bp, 2bp + 1; its copy
-      // goes to value slots 4 rank + 2hh, 4 rank + 2hh + 1 (same row layout)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const uint32_t src = smem + kPairKsOff + (2 * bp + e) * kPairChunk + tok * 128;
-        const uint32_t dst = smem + kPairKvOff + (4 * rank + 2 * hh + e) * kPairChunk + tok * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 v = ld_shared_v4(src + 16 * u);
-          st_shared_v4(dst + 16 * u, v.x, v.y, v.z, v.w);
-        }
-      }
-    }
-    // (D) the next tile's own blocks, as the score MMAs free their slots
-    if (nxt.valid && !issue_own(jt + 1, lk_n)) goto drain;
-    // (E) the partner blocks, dequantised in place
-    if (!pair_wait(bars + 8 * (kBRaw + 5 + hh), par, wd)) goto drain;
-    dequant_block_row(smem + kPairKvOff + (4 * tp + 2 * hh) * kPairChunk + tok * 128,
-                      smem + kPairKvOff + (4 * tp + 2 * hh + 1) * kPairChunk + tok * 128, tsw, lk_c.sc_p, lk_c.ok_p);
-    fence_proxy_async_smem();
-    warp_arrive_even(rank, bars + 8 * kBKvFull, bars_even + 8 * kBKvFull);
-    if (lane == 0 && tid == 0) PAIR_TR(rank, 4, jt);
-    cur = nxt;
-    lk_c = lk_n;
+    if (g == 0) PAIR_TR(rank, 3, jt);
+    prefetch(row_3);
+    if (it_1.valid && !issue(jt + 1, row_1)) goto drain;
+    it_c = it_1;
+    it_1 = it_2;
+    it_2 = it_3;
+    row_c = row_1;
+    row_1 = row_2;
+    row_2 = row_3;
   }
   return;
 drain:
-  // abort: wait (bounded) for this warp's row gathers still in flight
-  if (lane == 0) {
+  // abort: this thread's copies, then (bounded) the arrivals they trigger
+  cp_async_wait_all();
 #pragma unroll 1
-    for (int k = 0; k < 7; ++k)
-      if ((armed >> k) & 1u) pair_drain(bars + 8 * (kBRaw + k), ((next_par >> k) & 1u) ^ 1u, wd.limit_ns);
+  for (int k = 0; k < 5; ++k)
+    if ((armed >> k) & 1u) pair_drain(bars + 8 * (kBRaw + k), ((next_par >> k) & 1u) ^ 1u, wd.limit_ns);
+}
+
+// 16-byte aligned bulk copy of `bytes` from this CTA's shared memory to shared
+// memory of a CTA of the cluster, completing on a barrier of that CTA.
+__device__ __forceinline__ void bulk_copy_s2c(uint32_t dst_cluster, uint32_t src, uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(src), "r"(bytes), "r"(bar_cluster)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Warp 2 (sparse): the partner's value slots.  The value dims of block b of a
+// token sit, dequantised, in score slots 2b and 2b + 1 of the CTA that owns
+// the token (16 KB for its 64 tokens, the layout of a value-slot pair).  Per
+// tile and m = 0, 1: once this CTA's gather warps have dequantised block
+// 1 - rank + 2m (the partner's share) and the PV MMAs of the previous tile
+// have released the slots, one thread copies it into the partner's value
+// slots 4 rank + 2m, 4 rank + 2m + 1 with the bulk-copy engine, and releases
+// the score slots to the gather warps once the copy has read them.  When
+// this CTA's value slots of the tile are complete (its own share, written by
+// its gather warps, and its partner's copies), the PV issuer of the even CTA
+// is told.
+__device__ void pair_value_copier(const PairSeg& sg, int rank, uint32_t smem, uint32_t bars, uint32_t bars_even,
+                                  const Watchdog& wd) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t peer = static_cast<uint32_t>(rank ^ 1);
+  const uint32_t smem_peer = mapa_shared(smem, peer);
+  const uint32_t kv_in_peer = mapa_shared(bars + 8 * kBKvIn, peer);
+  bool pending = false;
+  int jt = 0;
+  for (int prob = sg.p0; prob <= sg.last(); ++prob) {
+    int tb, te;
+    sg.range(prob, tb, te);
+    for (int j = tb; j < te; ++j, ++jt) {
+      const uint32_t par = static_cast<uint32_t>(jt) & 1u;
+#pragma unroll 1
+      for (int m = 0; m < 2; ++m) {
+        if (!pair_wait(bars + 8 * (kBKsDone + m), par, wd)) goto drain;
+        if (m == 0) {
+          if (jt > 0 && !pair_wait(bars + 8 * kBKvEmpty, (jt - 1) & 1, wd)) goto drain;
+          // this CTA's slots receive the partner's two 16 KB copies
+          if (lane == 0) mbar_arrive_expect_tx_u32(bars + 8 * kBKvIn, 2 * 2 * kPairChunk);
+        }
+        if (lane == 0) {
+          if (m == 0) PAIR_TR(rank, 12, jt);
+          const int b = 1 - rank + 2 * m;
+          bulk_copy_s2c(smem_peer + kPairKvOff + (4 * rank + 2 * m) * kPairChunk, smem + kPairKsOff + 2 * b * kPairChunk,
+                        2 * kPairChunk, kv_in_peer);
+          bulk_commit();
+          pending = true;
+          bulk_wait_read_all();
+          mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + 8 * (kBKsRead + m))));
+        }
+        __syncwarp();
+      }
+      if (!pair_wait(bars + 8 * kBKvIn, par, wd)) goto drain;
+      if (lane == 0) {
+        bulk_wait_all();
+        pending = false;
+        PAIR_TR(rank, 13, jt);
+      }
+      warp_arrive_even(rank, bars + 8 * kBKvFull, bars_even + 8 * kBKvFull);
+    }
   }
+  return;
+drain:
+  if (lane == 0 && pending) bulk_wait_all();
   __syncwarp();
 }
 
@@ -839,7 +962,7 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
       uint32_t vbits = 0xffffffffu;
       if (SPARSE) {
         // the gather warps of this CTA wrote the tile's validity bits
-        if (!wait_all(kBFlags, jt & 1)) return;
+        if (!all_ok(pair_wait_thread(bars + 8 * (kBFlags + (jt & 3)), (jt >> 2) & 1, wd))) return;
         vbits = flags[4 * (jt & 3) + 2 * h + w];
       } else {
         page_ok = tile_page(p, b, L, j, h, false) >= 0;
@@ -1017,7 +1140,7 @@ __global__ void __launch_bounds__(PairCfg<SPARSE>::kThreads, 1)
       mbar_init(bp + kBKsFull + it, SPARSE ? 4 : 1);
       mbar_init(bp + kBKsEmpty + it, 1);
     }
-    mbar_init(bp + kBKvFull, SPARSE ? 8 : 1);  // sparse: four gather warps in each CTA
+    mbar_init(bp + kBKvFull, SPARSE ? 2 : 1);  // sparse: the value-slot copier of each CTA
     mbar_init(bp + kBKvEmpty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bp + kBSFull + i, 1);
@@ -1029,8 +1152,13 @@ __global__ void __launch_bounds__(PairCfg<SPARSE>::kThreads, 1)
     mbar_init(bp + kBOEmpty, 16);
     mbar_init(bp + kBMmaDone, 2);  // one commit per MMA-issuing warp
     if (SPARSE) {
-      for (int k = 0; k < 7; ++k) mbar_init(bp + kBRaw + k, 2);  // the two warps gathering the item
-      mbar_init(bp + kBFlags, 2);                                 // the two gather warps writing the bits
+      for (int k = 0; k < 5; ++k) mbar_init(bp + kBRaw + k, 64);   // the copies of the 64 threads of the item
+      for (int k = 0; k < 4; ++k) mbar_init(bp + kBFlags + k, 4);  // the hh = 0 gather warps of both CTAs
+      for (int k = 0; k < 2; ++k) {
+        mbar_init(bp + kBKsDone + k, 2);  // the two gather warps of the block
+        mbar_init(bp + kBKsRead + k, 1);  // the copier
+      }
+      mbar_init(bp + kBKvIn, 5);  // the four gather warps and the copier's arming, plus the partner's bytes
     }
     for (int k = 0; k < 16; ++k) flags[k] = 0;
     *abort_flag = 0;
@@ -1038,7 +1166,7 @@ __global__ void __launch_bounds__(PairCfg<SPARSE>::kThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_ks);
+    if (!SPARSE) tma_prefetch_desc(&tm_ks);
     if (!SPARSE) tma_prefetch_desc(&tm_kv);
   }
   if (warp == 2) {
@@ -1097,7 +1225,10 @@ __global__ void __launch_bounds__(PairCfg<SPARSE>::kThreads, 1)
     } else if (warp == 1) {
       if (rank == 0) pair_s_issuer<SPARSE>(sg, tmem, smem, bars, wd);
     } else if (warp == 2) {
-      if (!SPARSE) pair_producer_kv(&tm_kv, p, sg, rank, smem, bars, bars_even, wd);
+      if (SPARSE)
+        pair_value_copier(sg, rank, smem, bars, bars_even, wd);
+      else
+        pair_producer_kv(&tm_kv, p, sg, rank, smem, bars, bars_even, wd);
     } else if (rank == 0) {
       pair_pv_issuer(sg, tmem, smem, bars, wd);
     }
@@ -1106,7 +1237,7 @@ __global__ void __launch_bounds__(PairCfg<SPARSE>::kThreads, 1)
     pair_softmax<SPARSE>(p, sg, g, rank, split0, tmem, smem, bars, bars_even, m_s, red, flags, wd);
   } else if (SPARSE) {
     regs_to<C::kRegsGather, C::kLaunchRegs>();
-    pair_gather(&tm_ks, p, sg, rank, smem, bars, bars_even, flags, wd);
+    pair_gather(p, sg, rank, smem, bars, bars_even, flags, wd);
   }
 
   tc_fence_before();
