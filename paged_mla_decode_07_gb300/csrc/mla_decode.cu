@@ -66,8 +66,8 @@ enum TraceEvent {
 #ifdef MLA_TRACE
 constexpr int kTraceTiles = 1024;
 __device__ unsigned long long g_mla_trace[kTrNumEvents * kTraceTiles];
-// per CTA (up to 1024): %globaltimer when its work starts and when it ends
-__device__ unsigned long long g_mla_cta[2 * 1024];
+// per CTA (up to 1024): %globaltimer when its work starts and when it ends, its SM
+__device__ unsigned long long g_mla_cta[3 * 1024];
 #define MLA_TR(ev, idx)                                                                      \
   do {                                                                                       \
     if (blockIdx.x == 0 && (idx) < kTraceTiles) g_mla_trace[(ev) * kTraceTiles + (idx)] = clock64(); \
@@ -1304,7 +1304,12 @@ __global__ void __launch_bounds__(Cfg<R, MODE>::kThreads, 1)
   // grid to complete, but are resident when it does
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 #ifdef MLA_TRACE
-  if (threadIdx.x == 0 && blockIdx.x < 1024) g_mla_cta[2 * blockIdx.x] = global_timer_ns();
+  if (threadIdx.x == 0 && blockIdx.x < 1024) {
+    g_mla_cta[3 * blockIdx.x] = global_timer_ns();
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    g_mla_cta[3 * blockIdx.x + 2] = smid;
+  }
 #endif
   Segments sg;
   int split0 = 0;
@@ -1351,7 +1356,7 @@ __global__ void __launch_bounds__(Cfg<R, MODE>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
 #ifdef MLA_TRACE
-  if (threadIdx.x == 0 && blockIdx.x < 1024) g_mla_cta[2 * blockIdx.x + 1] = global_timer_ns();
+  if (threadIdx.x == 0 && blockIdx.x < 1024) g_mla_cta[3 * blockIdx.x + 1] = global_timer_ns();
 #endif
   if (warp == 2) {
     tc_fence_after();
@@ -1435,7 +1440,7 @@ extern "C" int mla_trace_read(unsigned long long* host, size_t n) {
     cudaMemcpyToSymbol(g_mla_trace, z, sizeof z, i);
   return static_cast<int>(n);
 }
-// Copies the per-CTA start/end stamps (2 x 1024 %globaltimer values).
+// Copies the per-CTA start/end stamps and SM ids (3 x 1024 values).
 extern "C" int mla_trace_cta_read(unsigned long long* host) {
   return cudaMemcpyFromSymbol(host, g_mla_cta, sizeof(g_mla_cta)) == cudaSuccess ? 0 : -1;
 }

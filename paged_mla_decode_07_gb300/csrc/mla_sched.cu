@@ -23,14 +23,16 @@
 // the pipeline, writing its rows) 8, so the cut weighs start-up against tiles
 // as the decode kernels spend them.
 //
-// One CTA of 1024 threads; per-problem prefix sums live in shared memory.
+// One CTA of 256 threads; per-problem prefix sums live in shared memory, and
+// every step is a parallel pass or a block-wide scan (the kernel sits on the
+// critical path of each decode step, before the decode kernel can start).
 #include "mla_device.cuh"
 #include "mla_internal.h"
 
 namespace mla {
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 256;
 
 struct Pos {
   int p, t;
@@ -74,35 +76,36 @@ __device__ int part_of(const Pos* starts, int num_parts, Pos x) {
 // In-place inclusive scan of v[0..n) by the whole block: each thread scans a
 // contiguous run, warps scan their run totals with shuffles, one warp scans
 // the warp totals.  warp_tot holds kThreads / 32 entries.
-__device__ void block_inclusive_scan(long long* v, int n, long long* warp_tot) {
+template <typename T>
+__device__ void block_inclusive_scan(T* v, int n, T* warp_tot) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int per = (n + kThreads - 1) / kThreads;
   const int b = tid * per;
   const int e = min(n, b + per);
-  long long s = 0;
+  T s = 0;
   for (int i = b; i < e; ++i) {
     s += v[i];
     v[i] = s;
   }
-  long long x = s;  // inclusive scan of run totals within the warp
+  T x = s;  // inclusive scan of run totals within the warp
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    const T y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
   if (lane == 31) warp_tot[w] = x;
   __syncthreads();
   if (w == 0) {
-    long long t = lane < kThreads / 32 ? warp_tot[lane] : 0;
+    T t = lane < kThreads / 32 ? warp_tot[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, t, o);
+      const T y = __shfl_up_sync(0xffffffffu, t, o);
       if (lane >= o) t += y;
     }
     if (lane < kThreads / 32) warp_tot[lane] = t;
   }
   __syncthreads();
-  const long long base = (x - s) + (w > 0 ? warp_tot[w - 1] : 0);
+  const T base = (x - s) + (w > 0 ? warp_tot[w - 1] : 0);
   for (int i = b; i < e; ++i) v[i] += base;
   __syncthreads();
 }
@@ -145,15 +148,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   // ne_pre[k] = number of non-empty parts before part k
-  if (tid == 0) {
-    int c = 0;
-    for (int k = 0; k < num_parts; ++k) {
-      ne_pre[k] = c;
-      c += pos_less(starts[k], starts[k + 1]) ? 1 : 0;
-    }
-    ne_pre[num_parts] = c;
-  }
+  for (int k = tid; k < num_parts; k += kThreads) ne_pre[k + 1] = pos_less(starts[k], starts[k + 1]) ? 1 : 0;
+  if (tid == 0) ne_pre[0] = 0;
   __syncthreads();
+  block_inclusive_scan(ne_pre + 1, num_parts, reinterpret_cast<int*>(warp_tot));
 
   // 3. pieces per problem.  Parts are contiguous, so the parts touching
   // problem p lie between first(p) = part(p, tile 0) and last(p) =
