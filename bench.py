@@ -72,19 +72,13 @@ def algorithmic(inp) -> dict:
                 bytes=kv_bytes + q_bytes + out_bytes + tab)
 
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one mla_decode_kernel launch per
-# workload, from one `ncu --set full --clock-control none` capture of the bench command with
-# --workload <name> --no-extras --steps 3 --warmup 3.  Each figure holds only for the kernel
-# sources it was taken with: their SHA-256 prefix is stored beside it and the bench reports
-# null once the sources differ.
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the dominant kernel
+# of the headline workload, from one `ncu --set full --clock-control none` capture of
+# `bench.py --no-extras --steps 3 --warmup 3`.  A
+# figure holds only for the kernel sources it was taken with: their SHA-256 prefix is stored beside
+# it and the bench reports null once the sources differ.
 NCU_TRAFFIC = {
-    "dense_membound": (651.62e6, "34b86f766f6da9f3"),
-    "dense_computebound": (357.01e6, "34b86f766f6da9f3"),
-    "sparse_fp8_long": (387.10e6, "34b86f766f6da9f3"),
-    "sparse_fp8": (466.69e6, "34b86f766f6da9f3"),
-    "dense_membound_fp8": (395.69e6, "34b86f766f6da9f3"),
-    "sparse_bf16": (663.91e6, "34b86f766f6da9f3"),
-    "sparse_fp8_token": (432.55e6, "34b86f766f6da9f3"),
+    "dense_membound": (651.43e6, "3a2def902218b5c9"),
 }
 KERNEL_SOURCES = ("mla_decode.cu", "mla_decode_pair.cu", "mla_device.cuh", "mla_internal.h")
 
