@@ -78,9 +78,10 @@ def algorithmic(inp) -> dict:
 # figure holds only for the kernel sources it was taken with: their SHA-256 prefix is stored beside
 # it and the bench reports null once the sources differ.
 NCU_TRAFFIC = {
-    "dense_membound": (651.43e6, "3a2def902218b5c9"),
+    "dense_membound": (651.43e6, "264958ef3a579d4b"),
 }
-KERNEL_SOURCES = ("mla_decode.cu", "mla_decode_pair.cu", "mla_device.cuh", "mla_internal.h")
+# the sources the headline's dominant kernel (the single-CTA decode kernel) is built from
+KERNEL_SOURCES = ("mla_decode.cu", "mla_device.cuh", "mla_internal.h")
 
 
 def kernel_source_hash() -> str:

@@ -130,6 +130,7 @@ constexpr uint32_t kPairTmemCols = 512;
 constexpr float kPairNegInf = -__builtin_huge_valf();
 constexpr float kPairRescale = 8.0f;     // log2 units: P <= 2^8 before a max update is forced
 constexpr uint32_t kPairSmBar = 1;       // named barrier of the 256 softmax threads
+constexpr uint32_t kPairGatherBar = 2;   // named barrier of the 128 gather threads (sparse)
 constexpr int kPairGatherWarp0 = 12;
 
 // Dense: 384 threads, the score operand arrives in three copies of three
@@ -172,7 +173,8 @@ enum PairBar {
   kBKsRead = 34,  // [2] (sparse) its copy to the partner's value slots has read it
   kBKvIn = 36,    // (sparse) this CTA's value slots of the tile are complete: its own share
                   // written by its gather warps, the partner's copies (transaction bytes)
-  kBCount = 37
+  kBKsDoneOwn = 37,  // (sparse) blocks rank and rank + 2 of the tile's score operand are dequantised
+  kBCount = 38
 };
 static_assert(kBCount * 8 <= kPairBarBytes, "barrier area");
 
@@ -462,30 +464,6 @@ __device__ __forceinline__ void dequant_block_row(uint32_t lo, uint32_t hi, uint
   }
 }
 
-// The same, also writing the values to a second place with the same row layout.
-__device__ __forceinline__ void dequant_block_row2(uint32_t lo, uint32_t hi, uint32_t lo2, uint32_t hi2, uint32_t tsw,
-                                                   float scale, bool ok) {
-  uint4 raw[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) raw[k] = ld_shared_v4(hi + ((k ^ tsw) << 4));
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint32_t u = k ^ tsw;
-    const uint32_t d1 = (u & 4) ? hi : lo, d2 = (u & 4) ? hi2 : lo2;
-    const uint32_t k0 = ((2 * (u & 3)) ^ tsw) << 4, k1 = ((2 * (u & 3) + 1) ^ tsw) << 4;
-    uint4 v = raw[k];
-    if (!ok) v = make_uint4(0, 0, 0, 0);
-    const uint32_t a0 = pair_dequant2(v.x & 0xffffu, scale), a1 = pair_dequant2(v.x >> 16, scale);
-    const uint32_t a2 = pair_dequant2(v.y & 0xffffu, scale), a3 = pair_dequant2(v.y >> 16, scale);
-    const uint32_t b0 = pair_dequant2(v.z & 0xffffu, scale), b1 = pair_dequant2(v.z >> 16, scale);
-    const uint32_t b2 = pair_dequant2(v.w & 0xffffu, scale), b3 = pair_dequant2(v.w >> 16, scale);
-    st_shared_v4(d1 + k0, a0, a1, a2, a3);
-    st_shared_v4(d1 + k1, b0, b1, b2, b3);
-    st_shared_v4(d2 + k0, a0, a1, a2, a3);
-    st_shared_v4(d2 + k1, b0, b1, b2, b3);
-  }
-}
-
 // Tile iterator of a role that runs ahead of the others.
 struct PairIt {
   int prob, j, te;
@@ -526,15 +504,6 @@ __device__ __forceinline__ int sparse_row(const DecodeParams& p, const PairSeg& 
   return page * kPageSize + (t & 63);
 }
 
-// fp32 scale of value block blk of cache row `row` (656-byte rows: four scales
-// in the row; 640-byte rows: one scale per token in kv_scales)
-__device__ __forceinline__ float sparse_scale(const DecodeParams& p, int row, int blk) {
-  if (row < 0) return 0.f;
-  if (p.kv_scales) return __ldg(p.kv_scales + row);
-  return __ldg(reinterpret_cast<const float*>(p.kv_fp8 + static_cast<int64_t>(row) * kFp8RowBytes + kFp8ScaleOffset) +
-               blk);
-}
-
 // Prefetch `bytes` (a multiple of 16) from a 16-byte aligned address into L2.
 __device__ __forceinline__ void l2_prefetch_bulk(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
@@ -553,6 +522,17 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// 4-byte asynchronous copy global -> shared (through L1); src_bytes 0 writes zeros.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
 
 // Row copies of a gather warp.  Copy instruction i (0..7) of lane l moves the
 // 16-byte unit l % 8 of warp token 4 i + l / 8, so that each instruction
@@ -581,31 +561,27 @@ __device__ __forceinline__ void copy_block_codes(const DecodeParams& p, int row_
   }
 }
 
-// Warps 12-15 (sparse): row copies and dequantisation.  Thread g (0..127)
-// owns token tok = g % 64 of the CTA's half of each tile (index slot
-// 64 rank + tok) and value blocks 2hh and 2hh + 1 (hh = g / 64): block
-// bs = 2hh + rank is in this CTA's share of the value dims, block
-// bp = 2hh + 1 - rank in its partner's.  Per tile:
+// Warps 12-15 (sparse): row lookups and row copies.  Thread g (0..127) owns
+// token tok = g % 64 of the CTA's half of each tile (index slot 64 rank + tok)
+// and value blocks 2hh and 2hh + 1 (hh = g / 64); block bs = 2hh + rank is in
+// this CTA's share of the value dims, block 2hh + 1 - rank in its partner's.
+// Per tile:
 //   * its warp copies the codes of those blocks for its 32 tokens into the
-//     score slots (block b as plain rows in chunk 2b + 1) as the score MMAs of
-//     the previous tile release them; the hh = 0 warps also copy the RoPE
+//     score slots (block b as plain rows in chunk 2b + 1, with the token's
+//     scales in the first bytes of its row of chunk 2b) as the score MMAs of
+//     the previous tile, and for the partner's block the copier
+//     (pair_value_copier), release them; the hh = 0 warps also copy the RoPE
 //     parts straight into the 128-byte swizzle of chunk 8 (zeros for invalid
-//     tokens);
-//   * the thread dequantises block bp in place (chunks 2bp, 2bp + 1), for the
-//     score MMAs and for the copier, which moves the block of all 64 tokens
-//     into the partner's value slots (pair_value_copier); then, once the PV
-//     MMAs of the previous tile are done, block bs, in place and into this
-//     CTA's value slots 4 rank + 2hh, 4 rank + 2hh + 1 (an own-share copy
-//     made later, on its own, delayed the next tile's row copies more than
-//     this wait delays the score MMAs);
-//   * the next tile's codes are copied in once the score MMAs, and for bp
-//     the copier, have read the slots.
-// So each token is fetched and dequantised once per pair.  The hh = 0 warps
-// write the tile's validity bits of their tokens to both CTAs, look the rows
-// up three tiles ahead and prefetch them whole into L2, so that the copies
-// on the tile's critical chain hit L2.
+//     tokens).  The softmax warps dequantise the blocks in place
+//     (pair_softmax);
+//   * once they have, and the PV MMAs of the previous tile are done, the
+//     thread copies its token's row of block bs into this CTA's value slots
+//     4 rank + 2hh, 4 rank + 2hh + 1.
+// The hh = 0 warps write the tile's validity bits of their tokens to both
+// CTAs, look the rows up three tiles ahead and prefetch them whole into L2,
+// so that the copies on the tile's critical chain hit L2.
 __device__ void pair_gather(const DecodeParams& p, const PairSeg& sg, int rank, uint32_t smem, uint32_t bars,
-                            uint32_t bars_even, uint32_t* flags, const Watchdog& wd) {
+                            const Watchdog& wd, uint32_t* flags) {
   const int g = threadIdx.x - 32 * kPairGatherWarp0;  // 0..127
   const int lane = g & 31;
   const int hh = g >> 6;
@@ -639,7 +615,15 @@ __device__ void pair_gather(const DecodeParams& p, const PairSeg& sg, int rank, 
       }
       if (i == 0 && g == 0) PAIR_TR(rank, 0, jt);
       if (item < 4) {
-        copy_block_codes(p, row_bytes, wr, item, smem + kPairKsOff + (2 * item + 1) * kPairChunk, wtok, lane);
+        const uint32_t lo = smem + kPairKsOff + 2 * item * kPairChunk;
+        copy_block_codes(p, row_bytes, wr, item, lo + kPairChunk, wtok, lane);
+        // the token's scale(s), read by the dequantising thread before it writes its row of chunk 2b
+        const uint32_t sdst = lo + tok * 128 + (tsw << 4);
+        const int r0 = row < 0 ? 0 : row;
+        if (p.kv_scales)
+          cp_async4(sdst, p.kv_scales + r0, row < 0 ? 0u : 4u);
+        else
+          cp_async16(sdst, p.kv_fp8 + static_cast<int64_t>(r0) * row_bytes + kFp8ScaleOffset, row < 0 ? 0u : 16u);
       } else {
         const uint32_t u = lane & 7;
 #pragma unroll
@@ -671,11 +655,9 @@ __device__ void pair_gather(const DecodeParams& p, const PairSeg& sg, int rank, 
     // rows of the tile three ahead (the loads of the lookup overlap the work below)
     const PairIt it_3 = pair_next(sg, it_2);
     const int row_3 = row_of(it_3);
-    const float sc_s = sparse_scale(p, row_c, bs), sc_p = sparse_scale(p, row_c, bp);
-    const bool ok = row_c >= 0;
     if (hh == 0) {
       // validity bits of this warp's tokens, to both CTAs
-      const uint32_t v = __ballot_sync(0xffffffffu, ok);
+      const uint32_t v = __ballot_sync(0xffffffffu, row_c >= 0);
       if (lane == 0) {
         const uint32_t word = 4 * (4 * (jt & 3) + 2 * rank + (wtok >> 5));
         const uint32_t fb = 8 * (kBFlags + (jt & 3));
@@ -687,30 +669,31 @@ __device__ void pair_gather(const DecodeParams& p, const PairSeg& sg, int rank, 
       __syncwarp();
     }
     const uint32_t par = static_cast<uint32_t>(jt) & 1u;
-    // block bp: score operand, and source of the copy to the partner
-    if (!pair_wait(bars + 8 * (kBRaw + bp), par, wd)) goto drain;
+    // this CTA's value slots of block bs, once it is dequantised and the PV
+    // MMAs of the previous tile are done (16-byte units in swizzled order:
+    // the eight threads of a shared-memory wavefront touch eight banks)
+    bool ok = pair_wait(bars + 8 * kBKsDoneOwn, par, wd);
     if (g == 0) PAIR_TR(rank, 2, jt);
-    dequant_block_row(smem + kPairKsOff + 2 * bp * kPairChunk + tok * 128,
-                      smem + kPairKsOff + (2 * bp + 1) * kPairChunk + tok * 128, tsw, sc_p, ok);
-    fence_proxy_async_smem();
-    warp_arrive_even(rank, bars + 8 * (kBKsFull + bp), bars_even + 8 * (kBKsFull + bp));
-    if (lane == 0) mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + 8 * (kBKsDone + hh))));
-    // block bs: score operand and, once the PV MMAs of the previous tile are
-    // done, this CTA's value slots
-    if (jt > 0 && !pair_wait(bars + 8 * kBKvEmpty, (jt - 1) & 1, wd)) goto drain;
-    if (!pair_wait(bars + 8 * (kBRaw + bs), par, wd)) goto drain;
-    dequant_block_row2(smem + kPairKsOff + 2 * bs * kPairChunk + tok * 128,
-                       smem + kPairKsOff + (2 * bs + 1) * kPairChunk + tok * 128, kv_own, kv_own + kPairChunk, tsw,
-                       sc_s, ok);
-    fence_proxy_async_smem();
-    warp_arrive_even(rank, bars + 8 * (kBKsFull + bs), bars_even + 8 * (kBKsFull + bs));
-    if (lane == 0) mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + 8 * kBKvIn)));
-    if (hh == 0) {
-      if (!pair_wait(bars + 8 * (kBRaw + 4), par, wd)) goto drain;
+    if (ok && jt > 0) ok = pair_wait(bars + 8 * kBKvEmpty, (jt - 1) & 1, wd);
+    if (ok) {
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const uint32_t src = smem + kPairKsOff + (2 * bs + h2) * kPairChunk + tok * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t off = (u ^ tsw) << 4;
+          const uint4 v = ld_shared_v4(src + off);
+          st_shared_v4(kv_own + h2 * kPairChunk + off, v.x, v.y, v.z, v.w);
+        }
+      }
       fence_proxy_async_smem();
-      warp_arrive_even(rank, bars + 8 * (kBKsFull + 4), bars_even + 8 * (kBKsFull + 4));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + 8 * kBKvIn)));
     }
     if (g == 0) PAIR_TR(rank, 3, jt);
+    // every own-share copy of the tile is done before its score slots are
+    // reloaded (every gather warp reaches this barrier: its waits are bounded)
+    if (!named_bar_and(kPairGatherBar, 128, ok)) goto drain;
     prefetch(row_3);
     if (it_1.valid && !issue(jt + 1, row_1)) goto drain;
     it_c = it_1;
@@ -935,6 +918,51 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
     // watchdog test: this barrier's first phase only completes when this role has finished
     if (!wait_all(kBMmaDone, 0)) return;
   }
+  // Sparse: the score operand of tile t is dequantised here, one block row per
+  // thread (warp 4 + 2b + k: block b, tokens 32k .. 32k + 31 of the CTA's
+  // half), as soon as P of the previous tile is handed over: the softmax
+  // warps are otherwise idle while the tile's rows arrive.  (Converting the
+  // blocks one after the other with all eight warps, so that the score MMAs
+  // of a block could start while the next is converted, measured slower: the
+  // conversions are bound by the conversion pipe's rate, and the per-block
+  // barriers of all 256 threads cost more than the overlap gave.)
+  int tiles = 0;
+  if (SPARSE) {
+    for (int pr = sg.p0; pr <= sg.last(); ++pr) {
+      int tb, te;
+      sg.range(pr, tb, te);
+      if (te > tb) tiles += te - tb;
+    }
+  }
+  auto dequant_tile = [&](int t) -> bool {
+    const int dw = warp - 4;
+    const int blk = dw >> 1, tg = dw & 1;
+    const int tok = 32 * tg + lane;
+    const uint32_t tsw = tok & 7;
+    if (!all_ok(pair_wait_thread(bars + 8 * (kBFlags + (t & 3)), (t >> 2) & 1, wd))) return false;
+    if (warp == 4 && lane == 0) PAIR_TR(rank, 14, t);
+    const bool ok = ((flags[4 * (t & 3) + 2 * rank + tg] >> lane) & 1u) != 0;
+    if (!all_ok(pair_wait_thread(bars + 8 * (kBRaw + blk), t & 1, wd))) return false;
+    if (warp == 4 && lane == 0) PAIR_TR(rank, 15, t);
+    const uint32_t lo = smem + kPairKsOff + 2 * blk * kPairChunk + tok * 128;
+    const float scale = ld_shared_f32(lo + (tsw << 4) + (p.kv_scales ? 0 : 4 * blk));
+    dequant_block_row(lo, lo + kPairChunk, tsw, scale, ok);
+    fence_proxy_async_smem();
+    arrive_even(kBKsFull + blk);
+    if (lane == 0)
+      mbar_arrive(reinterpret_cast<uint64_t*>(
+          __cvta_shared_to_generic(bars + 8 * ((blk & 1) == rank ? kBKsDoneOwn : kBKsDone + (blk >> 1)))));
+    // the RoPE part landed in its final layout
+    const bool rope_ok = dw < 2 ? pair_wait_thread(bars + 8 * (kBRaw + 4), t & 1, wd) : true;
+    if (!all_ok(rope_ok)) return false;
+    if (dw < 2) {
+      fence_proxy_async_smem();
+      arrive_even(kBKsFull + 4);
+    }
+    if (warp == 4 && lane == 0) PAIR_TR(rank, 4, t);
+    return true;
+  };
+  if (SPARSE && tiles > 0 && !dequant_tile(0)) return;
 
   int jt = 0, seg = 0;
   for (int prob = sg.p0; prob <= sg.last(); ++prob) {
@@ -1042,6 +1070,7 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
       tc_fence_before();
       arrive_even(kBPFull);
       if (tr) PAIR_TR(rank, 9, jt);
+      if (SPARSE && jt + 1 < tiles && !dequant_tile(jt + 1)) return;
     }
 
     // ---- epilogue: O / l -> out (single piece) or fp32 partial (split problem)
@@ -1137,6 +1166,7 @@ __global__ void __launch_bounds__(PairCfg<SPARSE>::kThreads, 1)
     for (int it = 0; it < C::kItems; ++it) {
       // dense: the even producer's arrival plus both CTAs' bytes; sparse: the
       // two gather warps converting the item in each CTA
+      // sparse: each item by two softmax warps of each CTA
       mbar_init(bp + kBKsFull + it, SPARSE ? 4 : 1);
       mbar_init(bp + kBKsEmpty + it, 1);
     }
@@ -1155,9 +1185,10 @@ __global__ void __launch_bounds__(PairCfg<SPARSE>::kThreads, 1)
       for (int k = 0; k < 5; ++k) mbar_init(bp + kBRaw + k, 64);   // the copies of the 64 threads of the item
       for (int k = 0; k < 4; ++k) mbar_init(bp + kBFlags + k, 4);  // the hh = 0 gather warps of both CTAs
       for (int k = 0; k < 2; ++k) {
-        mbar_init(bp + kBKsDone + k, 2);  // the two gather warps of the block
+        mbar_init(bp + kBKsDone + k, 2);  // the two softmax warps dequantising the block
         mbar_init(bp + kBKsRead + k, 1);  // the copier
       }
+      mbar_init(bp + kBKsDoneOwn, 4);     // the four softmax warps dequantising blocks rank, rank + 2
       mbar_init(bp + kBKvIn, 5);  // the four gather warps and the copier's arming, plus the partner's bytes
     }
     for (int k = 0; k < 16; ++k) flags[k] = 0;
@@ -1237,7 +1268,7 @@ __global__ void __launch_bounds__(PairCfg<SPARSE>::kThreads, 1)
     pair_softmax<SPARSE>(p, sg, g, rank, split0, tmem, smem, bars, bars_even, m_s, red, flags, wd);
   } else if (SPARSE) {
     regs_to<C::kRegsGather, C::kLaunchRegs>();
-    pair_gather(p, sg, rank, smem, bars, bars_even, flags, wd);
+    pair_gather(p, sg, rank, smem, bars, wd, flags);
   }
 
   tc_fence_before();
