@@ -561,10 +561,7 @@ done:
 // rows only put into the swizzled operand layout
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t dequant2(uint32_t codes16, float scale) {
-  const uint32_t h2 = e4m3x2_to_f16x2(static_cast<uint16_t>(codes16));
-  const float lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu)));
-  const float hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
-  return pack_bf16x2(lo * scale, hi * scale);
+  return e4m3x2_scaled_bf16x2(codes16, scale);
 }
 
 // Permute one 128-byte row of a chunk, copied in plain order, into the
