@@ -36,8 +36,9 @@
 // shared-memory address in both CTAs while holding different dims (dv 0-127
 // and 256-383 for the even CTA, 128-255 and 384-511 for the odd one), so
 // those dims of all 128 tokens of a tile live in a separate set of slots:
-// loaded (dense), or (sparse) bulk-copied from the dequantised score operand
-// of the CTA that owns the token, into its own slots or its partner's.
+// loaded (dense), or (sparse) copied from the dequantised score operand of
+// the CTA that owns the token: into its own slots by its gather warps, into
+// its partner's by one bulk shared-memory copy per block.
 //
 // Shared memory (1024-byte aligned, identical in both CTAs):
 //   Q    9 chunks [64 rows][64 dims] bf16, 128-byte swizzle         72 KB
@@ -52,14 +53,15 @@
 // its barriers with the bytes of both CTAs, and the odd CTA's copies
 // (cta_group::2 TMA) complete on them directly; pages without tokens or with
 // an unusable block-table entry are read past the end of the cache, as
-// zeros.  Sparse: the gather warps of both CTAs arrive on the even CTA's
-// barriers once they have dequantised an item, and each CTA's value-slot
-// copier once its slots of the tile are complete.  Sparse rows are copied with
-// 16-byte cp.async by all lanes of the gather warps rather than with TMA row
-// gathers: a warp issuing row gathers waits about 90 cycles per gather, which
-// at 40 gathers per warp and tile was longer than the tile's MMAs.  The MMA warps commit to the
-// barriers of both CTAs at once (multicast); the odd CTA's softmax warps
-// arrive remotely on the even CTA's barriers.  Every wait is bounded by the
+// zeros.  Sparse: the softmax warps of both CTAs arrive on the even CTA's
+// score-operand barriers once they have dequantised an item, and each CTA's
+// value-slot copier once its slots of the tile are complete.  Sparse rows are
+// copied with 16-byte cp.async by all lanes of the gather warps rather than
+// with TMA row gathers: a warp issuing row gathers waits about 90 cycles per
+// gather, which at 40 gathers per warp and tile was longer than the tile's
+// MMAs.  The MMA warps commit to the barriers of both CTAs at once
+// (multicast); the odd CTA's softmax warps arrive remotely on the even CTA's
+// barriers.  Every wait is bounded by the
 // watchdog; a CTA that gives up records MLA_DEVICE_TIMEOUT and unwinds, and
 // its partner's waits then run out too.
 //
@@ -71,8 +73,9 @@
 //   warp 3      PV MMA issuer (even CTA)
 //   warps 4-11  softmax + epilogue: warp w reads TMEM lane quarter w % 4, so
 //               a thread owns one row and one half of the tile, and the two
-//               warpgroups split that half's 64 tokens
-//   warps 12-15 (sparse) row lookups, row copies, dequantisation, value-slot copies
+//               warpgroups split that half's 64 tokens; sparse: also the
+//               dequantisation of the next tile's score operand
+//   warps 12-15 (sparse) row lookups, row copies, the own value share
 #include "mla_device.cuh"
 #include "mla_internal.h"
 
@@ -432,7 +435,7 @@ drain:
 }
 
 // ---------------------------------------------------------------------------
-// warps 12-15 (sparse): row lookups, row gathers and dequantisation
+// sparse: E4M3 dequantisation, row copies
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t pair_dequant2(uint32_t codes16, float scale) {
   return e4m3x2_scaled_bf16x2(codes16, scale);
