@@ -232,18 +232,36 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
     const int eg = (warp - 4) >> 2;
     const int kt = 32 * q4 + lane;  // key within the tile
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    // The key's page (block table) and scale: two dependent global reads,
+    // software-pipelined three and two tiles ahead so that their latency is
+    // not paid per tile.  -1: no page (past the keys or the table, or a bad
+    // id, which the producer flags).
+    auto page_of = [&](int tt) -> int {
+      const int key = tt * kKeysPerTile + kt;
+      const int jp = key >> 6;
+      if (tt >= te || key >= L || jp >= p.block_table_stride) return -1;
+      const int id = bt[jp];
+      return (id >= 0 && id < p.num_pages) ? id : -1;
+    };
+    auto scale_of = [&](int id, int tt) -> float {
+      return id >= 0 ? p.k_scales[static_cast<int64_t>(id) * kPageSize + ((tt * kKeysPerTile + kt) & 63)] : 0.f;
+    };
+    int pg0 = page_of(tb), pg1 = page_of(tb + 1), pg2 = page_of(tb + 2);
+    float ks0 = scale_of(pg0, tb), ks1 = scale_of(pg1, tb + 1);
     for (int t = tb, i = 0; t < te; ++t, ++i) {
       const int db = i & 1;
       if (!warp_wait_any(d_full + db, static_cast<uint32_t>(i >> 1) & 1u, wd)) break;
       tc_fence_after();
       const int key = t * kKeysPerTile + kt;
-      const int jp = key >> 6;
-      int page = -1;
-      if (key < L && jp < p.block_table_stride) {
-        page = bt[jp];
-        if (page < 0 || page >= p.num_pages) page = -1;
-      }
-      const float ks = page >= 0 ? p.k_scales[static_cast<int64_t>(page) * kPageSize + (key & 63)] : 0.f;
+      // this tile's page and scale were read ahead; start the reads for the
+      // tiles two (scale) and three (page) ahead
+      const int page = pg0;
+      const float ks = ks0;
+      pg0 = pg1;
+      pg1 = pg2;
+      ks0 = ks1;
+      ks1 = scale_of(pg1, t + 2);
+      pg2 = page_of(t + 3);
       const uint32_t dbase = tmem + lane_base + db * dcols;
       for (int j = eg; j < n_b; j += 2) {
         float acc = 0.f;
@@ -292,7 +310,9 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
 // ---------------------------------------------------------------------------
 constexpr int kTopkThreads = 512;                   // two CTAs per SM
 constexpr int kBinsPerThread = 4096 / kTopkThreads;  // of the 12-bit digit histogram
-constexpr int kBatch = 8;      // score loads in flight per thread
+constexpr int kVec = 8;        // float4 score loads in flight per thread (32 scores)
+constexpr int kBatch = 8;      // scalar score loads in flight per thread (ordered tie collection)
+constexpr int kRound = 4 * kVec * kTopkThreads;  // scores one round of loads covers
 constexpr int kCandCap = 4096;  // keys of the threshold's leading-digit bin kept in shared memory
 
 // Descending bitonic sort of n (a power of two) keys in shared memory by the
@@ -313,6 +333,91 @@ __device__ void bitonic_desc(unsigned long long* a, int n) {
       __syncthreads();
     }
   }
+}
+
+// Descending bitonic sort of n = E * kTopkThreads keys by the whole block,
+// thread t holding keys [E t, E t + E) in registers: exchanges within a
+// thread and between the lanes of a warp (shuffles) need no barrier; only
+// the strides that cross warps go through shared memory.  a[0..n) is read
+// at the start and written back sorted (the caller synchronised before).
+template <int E>
+__device__ void bitonic_desc_regs(unsigned long long* a, int n) {
+  constexpr int kWarpSpan = 32 * E;
+  const int tid = threadIdx.x;
+  unsigned long long x[E];
+#pragma unroll
+  for (int k = 0; k < E; ++k) x[k] = a[E * tid + k];
+  for (int size = 2; size <= n; size <<= 1) {
+    int stride = size >> 1;
+    if (stride >= kWarpSpan) {
+#pragma unroll
+      for (int k = 0; k < E; ++k) a[E * tid + k] = x[k];
+      __syncthreads();
+      for (; stride >= kWarpSpan; stride >>= 1) {
+        for (int i = tid; i < n / 2; i += kTopkThreads) {
+          const int x0 = 2 * i - (i & (stride - 1));
+          const int x1 = x0 + stride;
+          const bool desc = (x0 & size) == 0;
+          const unsigned long long u = a[x0], w = a[x1];
+          if ((u < w) == desc) {
+            a[x0] = w;
+            a[x1] = u;
+          }
+        }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int k = 0; k < E; ++k) x[k] = a[E * tid + k];
+    }
+    for (; stride >= E; stride >>= 1) {  // partner in lane ^ (stride / E), same slot k
+#pragma unroll
+      for (int k = 0; k < E; ++k) {
+        const int i = E * tid + k;
+        const unsigned long long y = __shfl_xor_sync(0xffffffffu, x[k], stride / E);
+        const bool take_max = ((i & stride) == 0) == ((i & size) == 0);
+        x[k] = take_max ? (x[k] > y ? x[k] : y) : (x[k] < y ? x[k] : y);
+      }
+    }
+#pragma unroll
+    for (int sk = E / 2; sk > 0; sk >>= 1) {  // partner in the same thread (strides below E)
+      if (sk < size) {
+#pragma unroll
+        for (int k = 0; k < E; ++k) {
+          if ((k & sk) == 0) {
+            const bool desc = ((E * tid + k) & size) == 0;
+            const unsigned long long u = x[k], w = x[k + sk];
+            if ((u < w) == desc) {
+              x[k] = w;
+              x[k + sk] = u;
+            }
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < E; ++k) a[E * tid + k] = x[k];
+  __syncthreads();
+}
+
+// Descending sort of n (a power of two) keys; a must have room for
+// max(n, kTopkThreads) keys (shorter arrays are padded with 0, which sorts last).
+__device__ void sort_desc(unsigned long long* a, int n) {
+  if (n < kTopkThreads) {
+    for (int i = n + threadIdx.x; i < kTopkThreads; i += kTopkThreads) a[i] = 0ull;
+    __syncthreads();
+    n = kTopkThreads;
+  }
+  if (n == kTopkThreads)
+    bitonic_desc_regs<1>(a, n);
+  else if (n == 2 * kTopkThreads)
+    bitonic_desc_regs<2>(a, n);
+  else if (n == 4 * kTopkThreads)
+    bitonic_desc_regs<4>(a, n);
+  else if (n == 8 * kTopkThreads)
+    bitonic_desc_regs<8>(a, n);
+  else
+    bitonic_desc(a, n);
 }
 
 // Append the keys of the lanes with `take` at *counter (one shared atomic per warp).
@@ -342,8 +447,8 @@ __device__ __forceinline__ unsigned long long pack_key(uint32_t u, int id) {
 
 __global__ void __launch_bounds__(kTopkThreads, 2)
     index_topk_kernel(const IndexParams p, int topk, int sort_cap, int32_t* __restrict__ out) {
-  extern __shared__ unsigned long long keys[];  // [sort_cap], then candidates [kCandCap]
-  unsigned long long* cand = keys + sort_cap;
+  extern __shared__ unsigned long long keys[];  // [max(sort_cap, kTopkThreads)], then candidates [kCandCap]
+  unsigned long long* cand = keys + (sort_cap > kTopkThreads ? sort_cap : kTopkThreads);
   __shared__ uint32_t hist[4096];
   __shared__ uint32_t warp_cnt[kTopkThreads / 32];
   __shared__ uint32_t sh_prefix, sh_mask, sh_remaining, sh_gt, sh_eq_taken, sh_eq_total;
@@ -388,19 +493,22 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
       __syncthreads();
       // read before any thread can update them (the digit search below)
       const uint32_t prefix = sh_prefix, mask = sh_mask, rem = sh_remaining;
-      // loads in batches of kBatch per thread (independent, so they are all
-      // in flight together), then the histogram updates
-      for (int i0 = 0; i0 < vis; i0 += kBatch * kTopkThreads) {
-        uint32_t u[kBatch];
+      // kVec float4 loads per thread (independent, so they are all in
+      // flight together), then the histogram updates
+      for (int i0 = 0; i0 < vis; i0 += kRound) {
+        float4 f[kVec];
 #pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-          const int i = i0 + k * kTopkThreads + tid;
-          u[k] = i < vis ? order_key(__ldcg(sc + i)) : 0u;
+        for (int k = 0; k < kVec; ++k) {
+          const int i = i0 + 4 * (k * kTopkThreads + tid);
+          f[k] = i < vis ? __ldcg(reinterpret_cast<const float4*>(sc + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-          const int i = i0 + k * kTopkThreads + tid;
-          if (i < vis && (u[k] & mask) == prefix) atomicAdd(&hist[(u[k] >> shift) & dmask], 1u);
+        for (int k = 0; k < kVec; ++k) {
+          const int i = i0 + 4 * (k * kTopkThreads + tid);
+          const uint32_t u[4] = {order_key(f[k].x), order_key(f[k].y), order_key(f[k].z), order_key(f[k].w)};
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (i + c < vis && (u[c] & mask) == prefix) atomicAdd(&hist[(u[c] >> shift) & dmask], 1u);
         }
       }
       __syncthreads();
@@ -449,31 +557,39 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
         sh_eq_taken = 0;
       }
       __syncthreads();
-      for (int i0 = 0; i0 < vis; i0 += kBatch * kTopkThreads) {
-        uint32_t ub[kBatch];
+      for (int i0 = 0; i0 < vis; i0 += kRound) {
+        float4 f[kVec];
 #pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-          const int i = i0 + k * kTopkThreads + tid;
-          ub[k] = i < vis ? order_key(__ldcg(sc + i)) : 0u;
+        for (int k = 0; k < kVec; ++k) {
+          const int i = i0 + 4 * (k * kTopkThreads + tid);
+          f[k] = i < vis ? __ldcg(reinterpret_cast<const float4*>(sc + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-          const int i = i0 + k * kTopkThreads + tid;
-          const uint32_t dig = ub[k] >> 20;
-          warp_append(keys, &sh_gt, i < vis && dig > d1, pack_key(ub[k], i));
-          warp_append(cand, &sh_eq_taken, i < vis && dig == d1, pack_key(ub[k], i));
+        for (int k = 0; k < kVec; ++k) {
+          const int i = i0 + 4 * (k * kTopkThreads + tid);
+          const uint32_t u[4] = {order_key(f[k].x), order_key(f[k].y), order_key(f[k].z), order_key(f[k].w)};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t dig = u[c] >> 20;
+            const bool in = i + c < vis;
+            // most scores fall below the threshold's bin: one vote skips both appends
+            if (__any_sync(0xffffffffu, in && dig >= d1)) {
+              warp_append(keys, &sh_gt, in && dig > d1, pack_key(u[c], i + c));
+              warp_append(cand, &sh_eq_taken, in && dig == d1, pack_key(u[c], i + c));
+            }
+          }
         }
       }
       int c2 = 1;
       while (c2 < static_cast<int>(n_cand)) c2 <<= 1;
       for (int i = static_cast<int>(n_cand) + tid; i < c2; i += kTopkThreads) cand[i] = 0ull;
       __syncthreads();
-      bitonic_desc(cand, c2);
+      sort_desc(cand, c2);
       const uint32_t n_gt1 = static_cast<uint32_t>(topk) - rem1;
       for (uint32_t k = tid; k < rem1; k += kTopkThreads) keys[n_gt1 + k] = cand[k];
       for (int i = topk + tid; i < sort_cap; i += kTopkThreads) keys[i] = 0ull;
       __syncthreads();
-      bitonic_desc(keys, sort_cap);
+      sort_desc(keys, sort_cap);
       const int n_out1 = min(vis, topk);
       const unsigned long long ninf1 = static_cast<unsigned long long>(order_key(-__int_as_float(0x7f800000)));
       for (int k = tid; k < topk; k += kTopkThreads)
@@ -534,7 +650,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
     for (int i = topk + tid; i < sort_cap; i += kTopkThreads) keys[i] = 0ull;
   }
   __syncthreads();
-  bitonic_desc(keys, sort_cap);
+  sort_desc(keys, sort_cap);
   // keys of unusable pages carry -inf: sorted last, reported as unused slots
   const int n_out = min(vis, topk);
   const unsigned long long ninf = static_cast<unsigned long long>(order_key(-__int_as_float(0x7f800000)));
@@ -560,7 +676,7 @@ cudaError_t launch_index(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const
   if (e != cudaSuccess) return e;
   int cap = 1;
   while (cap < topk) cap <<= 1;
-  const size_t smem = static_cast<size_t>(cap + kCandCap) * sizeof(unsigned long long);
+  const size_t smem = static_cast<size_t>((cap > kTopkThreads ? cap : kTopkThreads) + kCandCap) * sizeof(unsigned long long);
   e = cudaFuncSetAttribute(index_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   index_topk_kernel<<<p.num_tokens, kTopkThreads, smem, stream>>>(p, topk, cap, out);

@@ -147,6 +147,20 @@ def test_index_long_rows_and_many_tiles():
     check_selection(idx, inp)
 
 
+def test_index_runs_cross_many_short_elements():
+    """More elements than SMs, short and ragged: the score kernel's per-CTA runs of the tile line
+    cross several elements each, among them elements without query rows or without keys (no tiles)."""
+    rng = np.random.default_rng(77)
+    batch = 300
+    lens = tuple(0 if i % 37 == 5 else int(x) for i, x in enumerate(rng.integers(1, 700, size=batch)))
+    rows = tuple(0 if i % 23 == 7 else 1 + i % 2 for i in range(batch))
+    w = W.IndexWorkload("ishort", batch=batch, n_new=2, h_idx=32, topk=100, seqlens=lens, rows=rows, relu=True)
+    inp = W.make_index_inputs(w, seed=77)
+    idx, flags = run_index(inp)
+    assert flags == 0
+    check_selection(idx, inp)
+
+
 def test_index_bad_page_is_flagged_and_never_selected():
     w = W.IndexWorkload("ibad", batch=2, n_new=1, h_idx=16, topk=400, seqlens=(300, 200))
     inp = W.make_index_inputs(w, seed=4)
