@@ -313,6 +313,8 @@ constexpr int kBinsPerThread = 4096 / kTopkThreads;  // of the 12-bit digit hist
 constexpr int kVec = 8;        // float4 score loads in flight per thread (32 scores)
 constexpr int kBatch = 8;      // scalar score loads in flight per thread (ordered tie collection)
 constexpr int kRound = 4 * kVec * kTopkThreads;  // scores one round of loads covers
+constexpr int kVecC = 4;       // float4 loads per thread and round of the collection pass
+constexpr int kRoundC = 4 * kVecC * kTopkThreads;
 constexpr int kCandCap = 4096;  // keys of the threshold's leading-digit bin kept in shared memory
 
 // Descending bitonic sort of n (a power of two) keys in shared memory by the
@@ -557,25 +559,54 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
         sh_eq_taken = 0;
       }
       __syncthreads();
-      for (int i0 = 0; i0 < vis; i0 += kRound) {
-        float4 f[kVec];
+      for (int i0 = 0; i0 < vis; i0 += kRoundC) {
+        float4 f[kVecC];
 #pragma unroll
-        for (int k = 0; k < kVec; ++k) {
+        for (int k = 0; k < kVecC; ++k) {
           const int i = i0 + 4 * (k * kTopkThreads + tid);
           f[k] = i < vis ? __ldcg(reinterpret_cast<const float4*>(sc + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        // each lane counts its keys above and in the bin, a warp scan of the
+        // (packed) counts gives the lanes their slots: one atomic per list
+        // and warp for the whole round
+        uint32_t cnt = 0;  // above in the low half-word, in the bin in the high one
 #pragma unroll
-        for (int k = 0; k < kVec; ++k) {
+        for (int k = 0; k < kVecC; ++k) {
           const int i = i0 + 4 * (k * kTopkThreads + tid);
           const uint32_t u[4] = {order_key(f[k].x), order_key(f[k].y), order_key(f[k].z), order_key(f[k].w)};
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const uint32_t dig = u[c] >> 20;
-            const bool in = i + c < vis;
-            // most scores fall below the threshold's bin: one vote skips both appends
-            if (__any_sync(0xffffffffu, in && dig >= d1)) {
-              warp_append(keys, &sh_gt, in && dig > d1, pack_key(u[c], i + c));
-              warp_append(cand, &sh_eq_taken, in && dig == d1, pack_key(u[c], i + c));
+            if (i + c < vis) cnt += dig > d1 ? 1u : (dig == d1 ? 0x10000u : 0u);
+          }
+        }
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+        uint32_t base_gt = 0, base_eq = 0;
+        if (lane == 31) {
+          if (tot & 0xffffu) base_gt = atomicAdd(&sh_gt, tot & 0xffffu);
+          if (tot >> 16) base_eq = atomicAdd(&sh_eq_taken, tot >> 16);
+        }
+        uint32_t o_gt = __shfl_sync(0xffffffffu, base_gt, 31) + ((incl - cnt) & 0xffffu);
+        uint32_t o_eq = __shfl_sync(0xffffffffu, base_eq, 31) + ((incl - cnt) >> 16);
+#pragma unroll
+        for (int k = 0; k < kVecC; ++k) {
+          const int i = i0 + 4 * (k * kTopkThreads + tid);
+          const uint32_t u[4] = {order_key(f[k].x), order_key(f[k].y), order_key(f[k].z), order_key(f[k].w)};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t dig = u[c] >> 20;
+            if (i + c < vis && dig >= d1) {
+              const unsigned long long key = pack_key(u[c], i + c);
+              if (dig > d1)
+                keys[o_gt++] = key;
+              else
+                cand[o_eq++] = key;
             }
           }
         }
