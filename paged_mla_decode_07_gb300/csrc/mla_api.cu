@@ -676,15 +676,27 @@ mla_status mla_index_topk(const mla_index_topk_args* a, mla_stream_t stream) {
   p.num_pages = a->num_pages;
   p.block_table_stride = a->block_table_stride;
   p.relu = a->relu ? 1 : 0;
-  // key tiles per CTA: about four waves of two CTAs per SM when every element
-  // has the longest possible length (fewer, longer CTAs amortise the set-up)
+  // key tiles per CTA: the run length that minimises the modelled time when
+  // every element has the longest possible length -- whole waves of two CTAs
+  // per SM, each costing its tiles plus about three tiles of set-up and
+  // pipeline fill (a last, partly filled wave costs as much as a full one)
   {
     int sms = 0;
     st = device_info(nullptr, &sms);
     if (st != MLA_OK) return st;
     const long long max_tiles = (p.width + 127) / 128;
-    long long tpc = (static_cast<long long>(a->batch) * max_tiles + 8ll * sms - 1) / (8ll * sms);
-    p.tiles_per_cta = static_cast<int>(tpc < 4 ? 4 : (tpc > 64 ? 64 : tpc));
+    const long long slots = 2ll * (sms > 0 ? sms : 1);
+    long long best_cost = -1, best_tpc = 64;
+    for (long long tpc = 4; tpc <= 64; ++tpc) {
+      const long long ctas = static_cast<long long>(a->batch) * ((max_tiles + tpc - 1) / tpc);
+      const long long waves = (ctas + slots - 1) / slots;
+      const long long cost = waves * (tpc + 3);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best_tpc = tpc;
+      }
+    }
+    p.tiles_per_cta = static_cast<int>(best_tpc);
   }
   cudaError_t e = launch_index(tm_q, tm_k, p, a->topk, a->indices, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "indexer kernel launch");
