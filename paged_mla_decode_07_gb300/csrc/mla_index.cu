@@ -79,7 +79,7 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, 
 // w * f(qs * ks * dot) = ks * (w * qs) * f(dot), f = ReLU or identity: the
 // epilogue multiplies each dot by the per-row factor w * qs (kept in shared
 // memory) and the sum by the key's scale once.
-template <bool RELU>
+template <bool RELU, bool H64>
 __global__ void __launch_bounds__(kScoreThreads, 2)
     index_score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const IndexParams p) {
@@ -265,7 +265,33 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
       const uint32_t dbase = tmem + lane_base + db * dcols;
       for (int j = eg; j < n_b; j += 2) {
         float acc = 0.f;
-        for (int h0 = 0; h0 < p.h_idx; h0 += 32) {
+        if (H64) {
+          // 64 heads: two full 32-column reads, factors read before the FMAs
+          float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int h0 = 0; h0 < 64; h0 += 32) {
+            float v[32];
+            tmem_ld_x32(dbase + j * 64 + h0, v);
+            const float4* w4 = reinterpret_cast<const float4*>(wq + j * 64 + h0);
+            tmem_ld_wait();
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+              float4 w[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) w[k] = w4[4 * g + k];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int c = 16 * g + 4 * k;
+                a[0] = fmaf(w[k].x, RELU ? fmaxf(v[c], 0.f) : v[c], a[0]);
+                a[1] = fmaf(w[k].y, RELU ? fmaxf(v[c + 1], 0.f) : v[c + 1], a[1]);
+                a[2] = fmaf(w[k].z, RELU ? fmaxf(v[c + 2], 0.f) : v[c + 2], a[2]);
+                a[3] = fmaf(w[k].w, RELU ? fmaxf(v[c + 3], 0.f) : v[c + 3], a[3]);
+              }
+            }
+          }
+          acc = (a[0] + a[1]) + (a[2] + a[3]);
+        }
+        for (int h0 = 0; !H64 && h0 < p.h_idx; h0 += 32) {
           // up to 32 columns per wait (h_idx is a multiple of 8)
           const int nc = min(32, p.h_idx - h0);
           float v[32];
@@ -420,17 +446,6 @@ __device__ void sort_desc(unsigned long long* a, int n) {
     bitonic_desc_regs<8>(a, n);
   else
     bitonic_desc(a, n);
-}
-
-// Append the keys of the lanes with `take` at *counter (one shared atomic per warp).
-__device__ __forceinline__ void warp_append(unsigned long long* dst, uint32_t* counter, bool take,
-                                            unsigned long long key) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t bal = __ballot_sync(0xffffffffu, take);
-  uint32_t base = 0;
-  if (lane == 0 && bal) base = atomicAdd(counter, static_cast<uint32_t>(__popc(bal)));
-  base = __shfl_sync(0xffffffffu, base, 0);
-  if (take) dst[base + __popc(bal & ((1u << lane) - 1u))] = key;
 }
 
 // Order-preserving image of a finite float (larger float -> larger unsigned);
@@ -697,7 +712,8 @@ size_t index_score_smem_bytes() { return kScoreSmem; }
 
 cudaError_t launch_index(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const IndexParams& p, int topk,
                          int32_t* out, cudaStream_t stream) {
-  auto kern = p.relu ? index_score_kernel<true> : index_score_kernel<false>;
+  auto kern = p.h_idx == 64 ? (p.relu ? index_score_kernel<true, true> : index_score_kernel<false, true>)
+                            : (p.relu ? index_score_kernel<true, false> : index_score_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
   if (e != cudaSuccess) return e;
   const int max_tiles = static_cast<int>((p.width + kKeysPerTile - 1) / kKeysPerTile);
