@@ -147,6 +147,10 @@ __global__ void __launch_bounds__(kScoreThreads, 2)
   const uint32_t tmem = *tmem_slot;
   const uint32_t dcols = p.tmem_cols / 2;  // columns of one accumulator buffer
   Watchdog wd{abort_flag, p.status, p.timeout_ns};
+  // the top-k kernel (a programmatic dependent of this one) may be scheduled
+  // once every CTA of this grid has started: its blocks take the SMs that
+  // the last wave frees and wait (griddepcontrol.wait) for this grid to end
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
 
   if (warp == 0) {
@@ -397,22 +401,24 @@ __device__ void bitonic_desc_regs(unsigned long long* a, int n) {
 #pragma unroll
       for (int k = 0; k < E; ++k) x[k] = a[E * tid + k];
     }
+    // for strides and sizes of at least E the direction bits of key E t + k
+    // are those of E t: one decision per thread and stage
     for (; stride >= E; stride >>= 1) {  // partner in lane ^ (stride / E), same slot k
+      const bool take_max = (((E * tid) & stride) == 0) == (((E * tid) & size) == 0);
 #pragma unroll
       for (int k = 0; k < E; ++k) {
-        const int i = E * tid + k;
         const unsigned long long y = __shfl_xor_sync(0xffffffffu, x[k], stride / E);
-        const bool take_max = ((i & stride) == 0) == ((i & size) == 0);
         x[k] = take_max ? (x[k] > y ? x[k] : y) : (x[k] < y ? x[k] : y);
       }
     }
+    const bool desc_t = ((E * tid) & size) == 0;
 #pragma unroll
     for (int sk = E / 2; sk > 0; sk >>= 1) {  // partner in the same thread (strides below E)
       if (sk < size) {
 #pragma unroll
         for (int k = 0; k < E; ++k) {
           if ((k & sk) == 0) {
-            const bool desc = ((E * tid + k) & size) == 0;
+            const bool desc = size >= E ? desc_t : (k & size) == 0;
             const unsigned long long u = x[k], w = x[k + sk];
             if ((u < w) == desc) {
               x[k] = w;
@@ -488,6 +494,9 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
   if (vis < 0 || n_b > p.max_new) vis = 0;
   if (vis > p.width) vis = static_cast<int>(p.width);
   const float* sc = p.scores + t * p.width;
+  // launched as a programmatic dependent of the score kernel: the scores are
+  // complete and visible from here on
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int32_t* o = out + t * topk;
 
   if (vis <= topk) {
@@ -726,8 +735,17 @@ cudaError_t launch_index(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const
   const size_t smem = static_cast<size_t>((cap > kTopkThreads ? cap : kTopkThreads) + kCandCap) * sizeof(unsigned long long);
   e = cudaFuncSetAttribute(index_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  index_topk_kernel<<<p.num_tokens, kTopkThreads, smem, stream>>>(p, topk, cap, out);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.num_tokens));
+  cfg.blockDim = dim3(kTopkThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, index_topk_kernel, p, topk, cap, out);
 }
 
 }  // namespace mla
