@@ -124,7 +124,8 @@ constexpr int kPairMOff = kPairBarBytes;
 constexpr int kPairRedOff = kPairMOff + 64 * 4;
 constexpr int kPairIntOff = kPairRedOff + 4 * 64 * 4;
 constexpr int kPairFlagOff = kPairIntOff + 64;
-constexpr int kPairAuxBytes = kPairFlagOff + 4 * 16;
+constexpr int kPairSigOff = kPairFlagOff + 4 * 16;   // 16 bytes: the odd CTA's P-ready signal copy
+constexpr int kPairAuxBytes = kPairSigOff + 16;
 constexpr int kPairSmemBytes = kPairAuxOff + kPairAuxBytes + 1024;  // + alignment slack
 static_assert(kPairSmemBytes <= 232448, "shared memory budget");
 constexpr uint32_t kPairOCol = 0;
@@ -912,6 +913,9 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
   const float sc = p.scale_log2;
   auto arrive_even = [&](int bar) { warp_arrive_even(rank, bars + 8 * bar, bars_even + 8 * bar); };
   auto all_ok = [&](bool ok) { return named_bar_and(kPairSmBar, 256, ok); };
+  // signal slot of this CTA and of the even CTA (see the P-ready hand-over below)
+  const uint32_t sig = smem + kPairAuxOff + kPairSigOff;
+  const uint32_t sig_even = mapa_shared(sig, 0);
   auto wait_all = [&](int bar, uint32_t parity) { return all_ok(mbar_wait(
       reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + 8 * bar)), parity, wd)); };
   if (p.debug_stall) {
@@ -984,7 +988,17 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
       tmem_ld_x32(tmem + lane_base + kPairSCol + sb * (kPairTile / 2) + 32 * w, x);
       tmem_ld_wait();
       tc_fence_before();
-      arrive_even(kBSEmpty + sb);
+      // S read: the loads have completed (wait::ld) and the tcgen05 fence
+      // orders them before the signal, which orders no memory access of its
+      // own, so the odd CTA's arrival on the even CTA's barrier is relaxed (a
+      // cluster-scope release would stall these warps for ~1k cycles per tile)
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0)
+          mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + 8 * (kBSEmpty + sb))));
+        else
+          mbar_arrive_cluster_relaxed(bars_even + 8 * (kBSEmpty + sb));
+      }
       // mask and scale (log2 units); tokens of this thread: h * 64 + 32 w + i
       bool page_ok = true;
       uint32_t vbits = 0xffffffffu;
@@ -1068,7 +1082,29 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      arrive_even(kBPFull);
+      // P ready.  Even CTA: one arrival per warp (the first also expects the
+      // odd CTA's 16 signal bytes).  Odd CTA: its P (and any zeroed value rows)
+      // were made visible to the async proxy by each thread's proxy fence; the
+      // softmax threads meet, and one of them issues a 16-byte async copy into
+      // the even CTA that completes on its P-ready barrier -- the hand-over of
+      // data written by threads to the tensor core that TMA stores use, and it
+      // does not stall the issuing warps as a cluster-scope release does.
+      if (rank == 0) {
+        __syncwarp();
+        if (lane == 0) {
+          uint64_t* pb = reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + 8 * kBPFull));
+          if (warp == 4)
+            mbar_arrive_expect_tx(pb, 16);
+          else
+            mbar_arrive(pb);
+        }
+      } else {
+        named_bar_sync(kPairSmBar, 256);
+        if (threadIdx.x == 128) {
+          bulk_copy_s2c(sig_even, sig, 16, bars_even + 8 * kBPFull);
+          bulk_commit();
+        }
+      }
       if (tr) PAIR_TR(rank, 9, jt);
       if (SPARSE && jt + 1 < tiles && !dequant_tile(jt + 1)) return;
     }
@@ -1176,7 +1212,7 @@ __global__ void __launch_bounds__(PairCfg<SPARSE>::kThreads, 1)
       mbar_init(bp + kBSFull + i, 1);
       mbar_init(bp + kBSEmpty + i, 16);  // 8 softmax warps in each CTA
     }
-    mbar_init(bp + kBPFull, 16);
+    mbar_init(bp + kBPFull, 8);  // the even CTA's 8 softmax warps (+ 16 bytes from the odd CTA)
     mbar_init(bp + kBPEmpty, 1);
     mbar_init(bp + kBOFull, 1);
     mbar_init(bp + kBOEmpty, 16);
@@ -1266,6 +1302,8 @@ __global__ void __launch_bounds__(PairCfg<SPARSE>::kThreads, 1)
   } else if (warp < kPairGatherWarp0) {
     regs_to<C::kRegsSm, C::kLaunchRegs>();
     pair_softmax<SPARSE>(p, sg, g, rank, split0, tmem, smem, bars, bars_even, m_s, red, flags, wd);
+    // the odd CTA's signal copies are complete before the pair's final sync
+    if (rank == 1 && threadIdx.x == 128) bulk_wait_all();
   } else if (SPARSE) {
     regs_to<C::kRegsGather, C::kLaunchRegs>();
     pair_gather(p, sg, rank, smem, bars, wd, flags);
