@@ -124,8 +124,12 @@ constexpr int kPairMOff = kPairBarBytes;
 constexpr int kPairRedOff = kPairMOff + 64 * 4;
 constexpr int kPairIntOff = kPairRedOff + 4 * 64 * 4;
 constexpr int kPairFlagOff = kPairIntOff + 64;
-constexpr int kPairSigOff = kPairFlagOff + 4 * 16;   // 16 bytes: the odd CTA's P-ready signal copy
-constexpr int kPairAuxBytes = kPairSigOff + 16;
+// 16-byte slots the odd CTA's async signal copies write into (their contents
+// are never read): 0..7 dequantised score blocks (per softmax warp), 8..9 the
+// RoPE item, 10 P ready
+constexpr int kPairSigOff = kPairFlagOff + 4 * 16;
+constexpr int kPairSigSlots = 11;
+constexpr int kPairAuxBytes = kPairSigOff + 16 * kPairSigSlots;
 constexpr int kPairSmemBytes = kPairAuxOff + kPairAuxBytes + 1024;  // + alignment slack
 static_assert(kPairSmemBytes <= 232448, "shared memory budget");
 constexpr uint32_t kPairOCol = 0;
@@ -913,9 +917,30 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
   const float sc = p.scale_log2;
   auto arrive_even = [&](int bar) { warp_arrive_even(rank, bars + 8 * bar, bars_even + 8 * bar); };
   auto all_ok = [&](bool ok) { return named_bar_and(kPairSmBar, 256, ok); };
-  // signal slot of this CTA and of the even CTA (see the P-ready hand-over below)
+  // signal slots of this CTA and of the even CTA (see the P-ready hand-over below)
   const uint32_t sig = smem + kPairAuxOff + kPairSigOff;
   const uint32_t sig_even = mapa_shared(sig, 0);
+  // Hand-over of shared memory written by this warp's threads (after each
+  // thread's proxy fence) to the pair's MMAs, on the even CTA's barrier
+  // `bar`: the even CTA's two writing warps arrive (the first expecting the
+  // odd CTA's 32 signal bytes); each of the odd CTA's two writing warps has
+  // one lane issue a 16-byte async copy into the even CTA that completes on
+  // the barrier -- no cluster-scope release stalls these warps.
+  auto hand_over = [&](int bar, bool first, int slot) {
+    __syncwarp();
+    if (lane == 0) {
+      if (rank == 0) {
+        uint64_t* b = reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + 8 * bar));
+        if (first)
+          mbar_arrive_expect_tx(b, 32);
+        else
+          mbar_arrive(b);
+      } else {
+        bulk_copy_s2c(sig_even + 16 * slot, sig + 16 * slot, 16, bars_even + 8 * bar);
+        bulk_commit();
+      }
+    }
+  };
   auto wait_all = [&](int bar, uint32_t parity) { return all_ok(mbar_wait(
       reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + 8 * bar)), parity, wd)); };
   if (p.debug_stall) {
@@ -952,7 +977,7 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
     const float scale = ld_shared_f32(lo + (tsw << 4) + (p.kv_scales ? 0 : 4 * blk));
     dequant_block_row(lo, lo + kPairChunk, tsw, scale, ok);
     fence_proxy_async_smem();
-    arrive_even(kBKsFull + blk);
+    hand_over(kBKsFull + blk, tg == 0, dw);
     if (lane == 0)
       mbar_arrive(reinterpret_cast<uint64_t*>(
           __cvta_shared_to_generic(bars + 8 * ((blk & 1) == rank ? kBKsDoneOwn : kBKsDone + (blk >> 1)))));
@@ -961,7 +986,7 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
     if (!all_ok(rope_ok)) return false;
     if (dw < 2) {
       fence_proxy_async_smem();
-      arrive_even(kBKsFull + 4);
+      hand_over(kBKsFull + 4, dw == 0, 8 + dw);
     }
     if (warp == 4 && lane == 0) PAIR_TR(rank, 4, t);
     return true;
@@ -1101,7 +1126,7 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
       } else {
         named_bar_sync(kPairSmBar, 256);
         if (threadIdx.x == 128) {
-          bulk_copy_s2c(sig_even, sig, 16, bars_even + 8 * kBPFull);
+          bulk_copy_s2c(sig_even + 16 * 10, sig + 16 * 10, 16, bars_even + 8 * kBPFull);
           bulk_commit();
         }
       }
@@ -1203,7 +1228,7 @@ __global__ void __launch_bounds__(PairCfg<SPARSE>::kThreads, 1)
       // dense: the even producer's arrival plus both CTAs' bytes; sparse: the
       // two gather warps converting the item in each CTA
       // sparse: each item by two softmax warps of each CTA
-      mbar_init(bp + kBKsFull + it, SPARSE ? 4 : 1);
+      mbar_init(bp + kBKsFull + it, SPARSE ? 2 : 1);  // sparse: the even CTA's two writing warps (+ 32 bytes)
       mbar_init(bp + kBKsEmpty + it, 1);
     }
     mbar_init(bp + kBKvFull, SPARSE ? 2 : 1);  // sparse: the value-slot copier of each CTA
@@ -1303,7 +1328,7 @@ __global__ void __launch_bounds__(PairCfg<SPARSE>::kThreads, 1)
     regs_to<C::kRegsSm, C::kLaunchRegs>();
     pair_softmax<SPARSE>(p, sg, g, rank, split0, tmem, smem, bars, bars_even, m_s, red, flags, wd);
     // the odd CTA's signal copies are complete before the pair's final sync
-    if (rank == 1 && threadIdx.x == 128) bulk_wait_all();
+    if (rank == 1 && (threadIdx.x & 31) == 0) bulk_wait_all();
   } else if (SPARSE) {
     regs_to<C::kRegsGather, C::kLaunchRegs>();
     pair_gather(p, sg, rank, smem, bars, wd, flags);
