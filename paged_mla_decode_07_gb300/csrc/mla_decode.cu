@@ -579,11 +579,28 @@ __device__ __forceinline__ void swizzle_row_in_place(uint32_t row_addr, uint32_t
   }
 }
 
+constexpr int kBf16RowBytes = kDqk * 2;  // a bf16 cache row: 576 dims
+
+// 16-byte asynchronous copy global -> shared (src_bytes 0 writes zeros), and
+// one arrival on `bar` once every copy this thread started has completed
+// (the barrier's expected count includes it).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 template <int R, int MODE>
 __device__ void gather_rows(const CUtensorMap* tm_rows, const DecodeParams& p, const Segments& sg, uint8_t* kv,
                             const Bars& bars, volatile uint8_t* flags, const Watchdog& wd) {
   using C = Cfg<R, MODE>;
   using RG = Ring<C>;
+  // gathered bf16 rows (sparse over the bf16 cache, sparse prefill) are copied
+  // by the threads, 16 bytes at a time, into their swizzled places
+  constexpr bool kRowCopies = C::kIndexed && !C::kFp8;
   // 128 threads, two per token: half h = 0 (warps 0, 1) converts value blocks
   // 0 and 1 and the RoPE dims, half 1 (warps 2, 3) value blocks 2 and 3.
   // FP8 rows: a block's 128 codes land in the upper chunk of its pair slot
@@ -673,6 +690,56 @@ __device__ void gather_rows(const CUtensorMap* tm_rows, const DecodeParams& p, c
   // the upper chunks of their pair slots; bf16: both chunks of each block;
   // half 0 also the RoPE bytes).  A 4-row gather covers tokens g4 .. g4 + 3.
   auto issue = [&](int jt, int row, bool ok) -> bool {
+    if (kRowCopies) {
+      // bf16 rows, copied in 16-byte units straight into the 128-byte swizzle
+      // (unit u of a row goes to u ^ (token & 7)): per instruction the warp
+      // copies one 128-byte chunk of four of its 32 tokens' rows, eight lanes
+      // per row, so every row segment is one coalesced 128-byte request.  Half
+      // h copies its two blocks and, half 0, the RoPE chunk; an unusable token
+      // is zero-filled by the copies (source bytes 0)
+      const int set = 5 * (jt & 1);
+      const int u = lane & 7;
+      int rs[8];
+      uint32_t nbs[8];
+#pragma unroll
+      for (int st = 0; st < 8; ++st) {
+        const int tl = 4 * st + (lane >> 3);
+        const int r = __shfl_sync(0xffffffffu, row, tl);
+        const bool o = __shfl_sync(0xffffffffu, ok ? 1 : 0, tl) != 0;
+        rs[st] = o ? r : 0;
+        nbs[st] = o ? 16u : 0u;
+      }
+      auto copy_chunk = [&](int c) {
+        const uint32_t cbase = kv_base + RG::chunk_off(jt, c);
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+          const int tk = wtok + 4 * st + (lane >> 3);
+          cp_async16(cbase + tk * 128 + ((u ^ (tk & 7)) << 4),
+                     p.kv_fp8 + static_cast<int64_t>(rs[st]) * kBf16RowBytes + 128 * c + 16 * u, nbs[st]);
+        }
+      };
+#pragma unroll 1
+      for (int i = 0; i < 2; ++i) {
+        const int blk = 2 * h + i;
+        const uint32_t use = RG::pair_use(jt, blk);
+        if (use > 0 && !warp_wait(bars.pair_empty + RG::pair_slot(jt, blk), (use - 1) & 1, wd)) return false;
+        if (blk == 0) flags[(jt & 3) * 128 + tok] = ok ? 1 : 0;  // token validity for the softmax
+        copy_chunk(2 * blk);
+        copy_chunk(2 * blk + 1);
+        cp_async_arrive(bars.raw_full + set + blk);
+        armed |= 1u << (set + blk);
+        next_par ^= 1u << (set + blk);
+      }
+      if (h == 0) {
+        const uint32_t use = RG::rope_use(jt);
+        if (use > 0 && !warp_wait(bars.rope_empty + RG::rope_slot(jt), (use - 1) & 1, wd)) return false;
+        copy_chunk(8);
+        cp_async_arrive(bars.raw_full + set + 4);
+        armed |= 1u << (set + 4);
+        next_par ^= 1u << (set + 4);
+      }
+      return true;
+    }
     const int gl = lane & 7;
     const int g4 = wtok + 4 * gl;
     const int r0 = __shfl_sync(0xffffffffu, row, 4 * gl);
@@ -760,8 +827,10 @@ __device__ void gather_rows(const CUtensorMap* tm_rows, const DecodeParams& p, c
         const int blk = 2 * h + i;
         if (!warp_wait(bars.raw_full + set + blk, par, wd)) goto drain;
         if (!C::kFp8) {
-          swizzle_row_in_place(kv_base + RG::chunk_off(jt, 2 * blk) + tok * 128, tsw, ok_c);
-          swizzle_row_in_place(kv_base + RG::chunk_off(jt, 2 * blk + 1) + tok * 128, tsw, ok_c);
+          if (!kRowCopies) {
+            swizzle_row_in_place(kv_base + RG::chunk_off(jt, 2 * blk) + tok * 128, tsw, ok_c);
+            swizzle_row_in_place(kv_base + RG::chunk_off(jt, 2 * blk + 1) + tok * 128, tsw, ok_c);
+          }
           if (C::kItemFull) {
             fence_proxy_async_smem();
             __syncwarp();
@@ -791,7 +860,7 @@ __device__ void gather_rows(const CUtensorMap* tm_rows, const DecodeParams& p, c
       if (h == 0) {
         // RoPE: already bf16; permute the 16-byte units into the swizzled order
         if (!warp_wait(bars.raw_full + set + 4, par, wd)) goto drain;
-        swizzle_row_in_place(kv_base + RG::chunk_off(jt, 8) + tok * 128, tsw, ok_c);
+        if (!kRowCopies) swizzle_row_in_place(kv_base + RG::chunk_off(jt, 8) + tok * 128, tsw, ok_c);
         if (C::kItemFull) {
           fence_proxy_async_smem();
           __syncwarp();
@@ -817,7 +886,8 @@ __device__ void gather_rows(const CUtensorMap* tm_rows, const DecodeParams& p, c
   return;
 drain:
   // abort: wait (bounded) for this warp's row gathers still in flight (the
-  // latest armed phase of each raw barrier)
+  // latest armed phase of each raw barrier); row copies: this thread's own
+  if (kRowCopies) asm volatile("cp.async.wait_all;" ::: "memory");
   if (lane == 0) {
 #pragma unroll 1
     for (int k = 0; k < C::kNumRaw; ++k)
@@ -1274,7 +1344,9 @@ __global__ void __launch_bounds__(Cfg<R, MODE>::kThreads, 1)
     mbar_init(bars.o_full, 1);
     mbar_init(bars.o_empty, 4 * C::kSmWG);
     mbar_init(bars.mma_done, 2);  // one commit per MMA-issuing warp
-    for (int k = 0; k < C::kNumRaw; ++k) mbar_init(bars.raw_full + k, 2);  // one arrive_expect_tx per issuing warp
+    // one arrive_expect_tx per issuing warp; bf16 row copies: one arrival per
+    // copying thread (the 64 threads of a half)
+    for (int k = 0; k < C::kNumRaw; ++k) mbar_init(bars.raw_full + k, (C::kIndexed && !C::kFp8) ? 64 : 2);
     *abort_flag = 0;
     fence_barrier_init();
   }
