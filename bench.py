@@ -78,7 +78,7 @@ def algorithmic(inp) -> dict:
 # figure holds only for the kernel sources it was taken with: their SHA-256 prefix is stored beside
 # it and the bench reports null once the sources differ.
 NCU_TRAFFIC = {
-    "dense_membound": (651.43e6, "739b709e70b25e66"),
+    "dense_membound": (651.42e6, "c2a831d2bca52fc6"),
 }
 # the sources the headline's dominant kernel (the single-CTA decode kernel) is built from
 KERNEL_SOURCES = ("mla_decode.cu", "mla_device.cuh", "mla_internal.h")
