@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
     index_topk_kernel(const IndexParams p, int topk, int sort_cap, int32_t* __restrict__ out) {
   extern __shared__ unsigned long long keys[];  // [max(sort_cap, kTopkThreads)], then candidates [kCandCap]
   unsigned long long* cand = keys + (sort_cap > kTopkThreads ? sort_cap : kTopkThreads);
-  __shared__ uint32_t hist[4096];
+  __shared__ __align__(16) uint32_t hist[4096];  // (also scratch for 2048 keys: 8-byte aligned)
   __shared__ uint32_t warp_cnt[kTopkThreads / 32];
   __shared__ uint32_t sh_prefix, sh_mask, sh_remaining, sh_gt, sh_eq_taken, sh_eq_total;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -635,13 +635,95 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
           }
         }
       }
-      int c2 = 1;
-      while (c2 < static_cast<int>(n_cand)) c2 <<= 1;
-      for (int i = static_cast<int>(n_cand) + tid; i < c2; i += kTopkThreads) cand[i] = 0ull;
-      __syncthreads();
-      sort_desc(cand, c2);
       const uint32_t n_gt1 = static_cast<uint32_t>(topk) - rem1;
-      for (uint32_t k = tid; k < rem1; k += kTopkThreads) keys[n_gt1 + k] = cand[k];
+      // The rem1 largest candidates, as a set (the final sort orders them):
+      // one more radix step over the candidates in shared memory, on the next
+      // twelve bits of the score image (bits 40..51 of the key); the keys of
+      // higher sub-bins are taken, and the few keys of the chosen sub-bin are
+      // sorted by one warp (by the block when there are many).
+      __syncthreads();  // the collection pass is complete
+      for (int i = tid; i < 4096; i += kTopkThreads) hist[i] = 0;
+      if (tid == 0) {
+        sh_gt = 0;
+        sh_eq_taken = 0;
+      }
+      __syncthreads();
+      for (uint32_t i = tid; i < n_cand; i += kTopkThreads)
+        atomicAdd(&hist[static_cast<uint32_t>(cand[i] >> 40) & 4095u], 1u);
+      __syncthreads();
+      {
+        uint32_t c = 0;
+#pragma unroll
+        for (int q = 0; q < kBinsPerThread; ++q) c += hist[kBinsPerThread * tid + q];
+        uint32_t x = c;  // inclusive suffix sum within the warp
+#pragma unroll
+        for (int o2 = 1; o2 < 32; o2 <<= 1) {
+          const uint32_t y = __shfl_down_sync(0xffffffffu, x, o2);
+          if (lane + o2 < 32) x += y;
+        }
+        if (lane == 0) warp_cnt[warp] = x;
+        __syncthreads();
+        uint32_t above = x - c;
+        for (int w = warp + 1; w < kTopkThreads / 32; ++w) above += warp_cnt[w];
+        if (above < rem1 && above + c >= rem1) {
+          uint32_t acc = above;
+          int d = kBinsPerThread * tid + kBinsPerThread - 1;
+          for (; d > kBinsPerThread * tid; --d) {
+            if (acc + hist[d] >= rem1) break;
+            acc += hist[d];
+          }
+          sh_prefix = static_cast<uint32_t>(d);
+          sh_remaining = rem1 - acc;  // keys to take from sub-bin d
+          sh_eq_total = hist[d];
+        }
+        __syncthreads();
+      }
+      const uint32_t d2 = sh_prefix, rem2 = sh_remaining, cnt2 = sh_eq_total;
+      const uint32_t above2 = rem1 - rem2;  // keys of higher sub-bins, all taken
+      unsigned long long* sub = reinterpret_cast<unsigned long long*>(hist);  // 2048 keys of scratch
+      __syncthreads();  // every thread has read the histogram
+      if (cnt2 <= 2048) {
+        for (uint32_t i = tid; i < n_cand; i += kTopkThreads) {
+          const unsigned long long key = cand[i];
+          const uint32_t dd = static_cast<uint32_t>(key >> 40) & 4095u;
+          if (dd > d2)
+            keys[n_gt1 + atomicAdd(&sh_gt, 1u)] = key;
+          else if (dd == d2)
+            sub[atomicAdd(&sh_eq_taken, 1u)] = key;
+        }
+        __syncthreads();
+        if (cnt2 <= 32) {
+          if (warp == 0) {
+            // descending bitonic sort of up to 32 keys, one per lane
+            unsigned long long x = static_cast<uint32_t>(lane) < cnt2 ? sub[lane] : 0ull;
+#pragma unroll
+            for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+              for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, stride);
+                const bool take_max = ((lane & stride) == 0) == ((lane & size) == 0);
+                x = take_max ? (x > y ? x : y) : (x < y ? x : y);
+              }
+            }
+            if (static_cast<uint32_t>(lane) < rem2) keys[n_gt1 + above2 + lane] = x;
+          }
+        } else {
+          int c3 = 1;
+          while (c3 < static_cast<int>(cnt2)) c3 <<= 1;
+          for (int i = static_cast<int>(cnt2) + tid; i < c3; i += kTopkThreads) sub[i] = 0ull;
+          __syncthreads();
+          sort_desc(sub, c3);
+          for (uint32_t k = tid; k < rem2; k += kTopkThreads) keys[n_gt1 + above2 + k] = sub[k];
+        }
+      } else {
+        // (a sub-bin of more than 2048 keys: sort all candidates)
+        int c2 = 1;
+        while (c2 < static_cast<int>(n_cand)) c2 <<= 1;
+        for (int i = static_cast<int>(n_cand) + tid; i < c2; i += kTopkThreads) cand[i] = 0ull;
+        __syncthreads();
+        sort_desc(cand, c2);
+        for (uint32_t k = tid; k < rem1; k += kTopkThreads) keys[n_gt1 + k] = cand[k];
+      }
       for (int i = topk + tid; i < sort_cap; i += kTopkThreads) keys[i] = 0ull;
       __syncthreads();
       sort_desc(keys, sort_cap);
