@@ -248,10 +248,13 @@ __device__ __forceinline__ void tma_prefetch3(const void* map, int c0, int c1, i
 }
 
 // Warp-uniform bounded wait on a barrier of this CTA (acquire at cluster
-// scope: many phases are completed by the other CTA's arrivals).
+// scope: many phases are completed by the other CTA's arrivals).  The polls
+// are try_waits, which may suspend the warp until the phase completes: hot
+// test_wait loops of the waiting roles cost the score MMAs issue slots and
+// shared-memory cycles (pair decode calls 2-3 % slower).
 __device__ __forceinline__ bool pair_wait(uint32_t bar, uint32_t parity, const Watchdog& wd) {
   uint64_t t0 = 0;
-  while (__shfl_sync(0xffffffffu, mbar_test_wait_cluster_u32(bar, parity) ? 1 : 0, 0) == 0) {
+  while (__shfl_sync(0xffffffffu, mbar_try_wait_cluster_u32(bar, parity) ? 1 : 0, 0) == 0) {
     if (t0 == 0) {
       t0 = global_timer_ns();
     } else if (__shfl_sync(0xffffffffu, wd.aborted() ? 1 : 0, 0)) {
@@ -271,7 +274,7 @@ __device__ __forceinline__ bool pair_wait_thread(uint32_t bar, uint32_t parity, 
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_test_wait_cluster_u32(bar, parity)) return true;
+      if (mbar_try_wait_cluster_u32(bar, parity)) return true;
     if (wd.aborted()) return false;
     if (global_timer_ns() - t0 > wd.limit_ns) {
       wd.trip(MLA_DEVICE_TIMEOUT);
@@ -648,6 +651,20 @@ __device__ void pair_gather(const DecodeParams& p, const PairSeg& sg, int rank, 
     return true;
   };
 
+  // validity bits of this warp's tokens of tile t, to both CTAs (hh = 0 warps)
+  auto put_flags = [&](int t, int row) {
+    const uint32_t v = __ballot_sync(0xffffffffu, row >= 0);
+    if (lane == 0) {
+      const uint32_t word = 4 * (4 * (t & 3) + 2 * rank + (wtok >> 5));
+      const uint32_t fb = 8 * (kBFlags + (t & 3));
+      st_shared_u32(flags_here + word, v);
+      st_cluster_u32(flags_peer + word, v);
+      mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + fb)));
+      mbar_arrive_cluster(bars_peer + fb);
+    }
+    __syncwarp();
+  };
+
   PairIt it_c = pair_first_from(sg, sg.p0);
   PairIt it_1 = pair_next(sg, it_c);
   PairIt it_2 = pair_next(sg, it_1);
@@ -655,24 +672,18 @@ __device__ void pair_gather(const DecodeParams& p, const PairSeg& sg, int rank, 
   prefetch(row_1);
   prefetch(row_2);
   int jt = 0;
+  if (hh == 0 && it_c.valid) put_flags(0, row_c);
   if (it_c.valid && !issue(0, row_c)) goto drain;
   for (; it_c.valid; ++jt) {
-    // rows of the tile three ahead (the loads of the lookup overlap the work below)
+    // the bits of the next tile, a tile before its dequantisation needs them.
+    // Their ring slot last held tile jt - 3's, which both CTAs' softmax warps
+    // have read: issue(jt) waited for the score MMAs of tile jt - 1, which
+    // follow the dequantisation of tile jt - 1, which each CTA's softmax warps
+    // start after the softmax of tile jt - 2.
+    if (hh == 0 && it_1.valid) put_flags(jt + 1, row_1);
+    // rows of the tile three ahead (the lookup's dependent loads stall this warp)
     const PairIt it_3 = pair_next(sg, it_2);
     const int row_3 = row_of(it_3);
-    if (hh == 0) {
-      // validity bits of this warp's tokens, to both CTAs
-      const uint32_t v = __ballot_sync(0xffffffffu, row_c >= 0);
-      if (lane == 0) {
-        const uint32_t word = 4 * (4 * (jt & 3) + 2 * rank + (wtok >> 5));
-        const uint32_t fb = 8 * (kBFlags + (jt & 3));
-        st_shared_u32(flags_here + word, v);
-        st_cluster_u32(flags_peer + word, v);
-        mbar_arrive(reinterpret_cast<uint64_t*>(__cvta_shared_to_generic(bars + fb)));
-        mbar_arrive_cluster(bars_peer + fb);
-      }
-      __syncwarp();
-    }
     const uint32_t par = static_cast<uint32_t>(jt) & 1u;
     // this CTA's value slots of block bs, once it is dequantised and the PV
     // MMAs of the previous tile are done (16-byte units in swizzled order:
