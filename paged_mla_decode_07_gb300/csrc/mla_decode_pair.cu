@@ -247,6 +247,21 @@ __device__ __forceinline__ void tma_prefetch3(const void* map, int c0, int c1, i
                : "memory");
 }
 
+// try_wait on a barrier of this CTA with acquire at cluster scope (the thread
+// may be suspended until the phase completes or a time limit of the hardware
+// passes).
+__device__ __forceinline__ bool mbar_try_wait_cluster_u32(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Warp-uniform bounded wait on a barrier of this CTA (acquire at cluster
 // scope: many phases are completed by the other CTA's arrivals).  The polls
 // are try_waits, which may suspend the warp until the phase completes: hot

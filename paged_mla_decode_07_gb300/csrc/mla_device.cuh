@@ -312,19 +312,6 @@ __device__ __forceinline__ bool mbar_test_wait_cluster_u32(uint32_t bar, uint32_
       : "memory");
   return ok != 0;
 }
-// try_wait form of the same (the thread may be suspended until the phase
-// completes or a time limit of the hardware passes).
-__device__ __forceinline__ bool mbar_try_wait_cluster_u32(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 __device__ __forceinline__ void umma_bf16_ss_fast(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                                   uint32_t accumulate) {
   asm volatile(
