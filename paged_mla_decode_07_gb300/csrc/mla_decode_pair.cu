@@ -1031,6 +1031,9 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
     float l_part = 0.f;
     for (int j = tb; j < te; ++j, ++jt) {
       const int sb = jt & 1;
+      // dense: the block-table entry of this thread's page, read before the
+      // wait for S so that the load overlaps it
+      const bool page_ok = SPARSE ? true : tile_page(p, b, L, j, h, false) >= 0;
       if (!wait_all(kBSFull + sb, (jt >> 1) & 1)) return;
       tc_fence_after();
       const bool tr = (warp == 4 && lane == 0);
@@ -1051,14 +1054,11 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
           mbar_arrive_cluster_relaxed(bars_even + 8 * (kBSEmpty + sb));
       }
       // mask and scale (log2 units); tokens of this thread: h * 64 + 32 w + i
-      bool page_ok = true;
       uint32_t vbits = 0xffffffffu;
       if (SPARSE) {
         // the gather warps of this CTA wrote the tile's validity bits
         if (!all_ok(pair_wait_thread(bars + 8 * (kBFlags + (jt & 3)), (jt >> 2) & 1, wd))) return;
         vbits = flags[4 * (jt & 3) + 2 * h + w];
-      } else {
-        page_ok = tile_page(p, b, L, j, h, false) >= 0;
       }
       const int pos0 = j * kPairTile + h * 64 + 32 * w;
       float mx = kPairNegInf;
