@@ -81,9 +81,9 @@ mla_status device_info(uint32_t** status, int* sm_count, int* pair_capacity = nu
 }
 
 // The CTA-pair decode kernel for problems of more than 64 rows, dense over
-// the bf16 cache or sparse over the FP8 cache (mla_decode_pair.cu).
+// the bf16 cache or sparse over FP8 or bf16 rows (mla_decode_pair.cu).
 constexpr bool kPairDecode = true;
-// Sparse over the FP8 cache on CTA pairs.
+// Sparse on CTA pairs.
 constexpr bool kPairSparse = true;
 
 // Test hooks (mla_test_hooks): a forced part count and a stalled softmax role.
@@ -116,10 +116,12 @@ mla_status geometry(int batch, int h_q, int s_q, int topk, int is_fp8, Geometry*
   g->rows = static_cast<int>(rows);
   g->mode = decode_mode(topk, is_fp8);
   g->sm_count = sms;
-  // problems of more than 64 rows, dense over the bf16 cache or sparse over
-  // the FP8 cache, run on CTA pairs (128 rows and 128-token tiles per pair);
+  // problems of more than 64 rows, dense over the bf16 cache or sparse (FP8
+  // or bf16 rows), run on CTA pairs (128 rows and 128-token tiles per pair);
   // everything else on single CTAs
-  g->pair = (kPairDecode && (g->mode == 0 || (kPairSparse && g->mode == 1)) && g->rows > 64) ? 1 : 0;
+  g->pair = (kPairDecode && (g->mode == 0 || (kPairSparse && (g->mode == 1 || g->mode == 3))) && g->rows > 64)
+                ? 1
+                : 0;
   g->rpc = g->pair ? 128 : rows_per_cta(g->rows);
   g->tile_tokens = g->pair ? 128 : kTileTokens;
   g->row_groups = (g->rows + g->rpc - 1) / g->rpc;
@@ -385,13 +387,13 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
   if (g.pair) {
     // chunk-major boxes: Q of a CTA in one copy; dense: a page's score operand
     // in three copies of three chunks, its value shares in copies of two
-    // chunks.  Sparse: the FP8 rows are copied by the gather warps with
-    // cp.async and the two cache maps go unused.
+    // chunks.  Sparse: the rows are copied by the gather warps with cp.async
+    // and the two cache maps go unused.
     st = encode_chunk_major_map(&tm_q, a->q, qrows, kNumChunks, "q");
     if (st == MLA_OK && g.mode == 0) st = encode_chunk_major_map(&tm_kv, a->kvcache, cache_rows, 3, "kvcache");
     if (st == MLA_OK && g.mode == 0) st = encode_chunk_major_map(&tm_kv2, a->kvcache, cache_rows, 2, "kvcache");
     if (st != MLA_OK) return st;
-    if (g.mode == 1) tm_kv = tm_kv2 = tm_q;
+    if (g.mode == 1 || g.mode == 3) tm_kv = tm_kv2 = tm_q;
   } else {
     st = encode_rows_map(&tm_q, a->q, qrows, g.rpc, "q");
   }
@@ -439,10 +441,11 @@ mla_status mla_decode(const mla_decode_args* a, mla_stream_t stream) {
   p.scale_log2 = a->sm_scale * 1.4426950408889634f;
   p.kv_scales = a->kv_scales;
   p.topk_lengths = a->topk_lengths;
-  p.fp8_rope_off = a->kv_scales ? kDv : kFp8RopeOffset;
+  p.fp8_rope_off = mode == 3 ? 2 * kDv : (a->kv_scales ? kDv : kFp8RopeOffset);
+  p.rows16 = mode == 3 ? 1 : 0;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = g.pair ? launch_decode_pair(tm_q, tm_kv, tm_kv2, p, g.mode == 1, s)
+  cudaError_t e = g.pair ? launch_decode_pair(tm_q, tm_kv, tm_kv2, p, g.mode == 1 || g.mode == 3, s)
                          : launch_decode(tm_q, tm_kv, p, g.rpc, mode, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
 
@@ -546,7 +549,8 @@ mla_status mla_sparse_prefill(const mla_sparse_prefill_args* a, mla_stream_t str
     if (st != MLA_OK) return st;
     const char* q = static_cast<const char*>(a->q) + static_cast<size_t>(c0) * a->h_q * kDqk * 2;
     CUtensorMap tm_q;
-    st = encode_rows_map(&tm_q, q, static_cast<long long>(chunk) * a->h_q, gc.rpc, "q");
+    st = gc.pair ? encode_chunk_major_map(&tm_q, q, static_cast<long long>(chunk) * a->h_q, kNumChunks, "q")
+                 : encode_rows_map(&tm_q, q, static_cast<long long>(chunk) * a->h_q, gc.rpc, "q");
     if (st != MLA_OK) return st;
     cudaError_t e = launch_metadata(nullptr, chunk, a->topk, gc, sched, num_splits, s);
     if (e != cudaSuccess) return cuda_fail(e, "metadata kernel launch");
@@ -574,11 +578,13 @@ mla_status mla_sparse_prefill(const mla_sparse_prefill_args* a, mla_stream_t str
     p.row_groups = gc.row_groups;
     p.num_parts = gc.num_parts;
     p.max_slots = max_slots(gc);
-    p.evict_first = gc.row_groups == 1 ? 1 : 0;
+    p.evict_first = (gc.row_groups == 1 && !gc.pair) ? 1 : 0;
     p.sched_tag = gc.tag;
     p.flat_rows = a->s_kv;
     p.scale_log2 = a->sm_scale * 1.4426950408889634f;
-    e = launch_decode(tm_q, tm_kv, p, gc.rpc, 3, s);
+    p.fp8_rope_off = 2 * kDv;
+    p.rows16 = 1;
+    e = gc.pair ? launch_decode_pair(tm_q, tm_q, tm_q, p, true, s) : launch_decode(tm_q, tm_kv, p, gc.rpc, 3, s);
     if (e != cudaSuccess) return cuda_fail(e, "sparse prefill attention kernel launch");
     CombineParams cp;
     cp.num_splits = num_splits;

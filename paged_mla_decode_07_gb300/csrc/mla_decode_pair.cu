@@ -1,6 +1,7 @@
 // K1p — paged MLA decode on CTA pairs (tcgen05 cta_group::2) for problems of
 // more than 64 query rows: dense over the bf16 cache, and sparse (top-k) over
-// the FP8 cache.
+// the FP8 cache or over bf16 rows (the bf16 cache, or the unpaged rows of
+// sparse prefill).
 //
 // What is computed is the same as in the single-CTA kernel (mla_decode.cu):
 // per query row, softmax(q K^T * sm_scale) V over the row's keys with
@@ -11,7 +12,7 @@
 // article, Design 5; merged by the combine kernel).  In sparse mode the keys
 // of a query token are the valid ids of its index row and each FP8 row is
 // dequantised as bf16_rn(fp32(e4m3) * scale) before the MMAs (FlashMLA
-// article, Design 2).
+// article, Design 2); bf16 rows are used as they are.
 //
 // Formulation.  The two CTAs of a cluster (one TPC) work together on 128
 // query rows of a problem, 64 rows each, and on 128-token tiles, 64 tokens
@@ -509,8 +510,9 @@ __device__ __forceinline__ PairIt pair_next(const PairSeg& sg, const PairIt& it)
 // Cache row of the token in index slot k of problem prob, or -1 for an
 // invalid id (outside [0, length) or on an unusable page, flagged when asked).
 __device__ __forceinline__ int sparse_row(const DecodeParams& p, const PairSeg& sg, int prob, int k, bool flag) {
+  // (the length, the list length and the index are independent loads, in flight together)
   const int b = prob / p.s_q;
-  const int L = sg.seqlens[b];
+  const int L = p.flat_rows > 0 ? p.flat_rows : sg.seqlens[b];
   int tk = p.topk;
   if (p.topk_lengths) {
     const int len = p.topk_lengths[prob];
@@ -518,6 +520,7 @@ __device__ __forceinline__ int sparse_row(const DecodeParams& p, const PairSeg& 
   }
   const int t = k < tk ? p.indices[static_cast<int64_t>(prob) * p.topk + k] : -1;
   if (t < 0 || t >= L) return -1;
+  if (p.flat_rows > 0) return t;  // unpaged rows: the index is the row
   const int32_t* bt = p.block_table + static_cast<int64_t>(b) * p.block_table_stride;
   const int page = (t >> 6) < p.block_table_stride ? bt[t >> 6] : -1;
   if (page < 0 || page >= p.num_pages) {
@@ -584,10 +587,13 @@ __device__ __forceinline__ void copy_block_codes(const DecodeParams& p, int row_
   }
 }
 
-// Warps 12-15 (sparse): row lookups and row copies.  Thread g (0..127) owns
-// token tok = g % 64 of the CTA's half of each tile (index slot 64 rank + tok)
-// and value blocks 2hh and 2hh + 1 (hh = g / 64); block bs = 2hh + rank is in
-// this CTA's share of the value dims, block 2hh + 1 - rank in its partner's.
+// Warps 12-15 (sparse): row lookups and row copies (FP8 rows: codes and
+// scales, dequantised by the softmax warps; bf16 rows: both chunks of each
+// block straight into the swizzle, to be handed over as they are).  Thread
+// g (0..127) owns token tok = g % 64 of the CTA's half of each tile (index
+// slot 64 rank + tok) and value blocks 2hh and 2hh + 1 (hh = g / 64); block
+// bs = 2hh + rank is in this CTA's share of the value dims, block
+// 2hh + 1 - rank in its partner's.
 // Per tile:
 //   * its warp copies the codes of those blocks for its 32 tokens into the
 //     score slots (block b as plain rows in chunk 2b + 1, with the token's
@@ -603,6 +609,7 @@ __device__ __forceinline__ void copy_block_codes(const DecodeParams& p, int row_
 // The hh = 0 warps write the tile's validity bits of their tokens to both
 // CTAs, look the rows up three tiles ahead and prefetch them whole into L2,
 // so that the copies on the tile's critical chain hit L2.
+template <bool ROWS16>
 __device__ void pair_gather(const DecodeParams& p, const PairSeg& sg, int rank, uint32_t smem, uint32_t bars,
                             const Watchdog& wd, uint32_t* flags) {
   const int g = threadIdx.x - 32 * kPairGatherWarp0;  // 0..127
@@ -612,7 +619,7 @@ __device__ void pair_gather(const DecodeParams& p, const PairSeg& sg, int rank, 
   const int wtok = tok & ~31;
   const uint32_t tsw = tok & 7;
   const int bs = 2 * hh + rank, bp = 2 * hh + 1 - rank;
-  const int row_bytes = p.kv_scales ? 640 : kFp8RowBytes;
+  const int row_bytes = ROWS16 ? 2 * kDqk : (p.kv_scales ? 640 : kFp8RowBytes);
   const uint32_t peer = static_cast<uint32_t>(rank ^ 1);
   const uint32_t kv_own = smem + kPairKvOff + (4 * rank + 2 * hh) * kPairChunk + tok * 128;
   const uint32_t flags_here = static_cast<uint32_t>(__cvta_generic_to_shared(flags));
@@ -637,7 +644,23 @@ __device__ void pair_gather(const DecodeParams& p, const PairSeg& sg, int rank, 
         if (i == 1 && !pair_wait(bars + 8 * (kBKsRead + hh), (jt - 1) & 1, wd)) return false;
       }
       if (i == 0 && g == 0) PAIR_TR(rank, 0, jt);
-      if (item < 4) {
+      if (ROWS16 && item < 4) {
+        // bf16 rows: the block's two chunks straight into the 128-byte swizzle
+        // (zeros for invalid tokens)
+        const uint32_t u = lane & 7;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t cbase = smem + kPairKsOff + (2 * item + c) * kPairChunk;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int tk = wtok + 4 * k + (lane >> 3);
+            const int r = wr.r[k];
+            cp_async16(cbase + tk * 128 + ((u ^ (tk & 7)) << 4),
+                       p.kv_fp8 + static_cast<int64_t>(r < 0 ? 0 : r) * row_bytes + 128 * (2 * item + c) + 16 * u,
+                       r < 0 ? 0u : 16u);
+          }
+        }
+      } else if (item < 4) {
         const uint32_t lo = smem + kPairKsOff + 2 * item * kPairChunk;
         copy_block_codes(p, row_bytes, wr, item, lo + kPairChunk, wtok, lane);
         // the token's scale(s), read by the dequantising thread before it writes its row of chunk 2b
@@ -926,7 +949,7 @@ done:
 // ---------------------------------------------------------------------------
 // warps 4-11: online softmax and epilogue
 // ---------------------------------------------------------------------------
-template <bool SPARSE>
+template <bool SPARSE, bool ROWS16>
 __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, int rank, int split0, uint32_t tmem,
                              uint32_t smem, uint32_t bars, uint32_t bars_even, float* m_s, float* red,
                              const volatile uint32_t* flags, const Watchdog& wd) {
@@ -999,9 +1022,12 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
     const bool ok = ((flags[4 * (t & 3) + 2 * rank + tg] >> lane) & 1u) != 0;
     if (!all_ok(pair_wait_thread(bars + 8 * (kBRaw + blk), t & 1, wd))) return false;
     if (warp == 4 && lane == 0) PAIR_TR(rank, 15, t);
-    const uint32_t lo = smem + kPairKsOff + 2 * blk * kPairChunk + tok * 128;
-    const float scale = ld_shared_f32(lo + (tsw << 4) + (p.kv_scales ? 0 : 4 * blk));
-    dequant_block_row(lo, lo + kPairChunk, tsw, scale, ok);
+    if (!ROWS16) {
+      const uint32_t lo = smem + kPairKsOff + 2 * blk * kPairChunk + tok * 128;
+      const float scale = ld_shared_f32(lo + (tsw << 4) + (p.kv_scales ? 0 : 4 * blk));
+      dequant_block_row(lo, lo + kPairChunk, tsw, scale, ok);
+    }
+    // (bf16 rows were copied into place: only their hand-over to the MMAs)
     fence_proxy_async_smem();
     hand_over(kBKsFull + blk, tg == 0, dw);
     if (lane == 0)
@@ -1025,7 +1051,7 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
     sg.range(prob, tb, te);
     if (tb >= te) continue;
     const int b = SPARSE ? prob / p.s_q : prob;
-    const int L = sg.seqlens[b];
+    const int L = SPARSE ? 0 : sg.seqlens[b];  // (sparse: the validity bits, and no lengths for unpaged rows)
     // last visible key of this row (dense: bottom-right causal alignment)
     const int lim = (!SPARSE && p.is_causal) ? L - p.s_q + grow / p.h_q : L - 1;
     float l_part = 0.f;
@@ -1223,7 +1249,7 @@ __device__ void pair_softmax(const DecodeParams& p, const PairSeg& sg, int g, in
 // ---------------------------------------------------------------------------
 // kernel
 // ---------------------------------------------------------------------------
-template <bool SPARSE>
+template <bool SPARSE, bool ROWS16>
 __global__ void __launch_bounds__(PairCfg<SPARSE>::kThreads, 1)
     mla_decode_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_ks,
                            const __grid_constant__ CUtensorMap tm_kv, const DecodeParams p) {
@@ -1352,12 +1378,12 @@ __global__ void __launch_bounds__(PairCfg<SPARSE>::kThreads, 1)
     }
   } else if (warp < kPairGatherWarp0) {
     regs_to<C::kRegsSm, C::kLaunchRegs>();
-    pair_softmax<SPARSE>(p, sg, g, rank, split0, tmem, smem, bars, bars_even, m_s, red, flags, wd);
+    pair_softmax<SPARSE, ROWS16>(p, sg, g, rank, split0, tmem, smem, bars, bars_even, m_s, red, flags, wd);
     // the odd CTA's signal copies are complete before the pair's final sync
     if (rank == 1 && (threadIdx.x & 31) == 0) bulk_wait_all();
   } else if (SPARSE) {
     regs_to<C::kRegsGather, C::kLaunchRegs>();
-    pair_gather(p, sg, rank, smem, bars, wd, flags);
+    pair_gather<ROWS16>(p, sg, rank, smem, bars, wd, flags);
   }
 
   tc_fence_before();
@@ -1381,11 +1407,11 @@ __global__ void __launch_bounds__(PairCfg<SPARSE>::kThreads, 1)
   }
 }
 
-template <bool SPARSE>
+template <bool SPARSE, bool ROWS16>
 cudaError_t launch_pair(const CUtensorMap& tm_q, const CUtensorMap& tm_ks, const CUtensorMap& tm_kv,
                         const DecodeParams& p, cudaStream_t stream) {
   using C = PairCfg<SPARSE>;
-  auto kern = mla_decode_pair_kernel<SPARSE>;
+  auto kern = mla_decode_pair_kernel<SPARSE, ROWS16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes fa;
@@ -1412,7 +1438,7 @@ cudaError_t launch_pair(const CUtensorMap& tm_q, const CUtensorMap& tm_ks, const
 }  // namespace
 
 int pair_cluster_capacity() {
-  auto kern = mla_decode_pair_kernel<true>;
+  auto kern = mla_decode_pair_kernel<true, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
@@ -1432,7 +1458,9 @@ int pair_cluster_capacity() {
 
 cudaError_t launch_decode_pair(const CUtensorMap& tm_q, const CUtensorMap& tm_ks, const CUtensorMap& tm_kv,
                                const DecodeParams& p, bool sparse, cudaStream_t stream) {
-  return sparse ? launch_pair<true>(tm_q, tm_ks, tm_kv, p, stream) : launch_pair<false>(tm_q, tm_ks, tm_kv, p, stream);
+  if (!sparse) return launch_pair<false, false>(tm_q, tm_ks, tm_kv, p, stream);
+  return p.rows16 ? launch_pair<true, true>(tm_q, tm_ks, tm_kv, p, stream)
+                  : launch_pair<true, false>(tm_q, tm_ks, tm_kv, p, stream);
 }
 
 }  // namespace mla

@@ -92,7 +92,10 @@ struct DecodeParams {
                               // block table or cache_seqlens); 0: paged cache
   const float* kv_scales;     // FP8 rows with one scale per token ([rows] fp32), else NULL
   const int32_t* topk_lengths;  // sparse: valid index slots per problem, else NULL
-  int fp8_rope_off;           // byte offset of the RoPE dims in an FP8 row (528, or 512 with kv_scales)
+  int fp8_rope_off;           // byte offset of the RoPE dims in a row (FP8: 528, or 512 with kv_scales;
+                              // bf16 rows: 1024)
+  int rows16;                 // CTA-pair sparse decode: the rows are bf16 (1152 bytes, used as they
+                              // are), 0: FP8 rows, dequantised
 
   float scale_log2;           // sm_scale * log2(e)
 };

@@ -146,16 +146,18 @@ def test_pair_rescale_path():
           parts=1)
 
 
+@pytest.mark.parametrize("fp8", [True, False], ids=["fp8", "bf16"])
 @pytest.mark.parametrize("h_q,topk", [(128, 64), (128, 127), (128, 129), (128, 640), (96, 200), (256, 300)])
-def test_pair_sparse_shapes(h_q, topk):
-    """Sparse FP8 decode on CTA pairs: 128-slot tiles (a partial last tile, a single one), ghost
-    rows, two pairs per query token."""
-    check(W.custom(name=f"ps{h_q}_{topk}", batch=2, h_q=h_q, s_q=2, mode="sparse", seqlens=(3000, 700),
+def test_pair_sparse_shapes(h_q, topk, fp8):
+    """Sparse decode on CTA pairs over FP8 or bf16 rows: 128-slot tiles (a partial last tile, a
+    single one), ghost rows, two pairs per query token."""
+    check(W.custom(name=f"ps{h_q}_{topk}", batch=2, h_q=h_q, s_q=2, mode="sparse", fp8=fp8, seqlens=(3000, 700),
                    topk=topk), 1900 + h_q + topk)
 
 
-def test_pair_sparse_duplicates_invalid_and_bad_pages():
-    w = W.custom(name="psdup", batch=2, h_q=128, s_q=2, mode="sparse", seqlens=(300, 900), topk=256)
+@pytest.mark.parametrize("fp8", [True, False], ids=["fp8", "bf16"])
+def test_pair_sparse_duplicates_invalid_and_bad_pages(fp8):
+    w = W.custom(name="psdup", batch=2, h_q=128, s_q=2, mode="sparse", fp8=fp8, seqlens=(300, 900), topk=256)
     inp = W.make_inputs(w, seed=23)
     idx = inp.indices.clone()
     idx[0, 0, :40] = 7           # one id forty times
@@ -182,9 +184,11 @@ def test_pair_sparse_duplicates_invalid_and_bad_pages():
     compare(out, lse, ref_out, ref_lse, "psbad")
 
 
+@pytest.mark.parametrize("fp8", [True, False], ids=["fp8", "bf16"])
 @pytest.mark.parametrize("parts", [1, 5, 300])
-def test_pair_sparse_forced_splits(parts):
-    w = W.custom(name=f"psp{parts}", batch=3, h_q=128, s_q=2, mode="sparse", seqlens=(5000, 3000, 700), topk=640)
+def test_pair_sparse_forced_splits(parts, fp8):
+    w = W.custom(name=f"psp{parts}", batch=3, h_q=128, s_q=2, mode="sparse", fp8=fp8, seqlens=(5000, 3000, 700),
+                 topk=640)
     check(w, 2000 + parts, parts=parts)
 
 
