@@ -175,14 +175,14 @@ enum PairBar {
   kBOFull = 20,   // the segment's last PV MMAs are done
   kBOEmpty = 21,  // (even) both CTAs' epilogues have read O
   kBMmaDone = 22, // (even) drain of the MMA issuers
-  kBRaw = 23,     // [5] (sparse) the codes of item i (block i, 4: RoPE) landed in this CTA
+  kBRaw = 23,     // [5] (sparse) the rows of item i (block i, 4: RoPE) landed in this CTA
   kBFlags = 28,   // [4] (sparse) the validity bits of tile jt (barrier jt % 4) are written by the
                   // gather warps of both CTAs, which can run up to three tiles ahead of the softmax
-  kBKsDone = 32,  // [2] (sparse) block 1 - rank + 2m of the tile's score operand is dequantised
+  kBKsDone = 32,  // [2] (sparse) block 1 - rank + 2m of the tile's score operand is in place
   kBKsRead = 34,  // [2] (sparse) its copy to the partner's value slots has read it
   kBKvIn = 36,    // (sparse) this CTA's value slots of the tile are complete: its own share
                   // written by its gather warps, the partner's copies (transaction bytes)
-  kBKsDoneOwn = 37,  // (sparse) blocks rank and rank + 2 of the tile's score operand are dequantised
+  kBKsDoneOwn = 37,  // (sparse) blocks rank and rank + 2 of the tile's score operand are in place
   kBCount = 38
 };
 static_assert(kBCount * 8 <= kPairBarBytes, "barrier area");
@@ -595,14 +595,15 @@ __device__ __forceinline__ void copy_block_codes(const DecodeParams& p, int row_
 // bs = 2hh + rank is in this CTA's share of the value dims, block
 // 2hh + 1 - rank in its partner's.
 // Per tile:
-//   * its warp copies the codes of those blocks for its 32 tokens into the
-//     score slots (block b as plain rows in chunk 2b + 1, with the token's
-//     scales in the first bytes of its row of chunk 2b) as the score MMAs of
-//     the previous tile, and for the partner's block the copier
-//     (pair_value_copier), release them; the hh = 0 warps also copy the RoPE
-//     parts straight into the 128-byte swizzle of chunk 8 (zeros for invalid
-//     tokens).  The softmax warps dequantise the blocks in place
-//     (pair_softmax);
+//   * its warp copies those blocks for its 32 tokens into the score slots
+//     (FP8: the codes of block b as plain rows in chunk 2b + 1, with the
+//     token's scales in the first bytes of its row of chunk 2b; bf16: chunks
+//     2b and 2b + 1 in the swizzle) as the score MMAs of the previous tile,
+//     and for the partner's block the copier (pair_value_copier), release
+//     them; the hh = 0 warps also copy the RoPE parts straight into the
+//     128-byte swizzle of chunk 8 (zeros for invalid tokens).  The softmax
+//     warps dequantise FP8 blocks in place and hand the blocks over to the
+//     score MMAs (pair_softmax);
 //   * once they have, and the PV MMAs of the previous tile are done, the
 //     thread copies its token's row of block bs into this CTA's value slots
 //     4 rank + 2hh, 4 rank + 2hh + 1.
